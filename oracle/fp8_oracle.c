@@ -1,0 +1,311 @@
+/*
+ * fp8_oracle.c -- CPU oracle for the FP8 delayed-scaling linear layer.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This file is the slow, plain reference that the
+ * GPU path is checked against.  Only the test suite, the smoke check and the
+ * benchmark's CPU-baseline leg may load it.  It shares no code, header, table
+ * or constant generator with the CUDA library, and it includes nothing from
+ * it.
+ *
+ * Sources (the three web pages this method is described on):
+ *  [P1] "NVIDIA Transformer Engine and FP8 mixed precision: implementation
+ *       guide" (ai-tool-zukan.com) -- section "What are Transformer Engine and
+ *       FP8 mixed precision" (E4M3 = 4 exponent / 3 mantissa bits for the
+ *       forward pass, E5M2 = 5 / 2 for the backward pass; dynamic scaling
+ *       watches each tensor's range) and section "Dynamic scaling and the FP8
+ *       recipe" (DelayedScaling: margin, fp8_format, amax_history_len;
+ *       Format.HYBRID = E4M3 forward, E5M2 backward).
+ *  [P2] "FP8 quantization with NVIDIA TensorRT" (ai.warp-studio.com) -- section
+ *       on the FP8 workflow (Q/DQ nodes, Absolute-Max calibration).
+ *  [P3] "Mixed-precision training" wiki note (notes.yuuk.io) -- "Definition"
+ *       table: FP8 E4M3 (S1E4M3) max 448, relative error ~1e-1; FP8 E5M2
+ *       (S1E5M2) max 57,344, relative error ~2e-1, same range as FP16; and the
+ *       "per-tensor scaling is the key" bullet (delayed or just-in-time
+ *       scaling), "extension to FP8" bullet (only the GEMMs run in FP8, with
+ *       higher-precision accumulation).
+ *
+ * Readings taken where the pages are silent (each one is listed in the design
+ * notes of the repository):
+ *  - The E4M3 variant is the one whose largest finite value is 448: exponent
+ *    field 15 holds finite values, only S.1111.111 is NaN, no infinities.  An
+ *    IEEE-style E4M3 would stop at 240, which contradicts the 448 of [P3].
+ *    E5M2 is IEEE-style (bias 15, infinities and NaNs at exponent 31), which
+ *    gives 57,344 and "the same range as FP16".
+ *  - Scaled cast: v = fl32(x * s) (one IEEE binary32 multiply), then v is
+ *    rounded to the nearest FP8 value with ties to the even code; |v| beyond
+ *    the largest finite value (and +-inf) saturates to +-max; NaN stays NaN;
+ *    the sign of zero is kept.
+ *  - amax = max |x| over the tensor, NaN entries skipped, result exact.
+ *  - Scale update (the formula of the delayed-scaling recipe):
+ *    history <- [amax, history[0 .. L-2]];  m = max(history);
+ *    if 0 < m < inf:  s = fl32(fl32(fmax / m) * 2^-margin), +inf clamped to
+ *    FLT_MAX, s_inv = fl32(1 / s);  otherwise s and s_inv stay as they were.
+ *  - GEMM: operands decoded exactly, products and sums exact (integer path)
+ *    or in double (sampled path); dequant epilogue
+ *    y = bf16_rne(fl32(fl32(acc) * fl32(sa_inv * sb_inv))).
+ */
+#include <float.h>
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#if !defined(FLT_EVAL_METHOD) || FLT_EVAL_METHOD != 0
+#error "the oracle needs float expressions evaluated in binary32 (FLT_EVAL_METHOD == 0)"
+#endif
+
+#define OR_E4M3 0
+#define OR_E5M2 1
+
+/* ------------------------------------------------------------------------ */
+/* BF16 (S1E8M7, [P3] Definition table): the top 16 bits of a binary32.      */
+/* ------------------------------------------------------------------------ */
+
+float or_bf16_to_f32(uint16_t b)
+{
+    uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return f;
+}
+
+/* Round a binary32 value to the nearest BF16 value, ties to an even last
+ * mantissa bit; NaN stays a (quiet) NaN.  The 16 dropped bits are compared
+ * with the halfway pattern 0x8000 directly. */
+uint16_t or_f32_to_bf16(float f)
+{
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    if ((u & 0x7fffffffu) > 0x7f800000u)
+        return (uint16_t)((u >> 16) | 0x0040u);
+    uint32_t keep = u >> 16;
+    uint32_t drop = u & 0xffffu;
+    if (drop > 0x8000u || (drop == 0x8000u && (keep & 1u)))
+        keep += 1u; /* may carry into the exponent: that is the next binade (or inf) */
+    return (uint16_t)keep;
+}
+
+/* ------------------------------------------------------------------------ */
+/* FP8 decode from the bit fields ([P1] format section, [P3] Definition).    */
+/* ------------------------------------------------------------------------ */
+
+double or_fp8_decode(uint8_t code, int fmt)
+{
+    int s = code >> 7;
+    double v;
+    if (fmt == OR_E4M3) {
+        int e = (code >> 3) & 0xf, m = code & 7;
+        if (e == 15 && m == 7)
+            return NAN;
+        if (e == 0)
+            v = ldexp((double)m, -9);             /* m/8 * 2^(1-7) */
+        else
+            v = ldexp(1.0 + m / 8.0, e - 7);
+    } else {
+        int e = (code >> 2) & 0x1f, m = code & 3;
+        if (e == 31)
+            return m == 0 ? (s ? -INFINITY : INFINITY) : NAN;
+        if (e == 0)
+            v = ldexp((double)m, -16);            /* m/4 * 2^(1-15) */
+        else
+            v = ldexp(1.0 + m / 4.0, e - 15);
+    }
+    return s ? -v : v;
+}
+
+/* Largest finite code (sign bit clear) and its value. */
+static int max_code(int fmt) { return fmt == OR_E4M3 ? 0x7e : 0x7b; }
+
+double or_fp8_max(int fmt) { return or_fp8_decode((uint8_t)max_code(fmt), fmt); }
+
+/* ------------------------------------------------------------------------ */
+/* FP8 encode of a binary32 value: nearest representable value, ties to the */
+/* even code, saturating.  Non-negative finite codes 0..max_code are in      */
+/* increasing order of value, so a binary search finds the two neighbours.  */
+/* ------------------------------------------------------------------------ */
+
+uint8_t or_fp8_encode_f32(float v, int fmt)
+{
+    if (isnan(v))
+        return 0x7f; /* a NaN code of either format; compared as a class */
+    int neg = signbit(v) ? 1 : 0;
+    double a = fabs((double)v);
+    int top = max_code(fmt);
+    int code;
+    if (a >= or_fp8_decode((uint8_t)top, fmt)) {
+        code = top;                                   /* saturate (also +-inf) */
+    } else {
+        int lo = 0, hi = top;                         /* value(lo) <= a < value(hi) */
+        while (hi - lo > 1) {
+            int mid = (lo + hi) / 2;
+            if (or_fp8_decode((uint8_t)mid, fmt) <= a)
+                lo = mid;
+            else
+                hi = mid;
+        }
+        double vlo = or_fp8_decode((uint8_t)lo, fmt);
+        double vhi = or_fp8_decode((uint8_t)hi, fmt);
+        double twice = 2.0 * a, mid = vlo + vhi;      /* both exact in double */
+        if (twice < mid)
+            code = lo;
+        else if (twice > mid)
+            code = hi;
+        else
+            code = (lo % 2 == 0) ? lo : hi;           /* tie: even code */
+    }
+    return (uint8_t)((neg << 7) | code);
+}
+
+void or_fp8_encode_f32_array(const float *v, int64_t n, int fmt, uint8_t *out)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = or_fp8_encode_f32(v[i], fmt);
+}
+
+/* ------------------------------------------------------------------------ */
+/* amax: max |x| over a BF16 tensor ([P1] dynamic scaling; [P2] Absolute-    */
+/* Max).  NaN entries never compare greater, so they are skipped.           */
+/* ------------------------------------------------------------------------ */
+
+float or_amax_bf16(const uint16_t *x, int64_t n)
+{
+    float m = 0.0f;
+#pragma omp parallel for reduction(max : m) schedule(static)
+    for (int64_t i = 0; i < n; ++i) {
+        float a = fabsf(or_bf16_to_f32(x[i]));
+        if (a > m)
+            m = a;
+    }
+    return m;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Scaled cast with transposed copy: out[r][c] = enc(fl32(x[r][c] * s)) and  */
+/* out_t[c][r] = out[r][c] ([P2] Q node; the transpose lets every GEMM take  */
+/* both operands contiguous along the contracted dimension).                 */
+/* ------------------------------------------------------------------------ */
+
+void or_quantize(const uint16_t *x, int64_t rows, int64_t cols, float scale, int fmt,
+                 uint8_t *out, uint8_t *out_t)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < rows; ++r) {
+        for (int64_t c = 0; c < cols; ++c) {
+            float v = or_bf16_to_f32(x[r * cols + c]) * scale; /* binary32 multiply */
+            uint8_t q = or_fp8_encode_f32(v, fmt);
+            if (out)
+                out[r * cols + c] = q;
+            if (out_t)
+                out_t[c * rows + r] = q;
+        }
+    }
+}
+
+/* ------------------------------------------------------------------------ */
+/* Delayed-scaling update of one tensor's state ([P1] DelayedScaling:        */
+/* margin, amax_history_len; the scale formula above).                       */
+/* ------------------------------------------------------------------------ */
+
+void or_history_update(float *hist, int32_t L, float amax, float *scale, float *scale_inv,
+                       int fmt, int32_t margin)
+{
+    for (int32_t i = L - 1; i > 0; --i)
+        hist[i] = hist[i - 1];
+    hist[0] = amax;
+    float m = 0.0f;
+    for (int32_t i = 0; i < L; ++i)
+        if (hist[i] > m)
+            m = hist[i];
+    if (m > 0.0f && isfinite(m)) {
+        float fmax = (float)or_fp8_max(fmt);
+        float q = fmax / m;                           /* binary32 divide */
+        float s = (float)ldexp((double)q, -margin);   /* exact, then one rounding */
+        if (isinf(s))
+            s = FLT_MAX;
+        *scale = s;
+        *scale_inv = 1.0f / s;                        /* binary32 divide */
+    }
+}
+
+/* ------------------------------------------------------------------------ */
+/* GEMM on FP8 operands, both stored with the contracted index contiguous:   */
+/* acc[i][j] = sum_k A[i][k] * B[j][k]  ([P3] "extension to FP8": FP8        */
+/* operands, higher-precision accumulation).                                 */
+/* ------------------------------------------------------------------------ */
+
+/* Double accumulation over output rows [row0, row0 + nrows).  Every product
+ * of two FP8 values is exact in double; only the running sum rounds. */
+void or_gemm_tn_f64(const uint8_t *A, int fa, const uint8_t *B, int fb, int64_t M, int64_t N,
+                    int64_t K, int64_t row0, int64_t nrows, double *acc)
+{
+    (void)M;
+    double ta[256], tb[256];
+    for (int c = 0; c < 256; ++c) {
+        ta[c] = or_fp8_decode((uint8_t)c, fa);
+        tb[c] = or_fp8_decode((uint8_t)c, fb);
+    }
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t i = 0; i < nrows; ++i) {
+        const uint8_t *a = A + (row0 + i) * K;
+        for (int64_t j = 0; j < N; ++j) {
+            const uint8_t *b = B + j * K;
+            double s = 0.0;
+            for (int64_t k = 0; k < K; ++k)
+                s += ta[a[k]] * tb[b[k]];
+            acc[i * N + j] = s;
+        }
+    }
+}
+
+/* Exact accumulation.  In units of 2^-16 every E4M3 value is an integer of
+ * magnitude <= 448 * 2^16 and every E5M2 value one of magnitude
+ * <= 57344 * 2^16 < 2^32, so a product is an integer (units 2^-32) below
+ * 2^64 and a sum over K <= 2^32 terms fits a signed 128-bit integer.  The
+ * exact sum is returned rounded once to double.  Non-finite codes are not
+ * allowed here (returns -1). */
+int or_gemm_tn_exact(const uint8_t *A, int fa, const uint8_t *B, int fb, int64_t M, int64_t N,
+                     int64_t K, double *acc)
+{
+    int64_t ia[256], ib[256];
+    for (int c = 0; c < 256; ++c) {
+        double da = or_fp8_decode((uint8_t)c, fa), db = or_fp8_decode((uint8_t)c, fb);
+        ia[c] = isfinite(da) ? (int64_t)ldexp(da, 16) : INT64_MIN;
+        ib[c] = isfinite(db) ? (int64_t)ldexp(db, 16) : INT64_MIN;
+    }
+    for (int64_t i = 0; i < M; ++i) {
+        for (int64_t j = 0; j < N; ++j) {
+            __int128 s = 0;
+            for (int64_t k = 0; k < K; ++k) {
+                int64_t x = ia[A[i * K + k]], y = ib[B[j * K + k]];
+                if (x == INT64_MIN || y == INT64_MIN)
+                    return -1;
+                s += (__int128)x * (__int128)y;
+            }
+            acc[i * N + j] = ldexp((double)s, -32);
+        }
+    }
+    return 0;
+}
+
+/* Dequant epilogue: y = bf16_rne(fl32(fl32(acc) * fl32(sa_inv * sb_inv))). */
+void or_epilogue(const double *acc, int64_t n, float sa_inv, float sb_inv, uint16_t *y)
+{
+    float sab = sa_inv * sb_inv;
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < n; ++i) {
+        float a = (float)acc[i];
+        y[i] = or_f32_to_bf16(a * sab);
+    }
+}
+
+int or_num_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
