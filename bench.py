@@ -1,0 +1,494 @@
+#!/usr/bin/env python3
+"""Throughput of the GB300 FP8 delayed-scaling linear layer (fwd + bwd + update).
+
+One step = one pass of the whole hot path over one batch: the fused amax +
+scaled cast + transposed copy of X, W and dY, the fprop / dgrad / wgrad FP8
+GEMMs with the dequant + amax epilogue, and the delayed-scaling update of all
+five tensors (Fp8Linear.step).  The headline workload is the 7B-shaped MLP
+up-projection (M = 8192 tokens, K = 4096, N = 11008; HYBRID, history 1024,
+margin 0).  Inputs are synthetic and seeded (fp8_workloads.py) and resident in
+HBM; two (X, dY) batches alternate, each step reading more than the 129 MB L2.
+
+Prints ONE JSON line (rank 0).  Metric: layer TFLOPS = 6 M N K per step over
+the device time of K steps (CUDA events, max over ranks).  Added keys:
+  roofline      the dominant kernel (the tcgen05 GEMM), achieved TFLOP/s vs the
+                FP8 peak derived from MEASURED_PEAKS.json (bf16 x 2)
+  cast_roofline the fused cast kernels, achieved GB/s vs measured HBM copy
+  e2e           same metric with X, dY copied in from pinned host memory and
+                Y, dX, dW copied back every step
+  cpu_baseline  the CPU oracle timed on a sample of the same layer
+  clocks        nvidia-smi SM clocks / throttle reasons sampled while timing
+
+``--impl reference`` times the CPU oracle (the only reference for this
+method) on a bounded per-step sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import dataclasses
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import fp8_workloads as wl  # noqa: E402
+
+METRIC = "FP8 linear fwd+bwd TFLOPS & % GB300 FP8 peak; cast/amax GB/s % of HBM peak"
+FP8_OVER_BF16 = 2.0       # nominal dense FP8 / BF16 tensor-core ratio (4.5 / 2.25 PFLOP/s)
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse_args():
+    p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=200)
+    p.add_argument("--warmup", type=int, default=10)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", default="mlp7b", choices=["mlp7b", "mlp70b", "drift", "tiny"])
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--secondary", action="store_true",
+                   help="also time the 70B-shaped layer and the cast sweep (extra keys)")
+    return p.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ------------------------------------------------------------- distributed --
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return world, rank
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ clocks --
+
+class ClockSampler:
+    """nvidia-smi SM clock / throttle-reason sampling (100 ms) around a region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self):
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            uuid = None
+            try:
+                uuid = str(torch.cuda.get_device_properties(torch.cuda.current_device()).uuid)
+            except Exception:
+                pass
+            target = f"GPU-{uuid}" if uuid and not uuid.startswith("GPU-") else uuid
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                   "-lms", "100"]
+            if target:
+                cmd += ["-i", target]
+            self.proc = subprocess.Popen(cmd, stdout=open(self.path, "w"),
+                                         stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            parts = [s.strip() for s in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                rows.append((float(parts[0]), float(parts[1]), parts[3:]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for _, _, r in rows:
+            for nm, v in zip(names, r[1:5]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        loaded = [s for s, _, _ in rows if s > 0.5 * rows[0][1]] or [s for s, _, _ in rows]
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(m for _, m, _ in rows),
+                "reasons": sorted(reasons), "samples": len(rows)}
+
+
+# ------------------------------------------------------------ our GPU path --
+
+class EventTimer:
+    def __init__(self):
+        self.pairs = {}
+
+    def time(self, key, fn):
+        s = torch.cuda.Event(enable_timing=True)
+        e = torch.cuda.Event(enable_timing=True)
+        s.record()
+        fn()
+        e.record()
+        self.pairs.setdefault(key, []).append((s, e))
+
+    def mean_ms(self, key):
+        return statistics.mean(s.elapsed_time(e) for s, e in self.pairs[key])
+
+
+def gemm_traffic(workload: str):
+    """Per-launch DRAM bytes of the GEMM from the committed ncu summary, or
+    None when the kernel source changed since the counters were taken."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", f"gemm_tn_kernel.{workload}.traffic.json")
+    if not os.path.exists(path):
+        return None
+    d = json.load(open(path))
+    src = open(os.path.join(ROOT, "fp8_mixed_precision_amax_gb300", "csrc", "gemm.cu"), "rb").read()
+    if hashlib.sha256(src).hexdigest() != d.get("gemm_cu_sha256"):
+        return None
+    return d.get("bytes_per_launch_mean")
+
+
+def run_layer_bench(f, w: wl.Workload, args, world, pk, peak_kind):
+    dev = torch.device("cuda")
+    W = wl.layer_weight(w, dev)
+    xs = [wl.layer_x(w, s, dev) for s in (0, 1)]
+    dys = [wl.layer_dy(w, s, dev) for s in (0, 1)]
+    lin = f.Fp8Linear(W, w.M, f.Recipe(margin=w.margin, history_len=w.history_len,
+                                       hybrid=w.hybrid))
+    stream = torch.cuda.current_stream()
+    allreduce = None
+    if world > 1:
+        import torch.distributed as dist
+        # data-parallel replicas agree on scales: MAX of the five amaxes
+        allreduce = lambda: dist.all_reduce(lin.meta.amax, op=dist.ReduceOp.MAX)
+
+    def step(i):
+        lin.forward(xs[i % 2])
+        lin.backward(dys[i % 2])
+        if allreduce:
+            allreduce()
+        lin.update()
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    f.fp8_sync_status()
+
+    clocks = ClockSampler()
+    clocks.start()
+    time.sleep(0.25)
+    barrier(world)
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for i in range(args.steps):
+        step(i)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    ms = max_over_ranks(t0.elapsed_time(t1), world)
+
+    # per-kernel breakdown: the same step issued as its individual C-ABI calls
+    tm = EventTimer()
+    m = lin.meta
+    fg = f.E5M2 if w.hybrid else f.E4M3
+    E4 = f.E4M3
+    nb = max(10, min(args.steps, 100))
+    for i in range(nb):
+        X, dY = xs[i % 2], dys[i % 2]
+        tm.time("cast_X", lambda: f.fp8_quantize_transpose(X, m.scale[0:1], E4, lin.X8, lin.X8t,
+                                                           m.amax[0:1]))
+        tm.time("cast_W", lambda: f.fp8_quantize_transpose(W, m.scale[1:2], E4, lin.W8, lin.W8t,
+                                                           m.amax[1:2]))
+        tm.time("gemm_fprop", lambda: f.fp8_gemm_tn(lin.X8, E4, lin.W8, E4, m.scale_inv[0:1],
+                                                    m.scale_inv[1:2], lin.Y, m.amax[2:3]))
+        tm.time("cast_dY", lambda: f.fp8_quantize_transpose(dY, m.scale[3:4], fg, lin.dY8,
+                                                            lin.dY8t, m.amax[3:4]))
+        tm.time("gemm_dgrad", lambda: f.fp8_gemm_tn(lin.dY8, fg, lin.W8t, E4, m.scale_inv[3:4],
+                                                    m.scale_inv[1:2], lin.dX, m.amax[4:5]))
+        tm.time("gemm_wgrad", lambda: f.fp8_gemm_tn(lin.dY8t, fg, lin.X8t, E4, m.scale_inv[3:4],
+                                                    m.scale_inv[0:1], lin.dW))
+        tm.time("update", lambda: lin.update())
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    f.fp8_sync_status()
+
+    M, N, K = w.M, w.N, w.K
+    flops = 6 * M * N * K
+    value = world * args.steps * flops / (ms / 1e3) / 1e12
+    gemm_ms = {k: tm.mean_ms(k) for k in ("gemm_fprop", "gemm_dgrad", "gemm_wgrad")}
+    cast_ms = {k: tm.mean_ms(k) for k in ("cast_X", "cast_W", "cast_dY")}
+    upd_ms = tm.mean_ms("update")
+    gemm_avg = statistics.mean(gemm_ms.values())
+    fp8_peak = pk["bf16_tflops"] * FP8_OVER_BF16
+    achieved = 2 * M * N * K / (gemm_avg / 1e3) / 1e12
+    cast_bytes = {"cast_X": 4 * M * K, "cast_W": 4 * N * K, "cast_dY": 4 * M * N}
+    cast_gbs = sum(cast_bytes.values()) / (sum(cast_ms.values()) / 1e3) / 1e9
+    traffic = gemm_traffic(w.name)
+    res = {
+        "value": value, "ms_per_step": ms / args.steps,
+        "roofline": {"bound": "tensor", "kernel": "gemm_tn_kernel", "achieved": achieved,
+                     "peak": fp8_peak, "unit": "TFLOP/s", "frac": achieved / fp8_peak,
+                     "traffic": traffic,
+                     "peak_basis": f"{peak_kind} bf16 burst {pk['bf16_tflops']} x {FP8_OVER_BF16}",
+                     "per_gemm_ms": gemm_ms,
+                     "per_gemm_tflops": {k: 2 * M * N * K / (v / 1e3) / 1e12
+                                         for k, v in gemm_ms.items()}},
+        "cast_roofline": {"bound": "hbm", "kernel": "quantize_transpose_kernel",
+                          "achieved": cast_gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                          "frac": cast_gbs / pk["hbm_gbs"],
+                          "bytes_per_element": 4,
+                          "per_cast_gbs": {k: cast_bytes[k] / (v / 1e3) / 1e9
+                                           for k, v in cast_ms.items()},
+                          "update_us": upd_ms * 1e3},
+        "clocks": clk,
+        "gpu_launches": 7 * args.steps,
+        "breakdown_ms": {**gemm_ms, **cast_ms, "update": upd_ms},
+    }
+
+    if not args.no_e2e:
+        res["e2e"] = run_e2e(f, lin, xs[0], dys[0], args, world, flops)
+    return res
+
+
+def run_e2e(f, lin, X, dY, args, world, flops):
+    """Same metric through the public API from pinned host buffers: each step
+    copies X and dY in and Y, dX, dW out, inside the timed region."""
+    hX = torch.empty_like(X, device="cpu").pin_memory()
+    hdY = torch.empty_like(dY, device="cpu").pin_memory()
+    hX.copy_(X)
+    hdY.copy_(dY)
+    dX_in = torch.empty_like(X)
+    ddY_in = torch.empty_like(dY)
+    outs = [torch.empty_like(t, device="cpu").pin_memory() for t in (lin.Y, lin.dX, lin.dW)]
+    n = max(5, min(args.steps, 50))
+
+    def step():
+        dX_in.copy_(hX, non_blocking=True)
+        ddY_in.copy_(hdY, non_blocking=True)
+        lin.step(dX_in, ddY_in)
+        for h, d in zip(outs, (lin.Y, lin.dX, lin.dW)):
+            h.copy_(d, non_blocking=True)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    barrier(world)
+    s = torch.cuda.Event(enable_timing=True)
+    e = torch.cuda.Event(enable_timing=True)
+    s.record()
+    for _ in range(n):
+        step()
+    e.record()
+    torch.cuda.synchronize()
+    barrier(world)
+    ms = max_over_ranks(s.elapsed_time(e), world)
+    h2d = X.numel() * 2 + dY.numel() * 2
+    d2h = sum(t.numel() * 2 for t in outs)
+    return {"value": world * n * flops / (ms / 1e3) / 1e12, "unit": "TFLOPS",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n}
+
+
+# ------------------------------------------------------------- CPU oracle --
+
+def oracle_sample_step(o, w: wl.Workload, Mp: int, Np: int, state):
+    """One oracle layer step on a Mp-token x Np-feature slice of the workload
+    (full K): casts of the slice's X, W and dY, the three GEMMs, the update."""
+    s = dataclasses.replace(w, M=Mp, N=Np)
+    X = wl.bf16_bits(wl.layer_x(s, 0))
+    W = wl.bf16_bits(wl.layer_weight(s))
+    dY = wl.bf16_bits(wl.layer_dy(s, 0))
+    rc = o.Recipe(margin=w.margin, history_len=w.history_len, hybrid=w.hybrid)
+    st = state if state is not None else o.State.initial(w.history_len)
+    t = time.perf_counter()
+    fo = o.layer_fwd(st, rc, X, W)
+    o.layer_bwd(st, rc, dY, fo["X8t"], fo["W8t"])
+    o.layer_update(st, rc)
+    return time.perf_counter() - t, 6 * Mp * Np * w.K, st
+
+
+def cpu_baseline(w: wl.Workload, seconds: float = 12.0, Mp: int = 256, Np: int = 1024):
+    import oracle as o
+    st = None
+    total_t, total_f, reps = 0.0, 0, 0
+    while total_t < seconds or reps < 2:
+        dt, fl, st = oracle_sample_step(o, w, Mp, Np, st)
+        total_t += dt
+        total_f += fl
+        reps += 1
+    return {"value": total_f / total_t / 1e12, "unit": "TFLOPS", "cores": o.num_threads(),
+            "kind": "oracle",
+            "sample": f"{reps} oracle layer steps on a {Mp}-token x {Np}-feature slice of "
+                      f"{w.name} (K={w.K}), {total_t:.1f} s of CPU time"}
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return None
+    import oracle as o
+    w = wl.WORKLOADS[args.workload]
+    # size the per-step sample so the whole run takes about two minutes
+    dt, fl, _ = oracle_sample_step(o, w, 64, 256, None)
+    rate = fl / dt
+    budget = 120.0 / max(1, args.steps + args.warmup)
+    Mp, Np = 64, 256
+    for mp, np_ in [(128, 256), (128, 512), (256, 512), (256, 1024), (512, 1024)]:
+        if 6 * mp * np_ * w.K / rate <= budget:
+            Mp, Np = mp, np_
+    st = None
+    for _ in range(args.warmup):
+        _, _, st = oracle_sample_step(o, w, Mp, Np, st)
+    tt, ff = 0.0, 0
+    for _ in range(args.steps):
+        dt, fl, st = oracle_sample_step(o, w, Mp, Np, st)
+        tt += dt
+        ff += fl
+    value = ff / tt / 1e12
+    sample = (f"each step: oracle layer step on a {Mp}-token x {Np}-feature slice of "
+              f"{w.name} (full K={w.K})")
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOPS",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": tt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64 (oracle, exact FP8 decode)", "data": "synthetic",
+            "config": workload_config(w),
+            "cpu_baseline": {"kind": "oracle", "cores": o.num_threads(), "sample": sample,
+                             "value": value, "unit": "TFLOPS"},
+            "e2e": {"value": value, "unit": "TFLOPS", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def workload_config(w: wl.Workload):
+    return {"workload": f"{w.name}: single FP8 linear fwd+bwd+update, M={w.M} tokens, K={w.K}, "
+                        f"N={w.N}, {'HYBRID' if w.hybrid else 'E4M3'}, history {w.history_len}, "
+                        f"margin {w.margin}",
+            "M": w.M, "K": w.K, "N": w.N, "x": w.x_kind, "history_len": w.history_len,
+            "margin": w.margin, "format": "HYBRID" if w.hybrid else "E4M3",
+            "l2": "inputs larger than L2: X, W, dY = %d MB read per step, two batches alternate"
+                  % ((2 * w.M * w.K + 2 * w.N * w.K + 2 * w.M * w.N) // 2 ** 20)}
+
+
+def run_secondary(f, args, pk):
+    """The 70B-shaped layer (device time only) and the cast sweep GB/s."""
+    out = {}
+    w = wl.WORKLOADS["mlp70b"]
+    sub = argparse.Namespace(**{**vars(args), "steps": max(10, min(args.steps, 30)),
+                                "warmup": 3, "no_e2e": True})
+    r = run_layer_bench(f, w, sub, 1, pk, "measured")
+    out["mlp70b"] = {"value": r["value"], "unit": "TFLOPS", "ms_per_step": r["ms_per_step"],
+                     "gemm_frac": r["roofline"]["frac"],
+                     "gemm_tflops": r["roofline"]["achieved"],
+                     "cast_gbs": r["cast_roofline"]["achieved"]}
+    sweep = {}
+    for n in (24, 26, 28):
+        x = wl.sweep_tensor(n, device="cuda")
+        rows, cols = x.shape
+        o8 = torch.empty((rows, cols), dtype=torch.uint8, device="cuda")
+        o8t = torch.empty((cols, rows), dtype=torch.uint8, device="cuda")
+        am = torch.empty(1, device="cuda")
+        sc = torch.ones(1, device="cuda")
+        tm = EventTimer()
+        for i in range(23):
+            tm.time("amax", lambda: f.fp8_amax(x, am))
+            tm.time("cast", lambda: f.fp8_quantize_transpose(x, sc, 0, o8, o8t, am))
+        torch.cuda.synchronize()
+        tm.pairs = {k: v[3:] for k, v in tm.pairs.items()}
+        ne = rows * cols
+        sweep[f"2^{n}"] = {"amax_gbs": 2 * ne / (tm.mean_ms("amax") / 1e3) / 1e9,
+                           "cast_transpose_gbs": 4 * ne / (tm.mean_ms("cast") / 1e3) / 1e9}
+        del x, o8, o8t
+    out["cast_sweep"] = sweep
+    return out
+
+
+def main():
+    args = parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    world, rank = dist_setup(args)
+    if args.impl == "reference":
+        line = run_reference(args, world, rank)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return
+    from fp8_mixed_precision_amax_gb300 import build as _build
+    _build.build()
+    import fp8_mixed_precision_amax_gb300 as f
+    pk, peak_kind = peaks()
+    w = wl.WORKLOADS[args.workload]
+    r = run_layer_bench(f, w, args, world, pk, peak_kind)
+    line = {
+        "metric": METRIC, "value": r["value"], "unit": "TFLOPS", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": r["ms_per_step"],
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "fp8 e4m3/e5m2 operands, f32 accumulate, bf16 out",
+        "data": "synthetic (seeded fp8_workloads, resident in HBM)",
+        "config": {**workload_config(w), "parallelism": f"dp{world} replicas"
+                   + (" + amax MAX all-reduce" if world > 1 else "")},
+        "roofline": r["roofline"], "cast_roofline": r["cast_roofline"], "clocks": r["clocks"],
+        "gpu_launches": r["gpu_launches"], "breakdown_ms": r["breakdown_ms"],
+        "peaks_source": peak_kind,
+    }
+    if "e2e" in r:
+        line["e2e"] = r["e2e"]
+    if args.secondary and rank == 0:
+        line["secondary"] = run_secondary(f, args, pk)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

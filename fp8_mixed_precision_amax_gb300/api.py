@@ -1,0 +1,289 @@
+"""Python binding of the C ABI in include/fp8amax.h (argument marshalling only).
+
+Every function here has the name of the C entry point it calls.  It checks
+that the torch tensors it is given are CUDA tensors of the right dtype,
+shape and layout, passes their device pointers and the current torch CUDA
+stream to the library, and raises ``Fp8Error`` on a non-OK status.  Every
+step of the computation runs in the library's sm_103a kernels; there is no
+fallback: if ``libfp8amax.so`` is missing, importing this module fails.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+from dataclasses import dataclass
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libfp8amax.so")
+HEADER_PATH = os.path.join(os.path.dirname(_PKG), "include", "fp8amax.h")
+
+E4M3, E5M2 = 0, 1
+SLOT_X, SLOT_W, SLOT_Y, SLOT_DY, SLOT_DX = range(5)
+NUM_SLOTS = 5
+STATUS = {0: "FP8_OK", 1: "FP8_ERR_ARG", 2: "FP8_ERR_ALIGN", 3: "FP8_ERR_CUDA",
+          4: "FP8_ERR_TIMEOUT", 5: "FP8_ERR_UNSUPPORTED"}
+
+
+class Fp8Error(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS.get(status, status)}: {message}")
+        self.status = status
+
+
+class fp8_meta(ctypes.Structure):
+    _fields_ = [("history", ctypes.c_void_p), ("amax", ctypes.c_void_p),
+                ("scale", ctypes.c_void_p), ("scale_inv", ctypes.c_void_p),
+                ("history_len", ctypes.c_int32)]
+
+
+class fp8_recipe(ctypes.Structure):
+    _fields_ = [("margin", ctypes.c_int32), ("history_len", ctypes.c_int32),
+                ("hybrid", ctypes.c_int32)]
+
+
+def _load() -> ctypes.CDLL:
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"{LIB_PATH} is not built; call fp8_mixed_precision_amax_gb300.build.build()")
+    lib = ctypes.CDLL(LIB_PATH)
+    vp, i64, i32, u32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_uint32
+    sig = {
+        "fp8_abi_version": ([], i32),
+        "fp8_last_error": ([], ctypes.c_char_p),
+        "fp8_sync_status": ([vp], ctypes.c_int),
+        "fp8_amax": ([vp, i64, vp, vp], ctypes.c_int),
+        "fp8_quantize_transpose": ([vp, i64, i64, vp, i32, vp, vp, vp, vp], ctypes.c_int),
+        "fp8_scale_update": ([vp, vp, vp, vp, i32, i32, u32, i32, vp], ctypes.c_int),
+        "fp8_amax_scale_update": ([ctypes.POINTER(fp8_meta), ctypes.POINTER(fp8_recipe), vp],
+                                  ctypes.c_int),
+        "fp8_gemm_tn": ([vp, i32, vp, i32, i64, i64, i64, vp, vp, vp, vp, vp], ctypes.c_int),
+        "fp8_linear_fwd": ([vp, vp, i64, i64, i64, ctypes.POINTER(fp8_meta),
+                            ctypes.POINTER(fp8_recipe), vp, vp, vp, vp, vp, vp], ctypes.c_int),
+        "fp8_linear_bwd": ([vp, i64, i64, i64, ctypes.POINTER(fp8_meta),
+                            ctypes.POINTER(fp8_recipe), vp, vp, vp, vp, vp, vp, vp],
+                           ctypes.c_int),
+    }
+    for name, (args, res) in sig.items():
+        f = getattr(lib, name)
+        f.argtypes, f.restype = args, res
+    if lib.fp8_abi_version() != 1:
+        raise ImportError("libfp8amax.so ABI version mismatch")
+    return lib
+
+
+_lib = _load()
+
+
+def header_functions() -> list[str]:
+    """Names of the functions include/fp8amax.h declares."""
+    src = open(HEADER_PATH).read()
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(fp8_\w+)\s*\(", src, re.M)))
+
+
+def library() -> ctypes.CDLL:
+    return _lib
+
+
+def _check(status: int) -> None:
+    if status != 0:
+        raise Fp8Error(status, _lib.fp8_last_error().decode())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    if isinstance(stream, torch.cuda.Stream):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+def _ptr(t: torch.Tensor | None, dtype=None, name="tensor"):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+_U8 = torch.uint8
+
+
+def _fp8_view_ok(t):
+    return t.dtype in (torch.uint8, torch.float8_e4m3fn, torch.float8_e5m2)
+
+
+def _p8(t, name):
+    if t is None:
+        return None
+    if not _fp8_view_ok(t):
+        raise ValueError(f"{name} must hold FP8 codes (uint8 / float8), got {t.dtype}")
+    return _ptr(t, None, name)
+
+
+# ------------------------------------------------------------ entry points --
+
+def fp8_sync_status(stream=None) -> None:
+    _check(_lib.fp8_sync_status(_stream(stream)))
+
+
+def fp8_amax(x: torch.Tensor, amax: torch.Tensor, stream=None) -> None:
+    _check(_lib.fp8_amax(_ptr(x, torch.bfloat16, "x"), x.numel(), _ptr(amax, torch.float32, "amax"),
+                         _stream(stream)))
+
+
+def fp8_quantize_transpose(x: torch.Tensor, scale: torch.Tensor, fmt: int, out=None, out_t=None,
+                           amax=None, stream=None) -> None:
+    rows, cols = x.shape
+    if out is not None and tuple(out.shape) != (rows, cols):
+        raise ValueError("out must be [rows, cols]")
+    if out_t is not None and tuple(out_t.shape) != (cols, rows):
+        raise ValueError("out_t must be [cols, rows]")
+    _check(_lib.fp8_quantize_transpose(_ptr(x, torch.bfloat16, "x"), rows, cols,
+                                       _ptr(scale, torch.float32, "scale"), fmt, _p8(out, "out"),
+                                       _p8(out_t, "out_t"), _ptr(amax, torch.float32, "amax"),
+                                       _stream(stream)))
+
+
+def fp8_scale_update(history: torch.Tensor, amax: torch.Tensor, scale: torch.Tensor,
+                     scale_inv: torch.Tensor, format_mask: int, margin: int, stream=None) -> None:
+    n, L = history.shape
+    _check(_lib.fp8_scale_update(_ptr(history, torch.float32, "history"),
+                                 _ptr(amax, torch.float32, "amax"),
+                                 _ptr(scale, torch.float32, "scale"),
+                                 _ptr(scale_inv, torch.float32, "scale_inv"), n, L, format_mask,
+                                 margin, _stream(stream)))
+
+
+def fp8_gemm_tn(A: torch.Tensor, fa: int, B: torch.Tensor, fb: int, a_scale_inv: torch.Tensor,
+                b_scale_inv: torch.Tensor, D: torch.Tensor, d_amax=None, stream=None) -> None:
+    M, K = A.shape
+    N, K2 = B.shape
+    if K != K2 or tuple(D.shape) != (M, N):
+        raise ValueError("shapes: A [M,K], B [N,K], D [M,N]")
+    _check(_lib.fp8_gemm_tn(_p8(A, "A"), fa, _p8(B, "B"), fb, M, N, K,
+                            _ptr(a_scale_inv, torch.float32, "a_scale_inv"),
+                            _ptr(b_scale_inv, torch.float32, "b_scale_inv"),
+                            _ptr(D, torch.bfloat16, "D"), _ptr(d_amax, torch.float32, "d_amax"),
+                            _stream(stream)))
+
+
+# ------------------------------------------------------------------ layer --
+
+@dataclass
+class Recipe:
+    """DelayedScaling: margin (default 0), amax_history_len (default 1024),
+    HYBRID (E4M3 forward, E5M2 backward) or E4M3 everywhere."""
+    margin: int = 0
+    history_len: int = 1024
+    hybrid: bool = True
+
+    def c(self) -> fp8_recipe:
+        return fp8_recipe(self.margin, self.history_len, 1 if self.hybrid else 0)
+
+
+class Meta:
+    """Per-layer scaling state on the device: history [5, L], amax [5],
+    scale [5], scale_inv [5] (fp32), initialised to 0 / 0 / 1 / 1."""
+
+    def __init__(self, history_len: int, device="cuda"):
+        self.history = torch.zeros((NUM_SLOTS, history_len), dtype=torch.float32, device=device)
+        self.amax = torch.zeros(NUM_SLOTS, dtype=torch.float32, device=device)
+        self.scale = torch.ones(NUM_SLOTS, dtype=torch.float32, device=device)
+        self.scale_inv = torch.ones(NUM_SLOTS, dtype=torch.float32, device=device)
+        self.history_len = history_len
+
+    def c(self) -> fp8_meta:
+        return fp8_meta(self.history.data_ptr(), self.amax.data_ptr(), self.scale.data_ptr(),
+                        self.scale_inv.data_ptr(), self.history_len)
+
+    def state_dict(self) -> dict:
+        return {"history": self.history.clone(), "amax": self.amax.clone(),
+                "scale": self.scale.clone(), "scale_inv": self.scale_inv.clone()}
+
+    def load_state_dict(self, d: dict) -> None:
+        for k in ("history", "amax", "scale", "scale_inv"):
+            getattr(self, k).copy_(d[k])
+
+
+def fp8_amax_scale_update(meta: Meta, recipe: Recipe, stream=None) -> None:
+    m, r = meta.c(), recipe.c()
+    _check(_lib.fp8_amax_scale_update(ctypes.byref(m), ctypes.byref(r), _stream(stream)))
+
+
+def fp8_linear_fwd(X, W, meta: Meta, recipe: Recipe, X8, X8t, W8, W8t, Y, stream=None) -> None:
+    M, K = X.shape
+    N, K2 = W.shape
+    if K != K2 or tuple(Y.shape) != (M, N):
+        raise ValueError("shapes: X [M,K], W [N,K], Y [M,N]")
+    for t, shp, nm in [(X8, (M, K), "X8"), (X8t, (K, M), "X8t"), (W8, (N, K), "W8"),
+                       (W8t, (K, N), "W8t")]:
+        if tuple(t.shape) != shp:
+            raise ValueError(f"{nm} must be {list(shp)}")
+    m, r = meta.c(), recipe.c()
+    _check(_lib.fp8_linear_fwd(_ptr(X, torch.bfloat16, "X"), _ptr(W, torch.bfloat16, "W"), M, N, K,
+                               ctypes.byref(m), ctypes.byref(r), _p8(X8, "X8"), _p8(X8t, "X8t"),
+                               _p8(W8, "W8"), _p8(W8t, "W8t"), _ptr(Y, torch.bfloat16, "Y"),
+                               _stream(stream)))
+
+
+def fp8_linear_bwd(dY, meta: Meta, recipe: Recipe, X8t, W8t, dY8, dY8t, dX, dW,
+                   stream=None) -> None:
+    M, N = dY.shape
+    K = X8t.shape[0]
+    for t, shp, nm in [(X8t, (K, M), "X8t"), (W8t, (K, N), "W8t"), (dY8, (M, N), "dY8"),
+                       (dY8t, (N, M), "dY8t")]:
+        if tuple(t.shape) != shp:
+            raise ValueError(f"{nm} must be {list(shp)}")
+    if tuple(dX.shape) != (M, K) or tuple(dW.shape) != (N, K):
+        raise ValueError("dX must be [M,K] and dW [N,K]")
+    m, r = meta.c(), recipe.c()
+    _check(_lib.fp8_linear_bwd(_ptr(dY, torch.bfloat16, "dY"), M, N, K, ctypes.byref(m),
+                               ctypes.byref(r), _p8(X8t, "X8t"), _p8(W8t, "W8t"),
+                               _p8(dY8, "dY8"), _p8(dY8t, "dY8t"), _ptr(dX, torch.bfloat16, "dX"),
+                               _ptr(dW, torch.bfloat16, "dW"), _stream(stream)))
+
+
+class Fp8Linear:
+    """One FP8 linear layer Y = X W^T with delayed per-tensor scaling (the
+    te.Linear + fp8_autocast + DelayedScaling pattern): owns the weight, the
+    scaling state and the FP8 buffers kept between forward and backward.
+    ``step`` = forward, backward, then the recipe's scale update, all enqueued
+    on the current stream with no host synchronisation."""
+
+    def __init__(self, W: torch.Tensor, M: int, recipe: Recipe | None = None):
+        self.recipe = recipe or Recipe()
+        self.W = W
+        N, K = W.shape
+        dev = W.device
+        self.M, self.N, self.K = M, N, K
+        self.meta = Meta(self.recipe.history_len, dev)
+        e = lambda *s: torch.empty(s, dtype=torch.uint8, device=dev)
+        self.X8, self.X8t, self.W8, self.W8t = e(M, K), e(K, M), e(N, K), e(K, N)
+        self.dY8, self.dY8t = e(M, N), e(N, M)
+        b = lambda *s: torch.empty(s, dtype=torch.bfloat16, device=dev)
+        self.Y, self.dX, self.dW = b(M, N), b(M, K), b(N, K)
+
+    def forward(self, X: torch.Tensor, stream=None) -> torch.Tensor:
+        fp8_linear_fwd(X, self.W, self.meta, self.recipe, self.X8, self.X8t, self.W8, self.W8t,
+                       self.Y, stream)
+        return self.Y
+
+    def backward(self, dY: torch.Tensor, stream=None):
+        fp8_linear_bwd(dY, self.meta, self.recipe, self.X8t, self.W8t, self.dY8, self.dY8t,
+                       self.dX, self.dW, stream)
+        return self.dX, self.dW
+
+    def update(self, stream=None) -> None:
+        fp8_amax_scale_update(self.meta, self.recipe, stream)
+
+    def step(self, X: torch.Tensor, dY: torch.Tensor, stream=None):
+        self.forward(X, stream)
+        self.backward(dY, stream)
+        self.update(stream)
+        return self.Y, self.dX, self.dW

@@ -1,0 +1,299 @@
+// abi.cu -- the exported C entry points (include/fp8amax.h): argument checks
+// on the host, then the launches, in stream order, of the kernels in cast.cu
+// and gemm.cu.  No device memory is allocated here and the stream is never
+// synchronized (except by fp8_sync_status).
+#include <cuda_runtime.h>
+
+#include <cstdarg>
+#include <cstdint>
+#include <cstdio>
+#include <mutex>
+#include <string>
+
+#include "../../include/fp8amax.h"
+#include "kernels.h"
+
+namespace {
+
+thread_local std::string g_last_error;
+
+fp8_status fail(fp8_status s, const char *fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return s;
+}
+
+fp8_status cuda_fail(cudaError_t e, const char *where) {
+    return fail(FP8_ERR_CUDA, "%s: %s", where, cudaGetErrorString(e));
+}
+
+constexpr int kMaxDevices = 64;
+struct DeviceInfo {
+    int sm_count = 0;
+    bool supported = false;
+};
+DeviceInfo g_dev[kMaxDevices];
+std::once_flag g_dev_once[kMaxDevices];
+
+// SM count of the current device; FP8_ERR_UNSUPPORTED unless it is an sm_103 GPU.
+fp8_status current_device(int *sm_count) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices) return fail(FP8_ERR_UNSUPPORTED, "device index %d", dev);
+    std::call_once(g_dev_once[dev], [dev] {
+        int major = 0, minor = 0, sms = 0;
+        cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        g_dev[dev].sm_count = sms;
+        g_dev[dev].supported = (major == 10 && minor == 3);
+    });
+    if (!g_dev[dev].supported)
+        return fail(FP8_ERR_UNSUPPORTED, "device %d is not an sm_103 GPU", dev);
+    *sm_count = g_dev[dev].sm_count;
+    return FP8_OK;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+fp8_status check_dims16(const char *fn, int64_t a, const char *na, int64_t b, const char *nb) {
+    if (a < 0 || b < 0) return fail(FP8_ERR_ARG, "%s: negative size (%s=%lld, %s=%lld)", fn, na,
+                                    (long long)a, nb, (long long)b);
+    if (a % 16 || b % 16)
+        return fail(FP8_ERR_ALIGN, "%s: %s=%lld and %s=%lld must be multiples of 16", fn, na,
+                    (long long)a, nb, (long long)b);
+    if (a > (int64_t(1) << 31) || b > (int64_t(1) << 31))
+        return fail(FP8_ERR_ARG, "%s: dimension above 2^31", fn);
+    return FP8_OK;
+}
+
+fp8_status check_ptr(const char *fn, const void *p, const char *name, bool may_be_null) {
+    if (p == nullptr) {
+        if (may_be_null) return FP8_OK;
+        return fail(FP8_ERR_ARG, "%s: %s is NULL", fn, name);
+    }
+    if (!aligned16(p)) return fail(FP8_ERR_ALIGN, "%s: %s is not 16-byte aligned", fn, name);
+    return FP8_OK;
+}
+
+// A pointer to one fp32 scalar (scale, scale_inv, amax) needs 4-byte alignment.
+fp8_status check_scalar(const char *fn, const void *p, const char *name, bool may_be_null) {
+    if (p == nullptr) {
+        if (may_be_null) return FP8_OK;
+        return fail(FP8_ERR_ARG, "%s: %s is NULL", fn, name);
+    }
+    if (reinterpret_cast<uintptr_t>(p) & 3u)
+        return fail(FP8_ERR_ALIGN, "%s: %s is not 4-byte aligned", fn, name);
+    return FP8_OK;
+}
+
+#define FP8_TRY(expr)                       \
+    do {                                    \
+        fp8_status s_ = (expr);             \
+        if (s_ != FP8_OK) return s_;        \
+    } while (0)
+
+#define FP8_CUDA(expr, where)                          \
+    do {                                               \
+        cudaError_t e_ = (expr);                       \
+        if (e_ != cudaSuccess) return cuda_fail(e_, where); \
+    } while (0)
+
+fp8_status check_meta(const char *fn, const fp8_meta *m, const fp8_recipe *r) {
+    if (m == nullptr || r == nullptr) return fail(FP8_ERR_ARG, "%s: meta or recipe is NULL", fn);
+    if (m->history == nullptr || m->amax == nullptr || m->scale == nullptr ||
+        m->scale_inv == nullptr)
+        return fail(FP8_ERR_ARG, "%s: a meta buffer is NULL", fn);
+    if ((reinterpret_cast<uintptr_t>(m->history) | reinterpret_cast<uintptr_t>(m->amax) |
+         reinterpret_cast<uintptr_t>(m->scale) | reinterpret_cast<uintptr_t>(m->scale_inv)) & 3u)
+        return fail(FP8_ERR_ALIGN, "%s: a meta buffer is not 4-byte aligned", fn);
+    if (r->margin < 0 || r->margin > 64)
+        return fail(FP8_ERR_ARG, "%s: margin %d outside [0, 64]", fn, r->margin);
+    if (r->history_len < 1 || r->history_len > 8192 || m->history_len != r->history_len)
+        return fail(FP8_ERR_ARG, "%s: history_len %d (meta %d) must match and lie in [1, 8192]",
+                    fn, r->history_len, m->history_len);
+    if (r->hybrid != 0 && r->hybrid != 1)
+        return fail(FP8_ERR_ARG, "%s: hybrid must be 0 or 1", fn);
+    return FP8_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t fp8_abi_version(void) { return FP8AMAX_ABI_VERSION; }
+
+const char *fp8_last_error(void) { return g_last_error.c_str(); }
+
+fp8_status fp8_sync_status(void *stream) {
+    unsigned flags = 0;
+    cudaError_t e = fp8k::read_and_clear_error_flag(&flags, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "fp8_sync_status");
+    if (flags & 1u) return fail(FP8_ERR_TIMEOUT, "a kernel gave up a bounded wait");
+    return FP8_OK;
+}
+
+fp8_status fp8_amax(const void *x, int64_t n, float *amax, void *stream) {
+    const char *fn = "fp8_amax";
+    FP8_TRY(check_dims16(fn, n, "n", 0, "-"));
+    FP8_TRY(check_ptr(fn, x, "x", n == 0));
+    FP8_TRY(check_scalar(fn, amax, "amax", false));
+    int sms;
+    FP8_TRY(current_device(&sms));
+    FP8_CUDA(fp8k::launch_amax(x, n, amax, sms, static_cast<cudaStream_t>(stream)), fn);
+    return FP8_OK;
+}
+
+fp8_status fp8_quantize_transpose(const void *x, int64_t rows, int64_t cols, const float *scale,
+                                  int32_t fmt, uint8_t *out, uint8_t *out_t, float *amax,
+                                  void *stream) {
+    const char *fn = "fp8_quantize_transpose";
+    FP8_TRY(check_dims16(fn, rows, "rows", cols, "cols"));
+    if (fmt != FP8_E4M3 && fmt != FP8_E5M2) return fail(FP8_ERR_ARG, "%s: bad format %d", fn, fmt);
+    if (out == nullptr && out_t == nullptr)
+        return fail(FP8_ERR_ARG, "%s: out and out_t are both NULL", fn);
+    const bool empty = rows == 0 || cols == 0;
+    FP8_TRY(check_ptr(fn, x, "x", empty));
+    FP8_TRY(check_scalar(fn, scale, "scale", false));
+    FP8_TRY(check_ptr(fn, out, "out", true));
+    FP8_TRY(check_ptr(fn, out_t, "out_t", true));
+    FP8_TRY(check_scalar(fn, amax, "amax", true));
+    int sms;
+    FP8_TRY(current_device(&sms));
+    FP8_CUDA(fp8k::launch_quantize_transpose(x, rows, cols, scale, fmt, out, out_t, amax, true, sms,
+                                             static_cast<cudaStream_t>(stream)),
+             fn);
+    return FP8_OK;
+}
+
+fp8_status fp8_scale_update(float *history, const float *amax, float *scale, float *scale_inv,
+                            int32_t num_tensors, int32_t history_len, uint32_t format_mask,
+                            int32_t margin, void *stream) {
+    const char *fn = "fp8_scale_update";
+    if (num_tensors < 1 || num_tensors > 32)
+        return fail(FP8_ERR_ARG, "%s: num_tensors %d outside [1, 32]", fn, num_tensors);
+    if (history_len < 1 || history_len > 8192)
+        return fail(FP8_ERR_ARG, "%s: history_len %d outside [1, 8192]", fn, history_len);
+    if (margin < 0 || margin > 64)
+        return fail(FP8_ERR_ARG, "%s: margin %d outside [0, 64]", fn, margin);
+    FP8_TRY(check_scalar(fn, history, "history", false));
+    FP8_TRY(check_scalar(fn, amax, "amax", false));
+    FP8_TRY(check_scalar(fn, scale, "scale", false));
+    FP8_TRY(check_scalar(fn, scale_inv, "scale_inv", false));
+    int sms;
+    FP8_TRY(current_device(&sms));
+    FP8_CUDA(fp8k::launch_scale_update(history, amax, scale, scale_inv, num_tensors, history_len,
+                                       format_mask, margin, static_cast<cudaStream_t>(stream)),
+             fn);
+    return FP8_OK;
+}
+
+fp8_status fp8_amax_scale_update(const fp8_meta *meta, const fp8_recipe *recipe, void *stream) {
+    FP8_TRY(check_meta("fp8_amax_scale_update", meta, recipe));
+    const uint32_t mask = recipe->hybrid ? ((1u << FP8_SLOT_DY) | (1u << FP8_SLOT_DX)) : 0u;
+    return fp8_scale_update(meta->history, meta->amax, meta->scale, meta->scale_inv, FP8_NUM_SLOTS,
+                            meta->history_len, mask, recipe->margin, stream);
+}
+
+static fp8_status gemm_checked(const char *fn, const uint8_t *A, int32_t fa, const uint8_t *B,
+                               int32_t fb, int64_t M, int64_t N, int64_t K, const float *sa,
+                               const float *sb, void *D, float *d_amax, bool zero_amax, int sms,
+                               cudaStream_t st) {
+    const char *what = nullptr;
+    cudaError_t e =
+        fp8k::launch_gemm_tn(A, fa, B, fb, M, N, K, sa, sb, D, d_amax, zero_amax, sms, st, &what);
+    if (e != cudaSuccess)
+        return what ? fail(FP8_ERR_CUDA, "%s: %s", fn, what) : cuda_fail(e, fn);
+    return FP8_OK;
+}
+
+fp8_status fp8_gemm_tn(const uint8_t *A, int32_t fa, const uint8_t *B, int32_t fb, int64_t M,
+                       int64_t N, int64_t K, const float *a_scale_inv, const float *b_scale_inv,
+                       void *D, float *d_amax, void *stream) {
+    const char *fn = "fp8_gemm_tn";
+    FP8_TRY(check_dims16(fn, M, "M", N, "N"));
+    FP8_TRY(check_dims16(fn, K, "K", 16, "-"));
+    if (M < 16 || N < 16 || K < 16) return fail(FP8_ERR_ARG, "%s: M, N, K must be >= 16", fn);
+    if ((fa != FP8_E4M3 && fa != FP8_E5M2) || (fb != FP8_E4M3 && fb != FP8_E5M2))
+        return fail(FP8_ERR_ARG, "%s: bad operand format", fn);
+    FP8_TRY(check_ptr(fn, A, "A", false));
+    FP8_TRY(check_ptr(fn, B, "B", false));
+    FP8_TRY(check_ptr(fn, D, "D", false));
+    FP8_TRY(check_scalar(fn, a_scale_inv, "a_scale_inv", false));
+    FP8_TRY(check_scalar(fn, b_scale_inv, "b_scale_inv", false));
+    FP8_TRY(check_scalar(fn, d_amax, "d_amax", true));
+    int sms;
+    FP8_TRY(current_device(&sms));
+    return gemm_checked(fn, A, fa, B, fb, M, N, K, a_scale_inv, b_scale_inv, D, d_amax, true, sms,
+                        static_cast<cudaStream_t>(stream));
+}
+
+fp8_status fp8_linear_fwd(const void *X, const void *W, int64_t M, int64_t N, int64_t K,
+                          const fp8_meta *meta, const fp8_recipe *recipe, uint8_t *X8,
+                          uint8_t *X8t, uint8_t *W8, uint8_t *W8t, void *Y, void *stream) {
+    const char *fn = "fp8_linear_fwd";
+    FP8_TRY(check_meta(fn, meta, recipe));
+    FP8_TRY(check_dims16(fn, M, "M", N, "N"));
+    FP8_TRY(check_dims16(fn, K, "K", 16, "-"));
+    if (M < 16 || N < 16 || K < 16) return fail(FP8_ERR_ARG, "%s: M, N, K must be >= 16", fn);
+    FP8_TRY(check_ptr(fn, X, "X", false));
+    FP8_TRY(check_ptr(fn, W, "W", false));
+    FP8_TRY(check_ptr(fn, X8, "X8", false));
+    FP8_TRY(check_ptr(fn, X8t, "X8t", false));
+    FP8_TRY(check_ptr(fn, W8, "W8", false));
+    FP8_TRY(check_ptr(fn, W8t, "W8t", false));
+    FP8_TRY(check_ptr(fn, Y, "Y", false));
+    int sms;
+    FP8_TRY(current_device(&sms));
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    float *am = meta->amax;
+    // amax of X, W and Y are max-combined into slots cleared here.
+    FP8_CUDA(cudaMemsetAsync(am + FP8_SLOT_X, 0, 3 * sizeof(float), st), fn);
+    FP8_CUDA(fp8k::launch_quantize_transpose(X, M, K, meta->scale + FP8_SLOT_X, FP8_E4M3, X8, X8t,
+                                             am + FP8_SLOT_X, false, sms, st),
+             fn);
+    FP8_CUDA(fp8k::launch_quantize_transpose(W, N, K, meta->scale + FP8_SLOT_W, FP8_E4M3, W8, W8t,
+                                             am + FP8_SLOT_W, false, sms, st),
+             fn);
+    return gemm_checked(fn, X8, FP8_E4M3, W8, FP8_E4M3, M, N, K, meta->scale_inv + FP8_SLOT_X,
+                        meta->scale_inv + FP8_SLOT_W, Y, am + FP8_SLOT_Y, false, sms, st);
+}
+
+fp8_status fp8_linear_bwd(const void *dY, int64_t M, int64_t N, int64_t K, const fp8_meta *meta,
+                          const fp8_recipe *recipe, const uint8_t *X8t, const uint8_t *W8t,
+                          uint8_t *dY8, uint8_t *dY8t, void *dX, void *dW, void *stream) {
+    const char *fn = "fp8_linear_bwd";
+    FP8_TRY(check_meta(fn, meta, recipe));
+    FP8_TRY(check_dims16(fn, M, "M", N, "N"));
+    FP8_TRY(check_dims16(fn, K, "K", 16, "-"));
+    if (M < 16 || N < 16 || K < 16) return fail(FP8_ERR_ARG, "%s: M, N, K must be >= 16", fn);
+    FP8_TRY(check_ptr(fn, dY, "dY", false));
+    FP8_TRY(check_ptr(fn, X8t, "X8t", false));
+    FP8_TRY(check_ptr(fn, W8t, "W8t", false));
+    FP8_TRY(check_ptr(fn, dY8, "dY8", false));
+    FP8_TRY(check_ptr(fn, dY8t, "dY8t", false));
+    FP8_TRY(check_ptr(fn, dX, "dX", false));
+    FP8_TRY(check_ptr(fn, dW, "dW", false));
+    int sms;
+    FP8_TRY(current_device(&sms));
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    float *am = meta->amax;
+    const int32_t fg = recipe->hybrid ? FP8_E5M2 : FP8_E4M3;
+    FP8_CUDA(cudaMemsetAsync(am + FP8_SLOT_DY, 0, 2 * sizeof(float), st), fn);
+    FP8_CUDA(fp8k::launch_quantize_transpose(dY, M, N, meta->scale + FP8_SLOT_DY, fg, dY8, dY8t,
+                                             am + FP8_SLOT_DY, false, sms, st),
+             fn);
+    // dgrad: dX[M][K] = dY8[M][N] . W8t[K][N]^T
+    FP8_TRY(gemm_checked(fn, dY8, fg, W8t, FP8_E4M3, M, K, N, meta->scale_inv + FP8_SLOT_DY,
+                         meta->scale_inv + FP8_SLOT_W, dX, am + FP8_SLOT_DX, false, sms, st));
+    // wgrad: dW[N][K] = dY8t[N][M] . X8t[K][M]^T
+    return gemm_checked(fn, dY8t, fg, X8t, FP8_E4M3, N, K, M, meta->scale_inv + FP8_SLOT_DY,
+                        meta->scale_inv + FP8_SLOT_X, dW, nullptr, false, sms, st);
+}
+
+}  // extern "C"

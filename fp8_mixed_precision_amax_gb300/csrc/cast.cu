@@ -1,0 +1,294 @@
+// cast.cu -- the HBM-bound kernels of the FP8 delayed-scaling layer:
+//  * amax of a BF16 tensor (range monitoring of dynamic scaling, "NVIDIA
+//    Transformer Engine and FP8 mixed precision: implementation guide",
+//    section "What are Transformer Engine and FP8 mixed precision"; the
+//    Absolute-Max statistic of "FP8 quantization with NVIDIA TensorRT");
+//  * the fused scaled cast BF16 -> FP8 (E4M3 / E5M2) with transposed copy and
+//    amax (the Q node of the TensorRT page);
+//  * the delayed-scaling history / scale update (DelayedScaling's margin and
+//    amax_history_len, implementation guide section "Dynamic scaling and the
+//    FP8 recipe").
+#include <cfloat>
+#include <cstdint>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace fp8k {
+
+// ------------------------------------------------------------------- amax --
+
+// Grid-stride max of |x| over 16-byte vectors (8 BF16), 4 vectors in flight
+// per thread, integer max on magnitude bits, one atomicMax per block.
+__global__ void __launch_bounds__(512) amax_kernel(const uint4 *__restrict__ x, int64_t nvec,
+                                                   unsigned *__restrict__ amax_bits) {
+    uint32_t m = 0;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    for (; i + 3 * stride < nvec; i += 4 * stride) {
+        uint4 v[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) v[u] = __ldcs(x + i + u * stride);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            m = amax_bits2(m, v[u].x);
+            m = amax_bits2(m, v[u].y);
+            m = amax_bits2(m, v[u].z);
+            m = amax_bits2(m, v[u].w);
+        }
+    }
+    for (; i < nvec; i += stride) {
+        uint4 v = __ldcs(x + i);
+        m = amax_bits2(m, v.x);
+        m = amax_bits2(m, v.y);
+        m = amax_bits2(m, v.z);
+        m = amax_bits2(m, v.w);
+    }
+    m = __reduce_max_sync(0xFFFFFFFFu, m);
+    __shared__ uint32_t warp_max[32];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (lane == 0) warp_max[warp] = m;
+    __syncthreads();
+    if (warp == 0) {
+        m = lane < static_cast<int>(blockDim.x >> 5) ? warp_max[lane] : 0u;
+        m = __reduce_max_sync(0xFFFFFFFFu, m);
+        if (lane == 0 && m != 0) atomicMax(amax_bits, m << 16);
+    }
+}
+
+// ----------------------------------------------------- quantize_transpose --
+//
+// One CTA of 256 threads converts 128 x 128 tiles (grid-stride over tiles):
+//  phase 1  each thread loads 8 x 16 B of BF16 (8 rows' worth of 8 columns),
+//           scales, converts to FP8, stores 8 B to the row-major output and
+//           the same 8 B into a shared-memory tile of 32-bit words
+//           [128 rows][32 words]; the word column is XOR-swizzled with the
+//           row's 16-row block so phase 2 reads are bank-conflict free;
+//  phase 2  each thread owns 16 rows x 4 columns: it reads 16 words, turns
+//           four 4 x 4 byte blocks around with byte permutes and writes four
+//           16-byte runs of the transposed output; the 8 threads sharing a
+//           column write one contiguous 128-byte line.
+
+constexpr int kQtTile = 128;
+constexpr int kQtThreads = 256;
+
+__device__ __forceinline__ int qt_swz(int row) { return ((row >> 4) & 7) << 2; }
+
+// Transpose a 4 x 4 block of bytes held as 4 words (w[i] = row i, byte j =
+// column j) into t[j] = column j (byte i = row i).
+__device__ __forceinline__ void transpose4x4(uint32_t w0, uint32_t w1, uint32_t w2, uint32_t w3,
+                                             uint32_t &t0, uint32_t &t1, uint32_t &t2,
+                                             uint32_t &t3) {
+    const uint32_t a01 = __byte_perm(w0, w1, 0x5140);  // w0.b0 w1.b0 w0.b1 w1.b1
+    const uint32_t b01 = __byte_perm(w0, w1, 0x7362);  // w0.b2 w1.b2 w0.b3 w1.b3
+    const uint32_t a23 = __byte_perm(w2, w3, 0x5140);
+    const uint32_t b23 = __byte_perm(w2, w3, 0x7362);
+    t0 = __byte_perm(a01, a23, 0x5410);
+    t1 = __byte_perm(a01, a23, 0x7632);
+    t2 = __byte_perm(b01, b23, 0x5410);
+    t3 = __byte_perm(b01, b23, 0x7632);
+}
+
+template <int FMT>
+__global__ void __launch_bounds__(kQtThreads) quantize_transpose_kernel(
+    const uint16_t *__restrict__ x, int64_t rows, int64_t cols, const float *__restrict__ scale_p,
+    uint8_t *__restrict__ out, uint8_t *__restrict__ out_t, unsigned *__restrict__ amax_bits,
+    int64_t tiles_c, int64_t num_tiles) {
+    __shared__ __align__(16) uint32_t tile[kQtTile * (kQtTile / 4)];
+    const float s = *scale_p;
+    const int tid = threadIdx.x;
+    uint32_t tmax = 0;
+
+    for (int64_t t = blockIdx.x; t < num_tiles; t += gridDim.x) {
+        const int64_t r0 = (t / tiles_c) * kQtTile;
+        const int64_t c0 = (t % tiles_c) * kQtTile;
+
+        uint4 v[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int idx = i * kQtThreads + tid;
+            const int rr = idx >> 4, vv = idx & 15;
+            const int64_t r = r0 + rr, c = c0 + vv * 8;
+            v[i] = make_uint4(0, 0, 0, 0);
+            if (r < rows && c < cols)
+                v[i] = __ldcs(reinterpret_cast<const uint4 *>(x + r * cols + c));
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int idx = i * kQtThreads + tid;
+            const int rr = idx >> 4, vv = idx & 15;
+            const int64_t r = r0 + rr, c = c0 + vv * 8;
+            tmax = amax_bits2(tmax, v[i].x);
+            tmax = amax_bits2(tmax, v[i].y);
+            tmax = amax_bits2(tmax, v[i].z);
+            tmax = amax_bits2(tmax, v[i].w);
+            uint2 q;
+            q.x = cvt2_fp8<FMT>(__fmul_rn(bf16_lo(v[i].x), s), __fmul_rn(bf16_hi(v[i].x), s)) |
+                  (cvt2_fp8<FMT>(__fmul_rn(bf16_lo(v[i].y), s), __fmul_rn(bf16_hi(v[i].y), s))
+                   << 16);
+            q.y = cvt2_fp8<FMT>(__fmul_rn(bf16_lo(v[i].z), s), __fmul_rn(bf16_hi(v[i].z), s)) |
+                  (cvt2_fp8<FMT>(__fmul_rn(bf16_lo(v[i].w), s), __fmul_rn(bf16_hi(v[i].w), s))
+                   << 16);
+            const bool in = r < rows && c < cols;
+            if (out != nullptr && in) *reinterpret_cast<uint2 *>(out + r * cols + c) = q;
+            *reinterpret_cast<uint2 *>(&tile[rr * 32 + ((vv * 2) ^ qt_swz(rr))]) = q;
+        }
+        __syncthreads();
+
+        if (out_t != nullptr) {
+            const int lane = tid & 31, warp = tid >> 5;
+            const int rblk = lane & 7;              // 16-row block of the tile
+            const int cw = warp * 4 + (lane >> 3);  // word column = 4 tile columns
+            uint32_t w[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                const int rr = rblk * 16 + j;
+                w[j] = tile[rr * 32 + (cw ^ qt_swz(rr))];
+            }
+            uint32_t o[4][4];
+#pragma unroll
+            for (int g = 0; g < 4; ++g)
+                transpose4x4(w[4 * g], w[4 * g + 1], w[4 * g + 2], w[4 * g + 3], o[0][g], o[1][g],
+                             o[2][g], o[3][g]);
+            const int64_t r = r0 + rblk * 16;
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) {
+                const int64_t c = c0 + cw * 4 + cc;
+                if (r < rows && c < cols)
+                    *reinterpret_cast<uint4 *>(out_t + c * rows + r) =
+                        make_uint4(o[cc][0], o[cc][1], o[cc][2], o[cc][3]);
+            }
+        }
+        __syncthreads();
+    }
+
+    if (amax_bits != nullptr) {
+        __shared__ uint32_t warp_max[kQtThreads / 32];
+        tmax = __reduce_max_sync(0xFFFFFFFFu, tmax);
+        if ((tid & 31) == 0) warp_max[tid >> 5] = tmax;
+        __syncthreads();
+        if (tid < 32) {
+            uint32_t m = tid < kQtThreads / 32 ? warp_max[tid] : 0u;
+            m = __reduce_max_sync(0xFFFFFFFFu, m);
+            if (tid == 0 && m != 0) atomicMax(amax_bits, m << 16);
+        }
+    }
+}
+
+// ----------------------------------------------------------- scale update --
+//
+// One CTA per tensor: shift the history by one (newest at [0]), take its max,
+// and recompute scale = fl32(fl32(fmax / m) * 2^-margin) (clamped to FLT_MAX)
+// and scale_inv = fl32(1 / scale) when 0 < m < inf; otherwise keep both.
+
+constexpr int kUpdThreads = 256;
+
+__global__ void __launch_bounds__(kUpdThreads) scale_update_kernel(
+    float *__restrict__ history, const float *__restrict__ amax, float *__restrict__ scale,
+    float *__restrict__ scale_inv, int L, uint32_t format_mask, int margin) {
+    extern __shared__ float old_hist[];
+    const int t = blockIdx.x;
+    float *h = history + static_cast<int64_t>(t) * L;
+    for (int i = threadIdx.x; i < L; i += blockDim.x) old_hist[i] = h[i];
+    __syncthreads();
+    const float a = amax[t];
+    float m = 0.0f;
+    for (int i = threadIdx.x; i < L; i += blockDim.x) {
+        const float nv = i == 0 ? a : old_hist[i - 1];
+        h[i] = nv;
+        m = fmaxf(m, nv);
+    }
+    __shared__ float warp_max[kUpdThreads / 32];
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, off));
+    if ((threadIdx.x & 31) == 0) warp_max[threadIdx.x >> 5] = m;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        for (int w = 1; w < kUpdThreads / 32; ++w) m = fmaxf(m, warp_max[w]);
+        m = fmaxf(m, warp_max[0]);
+        if (m > 0.0f && m <= FLT_MAX) {
+            const float fmax = ((format_mask >> t) & 1u) ? 57344.0f : 448.0f;
+            const float q = __fdiv_rn(fmax, m);
+            const float p2 = __uint_as_float(static_cast<uint32_t>(127 - margin) << 23);
+            float sc = __fmul_rn(q, p2);
+            if (sc > FLT_MAX) sc = FLT_MAX;
+            scale[t] = sc;
+            scale_inv[t] = __fdiv_rn(1.0f, sc);
+        }
+    }
+}
+
+// ---------------------------------------------------------------- launchers --
+
+cudaError_t launch_amax(const void *x, int64_t n, float *amax, int sm_count, cudaStream_t st) {
+    cudaError_t e = cudaMemsetAsync(amax, 0, sizeof(float), st);
+    if (e != cudaSuccess || n == 0) return e;
+    const int64_t nvec = n / 8;
+    const int threads = 512;
+    int64_t blocks = (nvec + threads * 4 - 1) / (threads * 4);
+    const int64_t cap = static_cast<int64_t>(sm_count) * 4;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    amax_kernel<<<static_cast<unsigned>(blocks), threads, 0, st>>>(
+        reinterpret_cast<const uint4 *>(x), nvec, reinterpret_cast<unsigned *>(amax));
+    return cudaGetLastError();
+}
+
+template <int FMT>
+static int qt_blocks_per_sm() {
+    static int cached = 0;
+    if (cached == 0) {
+        int b = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, quantize_transpose_kernel<FMT>,
+                                                          kQtThreads, 0) != cudaSuccess ||
+            b < 1)
+            b = 1;
+        cached = b;
+    }
+    return cached;
+}
+
+cudaError_t launch_quantize_transpose(const void *x, int64_t rows, int64_t cols,
+                                      const float *scale, int fmt, uint8_t *out, uint8_t *out_t,
+                                      float *amax, bool zero_amax, int sm_count,
+                                      cudaStream_t st) {
+    if (amax != nullptr && zero_amax) {
+        cudaError_t e = cudaMemsetAsync(amax, 0, sizeof(float), st);
+        if (e != cudaSuccess) return e;
+    }
+    if (rows == 0 || cols == 0) return cudaSuccess;
+    const int64_t tiles_c = (cols + kQtTile - 1) / kQtTile;
+    const int64_t num_tiles = ((rows + kQtTile - 1) / kQtTile) * tiles_c;
+    const int per_sm = fmt == 0 ? qt_blocks_per_sm<0>() : qt_blocks_per_sm<1>();
+    int64_t blocks = static_cast<int64_t>(sm_count) * per_sm;
+    if (blocks > num_tiles) blocks = num_tiles;
+    const auto *xb = reinterpret_cast<const uint16_t *>(x);
+    auto *ab = reinterpret_cast<unsigned *>(amax);
+    if (fmt == 0)
+        quantize_transpose_kernel<0><<<static_cast<unsigned>(blocks), kQtThreads, 0, st>>>(
+            xb, rows, cols, scale, out, out_t, ab, tiles_c, num_tiles);
+    else
+        quantize_transpose_kernel<1><<<static_cast<unsigned>(blocks), kQtThreads, 0, st>>>(
+            xb, rows, cols, scale, out, out_t, ab, tiles_c, num_tiles);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_scale_update(float *history, const float *amax, float *scale, float *scale_inv,
+                                int num_tensors, int L, uint32_t format_mask, int margin,
+                                cudaStream_t st) {
+    const size_t smem = static_cast<size_t>(L) * sizeof(float);
+    if (smem > 48 * 1024) {
+        static bool raised = false;
+        if (!raised) {
+            cudaError_t e = cudaFuncSetAttribute(
+                scale_update_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 64 * 1024);
+            if (e != cudaSuccess) return e;
+            raised = true;
+        }
+    }
+    scale_update_kernel<<<num_tensors, kUpdThreads, smem, st>>>(history, amax, scale, scale_inv, L,
+                                                                format_mask, margin);
+    return cudaGetLastError();
+}
+
+}  // namespace fp8k

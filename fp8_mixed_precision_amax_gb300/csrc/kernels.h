@@ -1,0 +1,37 @@
+// kernels.h -- host-side launchers of the sm_103a kernels (internal to the
+// library; the public C ABI is include/fp8amax.h).
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace fp8k {
+
+// amax of n BF16 values into *amax (zeroed first).
+cudaError_t launch_amax(const void *x, int64_t n, float *amax, int sm_count, cudaStream_t st);
+
+// Fused scaled cast + transposed copy + amax.  fmt: 0 = E4M3, 1 = E5M2.
+// With zero_amax the amax word is cleared first; otherwise the tensor's amax
+// is max-combined into it.
+cudaError_t launch_quantize_transpose(const void *x, int64_t rows, int64_t cols,
+                                      const float *scale, int fmt, uint8_t *out, uint8_t *out_t,
+                                      float *amax, bool zero_amax, int sm_count, cudaStream_t st);
+
+// History shift + scale / scale_inv update of num_tensors states.
+cudaError_t launch_scale_update(float *history, const float *amax, float *scale, float *scale_inv,
+                                int num_tensors, int L, uint32_t format_mask, int margin,
+                                cudaStream_t st);
+
+// FP8 "TN" GEMM on tcgen05 with the dequant + amax epilogue.  With
+// zero_amax the amax word is cleared first.  Returns cudaErrorInvalidValue
+// (with *what set) when a TMA descriptor cannot be built.
+cudaError_t launch_gemm_tn(const uint8_t *A, int fa, const uint8_t *B, int fb, int64_t M,
+                           int64_t N, int64_t K, const float *a_scale_inv,
+                           const float *b_scale_inv, void *D, float *d_amax, bool zero_amax,
+                           int sm_count, cudaStream_t st, const char **what);
+
+// Read and clear the device error flag the kernels set when a bounded wait
+// gives up (synchronizes the device flag's stream).
+cudaError_t read_and_clear_error_flag(unsigned *flags, cudaStream_t st);
+
+}  // namespace fp8k

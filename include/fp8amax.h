@@ -1,0 +1,196 @@
+/*
+ * fp8amax.h -- C ABI of the GB300 (sm_103a) FP8 delayed-scaling linear layer.
+ *
+ * The operations follow three web pages on FP8 mixed-precision training:
+ *  - "NVIDIA Transformer Engine and FP8 mixed precision: implementation guide"
+ *    (ai-tool-zukan.com): section "What are Transformer Engine and FP8 mixed
+ *    precision" (E4M3 = 4 exponent / 3 mantissa bits for the forward pass,
+ *    E5M2 = 5 / 2 for the backward pass; dynamic scaling watches each
+ *    tensor's range and adjusts its scale factor) and section "Dynamic
+ *    scaling and the FP8 recipe" (DelayedScaling with margin, fp8_format,
+ *    amax_history_len; Format.HYBRID = E4M3 forward / E5M2 backward; the
+ *    amax history is part of the model state).
+ *  - "FP8 quantization with NVIDIA TensorRT" (ai.warp-studio.com): explicit
+ *    quantize / dequantize (Q/DQ) nodes and the Absolute-Max statistic.
+ *  - "Mixed-precision training" wiki note (notes.yuuk.io): "Definition" table
+ *    (E4M3 max 448, E5M2 max 57,344) and the bullets "extension to FP8"
+ *    (only the GEMMs run in FP8) and "per-tensor scaling is the key"
+ *    (delayed or just-in-time per-tensor scaling).
+ *
+ * Numerics (identical on every call):
+ *  - amax(x) = max |x_i| over the tensor, NaN entries skipped, exact.
+ *  - cast: v = fl32(x * scale) (one binary32 multiply), then round to the
+ *    nearest FP8 value, ties to the even code; |v| above the largest finite
+ *    value and +-inf saturate to +-448 (E4M3) / +-57344 (E5M2); NaN stays NaN;
+ *    the sign of zero is kept.  E4M3 is the variant with no infinities whose
+ *    only NaN code is S.1111.111 (largest finite 448); E5M2 is IEEE-style.
+ *  - scale update: history <- [amax, history[0..L-2]]; m = max(history); if
+ *    0 < m < inf then scale = fl32(fl32(fmax / m) * 2^-margin) (+inf clamped
+ *    to FLT_MAX) and scale_inv = fl32(1 / scale); otherwise both unchanged.
+ *  - GEMM: D[i][j] = bf16_rne(fl32(acc[i][j] * fl32(a_scale_inv * b_scale_inv)))
+ *    with acc = sum_k A[i][k] * B[j][k] accumulated in fp32 by the tensor
+ *    cores, and d_amax = max |D| over the emitted BF16 values.
+ *
+ * Conventions for every entry point:
+ *  - Pointers named as DEVICE pointers must be device (or managed) memory of
+ *    the current device; the caller allocates and owns every buffer.  The
+ *    library allocates no device memory, never synchronizes the stream (except
+ *    fp8_sync_status), and keeps no state beyond cached device properties and
+ *    one device-side error flag.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *    stream).  All work is enqueued on it, in order; scales are read on the
+ *    device, so a training step needs no host round trip.
+ *  - Tensors are dense row-major.  Row and column counts must be multiples of
+ *    16 and tensor pointers 16-byte aligned (else FP8_ERR_ALIGN), so that
+ *    every row of every FP8 and BF16 tensor starts on a 16-byte boundary.
+ *    Pointers to fp32 scalars and to the fp8_meta buffers need 4-byte
+ *    alignment only.
+ *  - Arguments are checked on the host before anything is enqueued; on any
+ *    status other than FP8_OK nothing was enqueued, and fp8_last_error()
+ *    gives a message (thread-local).  Errors reported by the CUDA runtime at
+ *    launch give FP8_ERR_CUDA.
+ *  - Bounded waits: every spin-wait in a kernel gives up after about two
+ *    seconds, sets a device error flag and returns; fp8_sync_status() reports
+ *    it as FP8_ERR_TIMEOUT.
+ */
+#ifndef FP8AMAX_H
+#define FP8AMAX_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define FP8AMAX_ABI_VERSION 1
+
+typedef enum { FP8_E4M3 = 0, FP8_E5M2 = 1 } fp8_format;
+
+typedef enum {
+    FP8_OK = 0,
+    FP8_ERR_ARG = 1,         /* bad size, NULL pointer, bad format / margin / history length */
+    FP8_ERR_ALIGN = 2,       /* size not a multiple of 16 or a pointer misaligned */
+    FP8_ERR_CUDA = 3,        /* the CUDA runtime reported an error */
+    FP8_ERR_TIMEOUT = 4,     /* a kernel's bounded wait ran out (see fp8_sync_status) */
+    FP8_ERR_UNSUPPORTED = 5  /* the current device is not an sm_103 GPU */
+} fp8_status;
+
+/* The five tensors of one linear layer whose scaling state is tracked. */
+enum { FP8_SLOT_X = 0, FP8_SLOT_W = 1, FP8_SLOT_Y = 2, FP8_SLOT_DY = 3, FP8_SLOT_DX = 4,
+       FP8_NUM_SLOTS = 5 };
+
+/* Scaling state of one linear layer (the DelayedScaling state the
+ * implementation guide says is saved with the model).  All DEVICE pointers,
+ * caller-owned, fp32:
+ *   history   [5][history_len]  row = slot; history[slot*L + 0] is the newest
+ *   amax      [5]               this step's amax of each slot
+ *   scale     [5]               multiplier applied before the FP8 cast (init 1)
+ *   scale_inv [5]               1 / scale, applied in the GEMM epilogue (init 1)
+ * A fresh state is history = 0, amax = 0, scale = scale_inv = 1. */
+typedef struct {
+    float *history;
+    float *amax;
+    float *scale;
+    float *scale_inv;
+    int32_t history_len;
+} fp8_meta;
+
+/* DelayedScaling recipe (implementation guide, "Dynamic scaling and the FP8
+ * recipe"): margin (>= 0, default 0; larger = fewer overflows, more
+ * underflow), amax_history_len (default 1024) and the format choice.
+ * hybrid = 1: E4M3 for X, W, Y and E5M2 for dY, dX (Format.HYBRID);
+ * hybrid = 0: E4M3 for all five.  The scale is updated every step. */
+typedef struct {
+    int32_t margin;
+    int32_t history_len;
+    int32_t hybrid;
+} fp8_recipe;
+
+/* ABI version of the loaded library (FP8AMAX_ABI_VERSION). */
+int32_t fp8_abi_version(void);
+
+/* Message of the last non-OK status returned on this host thread. */
+const char *fp8_last_error(void);
+
+/* Synchronize `stream`, then report (and clear) the device error flag:
+ * FP8_ERR_TIMEOUT if a kernel gave up a bounded wait since the last call,
+ * FP8_ERR_CUDA if the stream reports an error, else FP8_OK. */
+fp8_status fp8_sync_status(void *stream);
+
+/* amax of a BF16 tensor (the implementation guide's range monitoring; the
+ * TensorRT page's Absolute-Max statistic).
+ *   x     DEVICE, n BF16 values (n >= 0, multiple of 16; n == 0 gives 0)
+ *   amax  DEVICE, 1 float, overwritten with max |x_i| (NaN skipped). */
+fp8_status fp8_amax(const void *x, int64_t n, float *amax, void *stream);
+
+/* Fused scaled cast BF16 -> FP8 with transposed copy and amax (the Q node of
+ * the TensorRT page; formats of the implementation guide / wiki table).
+ *   x      DEVICE, [rows][cols] BF16
+ *   scale  DEVICE, 1 float, read on the device
+ *   fmt    FP8_E4M3 or FP8_E5M2
+ *   out    DEVICE, [rows][cols] FP8 codes, or NULL
+ *   out_t  DEVICE, [cols][rows] FP8 codes (the transpose of out), or NULL
+ *   amax   DEVICE, 1 float overwritten with amax(x), or NULL
+ * rows, cols >= 0 and multiples of 16.  At least one of out / out_t. */
+fp8_status fp8_quantize_transpose(const void *x, int64_t rows, int64_t cols, const float *scale,
+                                  int32_t fmt, uint8_t *out, uint8_t *out_t, float *amax,
+                                  void *stream);
+
+/* Delayed-scaling update of `num_tensors` independent scaling states (the
+ * recipe section's margin and amax_history_len, with the scale formula in
+ * the header comment).  All DEVICE:
+ *   history    [num_tensors][history_len], shifted in place, [t][0] newest
+ *   amax       [num_tensors], the value pushed into each history (read only)
+ *   scale, scale_inv [num_tensors], updated in place
+ * format_mask: bit t set = tensor t is E5M2 (fmax 57344), clear = E4M3 (448).
+ * 1 <= num_tensors <= 32, 1 <= history_len <= 8192, 0 <= margin <= 64. */
+fp8_status fp8_scale_update(float *history, const float *amax, float *scale, float *scale_inv,
+                            int32_t num_tensors, int32_t history_len, uint32_t format_mask,
+                            int32_t margin, void *stream);
+
+/* The recipe's update of all five slots of one layer, run once per step
+ * after fp8_linear_fwd and fp8_linear_bwd: fp8_scale_update over meta with
+ * the recipe's formats (HYBRID: slots dY and dX are E5M2).
+ * meta->history_len must equal recipe->history_len. */
+fp8_status fp8_amax_scale_update(const fp8_meta *meta, const fp8_recipe *recipe, void *stream);
+
+/* FP8 GEMM with both operands contiguous along K ("TN"), fp32 accumulation
+ * in TMEM on the tcgen05 tensor cores, and the dequant epilogue (wiki note,
+ * "extension to FP8"; the DQ node of the TensorRT page).
+ *   A  DEVICE [M][K] FP8 codes of format fa;  B  DEVICE [N][K] of format fb
+ *   a_scale_inv, b_scale_inv  DEVICE, 1 float each
+ *   D  DEVICE [M][N] BF16 output
+ *   d_amax  DEVICE, 1 float overwritten with max |D|, or NULL
+ * M, N, K >= 16 and multiples of 16. */
+fp8_status fp8_gemm_tn(const uint8_t *A, int32_t fa, const uint8_t *B, int32_t fb, int64_t M,
+                       int64_t N, int64_t K, const float *a_scale_inv, const float *b_scale_inv,
+                       void *D, float *d_amax, void *stream);
+
+/* Forward of the FP8 linear layer Y = X W^T (te.Linear under fp8_autocast,
+ * implementation guide "Basic structure of FP8 training code" and the
+ * recipe section).  Uses this step's (delayed) scales of X and W.
+ *   X   DEVICE [M][K] BF16 input;   W  DEVICE [N][K] BF16 weight
+ *   X8, X8t  DEVICE [M][K] and [K][M] FP8 (E4M3), written; X8t is kept for wgrad
+ *   W8, W8t  DEVICE [N][K] and [K][N] FP8 (E4M3), written; W8t is kept for dgrad
+ *   Y   DEVICE [M][N] BF16 output
+ * Writes meta->amax[X], amax[W], amax[Y]. */
+fp8_status fp8_linear_fwd(const void *X, const void *W, int64_t M, int64_t N, int64_t K,
+                          const fp8_meta *meta, const fp8_recipe *recipe, uint8_t *X8,
+                          uint8_t *X8t, uint8_t *W8, uint8_t *W8t, void *Y, void *stream);
+
+/* Backward of the FP8 linear layer: dX = dY W (dgrad), dW = dY^T X (wgrad),
+ * with dY cast to E5M2 under HYBRID (E4M3 otherwise).
+ *   dY  DEVICE [M][N] BF16 output gradient
+ *   X8t, W8t  DEVICE, the transposed copies written by fp8_linear_fwd
+ *   dY8, dY8t DEVICE [M][N] and [N][M] FP8 work buffers, written
+ *   dX  DEVICE [M][K] BF16;  dW  DEVICE [N][K] BF16
+ * Writes meta->amax[dY], amax[dX]. */
+fp8_status fp8_linear_bwd(const void *dY, int64_t M, int64_t N, int64_t K, const fp8_meta *meta,
+                          const fp8_recipe *recipe, const uint8_t *X8t, const uint8_t *W8t,
+                          uint8_t *dY8, uint8_t *dY8t, void *dX, void *dW, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FP8AMAX_H */

@@ -1,0 +1,64 @@
+"""Shared helpers of the GPU parity tests: host copies, FP8 comparison with
+NaN codes compared as a class, and the GEMM tolerance.
+
+GEMM tolerance (per output tensor, against the oracle's BF16 output computed
+with the same dequant epilogue): relative Frobenius error <= 1e-3 and
+max |D_gpu - D_oracle| <= 2e-2 * sqrt(K) / 64 * max |D_oracle|.
+"""
+import math
+
+import numpy as np
+import torch
+
+import oracle as o
+
+FRO_TOL = 1e-3
+
+
+def host_u8(t: torch.Tensor) -> np.ndarray:
+    return t.detach().contiguous().view(torch.uint8).cpu().numpy()
+
+
+def host_bf16_bits(t: torch.Tensor) -> np.ndarray:
+    return t.detach().contiguous().cpu().view(torch.int16).numpy().view(np.uint16)
+
+
+def bf16_values(bits: np.ndarray) -> np.ndarray:
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16) \
+        .double().numpy()
+
+
+def f32_bits(x) -> np.ndarray:
+    return np.asarray(x, dtype=np.float32).view(np.uint32)
+
+
+def is_nan_code(q: np.ndarray, fmt: int) -> np.ndarray:
+    m = q & 0x7F
+    return (m == 0x7F) if fmt == o.E4M3 else (m > 0x7C)
+
+
+def assert_fp8_equal(gpu: np.ndarray, ref: np.ndarray, fmt: int, what=""):
+    assert gpu.shape == ref.shape, (what, gpu.shape, ref.shape)
+    same = (gpu == ref) | (is_nan_code(gpu, fmt) & is_nan_code(ref, fmt))
+    if not same.all():
+        idx = np.argwhere(~same)[:5]
+        raise AssertionError(f"{what}: {int((~same).sum())} FP8 codes differ, e.g. at "
+                             f"{idx.tolist()}: gpu {[int(gpu[tuple(i)]) for i in idx]} "
+                             f"oracle {[int(ref[tuple(i)]) for i in idx]}")
+
+
+def gemm_errors(gpu_bits: np.ndarray, ref_bits: np.ndarray, K: int) -> dict:
+    g, r = bf16_values(gpu_bits), bf16_values(ref_bits)
+    diff = np.abs(g - r)
+    ref_norm = np.linalg.norm(r)
+    fro = float(np.linalg.norm(g - r) / ref_norm) if ref_norm > 0 else float(np.linalg.norm(g))
+    scale = float(np.max(np.abs(r))) if r.size else 0.0
+    bound = 2e-2 * math.sqrt(K) / 64 * scale
+    return dict(fro=fro, max_err=float(diff.max()) if diff.size else 0.0, bound=bound,
+                flips=int(np.count_nonzero(gpu_bits != ref_bits)), n=int(g.size))
+
+
+def assert_gemm_close(gpu_bits, ref_bits, K, what=""):
+    e = gemm_errors(gpu_bits, ref_bits, K)
+    assert e["fro"] <= FRO_TOL and e["max_err"] <= e["bound"], (what, e)
+    return e

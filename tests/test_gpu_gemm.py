@@ -1,0 +1,95 @@
+"""GPU parity of the tcgen05 FP8 GEMM + dequant epilogue against the oracle.
+
+Outputs are compared with the oracle's BF16 output (same epilogue) within
+the tolerance in helpers.py; the fused output amax must equal max |D| over
+the GPU's own BF16 output exactly, and match the oracle's within one BF16
+rounding.  Shapes cover a single tile, several tiles, ragged M / N / K tails
+and long K, for every operand-format pair.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle as o
+from helpers import assert_gemm_close, bf16_values, f32_bits, host_bf16_bits
+
+pytestmark = pytest.mark.gpu
+
+PAIRS = [(o.E4M3, o.E4M3), (o.E5M2, o.E4M3), (o.E4M3, o.E5M2), (o.E5M2, o.E5M2)]
+
+
+def _lib():
+    import fp8_mixed_precision_amax_gb300 as f
+    return f
+
+
+def _codes(shape, fmt, std, seed):
+    """FP8 operands made the way the layer makes them: a scaled cast of
+    Gaussian data (so magnitudes follow a realistic spread)."""
+    g = torch.Generator().manual_seed(seed)
+    x = (torch.randn(shape, generator=g) * std).to(torch.bfloat16)
+    q, _ = o.quantize(host_bf16_bits(x), np.float32(1.0), fmt, transpose=False)
+    return q
+
+
+def _run(A, fa, B, fb, sa, sb):
+    f = _lib()
+    M, K = A.shape
+    N = B.shape[0]
+    dA = torch.from_numpy(A).cuda()
+    dB = torch.from_numpy(B).cuda()
+    D = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+    am = torch.full((1,), -1.0, device="cuda")
+    f.fp8_gemm_tn(dA, fa, dB, fb, torch.tensor([sa], device="cuda"),
+                  torch.tensor([sb], device="cuda"), D, am)
+    f.fp8_sync_status()
+    return host_bf16_bits(D), np.float32(am.cpu().numpy()[0])
+
+
+SHAPES = [(16, 16, 16), (128, 256, 128), (256, 256, 256), (144, 272, 48), (384, 512, 1040),
+          (1040, 784, 400), (128, 256, 4096)]
+
+
+@pytest.mark.parametrize("M,N,K", SHAPES)
+@pytest.mark.parametrize("fa,fb", PAIRS)
+def test_gemm_matches_oracle(M, N, K, fa, fb):
+    A = _codes((M, K), fa, 3.0 if fa == o.E4M3 else 300.0, M * 3 + K)
+    B = _codes((N, K), fb, 1.0, N * 5 + K)
+    sa, sb = np.float32(0.013), np.float32(0.77)
+    got, am = _run(A, fa, B, fb, sa, sb)
+    acc = o.gemm_tn(A, fa, B, fb)
+    ref = o.epilogue(acc, sa, sb)
+    e = assert_gemm_close(got, ref, K, f"{M}x{N}x{K} {fa}{fb}")
+    # fused amax == max |D| of the emitted output, exactly; and near the oracle's
+    assert f32_bits(am) == f32_bits(np.float32(np.max(np.abs(bf16_values(got))))), e
+    assert abs(float(am) - float(np.max(np.abs(bf16_values(ref))))) <= e["bound"] + 1e-30
+
+
+def test_gemm_exact_small_integers():
+    """Operands whose products and sums are exact in fp32 (small integers):
+    the GPU must reproduce the exact result bit for bit."""
+    rng = np.random.default_rng(3)
+    M, N, K = 256, 512, 384
+    vals = np.array([0, 1, 2, 3, 4, -1, -2, -3, -4], np.float32)
+    A = o.fp8_encode(rng.choice(vals, (M, K)), o.E4M3).reshape(M, K)
+    B = o.fp8_encode(rng.choice(vals, (N, K)), o.E5M2).reshape(N, K)
+    got, _ = _run(A, o.E4M3, B, o.E5M2, np.float32(1.0), np.float32(1.0))
+    ref = o.epilogue(o.gemm_tn_exact(A, o.E4M3, B, o.E5M2), 1.0, 1.0)
+    assert np.array_equal(got, ref)
+
+
+def test_gemm_extreme_operands_and_zero():
+    M, N, K = 128, 256, 256
+    A = np.full((M, K), 0x7E, np.uint8)                  # +448
+    B = np.full((N, K), 0xFB, np.uint8)                  # -57344 in E5M2
+    got, am = _run(A, o.E4M3, B, o.E5M2, np.float32(2.0 ** -20), np.float32(1.0))
+    ref = o.epilogue(o.gemm_tn_exact(A, o.E4M3, B, o.E5M2), 2.0 ** -20, 1.0)
+    assert np.array_equal(got, ref)
+    Z = np.zeros((M, K), np.uint8)
+    got, am = _run(Z, o.E4M3, B, o.E5M2, np.float32(1.0), np.float32(1.0))
+    assert np.all((got & 0x7FFF) == 0) and am == 0.0
+
+
+def test_gemm_sync_status_clean():
+    f = _lib()
+    f.fp8_sync_status()

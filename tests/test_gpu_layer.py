@@ -1,0 +1,163 @@
+"""GPU parity of the whole FP8 linear-layer step against the oracle, on the
+layer workloads of fp8_workloads.py, through the same Fp8Linear.step that
+bench.py times (fp8_linear_fwd, fp8_linear_bwd, fp8_amax_scale_update).
+
+Per checked step:
+  * bit-exact: amax of X, W, dY; every FP8 byte of X8, X8t, W8, W8t, dY8,
+    dY8t; history, scale and scale_inv of the X, W and dY slots;
+  * GEMM outputs Y, dX, dW within the tolerance of helpers.py (whole tensors
+    on the small workload, blocks of rows at full size);
+  * Y and dX slots: the fused amax equals max |output| of the GPU's own BF16
+    output exactly, the history holds those amaxes newest first, and the
+    scale follows from them by the recipe's formula.
+"""
+import numpy as np
+import pytest
+import torch
+
+import fp8_workloads as wl
+import oracle as o
+from helpers import (assert_fp8_equal, assert_gemm_close, bf16_values, f32_bits,
+                     host_bf16_bits, host_u8)
+
+pytestmark = pytest.mark.gpu
+
+
+def _lib():
+    import fp8_mixed_precision_amax_gb300 as f
+    return f
+
+
+def _row_blocks(n, width=16):
+    return sorted({0, (n // 2 // 16) * 16 + 48 if n > 128 else 0, n - width})
+
+
+def _gpu_slot_checks(lin, f, gpu_amax_hist, fmts, margin):
+    """Y / dX slots: properties that hold at any size."""
+    hist = lin.meta.history.cpu().numpy()
+    scale = lin.meta.scale.cpu().numpy()
+    for slot, out in ((f.SLOT_Y, lin.Y), (f.SLOT_DX, lin.dX)):
+        a = lin.meta.amax[slot].item()
+        mx = np.float32(np.max(np.abs(bf16_values(host_bf16_bits(out)))))
+        assert f32_bits(np.float32(a)) == f32_bits(mx), (slot, a, mx)
+        gpu_amax_hist[slot].insert(0, np.float32(a))
+        L = hist.shape[1]
+        seq = (gpu_amax_hist[slot] + [np.float32(0)] * L)[:L]
+        assert np.array_equal(hist[slot].view(np.uint32), np.array(seq, np.float32).view(np.uint32))
+        m = np.float32(max(seq))
+        if m > 0:
+            fmax = np.float32(448.0 if fmts[slot] == o.E4M3 else 57344.0)
+            expect = np.float32(np.float32(fmax / m) * np.float32(2.0 ** -margin))
+            assert f32_bits(scale[slot]) == f32_bits(expect)
+
+
+def run_layer(w: wl.Workload, steps, check_every=1, full=True, hybrid=None, extra_checks=()):
+    f = _lib()
+    hybrid = w.hybrid if hybrid is None else hybrid
+    W = wl.layer_weight(w, "cuda")
+    rc_gpu = f.Recipe(margin=w.margin, history_len=w.history_len, hybrid=hybrid)
+    lin = f.Fp8Linear(W, w.M, rc_gpu)
+    rc = o.Recipe(margin=w.margin, history_len=w.history_len, hybrid=hybrid)
+    st = o.State.initial(w.history_len)
+    fm = rc.formats()
+    Wb = host_bf16_bits(W)
+    gpu_amax_hist = {f.SLOT_Y: [], f.SLOT_DX: []}
+    report = []
+    for step in range(steps):
+        X = wl.layer_x(w, step, "cuda")
+        dY = wl.layer_dy(w, step, "cuda")
+        lin.forward(X)
+        lin.backward(dY)
+        torch.cuda.synchronize()
+        g_amax = lin.meta.amax.cpu().numpy().copy()
+        check = (step % check_every == 0) or step in extra_checks or step == steps - 1
+        Xb, dYb = host_bf16_bits(X), host_bf16_bits(dY)
+        if check:
+            # forward / backward in the oracle
+            st.amax[o.SLOT_X] = o.amax(Xb)
+            st.amax[o.SLOT_W] = o.amax(Wb)
+            st.amax[o.SLOT_DY] = o.amax(dYb)
+            X8, X8t = o.quantize(Xb, st.scale[o.SLOT_X], fm[o.SLOT_X])
+            W8, W8t = o.quantize(Wb, st.scale[o.SLOT_W], fm[o.SLOT_W])
+            dY8, dY8t = o.quantize(dYb, st.scale[o.SLOT_DY], fm[o.SLOT_DY])
+            for name, g, r, fmt in [("X8", lin.X8, X8, fm[0]), ("X8t", lin.X8t, X8t, fm[0]),
+                                    ("W8", lin.W8, W8, fm[1]), ("W8t", lin.W8t, W8t, fm[1]),
+                                    ("dY8", lin.dY8, dY8, fm[3]), ("dY8t", lin.dY8t, dY8t, fm[3])]:
+                assert_fp8_equal(host_u8(g), r, fmt, f"step {step} {name}")
+            si = st.scale_inv
+            gemms = [("Y", lin.Y, X8, fm[0], W8, fm[1], si[0], si[1], w.K),
+                     ("dX", lin.dX, dY8, fm[3], W8t, fm[1], si[3], si[1], w.N),
+                     ("dW", lin.dW, dY8t, fm[3], X8t, fm[0], si[3], si[0], w.M)]
+            for name, out, A, fa, B, fb, sa, sb, K in gemms:
+                gout = host_bf16_bits(out)
+                if full:
+                    ref = o.epilogue(o.gemm_tn(A, fa, B, fb), sa, sb)
+                    e = assert_gemm_close(gout, ref, K, f"step {step} {name}")
+                else:
+                    for r0 in _row_blocks(A.shape[0]):
+                        ref = o.epilogue(o.gemm_tn(A, fa, B, fb, r0, 16), sa, sb)
+                        e = assert_gemm_close(gout[r0:r0 + 16], ref, K,
+                                              f"step {step} {name} rows {r0}")
+                report.append((step, name, e))
+        else:
+            st.amax[o.SLOT_X] = o.amax(Xb)
+            st.amax[o.SLOT_W] = o.amax(Wb)
+            st.amax[o.SLOT_DY] = o.amax(dYb)
+        for slot in (o.SLOT_X, o.SLOT_W, o.SLOT_DY):
+            assert f32_bits(g_amax[slot]) == f32_bits(st.amax[slot]), (step, slot)
+        # the delayed-scaling update
+        lin.update()
+        torch.cuda.synchronize()
+        st.amax[o.SLOT_Y] = st.amax[o.SLOT_DX] = 0.0   # checked by property below
+        o.layer_update(st, rc)
+        hist = lin.meta.history.cpu().numpy()
+        for slot in (o.SLOT_X, o.SLOT_W, o.SLOT_DY):
+            assert np.array_equal(hist[slot].view(np.uint32), st.history[slot].view(np.uint32))
+            assert f32_bits(lin.meta.scale[slot].item()) == f32_bits(st.scale[slot]), (step, slot)
+            assert f32_bits(lin.meta.scale_inv[slot].item()) == f32_bits(st.scale_inv[slot])
+        _gpu_slot_checks(lin, f, gpu_amax_hist, fm, w.margin)
+    f.fp8_sync_status()
+    return report
+
+
+def test_tiny_layer_four_steps_whole_tensors():
+    w = wl.WORKLOADS["tiny"]
+    run_layer(w, w.steps, full=True)
+
+
+@pytest.mark.parametrize("hybrid", [True, False])
+def test_tiny_shape_long_run_history_window(hybrid):
+    """1000 drifting steps at a small shape with history 512: spikes enter,
+    persist exactly 512 steps and leave; all-zero steps keep the scale."""
+    d = wl.WORKLOADS["drift"]
+    small = wl.Workload("drift_small", 128, 256, 256, "drift", 1.0, 1 / 16, 1.0, 512, 0, True,
+                        1000)
+    run_layer(small, 1000, check_every=50, full=True, hybrid=hybrid,
+              extra_checks=(49, 50, 51, 75, 76, 150, 562, 563))
+    assert d.history_len == 512
+
+
+def test_mlp7b_full_size_sampled_rows():
+    w = wl.WORKLOADS["mlp7b"]
+    run_layer(w, 3, full=False)
+
+
+def test_mlp70b_full_size_sampled_rows():
+    w = wl.WORKLOADS["mlp70b"]
+    run_layer(w, 2, full=False)
+
+
+@pytest.mark.parametrize("hybrid", [True, False])
+def test_drift_full_size(hybrid):
+    """The drifting-scale stress at full size (4096^3) through its first 120
+    steps: the x1000 spike at step 50 and the all-zero step 75, in both the
+    HYBRID and the E4M3-everywhere arms."""
+    w = wl.WORKLOADS["drift"]
+    run_layer(w, 120, check_every=40, full=False, hybrid=hybrid,
+              extra_checks=(49, 50, 51, 75, 76, 100, 101))
+
+
+def test_ragged_layer_shape():
+    """A layer whose M, N, K are not multiples of the GEMM tiles."""
+    w = wl.Workload("ragged", 144, 272, 400, "normal", 1.0, 0.05, 0.01, 16, 0, True, 3)
+    run_layer(w, 3, full=True)
