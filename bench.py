@@ -206,9 +206,8 @@ def run_layer_bench(f, w: wl.Workload, args, world, pk, peak_kind):
     stream = torch.cuda.current_stream()
     allreduce = None
     if world > 1:
-        import torch.distributed as dist
         # data-parallel replicas agree on scales: MAX of the five amaxes
-        allreduce = lambda: dist.all_reduce(lin.meta.amax, op=dist.ReduceOp.MAX)
+        allreduce = lambda: f.allreduce_amax(lin.meta)
 
     def step(i):
         lin.forward(xs[i % 2])
@@ -459,8 +458,8 @@ def main():
         if line is not None:
             print(json.dumps(line), flush=True)
         return
-    from fp8_mixed_precision_amax_gb300 import build as _build
-    _build.build()
+    import __graft_entry__
+    __graft_entry__._build_module().build()
     import fp8_mixed_precision_amax_gb300 as f
     pk, peak_kind = peaks()
     w = wl.WORKLOADS[args.workload]

@@ -287,3 +287,12 @@ class Fp8Linear:
         self.backward(dY, stream)
         self.update(stream)
         return self.Y, self.dX, self.dW
+
+
+def allreduce_amax(meta: Meta, group=None) -> None:
+    """Data-parallel replicas each see their own shard of tokens; before the
+    scale update they take the MAX of the five amaxes over all ranks so every
+    replica derives the same scales (max is exact and order-free, so the
+    result is bit-identical on every rank).  Uses torch.distributed."""
+    import torch.distributed as dist
+    dist.all_reduce(meta.amax, op=dist.ReduceOp.MAX, group=group)
