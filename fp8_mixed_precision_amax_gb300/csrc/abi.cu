@@ -155,9 +155,9 @@ fp8_status fp8_quantize_transpose(const void *x, int64_t rows, int64_t cols, con
     const char *fn = "fp8_quantize_transpose";
     FP8_TRY(check_dims16(fn, rows, "rows", cols, "cols"));
     if (fmt != FP8_E4M3 && fmt != FP8_E5M2) return fail(FP8_ERR_ARG, "%s: bad format %d", fn, fmt);
-    if (out == nullptr && out_t == nullptr)
-        return fail(FP8_ERR_ARG, "%s: out and out_t are both NULL", fn);
     const bool empty = rows == 0 || cols == 0;
+    if (!empty && out == nullptr && out_t == nullptr)
+        return fail(FP8_ERR_ARG, "%s: out and out_t are both NULL", fn);
     FP8_TRY(check_ptr(fn, x, "x", empty));
     FP8_TRY(check_scalar(fn, scale, "scale", false));
     FP8_TRY(check_ptr(fn, out, "out", true));

@@ -131,7 +131,8 @@ fp8_status fp8_amax(const void *x, int64_t n, float *amax, void *stream);
  *   out    DEVICE, [rows][cols] FP8 codes, or NULL
  *   out_t  DEVICE, [cols][rows] FP8 codes (the transpose of out), or NULL
  *   amax   DEVICE, 1 float overwritten with amax(x), or NULL
- * rows, cols >= 0 and multiples of 16.  At least one of out / out_t. */
+ * rows, cols >= 0 and multiples of 16.  At least one of out / out_t unless
+ * the tensor is empty (then only the amax, 0, is written). */
 fp8_status fp8_quantize_transpose(const void *x, int64_t rows, int64_t cols, const float *scale,
                                   int32_t fmt, uint8_t *out, uint8_t *out_t, float *amax,
                                   void *stream);
