@@ -64,6 +64,9 @@ def _load() -> ctypes.CDLL:
         "fp8_linear_bwd": ([vp, i64, i64, i64, ctypes.POINTER(fp8_meta),
                             ctypes.POINTER(fp8_recipe), vp, vp, vp, vp, vp, vp, vp],
                            ctypes.c_int),
+        "fp8_linear_bwd_noalloc": ([vp, i64, i64, i64, ctypes.POINTER(fp8_meta),
+                                    ctypes.POINTER(fp8_recipe), vp, vp, vp, vp, vp],
+                                   ctypes.c_int),
     }
     for name, (args, res) in sig.items():
         f = getattr(lib, name)
@@ -247,6 +250,26 @@ def fp8_linear_bwd(dY, meta: Meta, recipe: Recipe, X8t, W8t, dY8, dY8t, dX, dW,
                                ctypes.byref(r), _p8(X8t, "X8t"), _p8(W8t, "W8t"),
                                _p8(dY8, "dY8"), _p8(dY8t, "dY8t"), _ptr(dX, torch.bfloat16, "dX"),
                                _ptr(dW, torch.bfloat16, "dW"), _stream(stream)))
+
+
+def fp8_linear_bwd_noalloc(dY, meta: Meta, recipe: Recipe, X8t, W8t, dX, dW,
+                           stream=None) -> None:
+    """fp8_linear_bwd without the dY8 / dY8t work buffers, for callers that
+    cannot allocate device memory: the library keeps them in a fixed 64 MiB
+    device array (M * N <= 2^25).  Calls that overlap on the GPU race on that
+    array; the first call on a device should come before any stream capture."""
+    M, N = dY.shape
+    K = X8t.shape[0]
+    for t, shp, nm in [(X8t, (K, M), "X8t"), (W8t, (K, N), "W8t")]:
+        if tuple(t.shape) != shp:
+            raise ValueError(f"{nm} must be {list(shp)}")
+    if tuple(dX.shape) != (M, K) or tuple(dW.shape) != (N, K):
+        raise ValueError("dX must be [M,K] and dW [N,K]")
+    m, r = meta.c(), recipe.c()
+    _check(_lib.fp8_linear_bwd_noalloc(_ptr(dY, torch.bfloat16, "dY"), M, N, K, ctypes.byref(m),
+                                       ctypes.byref(r), _p8(X8t, "X8t"), _p8(W8t, "W8t"),
+                                       _ptr(dX, torch.bfloat16, "dX"),
+                                       _ptr(dW, torch.bfloat16, "dW"), _stream(stream)))
 
 
 class Fp8Linear:

@@ -124,6 +124,8 @@ fp8_status check_meta(const char *fn, const fp8_meta *m, const fp8_recipe *r) {
 
 }  // namespace
 
+void fp8k::set_last_error(const char *msg) { g_last_error = msg; }
+
 extern "C" {
 
 int32_t fp8_abi_version(void) { return FP8AMAX_ABI_VERSION; }

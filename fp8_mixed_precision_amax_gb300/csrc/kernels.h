@@ -30,6 +30,9 @@ cudaError_t launch_gemm_tn(const uint8_t *A, int fa, const uint8_t *B, int fb, i
                            const float *b_scale_inv, void *D, float *d_amax, bool zero_amax,
                            int sm_count, cudaStream_t st, const char **what);
 
+// Set the message fp8_last_error() returns on this host thread.
+void set_last_error(const char *msg);
+
 // Read and clear the device error flag the kernels set when a bounded wait
 // gives up (synchronizes the device flag's stream).
 cudaError_t read_and_clear_error_flag(unsigned *flags, cudaStream_t st);

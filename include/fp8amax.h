@@ -190,6 +190,32 @@ fp8_status fp8_linear_bwd(const void *dY, int64_t M, int64_t N, int64_t K, const
                           const fp8_recipe *recipe, const uint8_t *X8t, const uint8_t *W8t,
                           uint8_t *dY8, uint8_t *dY8t, void *dX, void *dW, void *stream);
 
+/* fp8_linear_bwd for callers that cannot allocate device memory.  The pages
+ * have no counterpart: this is a calling convenience, not part of the method.
+ * It computes exactly what fp8_linear_bwd computes, but the two FP8 work
+ * buffers (dY8, dY8t) are not passed in: they live in a fixed array in the
+ * library's own device memory (64 MiB on every GPU that loads the library,
+ * held until the process exits).  Callers that need it: a plugin handed only
+ * its input and output tensors by a framework whose allocator owns the device
+ * memory, or code that must not call cudaMalloc / cudaFree (cudaFree waits
+ * for the whole device).
+ *   Arguments as fp8_linear_bwd, without dY8 / dY8t.
+ *   Limit: M * N <= 2^25 (33,554,432) elements; larger sizes return
+ *   FP8_ERR_ARG and nothing is enqueued.
+ *   Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
+ *   Set-up: the first call on a device looks up the array's device address
+ *   (cudaGetSymbolAddress) with that device current; make that first call
+ *   before any stream capture.
+ *   All calls share the one array: calls that overlap on the GPU (on
+ *   different streams, or from different threads without ordering) race on
+ *   it; calls ordered on one stream do not.  Every call overwrites the part it
+ *   uses before reading it, so it never depends on what a previous call left
+ *   there. */
+fp8_status fp8_linear_bwd_noalloc(const void *dY, int64_t M, int64_t N, int64_t K,
+                                  const fp8_meta *meta, const fp8_recipe *recipe,
+                                  const uint8_t *X8t, const uint8_t *W8t, void *dX, void *dW,
+                                  void *stream);
+
 #ifdef __cplusplus
 }
 #endif
