@@ -10,11 +10,15 @@
 //    FP8 recipe").
 #include <cfloat>
 #include <cstdint>
+#include <mutex>
 
 #include "common.cuh"
 #include "kernels.h"
 
 namespace fp8k {
+
+// Set when a cast kernel gives up a bounded wait (read by fp8_sync_status).
+__device__ unsigned g_cast_error_flags = 0;
 
 // ------------------------------------------------------------------- amax --
 
@@ -58,19 +62,26 @@ __global__ void __launch_bounds__(512) amax_kernel(const uint4 *__restrict__ x, 
 
 // ----------------------------------------------------- quantize_transpose --
 //
-// One CTA of 256 threads converts 128 x 128 tiles (grid-stride over tiles):
-//  phase 1  each thread loads 8 x 16 B of BF16 (8 rows' worth of 8 columns),
-//           scales, converts to FP8, stores 8 B to the row-major output and
-//           the same 8 B into a shared-memory tile of 32-bit words
-//           [128 rows][32 words]; the word column is XOR-swizzled with the
-//           row's 16-row block so phase 2 reads are bank-conflict free;
+// Persistent CTAs of 256 threads (two per SM) convert 128 x 128 tiles.  The
+// BF16 input reaches shared memory through a 3-stage TMA ring, so the loads of
+// the next tiles are in flight while the current one is converted:
+//  phase 1  each thread takes 8 x 16 B of BF16 from the staged tile, scales,
+//           converts to FP8, stores 8 B to the row-major output and the same
+//           8 B into a tile of 32-bit words [128 rows][32 words] whose word
+//           column is XOR-swizzled with the row's 16-row block, so that the
+//           phase 2 reads are bank-conflict free;
 //  phase 2  each thread owns 16 rows x 4 columns: it reads 16 words, turns
 //           four 4 x 4 byte blocks around with byte permutes and writes four
 //           16-byte runs of the transposed output; the 8 threads sharing a
 //           column write one contiguous 128-byte line.
+// The staged tile is released (and the TMA load of a later tile issued) as
+// soon as phase 1 is done with it.  Waits are bounded.
 
 constexpr int kQtTile = 128;
 constexpr int kQtThreads = 256;
+constexpr int kQtStages = 3;
+constexpr int kQtStageBytes = kQtTile * kQtTile * 2;
+constexpr size_t kQtSmem = 128 + kQtStages * kQtStageBytes + kQtTile * kQtTile + 64;
 
 __device__ __forceinline__ int qt_swz(int row) { return ((row >> 4) & 7) << 2; }
 
@@ -90,28 +101,65 @@ __device__ __forceinline__ void transpose4x4(uint32_t w0, uint32_t w1, uint32_t 
 }
 
 template <int FMT>
-__global__ void __launch_bounds__(kQtThreads) quantize_transpose_kernel(
-    const uint16_t *__restrict__ x, int64_t rows, int64_t cols, const float *__restrict__ scale_p,
-    uint8_t *__restrict__ out, uint8_t *__restrict__ out_t, unsigned *__restrict__ amax_bits,
-    int64_t tiles_c, int64_t num_tiles) {
-    __shared__ __align__(16) uint32_t tile[kQtTile * (kQtTile / 4)];
-    const float s = *scale_p;
-    const int tid = threadIdx.x;
-    uint32_t tmax = 0;
+__global__ void __launch_bounds__(kQtThreads, 2) quantize_transpose_kernel(
+    const __grid_constant__ CUtensorMap tmx, int64_t rows, int64_t cols,
+    const float *__restrict__ scale_p, uint8_t *__restrict__ out, uint8_t *__restrict__ out_t,
+    unsigned *__restrict__ amax_bits, int64_t tiles_c, int64_t num_tiles) {
+    extern __shared__ uint8_t qt_smem_raw[];
+    uint8_t *base = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(qt_smem_raw) + 127) & ~static_cast<uintptr_t>(127));
+    uint8_t *stage_base = base;
+    uint32_t *tile = reinterpret_cast<uint32_t *>(base + kQtStages * kQtStageBytes);
+    uint64_t *full = reinterpret_cast<uint64_t *>(base + kQtStages * kQtStageBytes +
+                                                  kQtTile * kQtTile);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(full + kQtStages);
 
-    for (int64_t t = blockIdx.x; t < num_tiles; t += gridDim.x) {
+    const int tid = threadIdx.x;
+    const float s = *scale_p;
+    uint32_t tmax = 0;
+    // thread 0's count of loads issued into / consumed from each stage
+    int issued[kQtStages] = {}, consumed[kQtStages] = {};
+
+    if (tid == 0) {
+        for (int st = 0; st < kQtStages; ++st) mbar_init(smem_u32(full + st), 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+        prefetch_tmap(&tmx);
+        for (int st = 0; st < kQtStages; ++st) {
+            const int64_t t = blockIdx.x + static_cast<int64_t>(st) * gridDim.x;
+            if (t < num_tiles) {
+                ++issued[st];
+                mbar_arrive_expect_tx(smem_u32(full + st), kQtStageBytes);
+                tma_load_2d(smem_u32(stage_base + st * kQtStageBytes), &tmx, smem_u32(full + st),
+                            static_cast<int32_t>((t % tiles_c) * kQtTile),
+                            static_cast<int32_t>((t / tiles_c) * kQtTile));
+            }
+        }
+    }
+    __syncthreads();
+
+    int64_t it = 0;
+    for (int64_t t = blockIdx.x; t < num_tiles; t += gridDim.x, ++it) {
+        const int st = static_cast<int>(it % kQtStages);
+        const uint32_t parity = static_cast<uint32_t>((it / kQtStages) & 1);
         const int64_t r0 = (t / tiles_c) * kQtTile;
         const int64_t c0 = (t % tiles_c) * kQtTile;
+        const bool ok = mbar_wait(smem_u32(full + st), parity, abort_flag);
+        if (__syncthreads_or(!ok)) {
+            if (tid == 0) {
+                atomicOr(&g_cast_error_flags, kErrWaitTimeout);
+                *abort_flag = 1;
+            }
+            break;
+        }
+        if (tid == 0) ++consumed[st];
+        const uint16_t *xs = reinterpret_cast<const uint16_t *>(stage_base + st * kQtStageBytes);
 
         uint4 v[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
             const int idx = i * kQtThreads + tid;
-            const int rr = idx >> 4, vv = idx & 15;
-            const int64_t r = r0 + rr, c = c0 + vv * 8;
-            v[i] = make_uint4(0, 0, 0, 0);
-            if (r < rows && c < cols)
-                v[i] = __ldcs(reinterpret_cast<const uint4 *>(x + r * cols + c));
+            v[i] = *reinterpret_cast<const uint4 *>(xs + (idx >> 4) * kQtTile + (idx & 15) * 8);
         }
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
@@ -129,11 +177,22 @@ __global__ void __launch_bounds__(kQtThreads) quantize_transpose_kernel(
             q.y = cvt2_fp8<FMT>(__fmul_rn(bf16_lo(v[i].z), s), __fmul_rn(bf16_hi(v[i].z), s)) |
                   (cvt2_fp8<FMT>(__fmul_rn(bf16_lo(v[i].w), s), __fmul_rn(bf16_hi(v[i].w), s))
                    << 16);
-            const bool in = r < rows && c < cols;
-            if (out != nullptr && in) *reinterpret_cast<uint2 *>(out + r * cols + c) = q;
+            if (out != nullptr && r < rows && c < cols)
+                *reinterpret_cast<uint2 *>(out + r * cols + c) = q;
             *reinterpret_cast<uint2 *>(&tile[rr * 32 + ((vv * 2) ^ qt_swz(rr))]) = q;
         }
-        __syncthreads();
+        __syncthreads();  // stage st fully read; word tile complete
+
+        if (tid == 0) {
+            const int64_t tn = t + static_cast<int64_t>(kQtStages) * gridDim.x;
+            if (tn < num_tiles) {
+                ++issued[st];
+                mbar_arrive_expect_tx(smem_u32(full + st), kQtStageBytes);
+                tma_load_2d(smem_u32(stage_base + st * kQtStageBytes), &tmx, smem_u32(full + st),
+                            static_cast<int32_t>((tn % tiles_c) * kQtTile),
+                            static_cast<int32_t>((tn / tiles_c) * kQtTile));
+            }
+        }
 
         if (out_t != nullptr) {
             const int lane = tid & 31, warp = tid >> 5;
@@ -159,7 +218,15 @@ __global__ void __launch_bounds__(kQtThreads) quantize_transpose_kernel(
                         make_uint4(o[cc][0], o[cc][1], o[cc][2], o[cc][3]);
             }
         }
-        __syncthreads();
+        __syncthreads();  // word tile free for the next tile
+    }
+
+    // Loads still in flight (only after an abandoned wait) must land before exit.
+    if (tid == 0 && *abort_flag) {
+        for (int st = 0; st < kQtStages; ++st)
+            if (issued[st] > consumed[st])
+                mbar_wait(smem_u32(full + st), static_cast<uint32_t>((issued[st] - 1) & 1),
+                          nullptr, 100000000ull);
     }
 
     if (amax_bits != nullptr) {
@@ -234,42 +301,41 @@ cudaError_t launch_amax(const void *x, int64_t n, float *amax, int sm_count, cud
     return cudaGetLastError();
 }
 
-template <int FMT>
-static int qt_blocks_per_sm() {
-    static int cached = 0;
-    if (cached == 0) {
-        int b = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, quantize_transpose_kernel<FMT>,
-                                                          kQtThreads, 0) != cudaSuccess ||
-            b < 1)
-            b = 1;
-        cached = b;
-    }
-    return cached;
-}
-
 cudaError_t launch_quantize_transpose(const void *x, int64_t rows, int64_t cols,
                                       const float *scale, int fmt, uint8_t *out, uint8_t *out_t,
                                       float *amax, bool zero_amax, int sm_count,
                                       cudaStream_t st) {
+    static std::once_flag attr_once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(attr_once, [] {
+        attr_err = cudaFuncSetAttribute(quantize_transpose_kernel<0>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        static_cast<int>(kQtSmem));
+        if (attr_err == cudaSuccess)
+            attr_err = cudaFuncSetAttribute(quantize_transpose_kernel<1>,
+                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                            static_cast<int>(kQtSmem));
+    });
+    if (attr_err != cudaSuccess) return attr_err;
     if (amax != nullptr && zero_amax) {
         cudaError_t e = cudaMemsetAsync(amax, 0, sizeof(float), st);
         if (e != cudaSuccess) return e;
     }
     if (rows == 0 || cols == 0) return cudaSuccess;
+    CUtensorMap tm;
+    if (!encode_tmap_2d(&tm, x, true, cols, rows, kQtTile, kQtTile, false))
+        return cudaErrorInvalidValue;
     const int64_t tiles_c = (cols + kQtTile - 1) / kQtTile;
     const int64_t num_tiles = ((rows + kQtTile - 1) / kQtTile) * tiles_c;
-    const int per_sm = fmt == 0 ? qt_blocks_per_sm<0>() : qt_blocks_per_sm<1>();
-    int64_t blocks = static_cast<int64_t>(sm_count) * per_sm;
+    int64_t blocks = static_cast<int64_t>(sm_count) * 2;
     if (blocks > num_tiles) blocks = num_tiles;
-    const auto *xb = reinterpret_cast<const uint16_t *>(x);
     auto *ab = reinterpret_cast<unsigned *>(amax);
     if (fmt == 0)
-        quantize_transpose_kernel<0><<<static_cast<unsigned>(blocks), kQtThreads, 0, st>>>(
-            xb, rows, cols, scale, out, out_t, ab, tiles_c, num_tiles);
+        quantize_transpose_kernel<0><<<static_cast<unsigned>(blocks), kQtThreads, kQtSmem, st>>>(
+            tm, rows, cols, scale, out, out_t, ab, tiles_c, num_tiles);
     else
-        quantize_transpose_kernel<1><<<static_cast<unsigned>(blocks), kQtThreads, 0, st>>>(
-            xb, rows, cols, scale, out, out_t, ab, tiles_c, num_tiles);
+        quantize_transpose_kernel<1><<<static_cast<unsigned>(blocks), kQtThreads, kQtSmem, st>>>(
+            tm, rows, cols, scale, out, out_t, ab, tiles_c, num_tiles);
     return cudaGetLastError();
 }
 
@@ -289,6 +355,17 @@ cudaError_t launch_scale_update(float *history, const float *amax, float *scale,
     scale_update_kernel<<<num_tensors, kUpdThreads, smem, st>>>(history, amax, scale, scale_inv, L,
                                                                 format_mask, margin);
     return cudaGetLastError();
+}
+
+}  // namespace fp8k
+
+namespace fp8k {
+
+cudaError_t read_and_clear_cast_error_flag(unsigned *flags) {
+    cudaError_t e = cudaMemcpyFromSymbol(flags, g_cast_error_flags, sizeof(unsigned));
+    if (e != cudaSuccess) return e;
+    const unsigned zero = 0;
+    return cudaMemcpyToSymbol(g_cast_error_flags, &zero, sizeof(unsigned));
 }
 
 }  // namespace fp8k

@@ -21,8 +21,6 @@
 //              so the next tile's MMAs overlap this tile's epilogue.
 // Tiles are visited in groups of 16 row-blocks so that concurrently running
 // CTAs share A and B slices in L2.  Every wait is bounded.
-#include <cuda.h>
-#include <cudaTypedefs.h>
 #include <cuda_bf16.h>
 
 #include <cstdint>
@@ -37,14 +35,29 @@ __device__ unsigned g_error_flags = 0;
 
 namespace {
 
-constexpr int BM = 128, BN = 256, BK = 128, STAGES = 4;
-constexpr int A_STAGE = BM * BK, B_STAGE = BN * BK;
+// Tile geometry.  Each CTA owns 128 output rows and a 256-column fp32
+// accumulator (double-buffered: 512 TMEM columns).  The single-CTA variant
+// loads all 256 B rows itself (4 stages of 48 KB); the CTA-pair variant
+// splits a 256 x 256 tile over two SMs, each loading its 128 A rows and 128
+// of the 256 B rows (6 stages of 32 KB), with the even CTA issuing M = 256
+// MMAs that read both CTAs' shared memory.
+constexpr int BM = 128, BN = 256, BK = 128;
 constexpr int NUM_THREADS = 192;
 constexpr int TMEM_COLS = 2 * BN;
 constexpr int GROUP_M = 16;
-constexpr int NUM_BARS = 2 * STAGES + 4 + 1;  // full, empty, acc_full x2, acc_empty x2, drain
-constexpr size_t SMEM_BYTES =
-    1024 /*alignment slack*/ + STAGES * (A_STAGE + B_STAGE) + NUM_BARS * 8 + 16;
+
+template <bool PAIR>
+struct Cfg {
+    static constexpr int B_ROWS = PAIR ? BN / 2 : BN;    // B rows loaded per CTA
+    static constexpr int STAGES = PAIR ? 6 : 4;
+    static constexpr int A_STAGE = BM * BK;
+    static constexpr int B_STAGE = B_ROWS * BK;
+    static constexpr int TILE_M = PAIR ? 2 * BM : BM;    // output rows per (pair) tile
+    static constexpr int NUM_BARS = 2 * STAGES + 4 + 1;  // full, empty, acc_full x2, acc_empty x2, drain
+    static constexpr size_t SMEM = 1024 + STAGES * (A_STAGE + B_STAGE) + NUM_BARS * 8 + 16;
+    static constexpr uint32_t STAGE_TX = (PAIR ? 2 : 1) * (A_STAGE + B_STAGE);
+    static constexpr uint32_t EPI_ARRIVALS = PAIR ? 8 : 4;  // epilogue warps per tile
+};
 
 struct GemmParams {
     __nv_bfloat16 *D;
@@ -70,31 +83,37 @@ __device__ __forceinline__ void raise_error(volatile int *abort_flag) {
     *abort_flag = 1;
 }
 
+template <bool PAIR>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_tn_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const GemmParams p) {
+    using C = Cfg<PAIR>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint8_t *sA = smem;
-    uint8_t *sB = smem + STAGES * A_STAGE;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(sB + STAGES * B_STAGE);
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + NUM_BARS);
+    uint8_t *sB = smem + C::STAGES * C::A_STAGE;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sB + C::STAGES * C::B_STAGE);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + C::NUM_BARS);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + STAGES);
-    const uint32_t accf0 = smem_u32(bars + 2 * STAGES), acce0 = smem_u32(bars + 2 * STAGES + 2);
-    const uint32_t drain_bar = smem_u32(bars + 2 * STAGES + 4);
+    const uint32_t rank = PAIR ? cluster_ctarank() : 0u;   // 0 = the CTA that issues MMAs
+    const int unit = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+    const int num_units = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
+    const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + C::STAGES);
+    const uint32_t accf0 = smem_u32(bars + 2 * C::STAGES);
+    const uint32_t acce0 = smem_u32(bars + 2 * C::STAGES + 2);
+    const uint32_t drain_bar = smem_u32(bars + 2 * C::STAGES + 4);
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < STAGES; ++s) {
+        for (int s = 0; s < C::STAGES; ++s) {
             mbar_init(full0 + 8 * s, 1);
             mbar_init(empty0 + 8 * s, 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(accf0 + 8 * b, 1);
-            mbar_init(acce0 + 8 * b, 4);  // one arrival per epilogue warp
+            mbar_init(acce0 + 8 * b, C::EPI_ARRIVALS);
         }
         mbar_init(drain_bar, 1);
         *abort_flag = 0;
@@ -103,14 +122,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         prefetch_tmap(&tmB);
     }
     if (warp == 1) {
-        tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
-        tmem_relinquish();
+        if constexpr (PAIR) {
+            tmem_alloc_pair(smem_u32(tmem_slot), TMEM_COLS);
+            tmem_relinquish_pair();
+        } else {
+            tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+            tmem_relinquish();
+        }
         tc_fence_before();
     }
     __syncthreads();
+    if constexpr (PAIR) {
+        __syncwarp();
+        cluster_sync();   // both CTAs' barriers exist before any remote signal
+    }
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
-
     const int num_tiles = p.tiles_m * p.tiles_n;
 
     if (warp == 0) {
@@ -120,9 +147,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             uint32_t phase = 0;
             int64_t issued = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+            for (int tile = unit; ok && tile < num_tiles; tile += num_units) {
                 int mb, nb;
                 tile_coords(tile, p.tiles_m, p.tiles_n, mb, nb);
+                const int32_t arow = mb * C::TILE_M + static_cast<int32_t>(rank) * BM;
+                const int32_t brow = nb * BN + static_cast<int32_t>(rank) * C::B_ROWS;
                 for (int kb = 0; kb < p.num_kb; ++kb) {
                     if (!mbar_wait(empty0 + 8 * stage, phase ^ 1u, abort_flag)) {
                         raise_error(abort_flag);
@@ -130,32 +159,52 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         break;
                     }
                     const uint32_t fb = full0 + 8 * stage;
-                    mbar_arrive_expect_tx(fb, A_STAGE + B_STAGE);
-                    tma_load_2d(smem_u32(sA + stage * A_STAGE), &tmA, fb, kb * BK, mb * BM);
-                    tma_load_2d(smem_u32(sB + stage * B_STAGE), &tmB, fb, kb * BK, nb * BN);
+                    const uint32_t dA = smem_u32(sA + stage * C::A_STAGE);
+                    const uint32_t dB = smem_u32(sB + stage * C::B_STAGE);
+                    if constexpr (PAIR) {
+                        // both halves complete on the even CTA's barrier
+                        const uint32_t fb0 = mapa_shared(fb, 0);
+                        if (rank == 0) mbar_arrive_expect_tx(fb, C::STAGE_TX);
+                        tma_load_2d_pair(dA, &tmA, fb0, kb * BK, arow);
+                        tma_load_2d_pair(dB, &tmB, fb0, kb * BK, brow);
+                    } else {
+                        mbar_arrive_expect_tx(fb, C::STAGE_TX);
+                        tma_load_2d(dA, &tmA, fb, kb * BK, arow);
+                        tma_load_2d(dB, &tmB, fb, kb * BK, brow);
+                    }
                     ++issued;
-                    if (++stage == STAGES) {
+                    if (++stage == C::STAGES) {
                         stage = 0;
                         phase ^= 1u;
                     }
                 }
             }
-            if (!ok) {
+            if (ok) {
+                // Every stage's last release must have arrived before the CTA exits
+                // (in a pair it is signalled from the other SM).
+                for (int i = 0; i < C::STAGES; ++i) {
+                    mbar_wait(empty0 + 8 * stage, phase ^ 1u, abort_flag);
+                    if (++stage == C::STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            } else if (!PAIR || rank == 0) {
                 // Let the copies already issued land before the CTA exits.
-                for (int i = 0; i < STAGES && issued > 0; ++i, --issued) {
-                    stage = stage == 0 ? STAGES - 1 : stage - 1;
-                    if (stage == STAGES - 1) phase ^= 1u;
+                for (int i = 0; i < C::STAGES && issued > 0; ++i, --issued) {
+                    stage = stage == 0 ? C::STAGES - 1 : stage - 1;
+                    if (stage == C::STAGES - 1) phase ^= 1u;
                     mbar_wait(full0 + 8 * stage, phase, nullptr, 100000000ull);
                 }
             }
         }
     } else if (warp == 1) {
         // ------------------------------------------------------- MMA issuer
-        if (lane == 0) {
+        if (lane == 0 && rank == 0) {
             int stage = 0, acc = 0;
             uint32_t phase = 0, acc_phase = 0;
             bool ok = true, any = false;
-            for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+            for (int tile = unit; ok && tile < num_tiles; tile += num_units) {
                 if (!mbar_wait(acce0 + 8 * acc, acc_phase ^ 1u, abort_flag)) {
                     raise_error(abort_flag);
                     ok = false;
@@ -170,21 +219,32 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t a0 = smem_u32(sA + stage * A_STAGE);
-                    const uint32_t b0 = smem_u32(sB + stage * B_STAGE);
+                    const uint32_t a0 = smem_u32(sA + stage * C::A_STAGE);
+                    const uint32_t b0 = smem_u32(sB + stage * C::B_STAGE);
 #pragma unroll
-                    for (int k = 0; k < BK / 32; ++k)
-                        mma_f8f6f4(d_tmem, smem_desc_sw128(a0 + 32 * k),
-                                   smem_desc_sw128(b0 + 32 * k), p.idesc, (kb | k) != 0);
-                    mma_commit(empty0 + 8 * stage);
+                    for (int k = 0; k < BK / 32; ++k) {
+                        const uint64_t ad = smem_desc_sw128(a0 + 32 * k);
+                        const uint64_t bd = smem_desc_sw128(b0 + 32 * k);
+                        if constexpr (PAIR)
+                            mma_f8f6f4_pair(d_tmem, ad, bd, p.idesc, (kb | k) != 0);
+                        else
+                            mma_f8f6f4(d_tmem, ad, bd, p.idesc, (kb | k) != 0);
+                    }
+                    if constexpr (PAIR)
+                        mma_commit_pair(empty0 + 8 * stage, 0x3);
+                    else
+                        mma_commit(empty0 + 8 * stage);
                     any = true;
-                    if (++stage == STAGES) {
+                    if (++stage == C::STAGES) {
                         stage = 0;
                         phase ^= 1u;
                     }
                 }
                 if (!ok) break;
-                mma_commit(accf0 + 8 * acc);
+                if constexpr (PAIR)
+                    mma_commit_pair(accf0 + 8 * acc, 0x3);
+                else
+                    mma_commit(accf0 + 8 * acc);
                 if (++acc == 2) {
                     acc = 0;
                     acc_phase ^= 1u;
@@ -192,7 +252,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
             if (!ok && any) {
                 // Wait (bounded) for the MMAs in flight before TMEM is freed.
-                mma_commit(drain_bar);
+                if constexpr (PAIR)
+                    mma_commit_pair(drain_bar, 0x1);
+                else
+                    mma_commit(drain_bar);
                 mbar_wait(drain_bar, 0, nullptr, 100000000ull);
             }
         }
@@ -203,7 +266,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         uint32_t tmax = 0;
         int acc = 0;
         uint32_t acc_phase = 0;
-        for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+        for (int tile = unit; tile < num_tiles; tile += num_units) {
             int mb, nb;
             tile_coords(tile, p.tiles_m, p.tiles_n, mb, nb);
             const bool got = mbar_wait(accf0 + 8 * acc, acc_phase, abort_flag);
@@ -213,7 +276,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 break;
             }
             tc_fence_after();
-            const int64_t row = static_cast<int64_t>(mb) * BM + q * 32 + lane;
+            const int64_t row = static_cast<int64_t>(mb) * C::TILE_M + rank * BM + q * 32 + lane;
             const bool row_in = row < p.M;
             __nv_bfloat16 *drow = p.D + row * p.N;
             const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
@@ -248,7 +311,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(acce0 + 8 * acc);
+            if (lane == 0) {
+                if constexpr (PAIR)
+                    mbar_arrive_cluster(mapa_shared(acce0 + 8 * acc, 0));
+                else
+                    mbar_arrive(acce0 + 8 * acc);
+            }
             if (++acc == 2) {
                 acc = 0;
                 acc_phase ^= 1u;
@@ -261,38 +329,78 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
 
     __syncthreads();
+    if constexpr (PAIR) {
+        __syncwarp();
+        cluster_sync();   // the other SM is done with this CTA's memory
+    }
     if (warp == 1) {
         __syncwarp();
         tc_fence_after();
-        tmem_dealloc(tmem_base, TMEM_COLS);
+        if constexpr (PAIR)
+            tmem_dealloc_pair(tmem_base, TMEM_COLS);
+        else
+            tmem_dealloc(tmem_base, TMEM_COLS);
     }
 }
 
 // --------------------------------------------------------------- host side --
 
-PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
-std::once_flag g_encode_once;
-
-bool encode_kmajor_fp8(CUtensorMap *map, const uint8_t *base, int64_t rows, int64_t K,
-                       uint32_t box_rows) {
-    std::call_once(g_encode_once, [] {
-        void *fn = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
-                                             cudaEnableDefault, &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+template <bool PAIR>
+static cudaError_t launch_variant(const CUtensorMap &ta, const CUtensorMap &tb, const GemmParams &p,
+                                  int grid, cudaStream_t st) {
+    static std::once_flag attr_once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(attr_once, [] {
+        attr_err = cudaFuncSetAttribute(gemm_tn_kernel<PAIR>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        static_cast<int>(Cfg<PAIR>::SMEM));
     });
-    if (g_encode == nullptr) return false;
-    cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
-    cuuint64_t strides[1] = {static_cast<cuuint64_t>(K)};
-    cuuint32_t box[2] = {static_cast<cuuint32_t>(BK), box_rows};
-    cuuint32_t estr[2] = {1, 1};
-    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(base), dims,
-                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS;
+    if (attr_err != cudaSuccess) return attr_err;
+    if constexpr (PAIR) {
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+        cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+        cfg.dynamicSmemBytes = Cfg<PAIR>::SMEM;
+        cfg.stream = st;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        return cudaLaunchKernelEx(&cfg, gemm_tn_kernel<PAIR>, ta, tb, p);
+    } else {
+        gemm_tn_kernel<PAIR><<<grid, NUM_THREADS, Cfg<PAIR>::SMEM, st>>>(ta, tb, p);
+        return cudaGetLastError();
+    }
+}
+
+// Number of CTA pairs that can be resident at once (clusters of two need two
+// SMs of the same GPC), cached per process.
+static int pair_slots(int sm_count) {
+    static std::once_flag once;
+    static int slots = 0;
+    std::call_once(once, [sm_count] {
+        cudaFuncSetAttribute(gemm_tn_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(Cfg<true>::SMEM));
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.gridDim = dim3(static_cast<unsigned>(sm_count & ~1), 1, 1);
+        cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+        cfg.dynamicSmemBytes = Cfg<true>::SMEM;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, gemm_tn_kernel<true>, &cfg) != cudaSuccess || n < 1)
+            n = 0;
+        slots = n;
+    });
+    return slots;
 }
 
 }  // namespace
@@ -301,19 +409,18 @@ cudaError_t launch_gemm_tn(const uint8_t *A, int fa, const uint8_t *B, int fb, i
                            int64_t N, int64_t K, const float *a_scale_inv,
                            const float *b_scale_inv, void *D, float *d_amax, bool zero_amax,
                            int sm_count, cudaStream_t st, const char **what) {
-    static std::once_flag attr_once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(attr_once, [] {
-        attr_err = cudaFuncSetAttribute(gemm_tn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        static_cast<int>(SMEM_BYTES));
-    });
-    if (attr_err != cudaSuccess) return attr_err;
     if (d_amax != nullptr && zero_amax) {
         cudaError_t e = cudaMemsetAsync(d_amax, 0, sizeof(float), st);
         if (e != cudaSuccess) return e;
     }
+    // CTA pairs for anything taller than one 128-row tile, when the GPU can
+    // hold them; single CTAs otherwise.
+    const int slots = M > BM ? pair_slots(sm_count) : 0;
+    const bool pair = slots > 0;
+    const uint32_t b_rows = pair ? BN / 2 : BN;
     CUtensorMap ta, tb;
-    if (!encode_kmajor_fp8(&ta, A, M, K, BM) || !encode_kmajor_fp8(&tb, B, N, K, BN)) {
+    if (!encode_tmap_2d(&ta, A, false, K, M, BK, BM, true) ||
+        !encode_tmap_2d(&tb, B, false, K, N, BK, b_rows, true)) {
         if (what) *what = "cuTensorMapEncodeTiled failed for an operand";
         return cudaErrorInvalidValue;
     }
@@ -324,14 +431,19 @@ cudaError_t launch_gemm_tn(const uint8_t *A, int fa, const uint8_t *B, int fb, i
     p.b_scale_inv = b_scale_inv;
     p.M = M;
     p.N = N;
-    p.tiles_m = static_cast<int>((M + BM - 1) / BM);
+    const int tile_m = pair ? 2 * BM : BM;
+    p.tiles_m = static_cast<int>((M + tile_m - 1) / tile_m);
     p.tiles_n = static_cast<int>((N + BN - 1) / BN);
     p.num_kb = static_cast<int>((K + BK - 1) / BK);
-    p.idesc = idesc_f8(static_cast<uint32_t>(fa), static_cast<uint32_t>(fb), BM, BN);
+    p.idesc = idesc_f8(static_cast<uint32_t>(fa), static_cast<uint32_t>(fb),
+                       static_cast<uint32_t>(tile_m), BN);
     const int num_tiles = p.tiles_m * p.tiles_n;
+    if (pair) {
+        const int units = num_tiles < slots ? num_tiles : slots;
+        return launch_variant<true>(ta, tb, p, 2 * units, st);
+    }
     const int grid = num_tiles < sm_count ? num_tiles : sm_count;
-    gemm_tn_kernel<<<grid, NUM_THREADS, SMEM_BYTES, st>>>(ta, tb, p);
-    return cudaGetLastError();
+    return launch_variant<false>(ta, tb, p, grid, st);
 }
 
 cudaError_t read_and_clear_error_flag(unsigned *flags, cudaStream_t st) {
@@ -340,7 +452,12 @@ cudaError_t read_and_clear_error_flag(unsigned *flags, cudaStream_t st) {
     e = cudaMemcpyFromSymbol(flags, g_error_flags, sizeof(unsigned));
     if (e != cudaSuccess) return e;
     const unsigned zero = 0;
-    return cudaMemcpyToSymbol(g_error_flags, &zero, sizeof(unsigned));
+    e = cudaMemcpyToSymbol(g_error_flags, &zero, sizeof(unsigned));
+    if (e != cudaSuccess) return e;
+    unsigned cast_flags = 0;
+    e = read_and_clear_cast_error_flag(&cast_flags);
+    *flags |= cast_flags;
+    return e;
 }
 
 }  // namespace fp8k

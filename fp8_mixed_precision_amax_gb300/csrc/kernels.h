@@ -2,17 +2,26 @@
 // library; the public C ABI is include/fp8amax.h).
 #pragma once
 
-#include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <cstdint>
+
 namespace fp8k {
+
+// Tiled 2-D TMA descriptor of a row-major [outer][inner] tensor of 1- or
+// 2-byte elements with a box of box_outer x box_inner elements, optionally
+// with 128-byte swizzling (tmap.cu).  False if the driver rejects it.
+bool encode_tmap_2d(CUtensorMap *map, const void *base, bool two_byte, int64_t inner,
+                    int64_t outer, uint32_t box_inner, uint32_t box_outer, bool swizzle128);
 
 // amax of n BF16 values into *amax (zeroed first).
 cudaError_t launch_amax(const void *x, int64_t n, float *amax, int sm_count, cudaStream_t st);
 
 // Fused scaled cast + transposed copy + amax.  fmt: 0 = E4M3, 1 = E5M2.
 // With zero_amax the amax word is cleared first; otherwise the tensor's amax
-// is max-combined into it.
+// is max-combined into it.  Returns cudaErrorInvalidValue when the input's
+// TMA descriptor cannot be built.
 cudaError_t launch_quantize_transpose(const void *x, int64_t rows, int64_t cols,
                                       const float *scale, int fmt, uint8_t *out, uint8_t *out_t,
                                       float *amax, bool zero_amax, int sm_count, cudaStream_t st);
@@ -32,6 +41,9 @@ cudaError_t launch_gemm_tn(const uint8_t *A, int fa, const uint8_t *B, int fb, i
 
 // Set the message fp8_last_error() returns on this host thread.
 void set_last_error(const char *msg);
+
+// Read and clear the cast kernels' device error flag (cast.cu).
+cudaError_t read_and_clear_cast_error_flag(unsigned *flags);
 
 // Read and clear the device error flag the kernels set when a bounded wait
 // gives up (synchronizes the device flag's stream).
