@@ -41,7 +41,10 @@ class fp8_meta(ctypes.Structure):
 
 class fp8_recipe(ctypes.Structure):
     _fields_ = [("margin", ctypes.c_int32), ("history_len", ctypes.c_int32),
-                ("hybrid", ctypes.c_int32)]
+                ("hybrid", ctypes.c_int32), ("scaling", ctypes.c_int32)]
+
+
+SCALING_DELAYED, SCALING_CURRENT = 0, 1
 
 
 def _load() -> ctypes.CDLL:
@@ -55,6 +58,8 @@ def _load() -> ctypes.CDLL:
         "fp8_sync_status": ([vp], ctypes.c_int),
         "fp8_amax": ([vp, i64, vp, vp], ctypes.c_int),
         "fp8_quantize_transpose": ([vp, i64, i64, vp, i32, vp, vp, vp, vp], ctypes.c_int),
+        "fp8_quantize_transpose_current": ([vp, i64, i64, i32, i32, vp, vp, vp, vp, vp, vp],
+                                           ctypes.c_int),
         "fp8_scale_update": ([vp, vp, vp, vp, i32, i32, u32, i32, vp], ctypes.c_int),
         "fp8_amax_scale_update": ([ctypes.POINTER(fp8_meta), ctypes.POINTER(fp8_recipe), vp],
                                   ctypes.c_int),
@@ -71,7 +76,7 @@ def _load() -> ctypes.CDLL:
     for name, (args, res) in sig.items():
         f = getattr(lib, name)
         f.argtypes, f.restype = args, res
-    if lib.fp8_abi_version() != 1:
+    if lib.fp8_abi_version() != 2:
         raise ImportError("libfp8amax.so ABI version mismatch")
     return lib
 
@@ -153,6 +158,20 @@ def fp8_quantize_transpose(x: torch.Tensor, scale: torch.Tensor, fmt: int, out=N
                                        _stream(stream)))
 
 
+def fp8_quantize_transpose_current(x: torch.Tensor, fmt: int, margin: int, amax: torch.Tensor,
+                                   scale: torch.Tensor, scale_inv: torch.Tensor, out=None,
+                                   out_t=None, stream=None) -> None:
+    rows, cols = x.shape
+    if out is not None and tuple(out.shape) != (rows, cols):
+        raise ValueError("out must be [rows, cols]")
+    if out_t is not None and tuple(out_t.shape) != (cols, rows):
+        raise ValueError("out_t must be [cols, rows]")
+    _check(_lib.fp8_quantize_transpose_current(
+        _ptr(x, torch.bfloat16, "x"), rows, cols, fmt, margin, _p8(out, "out"), _p8(out_t, "out_t"),
+        _ptr(amax, torch.float32, "amax"), _ptr(scale, torch.float32, "scale"),
+        _ptr(scale_inv, torch.float32, "scale_inv"), _stream(stream)))
+
+
 def fp8_scale_update(history: torch.Tensor, amax: torch.Tensor, scale: torch.Tensor,
                      scale_inv: torch.Tensor, format_mask: int, margin: int, stream=None) -> None:
     n, L = history.shape
@@ -181,13 +200,16 @@ def fp8_gemm_tn(A: torch.Tensor, fa: int, B: torch.Tensor, fb: int, a_scale_inv:
 @dataclass
 class Recipe:
     """DelayedScaling: margin (default 0), amax_history_len (default 1024),
-    HYBRID (E4M3 forward, E5M2 backward) or E4M3 everywhere."""
+    HYBRID (E4M3 forward, E5M2 backward) or E4M3 everywhere; ``current``
+    switches X, W and dY to just-in-time scaling from their own amax."""
     margin: int = 0
     history_len: int = 1024
     hybrid: bool = True
+    current: bool = False
 
     def c(self) -> fp8_recipe:
-        return fp8_recipe(self.margin, self.history_len, 1 if self.hybrid else 0)
+        return fp8_recipe(self.margin, self.history_len, 1 if self.hybrid else 0,
+                          SCALING_CURRENT if self.current else SCALING_DELAYED)
 
 
 class Meta:
@@ -292,24 +314,33 @@ class Fp8Linear:
         b = lambda *s: torch.empty(s, dtype=torch.bfloat16, device=dev)
         self.Y, self.dX, self.dW = b(M, N), b(M, K), b(N, K)
 
-    def forward(self, X: torch.Tensor, stream=None) -> torch.Tensor:
+    def forward(self, X: torch.Tensor, stream=None, Y: torch.Tensor | None = None) -> torch.Tensor:
+        """Y = X W^T; written into ``Y`` if given, else into the layer's own buffer."""
+        Y = self.Y if Y is None else Y
         fp8_linear_fwd(X, self.W, self.meta, self.recipe, self.X8, self.X8t, self.W8, self.W8t,
-                       self.Y, stream)
-        return self.Y
+                       Y, stream)
+        return Y
 
-    def backward(self, dY: torch.Tensor, stream=None):
+    def backward(self, dY: torch.Tensor, stream=None, dX: torch.Tensor | None = None,
+                 dW: torch.Tensor | None = None):
+        """dX = dY W and dW = dY^T X, into the given buffers or the layer's own."""
+        dX = self.dX if dX is None else dX
+        dW = self.dW if dW is None else dW
         fp8_linear_bwd(dY, self.meta, self.recipe, self.X8t, self.W8t, self.dY8, self.dY8t,
-                       self.dX, self.dW, stream)
-        return self.dX, self.dW
+                       dX, dW, stream)
+        return dX, dW
 
     def update(self, stream=None) -> None:
         fp8_amax_scale_update(self.meta, self.recipe, stream)
 
-    def step(self, X: torch.Tensor, dY: torch.Tensor, stream=None):
-        self.forward(X, stream)
-        self.backward(dY, stream)
+    def step(self, X: torch.Tensor, dY: torch.Tensor, stream=None, outs=None):
+        """Forward, backward and the recipe's update; ``outs`` = (Y, dX, dW)
+        buffers to write instead of the layer's own."""
+        Y, dX, dW = outs if outs is not None else (None, None, None)
+        Y = self.forward(X, stream, Y)
+        dX, dW = self.backward(dY, stream, dX, dW)
         self.update(stream)
-        return self.Y, self.dX, self.dW
+        return Y, dX, dW
 
 
 def allreduce_amax(meta: Meta, group=None) -> None:

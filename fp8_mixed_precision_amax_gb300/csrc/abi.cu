@@ -119,6 +119,8 @@ fp8_status check_meta(const char *fn, const fp8_meta *m, const fp8_recipe *r) {
                     fn, r->history_len, m->history_len);
     if (r->hybrid != 0 && r->hybrid != 1)
         return fail(FP8_ERR_ARG, "%s: hybrid must be 0 or 1", fn);
+    if (r->scaling != FP8_SCALING_DELAYED && r->scaling != FP8_SCALING_CURRENT)
+        return fail(FP8_ERR_ARG, "%s: scaling must be delayed (0) or current (1)", fn);
     return FP8_OK;
 }
 
@@ -169,6 +171,33 @@ fp8_status fp8_quantize_transpose(const void *x, int64_t rows, int64_t cols, con
     FP8_TRY(current_device(&sms));
     FP8_CUDA(fp8k::launch_quantize_transpose(x, rows, cols, scale, fmt, out, out_t, amax, true, sms,
                                              static_cast<cudaStream_t>(stream)),
+             fn);
+    return FP8_OK;
+}
+
+fp8_status fp8_quantize_transpose_current(const void *x, int64_t rows, int64_t cols, int32_t fmt,
+                                          int32_t margin, uint8_t *out, uint8_t *out_t,
+                                          float *amax, float *scale, float *scale_inv,
+                                          void *stream) {
+    const char *fn = "fp8_quantize_transpose_current";
+    FP8_TRY(check_dims16(fn, rows, "rows", cols, "cols"));
+    if (fmt != FP8_E4M3 && fmt != FP8_E5M2) return fail(FP8_ERR_ARG, "%s: bad format %d", fn, fmt);
+    if (margin < 0 || margin > 64)
+        return fail(FP8_ERR_ARG, "%s: margin %d outside [0, 64]", fn, margin);
+    const bool empty = rows == 0 || cols == 0;
+    if (!empty && out == nullptr && out_t == nullptr)
+        return fail(FP8_ERR_ARG, "%s: out and out_t are both NULL", fn);
+    FP8_TRY(check_ptr(fn, x, "x", empty));
+    FP8_TRY(check_ptr(fn, out, "out", true));
+    FP8_TRY(check_ptr(fn, out_t, "out_t", true));
+    FP8_TRY(check_scalar(fn, amax, "amax", false));
+    FP8_TRY(check_scalar(fn, scale, "scale", false));
+    FP8_TRY(check_scalar(fn, scale_inv, "scale_inv", false));
+    int sms;
+    FP8_TRY(current_device(&sms));
+    FP8_CUDA(fp8k::launch_quantize_transpose_current(x, rows, cols, fmt, margin, out, out_t, amax,
+                                                     scale, scale_inv, sms,
+                                                     static_cast<cudaStream_t>(stream)),
              fn);
     return FP8_OK;
 }
@@ -256,12 +285,23 @@ fp8_status fp8_linear_fwd(const void *X, const void *W, int64_t M, int64_t N, in
     float *am = meta->amax;
     // amax of X, W and Y are max-combined into slots cleared here.
     FP8_CUDA(cudaMemsetAsync(am + FP8_SLOT_X, 0, 3 * sizeof(float), st), fn);
-    FP8_CUDA(fp8k::launch_quantize_transpose(X, M, K, meta->scale + FP8_SLOT_X, FP8_E4M3, X8, X8t,
-                                             am + FP8_SLOT_X, false, sms, st),
-             fn);
-    FP8_CUDA(fp8k::launch_quantize_transpose(W, N, K, meta->scale + FP8_SLOT_W, FP8_E4M3, W8, W8t,
-                                             am + FP8_SLOT_W, false, sms, st),
-             fn);
+    if (recipe->scaling == FP8_SCALING_CURRENT) {
+        FP8_CUDA(fp8k::launch_quantize_transpose_current(
+                     X, M, K, FP8_E4M3, recipe->margin, X8, X8t, am + FP8_SLOT_X,
+                     meta->scale + FP8_SLOT_X, meta->scale_inv + FP8_SLOT_X, sms, st),
+                 fn);
+        FP8_CUDA(fp8k::launch_quantize_transpose_current(
+                     W, N, K, FP8_E4M3, recipe->margin, W8, W8t, am + FP8_SLOT_W,
+                     meta->scale + FP8_SLOT_W, meta->scale_inv + FP8_SLOT_W, sms, st),
+                 fn);
+    } else {
+        FP8_CUDA(fp8k::launch_quantize_transpose(X, M, K, meta->scale + FP8_SLOT_X, FP8_E4M3, X8,
+                                                 X8t, am + FP8_SLOT_X, false, sms, st),
+                 fn);
+        FP8_CUDA(fp8k::launch_quantize_transpose(W, N, K, meta->scale + FP8_SLOT_W, FP8_E4M3, W8,
+                                                 W8t, am + FP8_SLOT_W, false, sms, st),
+                 fn);
+    }
     return gemm_checked(fn, X8, FP8_E4M3, W8, FP8_E4M3, M, N, K, meta->scale_inv + FP8_SLOT_X,
                         meta->scale_inv + FP8_SLOT_W, Y, am + FP8_SLOT_Y, false, sms, st);
 }
@@ -287,9 +327,15 @@ fp8_status fp8_linear_bwd(const void *dY, int64_t M, int64_t N, int64_t K, const
     float *am = meta->amax;
     const int32_t fg = recipe->hybrid ? FP8_E5M2 : FP8_E4M3;
     FP8_CUDA(cudaMemsetAsync(am + FP8_SLOT_DY, 0, 2 * sizeof(float), st), fn);
-    FP8_CUDA(fp8k::launch_quantize_transpose(dY, M, N, meta->scale + FP8_SLOT_DY, fg, dY8, dY8t,
-                                             am + FP8_SLOT_DY, false, sms, st),
-             fn);
+    if (recipe->scaling == FP8_SCALING_CURRENT)
+        FP8_CUDA(fp8k::launch_quantize_transpose_current(
+                     dY, M, N, fg, recipe->margin, dY8, dY8t, am + FP8_SLOT_DY,
+                     meta->scale + FP8_SLOT_DY, meta->scale_inv + FP8_SLOT_DY, sms, st),
+                 fn);
+    else
+        FP8_CUDA(fp8k::launch_quantize_transpose(dY, M, N, meta->scale + FP8_SLOT_DY, fg, dY8,
+                                                 dY8t, am + FP8_SLOT_DY, false, sms, st),
+                 fn);
     // dgrad: dX[M][K] = dY8[M][N] . W8t[K][N]^T
     FP8_TRY(gemm_checked(fn, dY8, fg, W8t, FP8_E4M3, M, K, N, meta->scale_inv + FP8_SLOT_DY,
                          meta->scale_inv + FP8_SLOT_W, dX, am + FP8_SLOT_DX, false, sms, st));

@@ -60,6 +60,21 @@ __global__ void __launch_bounds__(512) amax_kernel(const uint4 *__restrict__ x, 
     }
 }
 
+// ------------------------------------------------------- the scale formula --
+// scale = fl32(fl32(fmax / m) * 2^-margin), +inf clamped to FLT_MAX, when
+// 0 < m < inf (m = the amax, or the max over the amax history); otherwise the
+// previous scale is kept (valid = false).
+__device__ __forceinline__ float recipe_scale(float m, float fmax, int margin, float prev,
+                                              bool &valid) {
+    valid = m > 0.0f && m <= FLT_MAX;
+    if (!valid) return prev;
+    const float q = __fdiv_rn(fmax, m);
+    const float p2 = __uint_as_float(static_cast<uint32_t>(127 - margin) << 23);
+    float sc = __fmul_rn(q, p2);
+    if (sc > FLT_MAX) sc = FLT_MAX;
+    return sc;
+}
+
 // ----------------------------------------------------- quantize_transpose --
 //
 // Persistent CTAs of 256 threads (two per SM) convert 128 x 128 tiles.  The
@@ -100,11 +115,14 @@ __device__ __forceinline__ void transpose4x4(uint32_t w0, uint32_t w1, uint32_t 
     t3 = __byte_perm(b01, b23, 0x7632);
 }
 
-template <int FMT>
+// CURRENT = just-in-time scaling: the scale is derived here from this tensor's
+// amax (computed by amax_kernel just before) instead of being read as given;
+// block 0 also writes it and its inverse back.
+template <int FMT, bool CURRENT>
 __global__ void __launch_bounds__(kQtThreads, 2) quantize_transpose_kernel(
-    const __grid_constant__ CUtensorMap tmx, int64_t rows, int64_t cols,
-    const float *__restrict__ scale_p, uint8_t *__restrict__ out, uint8_t *__restrict__ out_t,
-    unsigned *__restrict__ amax_bits, int64_t tiles_c, int64_t num_tiles) {
+    const __grid_constant__ CUtensorMap tmx, int64_t rows, int64_t cols, float *scale_p,
+    uint8_t *__restrict__ out, uint8_t *__restrict__ out_t, unsigned *__restrict__ amax_bits,
+    int64_t tiles_c, int64_t num_tiles, const float *amax_in, float *scale_inv_p, int margin) {
     extern __shared__ uint8_t qt_smem_raw[];
     uint8_t *base = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(qt_smem_raw) + 127) & ~static_cast<uintptr_t>(127));
@@ -115,7 +133,15 @@ __global__ void __launch_bounds__(kQtThreads, 2) quantize_transpose_kernel(
     volatile int *abort_flag = reinterpret_cast<volatile int *>(full + kQtStages);
 
     const int tid = threadIdx.x;
-    const float s = *scale_p;
+    float s = *scale_p;
+    if constexpr (CURRENT) {
+        bool valid;
+        s = recipe_scale(*amax_in, FMT == 0 ? 448.0f : 57344.0f, margin, s, valid);
+        if (valid && blockIdx.x == 0 && tid == 0) {
+            *scale_p = s;
+            *scale_inv_p = __fdiv_rn(1.0f, s);
+        }
+    }
     uint32_t tmax = 0;
     // thread 0's count of loads issued into / consumed from each stage
     int issued[kQtStages] = {}, consumed[kQtStages] = {};
@@ -273,12 +299,10 @@ __global__ void __launch_bounds__(kUpdThreads) scale_update_kernel(
     if (threadIdx.x == 0) {
         for (int w = 1; w < kUpdThreads / 32; ++w) m = fmaxf(m, warp_max[w]);
         m = fmaxf(m, warp_max[0]);
-        if (m > 0.0f && m <= FLT_MAX) {
-            const float fmax = ((format_mask >> t) & 1u) ? 57344.0f : 448.0f;
-            const float q = __fdiv_rn(fmax, m);
-            const float p2 = __uint_as_float(static_cast<uint32_t>(127 - margin) << 23);
-            float sc = __fmul_rn(q, p2);
-            if (sc > FLT_MAX) sc = FLT_MAX;
+        const float fmax = ((format_mask >> t) & 1u) ? 57344.0f : 448.0f;
+        bool valid;
+        const float sc = recipe_scale(m, fmax, margin, scale[t], valid);
+        if (valid) {
             scale[t] = sc;
             scale_inv[t] = __fdiv_rn(1.0f, sc);
         }
@@ -301,22 +325,31 @@ cudaError_t launch_amax(const void *x, int64_t n, float *amax, int sm_count, cud
     return cudaGetLastError();
 }
 
+template <int FMT, bool CURRENT>
+static cudaError_t qt_launch(const CUtensorMap &tm, int64_t rows, int64_t cols, float *scale,
+                             uint8_t *out, uint8_t *out_t, unsigned *ab, int64_t tiles_c,
+                             int64_t num_tiles, const float *amax_in, float *scale_inv, int margin,
+                             int sm_count, cudaStream_t st) {
+    static std::once_flag attr_once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(attr_once, [] {
+        attr_err = cudaFuncSetAttribute(quantize_transpose_kernel<FMT, CURRENT>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        static_cast<int>(kQtSmem));
+    });
+    if (attr_err != cudaSuccess) return attr_err;
+    int64_t blocks = static_cast<int64_t>(sm_count) * 2;
+    if (blocks > num_tiles) blocks = num_tiles;
+    quantize_transpose_kernel<FMT, CURRENT><<<static_cast<unsigned>(blocks), kQtThreads, kQtSmem,
+                                               st>>>(tm, rows, cols, scale, out, out_t, ab, tiles_c,
+                                                     num_tiles, amax_in, scale_inv, margin);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_quantize_transpose(const void *x, int64_t rows, int64_t cols,
                                       const float *scale, int fmt, uint8_t *out, uint8_t *out_t,
                                       float *amax, bool zero_amax, int sm_count,
                                       cudaStream_t st) {
-    static std::once_flag attr_once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(attr_once, [] {
-        attr_err = cudaFuncSetAttribute(quantize_transpose_kernel<0>,
-                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        static_cast<int>(kQtSmem));
-        if (attr_err == cudaSuccess)
-            attr_err = cudaFuncSetAttribute(quantize_transpose_kernel<1>,
-                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                            static_cast<int>(kQtSmem));
-    });
-    if (attr_err != cudaSuccess) return attr_err;
     if (amax != nullptr && zero_amax) {
         cudaError_t e = cudaMemsetAsync(amax, 0, sizeof(float), st);
         if (e != cudaSuccess) return e;
@@ -327,16 +360,31 @@ cudaError_t launch_quantize_transpose(const void *x, int64_t rows, int64_t cols,
         return cudaErrorInvalidValue;
     const int64_t tiles_c = (cols + kQtTile - 1) / kQtTile;
     const int64_t num_tiles = ((rows + kQtTile - 1) / kQtTile) * tiles_c;
-    int64_t blocks = static_cast<int64_t>(sm_count) * 2;
-    if (blocks > num_tiles) blocks = num_tiles;
     auto *ab = reinterpret_cast<unsigned *>(amax);
+    float *sc = const_cast<float *>(scale);   // read only in this mode
     if (fmt == 0)
-        quantize_transpose_kernel<0><<<static_cast<unsigned>(blocks), kQtThreads, kQtSmem, st>>>(
-            tm, rows, cols, scale, out, out_t, ab, tiles_c, num_tiles);
-    else
-        quantize_transpose_kernel<1><<<static_cast<unsigned>(blocks), kQtThreads, kQtSmem, st>>>(
-            tm, rows, cols, scale, out, out_t, ab, tiles_c, num_tiles);
-    return cudaGetLastError();
+        return qt_launch<0, false>(tm, rows, cols, sc, out, out_t, ab, tiles_c, num_tiles, nullptr,
+                                   nullptr, 0, sm_count, st);
+    return qt_launch<1, false>(tm, rows, cols, sc, out, out_t, ab, tiles_c, num_tiles, nullptr,
+                               nullptr, 0, sm_count, st);
+}
+
+cudaError_t launch_quantize_transpose_current(const void *x, int64_t rows, int64_t cols, int fmt,
+                                              int margin, uint8_t *out, uint8_t *out_t,
+                                              float *amax, float *scale, float *scale_inv,
+                                              int sm_count, cudaStream_t st) {
+    cudaError_t e = launch_amax(x, rows * cols, amax, sm_count, st);
+    if (e != cudaSuccess || rows == 0 || cols == 0) return e;
+    CUtensorMap tm;
+    if (!encode_tmap_2d(&tm, x, true, cols, rows, kQtTile, kQtTile, false))
+        return cudaErrorInvalidValue;
+    const int64_t tiles_c = (cols + kQtTile - 1) / kQtTile;
+    const int64_t num_tiles = ((rows + kQtTile - 1) / kQtTile) * tiles_c;
+    if (fmt == 0)
+        return qt_launch<0, true>(tm, rows, cols, scale, out, out_t, nullptr, tiles_c, num_tiles,
+                                  amax, scale_inv, margin, sm_count, st);
+    return qt_launch<1, true>(tm, rows, cols, scale, out, out_t, nullptr, tiles_c, num_tiles, amax,
+                              scale_inv, margin, sm_count, st);
 }
 
 cudaError_t launch_scale_update(float *history, const float *amax, float *scale, float *scale_inv,

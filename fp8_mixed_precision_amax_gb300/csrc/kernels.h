@@ -26,6 +26,14 @@ cudaError_t launch_quantize_transpose(const void *x, int64_t rows, int64_t cols,
                                       const float *scale, int fmt, uint8_t *out, uint8_t *out_t,
                                       float *amax, bool zero_amax, int sm_count, cudaStream_t st);
 
+// Just-in-time scaling: amax of x into *amax (overwritten), then the cast
+// with scale = recipe formula of that amax (history of one), written back to
+// *scale / *scale_inv (both kept when the amax is 0 or not finite).
+cudaError_t launch_quantize_transpose_current(const void *x, int64_t rows, int64_t cols, int fmt,
+                                              int margin, uint8_t *out, uint8_t *out_t,
+                                              float *amax, float *scale, float *scale_inv,
+                                              int sm_count, cudaStream_t st);
+
 // History shift + scale / scale_inv update of num_tensors states.
 cudaError_t launch_scale_update(float *history, const float *amax, float *scale, float *scale_inv,
                                 int num_tensors, int L, uint32_t format_mask, int margin,

@@ -62,7 +62,7 @@
 extern "C" {
 #endif
 
-#define FP8AMAX_ABI_VERSION 1
+#define FP8AMAX_ABI_VERSION 2
 
 typedef enum { FP8_E4M3 = 0, FP8_E5M2 = 1 } fp8_format;
 
@@ -99,11 +99,21 @@ typedef struct {
  * recipe"): margin (>= 0, default 0; larger = fewer overflows, more
  * underflow), amax_history_len (default 1024) and the format choice.
  * hybrid = 1: E4M3 for X, W, Y and E5M2 for dY, dX (Format.HYBRID);
- * hybrid = 0: E4M3 for all five.  The scale is updated every step. */
+ * hybrid = 0: E4M3 for all five.  The scale is updated every step.
+ * scaling selects between the two per-tensor scalings the wiki note names
+ * ("per-tensor scaling is the key": delayed or just-in-time):
+ *   FP8_SCALING_DELAYED  the casts use the scales the previous step's
+ *                        fp8_amax_scale_update derived from the history;
+ *   FP8_SCALING_CURRENT  X, W and dY are cast with a scale derived from
+ *                        their own amax in the same call (the formula with
+ *                        a history of one), written to meta->scale /
+ *                        scale_inv; the history update still runs. */
+enum { FP8_SCALING_DELAYED = 0, FP8_SCALING_CURRENT = 1 };
 typedef struct {
     int32_t margin;
     int32_t history_len;
     int32_t hybrid;
+    int32_t scaling;
 } fp8_recipe;
 
 /* ABI version of the loaded library (FP8AMAX_ABI_VERSION). */
@@ -137,6 +147,21 @@ fp8_status fp8_quantize_transpose(const void *x, int64_t rows, int64_t cols, con
                                   int32_t fmt, uint8_t *out, uint8_t *out_t, float *amax,
                                   void *stream);
 
+/* Just-in-time (current) scaling of one tensor (wiki note, "per-tensor
+ * scaling is the key": the scale comes from the tensor itself): amax(x),
+ * then scale = the recipe formula applied to that amax alone, then the fused
+ * cast with that scale.  Two kernels, in stream order.
+ *   x, rows, cols, fmt, out, out_t  as fp8_quantize_transpose
+ *   margin     0 <= margin <= 64
+ *   amax       DEVICE, 1 float, overwritten with amax(x)
+ *   scale, scale_inv  DEVICE, 1 float each: replaced by the new scale and
+ *              its inverse when 0 < amax < inf, left as they are otherwise
+ *              (the cast then uses the given scale). */
+fp8_status fp8_quantize_transpose_current(const void *x, int64_t rows, int64_t cols, int32_t fmt,
+                                          int32_t margin, uint8_t *out, uint8_t *out_t,
+                                          float *amax, float *scale, float *scale_inv,
+                                          void *stream);
+
 /* Delayed-scaling update of `num_tensors` independent scaling states (the
  * recipe section's margin and amax_history_len, with the scale formula in
  * the header comment).  All DEVICE:
@@ -169,7 +194,8 @@ fp8_status fp8_gemm_tn(const uint8_t *A, int32_t fa, const uint8_t *B, int32_t f
 
 /* Forward of the FP8 linear layer Y = X W^T (te.Linear under fp8_autocast,
  * implementation guide "Basic structure of FP8 training code" and the
- * recipe section).  Uses this step's (delayed) scales of X and W.
+ * recipe section).  Uses this step's (delayed) scales of X and W, or under
+ * FP8_SCALING_CURRENT derives them from X's and W's own amax first.
  *   X   DEVICE [M][K] BF16 input;   W  DEVICE [N][K] BF16 weight
  *   X8, X8t  DEVICE [M][K] and [K][M] FP8 (E4M3), written; X8t is kept for wgrad
  *   W8, W8t  DEVICE [N][K] and [K][N] FP8 (E4M3), written; W8t is kept for dgrad
@@ -180,7 +206,8 @@ fp8_status fp8_linear_fwd(const void *X, const void *W, int64_t M, int64_t N, in
                           uint8_t *X8t, uint8_t *W8, uint8_t *W8t, void *Y, void *stream);
 
 /* Backward of the FP8 linear layer: dX = dY W (dgrad), dW = dY^T X (wgrad),
- * with dY cast to E5M2 under HYBRID (E4M3 otherwise).
+ * with dY cast to E5M2 under HYBRID (E4M3 otherwise); under
+ * FP8_SCALING_CURRENT dY's scale is derived from its own amax first.
  *   dY  DEVICE [M][N] BF16 output gradient
  *   X8t, W8t  DEVICE, the transposed copies written by fp8_linear_fwd
  *   dY8, dY8t DEVICE [M][N] and [N][M] FP8 work buffers, written

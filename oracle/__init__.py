@@ -19,6 +19,9 @@ What each function follows:
 * ``history_update`` -- DelayedScaling's margin / amax_history_len
   (implementation guide, section "Dynamic scaling and the FP8 recipe") with
   the scale formula (fmax / max(history)) / 2^margin.
+* ``just_in_time_scale`` -- just-in-time per-tensor scaling (wiki note,
+  bullet "per-tensor scaling is the key"): the same formula on this step's
+  amax alone.
 * ``layer_fwd`` / ``layer_bwd`` -- te.Linear inside fp8_autocast with
   Format.HYBRID (E4M3 forward, E5M2 backward; same section) and FP8 GEMMs with
   higher-precision accumulation (wiki note, bullet "extension to FP8").
@@ -216,10 +219,16 @@ def epilogue(acc: np.ndarray, sa_inv, sb_inv) -> np.ndarray:
 @dataclass
 class Recipe:
     """DelayedScaling: margin (default 0), amax_history_len (default 1024),
-    HYBRID (E4M3 forward, E5M2 backward) or E4M3 everywhere."""
+    HYBRID (E4M3 forward, E5M2 backward) or E4M3 everywhere.
+
+    ``current`` selects just-in-time scaling for X, W and dY (the wiki note's
+    bullet "per-tensor scaling is the key" names it beside delayed scaling):
+    the scale of a tensor comes from its own amax in the same step, through
+    the same formula applied to a history of one entry."""
     margin: int = 0
     history_len: int = 1024
     hybrid: bool = True
+    current: bool = False
 
     def formats(self):
         bwd = E5M2 if self.hybrid else E4M3
@@ -243,12 +252,23 @@ class State:
                      self.scale_inv.copy())
 
 
+def just_in_time_scale(st: State, rc: Recipe, slot: int, fmt: int) -> None:
+    """Just-in-time scaling of one slot: its scale and inverse from this
+    step's amax alone (a history of one), kept when that amax is 0 or inf."""
+    _, s, si = history_update(np.zeros(1, np.float32), st.amax[slot], st.scale[slot],
+                              st.scale_inv[slot], fmt, rc.margin)
+    st.scale[slot], st.scale_inv[slot] = s, si
+
+
 def layer_fwd(st: State, rc: Recipe, X: np.ndarray, W: np.ndarray, rows=None):
     """Forward of the FP8 linear: Y = X W^T.  ``rows`` (start, count) limits the
     GEMM to a block of Y's rows; the casts always cover the whole tensors."""
     f = rc.formats()
     st.amax[SLOT_X] = amax(X)
     st.amax[SLOT_W] = amax(W)
+    if rc.current:
+        just_in_time_scale(st, rc, SLOT_X, f[SLOT_X])
+        just_in_time_scale(st, rc, SLOT_W, f[SLOT_W])
     X8, X8t = quantize(X, st.scale[SLOT_X], f[SLOT_X])
     W8, W8t = quantize(W, st.scale[SLOT_W], f[SLOT_W])
     r0, nr = rows if rows is not None else (0, X.shape[0])
@@ -266,6 +286,8 @@ def layer_bwd(st: State, rc: Recipe, dY: np.ndarray, X8t: np.ndarray, W8t: np.nd
     of dW's rows; the cast always covers the whole of dY."""
     f = rc.formats()
     st.amax[SLOT_DY] = amax(dY)
+    if rc.current:
+        just_in_time_scale(st, rc, SLOT_DY, f[SLOT_DY])
     dY8, dY8t = quantize(dY, st.scale[SLOT_DY], f[SLOT_DY])
     r0, nr = rows if rows is not None else (0, dY.shape[0])
     acc_dx = gemm_tn(dY8, f[SLOT_DY], W8t, f[SLOT_W], r0, nr)

@@ -17,7 +17,7 @@ def test_every_declared_function_is_exported():
     assert len(declared) >= 10
     for name in declared:
         assert hasattr(lib, name), name
-    assert lib.fp8_abi_version() == 1
+    assert lib.fp8_abi_version() == 2
 
 
 def test_header_structs_match_binding():
@@ -61,13 +61,19 @@ def test_host_side_argument_checks():
     s, _ = _err(lib.fp8_scale_update(p16, p16, p16, p16, 5, 9000, 0, 0, None))
     assert s == ERR_ARG
     meta = api.fp8_meta(0x1000, 0x1000, 0x1000, 0x1000, 16)
-    bad = api.fp8_recipe(0, 32, 1)            # history length mismatch
+    bad = api.fp8_recipe(0, 32, 1, 0)            # history length mismatch
     s, msg = _err(lib.fp8_amax_scale_update(ctypes.byref(meta), ctypes.byref(bad), None))
     assert s == ERR_ARG and "history_len" in msg
-    neg = api.fp8_recipe(-1, 16, 1)
+    sc = api.fp8_recipe(0, 16, 1, 2)            # neither delayed nor current
+    s, msg = _err(lib.fp8_amax_scale_update(ctypes.byref(meta), ctypes.byref(sc), None))
+    assert s == ERR_ARG and "scaling" in msg
+    s, _ = _err(lib.fp8_quantize_transpose_current(p16, 16, 16, 0, 65, p16, None, p16, p16, p16,
+                                                   None))
+    assert s == ERR_ARG
+    neg = api.fp8_recipe(-1, 16, 1, 0)
     s, _ = _err(lib.fp8_amax_scale_update(ctypes.byref(meta), ctypes.byref(neg), None))
     assert s == ERR_ARG
-    ok = api.fp8_recipe(0, 16, 1)
+    ok = api.fp8_recipe(0, 16, 1, 0)
     s, _ = _err(lib.fp8_linear_fwd(p16, p16, 16, 16, 24, ctypes.byref(meta), ctypes.byref(ok),
                                    p16, p16, p16, p16, p16, None))
     assert s == ERR_ALIGN

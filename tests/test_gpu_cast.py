@@ -157,3 +157,34 @@ def test_cast_sweep_amax_scale_cast(n):
         top = 0x7E if fmt == o.E4M3 else 0x7B
         assert int((host_u8(out[: min(rows, 4096)]) & 0x7F).max()) <= top
         del out, out_t
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("margin", [0, 2])
+def test_just_in_time_cast(fmt, margin):
+    """amax, then the scale from that amax alone, then the cast, in one call:
+    bit-exact amax, scale, scale_inv and FP8 bytes; an all-zero tensor keeps
+    the previous scale."""
+    f = _lib()
+    for i, (shape, mag) in enumerate([((128, 128), 1.0), ((144, 272), 3e4), ((1040, 1168), 1e-5),
+                                      ((256, 4112), 0.0)]):
+        g = torch.Generator().manual_seed(77 + i)
+        x = (torch.randn(shape, generator=g) * mag).to(torch.bfloat16).cuda()
+        rows, cols = shape
+        out = torch.empty((rows, cols), dtype=torch.uint8, device="cuda")
+        out_t = torch.empty((cols, rows), dtype=torch.uint8, device="cuda")
+        am = torch.full((1,), -1.0, device="cuda")
+        sc = torch.full((1,), 3.0, device="cuda")
+        si = torch.full((1,), 1 / 3.0, device="cuda")
+        f.fp8_quantize_transpose_current(x, fmt, margin, am, sc, si, out, out_t)
+        torch.cuda.synchronize()
+        xb = host_bf16_bits(x)
+        ra = o.amax(xb)
+        _, rs, rsi = o.history_update(np.zeros(1, np.float32), ra, np.float32(3.0),
+                                      np.float32(1 / 3.0), fmt, margin)
+        assert f32_bits(am.cpu().numpy()[0]) == f32_bits(ra)
+        assert f32_bits(sc.cpu().numpy()[0]) == f32_bits(rs)
+        assert f32_bits(si.cpu().numpy()[0]) == f32_bits(rsi)
+        q, qt = o.quantize(xb, rs, fmt)
+        assert_fp8_equal(host_u8(out), q, fmt, f"{shape}")
+        assert_fp8_equal(host_u8(out_t), qt, fmt, f"{shape} t")

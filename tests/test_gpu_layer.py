@@ -51,13 +51,14 @@ def _gpu_slot_checks(lin, f, gpu_amax_hist, fmts, margin):
             assert f32_bits(scale[slot]) == f32_bits(expect)
 
 
-def run_layer(w: wl.Workload, steps, check_every=1, full=True, hybrid=None, extra_checks=()):
+def run_layer(w: wl.Workload, steps, check_every=1, full=True, hybrid=None, extra_checks=(),
+              current=False):
     f = _lib()
     hybrid = w.hybrid if hybrid is None else hybrid
     W = wl.layer_weight(w, "cuda")
-    rc_gpu = f.Recipe(margin=w.margin, history_len=w.history_len, hybrid=hybrid)
+    rc_gpu = f.Recipe(margin=w.margin, history_len=w.history_len, hybrid=hybrid, current=current)
     lin = f.Fp8Linear(W, w.M, rc_gpu)
-    rc = o.Recipe(margin=w.margin, history_len=w.history_len, hybrid=hybrid)
+    rc = o.Recipe(margin=w.margin, history_len=w.history_len, hybrid=hybrid, current=current)
     st = o.State.initial(w.history_len)
     fm = rc.formats()
     Wb = host_bf16_bits(W)
@@ -72,11 +73,16 @@ def run_layer(w: wl.Workload, steps, check_every=1, full=True, hybrid=None, extr
         g_amax = lin.meta.amax.cpu().numpy().copy()
         check = (step % check_every == 0) or step in extra_checks or step == steps - 1
         Xb, dYb = host_bf16_bits(X), host_bf16_bits(dY)
+        g_scale = lin.meta.scale.cpu().numpy().copy()
+        g_scale_inv = lin.meta.scale_inv.cpu().numpy().copy()
         if check:
             # forward / backward in the oracle
             st.amax[o.SLOT_X] = o.amax(Xb)
             st.amax[o.SLOT_W] = o.amax(Wb)
             st.amax[o.SLOT_DY] = o.amax(dYb)
+            if current:
+                for slot in (o.SLOT_X, o.SLOT_W, o.SLOT_DY):
+                    o.just_in_time_scale(st, rc, slot, fm[slot])
             X8, X8t = o.quantize(Xb, st.scale[o.SLOT_X], fm[o.SLOT_X])
             W8, W8t = o.quantize(Wb, st.scale[o.SLOT_W], fm[o.SLOT_W])
             dY8, dY8t = o.quantize(dYb, st.scale[o.SLOT_DY], fm[o.SLOT_DY])
@@ -103,8 +109,14 @@ def run_layer(w: wl.Workload, steps, check_every=1, full=True, hybrid=None, extr
             st.amax[o.SLOT_X] = o.amax(Xb)
             st.amax[o.SLOT_W] = o.amax(Wb)
             st.amax[o.SLOT_DY] = o.amax(dYb)
+            if current:
+                for slot in (o.SLOT_X, o.SLOT_W, o.SLOT_DY):
+                    o.just_in_time_scale(st, rc, slot, fm[slot])
         for slot in (o.SLOT_X, o.SLOT_W, o.SLOT_DY):
             assert f32_bits(g_amax[slot]) == f32_bits(st.amax[slot]), (step, slot)
+            # the scales the casts of this step used
+            assert f32_bits(g_scale[slot]) == f32_bits(st.scale[slot]), (step, slot)
+            assert f32_bits(g_scale_inv[slot]) == f32_bits(st.scale_inv[slot]), (step, slot)
         # the delayed-scaling update
         lin.update()
         torch.cuda.synchronize()
@@ -161,3 +173,17 @@ def test_ragged_layer_shape():
     """A layer whose M, N, K are not multiples of the GEMM tiles."""
     w = wl.Workload("ragged", 144, 272, 400, "normal", 1.0, 0.05, 0.01, 16, 0, True, 3)
     run_layer(w, 3, full=True)
+
+
+def test_just_in_time_scaling_tiny_and_drift():
+    """Just-in-time scaling: X, W and dY are cast with scales from their own
+    amax in the same step (including the all-zero and x1000 steps)."""
+    run_layer(wl.WORKLOADS["tiny"], 4, full=True, current=True)
+    small = wl.Workload("drift_small", 128, 256, 256, "drift", 1.0, 1 / 16, 1.0, 512, 0, True,
+                        120)
+    run_layer(small, 120, check_every=10, full=True, current=True,
+              extra_checks=(49, 50, 51, 75, 76))
+
+
+def test_just_in_time_scaling_mlp7b_full_size():
+    run_layer(wl.WORKLOADS["mlp7b"], 2, full=False, current=True)

@@ -202,3 +202,47 @@ def test_state_save_restore_gives_identical_next_scales():
     assert np.array_equal(full.history.view(np.uint32), resumed.history.view(np.uint32))
     assert np.array_equal(full.scale.view(np.uint32), resumed.scale.view(np.uint32))
     assert np.array_equal(full.scale_inv.view(np.uint32), resumed.scale_inv.view(np.uint32))
+
+
+# -------------------------------------------------- just-in-time scaling --
+
+def test_just_in_time_scaling_uses_this_steps_amax():
+    """Under just-in-time scaling (margin 0) the scale is fmax / amax of the
+    tensor being cast, so its largest element lands on the largest code at
+    every step, including the first; an all-zero tensor keeps the scale."""
+    rng = np.random.default_rng(8)
+    rc = o.Recipe(margin=0, history_len=4, hybrid=True, current=True)
+    st = o.State.initial(4)
+    W = bf16_bits(rng.standard_normal((16, 32)) / 4)
+    for step, mag in enumerate([1.0, 300.0, 1e-3, 0.0, 7.0]):
+        X = bf16_bits(rng.standard_normal((16, 32)) * mag)
+        dY = bf16_bits(rng.standard_normal((16, 16)) * mag * 1e-2)
+        prev_x = st.scale[o.SLOT_X]
+        fo = o.layer_fwd(st, rc, X, W)
+        bo = o.layer_bwd(st, rc, dY, fo["X8t"], fo["W8t"])
+        if mag == 0.0:
+            assert st.scale[o.SLOT_X] == prev_x and np.all((fo["X8"] & 0x7F) == 0)
+        else:
+            assert st.scale[o.SLOT_X] == np.float32(448.0) / o.amax(X)
+            assert (fo["X8"] & 0x7F).max() == 0x7E
+            assert (bo["dY8"] & 0x7F).max() == 0x7B
+            assert st.scale_inv[o.SLOT_DY] == np.float32(1.0) / st.scale[o.SLOT_DY]
+        assert (fo["W8"] & 0x7F).max() == 0x7E
+        o.layer_update(st, rc)
+
+
+def test_just_in_time_differs_from_delayed_only_by_the_scale_source():
+    """The same step under the two recipes: delayed scaling casts with the
+    scale left by the previous update, just-in-time with fmax / amax now."""
+    rng = np.random.default_rng(9)
+    X = bf16_bits(rng.standard_normal((16, 32)) * 50)
+    W = bf16_bits(rng.standard_normal((16, 32)))
+    d = o.State.initial(4)
+    c = o.State.initial(4)
+    fd = o.layer_fwd(d, o.Recipe(history_len=4), X, W)
+    fc = o.layer_fwd(c, o.Recipe(history_len=4, current=True), X, W)
+    assert d.scale[o.SLOT_X] == 1.0
+    q, _ = o.quantize(X, np.float32(1.0), o.E4M3)
+    assert np.array_equal(fd["X8"], q)
+    q, _ = o.quantize(X, np.float32(448.0) / o.amax(X), o.E4M3)
+    assert np.array_equal(fc["X8"], q)

@@ -23,7 +23,7 @@ def test_noalloc_rejects_sizes_beyond_its_array():
     lib = api.library()
     p16 = ctypes.c_void_p(0x1000)
     meta = api.fp8_meta(0x1000, 0x1000, 0x1000, 0x1000, 16)
-    rec = api.fp8_recipe(0, 16, 1)
+    rec = api.fp8_recipe(0, 16, 1, 0)
     s = lib.fp8_linear_bwd_noalloc(p16, 8192, 8192, 16, ctypes.byref(meta), ctypes.byref(rec),
                                    p16, p16, p16, p16, None)
     assert s == 1
