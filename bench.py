@@ -221,22 +221,40 @@ def run_layer_bench(f, w: wl.Workload, args, world, pk, peak_kind):
     torch.cuda.synchronize()
     f.fp8_sync_status()
 
+    def timed(run_step):
+        barrier(world)
+        torch.cuda.synchronize()
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for i in range(args.steps):
+            run_step(i)
+        t1.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        return max_over_ranks(t0.elapsed_time(t1), world)
+
     clocks = ClockSampler()
     clocks.start()
     time.sleep(0.25)
-    barrier(world)
-    torch.cuda.synchronize()
-    t0 = torch.cuda.Event(enable_timing=True)
-    t1 = torch.cuda.Event(enable_timing=True)
-    t0.record(stream)
-    for i in range(args.steps):
-        step(i)
-    t1.record(stream)
-    torch.cuda.synchronize()
-    barrier(world)
-    ms = max_over_ranks(t0.elapsed_time(t1), world)
+    ms_eager = timed(step)
+    graphs = None
+    if world == 1:
+        # the same step recorded once per input batch and replayed
+        graphs = [lin.capture_step(xs[k], dys[k]) for k in (0, 1)]
+        for i in range(3):
+            graphs[i % 2].replay()
+        torch.cuda.synchronize()
+        ms_graph = timed(lambda i: graphs[i % 2].replay())
+        ms = min(ms_eager, ms_graph)
+    else:
+        ms_graph, ms = None, ms_eager
 
-    # per-kernel breakdown: the same step issued as its individual C-ABI calls
+    # per-kernel breakdown: the same step issued as its individual kernel
+    # launches through the C ABI (the grouped X+W cast, fprop, the dY cast,
+    # the grouped dgrad+wgrad GEMM, the update), each between CUDA events.
+    # Casts are timed without their amax pointers, so that the events hold
+    # the kernel alone and not the one-word memset that clears an amax.
     tm = EventTimer()
     m = lin.meta
     fg = f.E5M2 if w.hybrid else f.E4M3
@@ -244,18 +262,16 @@ def run_layer_bench(f, w: wl.Workload, args, world, pk, peak_kind):
     nb = max(10, min(args.steps, 100))
     for i in range(nb):
         X, dY = xs[i % 2], dys[i % 2]
-        # casts are timed without their amax pointer, so that the events hold
-        # the kernel alone and not the one-word memset that clears the amax
-        tm.time("cast_X", lambda: f.fp8_quantize_transpose(X, m.scale[0:1], E4, lin.X8, lin.X8t))
-        tm.time("cast_W", lambda: f.fp8_quantize_transpose(W, m.scale[1:2], E4, lin.W8, lin.W8t))
+        tm.time("cast_XW", lambda: f.fp8_quantize_transpose_grouped(
+            [(X, m.scale[0:1], lin.X8, lin.X8t, None), (W, m.scale[1:2], lin.W8, lin.W8t, None)],
+            E4))
         tm.time("gemm_fprop", lambda: f.fp8_gemm_tn(lin.X8, E4, lin.W8, E4, m.scale_inv[0:1],
                                                     m.scale_inv[1:2], lin.Y, m.amax[2:3]))
         tm.time("cast_dY", lambda: f.fp8_quantize_transpose(dY, m.scale[3:4], fg, lin.dY8,
                                                             lin.dY8t))
-        tm.time("gemm_dgrad", lambda: f.fp8_gemm_tn(lin.dY8, fg, lin.W8t, E4, m.scale_inv[3:4],
-                                                    m.scale_inv[1:2], lin.dX, m.amax[4:5]))
-        tm.time("gemm_wgrad", lambda: f.fp8_gemm_tn(lin.dY8t, fg, lin.X8t, E4, m.scale_inv[3:4],
-                                                    m.scale_inv[0:1], lin.dW))
+        tm.time("gemm_bwd", lambda: f.fp8_gemm_tn_grouped(
+            [(lin.dY8, fg, lin.W8t, E4, m.scale_inv[3:4], m.scale_inv[1:2], lin.dX, m.amax[4:5]),
+             (lin.dY8t, fg, lin.X8t, E4, m.scale_inv[3:4], m.scale_inv[0:1], lin.dW, None)]))
         tm.time("update", lambda: lin.update())
     torch.cuda.synchronize()
     clk = clocks.stop()
@@ -264,24 +280,29 @@ def run_layer_bench(f, w: wl.Workload, args, world, pk, peak_kind):
     M, N, K = w.M, w.N, w.K
     flops = 6 * M * N * K
     value = world * args.steps * flops / (ms / 1e3) / 1e12
-    gemm_ms = {k: tm.mean_ms(k) for k in ("gemm_fprop", "gemm_dgrad", "gemm_wgrad")}
-    cast_ms = {k: tm.mean_ms(k) for k in ("cast_X", "cast_W", "cast_dY")}
+    gemm_ms = {k: tm.mean_ms(k) for k in ("gemm_fprop", "gemm_bwd")}
+    gemm_flops = {"gemm_fprop": 2 * M * N * K, "gemm_bwd": 4 * M * N * K}
+    cast_ms = {k: tm.mean_ms(k) for k in ("cast_XW", "cast_dY")}
     upd_ms = tm.mean_ms("update")
-    gemm_avg = statistics.mean(gemm_ms.values())
     fp8_peak = pk["bf16_tflops"] * FP8_OVER_BF16
-    achieved = 2 * M * N * K / (gemm_avg / 1e3) / 1e12
-    cast_bytes = {"cast_X": 4 * M * K, "cast_W": 4 * N * K, "cast_dY": 4 * M * N}
+    # algorithmic flops of the GEMM launches over their summed durations
+    achieved = sum(gemm_flops.values()) / (sum(gemm_ms.values()) / 1e3) / 1e12
+    cast_bytes = {"cast_XW": 4 * M * K + 4 * N * K, "cast_dY": 4 * M * N}
     cast_gbs = sum(cast_bytes.values()) / (sum(cast_ms.values()) / 1e3) / 1e9
     traffic = gemm_traffic(w.name)
     res = {
         "value": value, "ms_per_step": ms / args.steps,
+        "launch": "CUDA graph replay" if graphs and ms == ms_graph else "eager",
+        "ms_per_step_eager": ms_eager / args.steps,
+        "ms_per_step_graph": ms_graph / args.steps if ms_graph else None,
         "roofline": {"bound": "tensor", "kernel": "gemm_tn_kernel", "achieved": achieved,
                      "peak": fp8_peak, "unit": "TFLOP/s", "frac": achieved / fp8_peak,
                      "traffic": traffic,
                      "peak_basis": f"{peak_kind} bf16 burst {pk['bf16_tflops']} x {FP8_OVER_BF16}",
-                     "per_gemm_ms": gemm_ms,
-                     "per_gemm_tflops": {k: 2 * M * N * K / (v / 1e3) / 1e12
-                                         for k, v in gemm_ms.items()}},
+                     "launches_per_step": {"gemm_fprop": "fprop", "gemm_bwd": "dgrad+wgrad"},
+                     "per_launch_ms": gemm_ms,
+                     "per_launch_tflops": {k: gemm_flops[k] / (v / 1e3) / 1e12
+                                           for k, v in gemm_ms.items()}},
         "cast_roofline": {"bound": "hbm", "kernel": "quantize_transpose_kernel",
                           "achieved": cast_gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
                           "frac": cast_gbs / pk["hbm_gbs"],
@@ -290,7 +311,7 @@ def run_layer_bench(f, w: wl.Workload, args, world, pk, peak_kind):
                                            for k, v in cast_ms.items()},
                           "update_us": upd_ms * 1e3},
         "clocks": clk,
-        "gpu_launches": 7 * args.steps,
+        "gpu_launches": 5 * args.steps,
         "breakdown_ms": {**gemm_ms, **cast_ms, "update": upd_ms},
     }
 
@@ -504,6 +525,8 @@ def main():
         "data": "synthetic (seeded fp8_workloads, resident in HBM)",
         "config": {**workload_config(w), "parallelism": f"dp{world} replicas"
                    + (" + amax MAX all-reduce" if world > 1 else "")},
+        "launch": r["launch"], "ms_per_step_eager": r["ms_per_step_eager"],
+        "ms_per_step_graph": r["ms_per_step_graph"],
         "roofline": r["roofline"], "cast_roofline": r["cast_roofline"], "clocks": r["clocks"],
         "gpu_launches": r["gpu_launches"], "breakdown_ms": r["breakdown_ms"],
         "peaks_source": peak_kind,

@@ -47,6 +47,19 @@ class fp8_recipe(ctypes.Structure):
 SCALING_DELAYED, SCALING_CURRENT = 0, 1
 
 
+class fp8_gemm_desc(ctypes.Structure):
+    _fields_ = [("A", ctypes.c_void_p), ("fa", ctypes.c_int32), ("B", ctypes.c_void_p),
+                ("fb", ctypes.c_int32), ("M", ctypes.c_int64), ("N", ctypes.c_int64),
+                ("K", ctypes.c_int64), ("a_scale_inv", ctypes.c_void_p),
+                ("b_scale_inv", ctypes.c_void_p), ("D", ctypes.c_void_p), ("d_amax", ctypes.c_void_p)]
+
+
+class fp8_cast_desc(ctypes.Structure):
+    _fields_ = [("x", ctypes.c_void_p), ("rows", ctypes.c_int64), ("cols", ctypes.c_int64),
+                ("scale", ctypes.c_void_p), ("out", ctypes.c_void_p), ("out_t", ctypes.c_void_p),
+                ("amax", ctypes.c_void_p)]
+
+
 def _load() -> ctypes.CDLL:
     if not os.path.exists(LIB_PATH):
         raise ImportError(f"{LIB_PATH} is not built; call fp8_mixed_precision_amax_gb300.build.build()")
@@ -64,6 +77,9 @@ def _load() -> ctypes.CDLL:
         "fp8_amax_scale_update": ([ctypes.POINTER(fp8_meta), ctypes.POINTER(fp8_recipe), vp],
                                   ctypes.c_int),
         "fp8_gemm_tn": ([vp, i32, vp, i32, i64, i64, i64, vp, vp, vp, vp, vp], ctypes.c_int),
+        "fp8_gemm_tn_grouped": ([ctypes.POINTER(fp8_gemm_desc), i32, vp], ctypes.c_int),
+        "fp8_quantize_transpose_grouped": ([ctypes.POINTER(fp8_cast_desc), i32, i32, vp],
+                                           ctypes.c_int),
         "fp8_linear_fwd": ([vp, vp, i64, i64, i64, ctypes.POINTER(fp8_meta),
                             ctypes.POINTER(fp8_recipe), vp, vp, vp, vp, vp, vp], ctypes.c_int),
         "fp8_linear_bwd": ([vp, i64, i64, i64, ctypes.POINTER(fp8_meta),
@@ -193,6 +209,43 @@ def fp8_gemm_tn(A: torch.Tensor, fa: int, B: torch.Tensor, fb: int, a_scale_inv:
                             _ptr(b_scale_inv, torch.float32, "b_scale_inv"),
                             _ptr(D, torch.bfloat16, "D"), _ptr(d_amax, torch.float32, "d_amax"),
                             _stream(stream)))
+
+
+def _val(p):
+    return None if p is None else p.value
+
+
+def fp8_gemm_tn_grouped(problems, stream=None) -> None:
+    """One or two GEMMs in one launch; ``problems`` = list of tuples
+    (A, fa, B, fb, a_scale_inv, b_scale_inv, D, d_amax-or-None)."""
+    if not 1 <= len(problems) <= 2:
+        raise ValueError("one or two problems")
+    arr = (fp8_gemm_desc * len(problems))()
+    for i, (A, fa, B, fb, sa, sb, D, am) in enumerate(problems):
+        M, K = A.shape
+        N, K2 = B.shape
+        if K != K2 or tuple(D.shape) != (M, N):
+            raise ValueError("shapes: A [M,K], B [N,K], D [M,N]")
+        arr[i] = fp8_gemm_desc(_val(_p8(A, "A")), fa, _val(_p8(B, "B")), fb, M, N, K,
+                               _val(_ptr(sa, torch.float32, "a_scale_inv")),
+                               _val(_ptr(sb, torch.float32, "b_scale_inv")),
+                               _val(_ptr(D, torch.bfloat16, "D")),
+                               _val(_ptr(am, torch.float32, "d_amax")))
+    _check(_lib.fp8_gemm_tn_grouped(arr, len(problems), _stream(stream)))
+
+
+def fp8_quantize_transpose_grouped(tensors, fmt: int, stream=None) -> None:
+    """One or two casts of one format in one launch; ``tensors`` = list of
+    tuples (x, scale, out-or-None, out_t-or-None, amax-or-None)."""
+    if not 1 <= len(tensors) <= 2:
+        raise ValueError("one or two tensors")
+    arr = (fp8_cast_desc * len(tensors))()
+    for i, (x, scale, out, out_t, am) in enumerate(tensors):
+        rows, cols = x.shape
+        arr[i] = fp8_cast_desc(_val(_ptr(x, torch.bfloat16, "x")), rows, cols,
+                               _val(_ptr(scale, torch.float32, "scale")), _val(_p8(out, "out")),
+                               _val(_p8(out_t, "out_t")), _val(_ptr(am, torch.float32, "amax")))
+    _check(_lib.fp8_quantize_transpose_grouped(arr, len(tensors), fmt, _stream(stream)))
 
 
 # ------------------------------------------------------------------ layer --
@@ -332,6 +385,23 @@ class Fp8Linear:
 
     def update(self, stream=None) -> None:
         fp8_amax_scale_update(self.meta, self.recipe, stream)
+
+    def capture_step(self, X: torch.Tensor, dY: torch.Tensor, outs=None) -> "torch.cuda.CUDAGraph":
+        """Record one whole step on these input (and output) buffers as a CUDA
+        graph; ``graph.replay()`` then re-runs forward, backward and the
+        update with one launch.  Every scale lives on the device, so replays
+        follow the recipe exactly as eager steps do.  The step is run once
+        eagerly first (kernel attributes and tensor maps are set up outside
+        the capture) -- that warm-up step advances the scaling state."""
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            self.step(X, dY, outs=outs)
+        torch.cuda.current_stream().wait_stream(side)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            self.step(X, dY, outs=outs)
+        return g
 
     def step(self, X: torch.Tensor, dY: torch.Tensor, stream=None, outs=None):
         """Forward, backward and the recipe's update; ``outs`` = (Y, dX, dW)

@@ -264,6 +264,67 @@ fp8_status fp8_gemm_tn(const uint8_t *A, int32_t fa, const uint8_t *B, int32_t f
                         static_cast<cudaStream_t>(stream));
 }
 
+static fp8_status check_gemm(const char *fn, const fp8_gemm_desc &d) {
+    FP8_TRY(check_dims16(fn, d.M, "M", d.N, "N"));
+    FP8_TRY(check_dims16(fn, d.K, "K", 16, "-"));
+    if (d.M < 16 || d.N < 16 || d.K < 16) return fail(FP8_ERR_ARG, "%s: M, N, K must be >= 16", fn);
+    if ((d.fa != FP8_E4M3 && d.fa != FP8_E5M2) || (d.fb != FP8_E4M3 && d.fb != FP8_E5M2))
+        return fail(FP8_ERR_ARG, "%s: bad operand format", fn);
+    FP8_TRY(check_ptr(fn, d.A, "A", false));
+    FP8_TRY(check_ptr(fn, d.B, "B", false));
+    FP8_TRY(check_ptr(fn, d.D, "D", false));
+    FP8_TRY(check_scalar(fn, d.a_scale_inv, "a_scale_inv", false));
+    FP8_TRY(check_scalar(fn, d.b_scale_inv, "b_scale_inv", false));
+    FP8_TRY(check_scalar(fn, d.d_amax, "d_amax", true));
+    return FP8_OK;
+}
+
+fp8_status fp8_gemm_tn_grouped(const fp8_gemm_desc *descs, int32_t n, void *stream) {
+    const char *fn = "fp8_gemm_tn_grouped";
+    if (descs == nullptr || n < 1 || n > 2) return fail(FP8_ERR_ARG, "%s: n must be 1 or 2", fn);
+    fp8k::GemmSpec g[2];
+    for (int i = 0; i < n; ++i) {
+        FP8_TRY(check_gemm(fn, descs[i]));
+        const fp8_gemm_desc &d = descs[i];
+        g[i] = fp8k::GemmSpec{d.A, d.fa, d.B, d.fb, d.M, d.N, d.K, d.a_scale_inv, d.b_scale_inv,
+                              d.D, d.d_amax, true};
+    }
+    int sms;
+    FP8_TRY(current_device(&sms));
+    const char *what = nullptr;
+    cudaError_t e = fp8k::launch_gemm_group(g, n, sms, static_cast<cudaStream_t>(stream), &what);
+    if (e != cudaSuccess)
+        return what ? fail(FP8_ERR_CUDA, "%s: %s", fn, what) : cuda_fail(e, fn);
+    return FP8_OK;
+}
+
+fp8_status fp8_quantize_transpose_grouped(const fp8_cast_desc *descs, int32_t n, int32_t fmt,
+                                          void *stream) {
+    const char *fn = "fp8_quantize_transpose_grouped";
+    if (descs == nullptr || n < 1 || n > 2) return fail(FP8_ERR_ARG, "%s: n must be 1 or 2", fn);
+    if (fmt != FP8_E4M3 && fmt != FP8_E5M2) return fail(FP8_ERR_ARG, "%s: bad format %d", fn, fmt);
+    fp8k::CastSpec c[2];
+    for (int i = 0; i < n; ++i) {
+        const fp8_cast_desc &d = descs[i];
+        FP8_TRY(check_dims16(fn, d.rows, "rows", d.cols, "cols"));
+        const bool empty = d.rows == 0 || d.cols == 0;
+        if (!empty && d.out == nullptr && d.out_t == nullptr)
+            return fail(FP8_ERR_ARG, "%s: out and out_t are both NULL", fn);
+        FP8_TRY(check_ptr(fn, d.x, "x", empty));
+        FP8_TRY(check_scalar(fn, d.scale, "scale", false));
+        FP8_TRY(check_ptr(fn, d.out, "out", true));
+        FP8_TRY(check_ptr(fn, d.out_t, "out_t", true));
+        FP8_TRY(check_scalar(fn, d.amax, "amax", true));
+        c[i] = fp8k::CastSpec{d.x, d.rows, d.cols, const_cast<float *>(d.scale), nullptr, d.out,
+                              d.out_t, d.amax, true};
+    }
+    int sms;
+    FP8_TRY(current_device(&sms));
+    FP8_CUDA(fp8k::launch_cast_group(c, n, fmt, false, 0, sms, static_cast<cudaStream_t>(stream)),
+             fn);
+    return FP8_OK;
+}
+
 fp8_status fp8_linear_fwd(const void *X, const void *W, int64_t M, int64_t N, int64_t K,
                           const fp8_meta *meta, const fp8_recipe *recipe, uint8_t *X8,
                           uint8_t *X8t, uint8_t *W8, uint8_t *W8t, void *Y, void *stream) {
@@ -285,23 +346,15 @@ fp8_status fp8_linear_fwd(const void *X, const void *W, int64_t M, int64_t N, in
     float *am = meta->amax;
     // amax of X, W and Y are max-combined into slots cleared here.
     FP8_CUDA(cudaMemsetAsync(am + FP8_SLOT_X, 0, 3 * sizeof(float), st), fn);
-    if (recipe->scaling == FP8_SCALING_CURRENT) {
-        FP8_CUDA(fp8k::launch_quantize_transpose_current(
-                     X, M, K, FP8_E4M3, recipe->margin, X8, X8t, am + FP8_SLOT_X,
-                     meta->scale + FP8_SLOT_X, meta->scale_inv + FP8_SLOT_X, sms, st),
-                 fn);
-        FP8_CUDA(fp8k::launch_quantize_transpose_current(
-                     W, N, K, FP8_E4M3, recipe->margin, W8, W8t, am + FP8_SLOT_W,
-                     meta->scale + FP8_SLOT_W, meta->scale_inv + FP8_SLOT_W, sms, st),
-                 fn);
-    } else {
-        FP8_CUDA(fp8k::launch_quantize_transpose(X, M, K, meta->scale + FP8_SLOT_X, FP8_E4M3, X8,
-                                                 X8t, am + FP8_SLOT_X, false, sms, st),
-                 fn);
-        FP8_CUDA(fp8k::launch_quantize_transpose(W, N, K, meta->scale + FP8_SLOT_W, FP8_E4M3, W8,
-                                                 W8t, am + FP8_SLOT_W, false, sms, st),
-                 fn);
-    }
+    // X and W (both E4M3) in one cast launch
+    const fp8k::CastSpec c[2] = {
+        {X, M, K, meta->scale + FP8_SLOT_X, meta->scale_inv + FP8_SLOT_X, X8, X8t,
+         am + FP8_SLOT_X, false},
+        {W, N, K, meta->scale + FP8_SLOT_W, meta->scale_inv + FP8_SLOT_W, W8, W8t,
+         am + FP8_SLOT_W, false}};
+    FP8_CUDA(fp8k::launch_cast_group(c, 2, FP8_E4M3, recipe->scaling == FP8_SCALING_CURRENT,
+                                     recipe->margin, sms, st),
+             fn);
     return gemm_checked(fn, X8, FP8_E4M3, W8, FP8_E4M3, M, N, K, meta->scale_inv + FP8_SLOT_X,
                         meta->scale_inv + FP8_SLOT_W, Y, am + FP8_SLOT_Y, false, sms, st);
 }
@@ -336,12 +389,19 @@ fp8_status fp8_linear_bwd(const void *dY, int64_t M, int64_t N, int64_t K, const
         FP8_CUDA(fp8k::launch_quantize_transpose(dY, M, N, meta->scale + FP8_SLOT_DY, fg, dY8,
                                                  dY8t, am + FP8_SLOT_DY, false, sms, st),
                  fn);
-    // dgrad: dX[M][K] = dY8[M][N] . W8t[K][N]^T
-    FP8_TRY(gemm_checked(fn, dY8, fg, W8t, FP8_E4M3, M, K, N, meta->scale_inv + FP8_SLOT_DY,
-                         meta->scale_inv + FP8_SLOT_W, dX, am + FP8_SLOT_DX, false, sms, st));
-    // wgrad: dW[N][K] = dY8t[N][M] . X8t[K][M]^T
-    return gemm_checked(fn, dY8t, fg, X8t, FP8_E4M3, N, K, M, meta->scale_inv + FP8_SLOT_DY,
-                        meta->scale_inv + FP8_SLOT_X, dW, nullptr, false, sms, st);
+    // One launch for both GEMMs, dgrad's (longer-K) tiles first:
+    //   dgrad: dX[M][K] = dY8[M][N] . W8t[K][N]^T
+    //   wgrad: dW[N][K] = dY8t[N][M] . X8t[K][M]^T
+    const fp8k::GemmSpec g[2] = {
+        {dY8, fg, W8t, FP8_E4M3, M, K, N, meta->scale_inv + FP8_SLOT_DY,
+         meta->scale_inv + FP8_SLOT_W, dX, am + FP8_SLOT_DX, false},
+        {dY8t, fg, X8t, FP8_E4M3, N, K, M, meta->scale_inv + FP8_SLOT_DY,
+         meta->scale_inv + FP8_SLOT_X, dW, nullptr, false}};
+    const char *what = nullptr;
+    cudaError_t e = fp8k::launch_gemm_group(g, 2, sms, st, &what);
+    if (e != cudaSuccess)
+        return what ? fail(FP8_ERR_CUDA, "%s: %s", fn, what) : cuda_fail(e, fn);
+    return FP8_OK;
 }
 
 }  // extern "C"

@@ -115,14 +115,31 @@ __device__ __forceinline__ void transpose4x4(uint32_t w0, uint32_t w1, uint32_t 
     t3 = __byte_perm(b01, b23, 0x7632);
 }
 
-// CURRENT = just-in-time scaling: the scale is derived here from this tensor's
-// amax (computed by amax_kernel just before) instead of being read as given;
-// block 0 also writes it and its inverse back.
+// One tensor of a cast launch (a launch may carry two tensors of the same
+// format, e.g. X and W of the forward pass, whose tiles form one list).
+struct CastTensor {
+    int64_t rows, cols, tiles_c, tile_begin;
+    float *scale;            // read; in just-in-time mode also written
+    float *scale_inv;        // written in just-in-time mode
+    const float *amax_in;    // just-in-time mode: this tensor's amax
+    uint8_t *out, *out_t;    // row-major and transposed FP8 outputs (either may be null)
+    unsigned *amax_bits;     // fused amax output (max-combined), or null
+};
+
+struct CastArgs {
+    CUtensorMap maps[2];
+    CastTensor t[2];
+    int num_tensors;
+    int margin;
+    int64_t num_tiles;
+};
+
+// CURRENT = just-in-time scaling: each tensor's scale is derived here from
+// its amax (computed by amax_kernel just before) instead of being read as
+// given; block 0 also writes it and its inverse back.
 template <int FMT, bool CURRENT>
-__global__ void __launch_bounds__(kQtThreads, 2) quantize_transpose_kernel(
-    const __grid_constant__ CUtensorMap tmx, int64_t rows, int64_t cols, float *scale_p,
-    uint8_t *__restrict__ out, uint8_t *__restrict__ out_t, unsigned *__restrict__ amax_bits,
-    int64_t tiles_c, int64_t num_tiles, const float *amax_in, float *scale_inv_p, int margin) {
+__global__ void __launch_bounds__(kQtThreads, 2)
+    quantize_transpose_kernel(const __grid_constant__ CastArgs a) {
     extern __shared__ uint8_t qt_smem_raw[];
     uint8_t *base = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(qt_smem_raw) + 127) & ~static_cast<uintptr_t>(127));
@@ -133,43 +150,60 @@ __global__ void __launch_bounds__(kQtThreads, 2) quantize_transpose_kernel(
     volatile int *abort_flag = reinterpret_cast<volatile int *>(full + kQtStages);
 
     const int tid = threadIdx.x;
-    float s = *scale_p;
-    if constexpr (CURRENT) {
-        bool valid;
-        s = recipe_scale(*amax_in, FMT == 0 ? 448.0f : 57344.0f, margin, s, valid);
-        if (valid && blockIdx.x == 0 && tid == 0) {
-            *scale_p = s;
-            *scale_inv_p = __fdiv_rn(1.0f, s);
+    float sc[2];
+    uint32_t tmax[2] = {0u, 0u};
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        sc[i] = i < a.num_tensors ? *a.t[i].scale : 0.0f;
+        if constexpr (CURRENT) {
+            if (i < a.num_tensors) {
+                bool valid;
+                sc[i] = recipe_scale(*a.t[i].amax_in, FMT == 0 ? 448.0f : 57344.0f, a.margin,
+                                     sc[i], valid);
+                if (valid && blockIdx.x == 0 && tid == 0) {
+                    *a.t[i].scale = sc[i];
+                    *a.t[i].scale_inv = __fdiv_rn(1.0f, sc[i]);
+                }
+            }
         }
     }
-    uint32_t tmax = 0;
     // thread 0's count of loads issued into / consumed from each stage
     int issued[kQtStages] = {}, consumed[kQtStages] = {};
+
+    auto issue = [&](int st, int64_t t) {
+        const int p = (a.num_tensors > 1 && t >= a.t[1].tile_begin) ? 1 : 0;
+        const int64_t lt = t - a.t[p].tile_begin;
+        ++issued[st];
+        mbar_arrive_expect_tx(smem_u32(full + st), kQtStageBytes);
+        tma_load_2d(smem_u32(stage_base + st * kQtStageBytes), &a.maps[p], smem_u32(full + st),
+                    static_cast<int32_t>((lt % a.t[p].tiles_c) * kQtTile),
+                    static_cast<int32_t>((lt / a.t[p].tiles_c) * kQtTile));
+    };
 
     if (tid == 0) {
         for (int st = 0; st < kQtStages; ++st) mbar_init(smem_u32(full + st), 1);
         *abort_flag = 0;
         fence_mbar_init();
-        prefetch_tmap(&tmx);
+        for (int i = 0; i < a.num_tensors; ++i)
+            if (a.t[i].rows > 0 && a.t[i].cols > 0) prefetch_tmap(&a.maps[i]);
         for (int st = 0; st < kQtStages; ++st) {
             const int64_t t = blockIdx.x + static_cast<int64_t>(st) * gridDim.x;
-            if (t < num_tiles) {
-                ++issued[st];
-                mbar_arrive_expect_tx(smem_u32(full + st), kQtStageBytes);
-                tma_load_2d(smem_u32(stage_base + st * kQtStageBytes), &tmx, smem_u32(full + st),
-                            static_cast<int32_t>((t % tiles_c) * kQtTile),
-                            static_cast<int32_t>((t / tiles_c) * kQtTile));
-            }
+            if (t < a.num_tiles) issue(st, t);
         }
     }
     __syncthreads();
 
     int64_t it = 0;
-    for (int64_t t = blockIdx.x; t < num_tiles; t += gridDim.x, ++it) {
+    for (int64_t t = blockIdx.x; t < a.num_tiles; t += gridDim.x, ++it) {
         const int st = static_cast<int>(it % kQtStages);
         const uint32_t parity = static_cast<uint32_t>((it / kQtStages) & 1);
-        const int64_t r0 = (t / tiles_c) * kQtTile;
-        const int64_t c0 = (t % tiles_c) * kQtTile;
+        const int p = (a.num_tensors > 1 && t >= a.t[1].tile_begin) ? 1 : 0;
+        const CastTensor &T = a.t[p];
+        const int64_t lt = t - T.tile_begin;
+        const int64_t r0 = (lt / T.tiles_c) * kQtTile;
+        const int64_t c0 = (lt % T.tiles_c) * kQtTile;
+        const int64_t rows = T.rows, cols = T.cols;
+        const float s = p ? sc[1] : sc[0];
         const bool ok = mbar_wait(smem_u32(full + st), parity, abort_flag);
         if (__syncthreads_or(!ok)) {
             if (tid == 0) {
@@ -187,15 +221,16 @@ __global__ void __launch_bounds__(kQtThreads, 2) quantize_transpose_kernel(
             const int idx = i * kQtThreads + tid;
             v[i] = *reinterpret_cast<const uint4 *>(xs + (idx >> 4) * kQtTile + (idx & 15) * 8);
         }
+        uint32_t m = 0;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
             const int idx = i * kQtThreads + tid;
             const int rr = idx >> 4, vv = idx & 15;
             const int64_t r = r0 + rr, c = c0 + vv * 8;
-            tmax = amax_bits2(tmax, v[i].x);
-            tmax = amax_bits2(tmax, v[i].y);
-            tmax = amax_bits2(tmax, v[i].z);
-            tmax = amax_bits2(tmax, v[i].w);
+            m = amax_bits2(m, v[i].x);
+            m = amax_bits2(m, v[i].y);
+            m = amax_bits2(m, v[i].z);
+            m = amax_bits2(m, v[i].w);
             uint2 q;
             q.x = cvt2_fp8<FMT>(__fmul_rn(bf16_lo(v[i].x), s), __fmul_rn(bf16_hi(v[i].x), s)) |
                   (cvt2_fp8<FMT>(__fmul_rn(bf16_lo(v[i].y), s), __fmul_rn(bf16_hi(v[i].y), s))
@@ -203,24 +238,22 @@ __global__ void __launch_bounds__(kQtThreads, 2) quantize_transpose_kernel(
             q.y = cvt2_fp8<FMT>(__fmul_rn(bf16_lo(v[i].z), s), __fmul_rn(bf16_hi(v[i].z), s)) |
                   (cvt2_fp8<FMT>(__fmul_rn(bf16_lo(v[i].w), s), __fmul_rn(bf16_hi(v[i].w), s))
                    << 16);
-            if (out != nullptr && r < rows && c < cols)
-                *reinterpret_cast<uint2 *>(out + r * cols + c) = q;
+            if (T.out != nullptr && r < rows && c < cols)
+                *reinterpret_cast<uint2 *>(T.out + r * cols + c) = q;
             *reinterpret_cast<uint2 *>(&tile[rr * 32 + ((vv * 2) ^ qt_swz(rr))]) = q;
         }
+        if (p)
+            tmax[1] = max(tmax[1], m);
+        else
+            tmax[0] = max(tmax[0], m);
         __syncthreads();  // stage st fully read; word tile complete
 
         if (tid == 0) {
             const int64_t tn = t + static_cast<int64_t>(kQtStages) * gridDim.x;
-            if (tn < num_tiles) {
-                ++issued[st];
-                mbar_arrive_expect_tx(smem_u32(full + st), kQtStageBytes);
-                tma_load_2d(smem_u32(stage_base + st * kQtStageBytes), &tmx, smem_u32(full + st),
-                            static_cast<int32_t>((tn % tiles_c) * kQtTile),
-                            static_cast<int32_t>((tn / tiles_c) * kQtTile));
-            }
+            if (tn < a.num_tiles) issue(st, tn);
         }
 
-        if (out_t != nullptr) {
+        if (T.out_t != nullptr) {
             const int lane = tid & 31, warp = tid >> 5;
             const int rblk = lane & 7;              // 16-row block of the tile
             const int cw = warp * 4 + (lane >> 3);  // word column = 4 tile columns
@@ -240,7 +273,7 @@ __global__ void __launch_bounds__(kQtThreads, 2) quantize_transpose_kernel(
             for (int cc = 0; cc < 4; ++cc) {
                 const int64_t c = c0 + cw * 4 + cc;
                 if (r < rows && c < cols)
-                    *reinterpret_cast<uint4 *>(out_t + c * rows + r) =
+                    *reinterpret_cast<uint4 *>(T.out_t + c * rows + r) =
                         make_uint4(o[cc][0], o[cc][1], o[cc][2], o[cc][3]);
             }
         }
@@ -255,15 +288,20 @@ __global__ void __launch_bounds__(kQtThreads, 2) quantize_transpose_kernel(
                           nullptr, 100000000ull);
     }
 
-    if (amax_bits != nullptr) {
-        __shared__ uint32_t warp_max[kQtThreads / 32];
-        tmax = __reduce_max_sync(0xFFFFFFFFu, tmax);
-        if ((tid & 31) == 0) warp_max[tid >> 5] = tmax;
-        __syncthreads();
-        if (tid < 32) {
-            uint32_t m = tid < kQtThreads / 32 ? warp_max[tid] : 0u;
+    __shared__ uint32_t warp_max[2][kQtThreads / 32];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const uint32_t m = __reduce_max_sync(0xFFFFFFFFu, tmax[i]);
+        if ((tid & 31) == 0) warp_max[i][tid >> 5] = m;
+    }
+    __syncthreads();
+    if (tid < 32) {
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            uint32_t m = tid < kQtThreads / 32 ? warp_max[i][tid] : 0u;
             m = __reduce_max_sync(0xFFFFFFFFu, m);
-            if (tid == 0 && m != 0) atomicMax(amax_bits, m << 16);
+            if (tid == 0 && m != 0 && i < a.num_tensors && a.t[i].amax_bits != nullptr)
+                atomicMax(a.t[i].amax_bits, m << 16);
         }
     }
 }
@@ -326,10 +364,7 @@ cudaError_t launch_amax(const void *x, int64_t n, float *amax, int sm_count, cud
 }
 
 template <int FMT, bool CURRENT>
-static cudaError_t qt_launch(const CUtensorMap &tm, int64_t rows, int64_t cols, float *scale,
-                             uint8_t *out, uint8_t *out_t, unsigned *ab, int64_t tiles_c,
-                             int64_t num_tiles, const float *amax_in, float *scale_inv, int margin,
-                             int sm_count, cudaStream_t st) {
+static cudaError_t qt_launch(const CastArgs &args, int sm_count, cudaStream_t st) {
     static std::once_flag attr_once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(attr_once, [] {
@@ -338,53 +373,88 @@ static cudaError_t qt_launch(const CUtensorMap &tm, int64_t rows, int64_t cols, 
                                         static_cast<int>(kQtSmem));
     });
     if (attr_err != cudaSuccess) return attr_err;
+    if (args.num_tiles == 0) return cudaSuccess;
     int64_t blocks = static_cast<int64_t>(sm_count) * 2;
-    if (blocks > num_tiles) blocks = num_tiles;
-    quantize_transpose_kernel<FMT, CURRENT><<<static_cast<unsigned>(blocks), kQtThreads, kQtSmem,
-                                               st>>>(tm, rows, cols, scale, out, out_t, ab, tiles_c,
-                                                     num_tiles, amax_in, scale_inv, margin);
+    if (blocks > args.num_tiles) blocks = args.num_tiles;
+    quantize_transpose_kernel<FMT, CURRENT>
+        <<<static_cast<unsigned>(blocks), kQtThreads, kQtSmem, st>>>(args);
     return cudaGetLastError();
+}
+
+// Fill the launch arguments for up to two tensors; false if a TMA
+// descriptor cannot be built.
+static bool cast_args(CastArgs &args, const CastSpec *specs, int n, int margin) {
+    args.num_tensors = n;
+    args.margin = margin;
+    int64_t tiles = 0;
+    for (int i = 0; i < n; ++i) {
+        const CastSpec &c = specs[i];
+        CastTensor &t = args.t[i];
+        t.rows = c.rows;
+        t.cols = c.cols;
+        t.tiles_c = (c.cols + kQtTile - 1) / kQtTile;
+        t.tile_begin = tiles;
+        t.scale = c.scale;
+        t.scale_inv = c.scale_inv;
+        t.amax_in = c.amax;
+        t.out = c.out;
+        t.out_t = c.out_t;
+        t.amax_bits = reinterpret_cast<unsigned *>(c.amax);
+        if (c.rows > 0 && c.cols > 0) {
+            if (!encode_tmap_2d(&args.maps[i], c.x, true, c.cols, c.rows, kQtTile, kQtTile, false))
+                return false;
+            tiles += ((c.rows + kQtTile - 1) / kQtTile) * t.tiles_c;
+        } else {
+            args.maps[i] = CUtensorMap{};
+        }
+    }
+    for (int i = n; i < 2; ++i) {
+        args.t[i] = args.t[0];
+        args.maps[i] = args.maps[0];
+    }
+    args.num_tiles = tiles;
+    return true;
+}
+
+cudaError_t launch_cast_group(const CastSpec *specs, int n, int fmt, bool current, int margin,
+                              int sm_count, cudaStream_t st) {
+    if (n < 1 || n > 2) return cudaErrorInvalidValue;
+    for (int i = 0; i < n; ++i) {
+        if (current) {
+            cudaError_t e = launch_amax(specs[i].x, specs[i].rows * specs[i].cols, specs[i].amax,
+                                        sm_count, st);
+            if (e != cudaSuccess) return e;
+        } else if (specs[i].amax != nullptr && specs[i].zero_amax) {
+            cudaError_t e = cudaMemsetAsync(specs[i].amax, 0, sizeof(float), st);
+            if (e != cudaSuccess) return e;
+        }
+    }
+    CastArgs args;
+    if (!cast_args(args, specs, n, margin)) return cudaErrorInvalidValue;
+    if (current) {
+        // the amax was computed by amax_kernel; the cast only derives the scale
+        for (int i = 0; i < n; ++i) args.t[i].amax_bits = nullptr;
+        return fmt == 0 ? qt_launch<0, true>(args, sm_count, st)
+                        : qt_launch<1, true>(args, sm_count, st);
+    }
+    return fmt == 0 ? qt_launch<0, false>(args, sm_count, st)
+                    : qt_launch<1, false>(args, sm_count, st);
 }
 
 cudaError_t launch_quantize_transpose(const void *x, int64_t rows, int64_t cols,
                                       const float *scale, int fmt, uint8_t *out, uint8_t *out_t,
                                       float *amax, bool zero_amax, int sm_count,
                                       cudaStream_t st) {
-    if (amax != nullptr && zero_amax) {
-        cudaError_t e = cudaMemsetAsync(amax, 0, sizeof(float), st);
-        if (e != cudaSuccess) return e;
-    }
-    if (rows == 0 || cols == 0) return cudaSuccess;
-    CUtensorMap tm;
-    if (!encode_tmap_2d(&tm, x, true, cols, rows, kQtTile, kQtTile, false))
-        return cudaErrorInvalidValue;
-    const int64_t tiles_c = (cols + kQtTile - 1) / kQtTile;
-    const int64_t num_tiles = ((rows + kQtTile - 1) / kQtTile) * tiles_c;
-    auto *ab = reinterpret_cast<unsigned *>(amax);
-    float *sc = const_cast<float *>(scale);   // read only in this mode
-    if (fmt == 0)
-        return qt_launch<0, false>(tm, rows, cols, sc, out, out_t, ab, tiles_c, num_tiles, nullptr,
-                                   nullptr, 0, sm_count, st);
-    return qt_launch<1, false>(tm, rows, cols, sc, out, out_t, ab, tiles_c, num_tiles, nullptr,
-                               nullptr, 0, sm_count, st);
+    CastSpec c{x, rows, cols, const_cast<float *>(scale), nullptr, out, out_t, amax, zero_amax};
+    return launch_cast_group(&c, 1, fmt, false, 0, sm_count, st);
 }
 
 cudaError_t launch_quantize_transpose_current(const void *x, int64_t rows, int64_t cols, int fmt,
                                               int margin, uint8_t *out, uint8_t *out_t,
                                               float *amax, float *scale, float *scale_inv,
                                               int sm_count, cudaStream_t st) {
-    cudaError_t e = launch_amax(x, rows * cols, amax, sm_count, st);
-    if (e != cudaSuccess || rows == 0 || cols == 0) return e;
-    CUtensorMap tm;
-    if (!encode_tmap_2d(&tm, x, true, cols, rows, kQtTile, kQtTile, false))
-        return cudaErrorInvalidValue;
-    const int64_t tiles_c = (cols + kQtTile - 1) / kQtTile;
-    const int64_t num_tiles = ((rows + kQtTile - 1) / kQtTile) * tiles_c;
-    if (fmt == 0)
-        return qt_launch<0, true>(tm, rows, cols, scale, out, out_t, nullptr, tiles_c, num_tiles,
-                                  amax, scale_inv, margin, sm_count, st);
-    return qt_launch<1, true>(tm, rows, cols, scale, out, out_t, nullptr, tiles_c, num_tiles, amax,
-                              scale_inv, margin, sm_count, st);
+    CastSpec c{x, rows, cols, scale, scale_inv, out, out_t, amax, true};
+    return launch_cast_group(&c, 1, fmt, true, margin, sm_count, st);
 }
 
 cudaError_t launch_scale_update(float *history, const float *amax, float *scale, float *scale_inv,

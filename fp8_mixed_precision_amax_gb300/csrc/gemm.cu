@@ -9,18 +9,24 @@
 //   d_amax = max |D| over the emitted BF16 values.
 // A is [M][K] and B is [N][K], both contiguous along K ("TN").
 //
-// Design (one CTA per SM, persistent over output tiles of 128 x 256):
-//   warp 0     TMA producer: 128-byte-swizzled K-slices of A (128 x 128 B)
-//              and B (256 x 128 B) into a 4-stage shared-memory ring;
-//   warp 1     allocates 512 TMEM columns (two 128 x 256 fp32 accumulators)
-//              and issues tcgen05.mma (128 x 256 x 32 per instruction, four
-//              per K-slice); tcgen05.commit frees ring stages and hands a
-//              finished accumulator to the epilogue;
+// Design (one CTA per SM, persistent over output tiles):
+//   warp 0     TMA producer: 128-byte-swizzled 128-deep K-slices of A and B
+//              into a shared-memory ring;
+//   warp 1     allocates 512 TMEM columns (two 256-column fp32 accumulators)
+//              and issues tcgen05.mma (four per K-slice); tcgen05.commit
+//              frees ring stages and hands a finished accumulator on;
 //   warps 2-5  epilogue: tcgen05.ld of their 32-lane quarter, scale, BF16
 //              round, running amax, 16-byte stores; releases the accumulator
 //              so the next tile's MMAs overlap this tile's epilogue.
-// Tiles are visited in groups of 16 row-blocks so that concurrently running
-// CTAs share A and B slices in L2.  Every wait is bounded.
+// Above 128 rows, two CTAs on two SMs (a cluster) share each 256 x 256 tile
+// (tcgen05 cta_group::2): each loads its own 128 A rows and 128 of the 256 B
+// rows, and the even CTA issues M = 256 MMAs that read both CTAs' shared
+// memory and write both CTAs' tensor memory.  No TMA multicast is used.
+// One launch may carry two independent GEMMs (the backward pass's dgrad and
+// wgrad): their tiles form one list, so the last, partly filled wave of one
+// is filled with tiles of the other.  Tiles are visited in groups of 16
+// row-blocks so that concurrently running CTAs share operand slices in L2.
+// Every wait is bounded.
 #include <cuda_bf16.h>
 
 #include <cstdint>
@@ -35,16 +41,11 @@ __device__ unsigned g_error_flags = 0;
 
 namespace {
 
-// Tile geometry.  Each CTA owns 128 output rows and a 256-column fp32
-// accumulator (double-buffered: 512 TMEM columns).  The single-CTA variant
-// loads all 256 B rows itself (4 stages of 48 KB); the CTA-pair variant
-// splits a 256 x 256 tile over two SMs, each loading its 128 A rows and 128
-// of the 256 B rows (6 stages of 32 KB), with the even CTA issuing M = 256
-// MMAs that read both CTAs' shared memory.
 constexpr int BM = 128, BN = 256, BK = 128;
 constexpr int NUM_THREADS = 192;
 constexpr int TMEM_COLS = 2 * BN;
 constexpr int GROUP_M = 16;
+constexpr int MAX_PROBLEMS = 2;
 
 template <bool PAIR>
 struct Cfg {
@@ -59,14 +60,22 @@ struct Cfg {
     static constexpr uint32_t EPI_ARRIVALS = PAIR ? 8 : 4;  // epilogue warps per tile
 };
 
-struct GemmParams {
+struct GemmProblem {
     __nv_bfloat16 *D;
     unsigned *amax_bits;
     const float *a_scale_inv;
     const float *b_scale_inv;
     int64_t M, N;
     int tiles_m, tiles_n, num_kb;
+    int tile_begin;   // first index of this problem's tiles in the launch's tile list
     uint32_t idesc;
+};
+
+struct GemmArgs {
+    CUtensorMap maps[2 * MAX_PROBLEMS];   // A0, B0, A1, B1
+    GemmProblem prob[MAX_PROBLEMS];
+    int num_problems;
+    int num_tiles;
 };
 
 __device__ __forceinline__ void tile_coords(int tile, int tiles_m, int tiles_n, int &mb, int &nb) {
@@ -78,15 +87,20 @@ __device__ __forceinline__ void tile_coords(int tile, int tiles_m, int tiles_n, 
     nb = in / gm;
 }
 
+// Problem and (row-block, column-block) of a tile of the launch's list.
+__device__ __forceinline__ int locate(const GemmArgs &a, int tile, int &mb, int &nb) {
+    const int p = (a.num_problems > 1 && tile >= a.prob[1].tile_begin) ? 1 : 0;
+    tile_coords(tile - a.prob[p].tile_begin, a.prob[p].tiles_m, a.prob[p].tiles_n, mb, nb);
+    return p;
+}
+
 __device__ __forceinline__ void raise_error(volatile int *abort_flag) {
     atomicOr(&g_error_flags, kErrWaitTimeout);
     *abort_flag = 1;
 }
 
 template <bool PAIR>
-__global__ void __launch_bounds__(NUM_THREADS, 1)
-    gemm_tn_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const GemmParams p) {
+__global__ void __launch_bounds__(NUM_THREADS, 1) gemm_tn_kernel(const __grid_constant__ GemmArgs a) {
     using C = Cfg<PAIR>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -118,8 +132,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         mbar_init(drain_bar, 1);
         *abort_flag = 0;
         fence_mbar_init();
-        prefetch_tmap(&tmA);
-        prefetch_tmap(&tmB);
+        for (int i = 0; i < 2 * a.num_problems; ++i) prefetch_tmap(&a.maps[i]);
     }
     if (warp == 1) {
         if constexpr (PAIR) {
@@ -138,7 +151,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
-    const int num_tiles = p.tiles_m * p.tiles_n;
 
     if (warp == 0) {
         // ------------------------------------------------------ TMA producer
@@ -147,12 +159,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             uint32_t phase = 0;
             int64_t issued = 0;
             bool ok = true;
-            for (int tile = unit; ok && tile < num_tiles; tile += num_units) {
+            for (int tile = unit; ok && tile < a.num_tiles; tile += num_units) {
                 int mb, nb;
-                tile_coords(tile, p.tiles_m, p.tiles_n, mb, nb);
+                const int pi = locate(a, tile, mb, nb);
+                const CUtensorMap *tmA = &a.maps[2 * pi];
+                const CUtensorMap *tmB = &a.maps[2 * pi + 1];
                 const int32_t arow = mb * C::TILE_M + static_cast<int32_t>(rank) * BM;
                 const int32_t brow = nb * BN + static_cast<int32_t>(rank) * C::B_ROWS;
-                for (int kb = 0; kb < p.num_kb; ++kb) {
+                const int num_kb = a.prob[pi].num_kb;
+                for (int kb = 0; kb < num_kb; ++kb) {
                     if (!mbar_wait(empty0 + 8 * stage, phase ^ 1u, abort_flag)) {
                         raise_error(abort_flag);
                         ok = false;
@@ -165,12 +180,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         // both halves complete on the even CTA's barrier
                         const uint32_t fb0 = mapa_shared(fb, 0);
                         if (rank == 0) mbar_arrive_expect_tx(fb, C::STAGE_TX);
-                        tma_load_2d_pair(dA, &tmA, fb0, kb * BK, arow);
-                        tma_load_2d_pair(dB, &tmB, fb0, kb * BK, brow);
+                        tma_load_2d_pair(dA, tmA, fb0, kb * BK, arow);
+                        tma_load_2d_pair(dB, tmB, fb0, kb * BK, brow);
                     } else {
                         mbar_arrive_expect_tx(fb, C::STAGE_TX);
-                        tma_load_2d(dA, &tmA, fb, kb * BK, arow);
-                        tma_load_2d(dB, &tmB, fb, kb * BK, brow);
+                        tma_load_2d(dA, tmA, fb, kb * BK, arow);
+                        tma_load_2d(dB, tmB, fb, kb * BK, brow);
                     }
                     ++issued;
                     if (++stage == C::STAGES) {
@@ -204,7 +219,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             int stage = 0, acc = 0;
             uint32_t phase = 0, acc_phase = 0;
             bool ok = true, any = false;
-            for (int tile = unit; ok && tile < num_tiles; tile += num_units) {
+            for (int tile = unit; ok && tile < a.num_tiles; tile += num_units) {
+                int mb, nb;
+                const int pi = locate(a, tile, mb, nb);
+                const int num_kb = a.prob[pi].num_kb;
+                const uint32_t idesc = a.prob[pi].idesc;
                 if (!mbar_wait(acce0 + 8 * acc, acc_phase ^ 1u, abort_flag)) {
                     raise_error(abort_flag);
                     ok = false;
@@ -212,7 +231,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
-                for (int kb = 0; kb < p.num_kb; ++kb) {
+                for (int kb = 0; kb < num_kb; ++kb) {
                     if (!mbar_wait(full0 + 8 * stage, phase, abort_flag)) {
                         raise_error(abort_flag);
                         ok = false;
@@ -226,9 +245,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         const uint64_t ad = smem_desc_sw128(a0 + 32 * k);
                         const uint64_t bd = smem_desc_sw128(b0 + 32 * k);
                         if constexpr (PAIR)
-                            mma_f8f6f4_pair(d_tmem, ad, bd, p.idesc, (kb | k) != 0);
+                            mma_f8f6f4_pair(d_tmem, ad, bd, idesc, (kb | k) != 0);
                         else
-                            mma_f8f6f4(d_tmem, ad, bd, p.idesc, (kb | k) != 0);
+                            mma_f8f6f4(d_tmem, ad, bd, idesc, (kb | k) != 0);
                     }
                     if constexpr (PAIR)
                         mma_commit_pair(empty0 + 8 * stage, 0x3);
@@ -262,13 +281,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     } else {
         // --------------------------------------------------------- epilogue
         const int q = warp & 3;  // TMEM lane quarter this warp may access
-        const float sab = __fmul_rn(*p.a_scale_inv, *p.b_scale_inv);
-        uint32_t tmax = 0;
+        float sab[MAX_PROBLEMS];
+        uint32_t tmax[MAX_PROBLEMS];
+#pragma unroll
+        for (int i = 0; i < MAX_PROBLEMS; ++i) {
+            sab[i] = i < a.num_problems ? __fmul_rn(*a.prob[i].a_scale_inv, *a.prob[i].b_scale_inv)
+                                        : 0.0f;
+            tmax[i] = 0;
+        }
         int acc = 0;
         uint32_t acc_phase = 0;
-        for (int tile = unit; tile < num_tiles; tile += num_units) {
+        for (int tile = unit; tile < a.num_tiles; tile += num_units) {
             int mb, nb;
-            tile_coords(tile, p.tiles_m, p.tiles_n, mb, nb);
+            const int pi = locate(a, tile, mb, nb);
+            const GemmProblem &P = a.prob[pi];
             const bool got = mbar_wait(accf0 + 8 * acc, acc_phase, abort_flag);
             // the lanes leave the wait one by one; tcgen05.ld needs the whole warp
             if (!__all_sync(0xFFFFFFFFu, got)) {
@@ -276,9 +302,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 break;
             }
             tc_fence_after();
+            const float s = pi ? sab[1] : sab[0];
+            uint32_t m = 0;
             const int64_t row = static_cast<int64_t>(mb) * C::TILE_M + rank * BM + q * 32 + lane;
-            const bool row_in = row < p.M;
-            __nv_bfloat16 *drow = p.D + row * p.N;
+            const bool row_in = row < P.M;
+            __nv_bfloat16 *drow = P.D + row * P.N;
             const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                                     static_cast<uint32_t>(acc * BN);
 #pragma unroll 1
@@ -289,19 +317,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 uint32_t packed[16];
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
-                    const float y0 = __fmul_rn(__uint_as_float(r[2 * j]), sab);
-                    const float y1 = __fmul_rn(__uint_as_float(r[2 * j + 1]), sab);
+                    const float y0 = __fmul_rn(__uint_as_float(r[2 * j]), s);
+                    const float y1 = __fmul_rn(__uint_as_float(r[2 * j + 1]), s);
                     const __nv_bfloat162 h = __floats2bfloat162_rn(y0, y1);
                     packed[j] = *reinterpret_cast<const uint32_t *>(&h);
                 }
                 if (row_in) {
 #pragma unroll
                     for (int v = 0; v < 4; ++v) {
-                        if (col0 + 8 * v < p.N) {
-                            tmax = amax_bits2(tmax, packed[4 * v]);
-                            tmax = amax_bits2(tmax, packed[4 * v + 1]);
-                            tmax = amax_bits2(tmax, packed[4 * v + 2]);
-                            tmax = amax_bits2(tmax, packed[4 * v + 3]);
+                        if (col0 + 8 * v < P.N) {
+                            m = amax_bits2(m, packed[4 * v]);
+                            m = amax_bits2(m, packed[4 * v + 1]);
+                            m = amax_bits2(m, packed[4 * v + 2]);
+                            m = amax_bits2(m, packed[4 * v + 3]);
                             *reinterpret_cast<uint4 *>(drow + col0 + 8 * v) =
                                 make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2],
                                            packed[4 * v + 3]);
@@ -309,6 +337,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     }
                 }
             }
+            if (pi)
+                tmax[1] = max(tmax[1], m);
+            else
+                tmax[0] = max(tmax[0], m);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) {
@@ -322,9 +354,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 acc_phase ^= 1u;
             }
         }
-        if (p.amax_bits != nullptr) {
-            tmax = __reduce_max_sync(0xFFFFFFFFu, tmax);
-            if (lane == 0 && tmax != 0) atomicMax(p.amax_bits, tmax << 16);
+#pragma unroll
+        for (int i = 0; i < MAX_PROBLEMS; ++i) {
+            if (i < a.num_problems && a.prob[i].amax_bits != nullptr) {
+                const uint32_t m = __reduce_max_sync(0xFFFFFFFFu, tmax[i]);
+                if (lane == 0 && m != 0) atomicMax(a.prob[i].amax_bits, m << 16);
+            }
         }
     }
 
@@ -346,55 +381,40 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 // --------------------------------------------------------------- host side --
 
 template <bool PAIR>
-static cudaError_t launch_variant(const CUtensorMap &ta, const CUtensorMap &tb, const GemmParams &p,
-                                  int grid, cudaStream_t st) {
-    static std::once_flag attr_once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(attr_once, [] {
-        attr_err = cudaFuncSetAttribute(gemm_tn_kernel<PAIR>,
-                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        static_cast<int>(Cfg<PAIR>::SMEM));
+cudaError_t set_smem_attr() {
+    static std::once_flag once;
+    static cudaError_t err = cudaSuccess;
+    std::call_once(once, [] {
+        err = cudaFuncSetAttribute(gemm_tn_kernel<PAIR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   static_cast<int>(Cfg<PAIR>::SMEM));
     });
-    if (attr_err != cudaSuccess) return attr_err;
-    if constexpr (PAIR) {
-        cudaLaunchConfig_t cfg = {};
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = 2;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
-        cfg.blockDim = dim3(NUM_THREADS, 1, 1);
-        cfg.dynamicSmemBytes = Cfg<PAIR>::SMEM;
-        cfg.stream = st;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        return cudaLaunchKernelEx(&cfg, gemm_tn_kernel<PAIR>, ta, tb, p);
-    } else {
-        gemm_tn_kernel<PAIR><<<grid, NUM_THREADS, Cfg<PAIR>::SMEM, st>>>(ta, tb, p);
-        return cudaGetLastError();
-    }
+    return err;
+}
+
+cudaLaunchConfig_t pair_config(int grid, cudaLaunchAttribute *attr, cudaStream_t st) {
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+    cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = Cfg<true>::SMEM;
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cfg;
 }
 
 // Number of CTA pairs that can be resident at once (clusters of two need two
 // SMs of the same GPC), cached per process.
-static int pair_slots(int sm_count) {
+int pair_slots(int sm_count) {
     static std::once_flag once;
     static int slots = 0;
     std::call_once(once, [sm_count] {
-        cudaFuncSetAttribute(gemm_tn_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(Cfg<true>::SMEM));
-        cudaLaunchConfig_t cfg = {};
+        if (set_smem_attr<true>() != cudaSuccess) return;
         cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = 2;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.gridDim = dim3(static_cast<unsigned>(sm_count & ~1), 1, 1);
-        cfg.blockDim = dim3(NUM_THREADS, 1, 1);
-        cfg.dynamicSmemBytes = Cfg<true>::SMEM;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
+        cudaLaunchConfig_t cfg = pair_config(sm_count & ~1, attr, nullptr);
         int n = 0;
         if (cudaOccupancyMaxActiveClusters(&n, gemm_tn_kernel<true>, &cfg) != cudaSuccess || n < 1)
             n = 0;
@@ -405,45 +425,73 @@ static int pair_slots(int sm_count) {
 
 }  // namespace
 
+cudaError_t launch_gemm_group(const GemmSpec *specs, int n, int sm_count, cudaStream_t st,
+                              const char **what) {
+    if (n < 1 || n > MAX_PROBLEMS) return cudaErrorInvalidValue;
+    // CTA pairs when every problem is taller than one 128-row tile and the GPU
+    // can hold them; single CTAs otherwise.
+    bool tall = true;
+    for (int i = 0; i < n; ++i) tall = tall && specs[i].M > BM;
+    const int slots = tall ? pair_slots(sm_count) : 0;
+    const bool pair = slots > 0;
+    const int tile_m = pair ? 2 * BM : BM;
+    const uint32_t b_rows = pair ? BN / 2 : BN;
+    GemmArgs a;
+    a.num_problems = n;
+    int tiles = 0;
+    for (int i = 0; i < n; ++i) {
+        const GemmSpec &g = specs[i];
+        if (g.d_amax != nullptr && g.zero_amax) {
+            cudaError_t e = cudaMemsetAsync(g.d_amax, 0, sizeof(float), st);
+            if (e != cudaSuccess) return e;
+        }
+        if (!encode_tmap_2d(&a.maps[2 * i], g.A, false, g.K, g.M, BK, BM, true) ||
+            !encode_tmap_2d(&a.maps[2 * i + 1], g.B, false, g.K, g.N, BK, b_rows, true)) {
+            if (what) *what = "cuTensorMapEncodeTiled failed for an operand";
+            return cudaErrorInvalidValue;
+        }
+        GemmProblem &p = a.prob[i];
+        p.D = reinterpret_cast<__nv_bfloat16 *>(g.D);
+        p.amax_bits = reinterpret_cast<unsigned *>(g.d_amax);
+        p.a_scale_inv = g.a_scale_inv;
+        p.b_scale_inv = g.b_scale_inv;
+        p.M = g.M;
+        p.N = g.N;
+        p.tiles_m = static_cast<int>((g.M + tile_m - 1) / tile_m);
+        p.tiles_n = static_cast<int>((g.N + BN - 1) / BN);
+        p.num_kb = static_cast<int>((g.K + BK - 1) / BK);
+        p.tile_begin = tiles;
+        p.idesc = idesc_f8(static_cast<uint32_t>(g.fa), static_cast<uint32_t>(g.fb),
+                           static_cast<uint32_t>(tile_m), BN);
+        tiles += p.tiles_m * p.tiles_n;
+    }
+    for (int i = n; i < MAX_PROBLEMS; ++i) {
+        a.prob[i] = a.prob[0];
+        a.maps[2 * i] = a.maps[0];
+        a.maps[2 * i + 1] = a.maps[1];
+    }
+    a.num_tiles = tiles;
+    if (pair) {
+        cudaError_t e = set_smem_attr<true>();
+        if (e != cudaSuccess) return e;
+        const int units = tiles < slots ? tiles : slots;
+        cudaLaunchAttribute attr[1];
+        cudaLaunchConfig_t cfg = pair_config(2 * units, attr, st);
+        return cudaLaunchKernelEx(&cfg, gemm_tn_kernel<true>, a);
+    }
+    cudaError_t e = set_smem_attr<false>();
+    if (e != cudaSuccess) return e;
+    const int grid = tiles < sm_count ? tiles : sm_count;
+    gemm_tn_kernel<false><<<grid, NUM_THREADS, Cfg<false>::SMEM, st>>>(a);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_gemm_tn(const uint8_t *A, int fa, const uint8_t *B, int fb, int64_t M,
                            int64_t N, int64_t K, const float *a_scale_inv,
                            const float *b_scale_inv, void *D, float *d_amax, bool zero_amax,
                            int sm_count, cudaStream_t st, const char **what) {
-    if (d_amax != nullptr && zero_amax) {
-        cudaError_t e = cudaMemsetAsync(d_amax, 0, sizeof(float), st);
-        if (e != cudaSuccess) return e;
-    }
-    // CTA pairs for anything taller than one 128-row tile, when the GPU can
-    // hold them; single CTAs otherwise.
-    const int slots = M > BM ? pair_slots(sm_count) : 0;
-    const bool pair = slots > 0;
-    const uint32_t b_rows = pair ? BN / 2 : BN;
-    CUtensorMap ta, tb;
-    if (!encode_tmap_2d(&ta, A, false, K, M, BK, BM, true) ||
-        !encode_tmap_2d(&tb, B, false, K, N, BK, b_rows, true)) {
-        if (what) *what = "cuTensorMapEncodeTiled failed for an operand";
-        return cudaErrorInvalidValue;
-    }
-    GemmParams p;
-    p.D = reinterpret_cast<__nv_bfloat16 *>(D);
-    p.amax_bits = reinterpret_cast<unsigned *>(d_amax);
-    p.a_scale_inv = a_scale_inv;
-    p.b_scale_inv = b_scale_inv;
-    p.M = M;
-    p.N = N;
-    const int tile_m = pair ? 2 * BM : BM;
-    p.tiles_m = static_cast<int>((M + tile_m - 1) / tile_m);
-    p.tiles_n = static_cast<int>((N + BN - 1) / BN);
-    p.num_kb = static_cast<int>((K + BK - 1) / BK);
-    p.idesc = idesc_f8(static_cast<uint32_t>(fa), static_cast<uint32_t>(fb),
-                       static_cast<uint32_t>(tile_m), BN);
-    const int num_tiles = p.tiles_m * p.tiles_n;
-    if (pair) {
-        const int units = num_tiles < slots ? num_tiles : slots;
-        return launch_variant<true>(ta, tb, p, 2 * units, st);
-    }
-    const int grid = num_tiles < sm_count ? num_tiles : sm_count;
-    return launch_variant<false>(ta, tb, p, grid, st);
+    GemmSpec g{A, fa, B, fb, M, N, K, a_scale_inv, b_scale_inv, D, d_amax, zero_amax};
+    return launch_gemm_group(&g, 1, sm_count, st, what);
 }
 
 cudaError_t read_and_clear_error_flag(unsigned *flags, cudaStream_t st) {

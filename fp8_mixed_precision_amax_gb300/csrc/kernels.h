@@ -26,6 +26,25 @@ cudaError_t launch_quantize_transpose(const void *x, int64_t rows, int64_t cols,
                                       const float *scale, int fmt, uint8_t *out, uint8_t *out_t,
                                       float *amax, bool zero_amax, int sm_count, cudaStream_t st);
 
+// One tensor of a grouped cast: x [rows][cols] BF16 -> out / out_t (FP8),
+// scale (read; in just-in-time mode replaced, with scale_inv, from the amax),
+// amax (max-combined; cleared first when zero_amax; always overwritten in
+// just-in-time mode).
+struct CastSpec {
+    const void *x;
+    int64_t rows, cols;
+    float *scale;
+    float *scale_inv;
+    uint8_t *out, *out_t;
+    float *amax;
+    bool zero_amax;
+};
+
+// Up to two tensors of one format in one persistent cast launch (tiles form
+// one list).  current = just-in-time scaling (an amax pass per tensor first).
+cudaError_t launch_cast_group(const CastSpec *specs, int n, int fmt, bool current, int margin,
+                              int sm_count, cudaStream_t st);
+
 // Just-in-time scaling: amax of x into *amax (overwritten), then the cast
 // with scale = recipe formula of that amax (history of one), written back to
 // *scale / *scale_inv (both kept when the amax is 0 or not finite).
@@ -38,6 +57,28 @@ cudaError_t launch_quantize_transpose_current(const void *x, int64_t rows, int64
 cudaError_t launch_scale_update(float *history, const float *amax, float *scale, float *scale_inv,
                                 int num_tensors, int L, uint32_t format_mask, int margin,
                                 cudaStream_t st);
+
+// One GEMM of a grouped launch: D[M][N] = A[M][K] . B[N][K]^T (FP8 codes of
+// formats fa / fb), dequantised by a_scale_inv * b_scale_inv into BF16, with
+// the output amax max-combined into *d_amax (cleared first when zero_amax).
+struct GemmSpec {
+    const uint8_t *A;
+    int fa;
+    const uint8_t *B;
+    int fb;
+    int64_t M, N, K;
+    const float *a_scale_inv;
+    const float *b_scale_inv;
+    void *D;
+    float *d_amax;
+    bool zero_amax;
+};
+
+// Up to two independent GEMMs in one persistent launch; their tiles form one
+// list (the first spec's tiles first), so one GEMM's last partial wave is
+// filled with the other's tiles.
+cudaError_t launch_gemm_group(const GemmSpec *specs, int n, int sm_count, cudaStream_t st,
+                              const char **what);
 
 // FP8 "TN" GEMM on tcgen05 with the dequant + amax epilogue.  With
 // zero_amax the amax word is cleared first.  Returns cudaErrorInvalidValue

@@ -192,6 +192,44 @@ fp8_status fp8_gemm_tn(const uint8_t *A, int32_t fa, const uint8_t *B, int32_t f
                        int64_t N, int64_t K, const float *a_scale_inv, const float *b_scale_inv,
                        void *D, float *d_amax, void *stream);
 
+/* One GEMM of fp8_gemm_tn_grouped; fields as the arguments of fp8_gemm_tn. */
+typedef struct {
+    const uint8_t *A;
+    int32_t fa;
+    const uint8_t *B;
+    int32_t fb;
+    int64_t M, N, K;
+    const float *a_scale_inv;
+    const float *b_scale_inv;
+    void *D;
+    float *d_amax;
+} fp8_gemm_desc;
+
+/* One or two independent fp8_gemm_tn problems in a single persistent launch
+ * (helper; the backward pass runs dgrad and wgrad this way): the tiles of
+ * both form one list, so one GEMM's last partial wave is filled with the
+ * other's tiles.  n is 1 or 2; each problem is checked as by fp8_gemm_tn,
+ * and each d_amax (when not NULL) is overwritten with its own output amax. */
+fp8_status fp8_gemm_tn_grouped(const fp8_gemm_desc *descs, int32_t n, void *stream);
+
+/* One tensor of fp8_quantize_transpose_grouped; fields as the arguments of
+ * fp8_quantize_transpose. */
+typedef struct {
+    const void *x;
+    int64_t rows, cols;
+    const float *scale;
+    uint8_t *out;
+    uint8_t *out_t;
+    float *amax;
+} fp8_cast_desc;
+
+/* One or two fp8_quantize_transpose casts of the same format in a single
+ * persistent launch (helper; the forward pass casts X and W this way).  Each
+ * tensor is checked as by fp8_quantize_transpose; each amax (when not NULL)
+ * is overwritten with its own tensor's amax. */
+fp8_status fp8_quantize_transpose_grouped(const fp8_cast_desc *descs, int32_t n, int32_t fmt,
+                                          void *stream);
+
 /* Forward of the FP8 linear layer Y = X W^T (te.Linear under fp8_autocast,
  * implementation guide "Basic structure of FP8 training code" and the
  * recipe section).  Uses this step's (delayed) scales of X and W, or under

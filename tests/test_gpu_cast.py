@@ -188,3 +188,29 @@ def test_just_in_time_cast(fmt, margin):
         q, qt = o.quantize(xb, rs, fmt)
         assert_fp8_equal(host_u8(out), q, fmt, f"{shape}")
         assert_fp8_equal(host_u8(out_t), qt, fmt, f"{shape} t")
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_grouped_cast_of_two_tensors(fmt):
+    """Two tensors cast in one launch (as the forward pass casts X and W), each
+    with its own scale and amax; also with one of the two empty."""
+    f = _lib()
+    for shapes in [((1040, 1168), (144, 272)), ((256, 4112), (0, 64))]:
+        xs, specs = [], []
+        for i, shape in enumerate(shapes):
+            g = torch.Generator().manual_seed(300 + i)
+            x = (torch.randn(shape, generator=g) * (10.0 ** i)).to(torch.bfloat16).cuda()
+            rows, cols = shape
+            sc = torch.tensor([np.float32(448.0 / 40.0 / 10.0 ** i)], device="cuda")
+            out = torch.empty((rows, cols), dtype=torch.uint8, device="cuda")
+            out_t = torch.empty((cols, rows), dtype=torch.uint8, device="cuda")
+            am = torch.full((1,), -1.0, device="cuda")
+            xs.append((x, sc, out, out_t, am))
+        f.fp8_quantize_transpose_grouped(xs, fmt)
+        torch.cuda.synchronize()
+        for x, sc, out, out_t, am in xs:
+            xb = host_bf16_bits(x)
+            q, qt = o.quantize(xb, np.float32(sc.item()), fmt)
+            assert_fp8_equal(host_u8(out), q, fmt, "grouped out")
+            assert_fp8_equal(host_u8(out_t), qt, fmt, "grouped out_t")
+            assert f32_bits(am.cpu().numpy()[0]) == f32_bits(o.amax(xb))

@@ -93,3 +93,35 @@ def test_gemm_extreme_operands_and_zero():
 def test_gemm_sync_status_clean():
     f = _lib()
     f.fp8_sync_status()
+
+
+@pytest.mark.parametrize("shapes", [((384, 512, 1040), (1040, 784, 400)),
+                                    ((128, 256, 128), (400, 272, 48)),
+                                    ((8192, 4096, 512), (4096, 1024, 8192))])
+def test_grouped_launch_matches_oracle(shapes):
+    """Two independent GEMMs in one launch (as the backward pass runs dgrad and
+    wgrad): each result matches its own oracle product, each amax its output."""
+    f = _lib()
+    probs, refs = [], []
+    for i, ((M, N, K), (fa, fb)) in enumerate(zip(shapes, [(o.E5M2, o.E4M3), (o.E4M3, o.E5M2)])):
+        A = _codes((M, K), fa, 300.0 if fa == o.E5M2 else 3.0, 11 * M + K + i)
+        B = _codes((N, K), fb, 1.0, 13 * N + K + i)
+        sa, sb = np.float32(0.011 * (i + 1)), np.float32(0.5)
+        D = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+        am = torch.full((1,), -1.0, device="cuda")
+        probs.append((torch.from_numpy(A).cuda(), fa, torch.from_numpy(B).cuda(), fb,
+                      torch.tensor([sa], device="cuda"), torch.tensor([sb], device="cuda"), D, am))
+        if M > 1024:   # sampled rows of the big ones
+            rows = [(0, 16), (M // 2, 16), (M - 16, 16)]
+            refs.append((K, [(r0, o.epilogue(o.gemm_tn(A, fa, B, fb, r0, n), sa, sb))
+                             for r0, n in rows]))
+        else:
+            refs.append((K, [(0, o.epilogue(o.gemm_tn(A, fa, B, fb), sa, sb))]))
+    f.fp8_gemm_tn_grouped(probs)
+    f.fp8_sync_status()
+    for (A, fa, B, fb, sa, sb, D, am), (K, blocks) in zip(probs, refs):
+        got = host_bf16_bits(D)
+        for r0, ref in blocks:
+            assert_gemm_close(got[r0:r0 + ref.shape[0]], ref, K, f"{tuple(D.shape)} rows {r0}")
+        full_max = np.float32(np.max(np.abs(bf16_values(got))))
+        assert f32_bits(np.float32(am.item())) == f32_bits(full_max)

@@ -175,6 +175,14 @@ def test_ragged_layer_shape():
     run_layer(w, 3, full=True)
 
 
+@pytest.mark.parametrize("M,K,N", [(128, 400, 272), (16, 48, 32), (512, 16, 1040)])
+def test_small_and_thin_layer_shapes(M, K, N):
+    """Shapes where some GEMMs fit one 128-row tile (single-CTA variant, also
+    inside the grouped backward launch), K = 16, and tiny layers."""
+    w = wl.Workload("thin", M, K, N, "normal", 1.0, 0.05, 0.01, 8, 0, True, 2)
+    run_layer(w, 2, full=True)
+
+
 def test_just_in_time_scaling_tiny_and_drift():
     """Just-in-time scaling: X, W and dY are cast with scales from their own
     amax in the same step (including the all-zero and x1000 steps)."""
@@ -187,3 +195,25 @@ def test_just_in_time_scaling_tiny_and_drift():
 
 def test_just_in_time_scaling_mlp7b_full_size():
     run_layer(wl.WORKLOADS["mlp7b"], 2, full=False, current=True)
+
+
+def test_graph_replay_matches_eager_steps():
+    """A captured step replays exactly what eager steps compute: two layers
+    from the same state, one stepping eagerly, one through graph replays, stay
+    bit-identical (outputs and scaling state) over several steps."""
+    f = _lib()
+    w = wl.Workload("graph", 384, 512, 272, "normal", 1.0, 0.05, 1e-2, 16, 0, True, 4)
+    W = wl.layer_weight(w, "cuda")
+    X, dY = wl.layer_x(w, 0, "cuda"), wl.layer_dy(w, 0, "cuda")
+    a = f.Fp8Linear(W, w.M, f.Recipe(w.margin, w.history_len, w.hybrid))
+    b = f.Fp8Linear(W, w.M, f.Recipe(w.margin, w.history_len, w.hybrid))
+    g = b.capture_step(X, dY)      # includes one eager warm-up step
+    a.step(X, dY)
+    for _ in range(4):
+        a.step(X, dY)
+        g.replay()
+        torch.cuda.synchronize()
+        for t1, t2 in [(a.Y, b.Y), (a.dX, b.dX), (a.dW, b.dW), (a.meta.history, b.meta.history),
+                       (a.meta.scale, b.meta.scale), (a.meta.scale_inv, b.meta.scale_inv)]:
+            assert torch.equal(t1.view(torch.uint8), t2.view(torch.uint8))
+    f.fp8_sync_status()
