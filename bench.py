@@ -498,6 +498,32 @@ def run_secondary(f, args, pk):
                            "cast_transpose_gbs": 4 * ne / (tm.mean_ms("cast") / 1e3) / 1e9}
         del x, o8, o8t
     out["cast_sweep"] = sweep
+    # LayerNorm + cast of the 7B layer's X (statistics kernel + fused cast),
+    # against the plain cast of the same tensor; 4 B/element algorithmic
+    w7 = wl.WORKLOADS["mlp7b"]
+    X = wl.layer_x(w7, 0, "cuda")
+    g = torch.ones(w7.K, dtype=torch.bfloat16, device="cuda")
+    b = torch.zeros(w7.K, dtype=torch.bfloat16, device="cuda")
+    o8 = torch.empty((w7.M, w7.K), dtype=torch.uint8, device="cuda")
+    o8t = torch.empty((w7.K, w7.M), dtype=torch.uint8, device="cuda")
+    mean = torch.empty(w7.M, device="cuda")
+    rstd = torch.empty(w7.M, device="cuda")
+    sc = torch.ones(1, device="cuda")
+    tm = EventTimer()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    for i in range(23):
+        flush.zero_()
+        tm.time("ln_cast", lambda: f.fp8_layernorm_quantize_transpose(X, g, b, 1e-5, sc, 0, mean,
+                                                                      rstd, o8, o8t))
+        flush.zero_()
+        tm.time("cast", lambda: f.fp8_quantize_transpose(X, sc, 0, o8, o8t))
+    torch.cuda.synchronize()
+    tm.pairs = {k: v[3:] for k, v in tm.pairs.items()}
+    ne = w7.M * w7.K
+    out["layernorm_cast_mlp7b_X"] = {
+        "ln_cast_us": tm.mean_ms("ln_cast") * 1e3, "cast_us": tm.mean_ms("cast") * 1e3,
+        "ln_cast_gbs": 4 * ne / (tm.mean_ms("ln_cast") / 1e3) / 1e9,
+        "note": "4 B/element algorithmic; L2 flushed before each launch"}
     return out
 
 

@@ -85,6 +85,11 @@ def _load() -> ctypes.CDLL:
         "fp8_linear_bwd": ([vp, i64, i64, i64, ctypes.POINTER(fp8_meta),
                             ctypes.POINTER(fp8_recipe), vp, vp, vp, vp, vp, vp, vp],
                            ctypes.c_int),
+        "fp8_layernorm_quantize_transpose": ([vp, vp, vp, i64, i64, ctypes.c_float, vp, i32, vp,
+                                              vp, vp, vp, vp, vp], ctypes.c_int),
+        "fp8_layernorm_linear_fwd": ([vp, vp, vp, ctypes.c_float, vp, i64, i64, i64,
+                                      ctypes.POINTER(fp8_meta), ctypes.POINTER(fp8_recipe), vp, vp,
+                                      vp, vp, vp, vp, vp, vp], ctypes.c_int),
         "fp8_linear_bwd_noalloc": ([vp, i64, i64, i64, ctypes.POINTER(fp8_meta),
                                     ctypes.POINTER(fp8_recipe), vp, vp, vp, vp, vp],
                                    ctypes.c_int),
@@ -310,6 +315,32 @@ def fp8_linear_fwd(X, W, meta: Meta, recipe: Recipe, X8, X8t, W8, W8t, Y, stream
                                _stream(stream)))
 
 
+def fp8_layernorm_quantize_transpose(x, gamma, beta, eps: float, scale, fmt: int, mean, rstd,
+                                     out=None, out_t=None, amax=None, stream=None) -> None:
+    rows, cols = x.shape
+    _check(_lib.fp8_layernorm_quantize_transpose(
+        _ptr(x, torch.bfloat16, "x"), _ptr(gamma, torch.bfloat16, "gamma"),
+        _ptr(beta, torch.bfloat16, "beta"), rows, cols, float(eps),
+        _ptr(scale, torch.float32, "scale"), fmt, _p8(out, "out"), _p8(out_t, "out_t"),
+        _ptr(amax, torch.float32, "amax"), _ptr(mean, torch.float32, "mean"),
+        _ptr(rstd, torch.float32, "rstd"), _stream(stream)))
+
+
+def fp8_layernorm_linear_fwd(X, gamma, beta, eps: float, W, meta: "Meta", recipe: "Recipe", X8, X8t,
+                             W8, W8t, Y, mean, rstd, stream=None) -> None:
+    M, K = X.shape
+    N, K2 = W.shape
+    if K != K2 or tuple(Y.shape) != (M, N):
+        raise ValueError("shapes: X [M,K], W [N,K], Y [M,N]")
+    m, r = meta.c(), recipe.c()
+    _check(_lib.fp8_layernorm_linear_fwd(
+        _ptr(X, torch.bfloat16, "X"), _ptr(gamma, torch.bfloat16, "gamma"),
+        _ptr(beta, torch.bfloat16, "beta"), float(eps), _ptr(W, torch.bfloat16, "W"), M, N, K,
+        ctypes.byref(m), ctypes.byref(r), _p8(X8, "X8"), _p8(X8t, "X8t"), _p8(W8, "W8"),
+        _p8(W8t, "W8t"), _ptr(Y, torch.bfloat16, "Y"), _ptr(mean, torch.float32, "mean"),
+        _ptr(rstd, torch.float32, "rstd"), _stream(stream)))
+
+
 def fp8_linear_bwd(dY, meta: Meta, recipe: Recipe, X8t, W8t, dY8, dY8t, dX, dW,
                    stream=None) -> None:
     M, N = dY.shape
@@ -420,3 +451,24 @@ def allreduce_amax(meta: Meta, group=None) -> None:
     result is bit-identical on every rank).  Uses torch.distributed."""
     import torch.distributed as dist
     dist.all_reduce(meta.amax, op=dist.ReduceOp.MAX, group=group)
+
+
+class Fp8LayerNormLinear(Fp8Linear):
+    """LayerNorm in front of an FP8 linear (te.LayerNormLinear): the forward
+    normalises X with gamma / beta and casts the result straight to E4M3
+    (fp8_layernorm_linear_fwd); the backward is the linear's, on that FP8
+    LayerNorm output.  mean / rstd are kept for a LayerNorm backward."""
+
+    def __init__(self, W: torch.Tensor, M: int, gamma: torch.Tensor, beta: torch.Tensor,
+                 eps: float = 1e-5, recipe: Recipe | None = None):
+        super().__init__(W, M, recipe)
+        self.gamma, self.beta, self.eps = gamma, beta, eps
+        self.mean = torch.empty(M, dtype=torch.float32, device=W.device)
+        self.rstd = torch.empty(M, dtype=torch.float32, device=W.device)
+
+    def forward(self, X: torch.Tensor, stream=None, Y: torch.Tensor | None = None) -> torch.Tensor:
+        Y = self.Y if Y is None else Y
+        fp8_layernorm_linear_fwd(X, self.gamma, self.beta, self.eps, self.W, self.meta,
+                                 self.recipe, self.X8, self.X8t, self.W8, self.W8t, Y, self.mean,
+                                 self.rstd, stream)
+        return Y

@@ -316,7 +316,7 @@ fp8_status fp8_quantize_transpose_grouped(const fp8_cast_desc *descs, int32_t n,
         FP8_TRY(check_ptr(fn, d.out_t, "out_t", true));
         FP8_TRY(check_scalar(fn, d.amax, "amax", true));
         c[i] = fp8k::CastSpec{d.x, d.rows, d.cols, const_cast<float *>(d.scale), nullptr, d.out,
-                              d.out_t, d.amax, true};
+                              d.out_t, d.amax, true, nullptr, nullptr, nullptr, nullptr};
     }
     int sms;
     FP8_TRY(current_device(&sms));
@@ -325,10 +325,72 @@ fp8_status fp8_quantize_transpose_grouped(const fp8_cast_desc *descs, int32_t n,
     return FP8_OK;
 }
 
+fp8_status fp8_layernorm_quantize_transpose(const void *x, const void *gamma, const void *beta,
+                                            int64_t rows, int64_t cols, float eps,
+                                            const float *scale, int32_t fmt, uint8_t *out,
+                                            uint8_t *out_t, float *amax, float *mean, float *rstd,
+                                            void *stream) {
+    const char *fn = "fp8_layernorm_quantize_transpose";
+    FP8_TRY(check_dims16(fn, rows, "rows", cols, "cols"));
+    if (cols < 16) return fail(FP8_ERR_ARG, "%s: cols must be >= 16", fn);
+    if (fmt != FP8_E4M3 && fmt != FP8_E5M2) return fail(FP8_ERR_ARG, "%s: bad format %d", fn, fmt);
+    if (!(eps >= 0.0f)) return fail(FP8_ERR_ARG, "%s: eps must be >= 0", fn);
+    const bool empty = rows == 0;
+    if (!empty && out == nullptr && out_t == nullptr)
+        return fail(FP8_ERR_ARG, "%s: out and out_t are both NULL", fn);
+    FP8_TRY(check_ptr(fn, x, "x", empty));
+    FP8_TRY(check_ptr(fn, gamma, "gamma", false));
+    FP8_TRY(check_ptr(fn, beta, "beta", false));
+    FP8_TRY(check_scalar(fn, scale, "scale", false));
+    FP8_TRY(check_ptr(fn, out, "out", true));
+    FP8_TRY(check_ptr(fn, out_t, "out_t", true));
+    FP8_TRY(check_scalar(fn, amax, "amax", true));
+    FP8_TRY(check_scalar(fn, mean, "mean", empty));
+    FP8_TRY(check_scalar(fn, rstd, "rstd", empty));
+    int sms;
+    FP8_TRY(current_device(&sms));
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    FP8_CUDA(fp8k::launch_ln_stats(x, gamma, beta, rows, cols, eps, mean, rstd, nullptr, sms, st),
+             fn);
+    const fp8k::CastSpec c{x, rows, cols, const_cast<float *>(scale), nullptr, out, out_t, amax,
+                           true, mean, rstd, gamma, beta};
+    FP8_CUDA(fp8k::launch_cast_group(&c, 1, fmt, false, 0, sms, st), fn);
+    return FP8_OK;
+}
+
+static fp8_status linear_fwd_impl(const char *fn, const void *X, const void *gamma,
+                                  const void *beta, float eps, const void *W, int64_t M, int64_t N,
+                                  int64_t K, const fp8_meta *meta, const fp8_recipe *recipe,
+                                  uint8_t *X8, uint8_t *X8t, uint8_t *W8, uint8_t *W8t, void *Y,
+                                  float *mean, float *rstd, void *stream);
+
+fp8_status fp8_layernorm_linear_fwd(const void *X, const void *gamma, const void *beta, float eps,
+                                    const void *W, int64_t M, int64_t N, int64_t K,
+                                    const fp8_meta *meta, const fp8_recipe *recipe, uint8_t *X8,
+                                    uint8_t *X8t, uint8_t *W8, uint8_t *W8t, void *Y, float *mean,
+                                    float *rstd, void *stream) {
+    const char *fn = "fp8_layernorm_linear_fwd";
+    FP8_TRY(check_ptr(fn, gamma, "gamma", false));
+    FP8_TRY(check_ptr(fn, beta, "beta", false));
+    FP8_TRY(check_scalar(fn, mean, "mean", false));
+    FP8_TRY(check_scalar(fn, rstd, "rstd", false));
+    if (!(eps >= 0.0f)) return fail(FP8_ERR_ARG, "%s: eps must be >= 0", fn);
+    return linear_fwd_impl(fn, X, gamma, beta, eps, W, M, N, K, meta, recipe, X8, X8t, W8, W8t, Y,
+                           mean, rstd, stream);
+}
+
 fp8_status fp8_linear_fwd(const void *X, const void *W, int64_t M, int64_t N, int64_t K,
                           const fp8_meta *meta, const fp8_recipe *recipe, uint8_t *X8,
                           uint8_t *X8t, uint8_t *W8, uint8_t *W8t, void *Y, void *stream) {
-    const char *fn = "fp8_linear_fwd";
+    return linear_fwd_impl("fp8_linear_fwd", X, nullptr, nullptr, 0.0f, W, M, N, K, meta, recipe,
+                           X8, X8t, W8, W8t, Y, nullptr, nullptr, stream);
+}
+
+static fp8_status linear_fwd_impl(const char *fn, const void *X, const void *gamma,
+                                  const void *beta, float eps, const void *W, int64_t M, int64_t N,
+                                  int64_t K, const fp8_meta *meta, const fp8_recipe *recipe,
+                                  uint8_t *X8, uint8_t *X8t, uint8_t *W8, uint8_t *W8t, void *Y,
+                                  float *mean, float *rstd, void *stream) {
     FP8_TRY(check_meta(fn, meta, recipe));
     FP8_TRY(check_dims16(fn, M, "M", N, "N"));
     FP8_TRY(check_dims16(fn, K, "K", 16, "-"));
@@ -346,15 +408,18 @@ fp8_status fp8_linear_fwd(const void *X, const void *W, int64_t M, int64_t N, in
     float *am = meta->amax;
     // amax of X, W and Y are max-combined into slots cleared here.
     FP8_CUDA(cudaMemsetAsync(am + FP8_SLOT_X, 0, 3 * sizeof(float), st), fn);
-    // X and W (both E4M3) in one cast launch
+    const bool cur = recipe->scaling == FP8_SCALING_CURRENT;
+    if (mean != nullptr)   // LayerNorm statistics (and, for current scaling, amax of LN(X))
+        FP8_CUDA(fp8k::launch_ln_stats(X, gamma, beta, M, K, eps, mean, rstd,
+                                       cur ? am + FP8_SLOT_X : nullptr, sms, st),
+                 fn);
+    // X (or LN(X)) and W (both E4M3) in one cast launch
     const fp8k::CastSpec c[2] = {
         {X, M, K, meta->scale + FP8_SLOT_X, meta->scale_inv + FP8_SLOT_X, X8, X8t,
-         am + FP8_SLOT_X, false},
+         am + FP8_SLOT_X, false, mean, rstd, gamma, beta},
         {W, N, K, meta->scale + FP8_SLOT_W, meta->scale_inv + FP8_SLOT_W, W8, W8t,
-         am + FP8_SLOT_W, false}};
-    FP8_CUDA(fp8k::launch_cast_group(c, 2, FP8_E4M3, recipe->scaling == FP8_SCALING_CURRENT,
-                                     recipe->margin, sms, st),
-             fn);
+         am + FP8_SLOT_W, false, nullptr, nullptr, nullptr, nullptr}};
+    FP8_CUDA(fp8k::launch_cast_group(c, 2, FP8_E4M3, cur, recipe->margin, sms, st), fn);
     return gemm_checked(fn, X8, FP8_E4M3, W8, FP8_E4M3, M, N, K, meta->scale_inv + FP8_SLOT_X,
                         meta->scale_inv + FP8_SLOT_W, Y, am + FP8_SLOT_Y, false, sms, st);
 }

@@ -124,6 +124,11 @@ struct CastTensor {
     const float *amax_in;    // just-in-time mode: this tensor's amax
     uint8_t *out, *out_t;    // row-major and transposed FP8 outputs (either may be null)
     unsigned *amax_bits;     // fused amax output (max-combined), or null
+    // LayerNorm in front of the cast (null = plain cast): per-row mean and
+    // rstd (fp32), per-column gamma and beta (BF16).  The cast then takes
+    // y = ((x - mean) * rstd) * gamma + beta, and the amax is of y.
+    const float *ln_mean, *ln_rstd;
+    const uint16_t *ln_gamma, *ln_beta;
 };
 
 struct CastArgs {
@@ -222,25 +227,83 @@ __global__ void __launch_bounds__(kQtThreads, 2)
             v[i] = *reinterpret_cast<const uint4 *>(xs + (idx >> 4) * kQtTile + (idx & 15) * 8);
         }
         uint32_t m = 0;
+        if (T.ln_mean == nullptr) {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const int idx = i * kQtThreads + tid;
-            const int rr = idx >> 4, vv = idx & 15;
-            const int64_t r = r0 + rr, c = c0 + vv * 8;
-            m = amax_bits2(m, v[i].x);
-            m = amax_bits2(m, v[i].y);
-            m = amax_bits2(m, v[i].z);
-            m = amax_bits2(m, v[i].w);
-            uint2 q;
-            q.x = cvt2_fp8<FMT>(__fmul_rn(bf16_lo(v[i].x), s), __fmul_rn(bf16_hi(v[i].x), s)) |
-                  (cvt2_fp8<FMT>(__fmul_rn(bf16_lo(v[i].y), s), __fmul_rn(bf16_hi(v[i].y), s))
-                   << 16);
-            q.y = cvt2_fp8<FMT>(__fmul_rn(bf16_lo(v[i].z), s), __fmul_rn(bf16_hi(v[i].z), s)) |
-                  (cvt2_fp8<FMT>(__fmul_rn(bf16_lo(v[i].w), s), __fmul_rn(bf16_hi(v[i].w), s))
-                   << 16);
-            if (T.out != nullptr && r < rows && c < cols)
-                *reinterpret_cast<uint2 *>(T.out + r * cols + c) = q;
-            *reinterpret_cast<uint2 *>(&tile[rr * 32 + ((vv * 2) ^ qt_swz(rr))]) = q;
+            for (int i = 0; i < 8; ++i) {
+                const int idx = i * kQtThreads + tid;
+                const int rr = idx >> 4, vv = idx & 15;
+                const int64_t r = r0 + rr, c = c0 + vv * 8;
+                m = amax_bits2(m, v[i].x);
+                m = amax_bits2(m, v[i].y);
+                m = amax_bits2(m, v[i].z);
+                m = amax_bits2(m, v[i].w);
+                uint2 q;
+                q.x = cvt2_fp8<FMT>(__fmul_rn(bf16_lo(v[i].x), s), __fmul_rn(bf16_hi(v[i].x), s)) |
+                      (cvt2_fp8<FMT>(__fmul_rn(bf16_lo(v[i].y), s), __fmul_rn(bf16_hi(v[i].y), s))
+                       << 16);
+                q.y = cvt2_fp8<FMT>(__fmul_rn(bf16_lo(v[i].z), s), __fmul_rn(bf16_hi(v[i].z), s)) |
+                      (cvt2_fp8<FMT>(__fmul_rn(bf16_lo(v[i].w), s), __fmul_rn(bf16_hi(v[i].w), s))
+                       << 16);
+                if (T.out != nullptr && r < rows && c < cols)
+                    *reinterpret_cast<uint2 *>(T.out + r * cols + c) = q;
+                *reinterpret_cast<uint2 *>(&tile[rr * 32 + ((vv * 2) ^ qt_swz(rr))]) = q;
+            }
+            m <<= 16;   // BF16 magnitude bits -> fp32 bits
+        } else {
+            // LayerNorm first: y = ((x - mean) * rstd) * gamma + beta in fp32.
+            // This thread's 8 columns are the same for all 8 of its vectors.
+            const int vv = tid & 15;
+            const int64_t c = c0 + vv * 8;
+            float gam[8], bet[8];
+            if (c < cols) {
+                const uint4 g4 = *reinterpret_cast<const uint4 *>(T.ln_gamma + c);
+                const uint4 b4 = *reinterpret_cast<const uint4 *>(T.ln_beta + c);
+                const uint32_t gw[4] = {g4.x, g4.y, g4.z, g4.w}, bw[4] = {b4.x, b4.y, b4.z, b4.w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    gam[2 * j] = bf16_lo(gw[j]);
+                    gam[2 * j + 1] = bf16_hi(gw[j]);
+                    bet[2 * j] = bf16_lo(bw[j]);
+                    bet[2 * j + 1] = bf16_hi(bw[j]);
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) gam[j] = bet[j] = 0.0f;
+            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int rr = (i * kQtThreads + tid) >> 4;
+                const int64_t r = r0 + rr;
+                const bool in = r < rows && c < cols;
+                const float mu = in ? T.ln_mean[r] : 0.0f;
+                const float rs = in ? T.ln_rstd[r] : 0.0f;
+                const uint32_t xw[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+                float yv[8];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const float x0 = bf16_lo(xw[j]), x1 = bf16_hi(xw[j]);
+                    yv[2 * j] = __fadd_rn(__fmul_rn(__fmul_rn(__fsub_rn(x0, mu), rs), gam[2 * j]),
+                                          bet[2 * j]);
+                    yv[2 * j + 1] = __fadd_rn(
+                        __fmul_rn(__fmul_rn(__fsub_rn(x1, mu), rs), gam[2 * j + 1]), bet[2 * j + 1]);
+                }
+                uint32_t qw[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    if (in) {
+                        const uint32_t a0 = __float_as_uint(yv[2 * j]) & 0x7FFFFFFFu;
+                        const uint32_t a1 = __float_as_uint(yv[2 * j + 1]) & 0x7FFFFFFFu;
+                        m = max(m, a0 > 0x7F800000u ? 0u : a0);
+                        m = max(m, a1 > 0x7F800000u ? 0u : a1);
+                    }
+                    qw[j] = cvt2_fp8<FMT>(__fmul_rn(yv[2 * j], s), __fmul_rn(yv[2 * j + 1], s));
+                }
+                uint2 q;
+                q.x = qw[0] | (qw[1] << 16);
+                q.y = qw[2] | (qw[3] << 16);
+                if (T.out != nullptr && in) *reinterpret_cast<uint2 *>(T.out + r * cols + c) = q;
+                *reinterpret_cast<uint2 *>(&tile[rr * 32 + ((vv * 2) ^ qt_swz(rr))]) = q;
+            }
         }
         if (p)
             tmax[1] = max(tmax[1], m);
@@ -301,9 +364,126 @@ __global__ void __launch_bounds__(kQtThreads, 2)
             uint32_t m = tid < kQtThreads / 32 ? warp_max[i][tid] : 0u;
             m = __reduce_max_sync(0xFFFFFFFFu, m);
             if (tid == 0 && m != 0 && i < a.num_tensors && a.t[i].amax_bits != nullptr)
-                atomicMax(a.t[i].amax_bits, m << 16);
+                atomicMax(a.t[i].amax_bits, m);   // fp32 bits of a value >= 0
         }
     }
+}
+
+// ------------------------------------------------------ LayerNorm row stats --
+//
+// One warp per row (grid-stride over rows): mean = sum(x) / C, then
+// var = sum((x - mean)^2) / C over a second read of the row (from L1 / L2),
+// rstd = 1 / sqrt(var + eps), all in fp32 with correctly rounded operations.
+// With amax_bits, a third read computes y = ((x - mean) * rstd) * gamma + beta
+// and max-combines max |y| (for just-in-time scaling of the LayerNorm output).
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) v = __fadd_rn(v, __shfl_xor_sync(0xFFFFFFFFu, v, off));
+    return v;
+}
+
+__global__ void __launch_bounds__(256) ln_stats_kernel(const uint16_t *__restrict__ x,
+                                                       const uint16_t *__restrict__ gamma,
+                                                       const uint16_t *__restrict__ beta,
+                                                       int64_t rows, int64_t cols, float eps,
+                                                       float *__restrict__ mean,
+                                                       float *__restrict__ rstd,
+                                                       unsigned *__restrict__ amax_bits) {
+    const int lane = threadIdx.x & 31;
+    const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+    const int64_t nvec = cols / 8;
+    const float inv_c = __fdiv_rn(1.0f, static_cast<float>(cols));
+    uint32_t m = 0;
+    for (int64_t r = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; r < rows;
+         r += warps) {
+        const uint4 *xr = reinterpret_cast<const uint4 *>(x + r * cols);
+        // four 16-byte loads in flight per lane in both passes
+        float sum = 0.0f;
+        for (int64_t i = lane; i < nvec; i += 128) {
+            uint4 v[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                v[u] = i + 32 * u < nvec ? xr[i + 32 * u] : make_uint4(0, 0, 0, 0);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    sum = __fadd_rn(__fadd_rn(sum, bf16_lo(w[j])), bf16_hi(w[j]));
+            }
+        }
+        const float mu = __fmul_rn(warp_sum(sum), inv_c);
+        float sq = 0.0f;
+        for (int64_t i = lane; i < nvec; i += 128) {
+            uint4 v[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                v[u] = i + 32 * u < nvec ? xr[i + 32 * u] : make_uint4(0, 0, 0, 0);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                if (i + 32 * u >= nvec) break;
+                const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const float d0 = __fsub_rn(bf16_lo(w[j]), mu);
+                    const float d1 = __fsub_rn(bf16_hi(w[j]), mu);
+                    sq = __fadd_rn(__fadd_rn(sq, __fmul_rn(d0, d0)), __fmul_rn(d1, d1));
+                }
+            }
+        }
+        const float var = __fmul_rn(warp_sum(sq), inv_c);
+        const float rs = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(var, eps)));
+        if (lane == 0) {
+            mean[r] = mu;
+            rstd[r] = rs;
+        }
+        if (amax_bits != nullptr) {
+            for (int64_t i = lane; i < nvec; i += 32) {
+                const uint4 v = xr[i];
+                const uint4 g4 = reinterpret_cast<const uint4 *>(gamma)[i];
+                const uint4 b4 = reinterpret_cast<const uint4 *>(beta)[i];
+                const uint32_t w[4] = {v.x, v.y, v.z, v.w}, gw[4] = {g4.x, g4.y, g4.z, g4.w},
+                               bw[4] = {b4.x, b4.y, b4.z, b4.w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const float y0 = __fadd_rn(
+                        __fmul_rn(__fmul_rn(__fsub_rn(bf16_lo(w[j]), mu), rs), bf16_lo(gw[j])),
+                        bf16_lo(bw[j]));
+                    const float y1 = __fadd_rn(
+                        __fmul_rn(__fmul_rn(__fsub_rn(bf16_hi(w[j]), mu), rs), bf16_hi(gw[j])),
+                        bf16_hi(bw[j]));
+                    const uint32_t a0 = __float_as_uint(y0) & 0x7FFFFFFFu;
+                    const uint32_t a1 = __float_as_uint(y1) & 0x7FFFFFFFu;
+                    m = max(m, a0 > 0x7F800000u ? 0u : a0);
+                    m = max(m, a1 > 0x7F800000u ? 0u : a1);
+                }
+            }
+        }
+    }
+    if (amax_bits != nullptr) {
+        m = __reduce_max_sync(0xFFFFFFFFu, m);
+        if (lane == 0 && m != 0) atomicMax(amax_bits, m);
+    }
+}
+
+cudaError_t launch_ln_stats(const void *x, const void *gamma, const void *beta, int64_t rows,
+                            int64_t cols, float eps, float *mean, float *rstd, float *amax,
+                            int sm_count, cudaStream_t st) {
+    if (amax != nullptr) {
+        cudaError_t e = cudaMemsetAsync(amax, 0, sizeof(float), st);
+        if (e != cudaSuccess) return e;
+    }
+    if (rows == 0) return cudaSuccess;
+    const int threads = 256;
+    int64_t blocks = (rows + 7) / 8;
+    const int64_t cap = static_cast<int64_t>(sm_count) * 8;
+    if (blocks > cap) blocks = cap;
+    ln_stats_kernel<<<static_cast<unsigned>(blocks), threads, 0, st>>>(
+        reinterpret_cast<const uint16_t *>(x), reinterpret_cast<const uint16_t *>(gamma),
+        reinterpret_cast<const uint16_t *>(beta), rows, cols, eps, mean, rstd,
+        reinterpret_cast<unsigned *>(amax));
+    return cudaGetLastError();
 }
 
 // ----------------------------------------------------------- scale update --
@@ -400,6 +580,10 @@ static bool cast_args(CastArgs &args, const CastSpec *specs, int n, int margin) 
         t.out = c.out;
         t.out_t = c.out_t;
         t.amax_bits = reinterpret_cast<unsigned *>(c.amax);
+        t.ln_mean = c.ln_mean;
+        t.ln_rstd = c.ln_rstd;
+        t.ln_gamma = reinterpret_cast<const uint16_t *>(c.ln_gamma);
+        t.ln_beta = reinterpret_cast<const uint16_t *>(c.ln_beta);
         if (c.rows > 0 && c.cols > 0) {
             if (!encode_tmap_2d(&args.maps[i], c.x, true, c.cols, c.rows, kQtTile, kQtTile, false))
                 return false;
@@ -420,7 +604,9 @@ cudaError_t launch_cast_group(const CastSpec *specs, int n, int fmt, bool curren
                               int sm_count, cudaStream_t st) {
     if (n < 1 || n > 2) return cudaErrorInvalidValue;
     for (int i = 0; i < n; ++i) {
-        if (current) {
+        if (current && specs[i].ln_mean != nullptr) {
+            // the LayerNorm statistics kernel has already written amax(y)
+        } else if (current) {
             cudaError_t e = launch_amax(specs[i].x, specs[i].rows * specs[i].cols, specs[i].amax,
                                         sm_count, st);
             if (e != cudaSuccess) return e;
@@ -445,7 +631,8 @@ cudaError_t launch_quantize_transpose(const void *x, int64_t rows, int64_t cols,
                                       const float *scale, int fmt, uint8_t *out, uint8_t *out_t,
                                       float *amax, bool zero_amax, int sm_count,
                                       cudaStream_t st) {
-    CastSpec c{x, rows, cols, const_cast<float *>(scale), nullptr, out, out_t, amax, zero_amax};
+    CastSpec c{x, rows, cols, const_cast<float *>(scale), nullptr, out, out_t, amax, zero_amax,
+               nullptr, nullptr, nullptr, nullptr};
     return launch_cast_group(&c, 1, fmt, false, 0, sm_count, st);
 }
 
@@ -453,7 +640,8 @@ cudaError_t launch_quantize_transpose_current(const void *x, int64_t rows, int64
                                               int margin, uint8_t *out, uint8_t *out_t,
                                               float *amax, float *scale, float *scale_inv,
                                               int sm_count, cudaStream_t st) {
-    CastSpec c{x, rows, cols, scale, scale_inv, out, out_t, amax, true};
+    CastSpec c{x, rows, cols, scale, scale_inv, out, out_t, amax, true,
+               nullptr, nullptr, nullptr, nullptr};
     return launch_cast_group(&c, 1, fmt, true, margin, sm_count, st);
 }
 

@@ -38,7 +38,17 @@ struct CastSpec {
     uint8_t *out, *out_t;
     float *amax;
     bool zero_amax;
+    // LayerNorm in front of the cast (all null for a plain cast): per-row
+    // mean / rstd from launch_ln_stats, per-column gamma / beta (BF16).
+    const float *ln_mean, *ln_rstd;
+    const void *ln_gamma, *ln_beta;
 };
+
+// LayerNorm statistics of x [rows][cols] (BF16): fp32 mean and rstd per row;
+// with amax, also max |y| of the LayerNorm output (cleared first).
+cudaError_t launch_ln_stats(const void *x, const void *gamma, const void *beta, int64_t rows,
+                            int64_t cols, float eps, float *mean, float *rstd, float *amax,
+                            int sm_count, cudaStream_t st);
 
 // Up to two tensors of one format in one persistent cast launch (tiles form
 // one list).  current = just-in-time scaling (an amax pass per tensor first).

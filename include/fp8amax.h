@@ -230,6 +230,37 @@ typedef struct {
 fp8_status fp8_quantize_transpose_grouped(const fp8_cast_desc *descs, int32_t n, int32_t fmt,
                                           void *stream);
 
+/* LayerNorm fused with the scaled cast (te.LayerNorm in front of an FP8
+ * linear; implementation guide, "Basic structure of FP8 training code"):
+ *   mean[r] = sum_c x[r][c] / C,  var[r] = sum_c (x[r][c] - mean[r])^2 / C,
+ *   rstd[r] = 1 / sqrt(var[r] + eps),
+ *   y[r][c] = ((x[r][c] - mean[r]) * rstd[r]) * gamma[c] + beta[c]   (fp32),
+ * then the cast of y exactly as fp8_quantize_transpose casts x (y is never
+ * written out in BF16).  Two kernels: row statistics, then LayerNorm + cast.
+ *   x      DEVICE [rows][cols] BF16;  gamma, beta  DEVICE [cols] BF16
+ *   eps    >= 0;  scale  DEVICE, 1 float;  fmt, out, out_t as fp8_quantize_transpose
+ *   amax   DEVICE, 1 float overwritten with max |y| (fp32 y, NaN skipped), or NULL
+ *   mean, rstd  DEVICE [rows] fp32 outputs (kept for the LayerNorm backward)
+ * rows, cols multiples of 16, cols >= 16.  Sums run in fp32 in a different
+ * order from a sequential sum, so y matches an exact evaluation to about
+ * 1e-6 relative, not bit for bit. */
+fp8_status fp8_layernorm_quantize_transpose(const void *x, const void *gamma, const void *beta,
+                                            int64_t rows, int64_t cols, float eps,
+                                            const float *scale, int32_t fmt, uint8_t *out,
+                                            uint8_t *out_t, float *amax, float *mean, float *rstd,
+                                            void *stream);
+
+/* Forward of LayerNorm + FP8 linear (te.LayerNormLinear): Y = LN(X) W^T with
+ * LN(X) cast to E4M3 by the fused kernel above (its amax is slot X's), W cast
+ * as in fp8_linear_fwd, then fprop.  Arguments as fp8_linear_fwd plus gamma,
+ * beta [K] (BF16), eps, and mean, rstd [M] (fp32 outputs).  X8 / X8t hold the
+ * FP8 LayerNorm output, so fp8_linear_bwd follows unchanged. */
+fp8_status fp8_layernorm_linear_fwd(const void *X, const void *gamma, const void *beta, float eps,
+                                    const void *W, int64_t M, int64_t N, int64_t K,
+                                    const fp8_meta *meta, const fp8_recipe *recipe, uint8_t *X8,
+                                    uint8_t *X8t, uint8_t *W8, uint8_t *W8t, void *Y, float *mean,
+                                    float *rstd, void *stream);
+
 /* Forward of the FP8 linear layer Y = X W^T (te.Linear under fp8_autocast,
  * implementation guide "Basic structure of FP8 training code" and the
  * recipe section).  Uses this step's (delayed) scales of X and W, or under

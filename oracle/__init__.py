@@ -22,6 +22,8 @@ What each function follows:
 * ``just_in_time_scale`` -- just-in-time per-tensor scaling (wiki note,
   bullet "per-tensor scaling is the key"): the same formula on this step's
   amax alone.
+* ``layernorm`` -- te.LayerNorm's forward (implementation guide, "Basic
+  structure of FP8 training code"), in double.
 * ``layer_fwd`` / ``layer_bwd`` -- te.Linear inside fp8_autocast with
   Format.HYBRID (E4M3 forward, E5M2 backward; same section) and FP8 GEMMs with
   higher-precision accumulation (wiki note, bullet "extension to FP8").
@@ -90,6 +92,8 @@ def _lib():
         lib.or_epilogue.argtypes = [vp, i64, f32, f32, vp]
         lib.or_epilogue.restype = None
         lib.or_num_threads.argtypes, lib.or_num_threads.restype = [], ctypes.c_int
+        lib.or_layernorm.argtypes = [vp, vp, vp, i64, i64, ctypes.c_double, vp, vp, vp]
+        lib.or_layernorm.restype = None
         _lib_handle = lib
     return _lib_handle
 
@@ -212,6 +216,23 @@ def epilogue(acc: np.ndarray, sa_inv, sb_inv) -> np.ndarray:
     _lib().or_epilogue(a.ctypes.data, a.size, float(np.float32(sa_inv)),
                        float(np.float32(sb_inv)), y.ctypes.data)
     return y
+
+
+# ------------------------------------------------------------- LayerNorm --
+
+def layernorm(x_bf16: np.ndarray, gamma_bf16: np.ndarray, beta_bf16: np.ndarray, eps: float):
+    """te.LayerNorm's forward (implementation guide, "Basic structure of FP8
+    training code") in double: returns y [rows, cols], mean [rows], rstd [rows]."""
+    x = _c(x_bf16, np.uint16)
+    g = _c(gamma_bf16, np.uint16)
+    b = _c(beta_bf16, np.uint16)
+    rows, cols = x.shape
+    y = np.empty((rows, cols), np.float64)
+    mean = np.empty(rows, np.float64)
+    rstd = np.empty(rows, np.float64)
+    _lib().or_layernorm(x.ctypes.data, g.ctypes.data, b.ctypes.data, rows, cols, float(eps),
+                        y.ctypes.data, mean.ctypes.data, rstd.ctypes.data)
+    return y, mean, rstd
 
 
 # ------------------------------------------------------------- the layer --

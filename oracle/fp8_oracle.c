@@ -309,3 +309,36 @@ int or_num_threads(void)
     return 1;
 #endif
 }
+
+/* ------------------------------------------------------------------------ */
+/* LayerNorm (the te.LayerNorm drop-in of the implementation guide, section  */
+/* "Basic structure of FP8 training code"), in double:                       */
+/*   mean_r = sum_c x[r][c] / C,  var_r = sum_c (x[r][c] - mean_r)^2 / C,    */
+/*   rstd_r = 1 / sqrt(var_r + eps),                                         */
+/*   y[r][c] = (x[r][c] - mean_r) * rstd_r * gamma[c] + beta[c].             */
+/* ------------------------------------------------------------------------ */
+
+void or_layernorm(const uint16_t *x, const uint16_t *gamma, const uint16_t *beta, int64_t rows,
+                  int64_t cols, double eps, double *y, double *mean, double *rstd)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < rows; ++r) {
+        const uint16_t *xr = x + r * cols;
+        double s = 0.0;
+        for (int64_t c = 0; c < cols; ++c)
+            s += (double)or_bf16_to_f32(xr[c]);
+        double mu = s / (double)cols;
+        double v = 0.0;
+        for (int64_t c = 0; c < cols; ++c) {
+            double d = (double)or_bf16_to_f32(xr[c]) - mu;
+            v += d * d;
+        }
+        v /= (double)cols;
+        double rs = 1.0 / sqrt(v + eps);
+        mean[r] = mu;
+        rstd[r] = rs;
+        for (int64_t c = 0; c < cols; ++c)
+            y[r * cols + c] = ((double)or_bf16_to_f32(xr[c]) - mu) * rs *
+                              (double)or_bf16_to_f32(gamma[c]) + (double)or_bf16_to_f32(beta[c]);
+    }
+}

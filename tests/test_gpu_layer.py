@@ -38,14 +38,15 @@ def _gpu_slot_checks(lin, f, gpu_amax_hist, fmts, margin):
     scale = lin.meta.scale.cpu().numpy()
     for slot, out in ((f.SLOT_Y, lin.Y), (f.SLOT_DX, lin.dX)):
         a = lin.meta.amax[slot].item()
-        mx = np.float32(np.max(np.abs(bf16_values(host_bf16_bits(out)))))
+        vals = np.abs(bf16_values(host_bf16_bits(out)))
+        mx = np.float32(np.nanmax(vals) if not np.isnan(vals).all() else 0.0)   # NaN skipped
         assert f32_bits(np.float32(a)) == f32_bits(mx), (slot, a, mx)
         gpu_amax_hist[slot].insert(0, np.float32(a))
         L = hist.shape[1]
         seq = (gpu_amax_hist[slot] + [np.float32(0)] * L)[:L]
         assert np.array_equal(hist[slot].view(np.uint32), np.array(seq, np.float32).view(np.uint32))
         m = np.float32(max(seq))
-        if m > 0:
+        if 0 < m < np.inf:
             fmax = np.float32(448.0 if fmts[slot] == o.E4M3 else 57344.0)
             expect = np.float32(np.float32(fmax / m) * np.float32(2.0 ** -margin))
             assert f32_bits(scale[slot]) == f32_bits(expect)
@@ -216,4 +217,51 @@ def test_graph_replay_matches_eager_steps():
         for t1, t2 in [(a.Y, b.Y), (a.dX, b.dX), (a.dW, b.dW), (a.meta.history, b.meta.history),
                        (a.meta.scale, b.meta.scale), (a.meta.scale_inv, b.meta.scale_inv)]:
             assert torch.equal(t1.view(torch.uint8), t2.view(torch.uint8))
+    f.fp8_sync_status()
+
+
+def test_special_values_through_the_layer():
+    """Degenerate inputs through whole steps: X holds +-inf, NaN and the
+    largest BF16 values.  The amax of X is inf, so the X history holds inf
+    and X's scale is kept (reading: a non-finite history max keeps the
+    scale); inf and huge values saturate to the largest E4M3 code, NaN stays
+    a NaN code; Y is NaN exactly in the rows (and dW in the columns) a NaN
+    reaches, and the fused output amaxes skip NaN."""
+    f = _lib()
+    w = wl.Workload("special", 144, 272, 256, "normal", 1.0, 0.05, 0.01, 4, 0, True, 3)
+    W = wl.layer_weight(w, "cuda")
+    lin = f.Fp8Linear(W, w.M, f.Recipe(w.margin, w.history_len, w.hybrid))
+    rc = o.Recipe(margin=w.margin, history_len=w.history_len, hybrid=w.hybrid)
+    st = o.State.initial(w.history_len)
+    fm = rc.formats()
+    Wb = host_bf16_bits(W)
+    for step in range(3):
+        X = wl.layer_x(w, step, "cuda").clone()
+        X[3, 5] = float("inf")
+        X[100, 7] = -float("inf")
+        X[17, 200] = float("nan")
+        X[40, :] = 3.3895e38          # near the largest BF16 value
+        dY = wl.layer_dy(w, step, "cuda")
+        lin.step(X, dY)
+        torch.cuda.synchronize()
+        Xb, dYb = host_bf16_bits(X), host_bf16_bits(dY)
+        fo = o.layer_fwd(st, rc, Xb, Wb)
+        bo = o.layer_bwd(st, rc, dYb, fo["X8t"], fo["W8t"])
+        for name, ref, fmt in [("X8", fo["X8"], fm[0]), ("X8t", fo["X8t"], fm[0]),
+                               ("W8", fo["W8"], fm[1]), ("dY8", bo["dY8"], fm[3])]:
+            assert_fp8_equal(host_u8(getattr(lin, name)), ref, fmt, f"step {step} {name}")
+        assert (host_u8(lin.X8)[3, 5] & 0x7F) == 0x7E and (host_u8(lin.X8)[100, 7] == 0xFE)
+        assert (host_u8(lin.X8)[17, 200] & 0x7F) == 0x7F
+        for name, ref, K in [("Y", fo["Y"], w.K), ("dX", bo["dX"], w.N), ("dW", bo["dW"], w.M)]:
+            assert_gemm_close(host_bf16_bits(getattr(lin, name)), ref, K, f"step {step} {name}")
+        y = bf16_values(host_bf16_bits(lin.Y))
+        assert np.isnan(y[17]).all() and not np.isnan(np.delete(y, 17, axis=0)).any()
+        dw = bf16_values(host_bf16_bits(lin.dW))
+        assert np.isnan(dw[:, 200]).all()
+        o.layer_update(st, rc)
+        hist = lin.meta.history.cpu().numpy()
+        for slot in (o.SLOT_X, o.SLOT_W, o.SLOT_DY):
+            assert np.array_equal(hist[slot].view(np.uint32), st.history[slot].view(np.uint32))
+            assert f32_bits(lin.meta.scale[slot].item()) == f32_bits(st.scale[slot])
+        assert hist[o.SLOT_X, 0] == np.inf and lin.meta.scale[o.SLOT_X].item() == 1.0
     f.fp8_sync_status()

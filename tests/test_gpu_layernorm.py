@@ -1,0 +1,103 @@
+"""GPU parity of LayerNorm fused with the scaled cast (te.LayerNorm in front of
+an FP8 linear) against the oracle's double-precision LayerNorm.
+
+The statistics are fp32 sums on the GPU and exact sums in the oracle, so y
+agrees to a few fp32 rounding errors of the terms it combines, not bit for
+bit.  Hence: mean / rstd / amax(y) within 1e-5 relative; every FP8 code is a
+correct cast of some value within that error band around the oracle's exact
+y * s (band = 2^-16 x ((|x| + |mean|) * rstd * |gamma| + |beta|) * s), and
+codes that differ from the cast of the exact value must be rare."""
+import numpy as np
+import pytest
+import torch
+
+import fp8_workloads as wl
+import oracle as o
+from helpers import assert_codes_in_band, assert_gemm_close, bf16_values, host_bf16_bits, host_u8
+
+pytestmark = pytest.mark.gpu
+REL = 2.0 ** -16
+
+
+def _lib():
+    import fp8_mixed_precision_amax_gb300 as f
+    return f
+
+
+def _inputs(rows, cols, seed, mag=1.0):
+    g = torch.Generator().manual_seed(seed)
+    x = (torch.randn(rows, cols, generator=g) * mag * 3 + mag).to(torch.bfloat16)
+    gamma = (1 + 0.2 * torch.randn(cols, generator=g)).to(torch.bfloat16)
+    beta = (0.1 * torch.randn(cols, generator=g)).to(torch.bfloat16)
+    return x.cuda(), gamma.cuda(), beta.cuda()
+
+
+def check_codes(gpu, x, gamma, beta, mean, rstd, y, s, fmt, what):
+    """x, gamma, beta as BF16 bits; mean, rstd, y from the oracle (double)."""
+    xd = bf16_values(x)
+    mag = (np.abs(xd) + np.abs(mean)[:, None]) * rstd[:, None] * np.abs(bf16_values(gamma)) + \
+        np.abs(bf16_values(beta))
+    return assert_codes_in_band(gpu, y * np.float64(s), REL * mag * np.float64(s), fmt, what)
+
+
+@pytest.mark.parametrize("rows,cols", [(16, 16), (144, 272), (1040, 4096), (256, 8192)])
+@pytest.mark.parametrize("fmt", [o.E4M3, o.E5M2])
+def test_layernorm_cast_matches_oracle(rows, cols, fmt):
+    f = _lib()
+    x, gamma, beta = _inputs(rows, cols, rows + cols + fmt)
+    s = np.float32(448.0 / 6.0) if fmt == o.E4M3 else np.float32(57344.0 / 6.0)
+    out = torch.empty((rows, cols), dtype=torch.uint8, device="cuda")
+    out_t = torch.empty((cols, rows), dtype=torch.uint8, device="cuda")
+    am = torch.full((1,), -1.0, device="cuda")
+    mean = torch.empty(rows, device="cuda")
+    rstd = torch.empty(rows, device="cuda")
+    f.fp8_layernorm_quantize_transpose(x, gamma, beta, 1e-5, torch.tensor([s], device="cuda"),
+                                       fmt, mean, rstd, out, out_t, am)
+    torch.cuda.synchronize()
+    xb, gb, bb = host_bf16_bits(x), host_bf16_bits(gamma), host_bf16_bits(beta)
+    y, mu, rs = o.layernorm(xb, gb, bb, 1e-5)
+    assert np.allclose(mean.cpu().numpy(), mu, rtol=1e-5, atol=1e-5 * np.abs(mu).max())
+    assert np.allclose(rstd.cpu().numpy(), rs, rtol=1e-5)
+    assert abs(am.item() - np.abs(y).max()) <= 1e-5 * np.abs(y).max()
+    q = host_u8(out)
+    check_codes(q, xb, gb, bb, mu, rs, y, s, fmt, f"{rows}x{cols} out")
+    assert np.array_equal(host_u8(out_t), q.T)
+
+
+def test_layernorm_linear_step_matches_oracle():
+    """One step of LayerNorm + FP8 linear (te.LayerNormLinear) then the
+    linear's backward, against the oracle: LN(X) codes as above, Y / dX / dW
+    within the GEMM tolerance; a second step under just-in-time scaling."""
+    f = _lib()
+    w = wl.Workload("ln", 1040, 1024, 784, "normal", 1.0, 0.03, 1e-2, 16, 0, True, 2)
+    W = wl.layer_weight(w, "cuda")
+    for current in (False, True):
+        _, gamma, beta = _inputs(16, w.K, 5)
+        lin = f.Fp8LayerNormLinear(W, w.M, gamma, beta, 1e-5,
+                                   f.Recipe(w.margin, w.history_len, w.hybrid, current=current))
+        X, dY = wl.layer_x(w, 0, "cuda"), wl.layer_dy(w, 0, "cuda")
+        lin.forward(X)
+        lin.backward(dY)
+        torch.cuda.synchronize()
+        xb, gb, bb = host_bf16_bits(X), host_bf16_bits(gamma), host_bf16_bits(beta)
+        y, mu, rs = o.layernorm(xb, gb, bb, 1e-5)
+        sx = np.float32(448.0 / np.abs(y).max()) if current else np.float32(1.0)
+        assert abs(lin.meta.scale[o.SLOT_X].item() - sx) <= 1e-5 * sx
+        assert abs(lin.meta.amax[o.SLOT_X].item() - np.abs(y).max()) <= 1e-5 * np.abs(y).max()
+        X8 = host_u8(lin.X8)
+        check_codes(X8, xb, gb, bb, mu, rs, y, lin.meta.scale[o.SLOT_X].item(), o.E4M3,
+                    "LN(X) codes")
+        # the GEMMs from the GPU's own FP8 operands (parity of the GEMM itself is
+        # tested elsewhere); the operands must be the oracle's up to tie codes
+        rc = o.Recipe(w.margin, w.history_len, w.hybrid)
+        fm = rc.formats()
+        W8, W8t = o.quantize(host_bf16_bits(W), np.float32(lin.meta.scale[o.SLOT_W].item()), fm[1])
+        assert np.array_equal(host_u8(lin.W8), W8)
+        si = lin.meta.scale_inv.cpu().numpy()
+        ref = o.epilogue(o.gemm_tn(X8, fm[0], W8, fm[1]), si[0], si[1])
+        assert_gemm_close(host_bf16_bits(lin.Y), ref, w.K, "Y")
+        dY8, dY8t = o.quantize(host_bf16_bits(dY), np.float32(lin.meta.scale[o.SLOT_DY].item()),
+                               fm[3])
+        ref = o.epilogue(o.gemm_tn(dY8t, fm[3], X8.T.copy(), fm[0]), si[3], si[0])
+        assert_gemm_close(host_bf16_bits(lin.dW), ref, w.M, "dW")
+    f.fp8_sync_status()
