@@ -60,6 +60,13 @@ class fp8_cast_desc(ctypes.Structure):
                 ("amax", ctypes.c_void_p)]
 
 
+class fp8_adam_hyper(ctypes.Structure):
+    _fields_ = [("lr", ctypes.c_float), ("beta1", ctypes.c_float), ("beta2", ctypes.c_float),
+                ("eps", ctypes.c_float), ("weight_decay", ctypes.c_float),
+                ("bias_correction1", ctypes.c_float), ("bias_correction2", ctypes.c_float),
+                ("margin", ctypes.c_int32)]
+
+
 def _load() -> ctypes.CDLL:
     if not os.path.exists(LIB_PATH):
         raise ImportError(f"{LIB_PATH} is not built; call fp8_mixed_precision_amax_gb300.build.build()")
@@ -90,6 +97,8 @@ def _load() -> ctypes.CDLL:
         "fp8_layernorm_linear_fwd": ([vp, vp, vp, ctypes.c_float, vp, i64, i64, i64,
                                       ctypes.POINTER(fp8_meta), ctypes.POINTER(fp8_recipe), vp, vp,
                                       vp, vp, vp, vp, vp, vp], ctypes.c_int),
+        "fp8_adam_step": ([vp, i64, vp, vp, vp, vp, vp, vp, vp, vp, vp,
+                           ctypes.POINTER(fp8_adam_hyper), vp], ctypes.c_int),
         "fp8_linear_bwd_noalloc": ([vp, i64, i64, i64, ctypes.POINTER(fp8_meta),
                                     ctypes.POINTER(fp8_recipe), vp, vp, vp, vp, vp],
                                    ctypes.c_int),
@@ -472,3 +481,55 @@ class Fp8LayerNormLinear(Fp8Linear):
                                  self.recipe, self.X8, self.X8t, self.W8, self.W8t, Y, self.mean,
                                  self.rstd, stream)
         return Y
+
+
+@dataclass
+class AdamHyper:
+    """Adam / AdamW hyper-parameters; ``margin`` is the state scales' margin."""
+    lr: float = 1e-3
+    beta1: float = 0.9
+    beta2: float = 0.999
+    eps: float = 1e-8
+    weight_decay: float = 0.0
+    margin: int = 0
+
+    def c(self, t: int) -> fp8_adam_hyper:
+        return fp8_adam_hyper(self.lr, self.beta1, self.beta2, self.eps, self.weight_decay,
+                              1.0 - self.beta1 ** t, 1.0 - self.beta2 ** t, self.margin)
+
+
+class Fp8AdamState:
+    """Decoupled-precision Adam state of one parameter tensor (wiki note,
+    bullet "precision decoupling"): first moment E4M3 with a per-tensor scale,
+    second moment FP16, master weights FP16 with a per-tensor scale -- 5 bytes
+    of state per parameter.  ``scales`` = [m1_scale, m1_scale_inv, w_scale, w_scale_inv]."""
+
+    def __init__(self, w: torch.Tensor):
+        n = w.numel()
+        dev = w.device
+        self.n = n
+        self.m1 = torch.zeros(n, dtype=torch.uint8, device=dev)
+        self.m2 = torch.zeros(n, dtype=torch.float16, device=dev)
+        wf = w.detach().float().reshape(-1)
+        amax = wf.abs().max().item()
+        ws = (65504.0 / amax) if amax > 0 else 1.0
+        self.scales = torch.tensor([1.0, 1.0, ws, 1.0 / ws], dtype=torch.float32, device=dev)
+        self.w16 = (wf * self.scales[2]).clamp(-65504, 65504).to(torch.float16)
+        self.amax = torch.zeros(2, dtype=torch.float32, device=dev)
+        self.t = 0
+
+    def step(self, grad: torch.Tensor, w_bf16: torch.Tensor, hp: AdamHyper, stream=None) -> None:
+        """One step with ``grad`` (BF16, n elements); writes the new weights
+        into ``w_bf16`` (BF16, n elements)."""
+        if grad.numel() != self.n or w_bf16.numel() != self.n:
+            raise ValueError("grad and w_bf16 must have the state's number of elements")
+        self.t += 1
+        h = hp.c(self.t)
+        sc = self.scales
+        _check(_lib.fp8_adam_step(
+            _ptr(grad, torch.bfloat16, "grad"), self.n, _p8(self.m1, "m1"),
+            ctypes.c_void_p(sc.data_ptr()), ctypes.c_void_p(sc.data_ptr() + 4),
+            _ptr(self.m2, torch.float16, "m2"), _ptr(self.w16, torch.float16, "w16"),
+            ctypes.c_void_p(sc.data_ptr() + 8), ctypes.c_void_p(sc.data_ptr() + 12),
+            _ptr(w_bf16, torch.bfloat16, "w_bf16"), _ptr(self.amax, torch.float32, "amax"),
+            ctypes.byref(h), _stream(stream)))

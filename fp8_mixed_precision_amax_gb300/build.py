@@ -18,7 +18,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OBJDIR = os.path.join(ROOT, "_build", "obj")
 LIB = os.path.join(PKG, "libfp8amax.so")
-SOURCES = ["abi.cu", "cast.cu", "gemm.cu", "noalloc.cu", "tmap.cu"]
+SOURCES = ["abi.cu", "cast.cu", "gemm.cu", "noalloc.cu", "optim.cu", "tmap.cu"]
 HEADERS = ["common.cuh", "kernels.h"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -325,6 +325,37 @@ fp8_status fp8_quantize_transpose_grouped(const fp8_cast_desc *descs, int32_t n,
     return FP8_OK;
 }
 
+fp8_status fp8_adam_step(const void *grad, int64_t n, uint8_t *m1, float *m1_scale,
+                         float *m1_scale_inv, uint16_t *m2, uint16_t *w16, float *w_scale,
+                         float *w_scale_inv, void *w_bf16, float *amax, const fp8_adam_hyper *hp,
+                         void *stream) {
+    const char *fn = "fp8_adam_step";
+    FP8_TRY(check_dims16(fn, n, "n", 0, "-"));
+    if (hp == nullptr) return fail(FP8_ERR_ARG, "%s: hyper-parameters are NULL", fn);
+    if (hp->margin < 0 || hp->margin > 64)
+        return fail(FP8_ERR_ARG, "%s: margin %d outside [0, 64]", fn, hp->margin);
+    if (!(hp->bias_correction1 > 0.0f) || !(hp->bias_correction2 > 0.0f))
+        return fail(FP8_ERR_ARG, "%s: bias corrections must be > 0 (step >= 1)", fn);
+    const bool empty = n == 0;
+    FP8_TRY(check_ptr(fn, grad, "grad", empty));
+    FP8_TRY(check_ptr(fn, m1, "m1", empty));
+    FP8_TRY(check_ptr(fn, m2, "m2", empty));
+    FP8_TRY(check_ptr(fn, w16, "w16", empty));
+    FP8_TRY(check_ptr(fn, w_bf16, "w_bf16", empty));
+    FP8_TRY(check_scalar(fn, m1_scale, "m1_scale", false));
+    FP8_TRY(check_scalar(fn, m1_scale_inv, "m1_scale_inv", false));
+    FP8_TRY(check_scalar(fn, w_scale, "w_scale", false));
+    FP8_TRY(check_scalar(fn, w_scale_inv, "w_scale_inv", false));
+    FP8_TRY(check_scalar(fn, amax, "amax", false));
+    int sms;
+    FP8_TRY(current_device(&sms));
+    const fp8k::AdamSpec a{grad, n, m1, m1_scale, m1_scale_inv, m2, w16, w_scale, w_scale_inv,
+                           w_bf16, amax, hp->lr, hp->beta1, hp->beta2, hp->eps, hp->weight_decay,
+                           hp->bias_correction1, hp->bias_correction2, hp->margin};
+    FP8_CUDA(fp8k::launch_adam_step(a, sms, static_cast<cudaStream_t>(stream)), fn);
+    return FP8_OK;
+}
+
 fp8_status fp8_layernorm_quantize_transpose(const void *x, const void *gamma, const void *beta,
                                             int64_t rows, int64_t cols, float eps,
                                             const float *scale, int32_t fmt, uint8_t *out,

@@ -60,21 +60,6 @@ __global__ void __launch_bounds__(512) amax_kernel(const uint4 *__restrict__ x, 
     }
 }
 
-// ------------------------------------------------------- the scale formula --
-// scale = fl32(fl32(fmax / m) * 2^-margin), +inf clamped to FLT_MAX, when
-// 0 < m < inf (m = the amax, or the max over the amax history); otherwise the
-// previous scale is kept (valid = false).
-__device__ __forceinline__ float recipe_scale(float m, float fmax, int margin, float prev,
-                                              bool &valid) {
-    valid = m > 0.0f && m <= FLT_MAX;
-    if (!valid) return prev;
-    const float q = __fdiv_rn(fmax, m);
-    const float p2 = __uint_as_float(static_cast<uint32_t>(127 - margin) << 23);
-    float sc = __fmul_rn(q, p2);
-    if (sc > FLT_MAX) sc = FLT_MAX;
-    return sc;
-}
-
 // ----------------------------------------------------- quantize_transpose --
 //
 // Persistent CTAs of 256 threads (two per SM) convert 128 x 128 tiles.  The

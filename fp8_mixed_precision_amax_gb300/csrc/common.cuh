@@ -292,4 +292,19 @@ __device__ __forceinline__ uint32_t amax_bits2(uint32_t m, uint32_t w) {
     return max(m, max(lo, hi));
 }
 
+// ------------------------------------------------------- the scale formula --
+// scale = fl32(fl32(fmax / m) * 2^-margin), +inf clamped to FLT_MAX, when
+// 0 < m < inf (m = the amax, or the max over the amax history); otherwise the
+// previous scale is kept (valid = false).  0 <= margin <= 64.
+__device__ __forceinline__ float recipe_scale(float m, float fmax, int margin, float prev,
+                                              bool &valid) {
+    valid = m > 0.0f && m <= 3.402823466e38f;
+    if (!valid) return prev;
+    const float q = __fdiv_rn(fmax, m);
+    const float p2 = __uint_as_float(static_cast<uint32_t>(127 - margin) << 23);
+    float sc = __fmul_rn(q, p2);
+    if (sc > 3.402823466e38f) sc = 3.402823466e38f;
+    return sc;
+}
+
 }  // namespace fp8k

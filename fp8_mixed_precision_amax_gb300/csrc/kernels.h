@@ -98,6 +98,23 @@ cudaError_t launch_gemm_tn(const uint8_t *A, int fa, const uint8_t *B, int fb, i
                            const float *b_scale_inv, void *D, float *d_amax, bool zero_amax,
                            int sm_count, cudaStream_t st, const char **what);
 
+// One decoupled-precision Adam step (optim.cu): first moment E4M3 + scale,
+// second moment FP16, master weights FP16 + scale; writes the model's BF16
+// weights and amax[2] (new first moment, new weights), then the new scales.
+struct AdamSpec {
+    const void *grad;
+    int64_t n;
+    uint8_t *m1;
+    float *m1_scale, *m1_scale_inv;
+    uint16_t *m2, *w16;
+    float *w_scale, *w_scale_inv;
+    void *w_bf16;
+    float *amax;
+    float lr, b1, b2, eps, wd, bc1, bc2;
+    int margin;
+};
+cudaError_t launch_adam_step(const AdamSpec &s, int sm_count, cudaStream_t st);
+
 // Set the message fp8_last_error() returns on this host thread.
 void set_last_error(const char *msg);
 

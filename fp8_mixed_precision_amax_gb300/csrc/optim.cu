@@ -1,0 +1,192 @@
+// optim.cu -- one Adam step on optimizer states of decoupled precision
+// ("Mixed-precision training" wiki note, bullet "precision decoupling": the
+// first moment in FP8, the second moment in FP16, master weights in FP16
+// with tensor scaling -- 5 bytes of state per parameter instead of 12).
+//
+// Per element, in binary32 with one rounding per operation (AdamW's
+// decoupled weight decay):
+//   m = b1*m + (1-b1)*g;  v = b2*v + (1-b2)*(g*g)
+//   u = (m / bc1) / (sqrt(v / bc2) + eps);  w = w - lr*(u + wd*w)
+// m is decoded from E4M3 codes times the first moment's scale_inv, w from
+// FP16 codes times the weights' scale_inv.  The new states get just-in-time
+// per-tensor scales (fmax / amax of the new values, a history of one):
+//   adam_amax_kernel    the amax of the new m and w (no stores);
+//   adam_apply_kernel   recomputes, encodes with the new scales, stores m, v,
+//                       w and the model's BF16 copy of w;
+//   adam_scales_kernel  records the new scales after every block has decoded
+//                       with the old ones.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include <cstdint>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace fp8k {
+
+namespace {
+
+constexpr float kF16Max = 65504.0f;
+
+__device__ __forceinline__ float f16_dec(uint16_t h) { return __half2float(__ushort_as_half(h)); }
+
+// Nearest FP16 value, ties to even, saturating at +-65504; NaN stays NaN.
+__device__ __forceinline__ uint16_t f16_enc_sat(float v) {
+    if (v != v) return 0x7e00;
+    v = fminf(fmaxf(v, -kF16Max), kF16Max);
+    return __half_as_ushort(__float2half_rn(v));
+}
+
+// Two E4M3 codes (low byte first) to two floats, exactly.
+__device__ __forceinline__ void e4m3x2_dec(uint16_t c, float &lo, float &hi) {
+    uint32_t h2;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(c));
+    lo = __half2float(__ushort_as_half(static_cast<uint16_t>(h2 & 0xFFFF)));
+    hi = __half2float(__ushort_as_half(static_cast<uint16_t>(h2 >> 16)));
+}
+
+struct AdamArgs {
+    const uint16_t *grad;
+    uint8_t *m1;
+    float *m1_scale, *m1_scale_inv;
+    uint16_t *m2, *w16;
+    float *w_scale, *w_scale_inv;
+    uint16_t *w_bf16;
+    float *amax;              // [2]: new m, new w
+    int64_t n;
+    float lr, b1, b2, eps, wd, bc1, bc2;
+    int margin;
+};
+
+struct Elem8 {
+    float m[8], v[8], w[8];
+};
+
+// The update of the 8 elements at [i, i + 8).
+__device__ __forceinline__ void adam8(const AdamArgs &a, int64_t i, float msi, float wsi, Elem8 &e) {
+    const uint4 g4 = *reinterpret_cast<const uint4 *>(a.grad + i);
+    const uint2 m8 = *reinterpret_cast<const uint2 *>(a.m1 + i);
+    const uint4 v4 = *reinterpret_cast<const uint4 *>(a.m2 + i);
+    const uint4 w4 = *reinterpret_cast<const uint4 *>(a.w16 + i);
+    const uint32_t gw[4] = {g4.x, g4.y, g4.z, g4.w}, vw[4] = {v4.x, v4.y, v4.z, v4.w},
+                   ww[4] = {w4.x, w4.y, w4.z, w4.w}, mw[2] = {m8.x, m8.y};
+    const float omb1 = __fsub_rn(1.0f, a.b1), omb2 = __fsub_rn(1.0f, a.b2);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        float md[2];
+        e4m3x2_dec(static_cast<uint16_t>(mw[j >> 1] >> (16 * (j & 1))), md[0], md[1]);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int k = 2 * j + h;
+            const float g = h ? bf16_hi(gw[j]) : bf16_lo(gw[j]);
+            float m = __fmul_rn(md[h], msi);
+            float v = f16_dec(static_cast<uint16_t>(vw[j] >> (16 * h)));
+            float w = __fmul_rn(f16_dec(static_cast<uint16_t>(ww[j] >> (16 * h))), wsi);
+            m = __fadd_rn(__fmul_rn(a.b1, m), __fmul_rn(omb1, g));
+            v = __fadd_rn(__fmul_rn(a.b2, v), __fmul_rn(omb2, __fmul_rn(g, g)));
+            const float u = __fdiv_rn(__fdiv_rn(m, a.bc1),
+                                      __fadd_rn(__fsqrt_rn(__fdiv_rn(v, a.bc2)), a.eps));
+            w = __fsub_rn(w, __fmul_rn(a.lr, __fadd_rn(u, __fmul_rn(a.wd, w))));
+            e.m[k] = m;
+            e.v[k] = v;
+            e.w[k] = w;
+        }
+    }
+}
+
+__device__ __forceinline__ uint32_t abs_bits(float x) {
+    const uint32_t b = __float_as_uint(x) & 0x7FFFFFFFu;
+    return b > 0x7F800000u ? 0u : b;   // NaN skipped
+}
+
+__global__ void __launch_bounds__(256) adam_amax_kernel(const AdamArgs a) {
+    const float msi = *a.m1_scale_inv, wsi = *a.w_scale_inv;
+    uint32_t mm = 0, mw = 0;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x * 8;
+    for (int64_t i = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) * 8; i < a.n;
+         i += stride) {
+        Elem8 e;
+        adam8(a, i, msi, wsi, e);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            mm = max(mm, abs_bits(e.m[k]));
+            mw = max(mw, abs_bits(e.w[k]));
+        }
+    }
+    mm = __reduce_max_sync(0xFFFFFFFFu, mm);
+    mw = __reduce_max_sync(0xFFFFFFFFu, mw);
+    if ((threadIdx.x & 31) == 0) {
+        if (mm) atomicMax(reinterpret_cast<unsigned *>(a.amax), mm);
+        if (mw) atomicMax(reinterpret_cast<unsigned *>(a.amax + 1), mw);
+    }
+}
+
+__global__ void __launch_bounds__(256) adam_apply_kernel(const AdamArgs a) {
+    const float msi = *a.m1_scale_inv, wsi = *a.w_scale_inv;
+    bool valid;
+    const float sm = recipe_scale(a.amax[0], 448.0f, a.margin, *a.m1_scale, valid);
+    const float sw = recipe_scale(a.amax[1], kF16Max, a.margin, *a.w_scale, valid);
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x * 8;
+    for (int64_t i = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) * 8; i < a.n;
+         i += stride) {
+        Elem8 e;
+        adam8(a, i, msi, wsi, e);
+        uint32_t mq[2], vq[4], wq[4], bq[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const uint32_t c = cvt2_e4m3(__fmul_rn(e.m[2 * j], sm), __fmul_rn(e.m[2 * j + 1], sm));
+            if (j & 1)
+                mq[j >> 1] |= c << 16;
+            else
+                mq[j >> 1] = c;
+            vq[j] = f16_enc_sat(e.v[2 * j]) | (static_cast<uint32_t>(f16_enc_sat(e.v[2 * j + 1])) << 16);
+            wq[j] = f16_enc_sat(__fmul_rn(e.w[2 * j], sw)) |
+                    (static_cast<uint32_t>(f16_enc_sat(__fmul_rn(e.w[2 * j + 1], sw))) << 16);
+            const __nv_bfloat162 b2 = __floats2bfloat162_rn(e.w[2 * j], e.w[2 * j + 1]);
+            bq[j] = *reinterpret_cast<const uint32_t *>(&b2);
+        }
+        *reinterpret_cast<uint2 *>(a.m1 + i) = make_uint2(mq[0], mq[1]);
+        *reinterpret_cast<uint4 *>(a.m2 + i) = make_uint4(vq[0], vq[1], vq[2], vq[3]);
+        *reinterpret_cast<uint4 *>(a.w16 + i) = make_uint4(wq[0], wq[1], wq[2], wq[3]);
+        *reinterpret_cast<uint4 *>(a.w_bf16 + i) = make_uint4(bq[0], bq[1], bq[2], bq[3]);
+    }
+}
+
+__global__ void adam_scales_kernel(const AdamArgs a) {
+    bool valid;
+    const float sm = recipe_scale(a.amax[0], 448.0f, a.margin, *a.m1_scale, valid);
+    if (valid) {
+        *a.m1_scale = sm;
+        *a.m1_scale_inv = __fdiv_rn(1.0f, sm);
+    }
+    const float sw = recipe_scale(a.amax[1], kF16Max, a.margin, *a.w_scale, valid);
+    if (valid) {
+        *a.w_scale = sw;
+        *a.w_scale_inv = __fdiv_rn(1.0f, sw);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_adam_step(const AdamSpec &s, int sm_count, cudaStream_t st) {
+    cudaError_t e = cudaMemsetAsync(s.amax, 0, 2 * sizeof(float), st);
+    if (e != cudaSuccess) return e;
+    AdamArgs a{static_cast<const uint16_t *>(s.grad), s.m1, s.m1_scale, s.m1_scale_inv, s.m2,
+               s.w16, s.w_scale, s.w_scale_inv, static_cast<uint16_t *>(s.w_bf16), s.amax, s.n,
+               s.lr, s.b1, s.b2, s.eps, s.wd, s.bc1, s.bc2, s.margin};
+    if (s.n > 0) {
+        const int threads = 256;
+        int64_t blocks = (s.n / 8 + threads - 1) / threads;
+        const int64_t cap = static_cast<int64_t>(sm_count) * 8;
+        if (blocks > cap) blocks = cap;
+        adam_amax_kernel<<<static_cast<unsigned>(blocks), threads, 0, st>>>(a);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        adam_apply_kernel<<<static_cast<unsigned>(blocks), threads, 0, st>>>(a);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    adam_scales_kernel<<<1, 1, 0, st>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace fp8k

@@ -286,6 +286,41 @@ fp8_status fp8_linear_bwd(const void *dY, int64_t M, int64_t N, int64_t K, const
                           const fp8_recipe *recipe, const uint8_t *X8t, const uint8_t *W8t,
                           uint8_t *dY8, uint8_t *dY8t, void *dX, void *dW, void *stream);
 
+/* Hyper-parameters of one Adam step (AdamW's decoupled weight decay).  The
+ * bias corrections 1 - beta1^t and 1 - beta2^t are computed by the caller
+ * for step t (>= 1) and passed as binary32. */
+typedef struct {
+    float lr, beta1, beta2, eps, weight_decay;
+    float bias_correction1, bias_correction2;
+    int32_t margin;   /* for the state scales, 0..64 */
+} fp8_adam_hyper;
+
+/* One Adam step on optimizer states of decoupled precision (wiki note,
+ * bullet "precision decoupling": first moment FP8, second moment FP16,
+ * master weights FP16 with tensor scaling: 5 bytes of state per parameter;
+ * the note's 6 also counts an FP8 gradient, which this path keeps BF16).  In
+ * binary32, one rounding per operation, for every element:
+ *   m = b1*m + (1-b1)*g;  v = b2*v + (1-b2)*(g*g);
+ *   u = (m / bc1) / (sqrt(v / bc2) + eps);  w = w - lr*(u + wd*w)
+ * with m = E4M3 code * m1_scale_inv and w = FP16 code * w_scale_inv.  The new
+ * states take just-in-time per-tensor scales: scale = (fmax / amax) /
+ * 2^margin of the new values (fmax 448 for m, 65504 for w), kept when that
+ * amax is 0 or not finite.  FP16 encodes round to nearest even and saturate
+ * at +-65504.  Four kernels, in stream order.
+ *   grad        DEVICE [n] BF16 gradient
+ *   m1          DEVICE [n] E4M3 codes, updated in place
+ *   m1_scale, m1_scale_inv   DEVICE 1 float each, updated
+ *   m2          DEVICE [n] FP16 second moment, updated in place
+ *   w16         DEVICE [n] FP16 master-weight codes, updated in place
+ *   w_scale, w_scale_inv     DEVICE 1 float each, updated
+ *   w_bf16      DEVICE [n] BF16 output: the weights for the next forward
+ *   amax        DEVICE [2] output: amax of the new m and w (fp32)
+ * n >= 0, a multiple of 16; arrays 16-byte aligned. */
+fp8_status fp8_adam_step(const void *grad, int64_t n, uint8_t *m1, float *m1_scale,
+                         float *m1_scale_inv, uint16_t *m2, uint16_t *w16, float *w_scale,
+                         float *w_scale_inv, void *w_bf16, float *amax, const fp8_adam_hyper *hp,
+                         void *stream);
+
 /* fp8_linear_bwd for callers that cannot allocate device memory.  The pages
  * have no counterpart: this is a calling convenience, not part of the method.
  * It computes exactly what fp8_linear_bwd computes, but the two FP8 work

@@ -24,6 +24,9 @@ What each function follows:
   amax alone.
 * ``layernorm`` -- te.LayerNorm's forward (implementation guide, "Basic
   structure of FP8 training code"), in double.
+* ``adam_step`` -- Adam with the optimizer-state precision decoupling of the
+  wiki note (first moment FP8, second moment FP16, master weights FP16 with
+  tensor scaling), in binary32.
 * ``layer_fwd`` / ``layer_bwd`` -- te.Linear inside fp8_autocast with
   Format.HYBRID (E4M3 forward, E5M2 backward; same section) and FP8 GEMMs with
   higher-precision accumulation (wiki note, bullet "extension to FP8").
@@ -94,6 +97,10 @@ def _lib():
         lib.or_num_threads.argtypes, lib.or_num_threads.restype = [], ctypes.c_int
         lib.or_layernorm.argtypes = [vp, vp, vp, i64, i64, ctypes.c_double, vp, vp, vp]
         lib.or_layernorm.restype = None
+        lib.or_f16_decode.argtypes, lib.or_f16_decode.restype = [ctypes.c_uint16], f32
+        lib.or_f16_encode.argtypes, lib.or_f16_encode.restype = [f32], ctypes.c_uint16
+        lib.or_adam_step.argtypes = [vp, i64, vp, vp, vp, vp, vp, vp, vp, vp, vp] + [f32] * 7 + [i32]
+        lib.or_adam_step.restype = None
         _lib_handle = lib
     return _lib_handle
 
@@ -233,6 +240,58 @@ def layernorm(x_bf16: np.ndarray, gamma_bf16: np.ndarray, beta_bf16: np.ndarray,
     _lib().or_layernorm(x.ctypes.data, g.ctypes.data, b.ctypes.data, rows, cols, float(eps),
                         y.ctypes.data, mean.ctypes.data, rstd.ctypes.data)
     return y, mean, rstd
+
+
+# ------------------------------------------------------- FP8 optimizer --
+
+def f16_encode(v) -> np.ndarray:
+    """Binary32 -> FP16 codes: nearest value, ties to even, saturating at 65504."""
+    v = _c(np.asarray(v), np.float32)
+    f = _lib().or_f16_encode
+    return np.array([f(float(x)) for x in v.reshape(-1)], dtype=np.uint16).reshape(v.shape)
+
+
+def f16_decode(h) -> np.ndarray:
+    h = _c(np.asarray(h), np.uint16)
+    f = _lib().or_f16_decode
+    return np.array([f(int(x)) for x in h.reshape(-1)], dtype=np.float32).reshape(h.shape)
+
+
+@dataclass
+class AdamHyper:
+    lr: float = 1e-3
+    beta1: float = 0.9
+    beta2: float = 0.999
+    eps: float = 1e-8
+    weight_decay: float = 0.0
+    margin: int = 0
+
+    def bias_corrections(self, t: int):
+        """(1 - beta1^t, 1 - beta2^t) as binary32, computed in double."""
+        return np.float32(1.0 - self.beta1 ** t), np.float32(1.0 - self.beta2 ** t)
+
+
+def adam_step(grad_bf16, m1, m1_scale, m1_scale_inv, m2, w16, w_scale, w_scale_inv, hp: AdamHyper,
+              t: int):
+    """One Adam step on decoupled-precision states (wiki note, bullet
+    "precision decoupling"): returns the new (m1, m1_scale, m1_scale_inv, m2,
+    w16, w_scale, w_scale_inv, w_bf16, amax[2]) as copies."""
+    g = _c(grad_bf16, np.uint16).reshape(-1)
+    n = g.size
+    m1o = np.array(m1, np.uint8).reshape(-1).copy()
+    m2o = np.array(m2, np.uint16).reshape(-1).copy()
+    w16o = np.array(w16, np.uint16).reshape(-1).copy()
+    wb = np.empty(n, np.uint16)
+    sc = np.array([m1_scale, m1_scale_inv, w_scale, w_scale_inv], np.float32)
+    am = np.zeros(2, np.float32)
+    bc1, bc2 = hp.bias_corrections(t)
+    _lib().or_adam_step(g.ctypes.data, n, m1o.ctypes.data, sc[0:].ctypes.data,
+                        sc[1:].ctypes.data, m2o.ctypes.data, w16o.ctypes.data,
+                        sc[2:].ctypes.data, sc[3:].ctypes.data, wb.ctypes.data, am.ctypes.data,
+                        float(np.float32(hp.lr)), float(np.float32(hp.beta1)),
+                        float(np.float32(hp.beta2)), float(np.float32(hp.eps)),
+                        float(np.float32(hp.weight_decay)), float(bc1), float(bc2), int(hp.margin))
+    return m1o, sc[0], sc[1], m2o, w16o, sc[2], sc[3], wb, am
 
 
 # ------------------------------------------------------------- the layer --

@@ -342,3 +342,124 @@ void or_layernorm(const uint16_t *x, const uint16_t *gamma, const uint16_t *beta
                               (double)or_bf16_to_f32(gamma[c]) + (double)or_bf16_to_f32(beta[c]);
     }
 }
+
+/* ------------------------------------------------------------------------ */
+/* FP16 (S1E5M10, [P3] Definition table: max 65,504): encode by nearest      */
+/* value with ties to the even code, saturating at +-65504 (the same reading */
+/* as the FP8 casts); decode from the fields.                                 */
+/* ------------------------------------------------------------------------ */
+
+float or_f16_decode(uint16_t h)
+{
+    int s = h >> 15, e = (h >> 10) & 0x1f, m = h & 0x3ff;
+    double v;
+    if (e == 31)
+        return m ? NAN : (s ? -INFINITY : INFINITY);
+    v = e == 0 ? ldexp((double)m, -24) : ldexp(1.0 + m / 1024.0, e - 15);
+    return (float)(s ? -v : v);
+}
+
+uint16_t or_f16_encode(float f)
+{
+    if (isnan(f))
+        return 0x7e00;
+    int neg = signbit(f) ? 1 : 0;
+    double a = fabs((double)f);
+    int top = 0x7bff, code;
+    if (a >= (double)or_f16_decode((uint16_t)top)) {
+        code = top;
+    } else {
+        int lo = 0, hi = top;
+        while (hi - lo > 1) {
+            int mid = (lo + hi) / 2;
+            if ((double)or_f16_decode((uint16_t)mid) <= a)
+                lo = mid;
+            else
+                hi = mid;
+        }
+        double vlo = or_f16_decode((uint16_t)lo), vhi = or_f16_decode((uint16_t)hi);
+        if (2.0 * a < vlo + vhi)
+            code = lo;
+        else if (2.0 * a > vlo + vhi)
+            code = hi;
+        else
+            code = (lo % 2 == 0) ? lo : hi;
+    }
+    return (uint16_t)((neg << 15) | code);
+}
+
+/* ------------------------------------------------------------------------ */
+/* One Adam step with decoupled optimizer-state precision ([P3] bullet       */
+/* "precision decoupling": first moment FP8, second moment FP16, master      */
+/* weights FP16 with tensor scaling).  All arithmetic in binary32, one       */
+/* rounding per operation, in this order (AdamW's decoupled weight decay):   */
+/*   m  = b1*m + (1-b1)*g,   v = b2*v + (1-b2)*(g*g)                         */
+/*   u  = (m / bc1) / (sqrt(v / bc2) + eps)                                   */
+/*   w  = w - lr*(u + wd*w)                                                   */
+/* with m decoded from its E4M3 codes times m_sinv and w from its FP16 codes */
+/* times w_sinv.  Just-in-time per-tensor scaling of the new states:         */
+/* amax over all elements first, then the scale formula with a history of    */
+/* one (fmax 448 for m, 65504 for w), then the encodes.  Outputs: new m      */
+/* codes, v (FP16), w codes (FP16), the model's BF16 weight, the two amaxes  */
+/* and the new scales / inverses (kept when an amax is 0 or not finite).     */
+/* ------------------------------------------------------------------------ */
+
+static void adam_elem(float g, float m, float v, float w, float lr, float b1, float b2, float eps,
+                      float wd, float bc1, float bc2, float *mo, float *vo, float *wo)
+{
+    m = b1 * m + (1.0f - b1) * g;
+    v = b2 * v + (1.0f - b2) * (g * g);
+    float u = (m / bc1) / (sqrtf(v / bc2) + eps);
+    w = w - lr * (u + wd * w);
+    *mo = m;
+    *vo = v;
+    *wo = w;
+}
+
+void or_adam_step(const uint16_t *grad, int64_t n, uint8_t *m1, float *m1_scale,
+                  float *m1_scale_inv, uint16_t *m2, uint16_t *w16, float *w_scale,
+                  float *w_scale_inv, uint16_t *w_bf16, float *amax, float lr, float b1, float b2,
+                  float eps, float wd, float bc1, float bc2, int32_t margin)
+{
+    float am_m = 0.0f, am_w = 0.0f;
+    const float msi = *m1_scale_inv, wsi = *w_scale_inv;
+    for (int64_t i = 0; i < n; ++i) {
+        float mo, vo, wo;
+        adam_elem(or_bf16_to_f32(grad[i]), (float)or_fp8_decode(m1[i], OR_E4M3) * msi,
+                  or_f16_decode(m2[i]), or_f16_decode(w16[i]) * wsi, lr, b1, b2, eps, wd, bc1,
+                  bc2, &mo, &vo, &wo);
+        if (fabsf(mo) > am_m)
+            am_m = fabsf(mo);
+        if (fabsf(wo) > am_w)
+            am_w = fabsf(wo);
+    }
+    amax[0] = am_m;
+    amax[1] = am_w;
+    /* the new scales: the update formula applied to a one-entry history */
+    float hm[1] = {0.0f}, hw[1] = {0.0f};
+    float sm = *m1_scale, smi = *m1_scale_inv, sw = *w_scale, swi = *w_scale_inv;
+    or_history_update(hm, 1, am_m, &sm, &smi, OR_E4M3, margin);
+    /* FP16's largest finite value replaces the FP8 one for the weights */
+    if (am_w > 0.0f && isfinite(am_w)) {
+        float q = 65504.0f / am_w;
+        float s = (float)ldexp((double)q, -margin);
+        if (isinf(s))
+            s = FLT_MAX;
+        sw = s;
+        swi = 1.0f / s;
+    }
+    for (int64_t i = 0; i < n; ++i) {
+        float mo, vo, wo;
+        adam_elem(or_bf16_to_f32(grad[i]), (float)or_fp8_decode(m1[i], OR_E4M3) * msi,
+                  or_f16_decode(m2[i]), or_f16_decode(w16[i]) * wsi, lr, b1, b2, eps, wd, bc1,
+                  bc2, &mo, &vo, &wo);
+        m1[i] = or_fp8_encode_f32(mo * sm, OR_E4M3);
+        m2[i] = or_f16_encode(vo);
+        w16[i] = or_f16_encode(wo * sw);
+        w_bf16[i] = or_f32_to_bf16(wo);
+    }
+    *m1_scale = sm;
+    *m1_scale_inv = smi;
+    *w_scale = sw;
+    *w_scale_inv = swi;
+}

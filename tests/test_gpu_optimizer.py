@@ -1,0 +1,66 @@
+"""GPU parity of the decoupled-precision Adam step (first moment FP8, second
+moment FP16, master weights FP16 with tensor scaling) against the oracle:
+bit-exact first-moment codes, FP16 second moments and master weights, BF16
+weights, amaxes and scales, over several steps (both sides evaluate the same
+binary32 operations in the same order)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as o
+from helpers import f32_bits
+
+pytestmark = pytest.mark.gpu
+
+
+def _lib():
+    import fp8_mixed_precision_amax_gb300 as f
+    return f
+
+
+def _u16(t):
+    return t.detach().contiguous().cpu().view(torch.int16).numpy().view(np.uint16)
+
+
+@pytest.mark.parametrize("n", [16, 4096, 1 << 20, 11008 * 4096 // 64])
+@pytest.mark.parametrize("wd,margin", [(0.0, 0), (0.1, 1)])
+def test_adam_steps_bit_exact(n, wd, margin):
+    f = _lib()
+    g = torch.Generator().manual_seed(n + margin)
+    w = (torch.randn(n, generator=g) * 0.02).to(torch.bfloat16).cuda()
+    state = f.Fp8AdamState(w)
+    hp = f.AdamHyper(lr=3e-3, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=wd, margin=margin)
+    ohp = o.AdamHyper(lr=3e-3, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=wd, margin=margin)
+    sc = state.scales.cpu().numpy()
+    ost = dict(m1=state.m1.cpu().numpy(), m1_scale=sc[0], m1_scale_inv=sc[1],
+               m2=_u16(state.m2), w16=_u16(state.w16), w_scale=sc[2], w_scale_inv=sc[3])
+    wout = torch.empty(n, dtype=torch.bfloat16, device="cuda")
+    for t in range(1, 5):
+        grad = (torch.randn(n, generator=g) * 1e-2 * t).to(torch.bfloat16)
+        if t == 3:
+            grad[: n // 4] = 0.0
+        state.step(grad.cuda(), wout, hp)
+        torch.cuda.synchronize()
+        m1, ms, msi, m2, w16, ws, wsi, wb, am = o.adam_step(
+            _u16(grad), ost["m1"], ost["m1_scale"], ost["m1_scale_inv"], ost["m2"], ost["w16"],
+            ost["w_scale"], ost["w_scale_inv"], ohp, t)
+        assert np.array_equal(state.m1.cpu().numpy(), m1), t
+        assert np.array_equal(_u16(state.m2), m2), t
+        assert np.array_equal(_u16(state.w16), w16), t
+        assert np.array_equal(_u16(wout), wb), t
+        assert np.array_equal(state.amax.cpu().numpy().view(np.uint32), am.view(np.uint32)), t
+        gs = state.scales.cpu().numpy()
+        assert np.array_equal(gs.view(np.uint32), np.array([ms, msi, ws, wsi], np.float32).view(np.uint32)), t
+        ost = dict(m1=m1, m1_scale=ms, m1_scale_inv=msi, m2=m2, w16=w16, w_scale=ws,
+                   w_scale_inv=wsi)
+    f.fp8_sync_status()
+
+
+def test_state_is_five_bytes_per_parameter():
+    """First moment 1 B + second moment 2 B + master weights 2 B.  (FP8-LM's
+    6 B per parameter also counts an FP8 gradient; this path's gradient, the
+    layer's dW, stays BF16.)"""
+    f = _lib()
+    w = torch.zeros(4096, dtype=torch.bfloat16, device="cuda")
+    s = f.Fp8AdamState(w)
+    assert s.m1.element_size() + s.m2.element_size() + s.w16.element_size() == 5
