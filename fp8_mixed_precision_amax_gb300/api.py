@@ -97,6 +97,7 @@ def _load() -> ctypes.CDLL:
         "fp8_layernorm_linear_fwd": ([vp, vp, vp, ctypes.c_float, vp, i64, i64, i64,
                                       ctypes.POINTER(fp8_meta), ctypes.POINTER(fp8_recipe), vp, vp,
                                       vp, vp, vp, vp, vp, vp], ctypes.c_int),
+        "fp8_dequant_sum": ([vp, i32, i64, i32, vp, vp, vp], ctypes.c_int),
         "fp8_adam_step": ([vp, i64, vp, vp, vp, vp, vp, vp, vp, vp, vp,
                            ctypes.POINTER(fp8_adam_hyper), vp], ctypes.c_int),
         "fp8_linear_bwd_noalloc": ([vp, i64, i64, i64, ctypes.POINTER(fp8_meta),
@@ -533,3 +534,49 @@ class Fp8AdamState:
             ctypes.c_void_p(sc.data_ptr() + 8), ctypes.c_void_p(sc.data_ptr() + 12),
             _ptr(w_bf16, torch.bfloat16, "w_bf16"), _ptr(self.amax, torch.float32, "amax"),
             ctypes.byref(h), _stream(stream)))
+
+
+def fp8_dequant_sum(parts: torch.Tensor, fmt: int, scale: torch.Tensor, out: torch.Tensor,
+                    stream=None) -> None:
+    """out = BF16 of the sum over ranks of parts [nranks, n] (FP8 codes sharing
+    one scale) times 1 / scale."""
+    nranks, n = parts.shape
+    if out.numel() != n:
+        raise ValueError("out must hold n elements")
+    _check(_lib.fp8_dequant_sum(_p8(parts, "parts"), nranks, n, fmt,
+                                _ptr(scale, torch.float32, "scale"),
+                                _ptr(out, torch.bfloat16, "out"), _stream(stream)))
+
+
+def fp8_allreduce(grad: torch.Tensor, fmt: int, margin: int = 0, group=None,
+                  out: torch.Tensor | None = None) -> torch.Tensor:
+    """All-reduce (sum) of a BF16 gradient [rows, cols] over the ranks of
+    ``group`` with FP8 communication and one scale shared by all ranks, the
+    minimum of the ranks' own scales (wiki note, bullet "per-tensor scaling is
+    the key"):
+      1. this rank's scale: amax, then the recipe formula on a one-entry history;
+      2. the shared scale: all-reduce(MIN) of the scales;
+      3. the cast of the gradient with the shared scale (fp8_quantize_transpose);
+      4. all-gather of the FP8 codes (1 byte per element per rank);
+      5. fp8_dequant_sum of the gathered codes into BF16.
+    Every rank ends with the same result.  Uses torch.distributed."""
+    import torch.distributed as dist
+    rows, cols = grad.shape
+    n = rows * cols
+    dev = grad.device
+    world = dist.get_world_size(group)
+    amax = torch.empty(1, dtype=torch.float32, device=dev)
+    hist = torch.zeros((1, 1), dtype=torch.float32, device=dev)
+    scale = torch.ones(1, dtype=torch.float32, device=dev)
+    scale_inv = torch.ones(1, dtype=torch.float32, device=dev)
+    fp8_amax(grad, amax)
+    fp8_scale_update(hist, amax, scale, scale_inv, fmt, margin)
+    dist.all_reduce(scale, op=dist.ReduceOp.MIN, group=group)
+    q_all = torch.empty((world, n), dtype=torch.uint8, device=dev)
+    rank = dist.get_rank(group)
+    fp8_quantize_transpose(grad, scale, fmt, out=q_all[rank].view(rows, cols))
+    dist.all_gather([q_all[r] for r in range(world)], q_all[rank].clone(), group=group)
+    if out is None:
+        out = torch.empty((rows, cols), dtype=torch.bfloat16, device=dev)
+    fp8_dequant_sum(q_all, fmt, scale, out)
+    return out

@@ -325,6 +325,23 @@ fp8_status fp8_quantize_transpose_grouped(const fp8_cast_desc *descs, int32_t n,
     return FP8_OK;
 }
 
+fp8_status fp8_dequant_sum(const uint8_t *parts, int32_t nranks, int64_t n, int32_t fmt,
+                           const float *scale, void *out, void *stream) {
+    const char *fn = "fp8_dequant_sum";
+    FP8_TRY(check_dims16(fn, n, "n", 0, "-"));
+    if (nranks < 1 || nranks > 65536) return fail(FP8_ERR_ARG, "%s: nranks %d", fn, nranks);
+    if (fmt != FP8_E4M3 && fmt != FP8_E5M2) return fail(FP8_ERR_ARG, "%s: bad format %d", fn, fmt);
+    FP8_TRY(check_ptr(fn, parts, "parts", n == 0));
+    FP8_TRY(check_ptr(fn, out, "out", n == 0));
+    FP8_TRY(check_scalar(fn, scale, "scale", false));
+    int sms;
+    FP8_TRY(current_device(&sms));
+    FP8_CUDA(fp8k::launch_dequant_sum(parts, nranks, n, fmt, scale, out, sms,
+                                      static_cast<cudaStream_t>(stream)),
+             fn);
+    return FP8_OK;
+}
+
 fp8_status fp8_adam_step(const void *grad, int64_t n, uint8_t *m1, float *m1_scale,
                          float *m1_scale_inv, uint16_t *m2, uint16_t *w16, float *w_scale,
                          float *w_scale_inv, void *w_bf16, float *amax, const fp8_adam_hyper *hp,

@@ -115,6 +115,10 @@ struct AdamSpec {
 };
 cudaError_t launch_adam_step(const AdamSpec &s, int sm_count, cudaStream_t st);
 
+// Decode-and-sum of nranks FP8 parts [nranks][n] sharing one scale (optim.cu).
+cudaError_t launch_dequant_sum(const uint8_t *parts, int nranks, int64_t n, int fmt,
+                               const float *scale, void *out, int sm_count, cudaStream_t st);
+
 // Set the message fp8_last_error() returns on this host thread.
 void set_last_error(const char *msg);
 

@@ -167,7 +167,76 @@ __global__ void adam_scales_kernel(const AdamArgs a) {
     }
 }
 
+// ------------------------------------------------ FP8 all-reduce: the sum --
+//
+// out[i] = bf16_rne(fl32(sum_r dec(q[r][i]) * fl32(1 / scale))): the parts of
+// all ranks share one scale (the minimum of the ranks' own scales), so their
+// codes can be decoded and summed directly.  The sum runs in double in rank
+// order (exact: every FP8 value has at most 3 significant bits within a
+// 2^-16 .. 2^16 range), the product in double, then one rounding to fp32
+// and one to BF16.
+
+template <int FMT>
+__device__ __forceinline__ void fp8x2_dec(uint16_t c, float &lo, float &hi) {
+    uint32_t h2;
+    if constexpr (FMT == 0)
+        asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(c));
+    else
+        asm("cvt.rn.f16x2.e5m2x2 %0, %1;" : "=r"(h2) : "h"(c));
+    lo = __half2float(__ushort_as_half(static_cast<uint16_t>(h2 & 0xFFFF)));
+    hi = __half2float(__ushort_as_half(static_cast<uint16_t>(h2 >> 16)));
+}
+
+template <int FMT>
+__global__ void __launch_bounds__(256) dequant_sum_kernel(const uint8_t *__restrict__ q,
+                                                          int nranks, int64_t n,
+                                                          const float *__restrict__ scale,
+                                                          uint16_t *__restrict__ out) {
+    const double sinv = static_cast<double>(__fdiv_rn(1.0f, *scale));
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x * 8;
+    for (int64_t i = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) * 8; i < n;
+         i += stride) {
+        double acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+        for (int r = 0; r < nranks; ++r) {
+            const uint2 c = *reinterpret_cast<const uint2 *>(q + static_cast<int64_t>(r) * n + i);
+            const uint32_t cw[2] = {c.x, c.y};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                float lo, hi;
+                fp8x2_dec<FMT>(static_cast<uint16_t>(cw[j >> 1] >> (16 * (j & 1))), lo, hi);
+                acc[2 * j] += static_cast<double>(lo);
+                acc[2 * j + 1] += static_cast<double>(hi);
+            }
+        }
+        uint32_t o[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const __nv_bfloat162 b = __floats2bfloat162_rn(__double2float_rn(acc[2 * j] * sinv),
+                                                           __double2float_rn(acc[2 * j + 1] * sinv));
+            o[j] = *reinterpret_cast<const uint32_t *>(&b);
+        }
+        *reinterpret_cast<uint4 *>(out + i) = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_dequant_sum(const uint8_t *parts, int nranks, int64_t n, int fmt,
+                               const float *scale, void *out, int sm_count, cudaStream_t st) {
+    if (n == 0) return cudaSuccess;
+    const int threads = 256;
+    int64_t blocks = (n / 8 + threads - 1) / threads;
+    const int64_t cap = static_cast<int64_t>(sm_count) * 8;
+    if (blocks > cap) blocks = cap;
+    auto *o = static_cast<uint16_t *>(out);
+    if (fmt == 0)
+        dequant_sum_kernel<0><<<static_cast<unsigned>(blocks), threads, 0, st>>>(parts, nranks, n,
+                                                                                 scale, o);
+    else
+        dequant_sum_kernel<1><<<static_cast<unsigned>(blocks), threads, 0, st>>>(parts, nranks, n,
+                                                                                 scale, o);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_adam_step(const AdamSpec &s, int sm_count, cudaStream_t st) {
     cudaError_t e = cudaMemsetAsync(s.amax, 0, 2 * sizeof(float), st);

@@ -321,6 +321,19 @@ fp8_status fp8_adam_step(const void *grad, int64_t n, uint8_t *m1, float *m1_sca
                          float *w_scale_inv, void *w_bf16, float *amax, const fp8_adam_hyper *hp,
                          void *stream);
 
+/* The summing half of an FP8 all-reduce with one shared scale (wiki note,
+ * bullet "per-tensor scaling is the key": every rank casts with the one
+ * scalar s'_g = min(s'_1, ..., s'_N), so the exchanged FP8 codes of all ranks
+ * can be summed directly).  After the ranks' codes have been gathered:
+ *   out[i] = bf16_rne(fl32(sum_r dec(parts[r][i]) * fl32(1 / scale)))
+ * with the sum (in rank order, exact) and the product in double.
+ *   parts   DEVICE [nranks][n] FP8 codes of format fmt
+ *   scale   DEVICE, 1 float: the shared scale the parts were cast with
+ *   out     DEVICE [n] BF16 output
+ * 1 <= nranks <= 65536; n >= 0, a multiple of 16. */
+fp8_status fp8_dequant_sum(const uint8_t *parts, int32_t nranks, int64_t n, int32_t fmt,
+                           const float *scale, void *out, void *stream);
+
 /* fp8_linear_bwd for callers that cannot allocate device memory.  The pages
  * have no counterpart: this is a calling convenience, not part of the method.
  * It computes exactly what fp8_linear_bwd computes, but the two FP8 work

@@ -27,6 +27,9 @@ What each function follows:
 * ``adam_step`` -- Adam with the optimizer-state precision decoupling of the
   wiki note (first moment FP8, second moment FP16, master weights FP16 with
   tensor scaling), in binary32.
+* ``fp8_allreduce`` / ``dequant_sum`` -- FP8 all-reduce with one scale shared
+  by all ranks, s'_g = min(s'_1 .. s'_N) (wiki note, bullet "per-tensor
+  scaling is the key").
 * ``layer_fwd`` / ``layer_bwd`` -- te.Linear inside fp8_autocast with
   Format.HYBRID (E4M3 forward, E5M2 backward; same section) and FP8 GEMMs with
   higher-precision accumulation (wiki note, bullet "extension to FP8").
@@ -101,6 +104,8 @@ def _lib():
         lib.or_f16_encode.argtypes, lib.or_f16_encode.restype = [f32], ctypes.c_uint16
         lib.or_adam_step.argtypes = [vp, i64, vp, vp, vp, vp, vp, vp, vp, vp, vp] + [f32] * 7 + [i32]
         lib.or_adam_step.restype = None
+        lib.or_dequant_sum.argtypes = [vp, i32, i64, ctypes.c_int, f32, vp]
+        lib.or_dequant_sum.restype = None
         _lib_handle = lib
     return _lib_handle
 
@@ -292,6 +297,39 @@ def adam_step(grad_bf16, m1, m1_scale, m1_scale_inv, m2, w16, w_scale, w_scale_i
                         float(np.float32(hp.beta2)), float(np.float32(hp.eps)),
                         float(np.float32(hp.weight_decay)), float(bc1), float(bc2), int(hp.margin))
     return m1o, sc[0], sc[1], m2o, w16o, sc[2], sc[3], wb, am
+
+
+# ------------------------------------------------- FP8 all-reduce --
+
+def dequant_sum(parts: np.ndarray, fmt: int, scale) -> np.ndarray:
+    """Sum of [nranks, n] FP8 codes sharing one scale, as BF16 bits."""
+    q = _c(parts, np.uint8)
+    nranks, n = q.shape
+    out = np.empty(n, np.uint16)
+    _lib().or_dequant_sum(q.ctypes.data, nranks, n, fmt, float(np.float32(scale)),
+                          out.ctypes.data)
+    return out
+
+
+def local_scale(x_bf16: np.ndarray, fmt: int, margin: int) -> np.float32:
+    """A rank's own scale for its tensor: the recipe formula on its amax (a
+    history of one); 1 when the amax is 0 or not finite."""
+    _, s, _ = history_update(np.zeros(1, np.float32), amax(x_bf16), np.float32(1.0),
+                             np.float32(1.0), fmt, margin)
+    return np.float32(s)
+
+
+def fp8_allreduce(grads_bf16, fmt: int, margin: int = 0):
+    """FP8 all-reduce of per-rank BF16 tensors with the one shared scale
+    s'_g = min over ranks of each rank's own scale (wiki note, bullet
+    "per-tensor scaling is the key"): every rank casts its tensor with s'_g,
+    the FP8 codes are exchanged, and their values are summed and dequantised.
+    Returns (BF16 bits of the sum, s'_g, the per-rank codes)."""
+    scales = [local_scale(g, fmt, margin) for g in grads_bf16]
+    sg = np.float32(min(scales))
+    parts = np.stack([quantize(np.asarray(g).reshape(1, -1), sg, fmt, transpose=False)[0][0]
+                      for g in grads_bf16])
+    return dequant_sum(parts, fmt, sg), sg, parts
 
 
 # ------------------------------------------------------------- the layer --

@@ -463,3 +463,24 @@ void or_adam_step(const uint16_t *grad, int64_t n, uint8_t *m1, float *m1_scale,
     *w_scale = sw;
     *w_scale_inv = swi;
 }
+
+/* ------------------------------------------------------------------------ */
+/* Sum of FP8 tensors sharing one scale ([P3] bullet "per-tensor scaling is  */
+/* the key": FP8 all-reduce with one scalar shared by all ranks,             */
+/* s'_g = min(s'_1, ..., s'_N)).  q holds nranks parts of n codes each;      */
+/* out[i] = bf16_rne(fl32(sum_r dec(q[r][i]) * fl32(1 / scale))), the sum    */
+/* and the product in double (the sum is exact: at most 2^21 parts).         */
+/* ------------------------------------------------------------------------ */
+
+void or_dequant_sum(const uint8_t *q, int32_t nranks, int64_t n, int fmt, float scale,
+                    uint16_t *out)
+{
+    const float sinv = 1.0f / scale;
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < n; ++i) {
+        double acc = 0.0;
+        for (int32_t r = 0; r < nranks; ++r)
+            acc += or_fp8_decode(q[(int64_t)r * n + i], fmt);
+        out[i] = or_f32_to_bf16((float)(acc * (double)sinv));
+    }
+}

@@ -92,3 +92,49 @@ def test_rank_that_never_joins_fails_the_collective():
         if p.is_alive():
             p.kill()
     assert r == 0 and status == "error"
+
+
+def _fp8_worker(rank, world, port, grads, out_q):
+    import datetime
+
+    import oracle as o
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world,
+                            timeout=datetime.timedelta(seconds=10))
+    try:
+        # the exchange of the FP8 all-reduce: MIN of the ranks' own scales,
+        # then the FP8 codes of every rank, summed the same way everywhere
+        s = torch.tensor([float(o.local_scale(grads[rank], o.E5M2, 0))])
+        dist.all_reduce(s, op=dist.ReduceOp.MIN)
+        sg = np.float32(s.item())
+        q, _ = o.quantize(grads[rank].reshape(1, -1), sg, o.E5M2, transpose=False)
+        parts = [torch.empty(q.size, dtype=torch.uint8) for _ in range(world)]
+        dist.all_gather(parts, torch.from_numpy(q.reshape(-1)))
+        out = o.dequant_sum(np.stack([p.numpy() for p in parts]), o.E5M2, sg)
+        out_q.put((rank, sg, out))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_fp8_allreduce_exchange_shares_the_minimum_scale():
+    """The exchange step of the FP8 all-reduce (wiki note, 'per-tensor scaling
+    is the key'): three gloo ranks agree on s'_g = min(s'_i) and reach the
+    same sum, equal to the single-process reference."""
+    import oracle as o
+    rng = np.random.default_rng(3)
+    grads = [torch.from_numpy((rng.standard_normal(4096) * m).astype(np.float32))
+             .to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+             for m in (1e-3, 3e-2, 5e-4)]
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_fp8_worker, args=(r, 3, port, grads, q)) for r in range(3)]
+    for p in procs:
+        p.start()
+    res = [q.get(timeout=60) for _ in procs]
+    for p in procs:
+        p.join(timeout=60)
+    ref, sg, _ = o.fp8_allreduce(grads, o.E5M2)
+    for rank, s, out in res:
+        assert s == sg and np.array_equal(out, ref), rank

@@ -1,0 +1,96 @@
+"""GPU parity of the FP8 all-reduce with one shared scale (wiki note, bullet
+"per-tensor scaling is the key": s'_g = min(s'_1 .. s'_N)).
+
+* fp8_dequant_sum against the oracle, bit-exact, for 1..8 parts;
+* the whole product path (fp8_allreduce: amax, own scale, MIN all-reduce,
+  cast, all-gather of FP8 codes, decode-and-sum) as 2 and 3 gloo ranks that
+  share cuda:0 -- their kernels never wait on one another, the exchange runs
+  on the host -- against the oracle's all-reduce, bit-exact on every rank."""
+import os
+import socket
+
+import numpy as np
+import pytest
+import torch
+import torch.multiprocessing as mp
+
+import oracle as o
+
+pytestmark = pytest.mark.gpu
+
+
+def _u16(t):
+    return t.detach().contiguous().cpu().view(torch.int16).numpy().view(np.uint16)
+
+
+@pytest.mark.parametrize("fmt", [o.E4M3, o.E5M2])
+@pytest.mark.parametrize("nranks", [1, 2, 5, 8])
+def test_dequant_sum_bit_exact(fmt, nranks):
+    import fp8_mixed_precision_amax_gb300 as f
+    rng = np.random.default_rng(10 * nranks + fmt)
+    table = o.fp8_decode_table(fmt)
+    finite = np.nonzero(np.isfinite(table))[0].astype(np.uint8)
+    n = 65536 + 16
+    parts = rng.choice(finite, size=(nranks, n))
+    s = np.float32(10.0 ** rng.uniform(-3, 3))
+    out = torch.full((n,), float("nan"), dtype=torch.bfloat16, device="cuda")
+    f.fp8_dequant_sum(torch.from_numpy(parts).cuda(), fmt, torch.tensor([s], device="cuda"), out)
+    torch.cuda.synchronize()
+    assert np.array_equal(_u16(out), o.dequant_sum(parts, fmt, s))
+
+
+def _grads(world, shape, seed):
+    out = []
+    for r in range(world):
+        g = torch.Generator().manual_seed(seed + r)
+        out.append((torch.randn(shape, generator=g) * 10.0 ** (-3 + r)).to(torch.bfloat16))
+    return out
+
+
+def _worker(rank, world, port, shape, fmt, margin, q):
+    import datetime
+
+    import torch.distributed as dist
+    import fp8_mixed_precision_amax_gb300 as f
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    torch.cuda.set_device(0)
+    dist.init_process_group("gloo", rank=rank, world_size=world,
+                            timeout=datetime.timedelta(seconds=60))
+    try:
+        grads = _grads(world, shape, 1234)
+        out = f.fp8_allreduce(grads[rank].cuda(), fmt, margin)
+        torch.cuda.synchronize()
+        q.put((rank, _u16(out)))
+    except Exception as e:   # reported to the parent
+        q.put((rank, repr(e)))
+    finally:
+        dist.destroy_process_group()
+
+
+def _free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    p = s.getsockname()[1]
+    s.close()
+    return p
+
+
+@pytest.mark.parametrize("world,fmt,margin", [(2, o.E5M2, 0), (3, o.E4M3, 1)])
+def test_allreduce_ranks_sharing_one_gpu(world, fmt, margin):
+    shape = (272, 1040)
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, world, port, shape, fmt, margin, q))
+             for r in range(world)]
+    for p in procs:
+        p.start()
+    res = dict(q.get(timeout=300) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+    grads = [_u16(g) for g in _grads(world, shape, 1234)]
+    ref, sg, _ = o.fp8_allreduce(grads, fmt, margin)
+    for r in range(world):
+        assert not isinstance(res[r], str), res[r]
+        assert np.array_equal(res[r].reshape(-1), ref), r
