@@ -218,17 +218,25 @@ fp8_status fp8_scale_update(float *history, const float *amax, float *scale, flo
     FP8_TRY(check_scalar(fn, scale_inv, "scale_inv", false));
     int sms;
     FP8_TRY(current_device(&sms));
-    FP8_CUDA(fp8k::launch_scale_update(history, amax, scale, scale_inv, num_tensors, history_len,
-                                       format_mask, margin, static_cast<cudaStream_t>(stream)),
+    FP8_CUDA(fp8k::launch_scale_update(history, const_cast<float *>(amax), scale, scale_inv,
+                                       num_tensors, history_len, format_mask, margin, false,
+                                       static_cast<cudaStream_t>(stream)),
              fn);
     return FP8_OK;
 }
 
 fp8_status fp8_amax_scale_update(const fp8_meta *meta, const fp8_recipe *recipe, void *stream) {
-    FP8_TRY(check_meta("fp8_amax_scale_update", meta, recipe));
+    const char *fn = "fp8_amax_scale_update";
+    FP8_TRY(check_meta(fn, meta, recipe));
     const uint32_t mask = recipe->hybrid ? ((1u << FP8_SLOT_DY) | (1u << FP8_SLOT_DX)) : 0u;
-    return fp8_scale_update(meta->history, meta->amax, meta->scale, meta->scale_inv, FP8_NUM_SLOTS,
-                            meta->history_len, mask, recipe->margin, stream);
+    int sms;
+    FP8_TRY(current_device(&sms));
+    // the five amax slots are consumed here and cleared for the next step
+    FP8_CUDA(fp8k::launch_scale_update(meta->history, meta->amax, meta->scale, meta->scale_inv,
+                                       FP8_NUM_SLOTS, meta->history_len, mask, recipe->margin,
+                                       true, static_cast<cudaStream_t>(stream)),
+             fn);
+    return FP8_OK;
 }
 
 static fp8_status gemm_checked(const char *fn, const uint8_t *A, int32_t fa, const uint8_t *B,
@@ -454,8 +462,8 @@ static fp8_status linear_fwd_impl(const char *fn, const void *X, const void *gam
     FP8_TRY(current_device(&sms));
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     float *am = meta->amax;
-    // amax of X, W and Y are max-combined into slots cleared here.
-    FP8_CUDA(cudaMemsetAsync(am + FP8_SLOT_X, 0, 3 * sizeof(float), st), fn);
+    // amax of X, W and Y are max-combined into their slots, which the
+    // previous fp8_amax_scale_update cleared (a fresh meta starts at 0).
     const bool cur = recipe->scaling == FP8_SCALING_CURRENT;
     if (mean != nullptr)   // LayerNorm statistics (and, for current scaling, amax of LN(X))
         FP8_CUDA(fp8k::launch_ln_stats(X, gamma, beta, M, K, eps, mean, rstd,
@@ -492,7 +500,7 @@ fp8_status fp8_linear_bwd(const void *dY, int64_t M, int64_t N, int64_t K, const
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     float *am = meta->amax;
     const int32_t fg = recipe->hybrid ? FP8_E5M2 : FP8_E4M3;
-    FP8_CUDA(cudaMemsetAsync(am + FP8_SLOT_DY, 0, 2 * sizeof(float), st), fn);
+    // amax of dY and dX are max-combined into their slots (see fp8_linear_fwd)
     if (recipe->scaling == FP8_SCALING_CURRENT)
         FP8_CUDA(fp8k::launch_quantize_transpose_current(
                      dY, M, N, fg, recipe->margin, dY8, dY8t, am + FP8_SLOT_DY,

@@ -26,6 +26,8 @@ __device__ unsigned g_cast_error_flags = 0;
 // per thread, integer max on magnitude bits, one atomicMax per block.
 __global__ void __launch_bounds__(512) amax_kernel(const uint4 *__restrict__ x, int64_t nvec,
                                                    unsigned *__restrict__ amax_bits) {
+    pdl_wait();
+    pdl_trigger();
     uint32_t m = 0;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
     int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
@@ -140,6 +142,15 @@ __global__ void __launch_bounds__(kQtThreads, 2)
     volatile int *abort_flag = reinterpret_cast<volatile int *>(full + kQtStages);
 
     const int tid = threadIdx.x;
+    if (tid == 0) {
+        for (int st = 0; st < kQtStages; ++st) mbar_init(smem_u32(full + st), 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+        for (int i = 0; i < a.num_tensors; ++i)
+            if (a.t[i].rows > 0 && a.t[i].cols > 0) prefetch_tmap(&a.maps[i]);
+    }
+    pdl_wait();
+    pdl_trigger();
     float sc[2];
     uint32_t tmax[2] = {0u, 0u};
 #pragma unroll
@@ -171,11 +182,6 @@ __global__ void __launch_bounds__(kQtThreads, 2)
     };
 
     if (tid == 0) {
-        for (int st = 0; st < kQtStages; ++st) mbar_init(smem_u32(full + st), 1);
-        *abort_flag = 0;
-        fence_mbar_init();
-        for (int i = 0; i < a.num_tensors; ++i)
-            if (a.t[i].rows > 0 && a.t[i].cols > 0) prefetch_tmap(&a.maps[i]);
         for (int st = 0; st < kQtStages; ++st) {
             const int64_t t = blockIdx.x + static_cast<int64_t>(st) * gridDim.x;
             if (t < a.num_tiles) issue(st, t);
@@ -375,6 +381,8 @@ __global__ void __launch_bounds__(256) ln_stats_kernel(const uint16_t *__restric
                                                        float *__restrict__ mean,
                                                        float *__restrict__ rstd,
                                                        unsigned *__restrict__ amax_bits) {
+    pdl_wait();
+    pdl_trigger();
     const int lane = threadIdx.x & 31;
     const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
     const int64_t nvec = cols / 8;
@@ -383,8 +391,9 @@ __global__ void __launch_bounds__(256) ln_stats_kernel(const uint16_t *__restric
     for (int64_t r = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; r < rows;
          r += warps) {
         const uint4 *xr = reinterpret_cast<const uint4 *>(x + r * cols);
-        // four 16-byte loads in flight per lane in both passes
-        float sum = 0.0f;
+        // four 16-byte loads in flight per lane, eight independent partial
+        // sums per lane (one per element position of a 16-byte vector)
+        float part[8] = {0, 0, 0, 0, 0, 0, 0, 0};
         for (int64_t i = lane; i < nvec; i += 128) {
             uint4 v[4];
 #pragma unroll
@@ -394,12 +403,18 @@ __global__ void __launch_bounds__(256) ln_stats_kernel(const uint16_t *__restric
             for (int u = 0; u < 4; ++u) {
                 const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
 #pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    sum = __fadd_rn(__fadd_rn(sum, bf16_lo(w[j])), bf16_hi(w[j]));
+                for (int j = 0; j < 4; ++j) {
+                    part[2 * j] = __fadd_rn(part[2 * j], bf16_lo(w[j]));
+                    part[2 * j + 1] = __fadd_rn(part[2 * j + 1], bf16_hi(w[j]));
+                }
             }
         }
+        float sum = 0.0f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) sum = __fadd_rn(sum, part[j]);
         const float mu = __fmul_rn(warp_sum(sum), inv_c);
-        float sq = 0.0f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) part[j] = 0.0f;
         for (int64_t i = lane; i < nvec; i += 128) {
             uint4 v[4];
 #pragma unroll
@@ -413,10 +428,14 @@ __global__ void __launch_bounds__(256) ln_stats_kernel(const uint16_t *__restric
                 for (int j = 0; j < 4; ++j) {
                     const float d0 = __fsub_rn(bf16_lo(w[j]), mu);
                     const float d1 = __fsub_rn(bf16_hi(w[j]), mu);
-                    sq = __fadd_rn(__fadd_rn(sq, __fmul_rn(d0, d0)), __fmul_rn(d1, d1));
+                    part[2 * j] = __fadd_rn(part[2 * j], __fmul_rn(d0, d0));
+                    part[2 * j + 1] = __fadd_rn(part[2 * j + 1], __fmul_rn(d1, d1));
                 }
             }
         }
+        float sq = 0.0f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) sq = __fadd_rn(sq, part[j]);
         const float var = __fmul_rn(warp_sum(sq), inv_c);
         const float rs = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(var, eps)));
         if (lane == 0) {
@@ -464,11 +483,10 @@ cudaError_t launch_ln_stats(const void *x, const void *gamma, const void *beta, 
     int64_t blocks = (rows + 7) / 8;
     const int64_t cap = static_cast<int64_t>(sm_count) * 8;
     if (blocks > cap) blocks = cap;
-    ln_stats_kernel<<<static_cast<unsigned>(blocks), threads, 0, st>>>(
-        reinterpret_cast<const uint16_t *>(x), reinterpret_cast<const uint16_t *>(gamma),
-        reinterpret_cast<const uint16_t *>(beta), rows, cols, eps, mean, rstd,
-        reinterpret_cast<unsigned *>(amax));
-    return cudaGetLastError();
+    return launch_pdl(ln_stats_kernel, dim3(static_cast<unsigned>(blocks)), dim3(threads), 0, st,
+                      reinterpret_cast<const uint16_t *>(x), reinterpret_cast<const uint16_t *>(gamma),
+                      reinterpret_cast<const uint16_t *>(beta), rows, cols, eps, mean, rstd,
+                      reinterpret_cast<unsigned *>(amax));
 }
 
 // ----------------------------------------------------------- scale update --
@@ -480,9 +498,11 @@ cudaError_t launch_ln_stats(const void *x, const void *gamma, const void *beta, 
 constexpr int kUpdThreads = 256;
 
 __global__ void __launch_bounds__(kUpdThreads) scale_update_kernel(
-    float *__restrict__ history, const float *__restrict__ amax, float *__restrict__ scale,
-    float *__restrict__ scale_inv, int L, uint32_t format_mask, int margin) {
+    float *__restrict__ history, float *__restrict__ amax, float *__restrict__ scale,
+    float *__restrict__ scale_inv, int L, uint32_t format_mask, int margin, int clear_amax) {
     extern __shared__ float old_hist[];
+    pdl_wait();
+    pdl_trigger();
     const int t = blockIdx.x;
     float *h = history + static_cast<int64_t>(t) * L;
     for (int i = threadIdx.x; i < L; i += blockDim.x) old_hist[i] = h[i];
@@ -509,6 +529,8 @@ __global__ void __launch_bounds__(kUpdThreads) scale_update_kernel(
             scale[t] = sc;
             scale_inv[t] = __fdiv_rn(1.0f, sc);
         }
+        // the amax has been pushed into the history: start the next step at 0
+        if (clear_amax) amax[t] = 0.0f;
     }
 }
 
@@ -523,9 +545,8 @@ cudaError_t launch_amax(const void *x, int64_t n, float *amax, int sm_count, cud
     const int64_t cap = static_cast<int64_t>(sm_count) * 4;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
-    amax_kernel<<<static_cast<unsigned>(blocks), threads, 0, st>>>(
-        reinterpret_cast<const uint4 *>(x), nvec, reinterpret_cast<unsigned *>(amax));
-    return cudaGetLastError();
+    return launch_pdl(amax_kernel, dim3(static_cast<unsigned>(blocks)), dim3(threads), 0, st,
+                      reinterpret_cast<const uint4 *>(x), nvec, reinterpret_cast<unsigned *>(amax));
 }
 
 template <int FMT, bool CURRENT>
@@ -541,9 +562,8 @@ static cudaError_t qt_launch(const CastArgs &args, int sm_count, cudaStream_t st
     if (args.num_tiles == 0) return cudaSuccess;
     int64_t blocks = static_cast<int64_t>(sm_count) * 2;
     if (blocks > args.num_tiles) blocks = args.num_tiles;
-    quantize_transpose_kernel<FMT, CURRENT>
-        <<<static_cast<unsigned>(blocks), kQtThreads, kQtSmem, st>>>(args);
-    return cudaGetLastError();
+    return launch_pdl(quantize_transpose_kernel<FMT, CURRENT>, dim3(static_cast<unsigned>(blocks)),
+                      dim3(kQtThreads), kQtSmem, st, args);
 }
 
 // Fill the launch arguments for up to two tensors; false if a TMA
@@ -630,9 +650,9 @@ cudaError_t launch_quantize_transpose_current(const void *x, int64_t rows, int64
     return launch_cast_group(&c, 1, fmt, true, margin, sm_count, st);
 }
 
-cudaError_t launch_scale_update(float *history, const float *amax, float *scale, float *scale_inv,
+cudaError_t launch_scale_update(float *history, float *amax, float *scale, float *scale_inv,
                                 int num_tensors, int L, uint32_t format_mask, int margin,
-                                cudaStream_t st) {
+                                bool clear_amax, cudaStream_t st) {
     const size_t smem = static_cast<size_t>(L) * sizeof(float);
     if (smem > 48 * 1024) {
         static bool raised = false;
@@ -643,9 +663,8 @@ cudaError_t launch_scale_update(float *history, const float *amax, float *scale,
             raised = true;
         }
     }
-    scale_update_kernel<<<num_tensors, kUpdThreads, smem, st>>>(history, amax, scale, scale_inv, L,
-                                                                format_mask, margin);
-    return cudaGetLastError();
+    return launch_pdl(scale_update_kernel, dim3(num_tensors), dim3(kUpdThreads), smem, st, history,
+                      amax, scale, scale_inv, L, format_mask, margin, clear_amax ? 1 : 0);
 }
 
 }  // namespace fp8k

@@ -151,6 +151,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_tn_kernel(const __grid_co
     }
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    // the prologue above touched only this CTA's own memory
+    pdl_wait();
+    pdl_trigger();
 
     if (warp == 0) {
         // ------------------------------------------------------ TMA producer
@@ -391,18 +394,22 @@ cudaError_t set_smem_attr() {
     return err;
 }
 
-cudaLaunchConfig_t pair_config(int grid, cudaLaunchAttribute *attr, cudaStream_t st) {
+// attr must have room for two attributes: the cluster shape and, with pdl,
+// programmatic stream serialization.
+cudaLaunchConfig_t pair_config(int grid, cudaLaunchAttribute *attr, cudaStream_t st, bool pdl) {
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
     cfg.blockDim = dim3(NUM_THREADS, 1, 1);
     cfg.dynamicSmemBytes = Cfg<true>::SMEM;
     cfg.stream = st;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = pdl ? 2 : 1;
     return cfg;
 }
 
@@ -413,8 +420,8 @@ int pair_slots(int sm_count) {
     static int slots = 0;
     std::call_once(once, [sm_count] {
         if (set_smem_attr<true>() != cudaSuccess) return;
-        cudaLaunchAttribute attr[1];
-        cudaLaunchConfig_t cfg = pair_config(sm_count & ~1, attr, nullptr);
+        cudaLaunchAttribute attr[2];
+        cudaLaunchConfig_t cfg = pair_config(sm_count & ~1, attr, nullptr, false);
         int n = 0;
         if (cudaOccupancyMaxActiveClusters(&n, gemm_tn_kernel<true>, &cfg) != cudaSuccess || n < 1)
             n = 0;
@@ -475,15 +482,15 @@ cudaError_t launch_gemm_group(const GemmSpec *specs, int n, int sm_count, cudaSt
         cudaError_t e = set_smem_attr<true>();
         if (e != cudaSuccess) return e;
         const int units = tiles < slots ? tiles : slots;
-        cudaLaunchAttribute attr[1];
-        cudaLaunchConfig_t cfg = pair_config(2 * units, attr, st);
+        cudaLaunchAttribute attr[2];
+        cudaLaunchConfig_t cfg = pair_config(2 * units, attr, st, true);
         return cudaLaunchKernelEx(&cfg, gemm_tn_kernel<true>, a);
     }
     cudaError_t e = set_smem_attr<false>();
     if (e != cudaSuccess) return e;
     const int grid = tiles < sm_count ? tiles : sm_count;
-    gemm_tn_kernel<false><<<grid, NUM_THREADS, Cfg<false>::SMEM, st>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(gemm_tn_kernel<false>, dim3(grid), dim3(NUM_THREADS), Cfg<false>::SMEM, st,
+                      a);
 }
 
 cudaError_t launch_gemm_tn(const uint8_t *A, int fa, const uint8_t *B, int fb, int64_t M,

@@ -63,10 +63,11 @@ cudaError_t launch_quantize_transpose_current(const void *x, int64_t rows, int64
                                               float *amax, float *scale, float *scale_inv,
                                               int sm_count, cudaStream_t st);
 
-// History shift + scale / scale_inv update of num_tensors states.
-cudaError_t launch_scale_update(float *history, const float *amax, float *scale, float *scale_inv,
+// History shift + scale / scale_inv update of num_tensors states; with
+// clear_amax the amax words are set to 0 once pushed into the history.
+cudaError_t launch_scale_update(float *history, float *amax, float *scale, float *scale_inv,
                                 int num_tensors, int L, uint32_t format_mask, int margin,
-                                cudaStream_t st);
+                                bool clear_amax, cudaStream_t st);
 
 // One GEMM of a grouped launch: D[M][N] = A[M][K] . B[N][K]^T (FP8 codes of
 // formats fa / fb), dequantised by a_scale_inv * b_scale_inv into BF16, with

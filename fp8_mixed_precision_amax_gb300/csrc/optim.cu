@@ -6,7 +6,7 @@
 // Per element, in binary32 with one rounding per operation (AdamW's
 // decoupled weight decay):
 //   m = b1*m + (1-b1)*g;  v = b2*v + (1-b2)*(g*g)
-//   u = (m / bc1) / (sqrt(v / bc2) + eps);  w = w - lr*(u + wd*w)
+//   u = (m * fl32(1/bc1)) / (sqrt(v * fl32(1/bc2)) + eps);  w = w - lr*(u + wd*w)
 // m is decoded from E4M3 codes times the first moment's scale_inv, w from
 // FP16 codes times the weights' scale_inv.  The new states get just-in-time
 // per-tensor scales (fmax / amax of the new values, a history of one):
@@ -72,6 +72,7 @@ __device__ __forceinline__ void adam8(const AdamArgs &a, int64_t i, float msi, f
     const uint32_t gw[4] = {g4.x, g4.y, g4.z, g4.w}, vw[4] = {v4.x, v4.y, v4.z, v4.w},
                    ww[4] = {w4.x, w4.y, w4.z, w4.w}, mw[2] = {m8.x, m8.y};
     const float omb1 = __fsub_rn(1.0f, a.b1), omb2 = __fsub_rn(1.0f, a.b2);
+    const float rbc1 = __fdiv_rn(1.0f, a.bc1), rbc2 = __fdiv_rn(1.0f, a.bc2);
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
         float md[2];
@@ -85,8 +86,8 @@ __device__ __forceinline__ void adam8(const AdamArgs &a, int64_t i, float msi, f
             float w = __fmul_rn(f16_dec(static_cast<uint16_t>(ww[j] >> (16 * h))), wsi);
             m = __fadd_rn(__fmul_rn(a.b1, m), __fmul_rn(omb1, g));
             v = __fadd_rn(__fmul_rn(a.b2, v), __fmul_rn(omb2, __fmul_rn(g, g)));
-            const float u = __fdiv_rn(__fdiv_rn(m, a.bc1),
-                                      __fadd_rn(__fsqrt_rn(__fdiv_rn(v, a.bc2)), a.eps));
+            const float u = __fdiv_rn(__fmul_rn(m, rbc1),
+                                      __fadd_rn(__fsqrt_rn(__fmul_rn(v, rbc2)), a.eps));
             w = __fsub_rn(w, __fmul_rn(a.lr, __fadd_rn(u, __fmul_rn(a.wd, w))));
             e.m[k] = m;
             e.v[k] = v;
@@ -101,6 +102,8 @@ __device__ __forceinline__ uint32_t abs_bits(float x) {
 }
 
 __global__ void __launch_bounds__(256) adam_amax_kernel(const AdamArgs a) {
+    pdl_wait();
+    pdl_trigger();
     const float msi = *a.m1_scale_inv, wsi = *a.w_scale_inv;
     uint32_t mm = 0, mw = 0;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x * 8;
@@ -123,6 +126,8 @@ __global__ void __launch_bounds__(256) adam_amax_kernel(const AdamArgs a) {
 }
 
 __global__ void __launch_bounds__(256) adam_apply_kernel(const AdamArgs a) {
+    pdl_wait();
+    pdl_trigger();
     const float msi = *a.m1_scale_inv, wsi = *a.w_scale_inv;
     bool valid;
     const float sm = recipe_scale(a.amax[0], 448.0f, a.margin, *a.m1_scale, valid);
@@ -154,6 +159,8 @@ __global__ void __launch_bounds__(256) adam_apply_kernel(const AdamArgs a) {
 }
 
 __global__ void adam_scales_kernel(const AdamArgs a) {
+    pdl_wait();
+    pdl_trigger();
     bool valid;
     const float sm = recipe_scale(a.amax[0], 448.0f, a.margin, *a.m1_scale, valid);
     if (valid) {
@@ -192,6 +199,8 @@ __global__ void __launch_bounds__(256) dequant_sum_kernel(const uint8_t *__restr
                                                           int nranks, int64_t n,
                                                           const float *__restrict__ scale,
                                                           uint16_t *__restrict__ out) {
+    pdl_wait();
+    pdl_trigger();
     const double sinv = static_cast<double>(__fdiv_rn(1.0f, *scale));
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x * 8;
     for (int64_t i = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) * 8; i < n;
@@ -229,13 +238,9 @@ cudaError_t launch_dequant_sum(const uint8_t *parts, int nranks, int64_t n, int 
     const int64_t cap = static_cast<int64_t>(sm_count) * 8;
     if (blocks > cap) blocks = cap;
     auto *o = static_cast<uint16_t *>(out);
-    if (fmt == 0)
-        dequant_sum_kernel<0><<<static_cast<unsigned>(blocks), threads, 0, st>>>(parts, nranks, n,
-                                                                                 scale, o);
-    else
-        dequant_sum_kernel<1><<<static_cast<unsigned>(blocks), threads, 0, st>>>(parts, nranks, n,
-                                                                                 scale, o);
-    return cudaGetLastError();
+    const dim3 g(static_cast<unsigned>(blocks)), b(threads);
+    if (fmt == 0) return launch_pdl(dequant_sum_kernel<0>, g, b, 0, st, parts, nranks, n, scale, o);
+    return launch_pdl(dequant_sum_kernel<1>, g, b, 0, st, parts, nranks, n, scale, o);
 }
 
 cudaError_t launch_adam_step(const AdamSpec &s, int sm_count, cudaStream_t st) {
@@ -249,13 +254,11 @@ cudaError_t launch_adam_step(const AdamSpec &s, int sm_count, cudaStream_t st) {
         int64_t blocks = (s.n / 8 + threads - 1) / threads;
         const int64_t cap = static_cast<int64_t>(sm_count) * 8;
         if (blocks > cap) blocks = cap;
-        adam_amax_kernel<<<static_cast<unsigned>(blocks), threads, 0, st>>>(a);
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
-        adam_apply_kernel<<<static_cast<unsigned>(blocks), threads, 0, st>>>(a);
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        const dim3 g(static_cast<unsigned>(blocks)), b(threads);
+        if ((e = launch_pdl(adam_amax_kernel, g, b, 0, st, a)) != cudaSuccess) return e;
+        if ((e = launch_pdl(adam_apply_kernel, g, b, 0, st, a)) != cudaSuccess) return e;
     }
-    adam_scales_kernel<<<1, 1, 0, st>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(adam_scales_kernel, dim3(1), dim3(1), 0, st, a);
 }
 
 }  // namespace fp8k

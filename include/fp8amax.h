@@ -176,7 +176,8 @@ fp8_status fp8_scale_update(float *history, const float *amax, float *scale, flo
 
 /* The recipe's update of all five slots of one layer, run once per step
  * after fp8_linear_fwd and fp8_linear_bwd: fp8_scale_update over meta with
- * the recipe's formats (HYBRID: slots dY and dX are E5M2).
+ * the recipe's formats (HYBRID: slots dY and dX are E5M2), after which the
+ * five amax slots are cleared to 0 for the next step.
  * meta->history_len must equal recipe->history_len. */
 fp8_status fp8_amax_scale_update(const fp8_meta *meta, const fp8_recipe *recipe, void *stream);
 
@@ -269,7 +270,12 @@ fp8_status fp8_layernorm_linear_fwd(const void *X, const void *gamma, const void
  *   X8, X8t  DEVICE [M][K] and [K][M] FP8 (E4M3), written; X8t is kept for wgrad
  *   W8, W8t  DEVICE [N][K] and [K][N] FP8 (E4M3), written; W8t is kept for dgrad
  *   Y   DEVICE [M][N] BF16 output
- * Writes meta->amax[X], amax[W], amax[Y]. */
+ * Max-combines the amax of X, W and Y into meta->amax[X], [W], [Y]: the
+ * slots hold the running max since the last fp8_amax_scale_update, which
+ * clears them (a fresh meta has them at 0), so several forward calls before
+ * one update (micro-batches) record the max over all of them.  Under
+ * FP8_SCALING_CURRENT the X and W slots are overwritten with this call's
+ * amax instead. */
 fp8_status fp8_linear_fwd(const void *X, const void *W, int64_t M, int64_t N, int64_t K,
                           const fp8_meta *meta, const fp8_recipe *recipe, uint8_t *X8,
                           uint8_t *X8t, uint8_t *W8, uint8_t *W8t, void *Y, void *stream);
@@ -281,7 +287,9 @@ fp8_status fp8_linear_fwd(const void *X, const void *W, int64_t M, int64_t N, in
  *   X8t, W8t  DEVICE, the transposed copies written by fp8_linear_fwd
  *   dY8, dY8t DEVICE [M][N] and [N][M] FP8 work buffers, written
  *   dX  DEVICE [M][K] BF16;  dW  DEVICE [N][K] BF16
- * Writes meta->amax[dY], amax[dX]. */
+ * Max-combines the amax of dY and dX into meta->amax[dY], [dX] (as
+ * fp8_linear_fwd does for its slots; under FP8_SCALING_CURRENT the dY slot is
+ * overwritten with this call's amax). */
 fp8_status fp8_linear_bwd(const void *dY, int64_t M, int64_t N, int64_t K, const fp8_meta *meta,
                           const fp8_recipe *recipe, const uint8_t *X8t, const uint8_t *W8t,
                           uint8_t *dY8, uint8_t *dY8t, void *dX, void *dW, void *stream);
@@ -301,7 +309,7 @@ typedef struct {
  * the note's 6 also counts an FP8 gradient, which this path keeps BF16).  In
  * binary32, one rounding per operation, for every element:
  *   m = b1*m + (1-b1)*g;  v = b2*v + (1-b2)*(g*g);
- *   u = (m / bc1) / (sqrt(v / bc2) + eps);  w = w - lr*(u + wd*w)
+ *   u = (m * fl32(1/bc1)) / (sqrt(v * fl32(1/bc2)) + eps);  w = w - lr*(u + wd*w)
  * with m = E4M3 code * m1_scale_inv and w = FP16 code * w_scale_inv.  The new
  * states take just-in-time per-tensor scales: scale = (fmax / amax) /
  * 2^margin of the new values (fmax 448 for m, 65504 for w), kept when that

@@ -394,7 +394,7 @@ uint16_t or_f16_encode(float f)
 /* weights FP16 with tensor scaling).  All arithmetic in binary32, one       */
 /* rounding per operation, in this order (AdamW's decoupled weight decay):   */
 /*   m  = b1*m + (1-b1)*g,   v = b2*v + (1-b2)*(g*g)                         */
-/*   u  = (m / bc1) / (sqrt(v / bc2) + eps)                                   */
+/*   u  = (m * fl32(1/bc1)) / (sqrt(v * fl32(1/bc2)) + eps)                   */
 /*   w  = w - lr*(u + wd*w)                                                   */
 /* with m decoded from its E4M3 codes times m_sinv and w from its FP16 codes */
 /* times w_sinv.  Just-in-time per-tensor scaling of the new states:         */
@@ -409,7 +409,7 @@ static void adam_elem(float g, float m, float v, float w, float lr, float b1, fl
 {
     m = b1 * m + (1.0f - b1) * g;
     v = b2 * v + (1.0f - b2) * (g * g);
-    float u = (m / bc1) / (sqrtf(v / bc2) + eps);
+    float u = (m * (1.0f / bc1)) / (sqrtf(v * (1.0f / bc2)) + eps);
     w = w - lr * (u + wd * w);
     *mo = m;
     *vo = v;

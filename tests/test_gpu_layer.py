@@ -32,12 +32,14 @@ def _row_blocks(n, width=16):
     return sorted({0, (n // 2 // 16) * 16 + 48 if n > 128 else 0, n - width})
 
 
-def _gpu_slot_checks(lin, f, gpu_amax_hist, fmts, margin):
-    """Y / dX slots: properties that hold at any size."""
+def _gpu_slot_checks(lin, f, gpu_amax_hist, fmts, margin, g_amax):
+    """Y / dX slots: properties that hold at any size (g_amax: the amax slots
+    as the step left them, before the update consumed and cleared them)."""
     hist = lin.meta.history.cpu().numpy()
     scale = lin.meta.scale.cpu().numpy()
+    assert not lin.meta.amax.cpu().numpy().any()       # cleared by the update
     for slot, out in ((f.SLOT_Y, lin.Y), (f.SLOT_DX, lin.dX)):
-        a = lin.meta.amax[slot].item()
+        a = float(g_amax[slot])
         vals = np.abs(bf16_values(host_bf16_bits(out)))
         mx = np.float32(np.nanmax(vals) if not np.isnan(vals).all() else 0.0)   # NaN skipped
         assert f32_bits(np.float32(a)) == f32_bits(mx), (slot, a, mx)
@@ -128,7 +130,7 @@ def run_layer(w: wl.Workload, steps, check_every=1, full=True, hybrid=None, extr
             assert np.array_equal(hist[slot].view(np.uint32), st.history[slot].view(np.uint32))
             assert f32_bits(lin.meta.scale[slot].item()) == f32_bits(st.scale[slot]), (step, slot)
             assert f32_bits(lin.meta.scale_inv[slot].item()) == f32_bits(st.scale_inv[slot])
-        _gpu_slot_checks(lin, f, gpu_amax_hist, fm, w.margin)
+        _gpu_slot_checks(lin, f, gpu_amax_hist, fm, w.margin, g_amax)
     f.fp8_sync_status()
     return report
 

@@ -70,3 +70,4 @@ def test_layer_update_formats_follow_recipe():
         assert np.array_equal(meta.scale.cpu().numpy(), st.scale)
         assert np.array_equal(meta.scale_inv.cpu().numpy(), st.scale_inv)
         assert np.array_equal(meta.history.cpu().numpy(), st.history)
+        assert not meta.amax.cpu().numpy().any()       # consumed and cleared
