@@ -78,6 +78,7 @@ def _load() -> ctypes.CDLL:
         "fp8_sync_status": ([vp], ctypes.c_int),
         "fp8_amax": ([vp, i64, vp, vp], ctypes.c_int),
         "fp8_quantize_transpose": ([vp, i64, i64, vp, i32, vp, vp, vp, vp], ctypes.c_int),
+        "fp8_quantize_f32": ([vp, i64, vp, i32, vp, vp, vp], ctypes.c_int),
         "fp8_quantize_transpose_current": ([vp, i64, i64, i32, i32, vp, vp, vp, vp, vp, vp],
                                            ctypes.c_int),
         "fp8_scale_update": ([vp, vp, vp, vp, i32, i32, u32, i32, vp], ctypes.c_int),
@@ -107,7 +108,7 @@ def _load() -> ctypes.CDLL:
     for name, (args, res) in sig.items():
         f = getattr(lib, name)
         f.argtypes, f.restype = args, res
-    if lib.fp8_abi_version() != 2:
+    if lib.fp8_abi_version() != 3:
         raise ImportError("libfp8amax.so ABI version mismatch")
     return lib
 
@@ -174,6 +175,17 @@ def fp8_sync_status(stream=None) -> None:
 def fp8_amax(x: torch.Tensor, amax: torch.Tensor, stream=None) -> None:
     _check(_lib.fp8_amax(_ptr(x, torch.bfloat16, "x"), x.numel(), _ptr(amax, torch.float32, "amax"),
                          _stream(stream)))
+
+
+def fp8_quantize_f32(x: torch.Tensor, scale: torch.Tensor, fmt: int, out: torch.Tensor,
+                     amax=None, stream=None) -> None:
+    """Scaled cast of a contiguous fp32 tensor to FP8 codes (uint8, same
+    number of elements), optionally overwriting amax with max |x|."""
+    if out.numel() != x.numel():
+        raise ValueError("out must have as many elements as x")
+    _check(_lib.fp8_quantize_f32(_ptr(x, torch.float32, "x"), x.numel(),
+                                 _ptr(scale, torch.float32, "scale"), fmt, _p8(out, "out"),
+                                 _ptr(amax, torch.float32, "amax"), _stream(stream)))
 
 
 def fp8_quantize_transpose(x: torch.Tensor, scale: torch.Tensor, fmt: int, out=None, out_t=None,

@@ -153,6 +153,23 @@ fp8_status fp8_amax(const void *x, int64_t n, float *amax, void *stream) {
     return FP8_OK;
 }
 
+fp8_status fp8_quantize_f32(const float *x, int64_t n, const float *scale, int32_t fmt,
+                            uint8_t *out, float *amax, void *stream) {
+    const char *fn = "fp8_quantize_f32";
+    FP8_TRY(check_dims16(fn, n, "n", 0, "-"));
+    if (fmt != FP8_E4M3 && fmt != FP8_E5M2) return fail(FP8_ERR_ARG, "%s: bad format %d", fn, fmt);
+    FP8_TRY(check_ptr(fn, x, "x", n == 0));
+    FP8_TRY(check_scalar(fn, scale, "scale", false));
+    FP8_TRY(check_ptr(fn, out, "out", n == 0));
+    FP8_TRY(check_scalar(fn, amax, "amax", true));
+    int sms;
+    FP8_TRY(current_device(&sms));
+    FP8_CUDA(fp8k::launch_quantize_f32(x, n, scale, fmt, out, amax, sms,
+                                       static_cast<cudaStream_t>(stream)),
+             fn);
+    return FP8_OK;
+}
+
 fp8_status fp8_quantize_transpose(const void *x, int64_t rows, int64_t cols, const float *scale,
                                   int32_t fmt, uint8_t *out, uint8_t *out_t, float *amax,
                                   void *stream) {

@@ -62,6 +62,48 @@ __global__ void __launch_bounds__(512) amax_kernel(const uint4 *__restrict__ x, 
     }
 }
 
+// ------------------------------------------------------ fp32 scaled cast --
+
+// q_i = satRNE(fl32(x_i * s)) of an fp32 tensor, element order kept, with
+// amax(x) fused (NaN skipped, integer max on magnitude bits).  Grid-stride,
+// eight values per thread and iteration: two 16-byte streaming loads and one
+// 8-byte store.
+template <int FMT>
+__global__ void __launch_bounds__(256)
+    quantize_f32_kernel(const float4 *__restrict__ x, int64_t n8, const float *__restrict__ scale,
+                        uint2 *__restrict__ out, unsigned *__restrict__ amax_bits) {
+    pdl_wait();
+    pdl_trigger();
+    const float s = *scale;
+    uint32_t m = 0;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8;
+         i += stride) {
+        const float4 a = __ldcs(x + 2 * i), b = __ldcs(x + 2 * i + 1);
+        const float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const uint32_t u = __float_as_uint(v[j]) & 0x7FFFFFFFu;
+            m = max(m, u > 0x7F800000u ? 0u : u);
+        }
+        uint32_t w[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            w[j] = cvt2_fp8<FMT>(__fmul_rn(v[2 * j], s), __fmul_rn(v[2 * j + 1], s));
+        __stcs(out + i, make_uint2(w[0] | (w[1] << 16), w[2] | (w[3] << 16)));
+    }
+    m = __reduce_max_sync(0xFFFFFFFFu, m);
+    __shared__ uint32_t warp_max[8];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (lane == 0) warp_max[warp] = m;
+    __syncthreads();
+    if (warp == 0) {
+        m = lane < static_cast<int>(blockDim.x >> 5) ? warp_max[lane] : 0u;
+        m = __reduce_max_sync(0xFFFFFFFFu, m);
+        if (lane == 0 && m != 0 && amax_bits != nullptr) atomicMax(amax_bits, m);
+    }
+}
+
 // ----------------------------------------------------- quantize_transpose --
 //
 // Persistent CTAs of 256 threads (two per SM) convert 128 x 128 tiles.  The
@@ -547,6 +589,26 @@ cudaError_t launch_amax(const void *x, int64_t n, float *amax, int sm_count, cud
     if (blocks < 1) blocks = 1;
     return launch_pdl(amax_kernel, dim3(static_cast<unsigned>(blocks)), dim3(threads), 0, st,
                       reinterpret_cast<const uint4 *>(x), nvec, reinterpret_cast<unsigned *>(amax));
+}
+
+cudaError_t launch_quantize_f32(const float *x, int64_t n, const float *scale, int fmt,
+                                uint8_t *out, float *amax, int sm_count, cudaStream_t st) {
+    if (amax != nullptr) {
+        cudaError_t e = cudaMemsetAsync(amax, 0, sizeof(float), st);
+        if (e != cudaSuccess) return e;
+    }
+    if (n == 0) return cudaSuccess;
+    const int64_t n8 = n / 8;
+    const int threads = 256;
+    int64_t blocks = (n8 + threads - 1) / threads;
+    const int64_t cap = static_cast<int64_t>(sm_count) * 8;
+    if (blocks > cap) blocks = cap;
+    const dim3 grid(static_cast<unsigned>(blocks)), block(threads);
+    const float4 *xv = reinterpret_cast<const float4 *>(x);
+    uint2 *ov = reinterpret_cast<uint2 *>(out);
+    unsigned *ab = reinterpret_cast<unsigned *>(amax);
+    return fmt == 0 ? launch_pdl(quantize_f32_kernel<0>, grid, block, 0, st, xv, n8, scale, ov, ab)
+                    : launch_pdl(quantize_f32_kernel<1>, grid, block, 0, st, xv, n8, scale, ov, ab);
 }
 
 template <int FMT, bool CURRENT>

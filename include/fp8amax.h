@@ -62,7 +62,7 @@
 extern "C" {
 #endif
 
-#define FP8AMAX_ABI_VERSION 2
+#define FP8AMAX_ABI_VERSION 3
 
 typedef enum { FP8_E4M3 = 0, FP8_E5M2 = 1 } fp8_format;
 
@@ -146,6 +146,18 @@ fp8_status fp8_amax(const void *x, int64_t n, float *amax, void *stream);
 fp8_status fp8_quantize_transpose(const void *x, int64_t rows, int64_t cols, const float *scale,
                                   int32_t fmt, uint8_t *out, uint8_t *out_t, float *amax,
                                   void *stream);
+
+/* Scaled cast of an fp32 tensor to FP8 (the Q node of the TensorRT page on
+ * fp32 values, such as the fp32 quantities that FP8-LM stores in FP8, wiki
+ * note "extension to FP8"): q_i = satRNE_fmt(fl32(x_i * scale)) in element
+ * order, with the same rounding, saturation and NaN rules as the BF16 cast.
+ *   x      DEVICE, n fp32 values, 16-byte aligned (n >= 0, multiple of 16)
+ *   scale  DEVICE, 1 float, read on the device
+ *   fmt    FP8_E4M3 or FP8_E5M2
+ *   out    DEVICE, n FP8 codes, 16-byte aligned (may be NULL when n == 0)
+ *   amax   DEVICE, 1 float overwritten with max |x_i| (NaN skipped), or NULL */
+fp8_status fp8_quantize_f32(const float *x, int64_t n, const float *scale, int32_t fmt,
+                            uint8_t *out, float *amax, void *stream);
 
 /* Just-in-time (current) scaling of one tensor (wiki note, "per-tensor
  * scaling is the key": the scale comes from the tensor itself): amax(x),

@@ -9,12 +9,12 @@ together in the order the pages give them.
 
 What each function follows:
 
-* ``quantize`` / ``fp8_encode`` / ``fp8_decode`` -- the E4M3 / E5M2 formats of
+* ``quantize`` / ``quantize_f32`` / ``fp8_encode`` / ``fp8_decode`` -- the E4M3 / E5M2 formats of
   "NVIDIA Transformer Engine and FP8 mixed precision: implementation guide",
   section "What are Transformer Engine and FP8 mixed precision", and the
   maxima 448 / 57,344 of the "Definition" table of the "Mixed-precision
   training" wiki note; the Q node of "FP8 quantization with NVIDIA TensorRT".
-* ``amax`` -- dynamic scaling's range monitoring (implementation guide, same
+* ``amax`` / ``amax_f32`` -- dynamic scaling's range monitoring (implementation guide, same
   section) and the Absolute-Max statistic (TensorRT page).
 * ``history_update`` -- DelayedScaling's margin / amax_history_len
   (implementation guide, section "Dynamic scaling and the FP8 recipe") with
@@ -89,6 +89,9 @@ def _lib():
         lib.or_amax_bf16.argtypes, lib.or_amax_bf16.restype = [vp, i64], f32
         lib.or_quantize.argtypes = [vp, i64, i64, f32, ctypes.c_int, vp, vp]
         lib.or_quantize.restype = None
+        lib.or_quantize_f32.argtypes = [vp, i64, f32, ctypes.c_int, vp]
+        lib.or_quantize_f32.restype = None
+        lib.or_amax_f32.argtypes, lib.or_amax_f32.restype = [vp, i64], f32
         lib.or_history_update.argtypes = [vp, i32, f32, vp, vp, ctypes.c_int, i32]
         lib.or_history_update.restype = None
         lib.or_gemm_tn_f64.argtypes = [vp, ctypes.c_int, vp, ctypes.c_int, i64, i64, i64, i64, i64, vp]
@@ -179,6 +182,20 @@ def quantize(x_bf16: np.ndarray, scale, fmt: int, transpose: bool = True):
     _lib().or_quantize(x.ctypes.data, rows, cols, float(np.float32(scale)), fmt,
                        q.ctypes.data, qt.ctypes.data if transpose else None)
     return q, qt
+
+
+def quantize_f32(x: np.ndarray, scale, fmt: int) -> np.ndarray:
+    """Scaled saturating cast of an fp32 tensor, element order kept."""
+    x = _c(x, np.float32)
+    q = np.empty(x.shape, dtype=np.uint8)
+    _lib().or_quantize_f32(x.ctypes.data, x.size, float(np.float32(scale)), fmt, q.ctypes.data)
+    return q
+
+
+def amax_f32(x: np.ndarray) -> np.float32:
+    """max |x| over an fp32 tensor, NaN skipped."""
+    x = _c(x, np.float32)
+    return np.float32(_lib().or_amax_f32(x.ctypes.data, x.size))
 
 
 def history_update(hist: np.ndarray, amax_new, scale, scale_inv, fmt: int, margin: int):

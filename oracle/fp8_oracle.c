@@ -204,6 +204,26 @@ void or_quantize(const uint16_t *x, int64_t rows, int64_t cols, float scale, int
     }
 }
 
+/* The same scaled cast of an fp32 tensor, in element order, and its amax   */
+/* (the Q node applied to binary32 values; amax as for BF16, NaN skipped).   */
+void or_quantize_f32(const float *x, int64_t n, float scale, int fmt, uint8_t *out)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = or_fp8_encode_f32(x[i] * scale, fmt); /* binary32 multiply */
+}
+
+float or_amax_f32(const float *x, int64_t n)
+{
+    float m = 0.0f;
+    for (int64_t i = 0; i < n; ++i) {
+        float a = fabsf(x[i]);
+        if (a > m) /* false for NaN */
+            m = a;
+    }
+    return m;
+}
+
 /* ------------------------------------------------------------------------ */
 /* Delayed-scaling update of one tensor's state ([P1] DelayedScaling:        */
 /* margin, amax_history_len; the scale formula above).                       */

@@ -214,3 +214,66 @@ def test_grouped_cast_of_two_tensors(fmt):
             assert_fp8_equal(host_u8(out), q, fmt, "grouped out")
             assert_fp8_equal(host_u8(out_t), qt, fmt, "grouped out_t")
             assert f32_bits(am.cpu().numpy()[0]) == f32_bits(o.amax(xb))
+
+
+# ------------------------------------------------- fp32 scaled cast (S3) --
+
+def _cast_f32(x: torch.Tensor, scale, fmt):
+    f = _lib()
+    out = torch.full((x.numel(),), 0xAA, dtype=torch.uint8, device="cuda")
+    am = torch.full((1,), -7.0, dtype=torch.float32, device="cuda")
+    f.fp8_quantize_f32(x, torch.tensor([scale], dtype=torch.float32, device="cuda"), fmt, out, am)
+    torch.cuda.synchronize()
+    return out, am
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_f32_cast_every_binary32_pattern(fmt):
+    """All 2^32 binary32 bit patterns, in 16 chunks, cast with scale 1 (so
+    fl32(x * 1) = x and the conversion itself is what is compared): every
+    code equals the oracle's encoder (NaN codes as a class)."""
+    chunk = 1 << 28
+    for c in range(16):
+        lo = -(1 << 31) + c * chunk
+        x = torch.arange(lo, lo + chunk, dtype=torch.int32, device="cuda").view(torch.float32)
+        out, _ = _cast_f32(x, np.float32(1.0), fmt)
+        ref = o.quantize_f32(np.arange(lo, lo + chunk, dtype=np.int32).view(np.float32),
+                             np.float32(1.0), fmt)
+        assert_fp8_equal(host_u8(out), ref, fmt, f"chunk {c}")
+        del x, out
+
+
+@pytest.mark.parametrize("n", [16, 4112, (1 << 20) + 48, 3 * (1 << 22)])
+@pytest.mark.parametrize("fmt", FMTS)
+def test_f32_cast_scaled_with_amax(n, fmt):
+    """Scaled casts of fp32 tensors (Gaussian spread over many binades, with
+    zeros, infinities, NaN and a planted maximum): codes and amax bit-exact."""
+    rng = np.random.default_rng(n + fmt)
+    x = (rng.standard_normal(n) * 10.0 ** rng.uniform(-6, 6, n)).astype(np.float32)
+    k = min(n, 64)
+    x[rng.integers(0, n, k)] = np.float32(0.0)
+    x[rng.integers(0, n, 2)] = np.float32(np.nan)
+    if n > 16:
+        x[rng.integers(0, n, 1)] = np.float32(-np.inf)
+    x[rng.integers(0, n)] = np.float32(-3.0e7)
+    dx = torch.from_numpy(x).cuda()
+    for s in (np.float32(1.0), np.float32(1 / 4096.0), np.float32(0.37), np.float32(2.0 ** 20)):
+        out, am = _cast_f32(dx, s, fmt)
+        assert_fp8_equal(host_u8(out), o.quantize_f32(x, s, fmt), fmt, f"n={n} s={s}")
+        assert f32_bits(am.cpu().numpy()[0]) == f32_bits(o.amax_f32(x))
+
+
+def test_f32_cast_empty_and_argument_checks():
+    f = _lib()
+    am = torch.full((1,), -7.0, dtype=torch.float32, device="cuda")
+    one = torch.ones(1, device="cuda")
+    f.fp8_quantize_f32(torch.empty(0, device="cuda"), one, o.E4M3,
+                       torch.empty(0, dtype=torch.uint8, device="cuda"), am)
+    torch.cuda.synchronize()
+    assert am.item() == 0.0
+    with pytest.raises(f.Fp8Error):        # n not a multiple of 16
+        f.fp8_quantize_f32(torch.ones(24, device="cuda"), one, o.E4M3,
+                           torch.empty(24, dtype=torch.uint8, device="cuda"))
+    with pytest.raises(f.Fp8Error):        # bad format
+        f.fp8_quantize_f32(torch.ones(32, device="cuda"), one, 7,
+                           torch.empty(32, dtype=torch.uint8, device="cuda"))

@@ -3,10 +3,15 @@
 Each check ties the oracle to something other than itself: the numbers the
 pages print (tests/golden/fp8_formats.txt), IEEE binary16 (numpy float16, a
 textbook routine), torch's CPU float8 / bfloat16 conversions (library
-routines), and invariants of round-to-nearest-even with saturation.
+routines), invariants of round-to-nearest-even with saturation, and an
+exhaustive run over all 2^32 binary32 patterns against an encoder written
+from the formats' bit layouts (tests/exhaustive_encode.c).
 """
+import ctypes
 import math
 import os
+import subprocess
+import tempfile
 
 import numpy as np
 import pytest
@@ -182,3 +187,44 @@ def test_bf16_round_nearest_even_matches_torch():
     nan = np.isnan(v)
     assert np.array_equal(mine[~nan], ref[~nan])
     assert np.all((mine[nan] & 0x7FFF) > 0x7F80)
+
+
+def _exhaustive_helper():
+    src = os.path.join(os.path.dirname(__file__), "exhaustive_encode.c")
+    so = os.path.join(tempfile.mkdtemp(prefix="fp8exh"), "libexhaustive_encode.so")
+    subprocess.run(["gcc", "-O2", "-std=gnu11", "-fPIC", "-shared", "-pthread", src, "-o", so],
+                   check=True, capture_output=True)
+    lib = ctypes.CDLL(so)
+    lib.count_mismatches.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
+                                     ctypes.POINTER(ctypes.c_uint32)]
+    lib.count_mismatches.restype = ctypes.c_int64
+    lib.encode_bits_one.argtypes = [ctypes.c_float, ctypes.c_int]
+    lib.encode_bits_one.restype = ctypes.c_uint8
+    return lib
+
+
+def test_bit_level_encoder_spot_values():
+    """The independent encoder itself on values fixed by the format table:
+    the maxima, the smallest subnormals, a tie on each side, saturation."""
+    h = _exhaustive_helper()
+    cases = {o.E4M3: [(448.0, 0x7E), (464.0, 0x7E), (1e9, 0x7E), (2.0 ** -9, 0x01),
+                      (2.0 ** -10, 0x00), (3 * 2.0 ** -10, 0x02), (1.0625, 0x38),
+                      (1.1875, 0x3A), (-2.0, 0xC0), (float("inf"), 0x7E)],
+             o.E5M2: [(57344.0, 0x7B), (61440.0, 0x7B), (2.0 ** -16, 0x01), (2.0 ** -17, 0x00),
+                      (3 * 2.0 ** -17, 0x02), (1.125, 0x3C), (1.375, 0x3E), (-1.0, 0xBC),
+                      (float("-inf"), 0xFB)]}
+    for fmt, cs in cases.items():
+        for v, code in cs:
+            assert h.encode_bits_one(v, fmt) == code, (fmt, v)
+
+
+@pytest.mark.parametrize("fmt", [o.E4M3, o.E5M2])
+def test_encode_exhaustive_against_bit_level_encoder(fmt):
+    """Every binary32 bit pattern (all 2^32, NaN codes as a class): the
+    oracle's nearest-value search over the code table equals an encoder that
+    rounds the binary32 significand with integer arithmetic."""
+    h = _exhaustive_helper()
+    fn = ctypes.cast(o._lib().or_fp8_encode_f32, ctypes.c_void_p)
+    first = ctypes.c_uint32(0)
+    bad = h.count_mismatches(fn, fmt, max(1, os.cpu_count() or 1), ctypes.byref(first))
+    assert bad == 0, (bad, hex(first.value))
