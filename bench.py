@@ -554,7 +554,56 @@ def run_secondary(f, args, pk):
         "ln_cast_us": tm.mean_ms("ln_cast") * 1e3, "cast_us": tm.mean_ms("cast") * 1e3,
         "ln_cast_gbs": 4 * ne / (tm.mean_ms("ln_cast") / 1e3) / 1e9,
         "note": "4 B/element algorithmic; L2 flushed before each launch"}
+    out["context_cublaslt_fp8_mlp7b"] = cublaslt_context(f, w7, flush)
     return out
+
+
+def cublaslt_context(f, w, flush):
+    """Context only (never on the product path): the vendor library's FP8
+    GEMM (torch._scaled_mm -> cuBLASLt) on the layer's own FP8 operands,
+    interleaved with this library's GEMM, L2 flushed before each launch,
+    median of 15.  cuBLASLt computes no output amax."""
+    try:
+        lin = f.Fp8Linear(wl.layer_weight(w, "cuda"), w.M,
+                          f.Recipe(margin=w.margin, history_len=w.history_len, hybrid=w.hybrid))
+        X, dY = wl.layer_x(w, 0, "cuda"), wl.layer_dy(w, 0, "cuda")
+        for _ in range(3):
+            lin.step(X, dY)
+        torch.cuda.synchronize()
+        m, E4, E5 = lin.meta, f.E4M3, f.E5M2
+        fg = E5 if w.hybrid else E4
+        t8 = {E4: torch.float8_e4m3fn, E5: torch.float8_e5m2}
+        one = torch.ones((), device="cuda")
+        cases = {
+            "fprop": ((lin.X8, E4, lin.W8, E4, 0, 1, lin.Y)),
+            "dgrad": ((lin.dY8, fg, lin.W8t, E4, 3, 1, lin.dX)),
+            "wgrad": ((lin.dY8t, fg, lin.X8t, E4, 3, 0, lin.dW)),
+        }
+        res = {}
+        for name, (A, fa, B, fb, ia, ib, D) in cases.items():
+            ours = lambda: f.fp8_gemm_tn(A, fa, B, fb, m.scale_inv[ia:ia + 1],
+                                         m.scale_inv[ib:ib + 1], D)
+            lib = lambda: torch._scaled_mm(A.view(t8[fa]), B.view(t8[fb]).t(), scale_a=one,
+                                           scale_b=one, out_dtype=torch.bfloat16)
+            lib()
+            to, tl = [], []
+            for _ in range(15):
+                for fn, acc in ((ours, to), (lib, tl)):
+                    flush.zero_()
+                    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    s.record()
+                    fn()
+                    e.record()
+                    torch.cuda.synchronize()
+                    acc.append(s.elapsed_time(e))
+            fl = 2 * w.M * w.N * w.K
+            mo, ml = statistics.median(to), statistics.median(tl)
+            res[name] = {"ours_us": mo * 1e3, "cublaslt_us": ml * 1e3,
+                         "ours_tflops": fl / (mo / 1e3) / 1e12,
+                         "cublaslt_tflops": fl / (ml / 1e3) / 1e12}
+        return res
+    except Exception as ex:   # the context row is optional
+        return {"unavailable": str(ex)[:200]}
 
 
 def main():

@@ -123,6 +123,39 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *tmap, uint
         : "memory");
 }
 
+// TMA store of a box from this CTA's shared memory (bulk-group completion,
+// tracked per issuing thread), and the waits on those groups.
+__device__ __forceinline__ void tma_store_2d(const void *tmap, uint32_t src, int32_t x, int32_t y) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+            reinterpret_cast<uint64_t>(tmap)),
+        "r"(src), "r"(x), "r"(y)
+        : "memory");
+}
+__device__ __forceinline__ void bulk_commit_group() {
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// at most N of this thread's most recent bulk groups still reading shared memory
+template <int N>
+__device__ __forceinline__ void bulk_wait_group_read() {
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+// at most N of this thread's most recent bulk groups not yet complete
+template <int N>
+__device__ __forceinline__ void bulk_wait_group() {
+    asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+                 "r"(d)
+                 : "memory");
+}
+// generic-proxy writes to shared memory become visible to the async proxy (TMA)
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- tcgen05 --
 
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
@@ -321,6 +354,36 @@ __device__ __forceinline__ uint32_t amax_bits2(uint32_t m, uint32_t w) {
     lo = lo > 0x7F80u ? 0u : lo;
     hi = hi > 0x7F80u ? 0u : hi;
     return max(m, max(lo, hi));
+}
+
+// Two fp32 values (bit patterns lo, hi) times s2 = {s, s} with one packed
+// IEEE multiply (round to nearest even per lane), rounded to BF16 and
+// packed (lo in the low half).
+__device__ __forceinline__ uint32_t scale_bf16x2(uint32_t lo, uint32_t hi, uint64_t s2) {
+    uint64_t v, p;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(v) : "r"(lo), "r"(hi));
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(p) : "l"(v), "l"(s2));
+    float a, b;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(p));
+    uint32_t h;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(h) : "f"(b), "f"(a));
+    return h;
+}
+
+__device__ __forceinline__ uint64_t splat_f32x2(float s) {
+    uint64_t s2;
+    asm("mov.b64 %0, {%1, %1};" : "=l"(s2) : "f"(s));
+    return s2;
+}
+
+// Running max of |x| over packed BF16 pairs: m2 holds two non-negative BF16
+// maxima.  max.bf16x2 returns the other operand when one is NaN, so NaN
+// entries are skipped and infinities kept, as in amax_bits2.
+__device__ __forceinline__ uint32_t absmax_bf16x2(uint32_t m2, uint32_t w) {
+    uint32_t a;
+    asm("abs.bf16x2 %0, %1;" : "=r"(a) : "r"(w));
+    asm("max.bf16x2 %0, %0, %1;" : "+r"(m2) : "r"(a));
+    return m2;
 }
 
 // ------------------------------------------------------- the scale formula --

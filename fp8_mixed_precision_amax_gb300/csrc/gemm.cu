@@ -15,9 +15,15 @@
 //   warp 1     allocates 512 TMEM columns (two 256-column fp32 accumulators)
 //              and issues tcgen05.mma (four per K-slice); tcgen05.commit
 //              frees ring stages and hands a finished accumulator on;
-//   warps 2-5  epilogue: tcgen05.ld of their 32-lane quarter, scale, BF16
-//              round, running amax, 16-byte stores; releases the accumulator
-//              so the next tile's MMAs overlap this tile's epilogue.
+//   warps 2-5  epilogue: tcgen05.ld of their 32-lane quarter, scale and
+//              round with packed fp32x2 / bf16x2 instructions (the epilogue
+//              shares issue slots with the single-thread producer and MMA
+//              loops, so its instruction count shows in the MMA rate),
+//              running amax; each 32-row x 64-column chunk goes to a
+//              128-byte-swizzled staging buffer (two per warp) and out with
+//              one TMA store, so the output leaves in whole lines.  The
+//              accumulator is released as soon as the tile's last tcgen05.ld
+//              has landed, so the next tile's MMAs overlap this epilogue.
 // Above 128 rows, two CTAs on two SMs (a cluster) share each 256 x 256 tile
 // (tcgen05 cta_group::2): each loads its own 128 A rows and 128 of the 256 B
 // rows, and the even CTA issues M = 256 MMAs that read both CTAs' shared
@@ -46,6 +52,9 @@ constexpr int NUM_THREADS = 192;
 constexpr int TMEM_COLS = 2 * BN;
 constexpr int GROUP_M = 16;
 constexpr int MAX_PROBLEMS = 2;
+constexpr int EPI_COLS = 64;                      // output columns per TMA store (128 B of BF16)
+constexpr int EPI_BUF = 32 * EPI_COLS * 2;        // one warp's staging buffer: 32 rows x 128 B
+constexpr int EPI_BYTES = 4 * 2 * EPI_BUF;        // four epilogue warps, two buffers each
 
 template <bool PAIR>
 struct Cfg {
@@ -55,7 +64,8 @@ struct Cfg {
     static constexpr int B_STAGE = B_ROWS * BK;
     static constexpr int TILE_M = PAIR ? 2 * BM : BM;    // output rows per (pair) tile
     static constexpr int NUM_BARS = 2 * STAGES + 4 + 1;  // full, empty, acc_full x2, acc_empty x2, drain
-    static constexpr size_t SMEM = 1024 + STAGES * (A_STAGE + B_STAGE) + NUM_BARS * 8 + 16;
+    static constexpr size_t SMEM =
+        1024 + STAGES * (A_STAGE + B_STAGE) + EPI_BYTES + NUM_BARS * 8 + 16;
     static constexpr uint32_t STAGE_TX = (PAIR ? 2 : 1) * (A_STAGE + B_STAGE);
     static constexpr uint32_t EPI_ARRIVALS = PAIR ? 8 : 4;  // epilogue warps per tile
 };
@@ -73,6 +83,7 @@ struct GemmProblem {
 
 struct GemmArgs {
     CUtensorMap maps[2 * MAX_PROBLEMS];   // A0, B0, A1, B1
+    CUtensorMap dmaps[MAX_PROBLEMS];      // D0, D1 (BF16, 64 x 32 boxes, 128-byte swizzle)
     GemmProblem prob[MAX_PROBLEMS];
     int num_problems;
     int num_tiles;
@@ -107,7 +118,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_tn_kernel(const __grid_co
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint8_t *sA = smem;
     uint8_t *sB = smem + C::STAGES * C::A_STAGE;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(sB + C::STAGES * C::B_STAGE);
+    uint8_t *sD = sB + C::STAGES * C::B_STAGE;   // epilogue staging, 1024-byte aligned
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sD + EPI_BYTES);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + C::NUM_BARS);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
@@ -133,6 +145,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_tn_kernel(const __grid_co
         *abort_flag = 0;
         fence_mbar_init();
         for (int i = 0; i < 2 * a.num_problems; ++i) prefetch_tmap(&a.maps[i]);
+        for (int i = 0; i < a.num_problems; ++i) prefetch_tmap(&a.dmaps[i]);
     }
     if (warp == 1) {
         if constexpr (PAIR) {
@@ -294,6 +307,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_tn_kernel(const __grid_co
         }
         int acc = 0;
         uint32_t acc_phase = 0;
+        uint32_t epi_chunk = 0;   // chunks staged so far (selects the staging buffer)
         for (int tile = unit; tile < a.num_tiles; tile += num_units) {
             int mb, nb;
             const int pi = locate(a, tile, mb, nb);
@@ -305,58 +319,81 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_tn_kernel(const __grid_co
                 break;
             }
             tc_fence_after();
-            const float s = pi ? sab[1] : sab[0];
-            uint32_t m = 0;
-            const int64_t row = static_cast<int64_t>(mb) * C::TILE_M + rank * BM + q * 32 + lane;
-            const bool row_in = row < P.M;
-            __nv_bfloat16 *drow = P.D + row * P.N;
+            const uint64_t s2 = splat_f32x2(pi ? sab[1] : sab[0]);
+            uint32_t m2 = 0;   // two BF16 magnitude maxima
+            const int64_t row0 = static_cast<int64_t>(mb) * C::TILE_M + rank * BM + q * 32;
+            const bool row_in = row0 + lane < P.M;
+            const CUtensorMap *tmD = &a.dmaps[pi];
             const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                                     static_cast<uint32_t>(acc * BN);
 #pragma unroll 1
-            for (int c = 0; c < BN / 32; ++c) {
-                uint32_t r[32];
-                tmem_load_32cols(t_lane + c * 32, r);
-                const int64_t col0 = static_cast<int64_t>(nb) * BN + c * 32;
-                uint32_t packed[16];
+            for (int c = 0; c < BN / EPI_COLS; ++c) {
+                uint32_t r[2][32];
+                tmem_load_32cols(t_lane + c * EPI_COLS, r[0]);
+                tmem_load_32cols(t_lane + c * EPI_COLS + 32, r[1]);
+                if (c == BN / EPI_COLS - 1) {
+                    // the whole accumulator is in registers: hand it back
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) {
+                        if constexpr (PAIR)
+                            mbar_arrive_cluster(mapa_shared(acce0 + 8 * acc, 0));
+                        else
+                            mbar_arrive(acce0 + 8 * acc);
+                    }
+                }
+                const int64_t col0 = static_cast<int64_t>(nb) * BN + c * EPI_COLS;
+                uint32_t packed[32];
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const float y0 = __fmul_rn(__uint_as_float(r[2 * j]), s);
-                    const float y1 = __fmul_rn(__uint_as_float(r[2 * j + 1]), s);
-                    const __nv_bfloat162 h = __floats2bfloat162_rn(y0, y1);
-                    packed[j] = *reinterpret_cast<const uint32_t *>(&h);
+                for (int h = 0; h < 2; ++h) {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j)
+                        packed[16 * h + j] = scale_bf16x2(r[h][2 * j], r[h][2 * j + 1], s2);
                 }
                 if (row_in) {
 #pragma unroll
-                    for (int v = 0; v < 4; ++v) {
+                    for (int v = 0; v < 8; ++v) {
                         if (col0 + 8 * v < P.N) {
-                            m = amax_bits2(m, packed[4 * v]);
-                            m = amax_bits2(m, packed[4 * v + 1]);
-                            m = amax_bits2(m, packed[4 * v + 2]);
-                            m = amax_bits2(m, packed[4 * v + 3]);
-                            *reinterpret_cast<uint4 *>(drow + col0 + 8 * v) =
-                                make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2],
-                                           packed[4 * v + 3]);
+                            m2 = absmax_bf16x2(m2, packed[4 * v]);
+                            m2 = absmax_bf16x2(m2, packed[4 * v + 1]);
+                            m2 = absmax_bf16x2(m2, packed[4 * v + 2]);
+                            m2 = absmax_bf16x2(m2, packed[4 * v + 3]);
                         }
                     }
                 }
+                // this buffer's previous store (two chunks back) has read it
+                if (lane == 0) bulk_wait_group_read<1>();
+                __syncwarp();
+                // row `lane` of the 32 x 128 B box; 16-byte chunk j sits at
+                // j ^ (row mod 8), the 128-byte swizzle the tensor map names
+                const uint32_t sbuf = smem_u32(sD + (q * 2 + (epi_chunk & 1)) * EPI_BUF);
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    st_shared_v4(sbuf + lane * 128 + ((j ^ (lane & 7)) << 4), packed[4 * j],
+                                 packed[4 * j + 1], packed[4 * j + 2], packed[4 * j + 3]);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    if (row0 < P.M && col0 < P.N)   // boxes wholly outside D are skipped
+                        tma_store_2d(tmD, sbuf, static_cast<int32_t>(col0),
+                                     static_cast<int32_t>(row0));
+                    bulk_commit_group();
+                }
+                ++epi_chunk;
             }
+            const uint32_t m = max(m2 & 0xFFFFu, m2 >> 16);   // BF16 magnitude bits
             if (pi)
                 tmax[1] = max(tmax[1], m);
             else
                 tmax[0] = max(tmax[0], m);
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) {
-                if constexpr (PAIR)
-                    mbar_arrive_cluster(mapa_shared(acce0 + 8 * acc, 0));
-                else
-                    mbar_arrive(acce0 + 8 * acc);
-            }
             if (++acc == 2) {
                 acc = 0;
                 acc_phase ^= 1u;
             }
         }
+        // every store has left shared memory and reached global memory
+        if (lane == 0) bulk_wait_group<0>();
+        __syncwarp();
 #pragma unroll
         for (int i = 0; i < MAX_PROBLEMS; ++i) {
             if (i < a.num_problems && a.prob[i].amax_bits != nullptr) {
@@ -457,6 +494,10 @@ cudaError_t launch_gemm_group(const GemmSpec *specs, int n, int sm_count, cudaSt
             if (what) *what = "cuTensorMapEncodeTiled failed for an operand";
             return cudaErrorInvalidValue;
         }
+        if (!encode_tmap_2d(&a.dmaps[i], g.D, true, g.N, g.M, EPI_COLS, 32, true)) {
+            if (what) *what = "cuTensorMapEncodeTiled failed for the output";
+            return cudaErrorInvalidValue;
+        }
         GemmProblem &p = a.prob[i];
         p.D = reinterpret_cast<__nv_bfloat16 *>(g.D);
         p.amax_bits = reinterpret_cast<unsigned *>(g.d_amax);
@@ -476,6 +517,7 @@ cudaError_t launch_gemm_group(const GemmSpec *specs, int n, int sm_count, cudaSt
         a.prob[i] = a.prob[0];
         a.maps[2 * i] = a.maps[0];
         a.maps[2 * i + 1] = a.maps[1];
+        a.dmaps[i] = a.dmaps[0];
     }
     a.num_tiles = tiles;
     if (pair) {
