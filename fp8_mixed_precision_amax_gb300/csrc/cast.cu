@@ -23,12 +23,12 @@ __device__ unsigned g_cast_error_flags = 0;
 // ------------------------------------------------------------------- amax --
 
 // Grid-stride max of |x| over 16-byte vectors (8 BF16), 4 vectors in flight
-// per thread, integer max on magnitude bits, one atomicMax per block.
+// per thread, packed BF16 abs / max (NaN skipped), one atomicMax per block.
 __global__ void __launch_bounds__(512) amax_kernel(const uint4 *__restrict__ x, int64_t nvec,
                                                    unsigned *__restrict__ amax_bits) {
     pdl_wait();
     pdl_trigger();
-    uint32_t m = 0;
+    uint32_t m2 = 0;   // two BF16 magnitude maxima
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
     int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     for (; i + 3 * stride < nvec; i += 4 * stride) {
@@ -37,19 +37,20 @@ __global__ void __launch_bounds__(512) amax_kernel(const uint4 *__restrict__ x, 
         for (int u = 0; u < 4; ++u) v[u] = __ldcs(x + i + u * stride);
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-            m = amax_bits2(m, v[u].x);
-            m = amax_bits2(m, v[u].y);
-            m = amax_bits2(m, v[u].z);
-            m = amax_bits2(m, v[u].w);
+            m2 = absmax_bf16x2(m2, v[u].x);
+            m2 = absmax_bf16x2(m2, v[u].y);
+            m2 = absmax_bf16x2(m2, v[u].z);
+            m2 = absmax_bf16x2(m2, v[u].w);
         }
     }
     for (; i < nvec; i += stride) {
         uint4 v = __ldcs(x + i);
-        m = amax_bits2(m, v.x);
-        m = amax_bits2(m, v.y);
-        m = amax_bits2(m, v.z);
-        m = amax_bits2(m, v.w);
+        m2 = absmax_bf16x2(m2, v.x);
+        m2 = absmax_bf16x2(m2, v.y);
+        m2 = absmax_bf16x2(m2, v.z);
+        m2 = absmax_bf16x2(m2, v.w);
     }
+    uint32_t m = max(m2 & 0xFFFFu, m2 >> 16);
     m = __reduce_max_sync(0xFFFFFFFFu, m);
     __shared__ uint32_t warp_max[32];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -261,27 +262,28 @@ __global__ void __launch_bounds__(kQtThreads, 2)
         }
         uint32_t m = 0;
         if (T.ln_mean == nullptr) {
+            // packed BF16 abs / max for the amax (NaN skipped), one packed
+            // fp32 multiply per pair, two-lane FP8 converts: the conversion
+            // is issue-bound enough that the instruction count matters
+            const uint64_t s2 = splat_f32x2(s);
+            uint32_t m2 = 0;
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 const int idx = i * kQtThreads + tid;
                 const int rr = idx >> 4, vv = idx & 15;
                 const int64_t r = r0 + rr, c = c0 + vv * 8;
-                m = amax_bits2(m, v[i].x);
-                m = amax_bits2(m, v[i].y);
-                m = amax_bits2(m, v[i].z);
-                m = amax_bits2(m, v[i].w);
+                m2 = absmax_bf16x2(m2, v[i].x);
+                m2 = absmax_bf16x2(m2, v[i].y);
+                m2 = absmax_bf16x2(m2, v[i].z);
+                m2 = absmax_bf16x2(m2, v[i].w);
                 uint2 q;
-                q.x = cvt2_fp8<FMT>(__fmul_rn(bf16_lo(v[i].x), s), __fmul_rn(bf16_hi(v[i].x), s)) |
-                      (cvt2_fp8<FMT>(__fmul_rn(bf16_lo(v[i].y), s), __fmul_rn(bf16_hi(v[i].y), s))
-                       << 16);
-                q.y = cvt2_fp8<FMT>(__fmul_rn(bf16_lo(v[i].z), s), __fmul_rn(bf16_hi(v[i].z), s)) |
-                      (cvt2_fp8<FMT>(__fmul_rn(bf16_lo(v[i].w), s), __fmul_rn(bf16_hi(v[i].w), s))
-                       << 16);
+                q.x = scale_fp8x2_bf16x2<FMT>(v[i].x, s2) | (scale_fp8x2_bf16x2<FMT>(v[i].y, s2) << 16);
+                q.y = scale_fp8x2_bf16x2<FMT>(v[i].z, s2) | (scale_fp8x2_bf16x2<FMT>(v[i].w, s2) << 16);
                 if (T.out != nullptr && r < rows && c < cols)
                     *reinterpret_cast<uint2 *>(T.out + r * cols + c) = q;
                 *reinterpret_cast<uint2 *>(&tile[rr * 32 + ((vv * 2) ^ qt_swz(rr))]) = q;
             }
-            m <<= 16;   // BF16 magnitude bits -> fp32 bits
+            m = max(m2 & 0xFFFFu, m2 >> 16) << 16;   // BF16 magnitude bits -> fp32 bits
         } else {
             // LayerNorm first: y = ((x - mean) * rstd) * gamma + beta in fp32.
             // This thread's 8 columns are the same for all 8 of its vectors.

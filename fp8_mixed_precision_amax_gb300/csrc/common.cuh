@@ -386,6 +386,19 @@ __device__ __forceinline__ uint32_t absmax_bf16x2(uint32_t m2, uint32_t w) {
     return m2;
 }
 
+// The two BF16 values of w (lo in the low half) widened to fp32, times
+// s2 = {s, s} with one packed IEEE multiply, and cast to FP8 (lo in the low
+// byte of the result).
+template <int FMT>
+__device__ __forceinline__ uint32_t scale_fp8x2_bf16x2(uint32_t w, uint64_t s2) {
+    uint64_t v, p;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(v) : "r"(w << 16), "r"(w & 0xFFFF0000u));
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(p) : "l"(v), "l"(s2));
+    float a, b;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(p));
+    return cvt2_fp8<FMT>(a, b);
+}
+
 // ------------------------------------------------------- the scale formula --
 // scale = fl32(fl32(fmax / m) * 2^-margin), +inf clamped to FLT_MAX, when
 // 0 < m < inf (m = the amax, or the max over the amax history); otherwise the
