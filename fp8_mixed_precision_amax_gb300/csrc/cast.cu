@@ -243,6 +243,25 @@ __global__ void __launch_bounds__(kQtThreads, 2)
         const int64_t c0 = (lt % T.tiles_c) * kQtTile;
         const int64_t rows = T.rows, cols = T.cols;
         const float s = p ? sc[1] : sc[0];
+        // LayerNorm parameters of this tile (independent of the staged x):
+        // loaded before the wait so that their latency overlaps it
+        const bool ln = T.ln_mean != nullptr;
+        const int lvv = tid & 15;
+        const int64_t lc = c0 + lvv * 8;
+        uint4 lg4 = make_uint4(0, 0, 0, 0), lb4 = make_uint4(0, 0, 0, 0);
+        float lmu[8], lrs[8];
+        if (ln) {
+            if (lc < cols) {
+                lg4 = *reinterpret_cast<const uint4 *>(T.ln_gamma + lc);
+                lb4 = *reinterpret_cast<const uint4 *>(T.ln_beta + lc);
+            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int64_t r = r0 + ((i * kQtThreads + tid) >> 4);
+                lmu[i] = r < rows ? T.ln_mean[r] : 0.0f;
+                lrs[i] = r < rows ? T.ln_rstd[r] : 0.0f;
+            }
+        }
         const bool ok = mbar_wait(smem_u32(full + st), parity, abort_flag);
         if (__syncthreads_or(!ok)) {
             if (tid == 0) {
@@ -261,7 +280,7 @@ __global__ void __launch_bounds__(kQtThreads, 2)
             v[i] = *reinterpret_cast<const uint4 *>(xs + (idx >> 4) * kQtTile + (idx & 15) * 8);
         }
         uint32_t m = 0;
-        if (T.ln_mean == nullptr) {
+        if (!ln) {
             // packed BF16 abs / max for the amax (NaN skipped), one packed
             // fp32 multiply per pair, two-lane FP8 converts: the conversion
             // is issue-bound enough that the instruction count matters
@@ -285,53 +304,43 @@ __global__ void __launch_bounds__(kQtThreads, 2)
             }
             m = max(m2 & 0xFFFFu, m2 >> 16) << 16;   // BF16 magnitude bits -> fp32 bits
         } else {
-            // LayerNorm first: y = ((x - mean) * rstd) * gamma + beta in fp32.
+            // LayerNorm first: y = ((x - mean) * rstd) * gamma + beta in fp32,
+            // one rounding per operation in that order, two lanes at a time.
             // This thread's 8 columns are the same for all 8 of its vectors.
-            const int vv = tid & 15;
-            const int64_t c = c0 + vv * 8;
-            float gam[8], bet[8];
-            if (c < cols) {
-                const uint4 g4 = *reinterpret_cast<const uint4 *>(T.ln_gamma + c);
-                const uint4 b4 = *reinterpret_cast<const uint4 *>(T.ln_beta + c);
-                const uint32_t gw[4] = {g4.x, g4.y, g4.z, g4.w}, bw[4] = {b4.x, b4.y, b4.z, b4.w};
+            const int vv = lvv;
+            const int64_t c = lc;
+            uint64_t gam2[4], bet2[4];
+            {
+                const uint32_t gw[4] = {lg4.x, lg4.y, lg4.z, lg4.w},
+                               bw[4] = {lb4.x, lb4.y, lb4.z, lb4.w};
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
-                    gam[2 * j] = bf16_lo(gw[j]);
-                    gam[2 * j + 1] = bf16_hi(gw[j]);
-                    bet[2 * j] = bf16_lo(bw[j]);
-                    bet[2 * j + 1] = bf16_hi(bw[j]);
+                    gam2[j] = f32x2_from_bf16x2(gw[j]);
+                    bet2[j] = f32x2_from_bf16x2(bw[j]);
                 }
-            } else {
-#pragma unroll
-                for (int j = 0; j < 8; ++j) gam[j] = bet[j] = 0.0f;
             }
+            const uint64_t s2 = splat_f32x2(s);
+            float ymax = 0.0f;   // max |y| over in-range elements; fmaxf skips NaN
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 const int rr = (i * kQtThreads + tid) >> 4;
                 const int64_t r = r0 + rr;
                 const bool in = r < rows && c < cols;
-                const float mu = in ? T.ln_mean[r] : 0.0f;
-                const float rs = in ? T.ln_rstd[r] : 0.0f;
+                const uint64_t mu2 = splat_f32x2(in ? lmu[i] : 0.0f);
+                const uint64_t rs2 = splat_f32x2(in ? lrs[i] : 0.0f);
                 const uint32_t xw[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
-                float yv[8];
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const float x0 = bf16_lo(xw[j]), x1 = bf16_hi(xw[j]);
-                    yv[2 * j] = __fadd_rn(__fmul_rn(__fmul_rn(__fsub_rn(x0, mu), rs), gam[2 * j]),
-                                          bet[2 * j]);
-                    yv[2 * j + 1] = __fadd_rn(
-                        __fmul_rn(__fmul_rn(__fsub_rn(x1, mu), rs), gam[2 * j + 1]), bet[2 * j + 1]);
-                }
                 uint32_t qw[4];
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
-                    if (in) {
-                        const uint32_t a0 = __float_as_uint(yv[2 * j]) & 0x7FFFFFFFu;
-                        const uint32_t a1 = __float_as_uint(yv[2 * j + 1]) & 0x7FFFFFFFu;
-                        m = max(m, a0 > 0x7F800000u ? 0u : a0);
-                        m = max(m, a1 > 0x7F800000u ? 0u : a1);
-                    }
-                    qw[j] = cvt2_fp8<FMT>(__fmul_rn(yv[2 * j], s), __fmul_rn(yv[2 * j + 1], s));
+                    const uint64_t y2 = f32x2_add(
+                        f32x2_mul(f32x2_mul(f32x2_sub(f32x2_from_bf16x2(xw[j]), mu2), rs2),
+                                  gam2[j]),
+                        bet2[j]);
+                    float y0, y1, q0, q1;
+                    f32x2_unpack(y2, y0, y1);
+                    if (in) ymax = fmaxf(ymax, fmaxf(fabsf(y0), fabsf(y1)));
+                    f32x2_unpack(f32x2_mul(y2, s2), q0, q1);
+                    qw[j] = cvt2_fp8<FMT>(q0, q1);
                 }
                 uint2 q;
                 q.x = qw[0] | (qw[1] << 16);
@@ -339,6 +348,7 @@ __global__ void __launch_bounds__(kQtThreads, 2)
                 if (T.out != nullptr && in) *reinterpret_cast<uint2 *>(T.out + r * cols + c) = q;
                 *reinterpret_cast<uint2 *>(&tile[rr * 32 + ((vv * 2) ^ qt_swz(rr))]) = q;
             }
+            m = __float_as_uint(ymax);   // fp32 bits of a value >= 0
         }
         if (p)
             tmax[1] = max(tmax[1], m);
@@ -515,6 +525,101 @@ __global__ void __launch_bounds__(256) ln_stats_kernel(const uint16_t *__restric
     }
 }
 
+// The same statistics for rows of at most 32 * MAXV * 8 columns, with the
+// row held in registers: one read of x, then the sum, the squared
+// deviations and the optional amax(y) from registers.  Each lane visits its
+// vectors in the same order as ln_stats_kernel, so the fp32 results are the
+// same bit for bit.
+template <int MAXV>
+__global__ void __launch_bounds__(256) ln_stats_reg_kernel(const uint16_t *__restrict__ x,
+                                                           const uint16_t *__restrict__ gamma,
+                                                           const uint16_t *__restrict__ beta,
+                                                           int64_t rows, int64_t cols, float eps,
+                                                           float *__restrict__ mean,
+                                                           float *__restrict__ rstd,
+                                                           unsigned *__restrict__ amax_bits) {
+    pdl_wait();
+    pdl_trigger();
+    const int lane = threadIdx.x & 31;
+    const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+    const int nvec = static_cast<int>(cols / 8);
+    const float inv_c = __fdiv_rn(1.0f, static_cast<float>(cols));
+    uint32_t m = 0;
+    for (int64_t r = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; r < rows;
+         r += warps) {
+        const uint4 *xr = reinterpret_cast<const uint4 *>(x + r * cols);
+        uint4 v[MAXV];
+#pragma unroll
+        for (int u = 0; u < MAXV; ++u)
+            v[u] = lane + 32 * u < nvec ? __ldcs(xr + lane + 32 * u) : make_uint4(0, 0, 0, 0);
+        float part[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+#pragma unroll
+        for (int u = 0; u < MAXV; ++u) {
+            if (lane + 32 * u >= nvec) break;
+            const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                part[2 * j] = __fadd_rn(part[2 * j], bf16_lo(w[j]));
+                part[2 * j + 1] = __fadd_rn(part[2 * j + 1], bf16_hi(w[j]));
+            }
+        }
+        float sum = 0.0f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) sum = __fadd_rn(sum, part[j]);
+        const float mu = __fmul_rn(warp_sum(sum), inv_c);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) part[j] = 0.0f;
+#pragma unroll
+        for (int u = 0; u < MAXV; ++u) {
+            if (lane + 32 * u >= nvec) break;
+            const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float d0 = __fsub_rn(bf16_lo(w[j]), mu);
+                const float d1 = __fsub_rn(bf16_hi(w[j]), mu);
+                part[2 * j] = __fadd_rn(part[2 * j], __fmul_rn(d0, d0));
+                part[2 * j + 1] = __fadd_rn(part[2 * j + 1], __fmul_rn(d1, d1));
+            }
+        }
+        float sq = 0.0f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) sq = __fadd_rn(sq, part[j]);
+        const float var = __fmul_rn(warp_sum(sq), inv_c);
+        const float rs = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(var, eps)));
+        if (lane == 0) {
+            mean[r] = mu;
+            rstd[r] = rs;
+        }
+        if (amax_bits != nullptr) {
+#pragma unroll
+            for (int u = 0; u < MAXV; ++u) {
+                if (lane + 32 * u >= nvec) break;
+                const uint4 g4 = reinterpret_cast<const uint4 *>(gamma)[lane + 32 * u];
+                const uint4 b4 = reinterpret_cast<const uint4 *>(beta)[lane + 32 * u];
+                const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w},
+                               gw[4] = {g4.x, g4.y, g4.z, g4.w}, bw[4] = {b4.x, b4.y, b4.z, b4.w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const float y0 = __fadd_rn(
+                        __fmul_rn(__fmul_rn(__fsub_rn(bf16_lo(w[j]), mu), rs), bf16_lo(gw[j])),
+                        bf16_lo(bw[j]));
+                    const float y1 = __fadd_rn(
+                        __fmul_rn(__fmul_rn(__fsub_rn(bf16_hi(w[j]), mu), rs), bf16_hi(gw[j])),
+                        bf16_hi(bw[j]));
+                    const uint32_t a0 = __float_as_uint(y0) & 0x7FFFFFFFu;
+                    const uint32_t a1 = __float_as_uint(y1) & 0x7FFFFFFFu;
+                    m = max(m, a0 > 0x7F800000u ? 0u : a0);
+                    m = max(m, a1 > 0x7F800000u ? 0u : a1);
+                }
+            }
+        }
+    }
+    if (amax_bits != nullptr) {
+        m = __reduce_max_sync(0xFFFFFFFFu, m);
+        if (lane == 0 && m != 0) atomicMax(amax_bits, m);
+    }
+}
+
 cudaError_t launch_ln_stats(const void *x, const void *gamma, const void *beta, int64_t rows,
                             int64_t cols, float eps, float *mean, float *rstd, float *amax,
                             int sm_count, cudaStream_t st) {
@@ -527,7 +632,20 @@ cudaError_t launch_ln_stats(const void *x, const void *gamma, const void *beta, 
     int64_t blocks = (rows + 7) / 8;
     const int64_t cap = static_cast<int64_t>(sm_count) * 8;
     if (blocks > cap) blocks = cap;
-    return launch_pdl(ln_stats_kernel, dim3(static_cast<unsigned>(blocks)), dim3(threads), 0, st,
+    const int64_t nvec = cols / 8;
+    const dim3 grid(static_cast<unsigned>(blocks)), block(threads);
+    const uint16_t *xb = reinterpret_cast<const uint16_t *>(x);
+    const uint16_t *gb = reinterpret_cast<const uint16_t *>(gamma);
+    const uint16_t *bb = reinterpret_cast<const uint16_t *>(beta);
+    unsigned *ab = reinterpret_cast<unsigned *>(amax);
+    // rows that fit in registers: one read of x
+    if (nvec <= 32 * 16)
+        return launch_pdl(ln_stats_reg_kernel<16>, grid, block, 0, st, xb, gb, bb, rows, cols, eps,
+                          mean, rstd, ab);
+    if (nvec <= 32 * 32)
+        return launch_pdl(ln_stats_reg_kernel<32>, grid, block, 0, st, xb, gb, bb, rows, cols, eps,
+                          mean, rstd, ab);
+    return launch_pdl(ln_stats_kernel, grid, block, 0, st,
                       reinterpret_cast<const uint16_t *>(x), reinterpret_cast<const uint16_t *>(gamma),
                       reinterpret_cast<const uint16_t *>(beta), rows, cols, eps, mean, rstd,
                       reinterpret_cast<unsigned *>(amax));

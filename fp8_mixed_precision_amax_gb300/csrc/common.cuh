@@ -356,24 +356,48 @@ __device__ __forceinline__ uint32_t amax_bits2(uint32_t m, uint32_t w) {
     return max(m, max(lo, hi));
 }
 
-// Two fp32 values (bit patterns lo, hi) times s2 = {s, s} with one packed
-// IEEE multiply (round to nearest even per lane), rounded to BF16 and
-// packed (lo in the low half).
+// Packed fp32 pairs (lo in the low word of a 64-bit register) and IEEE
+// round-to-nearest arithmetic on both lanes at once: each lane is rounded
+// exactly as the scalar operation would be.
+__device__ __forceinline__ uint64_t f32x2_pack(float lo, float hi) {
+    uint64_t v;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(v) : "f"(lo), "f"(hi));
+    return v;
+}
+__device__ __forceinline__ void f32x2_unpack(uint64_t v, float &lo, float &hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+// the two BF16 values of w (lo in the low half), widened to fp32
+__device__ __forceinline__ uint64_t f32x2_from_bf16x2(uint32_t w) {
+    uint64_t v;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(v) : "r"(w << 16), "r"(w & 0xFFFF0000u));
+    return v;
+}
+__device__ __forceinline__ uint64_t f32x2_add(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ uint64_t f32x2_sub(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ uint64_t f32x2_mul(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ uint64_t splat_f32x2(float s) { return f32x2_pack(s, s); }
+
+// Two fp32 values (bit patterns lo, hi) times s2 = {s, s}, rounded to BF16
+// and packed (lo in the low half).
 __device__ __forceinline__ uint32_t scale_bf16x2(uint32_t lo, uint32_t hi, uint64_t s2) {
-    uint64_t v, p;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(v) : "r"(lo), "r"(hi));
-    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(p) : "l"(v), "l"(s2));
     float a, b;
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(p));
+    f32x2_unpack(f32x2_mul(f32x2_pack(__uint_as_float(lo), __uint_as_float(hi)), s2), a, b);
     uint32_t h;
     asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(h) : "f"(b), "f"(a));
     return h;
-}
-
-__device__ __forceinline__ uint64_t splat_f32x2(float s) {
-    uint64_t s2;
-    asm("mov.b64 %0, {%1, %1};" : "=l"(s2) : "f"(s));
-    return s2;
 }
 
 // Running max of |x| over packed BF16 pairs: m2 holds two non-negative BF16
@@ -387,15 +411,11 @@ __device__ __forceinline__ uint32_t absmax_bf16x2(uint32_t m2, uint32_t w) {
 }
 
 // The two BF16 values of w (lo in the low half) widened to fp32, times
-// s2 = {s, s} with one packed IEEE multiply, and cast to FP8 (lo in the low
-// byte of the result).
+// s2 = {s, s}, and cast to FP8 (lo in the low byte of the result).
 template <int FMT>
 __device__ __forceinline__ uint32_t scale_fp8x2_bf16x2(uint32_t w, uint64_t s2) {
-    uint64_t v, p;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(v) : "r"(w << 16), "r"(w & 0xFFFF0000u));
-    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(p) : "l"(v), "l"(s2));
     float a, b;
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(p));
+    f32x2_unpack(f32x2_mul(f32x2_from_bf16x2(w), s2), a, b);
     return cvt2_fp8<FMT>(a, b);
 }
 

@@ -40,7 +40,8 @@ def check_codes(gpu, x, gamma, beta, mean, rstd, y, s, fmt, what):
     return assert_codes_in_band(gpu, y * np.float64(s), REL * mag * np.float64(s), fmt, what)
 
 
-@pytest.mark.parametrize("rows,cols", [(16, 16), (144, 272), (1040, 4096), (256, 8192)])
+@pytest.mark.parametrize("rows,cols", [(16, 16), (144, 272), (1040, 4096), (256, 8192),
+                                       (48, 12288)])
 @pytest.mark.parametrize("fmt", [o.E4M3, o.E5M2])
 def test_layernorm_cast_matches_oracle(rows, cols, fmt):
     f = _lib()
