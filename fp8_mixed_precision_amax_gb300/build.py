@@ -22,7 +22,7 @@ SOURCES = ["abi.cu", "cast.cu", "gemm.cu", "noalloc.cu", "optim.cu", "tmap.cu"]
 HEADERS = ["common.cuh", "kernels.h"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
+NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-fmad=false", "-Xcompiler", "-fPIC",
                      "-I" + INCLUDE, "-Xptxas", "-v"]
 
 

@@ -305,19 +305,18 @@ __global__ void __launch_bounds__(kQtThreads, 2)
             m = max(m2 & 0xFFFFu, m2 >> 16) << 16;   // BF16 magnitude bits -> fp32 bits
         } else {
             // LayerNorm first: y = ((x - mean) * rstd) * gamma + beta in fp32,
-            // one rounding per operation in that order, two lanes at a time.
+            // one rounding per operation in that order: the subtract and the
+            // two multiplies two lanes at a time, the add of beta scalar (a
+            // packed add of a packed product would be fused into an fma).
             // This thread's 8 columns are the same for all 8 of its vectors.
             const int vv = lvv;
             const int64_t c = lc;
-            uint64_t gam2[4], bet2[4];
+            uint64_t gam2[4];
+            const uint32_t bw[4] = {lb4.x, lb4.y, lb4.z, lb4.w};
             {
-                const uint32_t gw[4] = {lg4.x, lg4.y, lg4.z, lg4.w},
-                               bw[4] = {lb4.x, lb4.y, lb4.z, lb4.w};
+                const uint32_t gw[4] = {lg4.x, lg4.y, lg4.z, lg4.w};
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    gam2[j] = f32x2_from_bf16x2(gw[j]);
-                    bet2[j] = f32x2_from_bf16x2(bw[j]);
-                }
+                for (int j = 0; j < 4; ++j) gam2[j] = f32x2_from_bf16x2(gw[j]);
             }
             const uint64_t s2 = splat_f32x2(s);
             float ymax = 0.0f;   // max |y| over in-range elements; fmaxf skips NaN
@@ -332,12 +331,14 @@ __global__ void __launch_bounds__(kQtThreads, 2)
                 uint32_t qw[4];
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
-                    const uint64_t y2 = f32x2_add(
+                    float p0, p1, q0, q1;
+                    f32x2_unpack(
                         f32x2_mul(f32x2_mul(f32x2_sub(f32x2_from_bf16x2(xw[j]), mu2), rs2),
                                   gam2[j]),
-                        bet2[j]);
-                    float y0, y1, q0, q1;
-                    f32x2_unpack(y2, y0, y1);
+                        p0, p1);
+                    const float y0 = __fadd_rn(p0, bf16_lo(bw[j]));
+                    const float y1 = __fadd_rn(p1, bf16_hi(bw[j]));
+                    const uint64_t y2 = f32x2_pack(y0, y1);
                     if (in) ymax = fmaxf(ymax, fmaxf(fabsf(y0), fabsf(y1)));
                     f32x2_unpack(f32x2_mul(y2, s2), q0, q1);
                     qw[j] = cvt2_fp8<FMT>(q0, q1);

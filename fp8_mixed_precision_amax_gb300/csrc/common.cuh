@@ -358,7 +358,12 @@ __device__ __forceinline__ uint32_t amax_bits2(uint32_t m, uint32_t w) {
 
 // Packed fp32 pairs (lo in the low word of a 64-bit register) and IEEE
 // round-to-nearest arithmetic on both lanes at once: each lane is rounded
-// exactly as the scalar operation would be.
+// exactly as the scalar operation would be.  One caution: ptxas contracts a
+// packed multiply whose result feeds a packed add or subtract into one fused
+// multiply-add, even with .rn and -fmad=false (and it folds an explicit fma
+// with a -0 addend back into that pattern).  Where a product is added, the
+// add is therefore done with the scalar __fadd_rn / __fsub_rn, which are
+// never contracted.
 __device__ __forceinline__ uint64_t f32x2_pack(float lo, float hi) {
     uint64_t v;
     asm("mov.b64 %0, {%1, %2};" : "=l"(v) : "f"(lo), "f"(hi));

@@ -63,91 +63,161 @@ struct Elem8 {
     float m[8], v[8], w[8];
 };
 
-// The update of the 8 elements at [i, i + 8).
-__device__ __forceinline__ void adam8(const AdamArgs &a, int64_t i, float msi, float wsi, Elem8 &e) {
-    const uint4 g4 = *reinterpret_cast<const uint4 *>(a.grad + i);
-    const uint2 m8 = *reinterpret_cast<const uint2 *>(a.m1 + i);
-    const uint4 v4 = *reinterpret_cast<const uint4 *>(a.m2 + i);
-    const uint4 w4 = *reinterpret_cast<const uint4 *>(a.w16 + i);
-    const uint32_t gw[4] = {g4.x, g4.y, g4.z, g4.w}, vw[4] = {v4.x, v4.y, v4.z, v4.w},
-                   ww[4] = {w4.x, w4.y, w4.z, w4.w}, mw[2] = {m8.x, m8.y};
-    const float omb1 = __fsub_rn(1.0f, a.b1), omb2 = __fsub_rn(1.0f, a.b2);
-    const float rbc1 = __fdiv_rn(1.0f, a.bc1), rbc2 = __fdiv_rn(1.0f, a.bc2);
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        float md[2];
-        e4m3x2_dec(static_cast<uint16_t>(mw[j >> 1] >> (16 * (j & 1))), md[0], md[1]);
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int k = 2 * j + h;
-            const float g = h ? bf16_hi(gw[j]) : bf16_lo(gw[j]);
-            float m = __fmul_rn(md[h], msi);
-            float v = f16_dec(static_cast<uint16_t>(vw[j] >> (16 * h)));
-            float w = __fmul_rn(f16_dec(static_cast<uint16_t>(ww[j] >> (16 * h))), wsi);
-            m = __fadd_rn(__fmul_rn(a.b1, m), __fmul_rn(omb1, g));
-            v = __fadd_rn(__fmul_rn(a.b2, v), __fmul_rn(omb2, __fmul_rn(g, g)));
-            const float u = __fdiv_rn(__fmul_rn(m, rbc1),
-                                      __fadd_rn(__fsqrt_rn(__fmul_rn(v, rbc2)), a.eps));
-            w = __fsub_rn(w, __fmul_rn(a.lr, __fadd_rn(u, __fmul_rn(a.wd, w))));
-            e.m[k] = m;
-            e.v[k] = v;
-            e.w[k] = w;
-        }
-    }
+// Loop-invariant operands, each duplicated into both lanes of an fp32 pair.
+struct AdamConst {
+    uint64_t b1, omb1, b2, omb2, rbc1, rbc2, eps, lr, wd, msi, wsi;
+};
+
+__device__ __forceinline__ AdamConst adam_const(const AdamArgs &a, float msi, float wsi) {
+    AdamConst c;
+    c.b1 = splat_f32x2(a.b1);
+    c.omb1 = splat_f32x2(__fsub_rn(1.0f, a.b1));
+    c.b2 = splat_f32x2(a.b2);
+    c.omb2 = splat_f32x2(__fsub_rn(1.0f, a.b2));
+    c.rbc1 = splat_f32x2(__fdiv_rn(1.0f, a.bc1));
+    c.rbc2 = splat_f32x2(__fdiv_rn(1.0f, a.bc2));
+    c.eps = splat_f32x2(a.eps);
+    c.lr = splat_f32x2(a.lr);
+    c.wd = splat_f32x2(a.wd);
+    c.msi = splat_f32x2(msi);
+    c.wsi = splat_f32x2(wsi);
+    return c;
 }
 
-__device__ __forceinline__ uint32_t abs_bits(float x) {
-    const uint32_t b = __float_as_uint(x) & 0x7FFFFFFFu;
-    return b > 0x7F800000u ? 0u : b;   // NaN skipped
+__device__ __forceinline__ uint64_t f16x2_to_f32x2(uint32_t h2) {
+    return f32x2_pack(f16_dec(static_cast<uint16_t>(h2 & 0xFFFF)),
+                      f16_dec(static_cast<uint16_t>(h2 >> 16)));
+}
+
+// The update of the 8 elements at [i, i + 8): the multiplies two lanes at a
+// time, the adds and subtracts (which take products as operands), square
+// roots and divides scalar, since ptxas would fuse a packed add of a packed
+// product into an fma.  Every operation is one IEEE rounding, in the order
+// above.
+struct Raw8 {
+    uint4 g4, v4, w4;
+    uint2 m8;
+};
+
+__device__ __forceinline__ Raw8 adam_load8(const AdamArgs &a, int64_t i) {
+    Raw8 r;
+    r.g4 = *reinterpret_cast<const uint4 *>(a.grad + i);
+    r.m8 = *reinterpret_cast<const uint2 *>(a.m1 + i);
+    r.v4 = *reinterpret_cast<const uint4 *>(a.m2 + i);
+    r.w4 = *reinterpret_cast<const uint4 *>(a.w16 + i);
+    return r;
+}
+
+__device__ __forceinline__ void adam8(const Raw8 &raw, const AdamConst &k, Elem8 &e) {
+    const uint4 g4 = raw.g4, v4 = raw.v4, w4 = raw.w4;
+    const uint2 m8 = raw.m8;
+    const uint32_t gw[4] = {g4.x, g4.y, g4.z, g4.w}, vw[4] = {v4.x, v4.y, v4.z, v4.w},
+                   ww[4] = {w4.x, w4.y, w4.z, w4.w}, mw[2] = {m8.x, m8.y};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        float md0, md1;
+        e4m3x2_dec(static_cast<uint16_t>(mw[j >> 1] >> (16 * (j & 1))), md0, md1);
+        const uint64_t g = f32x2_from_bf16x2(gw[j]);
+        const uint64_t m_old = f32x2_mul(f32x2_pack(md0, md1), k.msi);
+        const uint64_t v_old = f16x2_to_f32x2(vw[j]);
+        const uint64_t w_old = f32x2_mul(f16x2_to_f32x2(ww[j]), k.wsi);
+        float a0, a1, b0, b1;
+        // m = b1*m + (1-b1)*g
+        f32x2_unpack(f32x2_mul(k.b1, m_old), a0, a1);
+        f32x2_unpack(f32x2_mul(k.omb1, g), b0, b1);
+        const float m0 = __fadd_rn(a0, b0), m1 = __fadd_rn(a1, b1);
+        // v = b2*v + (1-b2)*(g*g)
+        f32x2_unpack(f32x2_mul(k.b2, v_old), a0, a1);
+        f32x2_unpack(f32x2_mul(k.omb2, f32x2_mul(g, g)), b0, b1);
+        const float v0 = __fadd_rn(a0, b0), v1 = __fadd_rn(a1, b1);
+        // u = (m * rbc1) / (sqrt(v * rbc2) + eps)
+        float n0, n1, q0, q1, e0, e1;
+        f32x2_unpack(f32x2_mul(f32x2_pack(m0, m1), k.rbc1), n0, n1);
+        f32x2_unpack(f32x2_mul(f32x2_pack(v0, v1), k.rbc2), q0, q1);
+        f32x2_unpack(k.eps, e0, e1);
+        const float u0 = __fdiv_rn(n0, __fadd_rn(__fsqrt_rn(q0), e0));
+        const float u1 = __fdiv_rn(n1, __fadd_rn(__fsqrt_rn(q1), e1));
+        // w = w - lr * (u + wd*w)
+        float w0, w1, c0, c1;
+        f32x2_unpack(w_old, w0, w1);
+        f32x2_unpack(f32x2_mul(k.wd, w_old), c0, c1);
+        f32x2_unpack(f32x2_mul(k.lr, f32x2_pack(__fadd_rn(u0, c0), __fadd_rn(u1, c1))), c0, c1);
+        e.m[2 * j] = m0;
+        e.m[2 * j + 1] = m1;
+        e.v[2 * j] = v0;
+        e.v[2 * j + 1] = v1;
+        e.w[2 * j] = __fsub_rn(w0, c0);
+        e.w[2 * j + 1] = __fsub_rn(w1, c1);
+    }
 }
 
 __global__ void __launch_bounds__(256) adam_amax_kernel(const AdamArgs a) {
     pdl_wait();
     pdl_trigger();
-    const float msi = *a.m1_scale_inv, wsi = *a.w_scale_inv;
-    uint32_t mm = 0, mw = 0;
+    const AdamConst k = adam_const(a, *a.m1_scale_inv, *a.w_scale_inv);
+    float mm = 0.0f, mw = 0.0f;   // max |new m|, max |new w|; fmaxf skips NaN
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x * 8;
-    for (int64_t i = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) * 8; i < a.n;
-         i += stride) {
+    int64_t i = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) * 8;
+    // two groups of 8 in flight per thread: this pass reads and computes only
+    for (; i + stride < a.n; i += 2 * stride) {
+        const Raw8 r0 = adam_load8(a, i), r1 = adam_load8(a, i + stride);
         Elem8 e;
-        adam8(a, i, msi, wsi, e);
+        adam8(r0, k, e);
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            mm = max(mm, abs_bits(e.m[k]));
-            mw = max(mw, abs_bits(e.w[k]));
+        for (int j = 0; j < 8; ++j) {
+            mm = fmaxf(mm, fabsf(e.m[j]));
+            mw = fmaxf(mw, fabsf(e.w[j]));
+        }
+        adam8(r1, k, e);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            mm = fmaxf(mm, fabsf(e.m[j]));
+            mw = fmaxf(mw, fabsf(e.w[j]));
         }
     }
-    mm = __reduce_max_sync(0xFFFFFFFFu, mm);
-    mw = __reduce_max_sync(0xFFFFFFFFu, mw);
+    if (i < a.n) {
+        Elem8 e;
+        adam8(adam_load8(a, i), k, e);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            mm = fmaxf(mm, fabsf(e.m[j]));
+            mw = fmaxf(mw, fabsf(e.w[j]));
+        }
+    }
+    uint32_t bm = __reduce_max_sync(0xFFFFFFFFu, __float_as_uint(mm));
+    uint32_t bw = __reduce_max_sync(0xFFFFFFFFu, __float_as_uint(mw));
     if ((threadIdx.x & 31) == 0) {
-        if (mm) atomicMax(reinterpret_cast<unsigned *>(a.amax), mm);
-        if (mw) atomicMax(reinterpret_cast<unsigned *>(a.amax + 1), mw);
+        if (bm) atomicMax(reinterpret_cast<unsigned *>(a.amax), bm);
+        if (bw) atomicMax(reinterpret_cast<unsigned *>(a.amax + 1), bw);
     }
 }
 
 __global__ void __launch_bounds__(256) adam_apply_kernel(const AdamArgs a) {
     pdl_wait();
     pdl_trigger();
-    const float msi = *a.m1_scale_inv, wsi = *a.w_scale_inv;
+    const AdamConst k = adam_const(a, *a.m1_scale_inv, *a.w_scale_inv);
     bool valid;
     const float sm = recipe_scale(a.amax[0], 448.0f, a.margin, *a.m1_scale, valid);
     const float sw = recipe_scale(a.amax[1], kF16Max, a.margin, *a.w_scale, valid);
+    const uint64_t sm2 = splat_f32x2(sm), sw2 = splat_f32x2(sw);
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x * 8;
     for (int64_t i = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) * 8; i < a.n;
          i += stride) {
         Elem8 e;
-        adam8(a, i, msi, wsi, e);
+        adam8(adam_load8(a, i), k, e);
         uint32_t mq[2], vq[4], wq[4], bq[4];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            const uint32_t c = cvt2_e4m3(__fmul_rn(e.m[2 * j], sm), __fmul_rn(e.m[2 * j + 1], sm));
+            float a0, a1, c0, c1;
+            f32x2_unpack(f32x2_mul(f32x2_pack(e.m[2 * j], e.m[2 * j + 1]), sm2), a0, a1);
+            const uint32_t c = cvt2_e4m3(a0, a1);
             if (j & 1)
                 mq[j >> 1] |= c << 16;
             else
                 mq[j >> 1] = c;
             vq[j] = f16_enc_sat(e.v[2 * j]) | (static_cast<uint32_t>(f16_enc_sat(e.v[2 * j + 1])) << 16);
-            wq[j] = f16_enc_sat(__fmul_rn(e.w[2 * j], sw)) |
-                    (static_cast<uint32_t>(f16_enc_sat(__fmul_rn(e.w[2 * j + 1], sw))) << 16);
+            f32x2_unpack(f32x2_mul(f32x2_pack(e.w[2 * j], e.w[2 * j + 1]), sw2), c0, c1);
+            wq[j] = f16_enc_sat(c0) | (static_cast<uint32_t>(f16_enc_sat(c1)) << 16);
             const __nv_bfloat162 b2 = __floats2bfloat162_rn(e.w[2 * j], e.w[2 * j + 1]);
             bq[j] = *reinterpret_cast<const uint32_t *>(&b2);
         }

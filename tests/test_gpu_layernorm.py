@@ -6,7 +6,12 @@ agrees to a few fp32 rounding errors of the terms it combines, not bit for
 bit.  Hence: mean / rstd / amax(y) within 1e-5 relative; every FP8 code is a
 correct cast of some value within that error band around the oracle's exact
 y * s (band = 2^-16 x ((|x| + |mean|) * rstd * |gamma| + |beta|) * s), and
-codes that differ from the cast of the exact value must be rare."""
+codes that differ from the cast of the exact value must be rare.
+
+The elementwise part is checked bit for bit on its own: given the kernel's
+own mean and rstd, y = ((x - mean) * rstd) * gamma + beta evaluated in numpy
+float32 (one rounding per operation, nothing fused), times s and cast by the
+oracle's encoder, must reproduce every code and the amax exactly."""
 import numpy as np
 import pytest
 import torch
@@ -30,6 +35,22 @@ def _inputs(rows, cols, seed, mag=1.0):
     gamma = (1 + 0.2 * torch.randn(cols, generator=g)).to(torch.bfloat16)
     beta = (0.1 * torch.randn(cols, generator=g)).to(torch.bfloat16)
     return x.cuda(), gamma.cuda(), beta.cuda()
+
+
+def check_elementwise_exact(gpu, x, gamma, beta, mean_gpu, rstd_gpu, s, fmt, amax_gpu, what):
+    """x, gamma, beta as BF16 bits; mean_gpu, rstd_gpu the kernel's fp32 statistics."""
+    widen = lambda b: (np.asarray(b, np.uint16).astype(np.uint32) << 16).view(np.float32)
+    xf = widen(x)
+    mu = np.asarray(mean_gpu, np.float32)[:, None]
+    rs = np.asarray(rstd_gpu, np.float32)[:, None]
+    y = (((xf - mu) * rs) * widen(gamma)[None, :]) + widen(beta)[None, :]
+    assert y.dtype == np.float32
+    ref = o.fp8_encode((y * np.float32(s)).astype(np.float32), fmt).reshape(y.shape)
+    from helpers import assert_fp8_equal
+    assert_fp8_equal(gpu, ref, fmt, what + " (elementwise, bit-exact)")
+    if amax_gpu is not None:
+        a = np.abs(y)
+        assert np.float32(amax_gpu).view(np.uint32) == np.float32(a[~np.isnan(a)].max()).view(np.uint32)
 
 
 def check_codes(gpu, x, gamma, beta, mean, rstd, y, s, fmt, what):
@@ -62,6 +83,8 @@ def test_layernorm_cast_matches_oracle(rows, cols, fmt):
     assert abs(am.item() - np.abs(y).max()) <= 1e-5 * np.abs(y).max()
     q = host_u8(out)
     check_codes(q, xb, gb, bb, mu, rs, y, s, fmt, f"{rows}x{cols} out")
+    check_elementwise_exact(q, xb, gb, bb, mean.cpu().numpy(), rstd.cpu().numpy(), s, fmt,
+                            am.item(), f"{rows}x{cols}")
     assert np.array_equal(host_u8(out_t), q.T)
 
 
@@ -88,6 +111,8 @@ def test_layernorm_linear_step_matches_oracle():
         X8 = host_u8(lin.X8)
         check_codes(X8, xb, gb, bb, mu, rs, y, lin.meta.scale[o.SLOT_X].item(), o.E4M3,
                     "LN(X) codes")
+        check_elementwise_exact(X8, xb, gb, bb, lin.mean.cpu().numpy(), lin.rstd.cpu().numpy(),
+                                lin.meta.scale[o.SLOT_X].item(), o.E4M3, None, "LN(X)")
         # the GEMMs from the GPU's own FP8 operands (parity of the GEMM itself is
         # tested elsewhere); the operands must be the oracle's up to tie codes
         rc = o.Recipe(w.margin, w.history_len, w.hybrid)
