@@ -108,8 +108,8 @@ __global__ void __launch_bounds__(256)
 // ----------------------------------------------------- quantize_transpose --
 //
 // Persistent CTAs of 256 threads (two per SM) convert 128 x 128 tiles.  The
-// BF16 input reaches shared memory through a 3-stage TMA ring, so the loads of
-// the next tiles are in flight while the current one is converted:
+// BF16 input reaches shared memory through a 2-stage TMA ring, so the load of
+// the next tile is in flight while the current one is converted:
 //  phase 1  each thread takes 8 x 16 B of BF16 from the staged tile, scales,
 //           converts to FP8, stores 8 B to the row-major output and the same
 //           8 B into a tile of 32-bit words [128 rows][32 words] whose word
@@ -120,13 +120,17 @@ __global__ void __launch_bounds__(256)
 //           16-byte runs of the transposed output; the 8 threads sharing a
 //           column write one contiguous 128-byte line.
 // The staged tile is released (and the TMA load of a later tile issued) as
-// soon as phase 1 is done with it.  Waits are bounded.
+// soon as phase 1 is done with it.  Consecutive tiles use alternate word
+// tiles, so one barrier per tile suffices: a thread starting phase 1 of tile
+// t+1 has passed the barrier after phase 1 of tile t, which every thread
+// reached only after finishing phase 2 of tile t-1, the last reader of that
+// word tile.  Waits are bounded.
 
 constexpr int kQtTile = 128;
 constexpr int kQtThreads = 256;
-constexpr int kQtStages = 3;
+constexpr int kQtStages = 2;
 constexpr int kQtStageBytes = kQtTile * kQtTile * 2;
-constexpr size_t kQtSmem = 128 + kQtStages * kQtStageBytes + kQtTile * kQtTile + 64;
+constexpr size_t kQtSmem = 128 + kQtStages * kQtStageBytes + 2 * kQtTile * kQtTile + 64;
 
 __device__ __forceinline__ int qt_swz(int row) { return ((row >> 4) & 7) << 2; }
 
@@ -179,9 +183,9 @@ __global__ void __launch_bounds__(kQtThreads, 2)
     uint8_t *base = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(qt_smem_raw) + 127) & ~static_cast<uintptr_t>(127));
     uint8_t *stage_base = base;
-    uint32_t *tile = reinterpret_cast<uint32_t *>(base + kQtStages * kQtStageBytes);
+    uint32_t *tile0 = reinterpret_cast<uint32_t *>(base + kQtStages * kQtStageBytes);
     uint64_t *full = reinterpret_cast<uint64_t *>(base + kQtStages * kQtStageBytes +
-                                                  kQtTile * kQtTile);
+                                                  2 * kQtTile * kQtTile);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(full + kQtStages);
 
     const int tid = threadIdx.x;
@@ -263,15 +267,10 @@ __global__ void __launch_bounds__(kQtThreads, 2)
             }
         }
         const bool ok = mbar_wait(smem_u32(full + st), parity, abort_flag);
-        if (__syncthreads_or(!ok)) {
-            if (tid == 0) {
-                atomicOr(&g_cast_error_flags, kErrWaitTimeout);
-                *abort_flag = 1;
-            }
-            break;
-        }
-        if (tid == 0) ++consumed[st];
         const uint16_t *xs = reinterpret_cast<const uint16_t *>(stage_base + st * kQtStageBytes);
+        uint32_t *tile = tile0 + (it & 1) * (kQtTile * kQtTile / 4);   // word tile of this iteration
+        if (ok) {
+        if (tid == 0) ++consumed[st];
 
         uint4 v[8];
 #pragma unroll
@@ -355,7 +354,16 @@ __global__ void __launch_bounds__(kQtThreads, 2)
             tmax[1] = max(tmax[1], m);
         else
             tmax[0] = max(tmax[0], m);
-        __syncthreads();  // stage st fully read; word tile complete
+        }
+        // stage st fully read and this word tile complete; a thread whose
+        // wait gave up skipped phase 1 and makes every thread leave together
+        if (__syncthreads_or(!ok)) {
+            if (tid == 0) {
+                atomicOr(&g_cast_error_flags, kErrWaitTimeout);
+                *abort_flag = 1;
+            }
+            break;
+        }
 
         if (tid == 0) {
             const int64_t tn = t + static_cast<int64_t>(kQtStages) * gridDim.x;
@@ -386,7 +394,6 @@ __global__ void __launch_bounds__(kQtThreads, 2)
                         make_uint4(o[cc][0], o[cc][1], o[cc][2], o[cc][3]);
             }
         }
-        __syncthreads();  // word tile free for the next tile
     }
 
     // Loads still in flight (only after an abandoned wait) must land before exit.
