@@ -30,8 +30,8 @@
 // memory and write both CTAs' tensor memory.  No TMA multicast is used.
 // One launch may carry two independent GEMMs (the backward pass's dgrad and
 // wgrad): their tiles form one list, so the last, partly filled wave of one
-// is filled with tiles of the other.  Tiles are visited in groups of 16
-// row-blocks so that concurrently running CTAs share operand slices in L2.
+// is filled with tiles of the other.  Tiles are visited in groups of
+// row-blocks chosen per problem so that the smaller operand stays in L2.
 // Every wait is bounded.
 #include <cuda_bf16.h>
 
@@ -50,7 +50,8 @@ namespace {
 constexpr int BM = 128, BN = 256, BK = 128;
 constexpr int NUM_THREADS = 192;
 constexpr int TMEM_COLS = 2 * BN;
-constexpr int GROUP_M = 16;
+constexpr int GROUP_M = 16;                 // row-blocks per raster group when neither operand fits
+constexpr int64_t RESIDENT_BYTES = 48 << 20;   // an operand this small is kept in L2
 constexpr int MAX_PROBLEMS = 2;
 constexpr int EPI_COLS = 64;                      // output columns per TMA store (128 B of BF16)
 constexpr int EPI_BUF = 32 * EPI_COLS * 2;        // one warp's staging buffer: 32 rows x 128 B
@@ -77,6 +78,7 @@ struct GemmProblem {
     const float *b_scale_inv;
     int64_t M, N;
     int tiles_m, tiles_n, num_kb;
+    int group_m;      // row-blocks per raster group (see make_args)
     int tile_begin;   // first index of this problem's tiles in the launch's tile list
     uint32_t idesc;
 };
@@ -89,11 +91,12 @@ struct GemmArgs {
     int num_tiles;
 };
 
-__device__ __forceinline__ void tile_coords(int tile, int tiles_m, int tiles_n, int &mb, int &nb) {
-    const int group = tile / (GROUP_M * tiles_n);
-    const int first_m = group * GROUP_M;
-    const int gm = min(tiles_m - first_m, GROUP_M);
-    const int in = tile - group * GROUP_M * tiles_n;
+__device__ __forceinline__ void tile_coords(int tile, int tiles_m, int tiles_n, int group_m,
+                                            int &mb, int &nb) {
+    const int group = tile / (group_m * tiles_n);
+    const int first_m = group * group_m;
+    const int gm = min(tiles_m - first_m, group_m);
+    const int in = tile - group * group_m * tiles_n;
     mb = first_m + in % gm;
     nb = in / gm;
 }
@@ -101,7 +104,8 @@ __device__ __forceinline__ void tile_coords(int tile, int tiles_m, int tiles_n, 
 // Problem and (row-block, column-block) of a tile of the launch's list.
 __device__ __forceinline__ int locate(const GemmArgs &a, int tile, int &mb, int &nb) {
     const int p = (a.num_problems > 1 && tile >= a.prob[1].tile_begin) ? 1 : 0;
-    tile_coords(tile - a.prob[p].tile_begin, a.prob[p].tiles_m, a.prob[p].tiles_n, mb, nb);
+    tile_coords(tile - a.prob[p].tile_begin, a.prob[p].tiles_m, a.prob[p].tiles_n,
+                a.prob[p].group_m, mb, nb);
     return p;
 }
 
@@ -508,6 +512,18 @@ cudaError_t launch_gemm_group(const GemmSpec *specs, int n, int sm_count, cudaSt
         p.tiles_m = static_cast<int>((g.M + tile_m - 1) / tile_m);
         p.tiles_n = static_cast<int>((g.N + BN - 1) / BN);
         p.num_kb = static_cast<int>((g.K + BK - 1) / BK);
+        // Raster: tiles are walked down groups of group_m row-blocks.  When
+        // one operand is small enough to stay in L2, walk so that it does
+        // and the other streams through once: all row-blocks at a time when
+        // A is the smaller (A resident), two row-blocks when B is (B
+        // resident).  Otherwise groups of GROUP_M row-blocks.
+        const int64_t a_bytes = g.M * g.K, b_bytes = g.N * g.K;
+        if (a_bytes <= b_bytes && a_bytes <= RESIDENT_BYTES)
+            p.group_m = p.tiles_m;
+        else if (b_bytes < a_bytes && b_bytes <= RESIDENT_BYTES)
+            p.group_m = 2;
+        else
+            p.group_m = GROUP_M;
         p.tile_begin = tiles;
         p.idesc = idesc_f8(static_cast<uint32_t>(g.fa), static_cast<uint32_t>(g.fb),
                            static_cast<uint32_t>(tile_m), BN);
