@@ -617,7 +617,10 @@ def main():
             print(json.dumps(line), flush=True)
         return
     import __graft_entry__
-    __graft_entry__._build_module().build()
+    # one rank (re)builds the in-tree library if it is stale; the others wait
+    if rank == 0:
+        __graft_entry__._build_module().build()
+    barrier(world)
     import fp8_mixed_precision_amax_gb300 as f
     pk, peak_kind = peaks()
     w = wl.WORKLOADS[args.workload]
