@@ -554,6 +554,45 @@ def run_secondary(f, args, pk):
         "ln_cast_us": tm.mean_ms("ln_cast") * 1e3, "cast_us": tm.mean_ms("cast") * 1e3,
         "ln_cast_gbs": 4 * ne / (tm.mean_ms("ln_cast") / 1e3) / 1e9,
         "note": "4 B/element algorithmic; L2 flushed before each launch"}
+    # just-in-time (current) scaling: the same 7B layer step with X, W and dY
+    # scaled from their own amax (an amax pass before each cast)
+    lj = f.Fp8Linear(wl.layer_weight(w7, "cuda"), w7.M,
+                     f.Recipe(margin=w7.margin, history_len=w7.history_len, hybrid=w7.hybrid,
+                              current=True))
+    xs7 = [wl.layer_x(w7, k, "cuda") for k in (0, 1)]
+    dys7 = [wl.layer_dy(w7, k, "cuda") for k in (0, 1)]
+    for i in range(3):
+        lj.step(xs7[i % 2], dys7[i % 2])
+    torch.cuda.synchronize()
+    nj = 30
+    s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s0.record()
+    for i in range(nj):
+        lj.step(xs7[i % 2], dys7[i % 2])
+    s1.record()
+    torch.cuda.synchronize()
+    msj = s0.elapsed_time(s1) / nj
+    out["jit_scaling_layer_step_mlp7b"] = {
+        "ms_per_step": msj, "value": 6 * w7.M * w7.N * w7.K / (msj / 1e3) / 1e12,
+        "unit": "TFLOPS", "note": "X, W and dY scaled just in time from their own amax"}
+    del lj, xs7, dys7
+    # the device part of the FP8 gradient all-reduce: decode and sum 8 ranks'
+    # FP8 codes of the 7B dW (shared scale) into BF16; 8 B read + 2 B written
+    # per element for 8 ranks
+    nr, nd = 8, w7.N * w7.K
+    parts = torch.randint(0, 0x7B, (nr, nd), dtype=torch.uint8, device="cuda")
+    dsum = torch.empty(nd, dtype=torch.bfloat16, device="cuda")
+    sc1 = torch.full((1,), 64.0, device="cuda")
+    for i in range(23):
+        flush.zero_()
+        tm.time("dequant_sum", lambda: f.fp8_dequant_sum(parts, f.E5M2, sc1, dsum))
+    torch.cuda.synchronize()
+    tm.pairs["dequant_sum"] = tm.pairs["dequant_sum"][3:]
+    out["fp8_allreduce_sum_8ranks_mlp7b_dW"] = {
+        "us": tm.mean_ms("dequant_sum") * 1e3,
+        "gbs_algorithmic": (nr + 2) * nd / (tm.mean_ms("dequant_sum") / 1e3) / 1e9,
+        "note": "decode + rank-order sum of 8 ranks' E5M2 codes -> BF16; L2 flushed before each"}
+    del parts, dsum
     out["context_cublaslt_fp8_mlp7b"] = cublaslt_context(f, w7, flush)
     return out
 

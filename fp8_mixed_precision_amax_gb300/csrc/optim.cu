@@ -248,20 +248,30 @@ __global__ void adam_scales_kernel(const AdamArgs a) {
 //
 // out[i] = bf16_rne(fl32(sum_r dec(q[r][i]) * fl32(1 / scale))): the parts of
 // all ranks share one scale (the minimum of the ranks' own scales), so their
-// codes can be decoded and summed directly.  The sum runs in double in rank
-// order (exact: every FP8 value has at most 3 significant bits within a
-// 2^-16 .. 2^16 range), the product in double, then one rounding to fp32
-// and one to BF16.
+// codes can be decoded and summed directly.  The sum is exact and the product
+// is rounded in double, then to fp32 and to BF16.
+//
+// Every finite FP8 value is an integer number of the format's quantum (2^-9
+// for E4M3, 2^-16 for E5M2), at most 57344 * 2^16 < 2^32 of them, so the sum
+// over up to 65536 ranks is accumulated exactly in int64 through a 256-entry
+// table of quanta in shared memory (GB300's FP64 rate made a double
+// accumulation the bottleneck).  (double) sum * 2^-q is then exactly the
+// double sum of the decoded values, and folding 2^-q into the double scale
+// leaves the one rounding of the product unchanged.  Infinity and NaN codes
+// are rare: a four-codes-at-once test sends them to a path that records them,
+// and the result follows IEEE double addition (NaN, or +inf and -inf
+// together, give NaN; one infinity gives that infinity).
 
 template <int FMT>
-__device__ __forceinline__ void fp8x2_dec(uint16_t c, float &lo, float &hi) {
-    uint32_t h2;
-    if constexpr (FMT == 0)
-        asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(c));
-    else
-        asm("cvt.rn.f16x2.e5m2x2 %0, %1;" : "=r"(h2) : "h"(c));
-    lo = __half2float(__ushort_as_half(static_cast<uint16_t>(h2 & 0xFFFF)));
-    hi = __half2float(__ushort_as_half(static_cast<uint16_t>(h2 >> 16)));
+__device__ __forceinline__ int64_t fp8_quanta(uint32_t c) {
+    constexpr int MB = FMT == 0 ? 3 : 2;             // mantissa bits
+    constexpr uint32_t EMAX = FMT == 0 ? 15u : 31u;  // exponent field of specials
+    const uint32_t e = (c >> MB) & EMAX, m = c & ((1u << MB) - 1u);
+    const bool special = FMT == 0 ? (e == 15u && m == 7u) : (e == 31u);
+    int64_t mag = e == 0 ? static_cast<int64_t>(m)
+                         : static_cast<int64_t>((1u << MB) | m) << (e - 1u);
+    if (special) mag = 0;
+    return (c & 0x80u) ? -mag : mag;
 }
 
 template <int FMT>
@@ -269,29 +279,58 @@ __global__ void __launch_bounds__(256) dequant_sum_kernel(const uint8_t *__restr
                                                           int nranks, int64_t n,
                                                           const float *__restrict__ scale,
                                                           uint16_t *__restrict__ out) {
+    __shared__ long long lut[256];
+    lut[threadIdx.x] = fp8_quanta<FMT>(threadIdx.x);   // blockDim.x == 256
+    __syncthreads();
     pdl_wait();
     pdl_trigger();
-    const double sinv = static_cast<double>(__fdiv_rn(1.0f, *scale));
+    // 2^-q * fl32(1/scale), exact in double
+    const double k = static_cast<double>(__fdiv_rn(1.0f, *scale)) * (FMT == 0 ? 0x1p-9 : 0x1p-16);
+    const uint32_t smask = FMT == 0 ? 0x7F7F7F7Fu : 0x7C7C7C7Cu;   // bits that mark a special
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x * 8;
     for (int64_t i = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) * 8; i < n;
          i += stride) {
-        double acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+        long long acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+        uint32_t flags = 0;   // 3 bits per element: NaN, +inf, -inf
         for (int r = 0; r < nranks; ++r) {
             const uint2 c = *reinterpret_cast<const uint2 *>(q + static_cast<int64_t>(r) * n + i);
             const uint32_t cw[2] = {c.x, c.y};
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                float lo, hi;
-                fp8x2_dec<FMT>(static_cast<uint16_t>(cw[j >> 1] >> (16 * (j & 1))), lo, hi);
-                acc[2 * j] += static_cast<double>(lo);
-                acc[2 * j + 1] += static_cast<double>(hi);
+            for (int h = 0; h < 2; ++h) {
+                const uint32_t w = cw[h];
+#pragma unroll
+                for (int b = 0; b < 4; ++b) acc[4 * h + b] += lut[(w >> (8 * b)) & 0xFFu];
+                if (__vcmpeq4(w & smask, smask)) {
+#pragma unroll
+                    for (int b = 0; b < 4; ++b) {
+                        const uint32_t cb = (w >> (8 * b)) & 0xFFu;
+                        if ((cb & (smask & 0xFFu)) != (smask & 0xFFu)) continue;
+                        uint32_t fl;
+                        if (FMT == 0 || (cb & 3u) != 0u)
+                            fl = 1u;                       // NaN
+                        else
+                            fl = (cb & 0x80u) ? 4u : 2u;   // -inf : +inf
+                        flags |= fl << (3 * (4 * h + b));
+                    }
+                }
             }
         }
         uint32_t o[4];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            const __nv_bfloat162 b = __floats2bfloat162_rn(__double2float_rn(acc[2 * j] * sinv),
-                                                           __double2float_rn(acc[2 * j + 1] * sinv));
+            float y[2];
+#pragma unroll
+            for (int t = 0; t < 2; ++t) {
+                const int e = 2 * j + t;
+                const uint32_t fe = (flags >> (3 * e)) & 7u;
+                if (fe == 0u)
+                    y[t] = __double2float_rn(static_cast<double>(acc[e]) * k);
+                else if ((fe & 1u) || fe == 6u)
+                    y[t] = __int_as_float(0x7FFFFFFF);
+                else
+                    y[t] = (fe & 2u) ? __int_as_float(0x7F800000) : __int_as_float(0xFF800000);
+            }
+            const __nv_bfloat162 b = __floats2bfloat162_rn(y[0], y[1]);
             o[j] = *reinterpret_cast<const uint32_t *>(&b);
         }
         *reinterpret_cast<uint4 *>(out + i) = make_uint4(o[0], o[1], o[2], o[3]);

@@ -39,6 +39,58 @@ def test_dequant_sum_bit_exact(fmt, nranks):
     assert np.array_equal(_u16(out), o.dequant_sum(parts, fmt, s))
 
 
+def _same_bf16(a, b):
+    """Equal BF16 bits, NaN compared as a class."""
+    nan_a = ((a & 0x7F80) == 0x7F80) & ((a & 0x7F) != 0)
+    nan_b = ((b & 0x7F80) == 0x7F80) & ((b & 0x7F) != 0)
+    return np.array_equal(nan_a, nan_b) and np.array_equal(a[~nan_a], b[~nan_b])
+
+
+@pytest.mark.parametrize("fmt", [o.E4M3, o.E5M2])
+def test_dequant_sum_specials_and_extremes(fmt):
+    """Infinities and NaN among the parts follow IEEE double addition (NaN,
+    or +inf with -inf, give NaN); 64 ranks of the largest magnitudes and
+    mixed signs stay exact; a 4 M-element case runs several grid-stride
+    passes of the kernel."""
+    import fp8_mixed_precision_amax_gb300 as f
+    rng = np.random.default_rng(7 + fmt)
+    table = o.fp8_decode_table(fmt)
+    finite = np.nonzero(np.isfinite(table))[0].astype(np.uint8)
+    specials = np.nonzero(~np.isfinite(table))[0].astype(np.uint8)
+    top = 0x7E if fmt == o.E4M3 else 0x7B
+    cases = []
+    # sprinkle every special code into random finite parts
+    parts = rng.choice(finite, size=(5, 4096))
+    for j, c in enumerate(specials):
+        parts[j % 5, rng.integers(0, 4096, 64)] = c
+    cases.append(parts)
+    if fmt == o.E5M2:   # +inf and -inf in the same element, and each alone
+        p2 = rng.choice(finite, size=(3, 64))
+        p2[0, :16], p2[1, :16] = 0x7C, 0xFC
+        p2[0, 16:32] = 0x7C
+        p2[2, 32:48] = 0xFC
+        cases.append(p2)
+    cases.append(np.where(rng.random((64, 2048)) < 0.5, top, top | 0x80).astype(np.uint8))
+    cases.append(np.full((64, 1024), top, np.uint8))
+    cases.append(rng.choice(finite, size=(3, (1 << 22) + 16)))
+    scales = [np.float32(1e-30), np.float32(3e38), np.float32(1e36), np.float32(2.0 ** -100)]
+    for ci, parts in enumerate(cases):
+        s = np.float32(10.0 ** rng.uniform(-4, 2))
+        out = torch.empty(parts.shape[1], dtype=torch.bfloat16, device="cuda")
+        f.fp8_dequant_sum(torch.from_numpy(np.ascontiguousarray(parts)).cuda(), fmt,
+                          torch.tensor([s], device="cuda"), out)
+        torch.cuda.synchronize()
+        assert _same_bf16(_u16(out), o.dequant_sum(parts, fmt, s)), parts.shape
+    # results past FLT_MAX, in the fp32 subnormal range and at its edge
+    parts = rng.choice(finite, size=(4, 8192))
+    for s in scales:
+        out = torch.empty(parts.shape[1], dtype=torch.bfloat16, device="cuda")
+        f.fp8_dequant_sum(torch.from_numpy(parts).cuda(), fmt, torch.tensor([s], device="cuda"),
+                          out)
+        torch.cuda.synchronize()
+        assert _same_bf16(_u16(out), o.dequant_sum(parts, fmt, s)), s
+
+
 def _grads(world, shape, seed):
     out = []
     for r in range(world):
