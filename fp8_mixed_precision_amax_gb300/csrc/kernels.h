@@ -11,7 +11,7 @@ namespace fp8k {
 
 // Tiled 2-D TMA descriptor of a row-major [outer][inner] tensor of 1- or
 // 2-byte elements with a box of box_outer x box_inner elements, optionally
-// with 128-byte swizzling (tmap.cu).  False if the driver rejects it.
+// with 128-byte swizzling (tmap.cu).  False if cuTensorMapEncodeTiled rejects it.
 bool encode_tmap_2d(CUtensorMap *map, const void *base, bool two_byte, int64_t inner,
                     int64_t outer, uint32_t box_inner, uint32_t box_outer, bool swizzle128);
 
