@@ -292,25 +292,35 @@ __global__ void __launch_bounds__(256) dequant_sum_kernel(const uint8_t *__restr
          i += stride) {
         long long acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
         uint32_t flags = 0;   // 3 bits per element: NaN, +inf, -inf
-        for (int r = 0; r < nranks; ++r) {
-            const uint2 c = *reinterpret_cast<const uint2 *>(q + static_cast<int64_t>(r) * n + i);
-            const uint32_t cw[2] = {c.x, c.y};
+        // four ranks' codes in flight at a time (the sum is exact, so the
+        // order in which ranks are added does not matter)
+        for (int r0 = 0; r0 < nranks; r0 += 4) {
+            uint2 c[4];
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const uint32_t w = cw[h];
+            for (int u = 0; u < 4; ++u)
+                c[u] = r0 + u < nranks ? *reinterpret_cast<const uint2 *>(
+                                             q + static_cast<int64_t>(r0 + u) * n + i)
+                                       : make_uint2(0u, 0u);   // code 0 adds +0
 #pragma unroll
-                for (int b = 0; b < 4; ++b) acc[4 * h + b] += lut[(w >> (8 * b)) & 0xFFu];
-                if (__vcmpeq4(w & smask, smask)) {
+            for (int u = 0; u < 4; ++u) {
+                const uint32_t cw[2] = {c[u].x, c[u].y};
 #pragma unroll
-                    for (int b = 0; b < 4; ++b) {
-                        const uint32_t cb = (w >> (8 * b)) & 0xFFu;
-                        if ((cb & (smask & 0xFFu)) != (smask & 0xFFu)) continue;
-                        uint32_t fl;
-                        if (FMT == 0 || (cb & 3u) != 0u)
-                            fl = 1u;                       // NaN
-                        else
-                            fl = (cb & 0x80u) ? 4u : 2u;   // -inf : +inf
-                        flags |= fl << (3 * (4 * h + b));
+                for (int h = 0; h < 2; ++h) {
+                    const uint32_t w = cw[h];
+#pragma unroll
+                    for (int b = 0; b < 4; ++b) acc[4 * h + b] += lut[(w >> (8 * b)) & 0xFFu];
+                    if (__vcmpeq4(w & smask, smask)) {
+#pragma unroll
+                        for (int b = 0; b < 4; ++b) {
+                            const uint32_t cb = (w >> (8 * b)) & 0xFFu;
+                            if ((cb & (smask & 0xFFu)) != (smask & 0xFFu)) continue;
+                            uint32_t fl;
+                            if (FMT == 0 || (cb & 3u) != 0u)
+                                fl = 1u;                       // NaN
+                            else
+                                fl = (cb & 0x80u) ? 4u : 2u;   // -inf : +inf
+                            flags |= fl << (3 * (4 * h + b));
+                        }
                     }
                 }
             }
