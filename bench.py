@@ -430,10 +430,32 @@ def cpu_baseline(w: wl.Workload, seconds: float = 12.0, Mp: int = 256, Np: int =
         total_t += dt
         total_f += fl
         reps += 1
-    return {"value": total_f / total_t / 1e12, "unit": "TFLOPS", "cores": o.num_threads(),
+    line = {"value": total_f / total_t / 1e12, "unit": "TFLOPS", "cores": o.num_threads(),
             "kind": "oracle",
             "sample": f"{reps} oracle layer steps on a {Mp}-token x {Np}-feature slice of "
-                      f"{w.name} (K={w.K}), {total_t:.1f} s of CPU time"}
+                      f"{w.name} (K={w.K}), {total_t:.1f} s of CPU time",
+            "affinity_cores": len(os.sched_getaffinity(0))}
+    # the same oracle on one thread (OpenMP), on a quarter of the slice
+    try:
+        import ctypes
+        gomp = ctypes.CDLL("libgomp.so.1")
+        n0 = o.num_threads()
+        gomp.omp_set_num_threads(1)
+        try:
+            t1, f1, r1, st1 = 0.0, 0, 0, None
+            while t1 < 4.0 or r1 < 2:
+                dt, fl, st1 = oracle_sample_step(o, w, Mp // 2, Np // 2, st1)
+                t1 += dt
+                f1 += fl
+                r1 += 1
+        finally:
+            gomp.omp_set_num_threads(n0)
+        line["single_thread"] = {"value": f1 / t1 / 1e12, "unit": "TFLOPS", "cores": 1,
+                                 "sample": f"{r1} steps on a {Mp // 2}-token x {Np // 2}-feature "
+                                           f"slice, {t1:.1f} s"}
+    except OSError:
+        pass
+    return line
 
 
 def run_reference(args, world, rank):
