@@ -77,6 +77,7 @@ def _load() -> ctypes.CDLL:
         "fp8_last_error": ([], ctypes.c_char_p),
         "fp8_sync_status": ([vp], ctypes.c_int),
         "fp8_amax": ([vp, i64, vp, vp], ctypes.c_int),
+        "fp8_selftest_wait_timeout": ([i64, vp], ctypes.c_int),
         "fp8_quantize_transpose": ([vp, i64, i64, vp, i32, vp, vp, vp, vp], ctypes.c_int),
         "fp8_quantize_f32": ([vp, i64, vp, i32, vp, vp, vp], ctypes.c_int),
         "fp8_quantize_transpose_current": ([vp, i64, i64, i32, i32, vp, vp, vp, vp, vp, vp],
@@ -170,6 +171,12 @@ def _p8(t, name):
 
 def fp8_sync_status(stream=None) -> None:
     _check(_lib.fp8_sync_status(_stream(stream)))
+
+
+def fp8_selftest_wait_timeout(limit_ns: int, stream=None) -> None:
+    """Diagnostic: a kernel whose bounded wait runs out after ``limit_ns``;
+    the next fp8_sync_status raises Fp8Error with FP8_ERR_TIMEOUT."""
+    _check(_lib.fp8_selftest_wait_timeout(int(limit_ns), _stream(stream)))
 
 
 def fp8_amax(x: torch.Tensor, amax: torch.Tensor, stream=None) -> None:

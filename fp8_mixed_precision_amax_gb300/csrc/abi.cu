@@ -142,6 +142,17 @@ fp8_status fp8_sync_status(void *stream) {
     return FP8_OK;
 }
 
+fp8_status fp8_selftest_wait_timeout(int64_t limit_ns, void *stream) {
+    const char *fn = "fp8_selftest_wait_timeout";
+    if (limit_ns < 1 || limit_ns > 5000000000ll)
+        return fail(FP8_ERR_ARG, "%s: limit_ns %lld outside [1, 5e9]", fn,
+                    static_cast<long long>(limit_ns));
+    FP8_CUDA(fp8k::launch_selftest_wait(static_cast<uint64_t>(limit_ns),
+                                        static_cast<cudaStream_t>(stream)),
+             fn);
+    return FP8_OK;
+}
+
 fp8_status fp8_amax(const void *x, int64_t n, float *amax, void *stream) {
     const char *fn = "fp8_amax";
     FP8_TRY(check_dims16(fn, n, "n", 0, "-"));

@@ -861,6 +861,25 @@ cudaError_t launch_scale_update(float *history, float *amax, float *scale, float
 
 namespace fp8k {
 
+// Diagnostic: one warp waits, with the library's bounded wait, on an
+// mbarrier that nothing ever signals, gives up after limit_ns and reports it
+// through the error flag -- the path every kernel takes when a wait runs out.
+__global__ void selftest_wait_kernel(uint64_t limit_ns) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(&bar), 1);
+        fence_mbar_init();
+    }
+    __syncwarp();
+    if (threadIdx.x == 0 && !mbar_wait(smem_u32(&bar), 0, nullptr, limit_ns))
+        atomicOr(&g_cast_error_flags, kErrWaitTimeout);
+}
+
+cudaError_t launch_selftest_wait(uint64_t limit_ns, cudaStream_t st) {
+    selftest_wait_kernel<<<1, 32, 0, st>>>(limit_ns);
+    return cudaGetLastError();
+}
+
 cudaError_t read_and_clear_cast_error_flag(unsigned *flags) {
     cudaError_t e = cudaMemcpyFromSymbol(flags, g_cast_error_flags, sizeof(unsigned));
     if (e != cudaSuccess) return e;

@@ -17,6 +17,7 @@ bool encode_tmap_2d(CUtensorMap *map, const void *base, bool two_byte, int64_t i
 
 // amax of n BF16 values into *amax (zeroed first).
 cudaError_t launch_amax(const void *x, int64_t n, float *amax, int sm_count, cudaStream_t st);
+cudaError_t launch_selftest_wait(uint64_t limit_ns, cudaStream_t st);
 cudaError_t launch_quantize_f32(const float *x, int64_t n, const float *scale, int fmt,
                                 uint8_t *out, float *amax, int sm_count, cudaStream_t st);
 

@@ -127,6 +127,14 @@ const char *fp8_last_error(void);
  * FP8_ERR_CUDA if the stream reports an error, else FP8_OK. */
 fp8_status fp8_sync_status(void *stream);
 
+/* Diagnostic, not part of the method: launches one warp that waits with the
+ * library's bounded wait on a barrier nothing ever signals, so the wait runs
+ * out after limit_ns (1 .. 5e9) and the kernel records it in the device
+ * error flag and returns -- the path every kernel takes when a wait runs out.
+ * The next fp8_sync_status on the stream then returns FP8_ERR_TIMEOUT (and
+ * clears the flag); the context stays usable. */
+fp8_status fp8_selftest_wait_timeout(int64_t limit_ns, void *stream);
+
 /* amax of a BF16 tensor (the implementation guide's range monitoring; the
  * TensorRT page's Absolute-Max statistic).
  *   x     DEVICE, n BF16 values (n >= 0, multiple of 16; n == 0 gives 0)
