@@ -144,6 +144,7 @@ fp8_status fp8_sync_status(void *stream) {
 
 fp8_status fp8_selftest_wait_timeout(int64_t limit_ns, void *stream) {
     const char *fn = "fp8_selftest_wait_timeout";
+    const fp8k::CallRange range(fn);
     if (limit_ns < 1 || limit_ns > 5000000000ll)
         return fail(FP8_ERR_ARG, "%s: limit_ns %lld outside [1, 5e9]", fn,
                     static_cast<long long>(limit_ns));
@@ -155,6 +156,7 @@ fp8_status fp8_selftest_wait_timeout(int64_t limit_ns, void *stream) {
 
 fp8_status fp8_amax(const void *x, int64_t n, float *amax, void *stream) {
     const char *fn = "fp8_amax";
+    const fp8k::CallRange range(fn);
     FP8_TRY(check_dims16(fn, n, "n", 0, "-"));
     FP8_TRY(check_ptr(fn, x, "x", n == 0));
     FP8_TRY(check_scalar(fn, amax, "amax", false));
@@ -167,6 +169,7 @@ fp8_status fp8_amax(const void *x, int64_t n, float *amax, void *stream) {
 fp8_status fp8_quantize_f32(const float *x, int64_t n, const float *scale, int32_t fmt,
                             uint8_t *out, float *amax, void *stream) {
     const char *fn = "fp8_quantize_f32";
+    const fp8k::CallRange range(fn);
     FP8_TRY(check_dims16(fn, n, "n", 0, "-"));
     if (fmt != FP8_E4M3 && fmt != FP8_E5M2) return fail(FP8_ERR_ARG, "%s: bad format %d", fn, fmt);
     FP8_TRY(check_ptr(fn, x, "x", n == 0));
@@ -185,6 +188,7 @@ fp8_status fp8_quantize_transpose(const void *x, int64_t rows, int64_t cols, con
                                   int32_t fmt, uint8_t *out, uint8_t *out_t, float *amax,
                                   void *stream) {
     const char *fn = "fp8_quantize_transpose";
+    const fp8k::CallRange range(fn);
     FP8_TRY(check_dims16(fn, rows, "rows", cols, "cols"));
     if (fmt != FP8_E4M3 && fmt != FP8_E5M2) return fail(FP8_ERR_ARG, "%s: bad format %d", fn, fmt);
     const bool empty = rows == 0 || cols == 0;
@@ -208,6 +212,7 @@ fp8_status fp8_quantize_transpose_current(const void *x, int64_t rows, int64_t c
                                           float *amax, float *scale, float *scale_inv,
                                           void *stream) {
     const char *fn = "fp8_quantize_transpose_current";
+    const fp8k::CallRange range(fn);
     FP8_TRY(check_dims16(fn, rows, "rows", cols, "cols"));
     if (fmt != FP8_E4M3 && fmt != FP8_E5M2) return fail(FP8_ERR_ARG, "%s: bad format %d", fn, fmt);
     if (margin < 0 || margin > 64)
@@ -234,6 +239,7 @@ fp8_status fp8_scale_update(float *history, const float *amax, float *scale, flo
                             int32_t num_tensors, int32_t history_len, uint32_t format_mask,
                             int32_t margin, void *stream) {
     const char *fn = "fp8_scale_update";
+    const fp8k::CallRange range(fn);
     if (num_tensors < 1 || num_tensors > 32)
         return fail(FP8_ERR_ARG, "%s: num_tensors %d outside [1, 32]", fn, num_tensors);
     if (history_len < 1 || history_len > 8192)
@@ -255,6 +261,7 @@ fp8_status fp8_scale_update(float *history, const float *amax, float *scale, flo
 
 fp8_status fp8_amax_scale_update(const fp8_meta *meta, const fp8_recipe *recipe, void *stream) {
     const char *fn = "fp8_amax_scale_update";
+    const fp8k::CallRange range(fn);
     FP8_TRY(check_meta(fn, meta, recipe));
     const uint32_t mask = recipe->hybrid ? ((1u << FP8_SLOT_DY) | (1u << FP8_SLOT_DX)) : 0u;
     int sms;
@@ -283,6 +290,7 @@ fp8_status fp8_gemm_tn(const uint8_t *A, int32_t fa, const uint8_t *B, int32_t f
                        int64_t N, int64_t K, const float *a_scale_inv, const float *b_scale_inv,
                        void *D, float *d_amax, void *stream) {
     const char *fn = "fp8_gemm_tn";
+    const fp8k::CallRange range(fn);
     FP8_TRY(check_dims16(fn, M, "M", N, "N"));
     FP8_TRY(check_dims16(fn, K, "K", 16, "-"));
     if (M < 16 || N < 16 || K < 16) return fail(FP8_ERR_ARG, "%s: M, N, K must be >= 16", fn);
@@ -317,6 +325,7 @@ static fp8_status check_gemm(const char *fn, const fp8_gemm_desc &d) {
 
 fp8_status fp8_gemm_tn_grouped(const fp8_gemm_desc *descs, int32_t n, void *stream) {
     const char *fn = "fp8_gemm_tn_grouped";
+    const fp8k::CallRange range(fn);
     if (descs == nullptr || n < 1 || n > 2) return fail(FP8_ERR_ARG, "%s: n must be 1 or 2", fn);
     fp8k::GemmSpec g[2];
     for (int i = 0; i < n; ++i) {
@@ -337,6 +346,7 @@ fp8_status fp8_gemm_tn_grouped(const fp8_gemm_desc *descs, int32_t n, void *stre
 fp8_status fp8_quantize_transpose_grouped(const fp8_cast_desc *descs, int32_t n, int32_t fmt,
                                           void *stream) {
     const char *fn = "fp8_quantize_transpose_grouped";
+    const fp8k::CallRange range(fn);
     if (descs == nullptr || n < 1 || n > 2) return fail(FP8_ERR_ARG, "%s: n must be 1 or 2", fn);
     if (fmt != FP8_E4M3 && fmt != FP8_E5M2) return fail(FP8_ERR_ARG, "%s: bad format %d", fn, fmt);
     fp8k::CastSpec c[2];
@@ -364,6 +374,7 @@ fp8_status fp8_quantize_transpose_grouped(const fp8_cast_desc *descs, int32_t n,
 fp8_status fp8_dequant_sum(const uint8_t *parts, int32_t nranks, int64_t n, int32_t fmt,
                            const float *scale, void *out, void *stream) {
     const char *fn = "fp8_dequant_sum";
+    const fp8k::CallRange range(fn);
     FP8_TRY(check_dims16(fn, n, "n", 0, "-"));
     if (nranks < 1 || nranks > 65536) return fail(FP8_ERR_ARG, "%s: nranks %d", fn, nranks);
     if (fmt != FP8_E4M3 && fmt != FP8_E5M2) return fail(FP8_ERR_ARG, "%s: bad format %d", fn, fmt);
@@ -383,6 +394,7 @@ fp8_status fp8_adam_step(const void *grad, int64_t n, uint8_t *m1, float *m1_sca
                          float *w_scale_inv, void *w_bf16, float *amax, const fp8_adam_hyper *hp,
                          void *stream) {
     const char *fn = "fp8_adam_step";
+    const fp8k::CallRange range(fn);
     FP8_TRY(check_dims16(fn, n, "n", 0, "-"));
     if (hp == nullptr) return fail(FP8_ERR_ARG, "%s: hyper-parameters are NULL", fn);
     if (hp->margin < 0 || hp->margin > 64)
@@ -415,6 +427,7 @@ fp8_status fp8_layernorm_quantize_transpose(const void *x, const void *gamma, co
                                             uint8_t *out_t, float *amax, float *mean, float *rstd,
                                             void *stream) {
     const char *fn = "fp8_layernorm_quantize_transpose";
+    const fp8k::CallRange range(fn);
     FP8_TRY(check_dims16(fn, rows, "rows", cols, "cols"));
     if (cols < 16) return fail(FP8_ERR_ARG, "%s: cols must be >= 16", fn);
     if (fmt != FP8_E4M3 && fmt != FP8_E5M2) return fail(FP8_ERR_ARG, "%s: bad format %d", fn, fmt);
@@ -454,6 +467,7 @@ fp8_status fp8_layernorm_linear_fwd(const void *X, const void *gamma, const void
                                     uint8_t *X8t, uint8_t *W8, uint8_t *W8t, void *Y, float *mean,
                                     float *rstd, void *stream) {
     const char *fn = "fp8_layernorm_linear_fwd";
+    const fp8k::CallRange range(fn);
     FP8_TRY(check_ptr(fn, gamma, "gamma", false));
     FP8_TRY(check_ptr(fn, beta, "beta", false));
     FP8_TRY(check_scalar(fn, mean, "mean", false));
@@ -512,6 +526,7 @@ fp8_status fp8_linear_bwd(const void *dY, int64_t M, int64_t N, int64_t K, const
                           const fp8_recipe *recipe, const uint8_t *X8t, const uint8_t *W8t,
                           uint8_t *dY8, uint8_t *dY8t, void *dX, void *dW, void *stream) {
     const char *fn = "fp8_linear_bwd";
+    const fp8k::CallRange range(fn);
     FP8_TRY(check_meta(fn, meta, recipe));
     FP8_TRY(check_dims16(fn, M, "M", N, "N"));
     FP8_TRY(check_dims16(fn, K, "K", 16, "-"));

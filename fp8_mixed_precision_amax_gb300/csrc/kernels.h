@@ -7,7 +7,19 @@
 
 #include <cstdint>
 
+#include <nvtx3/nvToolsExt.h>
+
 namespace fp8k {
+
+// An NVTX range around each C-ABI call (a pointer check when no profiler is
+// attached), so a profile can attribute kernels to the calls that launched
+// them.
+struct CallRange {
+    explicit CallRange(const char *name) { nvtxRangePushA(name); }
+    ~CallRange() { nvtxRangePop(); }
+    CallRange(const CallRange &) = delete;
+    CallRange &operator=(const CallRange &) = delete;
+};
 
 // Tiled 2-D TMA descriptor of a row-major [outer][inner] tensor of 1- or
 // 2-byte elements with a box of box_outer x box_inner elements, optionally

@@ -47,6 +47,7 @@ fp8_status fp8_linear_bwd_noalloc(const void *dY, int64_t M, int64_t N, int64_t 
                                   const fp8_meta *meta, const fp8_recipe *recipe,
                                   const uint8_t *X8t, const uint8_t *W8t, void *dX, void *dW,
                                   void *stream) {
+    const fp8k::CallRange range("fp8_linear_bwd_noalloc");
     char msg[256];
     if (M < 0 || N < 0 || (M != 0 && N > kMaxElems / M)) {
         snprintf(msg, sizeof msg,
