@@ -346,16 +346,6 @@ __device__ __forceinline__ uint32_t cvt2_fp8(float lo, float hi) {
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
-// Magnitude bits of the two BF16 values in w, with NaN mapped to 0, maxed
-// into m.  For non-NaN BF16 values the magnitude bit pattern orders like the
-// magnitude itself, so an integer max is an exact amax.
-__device__ __forceinline__ uint32_t amax_bits2(uint32_t m, uint32_t w) {
-    uint32_t lo = w & 0x7FFFu, hi = (w >> 16) & 0x7FFFu;
-    lo = lo > 0x7F80u ? 0u : lo;
-    hi = hi > 0x7F80u ? 0u : hi;
-    return max(m, max(lo, hi));
-}
-
 // Packed fp32 pairs (lo in the low word of a 64-bit register) and IEEE
 // round-to-nearest arithmetic on both lanes at once: each lane is rounded
 // exactly as the scalar operation would be.  One caution: ptxas contracts a
@@ -377,11 +367,6 @@ __device__ __forceinline__ uint64_t f32x2_from_bf16x2(uint32_t w) {
     uint64_t v;
     asm("mov.b64 %0, {%1, %2};" : "=l"(v) : "r"(w << 16), "r"(w & 0xFFFF0000u));
     return v;
-}
-__device__ __forceinline__ uint64_t f32x2_add(uint64_t a, uint64_t b) {
-    uint64_t r;
-    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-    return r;
 }
 __device__ __forceinline__ uint64_t f32x2_sub(uint64_t a, uint64_t b) {
     uint64_t r;
@@ -407,7 +392,7 @@ __device__ __forceinline__ uint32_t scale_bf16x2(uint32_t lo, uint32_t hi, uint6
 
 // Running max of |x| over packed BF16 pairs: m2 holds two non-negative BF16
 // maxima.  max.bf16x2 returns the other operand when one is NaN, so NaN
-// entries are skipped and infinities kept, as in amax_bits2.
+// entries are skipped and infinities kept.
 __device__ __forceinline__ uint32_t absmax_bf16x2(uint32_t m2, uint32_t w) {
     uint32_t a;
     asm("abs.bf16x2 %0, %1;" : "=r"(a) : "r"(w));
