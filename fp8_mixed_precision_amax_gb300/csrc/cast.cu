@@ -50,7 +50,7 @@ __global__ void __launch_bounds__(512) amax_kernel(const uint4 *__restrict__ x, 
         m2 = absmax_bf16x2(m2, v.z);
         m2 = absmax_bf16x2(m2, v.w);
     }
-    uint32_t m = max(m2 & 0xFFFFu, m2 >> 16);
+    uint32_t m = absmax_bf16x2_finish(m2);
     m = __reduce_max_sync(0xFFFFFFFFu, m);
     __shared__ uint32_t warp_max[32];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -301,7 +301,7 @@ __global__ void __launch_bounds__(kQtThreads, 2)
                     *reinterpret_cast<uint2 *>(T.out + r * cols + c) = q;
                 *reinterpret_cast<uint2 *>(&tile[rr * 32 + ((vv * 2) ^ qt_swz(rr))]) = q;
             }
-            m = max(m2 & 0xFFFFu, m2 >> 16) << 16;   // BF16 magnitude bits -> fp32 bits
+            m = absmax_bf16x2_finish(m2) << 16;   // BF16 magnitude bits -> fp32 bits
         } else {
             // LayerNorm first: y = ((x - mean) * rstd) * gamma + beta in fp32,
             // one rounding per operation in that order: the subtract and the

@@ -390,14 +390,20 @@ __device__ __forceinline__ uint32_t scale_bf16x2(uint32_t lo, uint32_t hi, uint6
     return h;
 }
 
-// Running max of |x| over packed BF16 pairs: m2 holds two non-negative BF16
-// maxima.  max.bf16x2 returns the other operand when one is NaN, so NaN
-// entries are skipped and infinities kept.
+// Running max of |x| over packed BF16 pairs in one instruction per pair:
+// each lane of m2 holds the largest magnitude so far (its sign bit is the
+// xor of signs and carries no meaning).  max.xorsign.abs.bf16x2 returns the
+// other operand when one is NaN (checked on the GPU against abs + max over
+// all 2^32 lane pairs), so NaN entries are skipped and infinities kept; m2
+// starts at 0 and is never NaN.
 __device__ __forceinline__ uint32_t absmax_bf16x2(uint32_t m2, uint32_t w) {
-    uint32_t a;
-    asm("abs.bf16x2 %0, %1;" : "=r"(a) : "r"(w));
-    asm("max.bf16x2 %0, %0, %1;" : "+r"(m2) : "r"(a));
+    asm("max.xorsign.abs.bf16x2 %0, %0, %1;" : "+r"(m2) : "r"(w));
     return m2;
+}
+
+// The larger magnitude of m2's two lanes, as BF16 magnitude bits.
+__device__ __forceinline__ uint32_t absmax_bf16x2_finish(uint32_t m2) {
+    return max(m2 & 0x7FFFu, (m2 >> 16) & 0x7FFFu);
 }
 
 // The two BF16 values of w (lo in the low half) widened to fp32, times

@@ -385,7 +385,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_tn_kernel(const __grid_co
                 }
                 ++epi_chunk;
             }
-            const uint32_t m = max(m2 & 0xFFFFu, m2 >> 16);   // BF16 magnitude bits
+            const uint32_t m = absmax_bf16x2_finish(m2);   // BF16 magnitude bits
             if (pi)
                 tmax[1] = max(tmax[1], m);
             else
