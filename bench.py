@@ -616,6 +616,57 @@ def run_secondary(f, args, pk):
         "note": "decode + rank-order sum of 8 ranks' E5M2 codes -> BF16; L2 flushed before each"}
     del parts, dsum
     out["context_cublaslt_fp8_mlp7b"] = cublaslt_context(f, w7, flush)
+    del flush
+    out["drift_range_counts"] = drift_range_report(f)
+    return out
+
+
+def range_counts(x: torch.Tensor, codes: torch.Tensor, s: torch.Tensor, fmax: float):
+    """How a cast under scale ``s`` treated one tensor: ``saturated`` = elements
+    with |fl32(x * s)| above the format's largest finite value (clipped to it),
+    ``underflow`` = non-zero elements whose FP8 code is +-0.  ``x`` BF16,
+    ``codes`` the cast's FP8 bytes, ``s`` a one-element fp32 tensor; any device.
+    A diagnostic of the recipe, not part of the layer."""
+    v = x.float() * s
+    sat = int((v.abs() > fmax).sum())
+    under = int(((x != 0) & ((codes & 0x7F) == 0)).sum())
+    return sat, under
+
+
+def drift_range_report(f, steps: int = 130):
+    """Per-step saturation / underflow counts of the drifting-scale workload
+    (M = K = N = 4096, history 512, margin 0) under delayed scaling, in the
+    HYBRID and the E4M3-everywhere arms.  X and dY are drawn on the device
+    with the workload's recipe (a CUDA generator, so the bytes differ from the
+    host-drawn ones the parity tests use).  The x1000 spike at step 50 is cast
+    with the scale of the steps before it, so it saturates; at step 51 the
+    history holds the spike and the ordinary X loses its small values."""
+    w = wl.WORKLOADS["drift"]
+    n_el = w.M * w.K
+    out = {}
+    for hybrid in (True, False):
+        lin = f.Fp8Linear(wl.layer_weight(w, "cuda"), w.M,
+                          f.Recipe(margin=w.margin, history_len=w.history_len, hybrid=hybrid))
+        fmax_dy = 57344.0 if hybrid else 448.0
+        per = []
+        for t in range(steps):
+            X, dY = wl.layer_x(w, t, "cuda"), wl.layer_dy(w, t, "cuda")
+            sx, sdy = lin.meta.scale[0:1].clone(), lin.meta.scale[3:4].clone()
+            lin.step(X, dY)
+            xs, xu = range_counts(X, lin.X8, sx, 448.0)
+            ds, du = range_counts(dY, lin.dY8, sdy, fmax_dy)
+            per.append((t, xs, xu, ds, du, float(sx.item())))
+        torch.cuda.synchronize()
+        notable = {str(t): {"scale_X": sc, "X_saturated": xs, "X_underflow": xu,
+                            "dY_saturated": ds, "dY_underflow": du}
+                   for t, xs, xu, ds, du, sc in per if t in (0, 1, 49, 50, 51, 75, 76, 100)}
+        out["hybrid" if hybrid else "e4m3_everywhere"] = {
+            "steps": steps, "elements_per_tensor": n_el, "at_step": notable,
+            "X_saturated_total": sum(p[1] for p in per),
+            "X_underflow_total": sum(p[2] for p in per),
+            "dY_saturated_total": sum(p[3] for p in per),
+            "dY_underflow_total": sum(p[4] for p in per)}
+        del lin
     return out
 
 

@@ -45,3 +45,55 @@ def test_traffic_figure_follows_the_kernel_source(tmp_path, monkeypatch):
                                                      "gemm.cu"), "rb").read())
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
     assert bench.gemm_traffic("mlp7b") is None
+
+
+def test_range_counts_on_known_values():
+    """The drift report's saturation / underflow counts, on values whose fate
+    under E4M3 at scale 1 is fixed by the format (largest finite 448, smallest
+    subnormal 2^-9, ties to even): 450, 512, -9984 and inf are clipped; 1e-5,
+    -1e-6 and 2^-10 (exactly half the smallest subnormal, a tie that goes to
+    the even code 0) become zero; 448, 2^-9, zeros and NaN are neither.  The
+    oracle's cast of the same values must agree with that classification."""
+    import numpy as np
+    import torch
+    sys.path.insert(0, ROOT)
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    import bench
+    import oracle as o
+    vals = [0.0, -0.0, 448.0, 450.0, 512.0, -9984.0, 1e-5, -1e-6, 2.0 ** -10, 2.0 ** -9,
+            float("inf"), float("nan"), 1.0, -3.0]
+    x = torch.tensor(vals, dtype=torch.float32).to(torch.bfloat16)
+    bits = x.view(torch.int16).numpy().view(np.uint16)
+    codes, _ = o.quantize(bits[None, :], np.float32(1.0), o.E4M3)
+    codes = codes.reshape(-1)
+    sat, under = bench.range_counts(x, torch.from_numpy(codes.copy()), torch.ones(1), 448.0)
+    assert (sat, under) == (4, 3)
+    assert [int(c) & 0x7F for c in codes[[3, 4, 5, 10]]] == [0x7E] * 4
+    assert [int(c) & 0x7F for c in codes[[6, 7, 8]]] == [0] * 3
+    assert int(codes[9]) == 0x01 and int(codes[2]) == 0x7E
+
+
+def test_range_counts_agree_with_the_oracle_cast():
+    """On a seeded tensor with a scale that clips its tail and flushes its
+    smallest values: every element counted as saturated is cast by the oracle
+    to the largest-magnitude code, and the underflow count is the number of
+    non-zero inputs the oracle casts to +-0."""
+    import numpy as np
+    import torch
+    sys.path.insert(0, ROOT)
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    import bench
+    import oracle as o
+    g = torch.Generator().manual_seed(11)
+    x = (torch.randn(64, 256, generator=g) * torch.logspace(-10, 1, 256)).to(torch.bfloat16)
+    for fmt, fmax, s in ((o.E4M3, 448.0, 300.0), (o.E5M2, 57344.0, 1.0e4)):
+        bits = x.view(torch.int16).numpy().view(np.uint16)
+        codes, _ = o.quantize(bits, np.float32(s), fmt)
+        sat, under = bench.range_counts(x, torch.from_numpy(codes.copy()),
+                                        torch.tensor([s], dtype=torch.float32), fmax)
+        top = 0x7E if fmt == o.E4M3 else 0x7B
+        xd = o.bf16_to_f32(bits).astype(np.float64)
+        exact = np.abs(xd * np.float64(np.float32(s)))
+        assert sat > 0 and under > 0
+        assert np.all((codes[exact > fmax] & 0x7F) == top)
+        assert under == int(np.count_nonzero((xd != 0) & (o.fp8_decode_table(fmt)[codes] == 0)))
