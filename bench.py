@@ -57,7 +57,10 @@ def parse_args():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--secondary", action="store_true",
-                   help="also time the 70B-shaped layer and the cast sweep (extra keys)")
+                   help="also time the 70B-shaped layer, the cast sweep and the other "
+                        "kernels of the path (extra keys)")
+    p.add_argument("--part", action="append", default=[], choices=SECONDARY_PARTS,
+                   help="with --secondary: run only these parts (repeatable)")
     return p.parse_args()
 
 
@@ -503,17 +506,53 @@ def workload_config(w: wl.Workload):
                   % ((2 * w.M * w.K + 2 * w.N * w.K + 2 * w.M * w.N) // 2 ** 20)}
 
 
+SECONDARY_PARTS = ("mlp70b", "cast_sweep", "layernorm_cast", "fp8_adam", "jit_scaling",
+                   "fp8_allreduce", "cublaslt", "drift")
+
+
 def run_secondary(f, args, pk):
-    """The 70B-shaped layer (device time only) and the cast sweep GB/s."""
+    """The extra measurements: the 70B-shaped layer, the cast/amax sweep, the
+    LayerNorm + cast and FP8 Adam kernels, the just-in-time scaling step, the
+    FP8 all-reduce sum, the cuBLASLt context and the drift range counts.
+    ``args.part`` names the ones to run (all when empty)."""
+    want = lambda name: not args.part or name in args.part
     out = {}
+    w7 = wl.WORKLOADS["mlp7b"]
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    if want("mlp70b"):
+        out["mlp70b"] = secondary_mlp70b(f, args, pk)
+    if want("cast_sweep"):
+        out["cast_sweep"] = secondary_cast_sweep(f)
+    if want("layernorm_cast"):
+        out["layernorm_cast_mlp7b_X"] = secondary_layernorm_cast(f, w7, flush)
+    if want("fp8_adam"):
+        out["fp8_adam_step_mlp7b_W"] = secondary_adam(f, w7, flush)
+    if want("jit_scaling"):
+        out["jit_scaling_layer_step_mlp7b"] = secondary_jit_scaling(f, w7)
+    if want("fp8_allreduce"):
+        out["fp8_allreduce_sum_8ranks_mlp7b_dW"] = secondary_dequant_sum(f, w7, flush)
+    if want("cublaslt"):
+        out["context_cublaslt_fp8_mlp7b"] = cublaslt_context(f, w7, flush)
+    del flush
+    if want("drift"):
+        out["drift_range_counts"] = drift_range_report(f)
+    return out
+
+
+def secondary_mlp70b(f, args, pk):
+    """The 70B-shaped layer step (device time only)."""
     w = wl.WORKLOADS["mlp70b"]
     sub = argparse.Namespace(**{**vars(args), "steps": max(10, min(args.steps, 30)),
                                 "warmup": 3, "no_e2e": True})
     r = run_layer_bench(f, w, sub, 1, pk, "measured")
-    out["mlp70b"] = {"value": r["value"], "unit": "TFLOPS", "ms_per_step": r["ms_per_step"],
-                     "gemm_frac": r["roofline"]["frac"],
-                     "gemm_tflops": r["roofline"]["achieved"],
-                     "cast_gbs": r["cast_roofline"]["achieved"]}
+    return {"value": r["value"], "unit": "TFLOPS", "ms_per_step": r["ms_per_step"],
+            "gemm_frac": r["roofline"]["frac"], "gemm_tflops": r["roofline"]["achieved"],
+            "cast_gbs": r["cast_roofline"]["achieved"]}
+
+
+def secondary_cast_sweep(f):
+    """Standalone amax and cast+transpose GB/s on the 2^24 / 2^26 / 2^28 sweep
+    tensors (23 launches of each per size, the first 3 untimed)."""
     sweep = {}
     for n in (24, 26, 28):
         x = wl.sweep_tensor(n, device="cuda")
@@ -532,10 +571,12 @@ def run_secondary(f, args, pk):
         sweep[f"2^{n}"] = {"amax_gbs": 2 * ne / (tm.mean_ms("amax") / 1e3) / 1e9,
                            "cast_transpose_gbs": 4 * ne / (tm.mean_ms("cast") / 1e3) / 1e9}
         del x, o8, o8t
-    out["cast_sweep"] = sweep
-    # LayerNorm + cast of the 7B layer's X (statistics kernel + fused cast),
-    # against the plain cast of the same tensor; 4 B/element algorithmic
-    w7 = wl.WORKLOADS["mlp7b"]
+    return sweep
+
+
+def secondary_layernorm_cast(f, w7, flush):
+    """LayerNorm + cast of the 7B layer's X (statistics kernel + fused cast),
+    against the plain cast of the same tensor; 4 B/element algorithmic."""
     X = wl.layer_x(w7, 0, "cuda")
     g = torch.ones(w7.K, dtype=torch.bfloat16, device="cuda")
     b = torch.zeros(w7.K, dtype=torch.bfloat16, device="cuda")
@@ -545,7 +586,6 @@ def run_secondary(f, args, pk):
     rstd = torch.empty(w7.M, device="cuda")
     sc = torch.ones(1, device="cuda")
     tm = EventTimer()
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
     for i in range(23):
         flush.zero_()
         tm.time("ln_cast", lambda: f.fp8_layernorm_quantize_transpose(X, g, b, 1e-5, sc, 0, mean,
@@ -555,7 +595,14 @@ def run_secondary(f, args, pk):
     torch.cuda.synchronize()
     tm.pairs = {k: v[3:] for k, v in tm.pairs.items()}
     ne = w7.M * w7.K
-    # one decoupled-precision Adam step over the 7B layer's weight (45 M params)
+    return {"ln_cast_us": tm.mean_ms("ln_cast") * 1e3, "cast_us": tm.mean_ms("cast") * 1e3,
+            "ln_cast_gbs": 4 * ne / (tm.mean_ms("ln_cast") / 1e3) / 1e9,
+            "note": "4 B/element algorithmic; L2 flushed before each launch"}
+
+
+def secondary_adam(f, w7, flush):
+    """One decoupled-precision Adam step over the 7B layer's weight (45 M params)."""
+    tm = EventTimer()
     st = f.Fp8AdamState(wl.layer_weight(w7, "cuda"))
     grad = wl.layer_weight(w7, "cuda")
     wout = torch.empty_like(grad)
@@ -566,18 +613,17 @@ def run_secondary(f, args, pk):
     torch.cuda.synchronize()
     tm.pairs["adam"] = tm.pairs["adam"][3:]
     nw = w7.N * w7.K
-    out["fp8_adam_step_mlp7b_W"] = {
+    return {
         "us": tm.mean_ms("adam") * 1e3,
         "gbs_algorithmic": 14 * nw / (tm.mean_ms("adam") / 1e3) / 1e9,
         "note": "14 B/param algorithmic (grad 2 + m1 1 + m2 2 + w16 2 read, the same written "
                 "plus 2 B BF16 weights minus the grad); the kernel reads the inputs twice "
                 "(amax pass, then the update pass) for just-in-time state scales"}
-    out["layernorm_cast_mlp7b_X"] = {
-        "ln_cast_us": tm.mean_ms("ln_cast") * 1e3, "cast_us": tm.mean_ms("cast") * 1e3,
-        "ln_cast_gbs": 4 * ne / (tm.mean_ms("ln_cast") / 1e3) / 1e9,
-        "note": "4 B/element algorithmic; L2 flushed before each launch"}
-    # just-in-time (current) scaling: the same 7B layer step with X, W and dY
-    # scaled from their own amax (an amax pass before each cast)
+
+
+def secondary_jit_scaling(f, w7):
+    """Just-in-time (current) scaling: the 7B layer step with X, W and dY
+    scaled from their own amax (an amax pass before each cast)."""
     lj = f.Fp8Linear(wl.layer_weight(w7, "cuda"), w7.M,
                      f.Recipe(margin=w7.margin, history_len=w7.history_len, hybrid=w7.hybrid,
                               current=True))
@@ -594,13 +640,15 @@ def run_secondary(f, args, pk):
     s1.record()
     torch.cuda.synchronize()
     msj = s0.elapsed_time(s1) / nj
-    out["jit_scaling_layer_step_mlp7b"] = {
-        "ms_per_step": msj, "value": 6 * w7.M * w7.N * w7.K / (msj / 1e3) / 1e12,
-        "unit": "TFLOPS", "note": "X, W and dY scaled just in time from their own amax"}
-    del lj, xs7, dys7
-    # the device part of the FP8 gradient all-reduce: decode and sum 8 ranks'
-    # FP8 codes of the 7B dW (shared scale) into BF16; 8 B read + 2 B written
-    # per element for 8 ranks
+    return {"ms_per_step": msj, "value": 6 * w7.M * w7.N * w7.K / (msj / 1e3) / 1e12,
+            "unit": "TFLOPS", "note": "X, W and dY scaled just in time from their own amax"}
+
+
+def secondary_dequant_sum(f, w7, flush):
+    """The device part of the FP8 gradient all-reduce: decode and sum 8 ranks'
+    FP8 codes of the 7B dW (shared scale) into BF16; 8 B read + 2 B written
+    per element for 8 ranks."""
+    tm = EventTimer()
     nr, nd = 8, w7.N * w7.K
     parts = torch.randint(0, 0x7B, (nr, nd), dtype=torch.uint8, device="cuda")
     dsum = torch.empty(nd, dtype=torch.bfloat16, device="cuda")
@@ -610,15 +658,11 @@ def run_secondary(f, args, pk):
         tm.time("dequant_sum", lambda: f.fp8_dequant_sum(parts, f.E5M2, sc1, dsum))
     torch.cuda.synchronize()
     tm.pairs["dequant_sum"] = tm.pairs["dequant_sum"][3:]
-    out["fp8_allreduce_sum_8ranks_mlp7b_dW"] = {
-        "us": tm.mean_ms("dequant_sum") * 1e3,
-        "gbs_algorithmic": (nr + 2) * nd / (tm.mean_ms("dequant_sum") / 1e3) / 1e9,
-        "note": "decode + rank-order sum of 8 ranks' E5M2 codes -> BF16; L2 flushed before each"}
+    res = {"us": tm.mean_ms("dequant_sum") * 1e3,
+           "gbs_algorithmic": (nr + 2) * nd / (tm.mean_ms("dequant_sum") / 1e3) / 1e9,
+           "note": "decode + rank-order sum of 8 ranks' E5M2 codes -> BF16; L2 flushed before each"}
     del parts, dsum
-    out["context_cublaslt_fp8_mlp7b"] = cublaslt_context(f, w7, flush)
-    del flush
-    out["drift_range_counts"] = drift_range_report(f)
-    return out
+    return res
 
 
 def range_counts(x: torch.Tensor, codes: torch.Tensor, s: torch.Tensor, fmax: float):
