@@ -144,26 +144,42 @@ class ClockSampler:
             self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
+        with open(self.path) as fh:
+            lines = fh.readlines()
+        os.unlink(self.path)
+        return self.summarize(lines)
+
+    @staticmethod
+    def summarize(lines):
+        """Median SM clock under load, the range seen, the peak power draw and
+        the throttle reasons that were active in any sample, from nvidia-smi
+        CSV lines in FIELDS order."""
         rows = []
-        for line in open(self.path):
+        for line in lines:
             parts = [s.strip() for s in line.split(",")]
             if len(parts) < 8:
                 continue
             try:
-                rows.append((float(parts[0]), float(parts[1]), parts[3:]))
+                sm, smax = float(parts[0]), float(parts[1])
             except ValueError:
                 continue
-        os.unlink(self.path)
+            try:
+                pw = float(parts[2])
+            except ValueError:
+                pw = None
+            rows.append((sm, smax, pw, parts[3:]))
         if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = set()
-        for _, _, r in rows:
+        for *_, r in rows:
             for nm, v in zip(names, r[1:5]):
                 if v.lower() == "active":
                     reasons.add(nm)
-        loaded = [s for s, _, _ in rows if s > 0.5 * rows[0][1]] or [s for s, _, _ in rows]
-        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(m for _, m, _ in rows),
+        loaded = [r[0] for r in rows if r[0] > 0.5 * rows[0][1]] or [r[0] for r in rows]
+        powers = [r[2] for r in rows if r[2] is not None]
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(r[1] for r in rows),
+                "sm_min_mhz": min(loaded), "power_w_max": max(powers) if powers else None,
                 "reasons": sorted(reasons), "samples": len(rows)}
 
 

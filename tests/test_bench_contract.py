@@ -97,3 +97,22 @@ def test_range_counts_agree_with_the_oracle_cast():
         assert sat > 0 and under > 0
         assert np.all((codes[exact > fmax] & 0x7F) == top)
         assert under == int(np.count_nonzero((xd != 0) & (o.fp8_decode_table(fmt)[codes] == 0)))
+
+
+def test_clock_summary_from_nvidia_smi_lines():
+    """The clocks object: median SM clock over samples under load (above half
+    the maximum), the lowest of those, the peak power and every throttle
+    reason seen Active in any sample; unparsable lines are skipped."""
+    sys.path.insert(0, ROOT)
+    import bench
+    lines = ["2070, 2070, 900.5, 0x0, Not Active, Not Active, Not Active, Not Active\n",
+             "1605, 2070, 1391.0, 0x4, Not Active, Not Active, Not Active, Active\n",
+             "1800, 2070, [N/A], 0x4, Not Active, Not Active, Not Active, Active\n",
+             "345, 2070, 120.0, 0x0, Not Active, Not Active, Not Active, Not Active\n",
+             "garbage\n", "N/A, N/A, N/A, N/A, N/A, N/A, N/A, N/A\n"]
+    c = bench.ClockSampler.summarize(lines)
+    assert c["samples"] == 4 and c["sm_max_mhz"] == 2070.0
+    assert c["sm_mhz"] == 1800.0 and c["sm_min_mhz"] == 1605.0
+    assert c["power_w_max"] == 1391.0
+    assert c["reasons"] == ["sw_power_cap"]
+    assert bench.ClockSampler.summarize([])["reasons"] == ["no samples"]
