@@ -82,6 +82,74 @@ def test_host_side_argument_checks():
     assert s == ERR_ARG
 
 
+
+def test_host_side_checks_of_the_grouped_layernorm_optimizer_and_reduction_calls():
+    """Every argument error below is detected on the host, before any CUDA
+    call, with the documented status and a message naming the call."""
+    lib = f.library()
+    p16 = ctypes.c_void_p(0x1000)
+    odd = ctypes.c_void_p(0x1008)
+    # bounded-wait self-test: the limit must lie in [1 ns, 5 s]
+    for lim in (0, -5, 5_000_000_001):
+        s, msg = _err(lib.fp8_selftest_wait_timeout(lim, None))
+        assert s == ERR_ARG and "limit_ns" in msg
+    # fp32 cast
+    assert _err(lib.fp8_quantize_f32(p16, 24, p16, 0, p16, None, None))[0] == ERR_ALIGN
+    assert _err(lib.fp8_quantize_f32(p16, 16, p16, 2, p16, None, None))[0] == ERR_ARG
+    assert _err(lib.fp8_quantize_f32(odd, 16, p16, 0, p16, None, None))[0] == ERR_ALIGN
+    assert _err(lib.fp8_quantize_f32(p16, 16, None, 0, p16, None, None))[0] == ERR_ARG
+    # grouped GEMM: one or two problems, each checked like fp8_gemm_tn
+    good = api.fp8_gemm_desc(0x1000, 0, 0x1000, 0, 16, 16, 16, 0x1000, 0x1000, 0x1000, None)
+    for n in (0, 3):
+        s, msg = _err(lib.fp8_gemm_tn_grouped((api.fp8_gemm_desc * 3)(good, good, good), n, None))
+        assert s == ERR_ARG and "1 or 2" in msg
+    assert _err(lib.fp8_gemm_tn_grouped(None, 1, None))[0] == ERR_ARG
+    bad_k = api.fp8_gemm_desc(0x1000, 0, 0x1000, 0, 16, 16, 8, 0x1000, 0x1000, 0x1000, None)
+    assert _err(lib.fp8_gemm_tn_grouped((api.fp8_gemm_desc * 2)(good, bad_k), 2, None))[0] \
+        == ERR_ALIGN
+    bad_f = api.fp8_gemm_desc(0x1000, 5, 0x1000, 0, 16, 16, 16, 0x1000, 0x1000, 0x1000, None)
+    assert _err(lib.fp8_gemm_tn_grouped((api.fp8_gemm_desc * 1)(bad_f), 1, None))[0] == ERR_ARG
+    # grouped cast
+    cd = api.fp8_cast_desc(0x1000, 16, 16, 0x1000, 0x1000, None, None)
+    assert _err(lib.fp8_quantize_transpose_grouped((api.fp8_cast_desc * 1)(cd), 0, 0,
+                                                   None))[0] == ERR_ARG
+    assert _err(lib.fp8_quantize_transpose_grouped((api.fp8_cast_desc * 1)(cd), 1, 9,
+                                                   None))[0] == ERR_ARG
+    no_out = api.fp8_cast_desc(0x1000, 16, 16, 0x1000, None, None, None)
+    s, msg = _err(lib.fp8_quantize_transpose_grouped((api.fp8_cast_desc * 2)(cd, no_out), 2, 0,
+                                                     None))
+    assert s == ERR_ARG and "both NULL" in msg
+    # decode-and-sum of the FP8 all-reduce
+    assert _err(lib.fp8_dequant_sum(p16, 0, 16, 1, p16, p16, None))[0] == ERR_ARG
+    assert _err(lib.fp8_dequant_sum(p16, 65537, 16, 1, p16, p16, None))[0] == ERR_ARG
+    assert _err(lib.fp8_dequant_sum(p16, 2, 16, 3, p16, p16, None))[0] == ERR_ARG
+    assert _err(lib.fp8_dequant_sum(p16, 2, 8, 1, p16, p16, None))[0] == ERR_ALIGN
+    # Adam on FP8 / FP16 states
+    args = [p16, 16, p16, p16, p16, p16, p16, p16, p16, p16, p16]
+    assert _err(lib.fp8_adam_step(*args, None, None))[0] == ERR_ARG
+    for hp in (api.fp8_adam_hyper(1e-3, 0.9, 0.999, 1e-8, 0.0, 0.1, 0.001, 65),
+               api.fp8_adam_hyper(1e-3, 0.9, 0.999, 1e-8, 0.0, 0.1, 0.001, -1),
+               api.fp8_adam_hyper(1e-3, 0.9, 0.999, 1e-8, 0.0, 0.0, 0.001, 0),
+               api.fp8_adam_hyper(1e-3, 0.9, 0.999, 1e-8, 0.0, 0.1, float("nan"), 0)):
+        assert _err(lib.fp8_adam_step(*args, ctypes.byref(hp), None))[0] == ERR_ARG
+    ok_hp = api.fp8_adam_hyper(1e-3, 0.9, 0.999, 1e-8, 0.0, 0.1, 0.001, 0)
+    assert _err(lib.fp8_adam_step(p16, 8, *args[2:], ctypes.byref(ok_hp), None))[0] == ERR_ALIGN
+    # LayerNorm + cast
+    ln = lambda rows, cols, eps, out, out_t: lib.fp8_layernorm_quantize_transpose(
+        p16, p16, p16, rows, cols, eps, p16, 0, out, out_t, None, p16, p16, None)
+    s, msg = _err(ln(16, 0, 1e-5, p16, p16))
+    assert s == ERR_ARG and "cols" in msg
+    assert _err(ln(16, 16, -1.0, p16, p16))[0] == ERR_ARG
+    assert _err(ln(16, 16, float("nan"), p16, p16))[0] == ERR_ARG
+    assert _err(ln(16, 16, 1e-5, None, None))[0] == ERR_ARG
+    assert _err(ln(16, 24, 1e-5, p16, p16))[0] == ERR_ALIGN
+    # the allocation-free backward takes at most 2^25 dY elements
+    meta = api.fp8_meta(0x1000, 0x1000, 0x1000, 0x1000, 16)
+    rec = api.fp8_recipe(0, 16, 1, 0)
+    s, msg = _err(lib.fp8_linear_bwd_noalloc(p16, 8192, 8192, 16, ctypes.byref(meta),
+                                             ctypes.byref(rec), p16, p16, p16, p16, None))
+    assert s == ERR_ARG and "fixed work area" in msg
+
 def test_python_binding_rejects_cpu_tensors():
     import torch
     x = torch.zeros(16, 16, dtype=torch.bfloat16)
