@@ -35,8 +35,9 @@
  *  - Pointers named as DEVICE pointers must be device (or managed) memory of
  *    the current device; the caller allocates and owns every buffer.  The
  *    library allocates no device memory, never synchronizes the stream (except
- *    fp8_sync_status), and keeps no state beyond cached device properties and
- *    one device-side error flag.
+ *    fp8_sync_status), and keeps no state beyond cached device properties,
+ *    one device-side error flag and the fixed work array that
+ *    fp8_linear_bwd_noalloc uses (described there).
  *  - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
  *    stream).  All work is enqueued on it, in order; scales are read on the
  *    device, so a training step needs no host round trip.
