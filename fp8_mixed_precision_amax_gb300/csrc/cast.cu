@@ -7,7 +7,14 @@
 //    amax (the Q node of the TensorRT page);
 //  * the delayed-scaling history / scale update (DelayedScaling's margin and
 //    amax_history_len, implementation guide section "Dynamic scaling and the
-//    FP8 recipe").
+//    FP8 recipe");
+//  * just-in-time scaling: the cast deriving its scale from the amax of the
+//    same step ("Mixed-precision training" wiki note, bullet "per-tensor
+//    scaling is the key");
+//  * LayerNorm row statistics and the LayerNorm branch of the cast
+//    (te.LayerNorm ahead of an FP8 linear, implementation guide section
+//    "Basic structure of FP8 training code");
+//  * the scaled cast of fp32 tensors (no transposed copy).
 #include <cfloat>
 #include <cstdint>
 #include <mutex>
