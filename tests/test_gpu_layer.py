@@ -267,3 +267,98 @@ def test_special_values_through_the_layer():
             assert f32_bits(lin.meta.scale[slot].item()) == f32_bits(st.scale[slot])
         assert hist[o.SLOT_X, 0] == np.inf and lin.meta.scale[o.SLOT_X].item() == 1.0
     f.fp8_sync_status()
+
+
+def test_gradient_accumulation_records_the_max_over_micro_batches():
+    """Two forward + backward passes before one update (gradient
+    accumulation over two micro-batches): both passes cast with the same,
+    not yet updated scales; the amax slots hold the max over both passes
+    (X, W, dY against the oracle, Y and dX against the GPU's own outputs);
+    the update pushes exactly that max into each history and clears the
+    slots."""
+    f = _lib()
+    w = wl.Workload("accum", 256, 512, 384, "normal", 1.0, 0.05, 0.01, 16, 0, True, 2)
+    W = wl.layer_weight(w, "cuda")
+    lin = f.Fp8Linear(W, w.M, f.Recipe(w.margin, w.history_len, w.hybrid))
+    lin.step(wl.layer_x(w, 5, "cuda"), wl.layer_dy(w, 5, "cuda"))   # scales away from 1.0
+    torch.cuda.synchronize()
+    scale0 = lin.meta.scale.cpu().numpy().copy()
+    hist0 = lin.meta.history.cpu().numpy().copy()
+    passes = []
+    for k in (0, 1):
+        X, dY = wl.layer_x(w, k, "cuda"), wl.layer_dy(w, k, "cuda")
+        Y = torch.empty((w.M, w.N), dtype=torch.bfloat16, device="cuda")
+        dX = torch.empty((w.M, w.K), dtype=torch.bfloat16, device="cuda")
+        dW = torch.empty((w.N, w.K), dtype=torch.bfloat16, device="cuda")
+        lin.forward(X, Y=Y)
+        X8 = lin.X8.clone()
+        lin.backward(dY, dX=dX, dW=dW)
+        passes.append((host_bf16_bits(X), host_bf16_bits(dY), Y, dX, X8, lin.dY8.clone()))
+    torch.cuda.synchronize()
+    assert np.array_equal(lin.meta.scale.cpu().numpy().view(np.uint32), scale0.view(np.uint32))
+    amax = lin.meta.amax.cpu().numpy().copy()
+    absmax = lambda t: np.float32(np.max(np.abs(bf16_values(host_bf16_bits(t)))))
+    expect = {
+        f.SLOT_X: max(o.amax(p[0]) for p in passes),
+        f.SLOT_W: o.amax(host_bf16_bits(W)),
+        f.SLOT_DY: max(o.amax(p[1]) for p in passes),
+        f.SLOT_Y: max(absmax(p[2]) for p in passes),
+        f.SLOT_DX: max(absmax(p[3]) for p in passes),
+    }
+    for slot, v in expect.items():
+        assert f32_bits(np.float32(amax[slot])) == f32_bits(np.float32(v)), slot
+    for xb, dyb, _, _, X8, dY8 in passes:
+        q, _ = o.quantize(xb, np.float32(scale0[f.SLOT_X]), o.E4M3)
+        assert np.array_equal(host_u8(X8), q)
+        q, _ = o.quantize(dyb, np.float32(scale0[f.SLOT_DY]), o.E5M2)
+        assert np.array_equal(host_u8(dY8), q)
+    lin.update()
+    torch.cuda.synchronize()
+    hist = lin.meta.history.cpu().numpy()
+    assert np.array_equal(hist[:, 0].view(np.uint32), amax.view(np.uint32))
+    assert np.array_equal(hist[:, 1:].view(np.uint32), hist0[:, :-1].view(np.uint32))
+    assert not lin.meta.amax.cpu().numpy().any()
+    f.fp8_sync_status()
+
+
+def test_two_layers_on_two_streams_match_sequential_runs():
+    """The library keeps no hidden per-call state: two layers stepping
+    concurrently on two streams produce, bit for bit, what each produces when
+    run alone (every output, every FP8 buffer and the whole scaling state)."""
+    f = _lib()
+    wa = wl.Workload("sa", 1040, 1024, 784, "normal", 1.0, 0.03, 1e-2, 16, 0, True, 3)
+    wb = wl.Workload("sb", 512, 784, 1040, "normal", 1.0, 0.05, 1e-2, 16, 1, True, 3, seed=1)
+    works = (wa, wb)
+    inputs = {w.name: [(wl.layer_x(w, s, "cuda"), wl.layer_dy(w, s, "cuda")) for s in range(3)]
+              for w in works}
+
+    def make():
+        return [f.Fp8Linear(wl.layer_weight(w, "cuda"), w.M,
+                            f.Recipe(w.margin, w.history_len, w.hybrid)) for w in works]
+
+    seq = make()
+    for lin, w in zip(seq, works):
+        for X, dY in inputs[w.name]:
+            lin.step(X, dY)
+    torch.cuda.synchronize()
+    con = make()
+    torch.cuda.synchronize()
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    for s in streams:
+        s.wait_stream(torch.cuda.current_stream())
+    for k in range(3):
+        for lin, w, s in zip(con, works, streams):
+            with torch.cuda.stream(s):
+                X, dY = inputs[w.name][k]
+                lin.step(X, dY)
+    for s in streams:
+        torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    bits = lambda t: t.view(torch.int16) if t.dtype == torch.bfloat16 else \
+        (t.view(torch.int32) if t.dtype == torch.float32 else t)
+    for a, b in zip(seq, con):
+        for name in ("Y", "dX", "dW", "X8", "X8t", "W8", "W8t", "dY8", "dY8t"):
+            assert torch.equal(bits(getattr(a, name)), bits(getattr(b, name))), name
+        for name in ("history", "amax", "scale", "scale_inv"):
+            assert torch.equal(bits(getattr(a.meta, name)), bits(getattr(b.meta, name))), name
+    f.fp8_sync_status()
