@@ -477,10 +477,22 @@ def cpu_baseline(w: wl.Workload, seconds: float = 12.0, Mp: int = 256, Np: int =
     return line
 
 
+def _use_all_host_cores(o) -> None:
+    """Give the oracle's OpenMP loops every core this process may run on.
+    torchrun sets OMP_NUM_THREADS=1 for its workers by default, which would
+    otherwise time the oracle on one core whenever N > 1."""
+    try:
+        import ctypes
+        ctypes.CDLL("libgomp.so.1").omp_set_num_threads(len(os.sched_getaffinity(0)))
+    except (OSError, AttributeError):
+        pass
+
+
 def run_reference(args, world, rank):
     if rank != 0:
         return None
     import oracle as o
+    _use_all_host_cores(o)
     w = wl.WORKLOADS[args.workload]
     # size the per-step sample so the whole run takes about two minutes
     dt, fl, _ = oracle_sample_step(o, w, 64, 256, None)
@@ -507,7 +519,8 @@ def run_reference(args, world, rank):
             "vs_baseline": None, "dtype": "f64 (oracle, exact FP8 decode)", "data": "synthetic",
             "config": workload_config(w),
             "cpu_baseline": {"kind": "oracle", "cores": o.num_threads(), "sample": sample,
-                             "value": value, "unit": "TFLOPS"},
+                             "value": value, "unit": "TFLOPS",
+                             "affinity_cores": len(os.sched_getaffinity(0))},
             "e2e": {"value": value, "unit": "TFLOPS", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
 
