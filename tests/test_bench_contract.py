@@ -116,3 +116,25 @@ def test_clock_summary_from_nvidia_smi_lines():
     assert c["power_w_max"] == 1391.0
     assert c["reasons"] == ["sw_power_cap"]
     assert bench.ClockSampler.summarize([])["reasons"] == ["no samples"]
+
+
+def test_reference_arm_under_torchrun_two_ranks():
+    """With N = 2 ranks (gloo on the CPU), rank 0 alone times the oracle and
+    prints one line, the other rank exits 0, and the oracle uses every core
+    of rank 0's affinity mask although torchrun sets OMP_NUM_THREADS=1."""
+    import socket
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        port = s.getsockname()[1]
+    r = subprocess.run([sys.executable, "-m", "torch.distributed.run", "--nnodes=1",
+                        "--nproc-per-node", "2", "--master-addr", "127.0.0.1", "--master-port",
+                        str(port), "bench.py", "--impl", "reference", "--workload", "tiny",
+                        "--steps", "1", "--warmup", "3", "--gpus", "2"],
+                       cwd=ROOT, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
+    assert d["cpu_baseline"]["cores"] == d["cpu_baseline"]["affinity_cores"] == \
+        len(os.sched_getaffinity(0))
