@@ -127,3 +127,40 @@ def test_layernorm_linear_step_matches_oracle():
         ref = o.epilogue(o.gemm_tn(dY8t, fm[3], X8.T.copy(), fm[0]), si[3], si[0])
         assert_gemm_close(host_bf16_bits(lin.dW), ref, w.M, "dW")
     f.fp8_sync_status()
+
+
+@pytest.mark.parametrize("cols", [4096, 8192, 12288])
+def test_layernorm_constant_rows(cols):
+    """Degenerate rows whose elements are all equal: the variance is 0, so
+    rstd = 1/sqrt(eps) and the output is beta exactly.  At power-of-two
+    widths the fp32 mean is exact and those closed forms are checked bit for
+    bit; at every width (the register and the looping statistics kernels)
+    the elementwise result is exact given the kernel's own statistics."""
+    f = _lib()
+    rows = 32
+    x = torch.full((rows, cols), 3.25, dtype=torch.bfloat16, device="cuda")
+    x[1::2] = -0.5
+    g = torch.Generator().manual_seed(cols)
+    gamma = (1 + 0.2 * torch.randn(cols, generator=g)).to(torch.bfloat16).cuda()
+    beta = (0.1 * torch.randn(cols, generator=g)).to(torch.bfloat16).cuda()
+    s = np.float32(64.0)
+    out = torch.empty((rows, cols), dtype=torch.uint8, device="cuda")
+    out_t = torch.empty((cols, rows), dtype=torch.uint8, device="cuda")
+    am = torch.full((1,), -1.0, device="cuda")
+    mean = torch.empty(rows, device="cuda")
+    rstd = torch.empty(rows, device="cuda")
+    f.fp8_layernorm_quantize_transpose(x, gamma, beta, 1e-5, torch.tensor([s], device="cuda"),
+                                       o.E4M3, mean, rstd, out, out_t, am)
+    torch.cuda.synchronize()
+    xb, gb, bb = host_bf16_bits(x), host_bf16_bits(gamma), host_bf16_bits(beta)
+    q = host_u8(out)
+    check_elementwise_exact(q, xb, gb, bb, mean.cpu().numpy(), rstd.cpu().numpy(), s, o.E4M3,
+                            am.item(), f"constant rows x {cols}")
+    assert np.array_equal(host_u8(out_t), q.T)
+    if cols & (cols - 1) == 0:
+        m = mean.cpu().numpy()
+        assert np.all(m[0::2] == np.float32(3.25)) and np.all(m[1::2] == np.float32(-0.5))
+        rs = np.float32(np.float32(1.0) / np.sqrt(np.float32(1e-5)))
+        assert np.all(rstd.cpu().numpy().view(np.uint32) == rs.view(np.uint32))
+        ref, _ = o.quantize(np.tile(bb, (rows, 1)), s, o.E4M3)
+        assert np.array_equal(q, ref)

@@ -42,3 +42,25 @@ def test_layernorm_normalises_rows():
     b = _bf16(np.full(1024, 0.5))
     y2, _, _ = o.layernorm(x, g, b, 0.0)
     assert np.allclose(y2, 2 * y + 0.5, rtol=1e-14, atol=1e-14)
+
+
+def test_layernorm_closed_forms():
+    """Rows whose statistics are known exactly: a constant row has mean c,
+    variance 0, rstd 1/sqrt(eps) and output beta; a row alternating a and b
+    has mean (a+b)/2 and variance ((a-b)/2)^2, so its normalised values are
+    +-1 scaled by sqrt(var / (var + eps))."""
+    cols = 256
+    g = _bf16(np.full(cols, 1.5))
+    b = _bf16(np.linspace(-1, 1, cols))
+    x = _bf16(np.full((1, cols), 3.25))
+    y, mean, rstd = o.layernorm(x, g, b, 1e-5)
+    assert mean[0] == 3.25 and rstd[0] == 1 / np.sqrt(1e-5)
+    assert np.array_equal(y[0], _f64(b).numpy())
+    a_, b_ = 2.0, -6.0
+    x = _bf16(np.tile([a_, b_], cols // 2)[None, :])
+    y, mean, rstd = o.layernorm(x, _bf16(np.ones(cols)), _bf16(np.zeros(cols)), 1e-5)
+    var = ((a_ - b_) / 2) ** 2
+    assert mean[0] == (a_ + b_) / 2
+    assert np.isclose(rstd[0], 1 / np.sqrt(var + 1e-5), rtol=1e-15)
+    expect = np.tile([1.0, -1.0], cols // 2) * np.sqrt(var) / np.sqrt(var + 1e-5)
+    assert np.allclose(y[0], expect, rtol=1e-14, atol=0)
