@@ -46,7 +46,10 @@ def _check(x, scale, fmt, what=""):
 
 
 ALL_BF16_SCALES = [1.0, 0.5, 3.0, 448.0, 1 / 448.0, 57344.0, 2.0 ** -20, 2.0 ** 20, 1e-30, 1e30,
-                   0.0, -1.5, 3.4e38, 1.17549435e-38, 0.1234567, 7.654321e-5, 1234.5678]
+                   0.0, -1.5, 3.4e38, 1.17549435e-38, 0.1234567, 7.654321e-5, 1234.5678,
+                   # degenerate scales the update never produces but the ABI accepts:
+                   # IEEE products (inf * x saturates, 0 * inf and NaN give NaN codes)
+                   float("inf"), float("-inf"), float("nan"), 1e-45]
 
 
 @pytest.mark.parametrize("fmt", FMTS)
