@@ -125,3 +125,30 @@ def test_grouped_launch_matches_oracle(shapes):
             assert_gemm_close(got[r0:r0 + ref.shape[0]], ref, K, f"{tuple(D.shape)} rows {r0}")
         full_max = np.float32(np.max(np.abs(bf16_values(got))))
         assert f32_bits(np.float32(am.item())) == f32_bits(full_max)
+
+
+def test_gemm_degenerate_dequant_factors():
+    """The ABI takes any scale_inv, so fl32(a_scale_inv * b_scale_inv) may be
+    0, inf, NaN or underflow to 0.  With small-integer operands the fp32
+    accumulation is exact, so every output is fixed by IEEE arithmetic: D
+    matches the oracle's epilogue bit for bit (BF16 NaN as a class), and the
+    fused amax is max |D| over the non-NaN outputs (infinities included; 0
+    when every output is NaN)."""
+    rng = np.random.default_rng(17)
+    M, N, K = 128, 256, 64
+    vals = np.array([0, 1, 2, 3, 4, -1, -2, -3, -4], np.float32)
+    A = o.fp8_encode(rng.choice(vals, (M, K)), o.E4M3).reshape(M, K)
+    B = o.fp8_encode(rng.choice(vals, (N, K)), o.E4M3).reshape(N, K)
+    acc = o.gemm_tn_exact(A, o.E4M3, B, o.E4M3)
+    assert (acc == 0).any() and (acc > 0).any() and (acc < 0).any()
+    nan16 = lambda b: (b & 0x7FFF) > 0x7F80
+    for sa, sb in ((0.0, 1.0), (float("inf"), 1.0), (float("nan"), 2.0), (1e30, 1e30),
+                   (1e-30, 1e-30), (-float("inf"), 0.5)):
+        got, am = _run(A, o.E4M3, B, o.E4M3, np.float32(sa), np.float32(sb))
+        ref = o.epilogue(acc, np.float32(sa), np.float32(sb))
+        both_nan = nan16(got) & nan16(ref)
+        assert np.array_equal(nan16(got), nan16(ref)), (sa, sb)
+        assert np.array_equal(got[~both_nan], ref[~both_nan]), (sa, sb)
+        vals_ok = np.abs(bf16_values(got[~nan16(got)]))
+        expect = np.float32(vals_ok.max()) if vals_ok.size else np.float32(0.0)
+        assert f32_bits(am) == f32_bits(expect), (sa, sb, am, expect)
