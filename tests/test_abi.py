@@ -155,3 +155,14 @@ def test_python_binding_rejects_cpu_tensors():
     x = torch.zeros(16, 16, dtype=torch.bfloat16)
     with pytest.raises(ValueError):
         f.fp8_amax(x, torch.zeros(1))
+
+
+def test_header_enums_match_binding():
+    """Status codes, formats and scaling modes: the binding's constants are
+    the header's enum values."""
+    src = open(api.HEADER_PATH).read()
+    enum = dict((k, int(v)) for k, v in re.findall(r"\b(FP8_[A-Z0-9_]+)\s*=\s*(\d+)", src))
+    assert {v: k for k, v in api.STATUS.items()} == {k: enum[k] for k in api.STATUS.values()}
+    assert (enum["FP8_E4M3"], enum["FP8_E5M2"]) == (api.E4M3, api.E5M2)
+    assert (enum["FP8_SCALING_DELAYED"], enum["FP8_SCALING_CURRENT"]) == \
+        (api.SCALING_DELAYED, api.SCALING_CURRENT)
