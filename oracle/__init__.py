@@ -24,9 +24,10 @@ What each function follows:
   amax alone.
 * ``layernorm`` -- te.LayerNorm's forward (implementation guide, "Basic
   structure of FP8 training code"), in double.
-* ``adam_step`` -- Adam with the optimizer-state precision decoupling of the
+* ``adam_step`` / ``adam_init`` -- Adam (textbook bias correction, AdamW's
+  decoupled weight decay) with the optimizer-state precision decoupling of the
   wiki note (first moment FP8, second moment FP16, master weights FP16 with
-  tensor scaling), in binary32.
+  tensor scaling), in binary32; the initial state of a weight tensor.
 * ``fp8_allreduce`` / ``dequant_sum`` -- FP8 all-reduce with one scale shared
   by all ranks, s'_g = min(s'_1 .. s'_N) (wiki note, bullet "per-tensor
   scaling is the key").
@@ -107,6 +108,8 @@ def _lib():
         lib.or_f16_encode.argtypes, lib.or_f16_encode.restype = [f32], ctypes.c_uint16
         lib.or_adam_step.argtypes = [vp, i64, vp, vp, vp, vp, vp, vp, vp, vp, vp] + [f32] * 7 + [i32]
         lib.or_adam_step.restype = None
+        lib.or_adam_init.argtypes = [vp, i64, i32, vp, vp, vp, vp, vp, vp, vp, vp]
+        lib.or_adam_init.restype = None
         lib.or_dequant_sum.argtypes = [vp, i32, i64, ctypes.c_int, f32, vp]
         lib.or_dequant_sum.restype = None
         _lib_handle = lib
@@ -314,6 +317,24 @@ def adam_step(grad_bf16, m1, m1_scale, m1_scale_inv, m2, w16, w_scale, w_scale_i
                         float(np.float32(hp.beta2)), float(np.float32(hp.eps)),
                         float(np.float32(hp.weight_decay)), float(bc1), float(bc2), int(hp.margin))
     return m1o, sc[0], sc[1], m2o, w16o, sc[2], sc[3], wb, am
+
+
+def adam_init(w_bf16, margin: int = 0):
+    """Initial decoupled-precision Adam state of a BF16 weight tensor (wiki
+    note, bullet "precision decoupling"): zero moments, master weights FP16
+    under the just-in-time scale of w (fmax 65504, a history of one).
+    Returns (m1, m1_scale, m1_scale_inv, m2, w16, w_scale, w_scale_inv, amax[2])."""
+    w = _c(w_bf16, np.uint16).reshape(-1)
+    n = w.size
+    m1 = np.empty(n, np.uint8)
+    m2 = np.empty(n, np.uint16)
+    w16 = np.empty(n, np.uint16)
+    sc = np.zeros(4, np.float32)
+    am = np.zeros(2, np.float32)
+    _lib().or_adam_init(w.ctypes.data, n, int(margin), m1.ctypes.data, sc[0:].ctypes.data,
+                        sc[1:].ctypes.data, m2.ctypes.data, w16.ctypes.data, sc[2:].ctypes.data,
+                        sc[3:].ctypes.data, am.ctypes.data)
+    return m1, sc[0], sc[1], m2, w16, sc[2], sc[3], am
 
 
 # ------------------------------------------------- FP8 all-reduce --

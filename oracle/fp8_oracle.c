@@ -412,9 +412,11 @@ uint16_t or_f16_encode(float f)
 /* One Adam step with decoupled optimizer-state precision ([P3] bullet       */
 /* "precision decoupling": first moment FP8, second moment FP16, master      */
 /* weights FP16 with tensor scaling).  All arithmetic in binary32, one       */
-/* rounding per operation, in this order (AdamW's decoupled weight decay):   */
+/* rounding per operation, in this order (Adam with bias correction, the     */
+/* textbook form: m_hat = m / (1 - b1^t), v_hat = v / (1 - b2^t); AdamW's    */
+/* decoupled weight decay):                                                  */
 /*   m  = b1*m + (1-b1)*g,   v = b2*v + (1-b2)*(g*g)                         */
-/*   u  = (m * fl32(1/bc1)) / (sqrt(v * fl32(1/bc2)) + eps)                   */
+/*   u  = (m / bc1) / (sqrt(v / bc2) + eps)                                   */
 /*   w  = w - lr*(u + wd*w)                                                   */
 /* with m decoded from its E4M3 codes times m_sinv and w from its FP16 codes */
 /* times w_sinv.  Just-in-time per-tensor scaling of the new states:         */
@@ -429,7 +431,7 @@ static void adam_elem(float g, float m, float v, float w, float lr, float b1, fl
 {
     m = b1 * m + (1.0f - b1) * g;
     v = b2 * v + (1.0f - b2) * (g * g);
-    float u = (m * (1.0f / bc1)) / (sqrtf(v * (1.0f / bc2)) + eps);
+    float u = (m / bc1) / (sqrtf(v / bc2) + eps);
     w = w - lr * (u + wd * w);
     *mo = m;
     *vo = v;
@@ -482,6 +484,39 @@ void or_adam_step(const uint16_t *grad, int64_t n, uint8_t *m1, float *m1_scale,
     *m1_scale_inv = smi;
     *w_scale = sw;
     *w_scale_inv = swi;
+}
+
+/* Initial decoupled-precision Adam state of a BF16 weight tensor w (same     */
+/* bullet): zero moments (first-moment scale and inverse 1), and the master  */
+/* weights in FP16 under the just-in-time tensor scale of w itself: the      */
+/* recipe formula on a one-entry history with FP16's largest finite value,   */
+/*   s_w = fl32(fl32(65504 / amax(w)) * 2^-margin), s_w = 1 when amax(w) is   */
+/*   0 or not finite;  w16[i] = enc_f16(fl32(w[i] * s_w)).                   */
+/* amax[0] = 0 (the first moment), amax[1] = amax(w).                        */
+
+void or_adam_init(const uint16_t *w, int64_t n, int32_t margin, uint8_t *m1, float *m1_scale,
+                  float *m1_scale_inv, uint16_t *m2, uint16_t *w16, float *w_scale,
+                  float *w_scale_inv, float *amax)
+{
+    float am = or_amax_bf16(w, n);
+    float s = 1.0f;
+    if (am > 0.0f && isfinite(am)) {
+        float q = 65504.0f / am;                      /* binary32 divide */
+        s = (float)ldexp((double)q, -margin);         /* exact, then one rounding */
+        if (isinf(s))
+            s = FLT_MAX;
+    }
+    for (int64_t i = 0; i < n; ++i) {
+        m1[i] = 0;
+        m2[i] = 0;
+        w16[i] = or_f16_encode(or_bf16_to_f32(w[i]) * s); /* binary32 multiply */
+    }
+    *m1_scale = 1.0f;
+    *m1_scale_inv = 1.0f;
+    *w_scale = s;
+    *w_scale_inv = 1.0f / s;                          /* binary32 divide */
+    amax[0] = 0.0f;
+    amax[1] = am;
 }
 
 /* ------------------------------------------------------------------------ */

@@ -72,10 +72,16 @@ MUTANTS = {
     "Adam second moment without the squared gradient": (
         "v = b2 * v + (1.0f - b2) * (g * g);", "v = b2 * v + (1.0f - b2) * g;"),
     "Adam without the first bias correction": (
-        "float u = (m * (1.0f / bc1)) / (sqrtf(v * (1.0f / bc2)) + eps);",
-        "float u = m / (sqrtf(v * (1.0f / bc2)) + eps);"),
+        "float u = (m / bc1) / (sqrtf(v / bc2) + eps);",
+        "float u = m / (sqrtf(v / bc2) + eps);"),
     "Adam weight decay with the wrong sign": (
         "w = w - lr * (u + wd * w);", "w = w - lr * (u - wd * w);"),
+    "Adam initial master weights stored unscaled": (
+        "w16[i] = or_f16_encode(or_bf16_to_f32(w[i]) * s); /* binary32 multiply */",
+        "w16[i] = or_f16_encode(or_bf16_to_f32(w[i]));"),
+    "Adam initial weight scale ignores the margin": (
+        "        s = (float)ldexp((double)q, -margin);         /* exact, then one rounding */",
+        "        s = q;"),
     "FP8 sum multiplied by the scale instead of its inverse": (
         "out[i] = or_f32_to_bf16((float)(acc * (double)sinv));",
         "out[i] = or_f32_to_bf16((float)(acc * (double)scale));"),

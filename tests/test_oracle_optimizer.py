@@ -109,3 +109,43 @@ def test_zero_gradient_keeps_first_moment_scale():
     out = o.adam_step(g, st["m1"], np.float32(5.0), np.float32(0.2), st["m2"], st["w16"],
                       st["w_scale"], st["w_scale_inv"], o.AdamHyper(), 1)
     assert out[1] == 5.0 and out[2] == np.float32(0.2) and out[8][0] == 0.0
+
+
+def _np_f16_bits(v32):
+    """numpy's binary32 -> binary16 conversion (round to nearest even), after
+    clipping to the largest finite FP16 value (the saturating reading)."""
+    return np.clip(v32, -65504.0, 65504.0).astype(np.float16).view(np.uint16)
+
+
+def test_initial_state_of_a_weight_tensor():
+    """The initial master weights are the FP16 codes of w under the tensor
+    scale that puts w's largest magnitude on FP16's largest finite value
+    (65504, the wiki table): numpy's float16 conversion of the binary32
+    product gives every code, the largest element lands on 0x7bff (or its
+    negative), the decoded weights are within FP16 rounding of w, and the
+    moments start at zero with unit scales."""
+    rng = np.random.default_rng(4)
+    for n, mag in ((4096, 0.02), (1000 * 16, 3.0), (16, 1e-3)):
+        wb = _bf16(rng.standard_normal(n) * mag)
+        w = _bf16_vals(wb)
+        m1, ms, msi, m2, w16, ws, wsi, am = o.adam_init(wb, margin=0)
+        assert not m1.any() and not m2.any() and ms == 1.0 and msi == 1.0
+        assert am[0] == 0.0 and am[1] == np.float32(np.abs(w).max())
+        assert np.array_equal(w16, _np_f16_bits(w.astype(np.float32) * ws))
+        top = int(np.argmax(np.abs(w)))
+        assert w16[top] & 0x7FFF == 0x7BFF
+        back = o.f16_decode(w16).astype(np.float64) * np.float64(wsi)
+        assert np.all(np.abs(back - w) <= 2 ** -11 * np.abs(w) + 2 ** -24 * float(wsi))
+        assert wsi == np.float32(1.0) / ws
+
+
+def test_initial_state_margin_and_zero_weights():
+    rng = np.random.default_rng(5)
+    wb = _bf16(rng.standard_normal(256) * 0.1)
+    s0 = o.adam_init(wb, margin=0)[5]
+    s1 = o.adam_init(wb, margin=1)
+    assert s1[5] == s0 / 2
+    top = int(np.argmax(np.abs(_bf16_vals(wb))))
+    assert s1[4][top] & 0x7FFF == 0x77FF          # 32752 = 65504 / 2
+    z = o.adam_init(np.zeros(64, np.uint16))
+    assert z[5] == 1.0 and z[6] == 1.0 and not z[4].any() and z[7][1] == 0.0
