@@ -102,6 +102,7 @@ def _load() -> ctypes.CDLL:
         "fp8_dequant_sum": ([vp, i32, i64, i32, vp, vp, vp], ctypes.c_int),
         "fp8_adam_step": ([vp, i64, vp, vp, vp, vp, vp, vp, vp, vp, vp,
                            ctypes.POINTER(fp8_adam_hyper), vp], ctypes.c_int),
+        "fp8_adam_init": ([vp, i64, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp], ctypes.c_int),
         "fp8_linear_bwd_noalloc": ([vp, i64, i64, i64, ctypes.POINTER(fp8_meta),
                                     ctypes.POINTER(fp8_recipe), vp, vp, vp, vp, vp],
                                    ctypes.c_int),
@@ -109,7 +110,7 @@ def _load() -> ctypes.CDLL:
     for name, (args, res) in sig.items():
         f = getattr(lib, name)
         f.argtypes, f.restype = args, res
-    if lib.fp8_abi_version() != 3:
+    if lib.fp8_abi_version() != 4:
         raise ImportError("libfp8amax.so ABI version mismatch")
     return lib
 
@@ -524,19 +525,27 @@ class Fp8AdamState:
     second moment FP16, master weights FP16 with a per-tensor scale -- 5 bytes
     of state per parameter.  ``scales`` = [m1_scale, m1_scale_inv, w_scale, w_scale_inv]."""
 
-    def __init__(self, w: torch.Tensor):
+    def __init__(self, w: torch.Tensor, margin: int = 0, stream=None):
+        """State of the BF16 weight tensor ``w``, initialised on the device by
+        fp8_adam_init: zero moments, master weights FP16 under the
+        just-in-time scale of w (fmax 65504, ``margin``)."""
         n = w.numel()
         dev = w.device
         self.n = n
-        self.m1 = torch.zeros(n, dtype=torch.uint8, device=dev)
-        self.m2 = torch.zeros(n, dtype=torch.float16, device=dev)
-        wf = w.detach().float().reshape(-1)
-        amax = wf.abs().max().item()
-        ws = (65504.0 / amax) if amax > 0 else 1.0
-        self.scales = torch.tensor([1.0, 1.0, ws, 1.0 / ws], dtype=torch.float32, device=dev)
-        self.w16 = (wf * self.scales[2]).clamp(-65504, 65504).to(torch.float16)
-        self.amax = torch.zeros(2, dtype=torch.float32, device=dev)
+        self.m1 = torch.empty(n, dtype=torch.uint8, device=dev)
+        self.m2 = torch.empty(n, dtype=torch.float16, device=dev)
+        self.w16 = torch.empty(n, dtype=torch.float16, device=dev)
+        self.scales = torch.empty(4, dtype=torch.float32, device=dev)
+        self.amax = torch.empty(2, dtype=torch.float32, device=dev)
         self.t = 0
+        sc = self.scales
+        wc = w.detach().reshape(-1)
+        _check(_lib.fp8_adam_init(
+            _ptr(wc, torch.bfloat16, "w"), n, int(margin), _p8(self.m1, "m1"),
+            ctypes.c_void_p(sc.data_ptr()), ctypes.c_void_p(sc.data_ptr() + 4),
+            _ptr(self.m2, torch.float16, "m2"), _ptr(self.w16, torch.float16, "w16"),
+            ctypes.c_void_p(sc.data_ptr() + 8), ctypes.c_void_p(sc.data_ptr() + 12),
+            _ptr(self.amax, torch.float32, "amax"), _stream(stream)))
 
     def step(self, grad: torch.Tensor, w_bf16: torch.Tensor, hp: AdamHyper, stream=None) -> None:
         """One step with ``grad`` (BF16, n elements); writes the new weights

@@ -421,6 +421,31 @@ fp8_status fp8_adam_step(const void *grad, int64_t n, uint8_t *m1, float *m1_sca
     return FP8_OK;
 }
 
+fp8_status fp8_adam_init(const void *w, int64_t n, int32_t margin, uint8_t *m1, float *m1_scale,
+                         float *m1_scale_inv, uint16_t *m2, uint16_t *w16, float *w_scale,
+                         float *w_scale_inv, float *amax, void *stream) {
+    const char *fn = "fp8_adam_init";
+    const fp8k::CallRange range(fn);
+    FP8_TRY(check_dims16(fn, n, "n", 0, "-"));
+    if (margin < 0 || margin > 64) return fail(FP8_ERR_ARG, "%s: margin %d outside [0, 64]", fn, margin);
+    const bool empty = n == 0;
+    FP8_TRY(check_ptr(fn, w, "w", empty));
+    FP8_TRY(check_ptr(fn, m1, "m1", empty));
+    FP8_TRY(check_ptr(fn, m2, "m2", empty));
+    FP8_TRY(check_ptr(fn, w16, "w16", empty));
+    FP8_TRY(check_scalar(fn, m1_scale, "m1_scale", false));
+    FP8_TRY(check_scalar(fn, m1_scale_inv, "m1_scale_inv", false));
+    FP8_TRY(check_scalar(fn, w_scale, "w_scale", false));
+    FP8_TRY(check_scalar(fn, w_scale_inv, "w_scale_inv", false));
+    FP8_TRY(check_scalar(fn, amax, "amax", false));
+    int sms;
+    FP8_TRY(current_device(&sms));
+    const fp8k::AdamInitSpec a{w, n, margin, m1, m1_scale, m1_scale_inv, m2, w16, w_scale,
+                               w_scale_inv, amax};
+    FP8_CUDA(fp8k::launch_adam_init(a, sms, static_cast<cudaStream_t>(stream)), fn);
+    return FP8_OK;
+}
+
 fp8_status fp8_layernorm_quantize_transpose(const void *x, const void *gamma, const void *beta,
                                             int64_t rows, int64_t cols, float eps,
                                             const float *scale, int32_t fmt, uint8_t *out,

@@ -131,6 +131,21 @@ struct AdamSpec {
 };
 cudaError_t launch_adam_step(const AdamSpec &s, int sm_count, cudaStream_t st);
 
+// Initial decoupled-precision Adam state of a BF16 weight tensor: zero
+// moments, FP16 master weights under the just-in-time scale of w (fmax
+// 65504), the four scales, and amax = {0, amax(w)}.
+struct AdamInitSpec {
+    const void *w;
+    int64_t n;
+    int margin;
+    uint8_t *m1;
+    float *m1_scale, *m1_scale_inv;
+    uint16_t *m2, *w16;
+    float *w_scale, *w_scale_inv;
+    float *amax;
+};
+cudaError_t launch_adam_init(const AdamInitSpec &s, int sm_count, cudaStream_t st);
+
 // Decode-and-sum of nranks FP8 parts [nranks][n] sharing one scale (optim.cu).
 cudaError_t launch_dequant_sum(const uint8_t *parts, int nranks, int64_t n, int fmt,
                                const float *scale, void *out, int sm_count, cudaStream_t st);

@@ -3,10 +3,11 @@
 // first moment in FP8, the second moment in FP16, master weights in FP16
 // with tensor scaling -- 5 bytes of state per parameter instead of 12).
 //
-// Per element, in binary32 with one rounding per operation (AdamW's
-// decoupled weight decay):
+// Per element, in binary32 with one rounding per operation (Adam's bias
+// correction in its textbook form, m / (1 - b1^t) and v / (1 - b2^t), and
+// AdamW's decoupled weight decay):
 //   m = b1*m + (1-b1)*g;  v = b2*v + (1-b2)*(g*g)
-//   u = (m * fl32(1/bc1)) / (sqrt(v * fl32(1/bc2)) + eps);  w = w - lr*(u + wd*w)
+//   u = (m / bc1) / (sqrt(v / bc2) + eps);  w = w - lr*(u + wd*w)
 // m is decoded from E4M3 codes times the first moment's scale_inv, w from
 // FP16 codes times the weights' scale_inv.  The new states get just-in-time
 // per-tensor scales (fmax / amax of the new values, a history of one):
@@ -15,6 +16,8 @@
 //                       w and the model's BF16 copy of w;
 //   adam_scales_kernel  records the new scales after every block has decoded
 //                       with the old ones.
+// adam_init_kernel writes the initial state of a weight tensor: zero moments
+// and the FP16 master weights under the just-in-time scale of the weights.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -63,9 +66,11 @@ struct Elem8 {
     float m[8], v[8], w[8];
 };
 
-// Loop-invariant operands, each duplicated into both lanes of an fp32 pair.
+// Loop-invariant operands, each duplicated into both lanes of an fp32 pair
+// (the bias corrections are divisors, used one lane at a time).
 struct AdamConst {
-    uint64_t b1, omb1, b2, omb2, rbc1, rbc2, eps, lr, wd, msi, wsi;
+    uint64_t b1, omb1, b2, omb2, eps, lr, wd, msi, wsi;
+    float bc1, bc2;
 };
 
 __device__ __forceinline__ AdamConst adam_const(const AdamArgs &a, float msi, float wsi) {
@@ -74,8 +79,8 @@ __device__ __forceinline__ AdamConst adam_const(const AdamArgs &a, float msi, fl
     c.omb1 = splat_f32x2(__fsub_rn(1.0f, a.b1));
     c.b2 = splat_f32x2(a.b2);
     c.omb2 = splat_f32x2(__fsub_rn(1.0f, a.b2));
-    c.rbc1 = splat_f32x2(__fdiv_rn(1.0f, a.bc1));
-    c.rbc2 = splat_f32x2(__fdiv_rn(1.0f, a.bc2));
+    c.bc1 = a.bc1;
+    c.bc2 = a.bc2;
     c.eps = splat_f32x2(a.eps);
     c.lr = splat_f32x2(a.lr);
     c.wd = splat_f32x2(a.wd);
@@ -130,10 +135,10 @@ __device__ __forceinline__ void adam8(const Raw8 &raw, const AdamConst &k, Elem8
         f32x2_unpack(f32x2_mul(k.b2, v_old), a0, a1);
         f32x2_unpack(f32x2_mul(k.omb2, f32x2_mul(g, g)), b0, b1);
         const float v0 = __fadd_rn(a0, b0), v1 = __fadd_rn(a1, b1);
-        // u = (m * rbc1) / (sqrt(v * rbc2) + eps)
-        float n0, n1, q0, q1, e0, e1;
-        f32x2_unpack(f32x2_mul(f32x2_pack(m0, m1), k.rbc1), n0, n1);
-        f32x2_unpack(f32x2_mul(f32x2_pack(v0, v1), k.rbc2), q0, q1);
+        // u = (m / bc1) / (sqrt(v / bc2) + eps)
+        float e0, e1;
+        const float n0 = __fdiv_rn(m0, k.bc1), n1 = __fdiv_rn(m1, k.bc1);
+        const float q0 = __fdiv_rn(v0, k.bc2), q1 = __fdiv_rn(v1, k.bc2);
         f32x2_unpack(k.eps, e0, e1);
         const float u0 = __fdiv_rn(n0, __fadd_rn(__fsqrt_rn(q0), e0));
         const float u1 = __fdiv_rn(n1, __fadd_rn(__fsqrt_rn(q1), e1));
@@ -347,6 +352,45 @@ __global__ void __launch_bounds__(256) dequant_sum_kernel(const uint8_t *__restr
     }
 }
 
+// Initial state of a weight tensor w (BF16): m1 = 0, m2 = 0, w16 =
+// enc_f16(fl32(w * s_w)) with s_w the recipe formula on amax(w) and FP16's
+// largest finite value (1 when that amax is 0 or not finite); block 0 also
+// writes the four scales.  amax[1] holds amax(w) from the amax kernel.
+__global__ void __launch_bounds__(256) adam_init_kernel(const uint16_t *__restrict__ w,
+                                                        int64_t n, int margin, uint8_t *m1,
+                                                        float *m1_scale, float *m1_scale_inv,
+                                                        uint16_t *m2, uint16_t *w16,
+                                                        float *w_scale, float *w_scale_inv,
+                                                        const float *amax) {
+    pdl_wait();
+    pdl_trigger();
+    bool valid;
+    const float sw = recipe_scale(amax[1], kF16Max, margin, 1.0f, valid);
+    const uint64_t sw2 = splat_f32x2(sw);
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+        *m1_scale = 1.0f;
+        *m1_scale_inv = 1.0f;
+        *w_scale = sw;
+        *w_scale_inv = __fdiv_rn(1.0f, sw);
+    }
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x * 8;
+    for (int64_t i = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) * 8; i < n;
+         i += stride) {
+        const uint4 x4 = *reinterpret_cast<const uint4 *>(w + i);
+        const uint32_t xw[4] = {x4.x, x4.y, x4.z, x4.w};
+        uint32_t wq[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            float c0, c1;
+            f32x2_unpack(f32x2_mul(f32x2_from_bf16x2(xw[j]), sw2), c0, c1);
+            wq[j] = f16_enc_sat(c0) | (static_cast<uint32_t>(f16_enc_sat(c1)) << 16);
+        }
+        *reinterpret_cast<uint2 *>(m1 + i) = make_uint2(0u, 0u);
+        *reinterpret_cast<uint4 *>(m2 + i) = make_uint4(0u, 0u, 0u, 0u);
+        *reinterpret_cast<uint4 *>(w16 + i) = make_uint4(wq[0], wq[1], wq[2], wq[3]);
+    }
+}
+
 }  // namespace
 
 cudaError_t launch_dequant_sum(const uint8_t *parts, int nranks, int64_t n, int fmt,
@@ -360,6 +404,21 @@ cudaError_t launch_dequant_sum(const uint8_t *parts, int nranks, int64_t n, int 
     const dim3 g(static_cast<unsigned>(blocks)), b(threads);
     if (fmt == 0) return launch_pdl(dequant_sum_kernel<0>, g, b, 0, st, parts, nranks, n, scale, o);
     return launch_pdl(dequant_sum_kernel<1>, g, b, 0, st, parts, nranks, n, scale, o);
+}
+
+cudaError_t launch_adam_init(const AdamInitSpec &s, int sm_count, cudaStream_t st) {
+    cudaError_t e = cudaMemsetAsync(s.amax, 0, sizeof(float), st);   // the first moment's amax
+    if (e != cudaSuccess) return e;
+    if ((e = launch_amax(s.w, s.n, s.amax + 1, sm_count, st)) != cudaSuccess) return e;
+    const int threads = 256;
+    int64_t blocks = (s.n / 8 + threads - 1) / threads;
+    const int64_t cap = static_cast<int64_t>(sm_count) * 8;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    return launch_pdl(adam_init_kernel, dim3(static_cast<unsigned>(blocks)), dim3(threads), 0, st,
+                      static_cast<const uint16_t *>(s.w), s.n, s.margin, s.m1, s.m1_scale,
+                      s.m1_scale_inv, s.m2, s.w16, s.w_scale, s.w_scale_inv,
+                      static_cast<const float *>(s.amax));
 }
 
 cudaError_t launch_adam_step(const AdamSpec &s, int sm_count, cudaStream_t st) {

@@ -63,7 +63,7 @@
 extern "C" {
 #endif
 
-#define FP8AMAX_ABI_VERSION 3
+#define FP8AMAX_ABI_VERSION 4
 
 typedef enum { FP8_E4M3 = 0, FP8_E5M2 = 1 } fp8_format;
 
@@ -328,9 +328,10 @@ typedef struct {
  * bullet "precision decoupling": first moment FP8, second moment FP16,
  * master weights FP16 with tensor scaling: 5 bytes of state per parameter;
  * the note's 6 also counts an FP8 gradient, which this path keeps BF16).  In
- * binary32, one rounding per operation, for every element:
+ * binary32, one rounding per operation, for every element (Adam's textbook
+ * bias correction m / (1 - b1^t), v / (1 - b2^t); AdamW's decoupled decay):
  *   m = b1*m + (1-b1)*g;  v = b2*v + (1-b2)*(g*g);
- *   u = (m * fl32(1/bc1)) / (sqrt(v * fl32(1/bc2)) + eps);  w = w - lr*(u + wd*w)
+ *   u = (m / bc1) / (sqrt(v / bc2) + eps);  w = w - lr*(u + wd*w)
  * with m = E4M3 code * m1_scale_inv and w = FP16 code * w_scale_inv.  The new
  * states take just-in-time per-tensor scales: scale = (fmax / amax) /
  * 2^margin of the new values (fmax 448 for m, 65504 for w), kept when that
@@ -349,6 +350,24 @@ fp8_status fp8_adam_step(const void *grad, int64_t n, uint8_t *m1, float *m1_sca
                          float *m1_scale_inv, uint16_t *m2, uint16_t *w16, float *w_scale,
                          float *w_scale_inv, void *w_bf16, float *amax, const fp8_adam_hyper *hp,
                          void *stream);
+
+/* Initial state for fp8_adam_step of one BF16 weight tensor (same bullet):
+ * zero moments with first-moment scale and inverse 1, and the master weights
+ * in FP16 under the just-in-time scale of w itself -- the recipe formula on
+ * amax(w) alone with FP16's largest finite value:
+ *   s_w = fl32(fl32(65504 / amax(w)) * 2^-margin)  (FLT_MAX if it overflows;
+ *         1 when amax(w) is 0 or not finite),  w_scale_inv = fl32(1 / s_w),
+ *   w16[i] = FP16 code of fl32(w[i] * s_w), nearest even, saturating.
+ *   w       DEVICE [n] BF16 weights (read)
+ *   margin  0..64
+ *   m1 [n] E4M3 codes, m2 [n] FP16, w16 [n] FP16: DEVICE outputs
+ *   m1_scale, m1_scale_inv, w_scale, w_scale_inv: DEVICE, 1 float each, written
+ *   amax    DEVICE [2] output: {0, amax(w)}
+ * n >= 0, a multiple of 16; arrays 16-byte aligned.  Three kernels (after a
+ * one-word memset), in stream order. */
+fp8_status fp8_adam_init(const void *w, int64_t n, int32_t margin, uint8_t *m1, float *m1_scale,
+                         float *m1_scale_inv, uint16_t *m2, uint16_t *w16, float *w_scale,
+                         float *w_scale_inv, float *amax, void *stream);
 
 /* The summing half of an FP8 all-reduce with one shared scale (wiki note,
  * bullet "per-tensor scaling is the key": every rank casts with the one

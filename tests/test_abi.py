@@ -17,7 +17,7 @@ def test_every_declared_function_is_exported():
     assert len(declared) >= 10
     for name in declared:
         assert hasattr(lib, name), name
-    assert lib.fp8_abi_version() == 3
+    assert lib.fp8_abi_version() == 4
 
 
 def test_header_structs_match_binding():

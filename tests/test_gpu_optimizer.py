@@ -1,8 +1,9 @@
 """GPU parity of the decoupled-precision Adam step (first moment FP8, second
 moment FP16, master weights FP16 with tensor scaling) against the oracle:
-bit-exact first-moment codes, FP16 second moments and master weights, BF16
-weights, amaxes and scales, over several steps (both sides evaluate the same
-binary32 operations in the same order)."""
+bit-exact initial state (fp8_adam_init), first-moment codes, FP16 second
+moments and master weights, BF16 weights, amaxes and scales, over several
+steps (both sides evaluate the same binary32 operations -- textbook Adam, the
+bias corrections as IEEE divisions -- in the same order)."""
 import numpy as np
 import pytest
 import torch
@@ -27,13 +28,20 @@ def _u16(t):
 def test_adam_steps_bit_exact(n, wd, margin):
     f = _lib()
     g = torch.Generator().manual_seed(n + margin)
-    w = (torch.randn(n, generator=g) * 0.02).to(torch.bfloat16).cuda()
-    state = f.Fp8AdamState(w)
+    w = (torch.randn(n, generator=g) * 0.02).to(torch.bfloat16)
+    state = f.Fp8AdamState(w.cuda(), margin=margin)
     hp = f.AdamHyper(lr=3e-3, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=wd, margin=margin)
     ohp = o.AdamHyper(lr=3e-3, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=wd, margin=margin)
-    sc = state.scales.cpu().numpy()
-    ost = dict(m1=state.m1.cpu().numpy(), m1_scale=sc[0], m1_scale_inv=sc[1],
-               m2=_u16(state.m2), w16=_u16(state.w16), w_scale=sc[2], w_scale_inv=sc[3])
+    # the initial state: fp8_adam_init on the device against the oracle's
+    m1, ms, msi, m2, w16, ws, wsi, am = o.adam_init(_u16(w), margin)
+    torch.cuda.synchronize()
+    assert np.array_equal(state.m1.cpu().numpy(), m1)
+    assert np.array_equal(_u16(state.m2), m2)
+    assert np.array_equal(_u16(state.w16), w16)
+    assert np.array_equal(state.amax.cpu().numpy().view(np.uint32), am.view(np.uint32))
+    assert np.array_equal(state.scales.cpu().numpy().view(np.uint32),
+                          np.array([ms, msi, ws, wsi], np.float32).view(np.uint32))
+    ost = dict(m1=m1, m1_scale=ms, m1_scale_inv=msi, m2=m2, w16=w16, w_scale=ws, w_scale_inv=wsi)
     wout = torch.empty(n, dtype=torch.bfloat16, device="cuda")
     for t in range(1, 5):
         grad = (torch.randn(n, generator=g) * 1e-2 * t).to(torch.bfloat16)
@@ -64,3 +72,27 @@ def test_state_is_five_bytes_per_parameter():
     w = torch.zeros(4096, dtype=torch.bfloat16, device="cuda")
     s = f.Fp8AdamState(w)
     assert s.m1.element_size() + s.m2.element_size() + s.w16.element_size() == 5
+
+
+@pytest.mark.parametrize("n", [0, 16, 4096 + 16])
+def test_adam_init_edge_cases(n):
+    """Empty, one-vector and ragged tensors, all-zero weights (scale 1) and a
+    tensor with an infinite weight (scale kept at 1, codes saturate)."""
+    f = _lib()
+    g = torch.Generator().manual_seed(7 + n)
+    cases = [torch.zeros(n, dtype=torch.bfloat16),
+             (torch.randn(n, generator=g) * 3.0).to(torch.bfloat16)]
+    if n:
+        inf = cases[1].clone()
+        inf[n // 2] = float("inf")
+        cases.append(inf)
+    for w in cases:
+        st = f.Fp8AdamState(w.cuda(), margin=2)
+        torch.cuda.synchronize()
+        m1, ms, msi, m2, w16, ws, wsi, am = o.adam_init(_u16(w), 2)
+        assert np.array_equal(_u16(st.w16), w16)
+        assert np.array_equal(st.m1.cpu().numpy(), m1) and np.array_equal(_u16(st.m2), m2)
+        assert np.array_equal(st.scales.cpu().numpy().view(np.uint32),
+                              np.array([ms, msi, ws, wsi], np.float32).view(np.uint32))
+        assert np.array_equal(st.amax.cpu().numpy().view(np.uint32), am.view(np.uint32))
+    f.fp8_sync_status()
