@@ -340,7 +340,8 @@ def adam_init(w_bf16, margin: int = 0):
 # ------------------------------------------------- FP8 all-reduce --
 
 def dequant_sum(parts: np.ndarray, fmt: int, scale) -> np.ndarray:
-    """Sum of [nranks, n] FP8 codes sharing one scale, as BF16 bits."""
+    """Sum of [nranks, n] FP8 codes sharing one scale, as BF16 bits: the exact
+    sum of the decoded codes times fl32(1 / scale), rounded once to BF16."""
     q = _c(parts, np.uint8)
     nranks, n = q.shape
     out = np.empty(n, np.uint16)

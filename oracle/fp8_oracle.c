@@ -523,19 +523,88 @@ void or_adam_init(const uint16_t *w, int64_t n, int32_t margin, uint8_t *m1, flo
 /* Sum of FP8 tensors sharing one scale ([P3] bullet "per-tensor scaling is  */
 /* the key": FP8 all-reduce with one scalar shared by all ranks,             */
 /* s'_g = min(s'_1, ..., s'_N)).  q holds nranks parts of n codes each;      */
-/* out[i] = bf16_rne(fl32(sum_r dec(q[r][i]) * fl32(1 / scale))), the sum    */
-/* and the product in double (the sum is exact: at most 2^21 parts).         */
+/*   out[i] = bf16_rne( sum_r dec(q[r][i]) * fl32(1 / scale) ),              */
+/* the sum and the product exact, rounded once to BF16 (round to nearest,    */
+/* ties to even; overflow to +-inf; gradual underflow, a nonzero value that   */
+/* rounds to zero keeps its sign; an exact zero is +0).  Non-finite parts    */
+/* follow IEEE arithmetic: a NaN code, or +inf and -inf together, give NaN;  */
+/* one kind of infinity gives that infinity times fl32(1 / scale) (NaN when  */
+/* that factor is 0 or NaN); a finite sum times a non-finite factor is that  */
+/* factor's product with the sum's sign (NaN for a zero sum or a NaN factor). */
 /* ------------------------------------------------------------------------ */
+
+/* Every finite FP8 value is an integer number of quanta: 2^-9 for E4M3, 2^-16 */
+/* for E5M2 (the smallest subnormal of each format).                           */
+static int quantum_exp(int fmt) { return fmt == OR_E4M3 ? -9 : -16; }
+
+/* The nearest BF16 of the exact value (neg ? -1 : 1) * P * 2^e, P >= 0.       */
+static uint16_t bf16_of_exact(int neg, unsigned __int128 P, int e)
+{
+    if (P == 0)
+        return 0x0000;                                 /* an exact zero: +0 */
+    int nb = 0;                                        /* bit length of P */
+    for (unsigned __int128 t = P; t != 0; t >>= 1)
+        ++nb;
+    int lead = nb - 1 + e;                             /* 2^lead <= value < 2^(lead+1) */
+    int u = lead - 7;                                  /* BF16 keeps 8 significant bits */
+    if (u < -133)
+        u = -133;                                      /* the subnormal quantum 2^-133 */
+    int shift = u - e;                                 /* value = P * 2^e = (P >> shift) * 2^u + rest */
+    unsigned __int128 M;
+    if (shift <= 0) {
+        M = P << (-shift);                             /* exact: fewer than 9 bits */
+    } else {
+        M = P >> shift;
+        unsigned __int128 rest = P - (M << shift);
+        unsigned __int128 half = (unsigned __int128)1 << (shift - 1);
+        if (rest > half || (rest == half && (M & 1)))
+            M += 1;                                    /* may reach 2^8: still exact below */
+    }
+    double mag = ldexp((double)M, u);                  /* exact: M <= 256 */
+    float f = mag >= 0x1p128 ? INFINITY : (float)mag;  /* exact when finite */
+    uint32_t bits;
+    memcpy(&bits, &f, sizeof bits);
+    return (uint16_t)((bits >> 16) | (neg ? 0x8000u : 0u));
+}
 
 void or_dequant_sum(const uint8_t *q, int32_t nranks, int64_t n, int fmt, float scale,
                     uint16_t *out)
 {
-    const float sinv = 1.0f / scale;
+    const float sinv = 1.0f / scale;                   /* binary32 divide */
+    int se;
+    const float sm = frexpf(sinv, &se);                /* sinv = sm * 2^se, 0.5 <= |sm| < 1 */
+    const int64_t sig = (int64_t)ldexpf(fabsf(sm), 24); /* 24-bit integer significand */
+    const int sneg = sinv < 0.0f;
+    const int g = quantum_exp(fmt);
 #pragma omp parallel for schedule(static)
     for (int64_t i = 0; i < n; ++i) {
-        double acc = 0.0;
-        for (int32_t r = 0; r < nranks; ++r)
-            acc += or_fp8_decode(q[(int64_t)r * n + i], fmt);
-        out[i] = or_f32_to_bf16((float)(acc * (double)sinv));
+        int64_t acc = 0;                               /* exact: < 2^16 parts of < 2^32 quanta */
+        int nan = 0, pinf = 0, ninf = 0;
+        for (int32_t r = 0; r < nranks; ++r) {
+            double v = or_fp8_decode(q[(int64_t)r * n + i], fmt);
+            if (isnan(v))
+                nan = 1;
+            else if (v == INFINITY)
+                pinf = 1;
+            else if (v == -INFINITY)
+                ninf = 1;
+            else
+                acc += (int64_t)ldexp(v, -g);          /* exact integer count of quanta */
+        }
+        float res;
+        if (nan || (pinf && ninf)) {
+            res = NAN;
+        } else if (pinf || ninf) {
+            res = (pinf ? INFINITY : -INFINITY) * sinv; /* IEEE: NaN when sinv is 0 or NaN */
+        } else if (isnan(sinv) || isinf(sinv)) {
+            res = (float)acc * sinv;                   /* exact sign; 0 * inf = NaN */
+        } else {
+            int neg = (acc < 0) != sneg;
+            unsigned __int128 P = (unsigned __int128)(acc < 0 ? -acc : acc) *
+                                  (unsigned __int128)sig;
+            out[i] = bf16_of_exact(acc != 0 && sig != 0 ? neg : 0, P, g + se - 24);
+            continue;
+        }
+        out[i] = or_f32_to_bf16(res);
     }
 }

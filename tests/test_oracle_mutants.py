@@ -83,11 +83,19 @@ MUTANTS = {
         "        s = (float)ldexp((double)q, -margin);         /* exact, then one rounding */",
         "        s = q;"),
     "FP8 sum multiplied by the scale instead of its inverse": (
-        "out[i] = or_f32_to_bf16((float)(acc * (double)sinv));",
-        "out[i] = or_f32_to_bf16((float)(acc * (double)scale));"),
+        "const float sinv = 1.0f / scale;                   /* binary32 divide */",
+        "const float sinv = scale;"),
     "FP8 sum drops the last rank": (
-        "for (int32_t r = 0; r < nranks; ++r)\n            acc +=",
-        "for (int32_t r = 0; r + 1 < nranks; ++r)\n            acc +="),
+        "for (int32_t r = 0; r < nranks; ++r) {\n            double v = or_fp8_decode",
+        "for (int32_t r = 0; r + 1 < nranks; ++r) {\n            double v = or_fp8_decode"),
+    "FP8 sum rounds ties away from zero": (
+        "if (rest > half || (rest == half && (M & 1)))", "if (rest >= half)"),
+    "FP8 sum rounded to binary32 before BF16": (
+        "out[i] = bf16_of_exact(acc != 0 && sig != 0 ? neg : 0, P, g + se - 24);\n            continue;",
+        "res = (float)((double)acc * ldexp(1.0, g) * (double)sinv);"),
+    "FP8 sum without BF16 subnormals": (
+        "        u = -133;                                      /* the subnormal quantum 2^-133 */",
+        "        u = -126;"),
 }
 
 
