@@ -576,6 +576,38 @@ def fp8_dequant_sum(parts: torch.Tensor, fmt: int, scale: torch.Tensor, out: tor
                                 _ptr(out, torch.bfloat16, "out"), _stream(stream)))
 
 
+def fp8_shard_len(n: int, world: int) -> int:
+    """Elements per rank's shard in the FP8 all-reduce: n / world rounded up
+    to a multiple of 16 (the library's alignment unit)."""
+    per = -(-n // world)
+    return -(-per // 16) * 16
+
+
+def fp8_exchange_sum(q: torch.Tensor, shard: int, reduce_shard, group=None) -> torch.Tensor:
+    """The exchange of the FP8 all-reduce as a reduce-scatter plus an
+    all-gather, on codes every rank has cast with the one shared scale.
+
+    ``q`` is this rank's [world * shard] FP8 codes (padded with code 0, +0).
+    An all-to-all sends shard j to rank j, so every rank receives its own
+    shard from all ranks, in rank order ([world, shard]); ``reduce_shard``
+    turns those codes into the shard's reduced values ([shard], BF16); an
+    all-gather of the reduced shards gives every rank the whole result
+    ([world * shard]).  Each rank receives (world - 1) * shard FP8 bytes and
+    (world - 1) * shard BF16 values: 3 (N - 1) / N bytes per element, against
+    4 (N - 1) / N for a BF16 ring all-reduce and (N - 1) for an all-gather of
+    every rank's codes.  Uses torch.distributed."""
+    import torch.distributed as dist
+    world = dist.get_world_size(group)
+    if q.numel() != world * shard:
+        raise ValueError("q must hold world * shard codes")
+    recv = torch.empty_like(q)
+    dist.all_to_all_single(recv, q, group=group)
+    mine = reduce_shard(recv.view(world, shard))
+    full = torch.empty(world * shard, dtype=mine.dtype, device=mine.device)
+    dist.all_gather([full[r * shard:(r + 1) * shard] for r in range(world)], mine, group=group)
+    return full
+
+
 def fp8_allreduce(grad: torch.Tensor, fmt: int, margin: int = 0, group=None,
                   out: torch.Tensor | None = None) -> torch.Tensor:
     """All-reduce (sum) of a BF16 gradient [rows, cols] over the ranks of
@@ -585,9 +617,12 @@ def fp8_allreduce(grad: torch.Tensor, fmt: int, margin: int = 0, group=None,
       1. this rank's scale: amax, then the recipe formula on a one-entry history;
       2. the shared scale: all-reduce(MIN) of the scales;
       3. the cast of the gradient with the shared scale (fp8_quantize_transpose);
-      4. all-gather of the FP8 codes (1 byte per element per rank);
-      5. fp8_dequant_sum of the gathered codes into BF16.
-    Every rank ends with the same result.  Uses torch.distributed."""
+      4. reduce-scatter: all-to-all of the FP8 codes by shard, then
+         fp8_dequant_sum of this rank's shard (the exact sum of all ranks'
+         values times 1 / scale, rounded once to BF16);
+      5. all-gather of the reduced BF16 shards.
+    Every rank ends with the same result, the oracle's sum bit for bit.
+    Uses torch.distributed."""
     import torch.distributed as dist
     rows, cols = grad.shape
     n = rows * cols
@@ -600,11 +635,18 @@ def fp8_allreduce(grad: torch.Tensor, fmt: int, margin: int = 0, group=None,
     fp8_amax(grad, amax)
     fp8_scale_update(hist, amax, scale, scale_inv, fmt, margin)
     dist.all_reduce(scale, op=dist.ReduceOp.MIN, group=group)
-    q_all = torch.empty((world, n), dtype=torch.uint8, device=dev)
-    rank = dist.get_rank(group)
-    fp8_quantize_transpose(grad, scale, fmt, out=q_all[rank].view(rows, cols))
-    dist.all_gather([q_all[r] for r in range(world)], q_all[rank].clone(), group=group)
+    shard = fp8_shard_len(n, world)
+    q = torch.empty(world * shard, dtype=torch.uint8, device=dev)
+    q[n:].zero_()
+    fp8_quantize_transpose(grad, scale, fmt, out=q[:n].view(rows, cols))
+
+    def reduce_shard(parts):
+        mine = torch.empty(shard, dtype=torch.bfloat16, device=dev)
+        fp8_dequant_sum(parts, fmt, scale, mine)
+        return mine
+
+    full = fp8_exchange_sum(q, shard, reduce_shard, group)
     if out is None:
         out = torch.empty((rows, cols), dtype=torch.bfloat16, device=dev)
-    fp8_dequant_sum(q_all, fmt, scale, out)
+    out.view(-1).copy_(full[:n])
     return out

@@ -251,21 +251,22 @@ __global__ void adam_scales_kernel(const AdamArgs a) {
 
 // ------------------------------------------------ FP8 all-reduce: the sum --
 //
-// out[i] = bf16_rne(fl32(sum_r dec(q[r][i]) * fl32(1 / scale))): the parts of
-// all ranks share one scale (the minimum of the ranks' own scales), so their
-// codes can be decoded and summed directly.  The sum is exact and the product
-// is rounded in double, then to fp32 and to BF16.
+// out[i] = the exact sum_r dec(q[r][i]) times fl32(1 / scale), rounded once to
+// BF16 (nearest, ties to even; overflow to inf; gradual underflow; an exact
+// zero is +0).  The parts of all ranks share one scale (the minimum of the
+// ranks' own scales), so their codes can be decoded and summed directly.
 //
-// Every finite FP8 value is an integer number of the format's quantum (2^-9
-// for E4M3, 2^-16 for E5M2), at most 57344 * 2^16 < 2^32 of them, so the sum
-// over up to 65536 ranks is accumulated exactly in int64 through a 256-entry
-// table of quanta in shared memory (GB300's FP64 rate made a double
-// accumulation the bottleneck).  (double) sum * 2^-q is then exactly the
-// double sum of the decoded values, and folding 2^-q into the double scale
-// leaves the one rounding of the product unchanged.  Infinity and NaN codes
-// are rare: a four-codes-at-once test sends them to a path that records them,
-// and the result follows IEEE double addition (NaN, or +inf and -inf
-// together, give NaN; one infinity gives that infinity).
+// Integer arithmetic only.  Every finite FP8 value is an integer number of
+// the format's quantum (2^-9 for E4M3, 2^-16 for E5M2), below 2^32 of them,
+// so the sum over up to 65536 ranks is exact in int64 (a 256-entry table of
+// quanta in shared memory).  fl32(1 / scale) is sig * 2^es with a 24-bit
+// integer sig, so the exact result is |sum| * sig (below 2^72, two 64-bit
+// words) times 2^(es - q); it is rounded to BF16's 8 significant bits (or to
+// its subnormal quantum 2^-133) by one integer round-to-nearest-even, and
+// the BF16 bits are assembled directly.  Infinity and NaN codes are rare: a
+// four-codes-at-once test sends them to a path that records them, and they
+// follow IEEE arithmetic (a NaN code, or +inf with -inf, give NaN; one
+// infinity gives that infinity times the factor).
 
 template <int FMT>
 __device__ __forceinline__ int64_t fp8_quanta(uint32_t c) {
@@ -279,6 +280,80 @@ __device__ __forceinline__ int64_t fp8_quanta(uint32_t c) {
     return (c & 0x80u) ? -mag : mag;
 }
 
+constexpr uint32_t kBf16Nan = 0x7FC0u, kBf16Inf = 0x7F80u;
+
+// The factor fl32(1 / scale) as sig * 2^es (sig < 2^24; 0 for a zero factor)
+// with its sign and non-finite classes.
+struct DqFactor {
+    uint64_t sig;
+    int es;
+    uint32_t sign;      // 0x8000 when negative
+    bool is_nan, is_inf;
+};
+
+__device__ __forceinline__ DqFactor dq_factor(float sinv) {
+    const uint32_t b = __float_as_uint(sinv);
+    const uint32_t e = (b >> 23) & 0xFFu, m = b & 0x7FFFFFu;
+    DqFactor f;
+    f.sign = (b >> 16) & 0x8000u;
+    f.is_nan = e == 0xFFu && m != 0u;
+    f.is_inf = e == 0xFFu && m == 0u;
+    f.sig = e == 0u ? m : (m | 0x800000u);
+    f.es = e == 0u ? -149 : static_cast<int>(e) - 150;
+    return f;
+}
+
+// BF16 bits of acc * 2^-qexp * factor, exactly rounded (finite factor).
+template <int FMT>
+__device__ __forceinline__ uint32_t bf16_of_scaled_sum(int64_t acc, const DqFactor &f) {
+    constexpr int QEXP = FMT == 0 ? -9 : -16;
+    if (acc == 0 || f.sig == 0) return 0u;
+    const uint32_t sign = ((acc < 0) ? 0x8000u : 0u) ^ f.sign;
+    const uint64_t a = static_cast<uint64_t>(acc < 0 ? -acc : acc);
+    const uint64_t lo = a * f.sig, hi = __umul64hi(a, f.sig);   // |acc| * sig < 2^72
+    const int E = f.es + QEXP;                                  // value = (hi:lo) * 2^E
+    const int nb = hi ? 128 - __clzll(static_cast<long long>(hi))
+                      : 64 - __clzll(static_cast<long long>(lo));
+    int u = nb - 1 + E - 7;               // quantum of an 8-significant-bit result
+    if (u < -133) u = -133;               // BF16's subnormal quantum
+    const int shift = u - E;
+    uint64_t M;
+    if (shift <= 0) {
+        M = lo << (-shift);               // exact (then fewer than 9 bits)
+    } else {
+        uint64_t rest, half;
+        if (shift < 64) {
+            M = (lo >> shift) | (hi << (64 - shift));
+            rest = lo & ((uint64_t(1) << shift) - 1u);
+            half = uint64_t(1) << (shift - 1);
+        } else {                          // shift == 64 (|acc| * sig has 72 bits)
+            M = hi;
+            rest = lo;
+            half = uint64_t(1) << 63;
+        }
+        if (rest > half || (rest == half && (M & 1u))) ++M;   // M may become 2^8
+    }
+    // biased exponent u + 134 over a 7-bit mantissa M - 128; a carry to
+    // M = 256 moves into the exponent, and the subnormal case (u = -133)
+    // reduces to bits = M
+    uint32_t bits = static_cast<uint32_t>((u + 134) * 128 + static_cast<int>(M) - 128);
+    if (u + 134 >= 255 || bits >= kBf16Inf) bits = kBf16Inf;
+    return bits | sign;
+}
+
+template <int FMT>
+__device__ __forceinline__ uint32_t dq_finish(int64_t acc, uint32_t fe, const DqFactor &f) {
+    if (fe == 0u) {
+        if (f.is_nan) return kBf16Nan;
+        if (f.is_inf)   // a finite sum times an infinite factor: 0 * inf is NaN
+            return acc == 0 ? kBf16Nan : (kBf16Inf | (((acc < 0) ? 0x8000u : 0u) ^ f.sign));
+        return bf16_of_scaled_sum<FMT>(acc, f);
+    }
+    if ((fe & 1u) || fe == 6u) return kBf16Nan;        // a NaN code, or +inf with -inf
+    if (f.is_nan || f.sig == 0) return kBf16Nan;       // inf * NaN, inf * 0
+    return kBf16Inf | (((fe & 4u) ? 0x8000u : 0u) ^ f.sign);
+}
+
 template <int FMT>
 __global__ void __launch_bounds__(256) dequant_sum_kernel(const uint8_t *__restrict__ q,
                                                           int nranks, int64_t n,
@@ -289,8 +364,7 @@ __global__ void __launch_bounds__(256) dequant_sum_kernel(const uint8_t *__restr
     __syncthreads();
     pdl_wait();
     pdl_trigger();
-    // 2^-q * fl32(1/scale), exact in double
-    const double k = static_cast<double>(__fdiv_rn(1.0f, *scale)) * (FMT == 0 ? 0x1p-9 : 0x1p-16);
+    const DqFactor fac = dq_factor(__fdiv_rn(1.0f, *scale));
     const uint32_t smask = FMT == 0 ? 0x7F7F7F7Fu : 0x7C7C7C7Cu;   // bits that mark a special
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x * 8;
     for (int64_t i = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) * 8; i < n;
@@ -332,22 +406,9 @@ __global__ void __launch_bounds__(256) dequant_sum_kernel(const uint8_t *__restr
         }
         uint32_t o[4];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            float y[2];
-#pragma unroll
-            for (int t = 0; t < 2; ++t) {
-                const int e = 2 * j + t;
-                const uint32_t fe = (flags >> (3 * e)) & 7u;
-                if (fe == 0u)
-                    y[t] = __double2float_rn(static_cast<double>(acc[e]) * k);
-                else if ((fe & 1u) || fe == 6u)
-                    y[t] = __int_as_float(0x7FFFFFFF);
-                else
-                    y[t] = (fe & 2u) ? __int_as_float(0x7F800000) : __int_as_float(0xFF800000);
-            }
-            const __nv_bfloat162 b = __floats2bfloat162_rn(y[0], y[1]);
-            o[j] = *reinterpret_cast<const uint32_t *>(&b);
-        }
+        for (int j = 0; j < 4; ++j)
+            o[j] = dq_finish<FMT>(acc[2 * j], (flags >> (6 * j)) & 7u, fac) |
+                   (dq_finish<FMT>(acc[2 * j + 1], (flags >> (6 * j + 3)) & 7u, fac) << 16);
         *reinterpret_cast<uint4 *>(out + i) = make_uint4(o[0], o[1], o[2], o[3]);
     }
 }

@@ -98,43 +98,61 @@ def _fp8_worker(rank, world, port, grads, out_q):
     import datetime
 
     import oracle as o
+    from fp8_mixed_precision_amax_gb300.api import fp8_exchange_sum, fp8_shard_len
     os.environ["MASTER_ADDR"] = "127.0.0.1"
     os.environ["MASTER_PORT"] = str(port)
     dist.init_process_group("gloo", rank=rank, world_size=world,
                             timeout=datetime.timedelta(seconds=10))
     try:
         # the exchange of the FP8 all-reduce: MIN of the ranks' own scales,
-        # then the FP8 codes of every rank, summed the same way everywhere
+        # then the library's reduce-scatter + all-gather of the FP8 codes,
+        # with the oracle's sum on each rank's shard (CPU tensors)
         s = torch.tensor([float(o.local_scale(grads[rank], o.E5M2, 0))])
         dist.all_reduce(s, op=dist.ReduceOp.MIN)
         sg = np.float32(s.item())
-        q, _ = o.quantize(grads[rank].reshape(1, -1), sg, o.E5M2, transpose=False)
-        parts = [torch.empty(q.size, dtype=torch.uint8) for _ in range(world)]
-        dist.all_gather(parts, torch.from_numpy(q.reshape(-1)))
-        out = o.dequant_sum(np.stack([p.numpy() for p in parts]), o.E5M2, sg)
-        out_q.put((rank, sg, out))
+        n = grads[rank].size
+        shard = fp8_shard_len(n, world)
+        q = np.zeros(world * shard, np.uint8)
+        q[:n] = o.quantize(grads[rank].reshape(1, -1), sg, o.E5M2, transpose=False)[0][0]
+        seen = []
+
+        def reduce_shard(parts):
+            seen.append(parts.shape)
+            bits = o.dequant_sum(parts.numpy(), o.E5M2, sg)
+            return torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16)
+
+        full = fp8_exchange_sum(torch.from_numpy(q), shard, reduce_shard)
+        out = full.view(torch.int16).numpy().view(np.uint16)[:n]
+        out_q.put((rank, sg, out, seen))
     finally:
         dist.destroy_process_group()
 
 
-def test_fp8_allreduce_exchange_shares_the_minimum_scale():
+@pytest.mark.parametrize("world,n", [(3, 4096), (2, 4096 + 16), (3, 1000 * 16)])
+def test_fp8_allreduce_exchange_shares_the_minimum_scale(world, n):
     """The exchange step of the FP8 all-reduce (wiki note, 'per-tensor scaling
-    is the key'): three gloo ranks agree on s'_g = min(s'_i) and reach the
-    same sum, equal to the single-process reference."""
+    is the key'): gloo ranks agree on s'_g = min(s'_i), each sums only its
+    own shard of every rank's codes (padded to a multiple of 16), and the
+    all-gather of the shards equals the single-process reference sum."""
     import oracle as o
-    rng = np.random.default_rng(3)
-    grads = [torch.from_numpy((rng.standard_normal(4096) * m).astype(np.float32))
+    from fp8_mixed_precision_amax_gb300.api import fp8_shard_len
+    rng = np.random.default_rng(3 + world)
+    grads = [torch.from_numpy((rng.standard_normal(n) * m).astype(np.float32))
              .to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
-             for m in (1e-3, 3e-2, 5e-4)]
+             for m in (1e-3, 3e-2, 5e-4)[:world]]
     ctx = mp.get_context("spawn")
     q = ctx.Queue()
     port = _free_port()
-    procs = [ctx.Process(target=_fp8_worker, args=(r, 3, port, grads, q)) for r in range(3)]
+    procs = [ctx.Process(target=_fp8_worker, args=(r, world, port, grads, q))
+             for r in range(world)]
     for p in procs:
         p.start()
     res = [q.get(timeout=60) for _ in procs]
     for p in procs:
         p.join(timeout=60)
     ref, sg, _ = o.fp8_allreduce(grads, o.E5M2)
-    for rank, s, out in res:
+    shard = fp8_shard_len(n, world)
+    assert shard % 16 == 0 and world * shard >= n > (world - 1) * shard - 16 * world
+    for rank, s, out, seen in res:
         assert s == sg and np.array_equal(out, ref), rank
+        assert seen == [(world, shard)], rank

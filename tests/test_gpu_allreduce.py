@@ -1,11 +1,14 @@
 """GPU parity of the FP8 all-reduce with one shared scale (wiki note, bullet
 "per-tensor scaling is the key": s'_g = min(s'_1 .. s'_N)).
 
-* fp8_dequant_sum against the oracle, bit-exact, for 1..8 parts;
+* fp8_dequant_sum against the oracle (the exact sum times 1 / scale, rounded
+  once to BF16), bit-exact, for 1..8 parts, special codes, extreme and
+  non-finite scales, and a case where rounding twice would differ;
 * the whole product path (fp8_allreduce: amax, own scale, MIN all-reduce,
-  cast, all-gather of FP8 codes, decode-and-sum) as 2 and 3 gloo ranks that
-  share cuda:0 -- their kernels never wait on one another, the exchange runs
-  on the host -- against the oracle's all-reduce, bit-exact on every rank."""
+  cast, all-to-all of FP8 code shards, decode-and-sum of this rank's shard,
+  all-gather of the BF16 shards) as 2 and 3 gloo ranks that share cuda:0 --
+  their kernels never wait on one another, the exchange runs on the host --
+  against the oracle's all-reduce, bit-exact on every rank."""
 import os
 import socket
 
@@ -39,6 +42,23 @@ def test_dequant_sum_bit_exact(fmt, nranks):
     assert np.array_equal(_u16(out), o.dequant_sum(parts, fmt, s))
 
 
+def test_dequant_sum_rounds_once():
+    """E5M2 parts 57344 + 128 + 2^-16 at scale 1: the exact sum lies just
+    above the midpoint between the BF16 neighbours 57344 and 57600, so one
+    rounding gives 57600 (0x4761); the parts without 2^-16 are the midpoint
+    itself, which ties to the even 57344 (0x4760)."""
+    import fp8_mixed_precision_amax_gb300 as f
+    parts = np.zeros((3, 16), np.uint8)
+    parts[:, 0] = [0x7B, 0x58, 0x01]
+    parts[:2, 1] = [0x7B, 0x58]
+    out = torch.empty(16, dtype=torch.bfloat16, device="cuda")
+    f.fp8_dequant_sum(torch.from_numpy(parts).cuda(), o.E5M2, torch.ones(1, device="cuda"), out)
+    torch.cuda.synchronize()
+    got = _u16(out)
+    assert got[0] == 0x4761 and got[1] == 0x4760
+    assert np.array_equal(got, o.dequant_sum(parts, o.E5M2, np.float32(1.0)))
+
+
 def _same_bf16(a, b):
     """Equal BF16 bits, NaN compared as a class."""
     nan_a = ((a & 0x7F80) == 0x7F80) & ((a & 0x7F) != 0)
@@ -48,10 +68,11 @@ def _same_bf16(a, b):
 
 @pytest.mark.parametrize("fmt", [o.E4M3, o.E5M2])
 def test_dequant_sum_specials_and_extremes(fmt):
-    """Infinities and NaN among the parts follow IEEE double addition (NaN,
-    or +inf with -inf, give NaN); 64 ranks of the largest magnitudes and
-    mixed signs stay exact; a 4 M-element case runs several grid-stride
-    passes of the kernel."""
+    """Infinities and NaN among the parts follow IEEE arithmetic (NaN, or
+    +inf with -inf, give NaN); 64 ranks of the largest magnitudes and mixed
+    signs stay exact; a 4 M-element case runs several grid-stride passes of
+    the kernel; scales whose results overflow BF16, land in its subnormal
+    range or underflow, and zero, infinite, negative and NaN scales."""
     import fp8_mixed_precision_amax_gb300 as f
     rng = np.random.default_rng(7 + fmt)
     table = o.fp8_decode_table(fmt)
@@ -73,7 +94,9 @@ def test_dequant_sum_specials_and_extremes(fmt):
     cases.append(np.where(rng.random((64, 2048)) < 0.5, top, top | 0x80).astype(np.uint8))
     cases.append(np.full((64, 1024), top, np.uint8))
     cases.append(rng.choice(finite, size=(3, (1 << 22) + 16)))
-    scales = [np.float32(1e-30), np.float32(3e38), np.float32(1e36), np.float32(2.0 ** -100)]
+    scales = [np.float32(1e-30), np.float32(3e38), np.float32(1e36), np.float32(2.0 ** -100),
+              np.float32(2.0 ** -125 * 1.3), np.float32(1e-45), np.float32(0.0),
+              np.float32(np.inf), np.float32(-3.0), np.float32(np.nan), np.float32(2.0 ** 120)]
     for ci, parts in enumerate(cases):
         s = np.float32(10.0 ** rng.uniform(-4, 2))
         out = torch.empty(parts.shape[1], dtype=torch.bfloat16, device="cuda")
