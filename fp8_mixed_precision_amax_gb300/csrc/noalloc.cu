@@ -14,6 +14,9 @@
 // library holds it (64 MiB) until the process exits.  In host code the
 // array's name is only a host-side stand-in, not a device address, so its
 // device address is looked up once per device with cudaGetSymbolAddress.
+// That address belongs to the device's primary context: after a
+// cudaDeviceReset of a device this entry point must not be called again on
+// that device in the same process.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -49,7 +52,9 @@ fp8_status fp8_linear_bwd_noalloc(const void *dY, int64_t M, int64_t N, int64_t 
                                   void *stream) {
     const fp8k::CallRange range("fp8_linear_bwd_noalloc");
     char msg[256];
-    if (M < 0 || N < 0 || (M != 0 && N > kMaxElems / M)) {
+    // Only the work-area limit is checked here; negative or misaligned sizes
+    // and bad pointers are reported by fp8_linear_bwd's own checks below.
+    if (M > 0 && N > 0 && N > kMaxElems / M) {
         snprintf(msg, sizeof msg,
                  "fp8_linear_bwd_noalloc: M=%lld x N=%lld exceeds the fixed work area of "
                  "%lld elements; use fp8_linear_bwd with caller-provided buffers",

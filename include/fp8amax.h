@@ -393,11 +393,14 @@ fp8_status fp8_dequant_sum(const uint8_t *parts, int32_t nranks, int64_t n, int3
  * for the whole device).
  *   Arguments as fp8_linear_bwd, without dY8 / dY8t.
  *   Limit: M * N <= 2^25 (33,554,432) elements; larger sizes return
- *   FP8_ERR_ARG and nothing is enqueued.
+ *   FP8_ERR_ARG ("exceeds the fixed work area") and nothing is enqueued.
+ *   Other argument errors are those of fp8_linear_bwd.
  *   Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
  *   Set-up: the first call on a device looks up the array's device address
  *   (cudaGetSymbolAddress) with that device current; make that first call
- *   before any stream capture.
+ *   before any stream capture.  The address belongs to the device's primary
+ *   context: after cudaDeviceReset on a device, do not call this function on
+ *   that device again in the same process.
  *   All calls share the one array: calls that overlap on the GPU (on
  *   different streams, or from different threads without ordering) race on
  *   it; calls ordered on one stream do not.  Every call overwrites the part it
