@@ -4,16 +4,26 @@
 One step = one pass of the whole hot path over one batch: the fused amax +
 scaled cast + transposed copy of X, W and dY, the fprop / dgrad / wgrad FP8
 GEMMs with the dequant + amax epilogue, and the delayed-scaling update of all
-five tensors (Fp8Linear.step).  The headline workload is the 7B-shaped MLP
-up-projection (M = 8192 tokens, K = 4096, N = 11008; HYBRID, history 1024,
-margin 0).  Inputs are synthetic and seeded (fp8_workloads.py) and resident in
-HBM; two (X, dY) batches alternate, each step reading more than the 129 MB L2.
+five tensors (Fp8Linear.step).  The headline workload is the largest layer,
+the 70B-shaped MLP (M = 8192 tokens, K = 8192, N = 28672; Student-t X with
+outlier channels; HYBRID, history 1024, margin 1).  Inputs are synthetic and
+seeded (fp8_workloads.py) and resident in HBM; two (X, dY) batches alternate,
+each step reading more than the 129 MB L2.  Under torchrun (N > 1) each rank
+is a data-parallel replica on its own tokens: the five amaxes are combined by
+an all-reduce(MAX) and dW by the FP8 all-reduce (fp8_allreduce) every step.
 
 Prints ONE JSON line (rank 0).  Metric: layer TFLOPS = 6 M N K per step over
 the device time of K steps (CUDA events, max over ranks).  Added keys:
   roofline      the dominant kernel (the tcgen05 GEMM), achieved TFLOP/s vs the
-                FP8 peak derived from MEASURED_PEAKS.json (bf16 x 2)
+                FP8 peak derived from MEASURED_PEAKS.json (bf16 x 2), and vs
+                SMs x 16384 FLOP/clk x the SM clock sampled while timing
+                (peak_clock) and x the maximum SM clock (peak_boost)
   cast_roofline the fused cast kernels, achieved GB/s vs measured HBM copy
+  sustained     the same step back to back for a few seconds, with its own
+                clock record (the power-capped regime)
+  sweep_2e28    the standalone quantize sweep's largest tensor (2^28 BF16
+                elements): amax and cast + transposed copy GB/s, L2 flushed
+  mlp7b         the 7B-shaped layer step (M 8192, K 4096, N 11008)
   e2e           same metric with X, dY copied in from pinned host memory and
                 Y, dX, dW copied back every step
   cpu_baseline  the CPU oracle timed on a sample of the same layer
@@ -44,6 +54,7 @@ import fp8_workloads as wl  # noqa: E402
 
 METRIC = "FP8 linear fwd+bwd TFLOPS & % GB300 FP8 peak; cast/amax GB/s % of HBM peak"
 FP8_OVER_BF16 = 2.0       # nominal dense FP8 / BF16 tensor-core ratio (4.5 / 2.25 PFLOP/s)
+FP8_FLOP_PER_CLK_SM = 16384   # dense FP8 tensor-core FLOP per clock per SM (2 x BF16's 8192)
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -53,9 +64,13 @@ def parse_args():
     p.add_argument("--steps", type=int, default=200)
     p.add_argument("--warmup", type=int, default=10)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    p.add_argument("--workload", default="mlp7b", choices=["mlp7b", "mlp70b", "drift", "tiny"])
+    p.add_argument("--workload", default="mlp70b", choices=["mlp7b", "mlp70b", "drift", "tiny"])
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--sustained-seconds", type=float, default=3.0,
+                   help="length of the back-to-back sustained loop (0: skip)")
+    p.add_argument("--no-extras", action="store_true",
+                   help="skip the mlp7b and sweep_2e28 keys")
     p.add_argument("--secondary", action="store_true",
                    help="also time the 70B-shaped layer, the cast sweep and the other "
                         "kernels of the path (extra keys)")
@@ -219,7 +234,13 @@ def gemm_traffic(workload: str):
     return d.get("bytes_per_launch_mean")
 
 
-def run_layer_bench(f, w: wl.Workload, args, world, pk, peak_kind):
+def clock_peak(tflop_per_mhz: float, mhz):
+    """Dense FP8 tensor peak at an SM clock, TFLOP/s (None without a clock)."""
+    return None if not mhz else tflop_per_mhz * mhz
+
+
+def run_layer_bench(f, w: wl.Workload, args, world, pk, peak_kind, sustained_s: float = 0.0,
+                    e2e: bool = True):
     dev = torch.device("cuda")
     W = wl.layer_weight(w, dev)
     xs = [wl.layer_x(w, s, dev) for s in (0, 1)]
@@ -227,16 +248,28 @@ def run_layer_bench(f, w: wl.Workload, args, world, pk, peak_kind):
     lin = f.Fp8Linear(W, w.M, f.Recipe(margin=w.margin, history_len=w.history_len,
                                        hybrid=w.hybrid))
     stream = torch.cuda.current_stream()
-    allreduce = None
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    tflop_per_mhz = sms * FP8_FLOP_PER_CLK_SM * 1e6 / 1e12
+    launches_per_step = 5
+    exchange = None
     if world > 1:
-        # data-parallel replicas agree on scales: MAX of the five amaxes
-        allreduce = lambda: f.allreduce_amax(lin.meta)
+        # data-parallel replicas: MAX of the five amaxes so every replica
+        # derives the same scales, and the FP8 all-reduce of dW (amax, own
+        # scale, MIN of the scales, cast, all-to-all of code shards,
+        # decode-and-sum of this rank's shard, all-gather of BF16 shards)
+        dW_sum = torch.empty_like(lin.dW)
+        fg_w = f.E5M2 if w.hybrid else f.E4M3
+        launches_per_step += 4          # amax, scale, cast, decode-and-sum
+
+        def exchange():
+            f.allreduce_amax(lin.meta)
+            f.fp8_allreduce(lin.dW, fg_w, 0, out=dW_sum)
 
     def step(i):
         lin.forward(xs[i % 2])
         lin.backward(dys[i % 2])
-        if allreduce:
-            allreduce()
+        if exchange:
+            exchange()
         lin.update()
 
     for i in range(args.warmup):
@@ -244,13 +277,13 @@ def run_layer_bench(f, w: wl.Workload, args, world, pk, peak_kind):
     torch.cuda.synchronize()
     f.fp8_sync_status()
 
-    def timed(run_step):
+    def timed(run_step, steps):
         barrier(world)
         torch.cuda.synchronize()
         t0 = torch.cuda.Event(enable_timing=True)
         t1 = torch.cuda.Event(enable_timing=True)
         t0.record(stream)
-        for i in range(args.steps):
+        for i in range(steps):
             run_step(i)
         t1.record(stream)
         torch.cuda.synchronize()
@@ -260,7 +293,7 @@ def run_layer_bench(f, w: wl.Workload, args, world, pk, peak_kind):
     clocks = ClockSampler()
     clocks.start()
     time.sleep(0.25)
-    ms_eager = timed(step)
+    ms_eager = timed(step, args.steps)
     graphs = None
     if world == 1:
         # the same step recorded once per input batch and replayed
@@ -268,7 +301,7 @@ def run_layer_bench(f, w: wl.Workload, args, world, pk, peak_kind):
         for i in range(3):
             graphs[i % 2].replay()
         torch.cuda.synchronize()
-        ms_graph = timed(lambda i: graphs[i % 2].replay())
+        ms_graph = timed(lambda i: graphs[i % 2].replay(), args.steps)
         ms = min(ms_eager, ms_graph)
     else:
         ms_graph, ms = None, ms_eager
@@ -322,6 +355,8 @@ def run_layer_bench(f, w: wl.Workload, args, world, pk, peak_kind):
     cast_bytes = {"cast_XW": 4 * M * K + 4 * N * K, "cast_dY": 4 * M * N}
     cast_gbs = sum(cast_bytes.values()) / (sum(cast_ms.values()) / 1e3) / 1e9
     traffic = gemm_traffic(w.name)
+    pc = clock_peak(tflop_per_mhz, clk.get("sm_mhz"))
+    pb = clock_peak(tflop_per_mhz, clk.get("sm_max_mhz"))
     res = {
         "value": value, "ms_per_step": ms / args.steps,
         "launch": "CUDA graph replay" if graphs and ms == ms_graph else "eager",
@@ -330,7 +365,14 @@ def run_layer_bench(f, w: wl.Workload, args, world, pk, peak_kind):
         "roofline": {"bound": "tensor", "kernel": "gemm_tn_kernel", "achieved": achieved,
                      "peak": fp8_peak, "unit": "TFLOP/s", "frac": achieved / fp8_peak,
                      "traffic": traffic,
-                     "peak_basis": f"{peak_kind} bf16 burst {pk['bf16_tflops']} x {FP8_OVER_BF16}",
+                     "peak_basis": f"{peak_kind} bf16 burst {pk['bf16_tflops']} x {FP8_OVER_BF16} "
+                                   f"(of {peak_kind})",
+                     "peak_clock": {"value": pc, "frac": achieved / pc if pc else None,
+                                    "sm_mhz": clk.get("sm_mhz"), "sms": sms,
+                                    "basis": f"{sms} SMs x {FP8_FLOP_PER_CLK_SM} FLOP/clk x the "
+                                             "median SM clock sampled while timing"},
+                     "peak_boost": {"value": pb, "frac": achieved / pb if pb else None,
+                                    "sm_mhz": clk.get("sm_max_mhz")},
                      "launches_per_step": {"gemm_fprop": "fprop", "gemm_bwd": "dgrad+wgrad"},
                      "per_launch_ms": gemm_ms,
                      "per_launch_tflops": {k: gemm_flops[k] / (v / 1e3) / 1e12
@@ -343,13 +385,38 @@ def run_layer_bench(f, w: wl.Workload, args, world, pk, peak_kind):
                                            for k, v in cast_ms.items()},
                           "update_us": upd_ms * 1e3},
         "clocks": clk,
-        "gpu_launches": 5 * args.steps,
+        "gpu_launches": launches_per_step * args.steps,
         "breakdown_ms": {**gemm_ms, **cast_ms, "update": upd_ms},
     }
 
-    if not args.no_e2e:
+    if sustained_s > 0:
+        res["sustained"] = run_sustained(graphs, step, timed, sustained_s, ms / args.steps, flops,
+                                         world, tflop_per_mhz, pk)
+    if e2e:
         res["e2e"] = run_e2e(f, lin, xs[0], dys[0], args, world, flops)
     return res
+
+
+def run_sustained(graphs, step, timed, seconds, ms_step, flops, world, tflop_per_mhz, pk):
+    """The same step back to back for about ``seconds`` (graph replays at
+    N = 1), timed with CUDA events around the whole loop, with its own clock
+    record: the regime where the GPU runs at its power limit."""
+    n = max(10, int(seconds * 1e3 / max(ms_step, 1e-3)))
+    run = (lambda i: graphs[i % 2].replay()) if graphs else step
+    clocks = ClockSampler()
+    clocks.start()
+    time.sleep(0.25)
+    ms = timed(run, n)
+    clk = clocks.stop()
+    value = world * n * flops / (ms / 1e3) / 1e12
+    pc = clock_peak(tflop_per_mhz, clk.get("sm_mhz"))
+    return {"value": value, "unit": "TFLOPS", "ms_per_step": ms / n, "steps": n,
+            "seconds": ms / 1e3, "clocks": clk,
+            "step_frac_of_peak_clock": value / world / pc if pc else None,
+            "step_frac_of_sustained_bf16_x2": value / world / (pk["bf16_tflops_sustained"]
+                                                               * FP8_OVER_BF16),
+            "note": "whole step (casts, GEMMs, update) against the dense FP8 peak at the "
+                    "sampled clock and against the measured sustained BF16 peak x 2"}
 
 
 def run_e2e(f, lin, X, dY, args, world, flops):
@@ -517,7 +584,7 @@ def run_reference(args, world, rank):
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": tt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64 (oracle, exact FP8 decode)", "data": "synthetic",
-            "config": workload_config(w),
+            "config": workload_config(w, world),
             "cpu_baseline": {"kind": "oracle", "cores": o.num_threads(), "sample": sample,
                              "value": value, "unit": "TFLOPS",
                              "affinity_cores": len(os.sched_getaffinity(0))},
@@ -525,14 +592,61 @@ def run_reference(args, world, rank):
                     "d2h_bytes_per_step": 0}}
 
 
-def workload_config(w: wl.Workload):
+def workload_config(w: wl.Workload, world: int = 1):
     return {"workload": f"{w.name}: single FP8 linear fwd+bwd+update, M={w.M} tokens, K={w.K}, "
                         f"N={w.N}, {'HYBRID' if w.hybrid else 'E4M3'}, history {w.history_len}, "
                         f"margin {w.margin}",
             "M": w.M, "K": w.K, "N": w.N, "x": w.x_kind, "history_len": w.history_len,
             "margin": w.margin, "format": "HYBRID" if w.hybrid else "E4M3",
             "l2": "inputs larger than L2: X, W, dY = %d MB read per step, two batches alternate"
-                  % ((2 * w.M * w.K + 2 * w.N * w.K + 2 * w.M * w.N) // 2 ** 20)}
+                  % ((2 * w.M * w.K + 2 * w.N * w.K + 2 * w.M * w.N) // 2 ** 20),
+            "parallelism": f"dp{world} replicas" + (" + amax MAX all-reduce + FP8 dW all-reduce"
+                                                    if world > 1 else "")}
+
+
+def sweep_line(f, pk, n: int = 28, reps: int = 12):
+    """The standalone quantize sweep's largest tensor: 2^n BF16 elements
+    ((2^n / 4096) x 4096, N(0, 1) with 0.1 % of elements x 100).  Timed per
+    launch with CUDA events, L2 flushed (a 256 MB write) before each, median
+    of ``reps``: the amax (2 B/element), the cast + transposed copy to E4M3
+    and to E5M2 (4 B/element, scale 1), and the just-in-time sequence amax ->
+    scale -> cast (fp8_quantize_transpose_current, 6 B/element)."""
+    x = wl.sweep_tensor(n, device="cuda")
+    rows, cols = x.shape
+    ne = rows * cols
+    o8 = torch.empty((rows, cols), dtype=torch.uint8, device="cuda")
+    o8t = torch.empty((cols, rows), dtype=torch.uint8, device="cuda")
+    am = torch.empty(1, device="cuda")
+    one = torch.ones(1, device="cuda")
+    sc, si = torch.ones(1, device="cuda"), torch.ones(1, device="cuda")
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    ops = {"amax": (2, lambda: f.fp8_amax(x, am)),
+           "cast_e4m3": (4, lambda: f.fp8_quantize_transpose(x, one, f.E4M3, o8, o8t)),
+           "cast_e5m2": (4, lambda: f.fp8_quantize_transpose(x, one, f.E5M2, o8, o8t)),
+           "just_in_time_e4m3": (6, lambda: f.fp8_quantize_transpose_current(
+               x, f.E4M3, 0, am, sc, si, o8, o8t))}
+    times = {k: [] for k in ops}
+    for r in range(reps + 2):
+        for k, (_, fn) in ops.items():
+            flush.zero_()
+            s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s0.record()
+            fn()
+            s1.record()
+            torch.cuda.synchronize()
+            if r >= 2:
+                times[k].append(s0.elapsed_time(s1))
+    f.fp8_sync_status()
+    out = {"elements": ne, "peak_gbs": pk["hbm_gbs"], "unit": "GB/s",
+           "note": "event-timed per launch, L2 flushed before each, median of %d" % reps}
+    for k, (bpe, _) in ops.items():
+        ms = statistics.median(times[k])
+        gbs = bpe * ne / (ms / 1e3) / 1e9
+        out[k] = {"us": ms * 1e3, "gbs": gbs, "frac": gbs / pk["hbm_gbs"],
+                  "bytes_per_element": bpe}
+    del x, o8, o8t, flush
+    torch.cuda.empty_cache()
+    return out
 
 
 SECONDARY_PARTS = ("mlp70b", "cast_sweep", "layernorm_cast", "fp8_adam", "jit_scaling",
@@ -809,21 +923,34 @@ def main():
     import fp8_mixed_precision_amax_gb300 as f
     pk, peak_kind = peaks()
     w = wl.WORKLOADS[args.workload]
-    r = run_layer_bench(f, w, args, world, pk, peak_kind)
+    r = run_layer_bench(f, w, args, world, pk, peak_kind,
+                        sustained_s=args.sustained_seconds if world == 1 else 0.0,
+                        e2e=not args.no_e2e)
     line = {
         "metric": METRIC, "value": r["value"], "unit": "TFLOPS", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": r["ms_per_step"],
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "fp8 e4m3/e5m2 operands, f32 accumulate, bf16 out",
         "data": "synthetic (seeded fp8_workloads, resident in HBM)",
-        "config": {**workload_config(w), "parallelism": f"dp{world} replicas"
-                   + (" + amax MAX all-reduce" if world > 1 else "")},
+        "config": workload_config(w, world),
         "launch": r["launch"], "ms_per_step_eager": r["ms_per_step_eager"],
         "ms_per_step_graph": r["ms_per_step_graph"],
         "roofline": r["roofline"], "cast_roofline": r["cast_roofline"], "clocks": r["clocks"],
         "gpu_launches": r["gpu_launches"], "breakdown_ms": r["breakdown_ms"],
         "peaks_source": peak_kind,
     }
+    if "sustained" in r:
+        line["sustained"] = r["sustained"]
+    if world == 1 and not args.no_extras:
+        line["sweep_2e28"] = sweep_line(f, pk)
+        if w.name != "mlp7b":
+            sub = argparse.Namespace(**{**vars(args), "steps": max(args.steps, 20)})
+            r7 = run_layer_bench(f, wl.WORKLOADS["mlp7b"], sub, 1, pk, peak_kind, e2e=False)
+            line["mlp7b"] = {"value": r7["value"], "unit": "TFLOPS",
+                             "ms_per_step": r7["ms_per_step"], "steps": sub.steps,
+                             "config": workload_config(wl.WORKLOADS["mlp7b"])["workload"],
+                             "roofline": r7["roofline"], "cast_roofline": r7["cast_roofline"],
+                             "clocks": r7["clocks"]}
     if "e2e" in r:
         line["e2e"] = r["e2e"]
     if args.secondary and rank == 0:

@@ -27,6 +27,31 @@ def test_reference_arm_prints_one_contract_line():
     assert d["e2e"]["value"] == d["value"] and d["cpu_baseline"]["value"] == d["value"]
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
     assert d["config"]["workload"].startswith("tiny")
+    # the reference arm's config is the one this build's line carries
+    sys.path.insert(0, ROOT)
+    import bench
+    import fp8_workloads as wl
+    assert d["config"] == bench.workload_config(wl.WORKLOADS["tiny"], 1)
+    assert d["config"]["parallelism"] == "dp1 replicas"
+
+
+def test_headline_defaults_to_the_largest_layer():
+    """With no flags the headline is the 70B-shaped layer (M 8192, K 8192,
+    N 28672), the largest single-GPU configuration."""
+    sys.path.insert(0, ROOT)
+    import bench
+    old = sys.argv
+    try:
+        sys.argv = ["bench.py"]
+        args = bench.parse_args()
+    finally:
+        sys.argv = old
+    assert args.workload == "mlp70b" and args.gpus == 1
+    import fp8_workloads as wl
+    w = wl.WORKLOADS[args.workload]
+    assert (w.M, w.K, w.N) == (8192, 8192, 28672) and w.margin == 1
+    assert abs(bench.clock_peak(152 * 16384 * 1e6 / 1e12, 2070.0) - 5155.06176) < 1e-6
+    assert bench.clock_peak(1.0, None) is None
 
 
 def test_traffic_figure_follows_the_kernel_source(tmp_path, monkeypatch):
