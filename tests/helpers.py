@@ -95,3 +95,66 @@ def assert_codes_in_band(gpu: np.ndarray, v: np.ndarray, tol, fmt: int, what="",
     differ = int((gpu != exp).sum())
     assert differ <= max(2, int(rare * gpu.size)), (what, differ)
     return differ
+
+
+# ------------------------------------------------ full-size cast checks --
+
+_CODE_TABLES = {}
+
+
+def oracle_code_table(scale, fmt: int) -> np.ndarray:
+    """The oracle's FP8 code of every BF16 bit pattern under ``scale``: its
+    scaled cast (o.quantize) applied to all 65,536 patterns.  The cast is
+    elementwise, so table[x_bits] is the oracle's cast of a whole tensor and
+    table[x_bits].T its transposed copy.  Cached per (scale bits, format)."""
+    key = (int(np.float32(scale).view(np.uint32)), int(fmt))
+    t = _CODE_TABLES.get(key)
+    if t is None:
+        bits = np.arange(65536, dtype=np.uint32).astype(np.uint16).reshape(1, -1)
+        q, _ = o.quantize(bits, np.float32(scale), fmt, transpose=False)
+        t = q.reshape(-1)
+        t.setflags(write=False)
+        if len(_CODE_TABLES) > 4096:
+            _CODE_TABLES.clear()
+        _CODE_TABLES[key] = t
+    return t
+
+
+def oracle_codes_host(x_bits: np.ndarray, table: np.ndarray) -> np.ndarray:
+    """The oracle's codes of a host BF16 tensor through its code table."""
+    return table[x_bits]
+
+
+def assert_codes_on_device(gpu_codes, x, table: np.ndarray, fmt: int, transposed=False, what=""):
+    """Every FP8 byte of a GPU cast output against the oracle's codes of the
+    same BF16 input (through its 65,536-entry table; the lookup and the
+    comparison run on the device, the values are the oracle's), NaN codes
+    compared as a class.  ``transposed``: gpu_codes is the [cols, rows] copy."""
+    import torch
+    t = torch.from_numpy(np.ascontiguousarray(table)).to(gpu_codes.device)
+    idx = x.contiguous().view(torch.int16).to(torch.int64) & 0xFFFF
+    exp = t[idx]
+    if transposed:
+        exp = exp.t()
+    g = gpu_codes.view(torch.uint8)
+    assert tuple(g.shape) == tuple(exp.shape), (what, tuple(g.shape), tuple(exp.shape))
+    diff = g != exp
+    if bool(diff.any()):
+        def nan_code(c):
+            m = c & 0x7F
+            return (m == 0x7F) if fmt == o.E4M3 else (m > 0x7C)
+        bad = diff & ~(nan_code(g) & nan_code(exp))
+        nbad = int(bad.sum())
+        if nbad:
+            where = torch.nonzero(bad)[:5].cpu().tolist()
+            raise AssertionError(f"{what}: {nbad} FP8 codes differ from the oracle's, e.g. at "
+                                 f"{where}")
+
+
+def device_absmax_bits(t) -> np.float32:
+    """max |t| over a BF16 tensor with NaN skipped (0 when all NaN), as the
+    exact float32 -- a property of the GPU's own output."""
+    import torch
+    a = t.float().abs()
+    a = torch.where(torch.isnan(a), torch.zeros_like(a), a)
+    return np.float32(a.max().item()) if a.numel() else np.float32(0.0)

@@ -2,14 +2,18 @@
 layer workloads of fp8_workloads.py, through the same Fp8Linear.step that
 bench.py times (fp8_linear_fwd, fp8_linear_bwd, fp8_amax_scale_update).
 
-Per checked step:
+Every step:
   * bit-exact: amax of X, W, dY; every FP8 byte of X8, X8t, W8, W8t, dY8,
-    dY8t; history, scale and scale_inv of the X, W and dY slots;
-  * GEMM outputs Y, dX, dW within the tolerance of helpers.py (whole tensors
-    on the small workload, blocks of rows at full size);
+    dY8t (the oracle's cast through its 65,536-entry code table at that
+    step's scale, compared on the device); history, scale and scale_inv of
+    the X, W and dY slots, before and after the update;
   * Y and dX slots: the fused amax equals max |output| of the GPU's own BF16
     output exactly, the history holds those amaxes newest first, and the
     scale follows from them by the recipe's formula.
+On the GEMM-check steps (every ``gemm_every`` steps, listed extra steps and
+the last), Y, dX and dW within the tolerance of helpers.py: whole tensors on
+small shapes; at full size three 16-row blocks (every column tile) and 16
+columns over all rows (every row tile) of each output.
 """
 import numpy as np
 import pytest
@@ -17,8 +21,8 @@ import torch
 
 import fp8_workloads as wl
 import oracle as o
-from helpers import (assert_fp8_equal, assert_gemm_close, bf16_values, f32_bits,
-                     host_bf16_bits, host_u8)
+from helpers import (assert_codes_on_device, assert_fp8_equal, assert_gemm_close, bf16_values,
+                     device_absmax_bits, f32_bits, host_bf16_bits, host_u8, oracle_code_table)
 
 pytestmark = pytest.mark.gpu
 
@@ -32,6 +36,11 @@ def _row_blocks(n, width=16):
     return sorted({0, (n // 2 // 16) * 16 + 48 if n > 128 else 0, n - width})
 
 
+def _col_sample(n, count=16):
+    """``count`` output columns spread over [0, n), first and last included."""
+    return np.unique(np.linspace(0, n - 1, count).round().astype(np.int64))
+
+
 def _gpu_slot_checks(lin, f, gpu_amax_hist, fmts, margin, g_amax):
     """Y / dX slots: properties that hold at any size (g_amax: the amax slots
     as the step left them, before the update consumed and cleared them)."""
@@ -40,8 +49,7 @@ def _gpu_slot_checks(lin, f, gpu_amax_hist, fmts, margin, g_amax):
     assert not lin.meta.amax.cpu().numpy().any()       # cleared by the update
     for slot, out in ((f.SLOT_Y, lin.Y), (f.SLOT_DX, lin.dX)):
         a = float(g_amax[slot])
-        vals = np.abs(bf16_values(host_bf16_bits(out)))
-        mx = np.float32(np.nanmax(vals) if not np.isnan(vals).all() else 0.0)   # NaN skipped
+        mx = device_absmax_bits(out)                    # NaN skipped
         assert f32_bits(np.float32(a)) == f32_bits(mx), (slot, a, mx)
         gpu_amax_hist[slot].insert(0, np.float32(a))
         L = hist.shape[1]
@@ -54,7 +62,40 @@ def _gpu_slot_checks(lin, f, gpu_amax_hist, fmts, margin, g_amax):
             assert f32_bits(scale[slot]) == f32_bits(expect)
 
 
-def run_layer(w: wl.Workload, steps, check_every=1, full=True, hybrid=None, extra_checks=(),
+class _HostCopy:
+    """Pinned host buffers reused across steps for the BF16 inputs' bits."""
+
+    def __init__(self):
+        self.bufs = {}
+
+    def bits(self, name, t):
+        b = self.bufs.get(name)
+        if b is None or b.shape != t.shape:
+            b = torch.empty(t.shape, dtype=torch.int16, pin_memory=True)
+            self.bufs[name] = b
+        b.copy_(t.view(torch.int16))
+        return b.numpy().view(np.uint16)
+
+
+def _check_gemms(gemms, full, step, report):
+    """gemms: (name, GPU output, A codes, fa, B codes, fb, sa_inv, sb_inv, K)."""
+    for name, out, A, fa, B, fb, sa, sb, K in gemms:
+        gout = host_bf16_bits(out)
+        if full:
+            ref = o.epilogue(o.gemm_tn(A, fa, B, fb), sa, sb)
+            report.append((step, name, assert_gemm_close(gout, ref, K, f"step {step} {name}")))
+            continue
+        for r0 in _row_blocks(A.shape[0]):
+            ref = o.epilogue(o.gemm_tn(A, fa, B, fb, r0, 16), sa, sb)
+            report.append((step, name, assert_gemm_close(gout[r0:r0 + 16], ref, K,
+                                                         f"step {step} {name} rows {r0}")))
+        cols = _col_sample(B.shape[0])
+        ref = o.epilogue(o.gemm_tn(A, fa, np.ascontiguousarray(B[cols]), fb), sa, sb)
+        report.append((step, name, assert_gemm_close(np.ascontiguousarray(gout[:, cols]), ref, K,
+                                                     f"step {step} {name} columns")))
+
+
+def run_layer(w: wl.Workload, steps, gemm_every=1, full=True, hybrid=None, extra_checks=(),
               current=False):
     f = _lib()
     hybrid = w.hybrid if hybrid is None else hybrid
@@ -65,6 +106,8 @@ def run_layer(w: wl.Workload, steps, check_every=1, full=True, hybrid=None, extr
     st = o.State.initial(w.history_len)
     fm = rc.formats()
     Wb = host_bf16_bits(W)
+    w_amax = o.amax(Wb)
+    host = _HostCopy()
     gpu_amax_hist = {f.SLOT_Y: [], f.SLOT_DX: []}
     report = []
     for step in range(steps):
@@ -74,52 +117,41 @@ def run_layer(w: wl.Workload, steps, check_every=1, full=True, hybrid=None, extr
         lin.backward(dY)
         torch.cuda.synchronize()
         g_amax = lin.meta.amax.cpu().numpy().copy()
-        check = (step % check_every == 0) or step in extra_checks or step == steps - 1
-        Xb, dYb = host_bf16_bits(X), host_bf16_bits(dY)
         g_scale = lin.meta.scale.cpu().numpy().copy()
         g_scale_inv = lin.meta.scale_inv.cpu().numpy().copy()
-        if check:
-            # forward / backward in the oracle
-            st.amax[o.SLOT_X] = o.amax(Xb)
-            st.amax[o.SLOT_W] = o.amax(Wb)
-            st.amax[o.SLOT_DY] = o.amax(dYb)
-            if current:
-                for slot in (o.SLOT_X, o.SLOT_W, o.SLOT_DY):
-                    o.just_in_time_scale(st, rc, slot, fm[slot])
-            X8, X8t = o.quantize(Xb, st.scale[o.SLOT_X], fm[o.SLOT_X])
-            W8, W8t = o.quantize(Wb, st.scale[o.SLOT_W], fm[o.SLOT_W])
-            dY8, dY8t = o.quantize(dYb, st.scale[o.SLOT_DY], fm[o.SLOT_DY])
-            for name, g, r, fmt in [("X8", lin.X8, X8, fm[0]), ("X8t", lin.X8t, X8t, fm[0]),
-                                    ("W8", lin.W8, W8, fm[1]), ("W8t", lin.W8t, W8t, fm[1]),
-                                    ("dY8", lin.dY8, dY8, fm[3]), ("dY8t", lin.dY8t, dY8t, fm[3])]:
-                assert_fp8_equal(host_u8(g), r, fmt, f"step {step} {name}")
-            si = st.scale_inv
-            gemms = [("Y", lin.Y, X8, fm[0], W8, fm[1], si[0], si[1], w.K),
-                     ("dX", lin.dX, dY8, fm[3], W8t, fm[1], si[3], si[1], w.N),
-                     ("dW", lin.dW, dY8t, fm[3], X8t, fm[0], si[3], si[0], w.M)]
-            for name, out, A, fa, B, fb, sa, sb, K in gemms:
-                gout = host_bf16_bits(out)
-                if full:
-                    ref = o.epilogue(o.gemm_tn(A, fa, B, fb), sa, sb)
-                    e = assert_gemm_close(gout, ref, K, f"step {step} {name}")
-                else:
-                    for r0 in _row_blocks(A.shape[0]):
-                        ref = o.epilogue(o.gemm_tn(A, fa, B, fb, r0, 16), sa, sb)
-                        e = assert_gemm_close(gout[r0:r0 + 16], ref, K,
-                                              f"step {step} {name} rows {r0}")
-                report.append((step, name, e))
-        else:
-            st.amax[o.SLOT_X] = o.amax(Xb)
-            st.amax[o.SLOT_W] = o.amax(Wb)
-            st.amax[o.SLOT_DY] = o.amax(dYb)
-            if current:
-                for slot in (o.SLOT_X, o.SLOT_W, o.SLOT_DY):
-                    o.just_in_time_scale(st, rc, slot, fm[slot])
+        Xb, dYb = host.bits("X", X), host.bits("dY", dY)
+        # the oracle's view of this step: amaxes (and just-in-time scales)
+        st.amax[o.SLOT_X] = o.amax(Xb)
+        st.amax[o.SLOT_W] = w_amax
+        st.amax[o.SLOT_DY] = o.amax(dYb)
+        if current:
+            for slot in (o.SLOT_X, o.SLOT_W, o.SLOT_DY):
+                o.just_in_time_scale(st, rc, slot, fm[slot])
         for slot in (o.SLOT_X, o.SLOT_W, o.SLOT_DY):
             assert f32_bits(g_amax[slot]) == f32_bits(st.amax[slot]), (step, slot)
             # the scales the casts of this step used
             assert f32_bits(g_scale[slot]) == f32_bits(st.scale[slot]), (step, slot)
             assert f32_bits(g_scale_inv[slot]) == f32_bits(st.scale_inv[slot]), (step, slot)
+        # every FP8 byte, against the oracle's cast at this step's scales
+        tables = {slot: oracle_code_table(st.scale[slot], fm[slot])
+                  for slot in (o.SLOT_X, o.SLOT_W, o.SLOT_DY)}
+        for name, g, x, slot, tr in [("X8", lin.X8, X, o.SLOT_X, False),
+                                     ("X8t", lin.X8t, X, o.SLOT_X, True),
+                                     ("W8", lin.W8, W, o.SLOT_W, False),
+                                     ("W8t", lin.W8t, W, o.SLOT_W, True),
+                                     ("dY8", lin.dY8, dY, o.SLOT_DY, False),
+                                     ("dY8t", lin.dY8t, dY, o.SLOT_DY, True)]:
+            assert_codes_on_device(g, x, tables[slot], fm[slot], tr, f"step {step} {name}")
+        if (step % gemm_every == 0) or step in extra_checks or step == steps - 1:
+            X8 = tables[o.SLOT_X][Xb]
+            W8 = tables[o.SLOT_W][Wb]
+            dY8 = tables[o.SLOT_DY][dYb]
+            X8t, W8t, dY8t = (np.ascontiguousarray(a.T) for a in (X8, W8, dY8))
+            si = st.scale_inv
+            _check_gemms([("Y", lin.Y, X8, fm[0], W8, fm[1], si[0], si[1], w.K),
+                          ("dX", lin.dX, dY8, fm[3], W8t, fm[1], si[3], si[1], w.N),
+                          ("dW", lin.dW, dY8t, fm[3], X8t, fm[0], si[3], si[0], w.M)],
+                         full, step, report)
         # the delayed-scaling update
         lin.update()
         torch.cuda.synchronize()
@@ -147,29 +179,35 @@ def test_tiny_shape_long_run_history_window(hybrid):
     d = wl.WORKLOADS["drift"]
     small = wl.Workload("drift_small", 128, 256, 256, "drift", 1.0, 1 / 16, 1.0, 512, 0, True,
                         1000)
-    run_layer(small, 1000, check_every=50, full=True, hybrid=hybrid,
+    run_layer(small, 1000, gemm_every=50, full=True, hybrid=hybrid,
               extra_checks=(49, 50, 51, 75, 76, 150, 562, 563))
     assert d.history_len == 512
 
 
-def test_mlp7b_full_size_sampled_rows():
+def test_mlp7b_full_size_100_steps():
+    """The 7B-shaped layer's 100 steps: state and every FP8 byte each step,
+    the GEMMs (row blocks and column samples) every 10th step."""
     w = wl.WORKLOADS["mlp7b"]
-    run_layer(w, 3, full=False)
+    run_layer(w, w.steps, gemm_every=10, full=False)
 
 
-def test_mlp70b_full_size_sampled_rows():
+def test_mlp70b_full_size_50_steps():
+    """The 70B-shaped layer's 50 steps (Student-t X with outlier channels,
+    margin 1): state and every FP8 byte each step, the GEMMs every 10th."""
     w = wl.WORKLOADS["mlp70b"]
-    run_layer(w, 2, full=False)
+    run_layer(w, w.steps, gemm_every=10, full=False)
 
 
 @pytest.mark.parametrize("hybrid", [True, False])
-def test_drift_full_size(hybrid):
-    """The drifting-scale stress at full size (4096^3) through its first 120
-    steps: the x1000 spike at step 50 and the all-zero step 75, in both the
-    HYBRID and the E4M3-everywhere arms."""
+def test_drift_full_size_1000_steps(hybrid):
+    """The drifting-scale stress at full size (4096^3) through all 1000
+    steps, in both the HYBRID and the E4M3-everywhere arms: state and every
+    FP8 byte each step (the x1000 spikes at t % 100 == 50, the all-zero steps
+    at t % 100 == 75, the history window of 512), GEMMs every 50th step and
+    around the spikes and zero steps."""
     w = wl.WORKLOADS["drift"]
-    run_layer(w, 120, check_every=40, full=False, hybrid=hybrid,
-              extra_checks=(49, 50, 51, 75, 76, 100, 101))
+    run_layer(w, w.steps, gemm_every=50, full=False, hybrid=hybrid,
+              extra_checks=(49, 51, 75, 76, 562, 563, 950, 951))
 
 
 def test_ragged_layer_shape():
@@ -192,7 +230,7 @@ def test_just_in_time_scaling_tiny_and_drift():
     run_layer(wl.WORKLOADS["tiny"], 4, full=True, current=True)
     small = wl.Workload("drift_small", 128, 256, 256, "drift", 1.0, 1 / 16, 1.0, 512, 0, True,
                         120)
-    run_layer(small, 120, check_every=10, full=True, current=True,
+    run_layer(small, 120, gemm_every=10, full=True, current=True,
               extra_checks=(49, 50, 51, 75, 76))
 
 
