@@ -16,8 +16,9 @@ Prints ONE JSON line (rank 0).  Metric: layer TFLOPS = 6 M N K per step over
 the device time of K steps (CUDA events, max over ranks).  Added keys:
   roofline      the dominant kernel (the tcgen05 GEMM), achieved TFLOP/s vs the
                 FP8 peak derived from MEASURED_PEAKS.json (bf16 x 2), and vs
-                SMs x 16384 FLOP/clk x the SM clock sampled while timing
-                (peak_clock) and x the maximum SM clock (peak_boost)
+                SMs x 16384 FLOP/clk x the SM clock the timed GEMM launches
+                ran at, measured inside the kernel (peak_clock), and x the
+                maximum SM clock (peak_boost)
   cast_roofline the fused cast kernels, achieved GB/s vs measured HBM copy
   sustained     the same step back to back for a few seconds, with its own
                 clock record (the power-capped regime)
@@ -322,10 +323,15 @@ def run_layer_bench(f, w: wl.Workload, args, world, pk, peak_kind, sustained_s: 
     E4 = f.E4M3
     nb = max(10, min(args.steps, 100))
     nb_warm = max(args.warmup, 10)
+    # the SM clock the GEMM launches run at, measured inside the kernels
+    # (fp8_set_clock_probe: the first CTA's %clock64 cycles over its
+    # %globaltimer nanoseconds), for the clock-derived peak
+    probe = torch.zeros(2, dtype=torch.int64, device=dev)
     torch.cuda.synchronize()
     torch.cuda._sleep(50_000_000)          # ~25 ms at 2 GHz: room to enqueue ahead
     for i in range(nb_warm + nb):
         tm.enabled = i >= nb_warm
+        f.fp8_set_clock_probe(probe if tm.enabled else None)
         X, dY = xs[i % 2], dys[i % 2]
         tm.time("cast_XW", lambda: f.fp8_quantize_transpose_grouped(
             [(X, m.scale[0:1], lin.X8, lin.X8t, None), (W, m.scale[1:2], lin.W8, lin.W8t, None)],
@@ -338,9 +344,12 @@ def run_layer_bench(f, w: wl.Workload, args, world, pk, peak_kind, sustained_s: 
             [(lin.dY8, fg, lin.W8t, E4, m.scale_inv[3:4], m.scale_inv[1:2], lin.dX, None),
              (lin.dY8t, fg, lin.X8t, E4, m.scale_inv[3:4], m.scale_inv[0:1], lin.dW, None)]))
         tm.time("update", lambda: lin.update())
+    f.fp8_set_clock_probe(None)
     torch.cuda.synchronize()
     clk = clocks.stop()
     f.fp8_sync_status()
+    pcyc, pns = (int(v) for v in probe.cpu())
+    gemm_mhz = pcyc / pns * 1e3 if pns > 0 else None
 
     M, N, K = w.M, w.N, w.K
     flops = 6 * M * N * K
@@ -355,7 +364,7 @@ def run_layer_bench(f, w: wl.Workload, args, world, pk, peak_kind, sustained_s: 
     cast_bytes = {"cast_XW": 4 * M * K + 4 * N * K, "cast_dY": 4 * M * N}
     cast_gbs = sum(cast_bytes.values()) / (sum(cast_ms.values()) / 1e3) / 1e9
     traffic = gemm_traffic(w.name)
-    pc = clock_peak(tflop_per_mhz, clk.get("sm_mhz"))
+    pc = clock_peak(tflop_per_mhz, gemm_mhz)
     pb = clock_peak(tflop_per_mhz, clk.get("sm_max_mhz"))
     res = {
         "value": value, "ms_per_step": ms / args.steps,
@@ -368,9 +377,12 @@ def run_layer_bench(f, w: wl.Workload, args, world, pk, peak_kind, sustained_s: 
                      "peak_basis": f"{peak_kind} bf16 burst {pk['bf16_tflops']} x {FP8_OVER_BF16} "
                                    f"(of {peak_kind})",
                      "peak_clock": {"value": pc, "frac": achieved / pc if pc else None,
-                                    "sm_mhz": clk.get("sm_mhz"), "sms": sms,
+                                    "sm_mhz": gemm_mhz, "sms": sms,
                                     "basis": f"{sms} SMs x {FP8_FLOP_PER_CLK_SM} FLOP/clk x the "
-                                             "median SM clock sampled while timing"},
+                                             "SM clock the timed GEMM launches ran at, measured "
+                                             "in the kernel (%clock64 cycles over %globaltimer "
+                                             "ns of its first CTA, fp8_set_clock_probe)",
+                                    "nvidia_smi_median_mhz": clk.get("sm_mhz")},
                      "peak_boost": {"value": pb, "frac": achieved / pb if pb else None,
                                     "sm_mhz": clk.get("sm_max_mhz")},
                      "launches_per_step": {"gemm_fprop": "fprop", "gemm_bwd": "dgrad+wgrad"},
@@ -390,17 +402,20 @@ def run_layer_bench(f, w: wl.Workload, args, world, pk, peak_kind, sustained_s: 
     }
 
     if sustained_s > 0:
-        res["sustained"] = run_sustained(graphs, step, timed, sustained_s, ms / args.steps, flops,
-                                         world, tflop_per_mhz, pk)
+        # the launch mode (graph replays or eager steps) that timed faster
+        res["sustained"] = run_sustained(graphs if res["launch"] != "eager" else None, step, timed,
+                                         sustained_s, ms / args.steps, flops, world,
+                                         tflop_per_mhz, pk)
     if e2e:
         res["e2e"] = run_e2e(f, lin, xs[0], dys[0], args, world, flops)
     return res
 
 
 def run_sustained(graphs, step, timed, seconds, ms_step, flops, world, tflop_per_mhz, pk):
-    """The same step back to back for about ``seconds`` (graph replays at
-    N = 1), timed with CUDA events around the whole loop, with its own clock
-    record: the regime where the GPU runs at its power limit."""
+    """The same step back to back for about ``seconds`` (graph replays or
+    eager steps, whichever timed faster), timed with CUDA events around the
+    whole loop, with its own clock record: the regime where the GPU runs at
+    its power limit."""
     n = max(10, int(seconds * 1e3 / max(ms_step, 1e-3)))
     run = (lambda i: graphs[i % 2].replay()) if graphs else step
     clocks = ClockSampler()
@@ -411,6 +426,7 @@ def run_sustained(graphs, step, timed, seconds, ms_step, flops, world, tflop_per
     value = world * n * flops / (ms / 1e3) / 1e12
     pc = clock_peak(tflop_per_mhz, clk.get("sm_mhz"))
     return {"value": value, "unit": "TFLOPS", "ms_per_step": ms / n, "steps": n,
+            "launch": "CUDA graph replay" if graphs else "eager",
             "seconds": ms / 1e3, "clocks": clk,
             "step_frac_of_peak_clock": value / world / pc if pc else None,
             "step_frac_of_sustained_bf16_x2": value / world / (pk["bf16_tflops_sustained"]
@@ -790,21 +806,44 @@ def secondary_jit_scaling(f, w7):
 def secondary_dequant_sum(f, w7, flush):
     """The device part of the FP8 gradient all-reduce: decode and sum 8 ranks'
     FP8 codes of the 7B dW (shared scale) into BF16; 8 B read + 2 B written
-    per element for 8 ranks."""
-    tm = EventTimer()
+    per element for 8 ranks.  The codes are 8 ranks' gradient-shaped dW
+    (N(0, sigma_r) BF16, sigma_r = 1e-3 * (1 + r / 10)) cast with their
+    shared scale, the minimum of the ranks' own scales, as fp8_allreduce
+    does; a second row times uniformly random finite codes, whose sums span
+    the most binades (the kernel's slowest case)."""
     nr, nd = 8, w7.N * w7.K
-    parts = torch.randint(0, 0x7B, (nr, nd), dtype=torch.uint8, device="cuda")
+    g = torch.Generator(device="cuda").manual_seed(7)
+    grads, scales = [], []
+    for r in range(nr):
+        x = (torch.randn((w7.N, w7.K), generator=g, device="cuda") * (1e-3 * (1 + 0.1 * r))) \
+            .to(torch.bfloat16)
+        am, h = torch.empty(1, device="cuda"), torch.zeros((1, 1), device="cuda")
+        s1, si = torch.ones(1, device="cuda"), torch.ones(1, device="cuda")
+        f.fp8_amax(x, am)
+        f.fp8_scale_update(h, am, s1, si, f.E5M2, 0)
+        grads.append(x)
+        scales.append(s1)
+    sg = torch.min(torch.cat(scales)).reshape(1)
+    parts = torch.empty((nr, nd), dtype=torch.uint8, device="cuda")
+    for r in range(nr):
+        f.fp8_quantize_transpose(grads[r], sg, f.E5M2, out=parts[r].view(w7.N, w7.K))
+    del grads
+    uniform = torch.randint(0, 0x7B, (nr, nd), dtype=torch.uint8, device="cuda")
     dsum = torch.empty(nd, dtype=torch.bfloat16, device="cuda")
-    sc1 = torch.full((1,), 64.0, device="cuda")
-    for i in range(23):
-        flush.zero_()
-        tm.time("dequant_sum", lambda: f.fp8_dequant_sum(parts, f.E5M2, sc1, dsum))
-    torch.cuda.synchronize()
-    tm.pairs["dequant_sum"] = tm.pairs["dequant_sum"][3:]
-    res = {"us": tm.mean_ms("dequant_sum") * 1e3,
-           "gbs_algorithmic": (nr + 2) * nd / (tm.mean_ms("dequant_sum") / 1e3) / 1e9,
-           "note": "decode + rank-order sum of 8 ranks' E5M2 codes -> BF16; L2 flushed before each"}
-    del parts, dsum
+    res = {}
+    for name, (codes, sc) in {"gradient": (parts, sg),
+                              "uniform_codes": (uniform, torch.full((1,), 64.0, device="cuda"))}.items():
+        tm = EventTimer()
+        for i in range(23):
+            flush.zero_()
+            tm.time("dequant_sum", lambda: f.fp8_dequant_sum(codes, f.E5M2, sc, dsum))
+        torch.cuda.synchronize()
+        tm.pairs["dequant_sum"] = tm.pairs["dequant_sum"][3:]
+        us = tm.mean_ms("dequant_sum") * 1e3
+        res[name] = {"us": us, "gbs_algorithmic": (nr + 2) * nd / (us / 1e6) / 1e9}
+    res["note"] = ("exact decode + sum of 8 ranks' E5M2 codes -> BF16 (rounded once); "
+                   "L2 flushed before each; 10 B/element algorithmic")
+    del parts, uniform, dsum
     return res
 
 

@@ -77,6 +77,7 @@ def _load() -> ctypes.CDLL:
         "fp8_last_error": ([], ctypes.c_char_p),
         "fp8_sync_status": ([vp], ctypes.c_int),
         "fp8_amax": ([vp, i64, vp, vp], ctypes.c_int),
+        "fp8_set_clock_probe": ([vp], ctypes.c_int),
         "fp8_selftest_wait_timeout": ([i64, vp], ctypes.c_int),
         "fp8_quantize_transpose": ([vp, i64, i64, vp, i32, vp, vp, vp, vp], ctypes.c_int),
         "fp8_quantize_f32": ([vp, i64, vp, i32, vp, vp, vp], ctypes.c_int),
@@ -178,6 +179,16 @@ def fp8_selftest_wait_timeout(limit_ns: int, stream=None) -> None:
     """Diagnostic: a kernel whose bounded wait runs out after ``limit_ns``;
     the next fp8_sync_status raises Fp8Error with FP8_ERR_TIMEOUT."""
     _check(_lib.fp8_selftest_wait_timeout(int(limit_ns), _stream(stream)))
+
+
+def fp8_set_clock_probe(acc: torch.Tensor | None) -> None:
+    """Diagnostic: while ``acc`` (a zeroed CUDA int64 tensor of 2) is set, the
+    first CTA of every GEMM launch adds its SM cycles to acc[0] and its
+    nanoseconds to acc[1]; acc[0] / acc[1] is the average SM clock in GHz.
+    None turns the probe off."""
+    if acc is not None and (acc.dtype != torch.int64 or acc.numel() < 2):
+        raise ValueError("acc must be an int64 tensor of at least 2 elements")
+    _check(_lib.fp8_set_clock_probe(_ptr(acc, torch.int64, "acc")))
 
 
 def fp8_amax(x: torch.Tensor, amax: torch.Tensor, stream=None) -> None:

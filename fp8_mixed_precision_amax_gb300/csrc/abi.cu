@@ -154,6 +154,14 @@ fp8_status fp8_selftest_wait_timeout(int64_t limit_ns, void *stream) {
     return FP8_OK;
 }
 
+fp8_status fp8_set_clock_probe(uint64_t *acc) {
+    const fp8k::CallRange range("fp8_set_clock_probe");
+    if (acc != nullptr && (reinterpret_cast<uintptr_t>(acc) & 7u) != 0)
+        return fail(FP8_ERR_ALIGN, "fp8_set_clock_probe: acc must be 8-byte aligned");
+    fp8k::set_clock_probe(reinterpret_cast<unsigned long long *>(acc));
+    return FP8_OK;
+}
+
 fp8_status fp8_amax(const void *x, int64_t n, float *amax, void *stream) {
     const char *fn = "fp8_amax";
     const fp8k::CallRange range(fn);

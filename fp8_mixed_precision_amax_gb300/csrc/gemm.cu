@@ -35,6 +35,7 @@
 // Every wait is bounded.
 #include <cuda_bf16.h>
 
+#include <atomic>
 #include <cstdint>
 #include <mutex>
 
@@ -44,6 +45,12 @@
 namespace fp8k {
 
 __device__ unsigned g_error_flags = 0;
+
+// Diagnostic clock probe (fp8_set_clock_probe): a device pointer that every
+// GEMM launch passes to its kernel while it is set.
+std::atomic<unsigned long long *> g_clock_probe{nullptr};
+
+void set_clock_probe(unsigned long long *acc) { g_clock_probe.store(acc); }
 
 namespace {
 
@@ -89,6 +96,7 @@ struct GemmArgs {
     GemmProblem prob[MAX_PROBLEMS];
     int num_problems;
     int num_tiles;
+    unsigned long long *clock_probe;      // diagnostic: {SM cycles, ns} of CTA 0, or null
 };
 
 __device__ __forceinline__ void tile_coords(int tile, int tiles_m, int tiles_n, int group_m,
@@ -171,6 +179,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_tn_kernel(const __grid_co
     // the prologue above touched only this CTA's own memory
     pdl_wait();
     pdl_trigger();
+    uint64_t probe_clk = 0, probe_ns = 0;
+    if (a.clock_probe != nullptr && blockIdx.x == 0 && threadIdx.x == 0) {
+        probe_clk = clock64();
+        probe_ns = globaltimer_ns();
+    }
 
     if (warp == 0) {
         // ------------------------------------------------------ TMA producer
@@ -420,6 +433,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_tn_kernel(const __grid_co
         else
             tmem_dealloc(tmem_base, TMEM_COLS);
     }
+    if (a.clock_probe != nullptr && blockIdx.x == 0 && threadIdx.x == 0) {
+        atomicAdd(a.clock_probe, static_cast<unsigned long long>(clock64() - probe_clk));
+        atomicAdd(a.clock_probe + 1, static_cast<unsigned long long>(globaltimer_ns() - probe_ns));
+    }
 }
 
 // --------------------------------------------------------------- host side --
@@ -486,6 +503,7 @@ cudaError_t launch_gemm_group(const GemmSpec *specs, int n, int sm_count, cudaSt
     const uint32_t b_rows = pair ? BN / 2 : BN;
     GemmArgs a;
     a.num_problems = n;
+    a.clock_probe = g_clock_probe.load(std::memory_order_relaxed);
     int tiles = 0;
     for (int i = 0; i < n; ++i) {
         const GemmSpec &g = specs[i];
@@ -567,9 +585,12 @@ cudaError_t read_and_clear_error_flag(unsigned *flags, cudaStream_t st) {
     const unsigned zero = 0;
     e = cudaMemcpyToSymbol(g_error_flags, &zero, sizeof(unsigned));
     if (e != cudaSuccess) return e;
-    unsigned cast_flags = 0;
+    unsigned cast_flags = 0, sum_flags = 0;
     e = read_and_clear_cast_error_flag(&cast_flags);
     *flags |= cast_flags;
+    if (e != cudaSuccess) return e;
+    e = read_and_clear_sum_error_flag(&sum_flags);
+    *flags |= sum_flags;
     return e;
 }
 

@@ -150,11 +150,18 @@ cudaError_t launch_adam_init(const AdamInitSpec &s, int sm_count, cudaStream_t s
 cudaError_t launch_dequant_sum(const uint8_t *parts, int nranks, int64_t n, int fmt,
                                const float *scale, void *out, int sm_count, cudaStream_t st);
 
+// Diagnostic: while acc is not null, the first CTA of every GEMM launch adds
+// its SM clock cycles to acc[0] and its nanoseconds to acc[1] (gemm.cu).
+void set_clock_probe(unsigned long long *acc);
+
 // Set the message fp8_last_error() returns on this host thread.
 void set_last_error(const char *msg);
 
 // Read and clear the cast kernels' device error flag (cast.cu).
 cudaError_t read_and_clear_cast_error_flag(unsigned *flags);
+
+// Read and clear the FP8 sum kernel's device error flag (optim.cu).
+cudaError_t read_and_clear_sum_error_flag(unsigned *flags);
 
 // Read and clear the device error flag the kernels set when a bounded wait
 // gives up (synchronizes the device flag's stream).

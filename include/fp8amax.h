@@ -36,7 +36,8 @@
  *    the current device; the caller allocates and owns every buffer.  The
  *    library allocates no device memory, never synchronizes the stream (except
  *    fp8_sync_status), and keeps no state beyond cached device properties,
- *    one device-side error flag and the fixed work array that
+ *    one device-side error flag, the diagnostic clock-probe pointer
+ *    (fp8_set_clock_probe) and the fixed work array that
  *    fp8_linear_bwd_noalloc uses (described there).
  *  - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
  *    stream).  All work is enqueued on it, in order; scales are read on the
@@ -135,6 +136,19 @@ fp8_status fp8_sync_status(void *stream);
  * The next fp8_sync_status on the stream then returns FP8_ERR_TIMEOUT (and
  * clears the flag); the context stays usable. */
 fp8_status fp8_selftest_wait_timeout(int64_t limit_ns, void *stream);
+
+/* Diagnostic, not part of the method: a clock probe for measuring the SM
+ * clock the GEMMs actually run at.  While acc is not NULL, the first CTA of
+ * every GEMM launch (fp8_gemm_tn, fp8_gemm_tn_grouped and the GEMMs inside
+ * the layer calls) adds the SM clock cycles (%clock64) and the nanoseconds
+ * (%globaltimer) between its start and its end to acc[0] and acc[1] (atomic
+ * adds); acc[0] / acc[1] is then the average SM clock during those launches
+ * in GHz.  The kernels persist over all tiles, so that CTA lives as long as
+ * the launch.  acc: DEVICE, 2 uint64, 8-byte aligned, caller-owned and
+ * zeroed by the caller; NULL (the default) turns the probe off.  The
+ * setting is process-wide and is read when a launch is enqueued (a CUDA
+ * graph keeps the value it was captured with). */
+fp8_status fp8_set_clock_probe(uint64_t *acc);
 
 /* amax of a BF16 tensor (the implementation guide's range monitoring; the
  * TensorRT page's Absolute-Max statistic).

@@ -166,3 +166,13 @@ def test_header_enums_match_binding():
     assert (enum["FP8_E4M3"], enum["FP8_E5M2"]) == (api.E4M3, api.E5M2)
     assert (enum["FP8_SCALING_DELAYED"], enum["FP8_SCALING_CURRENT"]) == \
         (api.SCALING_DELAYED, api.SCALING_CURRENT)
+
+
+def test_clock_probe_pointer_must_be_aligned():
+    """fp8_set_clock_probe checks its pointer on the host: a misaligned one is
+    FP8_ERR_ALIGN; NULL (off) is accepted."""
+    from fp8_mixed_precision_amax_gb300 import api
+    lib = api.library()
+    assert lib.fp8_set_clock_probe(ctypes.c_void_p(0x1004)) == 2
+    assert b"8-byte aligned" in lib.fp8_last_error()
+    assert lib.fp8_set_clock_probe(None) == 0

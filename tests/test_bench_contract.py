@@ -55,21 +55,29 @@ def test_headline_defaults_to_the_largest_layer():
 
 
 def test_traffic_figure_follows_the_kernel_source(tmp_path, monkeypatch):
+    """bench.gemm_traffic reports a capture's DRAM bytes only while the sha256
+    it records matches the current gemm.cu."""
+    import hashlib
     sys.path.insert(0, ROOT)
     import bench
-    assert bench.gemm_traffic("mlp7b") is not None      # the committed capture matches
-    # a capture of another source is not reported
+    gemm_src = open(os.path.join(ROOT, "fp8_mixed_precision_amax_gb300", "csrc", "gemm.cu"),
+                    "rb").read()
     prof = tmp_path / "profiles"
     prof.mkdir()
-    src = json.load(open(os.path.join(ROOT, "profiles", "gemm_tn_kernel.mlp7b.traffic.json")))
-    src["gemm_cu_sha256"] = "0" * 64
-    (prof / "gemm_tn_kernel.mlp7b.traffic.json").write_text(json.dumps(src))
     pkg = tmp_path / "fp8_mixed_precision_amax_gb300" / "csrc"
     pkg.mkdir(parents=True)
-    (pkg / "gemm.cu").write_bytes(open(os.path.join(ROOT, "fp8_mixed_precision_amax_gb300", "csrc",
-                                                     "gemm.cu"), "rb").read())
+    (pkg / "gemm.cu").write_bytes(gemm_src)
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    rec = {"kernel": "gemm_tn_kernel", "workload": "mlp7b", "bytes_per_launch_mean": 123.0,
+           "gemm_cu_sha256": hashlib.sha256(gemm_src).hexdigest()}
+    (prof / "gemm_tn_kernel.mlp7b.traffic.json").write_text(json.dumps(rec))
+    assert bench.gemm_traffic("mlp7b") == 123.0
+    # a capture of another source is not reported
+    rec["gemm_cu_sha256"] = "0" * 64
+    (prof / "gemm_tn_kernel.mlp7b.traffic.json").write_text(json.dumps(rec))
     assert bench.gemm_traffic("mlp7b") is None
+    # nor is a workload without a capture
+    assert bench.gemm_traffic("drift") is None
 
 
 def test_range_counts_on_known_values():

@@ -152,3 +152,31 @@ def test_gemm_degenerate_dequant_factors():
         vals_ok = np.abs(bf16_values(got[~nan16(got)]))
         expect = np.float32(vals_ok.max()) if vals_ok.size else np.float32(0.0)
         assert f32_bits(am) == f32_bits(expect), (sa, sb, am, expect)
+
+
+def test_clock_probe_measures_the_gemm_clock():
+    """The diagnostic clock probe: while set, every GEMM launch adds its first
+    CTA's SM cycles and nanoseconds; the ratio is a plausible SM clock (the
+    part's maximum is 2.07 GHz); once cleared, launches add nothing."""
+    import fp8_mixed_precision_amax_gb300 as f
+    M, N, K = 1024, 2048, 4096
+    g = torch.Generator().manual_seed(5)
+    A = torch.randint(0, 0x7E, (M, K), generator=g, dtype=torch.uint8).cuda()
+    B = torch.randint(0, 0x7E, (N, K), generator=g, dtype=torch.uint8).cuda()
+    one = torch.ones(1, device="cuda")
+    D = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    acc = torch.zeros(2, dtype=torch.int64, device="cuda")
+    f.fp8_set_clock_probe(acc)
+    try:
+        for _ in range(5):
+            f.fp8_gemm_tn(A, f.E4M3, B, f.E4M3, one, one, D)
+    finally:
+        f.fp8_set_clock_probe(None)
+    torch.cuda.synchronize()
+    cyc, ns = (int(v) for v in acc.cpu())
+    assert cyc > 0 and ns > 0
+    assert 0.3 < cyc / ns < 2.2, (cyc, ns)
+    f.fp8_gemm_tn(A, f.E4M3, B, f.E4M3, one, one, D)
+    torch.cuda.synchronize()
+    assert [int(v) for v in acc.cpu()] == [cyc, ns]
+    f.fp8_sync_status()
