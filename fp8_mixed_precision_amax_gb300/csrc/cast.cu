@@ -433,7 +433,8 @@ __global__ void __launch_bounds__(kQtThreads, 2)
 //
 // One warp per row (grid-stride over rows): mean = sum(x) / C, then
 // var = sum((x - mean)^2) / C over a second read of the row (from L1 / L2),
-// rstd = 1 / sqrt(var + eps), all in fp32 with correctly rounded operations.
+// rstd = 1 / sqrt(var + eps), all in fp32 with correctly rounded operations;
+// each squared deviation is accumulated with one fused multiply-add.
 // With amax_bits, a third read computes y = ((x - mean) * rstd) * gamma + beta
 // and max-combines max |y| (for just-in-time scaling of the LayerNorm output).
 
@@ -497,8 +498,8 @@ __global__ void __launch_bounds__(256) ln_stats_kernel(const uint16_t *__restric
                 for (int j = 0; j < 4; ++j) {
                     const float d0 = __fsub_rn(bf16_lo(w[j]), mu);
                     const float d1 = __fsub_rn(bf16_hi(w[j]), mu);
-                    part[2 * j] = __fadd_rn(part[2 * j], __fmul_rn(d0, d0));
-                    part[2 * j + 1] = __fadd_rn(part[2 * j + 1], __fmul_rn(d1, d1));
+                    part[2 * j] = __fmaf_rn(d0, d0, part[2 * j]);
+                    part[2 * j + 1] = __fmaf_rn(d1, d1, part[2 * j + 1]);
                 }
             }
         }
@@ -540,65 +541,101 @@ __global__ void __launch_bounds__(256) ln_stats_kernel(const uint16_t *__restric
     }
 }
 
-// The same statistics for rows of at most 32 * MAXV * 8 columns, with the
-// row held in registers: one read of x, then the sum, the squared
-// deviations and the optional amax(y) from registers.  Each lane visits its
-// vectors in the same order as ln_stats_kernel, so the fp32 results are the
-// same bit for bit.
-template <int MAXV>
-__global__ void __launch_bounds__(256) ln_stats_reg_kernel(const uint16_t *__restrict__ x,
-                                                           const uint16_t *__restrict__ gamma,
-                                                           const uint16_t *__restrict__ beta,
-                                                           int64_t rows, int64_t cols, float eps,
-                                                           float *__restrict__ mean,
-                                                           float *__restrict__ rstd,
-                                                           unsigned *__restrict__ amax_bits) {
+// The same statistics for rows of at most 8192 columns, each row staged in
+// shared memory by an untiled bulk copy.  Every warp owns two row buffers:
+// while it reduces one row its next row is already in flight, so the loads
+// of all warps keep HBM busy through the reductions (a row read only into
+// registers left the loads idle while each warp reduced).  The sum, the
+// squared deviations and the optional amax(y) read the staged row; each lane
+// visits its vectors in the same order as ln_stats_kernel, so the fp32
+// results are the same bit for bit.  Waits are bounded.
+constexpr int kLnBufs = 2;
+
+__global__ void __launch_bounds__(512) ln_stats_bulk_kernel(const uint16_t *__restrict__ x,
+                                                            const uint16_t *__restrict__ gamma,
+                                                            const uint16_t *__restrict__ beta,
+                                                            int64_t rows, int64_t cols, float eps,
+                                                            float *__restrict__ mean,
+                                                            float *__restrict__ rstd,
+                                                            unsigned *__restrict__ amax_bits) {
+    extern __shared__ uint8_t ln_smem_raw[];
+    const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
+    const int nw = static_cast<int>(blockDim.x >> 5);
+    const uint32_t row_bytes = static_cast<uint32_t>(cols) * 2u;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(ln_smem_raw);            // [nw][kLnBufs]
+    uint8_t *bufs = ln_smem_raw + 16 * nw * kLnBufs;                       // 128-byte aligned below
+    bufs = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(bufs) + 127) &
+                                       ~static_cast<uintptr_t>(127));
+    uint8_t *mybuf = bufs + static_cast<size_t>(wib) * kLnBufs * row_bytes;
+    const uint32_t bar0 = smem_u32(bars + wib * kLnBufs);
+    if (lane == 0) {
+        for (int b = 0; b < kLnBufs; ++b) mbar_init(bar0 + 8 * b, 1);
+        fence_mbar_init();
+    }
+    __syncwarp();
     pdl_wait();
     pdl_trigger();
-    const int lane = threadIdx.x & 31;
-    const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+    const int64_t warps = static_cast<int64_t>(gridDim.x) * nw;
+    const int64_t first = static_cast<int64_t>(blockIdx.x) * nw + wib;
     const int nvec = static_cast<int>(cols / 8);
     const float inv_c = __fdiv_rn(1.0f, static_cast<float>(cols));
+    int issued[kLnBufs] = {0, 0}, consumed[kLnBufs] = {0, 0};   // lane 0's counts
+    auto issue = [&](int b, int64_t r) {
+        ++issued[b];
+        mbar_arrive_expect_tx(bar0 + 8 * b, row_bytes);
+        bulk_load_1d(smem_u32(mybuf + b * row_bytes), x + r * cols, row_bytes, bar0 + 8 * b);
+    };
+    if (lane == 0)
+        for (int b = 0; b < kLnBufs; ++b)
+            if (first + b * warps < rows) issue(b, first + b * warps);
     uint32_t m = 0;
-    for (int64_t r = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; r < rows;
-         r += warps) {
-        const uint4 *xr = reinterpret_cast<const uint4 *>(x + r * cols);
-        uint4 v[MAXV];
-#pragma unroll
-        for (int u = 0; u < MAXV; ++u)
-            v[u] = lane + 32 * u < nvec ? __ldcs(xr + lane + 32 * u) : make_uint4(0, 0, 0, 0);
-        float part[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-#pragma unroll
-        for (int u = 0; u < MAXV; ++u) {
-            if (lane + 32 * u >= nvec) break;
-            const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                part[2 * j] = __fadd_rn(part[2 * j], bf16_lo(w[j]));
-                part[2 * j + 1] = __fadd_rn(part[2 * j + 1], bf16_hi(w[j]));
-            }
+    bool failed = false;
+    int64_t j = 0;
+    for (int64_t r = first; r < rows; r += warps, ++j) {
+        const int b = static_cast<int>(j % kLnBufs);
+        const uint32_t parity = static_cast<uint32_t>((j / kLnBufs) & 1);
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait(bar0 + 8 * b, parity, nullptr))) {
+            failed = true;
+            break;
         }
+        if (lane == 0) ++consumed[b];
+        const uint4 *xr = reinterpret_cast<const uint4 *>(mybuf + b * row_bytes);
+        // the sum: eight partial sums per lane (one per element position of
+        // a 16-byte vector), vectors lane, lane + 32, ...; two lanes of an
+        // fp32 pair at a time (each lane one IEEE add, as the scalar adds)
+        uint64_t part2[4] = {0u, 0u, 0u, 0u};
+        for (int i = lane; i < nvec; i += 32) {
+            const uint4 v = xr[i];
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) part2[q] = f32x2_add(part2[q], f32x2_from_bf16x2(w[q]));
+        }
+        float part[8];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) f32x2_unpack(part2[q], part[2 * q], part[2 * q + 1]);
         float sum = 0.0f;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) sum = __fadd_rn(sum, part[j]);
+        for (int q = 0; q < 8; ++q) sum = __fadd_rn(sum, part[q]);
         const float mu = __fmul_rn(warp_sum(sum), inv_c);
+        // the squared deviations, each accumulated with one fused
+        // multiply-add (d * d + part, rounded once)
+        const uint64_t mu2 = splat_f32x2(mu);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) part[j] = 0.0f;
+        for (int q = 0; q < 4; ++q) part2[q] = 0u;
+        for (int i = lane; i < nvec; i += 32) {
+            const uint4 v = xr[i];
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-        for (int u = 0; u < MAXV; ++u) {
-            if (lane + 32 * u >= nvec) break;
-            const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const float d0 = __fsub_rn(bf16_lo(w[j]), mu);
-                const float d1 = __fsub_rn(bf16_hi(w[j]), mu);
-                part[2 * j] = __fadd_rn(part[2 * j], __fmul_rn(d0, d0));
-                part[2 * j + 1] = __fadd_rn(part[2 * j + 1], __fmul_rn(d1, d1));
+            for (int q = 0; q < 4; ++q) {
+                const uint64_t d = f32x2_sub(f32x2_from_bf16x2(w[q]), mu2);
+                part2[q] = f32x2_fma(d, d, part2[q]);
             }
         }
+#pragma unroll
+        for (int q = 0; q < 4; ++q) f32x2_unpack(part2[q], part[2 * q], part[2 * q + 1]);
         float sq = 0.0f;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) sq = __fadd_rn(sq, part[j]);
+        for (int q = 0; q < 8; ++q) sq = __fadd_rn(sq, part[q]);
         const float var = __fmul_rn(warp_sum(sq), inv_c);
         const float rs = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(var, eps)));
         if (lane == 0) {
@@ -606,21 +643,20 @@ __global__ void __launch_bounds__(256) ln_stats_reg_kernel(const uint16_t *__res
             rstd[r] = rs;
         }
         if (amax_bits != nullptr) {
+            for (int i = lane; i < nvec; i += 32) {
+                const uint4 v = xr[i];
+                const uint4 g4 = reinterpret_cast<const uint4 *>(gamma)[i];
+                const uint4 b4 = reinterpret_cast<const uint4 *>(beta)[i];
+                const uint32_t w[4] = {v.x, v.y, v.z, v.w}, gw[4] = {g4.x, g4.y, g4.z, g4.w},
+                               bw[4] = {b4.x, b4.y, b4.z, b4.w};
 #pragma unroll
-            for (int u = 0; u < MAXV; ++u) {
-                if (lane + 32 * u >= nvec) break;
-                const uint4 g4 = reinterpret_cast<const uint4 *>(gamma)[lane + 32 * u];
-                const uint4 b4 = reinterpret_cast<const uint4 *>(beta)[lane + 32 * u];
-                const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w},
-                               gw[4] = {g4.x, g4.y, g4.z, g4.w}, bw[4] = {b4.x, b4.y, b4.z, b4.w};
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
+                for (int q = 0; q < 4; ++q) {
                     const float y0 = __fadd_rn(
-                        __fmul_rn(__fmul_rn(__fsub_rn(bf16_lo(w[j]), mu), rs), bf16_lo(gw[j])),
-                        bf16_lo(bw[j]));
+                        __fmul_rn(__fmul_rn(__fsub_rn(bf16_lo(w[q]), mu), rs), bf16_lo(gw[q])),
+                        bf16_lo(bw[q]));
                     const float y1 = __fadd_rn(
-                        __fmul_rn(__fmul_rn(__fsub_rn(bf16_hi(w[j]), mu), rs), bf16_hi(gw[j])),
-                        bf16_hi(bw[j]));
+                        __fmul_rn(__fmul_rn(__fsub_rn(bf16_hi(w[q]), mu), rs), bf16_hi(gw[q])),
+                        bf16_hi(bw[q]));
                     const uint32_t a0 = __float_as_uint(y0) & 0x7FFFFFFFu;
                     const uint32_t a1 = __float_as_uint(y1) & 0x7FFFFFFFu;
                     m = max(m, a0 > 0x7F800000u ? 0u : a0);
@@ -628,11 +664,39 @@ __global__ void __launch_bounds__(256) ln_stats_reg_kernel(const uint16_t *__res
                 }
             }
         }
+        // every lane is done with this buffer: refill it with a later row
+        __syncwarp();
+        if (lane == 0 && r + kLnBufs * warps < rows) issue(b, r + kLnBufs * warps);
+    }
+    if (failed) {
+        // a wait gave up: record it, and let this warp's copies still in
+        // flight land (bounded) before the CTA may exit
+        if (lane == 0) {
+            atomicOr(&g_cast_error_flags, kErrWaitTimeout);
+            for (int b = 0; b < kLnBufs; ++b)
+                if (issued[b] > consumed[b])
+                    mbar_wait(bar0 + 8 * b, static_cast<uint32_t>((issued[b] - 1) & 1), nullptr,
+                              100000000ull);
+        }
+        __syncwarp();
     }
     if (amax_bits != nullptr) {
         m = __reduce_max_sync(0xFFFFFFFFu, m);
         if (lane == 0 && m != 0) atomicMax(amax_bits, m);
     }
+}
+
+// Warps per block and dynamic shared memory of ln_stats_bulk_kernel for
+// rows of `cols` columns: two row buffers per warp in at most ~200 KB.
+inline int ln_bulk_warps(int64_t cols) {
+    const int64_t per_warp = kLnBufs * cols * 2;
+    int64_t w = (200 * 1024) / per_warp;
+    if (w > 16) w = 16;
+    return static_cast<int>(w);
+}
+inline size_t ln_bulk_smem(int warps, int64_t cols) {
+    return static_cast<size_t>(16 * warps * kLnBufs + 128) +
+           static_cast<size_t>(warps) * kLnBufs * static_cast<size_t>(cols) * 2;
 }
 
 cudaError_t launch_ln_stats(const void *x, const void *gamma, const void *beta, int64_t rows,
@@ -653,13 +717,24 @@ cudaError_t launch_ln_stats(const void *x, const void *gamma, const void *beta, 
     const uint16_t *gb = reinterpret_cast<const uint16_t *>(gamma);
     const uint16_t *bb = reinterpret_cast<const uint16_t *>(beta);
     unsigned *ab = reinterpret_cast<unsigned *>(amax);
-    // rows that fit in registers: one read of x
-    if (nvec <= 32 * 16)
-        return launch_pdl(ln_stats_reg_kernel<16>, grid, block, 0, st, xb, gb, bb, rows, cols, eps,
-                          mean, rstd, ab);
-    if (nvec <= 32 * 32)
-        return launch_pdl(ln_stats_reg_kernel<32>, grid, block, 0, st, xb, gb, bb, rows, cols, eps,
-                          mean, rstd, ab);
+    // rows of up to 8192 columns: staged in shared memory, one HBM read of x
+    if (nvec <= 1024) {
+        const int warps = ln_bulk_warps(cols);
+        const size_t smem = ln_bulk_smem(warps, cols);
+        // at most 200 KB of row buffers plus the barriers (ln_bulk_warps)
+        static std::once_flag once;
+        static cudaError_t attr_err = cudaSuccess;
+        std::call_once(once, [] {
+            attr_err = cudaFuncSetAttribute(ln_stats_bulk_kernel,
+                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                            210 * 1024);
+        });
+        if (attr_err != cudaSuccess) return attr_err;
+        int64_t bgrid = (rows + warps - 1) / warps;
+        if (bgrid > sm_count) bgrid = sm_count;
+        return launch_pdl(ln_stats_bulk_kernel, dim3(static_cast<unsigned>(bgrid)),
+                          dim3(32 * warps), smem, st, xb, gb, bb, rows, cols, eps, mean, rstd, ab);
+    }
     return launch_pdl(ln_stats_kernel, grid, block, 0, st,
                       reinterpret_cast<const uint16_t *>(x), reinterpret_cast<const uint16_t *>(gamma),
                       reinterpret_cast<const uint16_t *>(beta), rows, cols, eps, mean, rstd,

@@ -22,6 +22,7 @@
 #include <cuda_fp16.h>
 
 #include <cstdint>
+#include <mutex>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -256,30 +257,40 @@ __global__ void adam_scales_kernel(const AdamArgs a) {
 // zero is +0).  The parts of all ranks share one scale (the minimum of the
 // ranks' own scales), so their codes can be decoded and summed directly.
 //
-// No table and no FP64.  Each thread owns 16 consecutive elements and reads
-// 16 codes of a rank with one 16-byte load.  The codes are decoded exactly
-// by the hardware FP8 -> FP16 conversion (two codes per instruction) and
-// widened to fp32, and summed in fp32 where every partial sum is an exact
-// integer multiple of a power of two below 2^24 units:
-//   E4M3  values are multiples of 2^-9 of magnitude <= 448 (< 2^18 units),
-//         so one accumulator holds the exact sum of 64 ranks;
-//   E5M2  values span 2^-16 .. 57344, so each value v is split exactly into
-//         hi = v rounded to a multiple of 2^-2 ((v + 1.5 * 2^21) - 1.5 * 2^21:
-//         the sum lands in [2^21, 2^22), whose spacing is 2^-2) and
-//         lo = v - hi (a multiple of 2^-16, |lo| <= 2^-3); 64 ranks of hi
-//         stay below 2^24 units of 2^-2 and of lo below 2^24 units of 2^-16.
-// After every 64 ranks the fp32 sums move into an int64 count of quanta
-// (2^-9 for E4M3, 2^-16 for E5M2).  fl32(1 / scale) is sig * 2^es with a
-// 24-bit integer sig, so the exact result is |sum| * sig * 2^(es - q): one
-// 64-bit product for up to 256 ranks (|sum| < 2^40), a 128-bit one beyond.
-// It is rounded to BF16's 8 significant bits (or to its subnormal quantum
-// 2^-133) by one integer round-to-nearest-even and the BF16 bits are
-// assembled directly.  Infinity and NaN codes are found four codes at a time
-// and follow IEEE arithmetic (a NaN code, or +inf with -inf, give NaN; one
-// infinity gives that infinity times the factor); they leave the fp32 sums
-// meaningless, which the flags then override.
+// Layout: persistent blocks of 8 consumer warps and 1 producer warp walk
+// chunks of 4096 elements.  The producer stages each rank's 4 KB of codes of
+// a chunk into shared memory with untiled bulk copies, 8 ranks per stage, in
+// a ring of 3 stages, so HBM stays busy while the consumers compute; every
+// consumer thread owns 16 consecutive elements of the chunk.  Waits are
+// bounded.
+//
+// Arithmetic: no table, no FP64 and no conversion to or from fp32 (GB300
+// runs those on its narrow FP64 / conversion pipe).  Codes become exact
+// FP16 values two at a time (an E5M2 code is the top byte of its FP16
+// pattern; E4M3 takes cvt.rn.f16x2.e4m3x2), and PTX mixed-precision adds
+// (add.rn.f32.f16) put them into fp32 accumulators whose partial sums stay
+// exact integer multiples below 2^22 units: E4M3 in one accumulator, E5M2
+// split exactly in packed FP16 into a 2^-2 grid part and the remainder
+// (DqSums).  The fp32 sums become int64 counts of quanta (2^-9 for E4M3,
+// 2^-16 for E5M2) by the exact "magic number" conversion (adding 1.5 * 2^23
+// units puts the integer in the low mantissa bits), after every stage of 8
+// ranks when there are more than 8.  fl32(1 / scale) is sig * 2^es with a
+// 24-bit integer sig.  Each element is rounded once, by the first of three
+// tiers that applies: (1) up to 8 ranks, a sum that is one binary32 value a
+// (always for E4M3; for E5M2 when its parts add exactly): p = fl32(a * sinv)
+// with its exact fma error; (2) a result in BF16's normal range: the exact
+// 64-bit product |sum| * sig, normalised, its top 8 bits rounded to nearest
+// even with a sticky bit; (3) the general integer path (subnormal and
+// overflowing results, special codes, non-finite factors; a 128-bit product
+// beyond 256 ranks).  Special codes are detected with three integer
+// operations per four codes; a thread that saw one re-reads its codes and
+// follows IEEE arithmetic (a NaN code, or +inf with -inf, give NaN; one
+// infinity gives that infinity times the factor).
 
 constexpr uint32_t kBf16Nan = 0x7FC0u, kBf16Inf = 0x7F80u;
+
+// Set when the sum kernel gives up a bounded wait (read by fp8_sync_status).
+__device__ unsigned g_sum_error_flags = 0;
 
 // The factor fl32(1 / scale) as sig * 2^es (sig < 2^24; 0 for a zero factor)
 // with its sign and non-finite classes.
@@ -302,8 +313,9 @@ __device__ __forceinline__ DqFactor dq_factor(float sinv) {
     return f;
 }
 
-// BF16 bits of M' * 2^u after rounding the exact (hi:lo) * 2^E at the
-// quantum 2^u: u = (its leading bit) - 7, or BF16's subnormal quantum 2^-133.
+// General rounding: BF16 bits of the exact (hi:lo) * 2^E (not zero), at the
+// quantum 2^u with u = (its leading bit) - 7, or BF16's subnormal quantum
+// 2^-133; overflow gives inf.
 __device__ __forceinline__ uint32_t bf16_assemble(uint64_t hi, uint64_t lo, int E) {
     const int nb = hi ? 128 - __clzll(static_cast<long long>(hi))
                       : 64 - __clzll(static_cast<long long>(lo));
@@ -334,9 +346,9 @@ __device__ __forceinline__ uint32_t bf16_assemble(uint64_t hi, uint64_t lo, int 
     return bits;
 }
 
-// BF16 bits of acc * 2^QEXP * factor, exactly rounded (finite factor).
-// WIDE: |acc| may reach 2^48 (more than 256 ranks), so the product takes
-// two 64-bit words; otherwise |acc| < 2^40 and it fits one.
+// BF16 bits of acc * 2^QEXP * factor for a finite factor, by the general
+// rounding.  WIDE: |acc| may reach 2^48 (more than 256 ranks), so the
+// product takes two 64-bit words; otherwise |acc| < 2^40 and it fits one.
 template <int FMT, bool WIDE>
 __device__ __forceinline__ uint32_t bf16_of_scaled_sum(int64_t acc, const DqFactor &f) {
     constexpr int QEXP = FMT == 0 ? -9 : -16;
@@ -347,6 +359,8 @@ __device__ __forceinline__ uint32_t bf16_of_scaled_sum(int64_t acc, const DqFact
     return bf16_assemble(hi, lo, f.es + QEXP) | sign;
 }
 
+// The general path of one element: fe = its special flags (NaN 1, +inf 2,
+// -inf 4), acc = its exact sum of the finite codes.
 template <int FMT, bool WIDE>
 __device__ __forceinline__ uint32_t dq_finish(int64_t acc, uint32_t fe, const DqFactor &f) {
     if (fe == 0u) {
@@ -360,146 +374,354 @@ __device__ __forceinline__ uint32_t dq_finish(int64_t acc, uint32_t fe, const Dq
     return kBf16Inf | (((fe & 4u) ? 0x8000u : 0u) ^ f.sign);
 }
 
-__device__ __forceinline__ uint64_t f32x2_add(uint64_t a, uint64_t b) {
-    uint64_t r;
-    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-    return r;
+// The fast path for a finite, nonzero factor and |acc| < 2^40: BF16 bits of
+// acc * 2^QEXP * factor when the result's leading bit lies in BF16's normal
+// range (2^-126 .. 2^127; rounding may still overflow to inf); otherwise
+// sets `slow`.
+template <int FMT>
+__device__ __forceinline__ uint32_t bf16_fast(int64_t acc, const DqFactor &f, bool &slow) {
+    constexpr int QEXP = FMT == 0 ? -9 : -16;
+    if (acc == 0) return 0u;
+    const uint32_t sign = ((acc < 0) ? 0x8000u : 0u) ^ f.sign;
+    const uint64_t P = static_cast<uint64_t>(acc < 0 ? -acc : acc) * f.sig;   // < 2^64
+    const int lz = __clzll(static_cast<long long>(P));
+    const int lead = 63 - lz + f.es + QEXP;            // P * 2^E in [2^lead, 2^(lead+1))
+    if (lead < -126 || lead > 127) {
+        slow = true;
+        return 0u;
+    }
+    const uint64_t N = P << lz;                        // leading bit at bit 63
+    const uint32_t hi = static_cast<uint32_t>(N >> 32);
+    uint32_t M = hi >> 24;                             // the 8 significant bits kept
+    const uint32_t rest = (hi & 0xFFFFFFu) | (static_cast<uint32_t>(N) != 0u ? 1u : 0u);
+    M += (rest > 0x800000u || (rest == 0x800000u && (M & 1u))) ? 1u : 0u;
+    uint32_t bits = static_cast<uint32_t>((lead + 127) * 128) + M - 128u;   // carry moves up
+    if (bits >= kBf16Inf) bits = kBf16Inf;
+    return bits | sign;
 }
 
-// Two FP8 codes (low byte first) -> their exact values as a packed fp32 pair.
+// The fast path of up to 8 ranks, in binary32 arithmetic.  The element's
+// exact sum is a single binary32 value a (always for E4M3, whose sum stays
+// below 2^22 quanta; for E5M2 when the hi and lo parts add without rounding,
+// which a TwoSum shows).  p = fl32(a * sinv) and its exact error
+// e = fma(a, sinv, -p) then give the BF16 of a * sinv: rounding p to BF16
+// rounds a * sinv correctly unless p lies exactly on a BF16 midpoint while
+// e != 0 (rounding twice can differ only there, since every midpoint is a
+// binary32 value); then a * sinv lies beyond the midpoint on e's side.  A
+// product below 2^-100 (where e may not be exact) or an E5M2 sum that does
+// not fit sets `slow`.  hs / ls: the fp32 sums (E4M3: hs alone).
 template <int FMT>
-__device__ __forceinline__ uint64_t fp8x2_to_f32x2(uint32_t c2) {
-    uint32_t h2;
-    if constexpr (FMT == 0)
-        asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(static_cast<uint16_t>(c2)));
-    else
-        asm("cvt.rn.f16x2.e5m2x2 %0, %1;" : "=r"(h2) : "h"(static_cast<uint16_t>(c2)));
-    return f32x2_pack(__half2float(__ushort_as_half(static_cast<uint16_t>(h2 & 0xFFFFu))),
-                      __half2float(__ushort_as_half(static_cast<uint16_t>(h2 >> 16))));
+__device__ __forceinline__ float dq_exact_value(float hs, float ls, bool &slow) {
+    if constexpr (FMT == 0) {
+        return hs;
+    } else {
+        const float a = __fadd_rn(hs, ls);
+        const float bb = __fsub_rn(a, hs);
+        const float err = __fadd_rn(__fsub_rn(hs, __fsub_rn(a, bb)), __fsub_rn(ls, bb));
+        if (err != 0.0f) slow = true;                     // hs + ls needs more than 24 bits
+        return a;
+    }
+}
+
+// BF16 bits (in a 32-bit word, low half) of the exact a * sinv, a finite and
+// nonzero, sinv finite and nonzero.
+__device__ __forceinline__ uint32_t dq_round_product(float a, float sinv, bool &slow) {
+    const float p = __fmul_rn(a, sinv);
+    const float e = __fmaf_rn(a, sinv, -p);
+    if (!(fabsf(p) >= 0x1p-100f)) slow = true;
+    const uint32_t pb = __float_as_uint(p);
+    if ((pb & 0xFFFFu) == 0x8000u && e != 0.0f)         // on a midpoint, rounded: go e's way
+        return (pb >> 16) + (((pb ^ __float_as_uint(e)) >> 31) ? 0u : 1u);
+    return static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(p)));
 }
 
 // Flags of one word of four codes: 3 bits per code (NaN, +inf, -inf) at bit
 // 3 * (base + b).
 template <int FMT>
 __device__ __forceinline__ void dq_special_flags(uint32_t w, int base, uint64_t &flags) {
-    constexpr uint32_t smask = FMT == 0 ? 0x7F7F7F7Fu : 0x7C7C7C7Cu;   // bits that mark a special
-    if (!__vcmpeq4(w & smask, smask)) return;
 #pragma unroll
     for (int b = 0; b < 4; ++b) {
         const uint32_t cb = (w >> (8 * b)) & 0xFFu;
-        if ((cb & (smask & 0xFFu)) != (smask & 0xFFu)) continue;
-        uint64_t fl;
-        if (FMT == 0 || (cb & 3u) != 0u)
-            fl = 1u;                       // NaN
-        else
-            fl = (cb & 0x80u) ? 4u : 2u;   // -inf : +inf
+        uint64_t fl = 0;
+        if (FMT == 0) {
+            if ((cb & 0x7Fu) == 0x7Fu) fl = 1u;                           // NaN
+        } else if ((cb & 0x7Cu) == 0x7Cu) {
+            fl = (cb & 3u) ? 1u : ((cb & 0x80u) ? 4u : 2u);              // NaN, -inf, +inf
+        }
         flags |= fl << (3 * (base + b));
     }
 }
 
-constexpr int kDqElems = 16;        // elements per thread per pass (one 16-byte load per rank)
-constexpr int kDqFlushRanks = 64;   // ranks whose fp32 sums stay exact
+// Bit 7 of a byte of the result is set where the code in that byte of w is
+// special (E4M3: S.1111.111; E5M2: exponent 31); the additions carry into no
+// other byte.
+template <int FMT>
+__device__ __forceinline__ uint32_t dq_special_bits(uint32_t w) {
+    return FMT == 0 ? (w & 0x7F7F7F7Fu) + 0x01010101u : (w & 0x7C7C7C7Cu) + 0x04040404u;
+}
 
-// The exact fp32 sums of ranks [r_begin, r_end) of this thread's 16
-// elements, as packed pairs (elements 2p, 2p + 1); E5M2 keeps the hi and lo
-// parts apart.  Special codes are recorded in flags.
-template <int FMT, int NA>
-__device__ __forceinline__ void dq_sum_ranks(const uint8_t *__restrict__ q, int64_t n, int64_t i,
-                                             int r_begin, int r_end,
-                                             uint64_t (&s)[NA][kDqElems / 2], uint64_t &flags) {
-    const uint64_t C2 = splat_f32x2(3145728.0f);   // 1.5 * 2^21
+// 1.5 * 2^k as a binary32 constant (normal k).
+__host__ __device__ constexpr uint32_t magic_bits(int k) {
+    return (static_cast<uint32_t>(k + 127) << 23) | 0x400000u;
+}
+
+// An fp32 value that is an integer multiple n of 2^U with |n| < 2^22, as n:
+// adding 1.5 * 2^(23 + U) (exact: the sum keeps spacing 2^U) leaves n in the
+// low mantissa bits.
+template <int U>
+__device__ __forceinline__ long long f32_units(float a) {
+    const float m = __uint_as_float(magic_bits(U + 23));
+    return static_cast<long long>(static_cast<int32_t>(__float_as_uint(__fadd_rn(a, m)) -
+                                                       magic_bits(U + 23)));
+}
+
+constexpr int kDqElems = 16;                          // elements per consumer thread
+constexpr int kDqConsumers = 256;                     // consumer threads per block
+constexpr int kDqChunk = kDqConsumers * kDqElems;     // elements per chunk (4096)
+constexpr int kDqGroup = 8;                           // ranks per stage
+constexpr int kDqStages = 3;
+constexpr size_t kDqSmem = 128 + static_cast<size_t>(kDqStages) * kDqGroup * kDqChunk +
+                           2 * kDqStages * 8 + 16;
+
+// fp32 += FP16 value, one instruction: the FP16 operand is widened exactly
+// and the sum rounded once (PTX mixed-precision add).
+__device__ __forceinline__ float add_f32_f16(float acc, uint16_t h) {
+    asm("add.rn.f32.f16 %0, %1, %0;" : "+f"(acc) : "h"(h));
+    return acc;
+}
+
+// The fp32 sums of one thread's 16 elements.  Codes become exact FP16
+// values two at a time (E5M2: the code is the top byte of its FP16 pattern,
+// one byte permute per pair; E4M3: one cvt.rn.f16x2.e4m3x2 per pair) and
+// are added into fp32 accumulators by mixed-precision adds.  E4M3 values
+// are multiples of 2^-9 of magnitude <= 448 (< 2^18 units), so one
+// accumulator holds the exact sum of 16 ranks.  E5M2 values span
+// 2^-16 .. 57344, so each pair is split exactly in packed FP16: hi = v
+// rounded to a multiple of 2^-2 ((v + 384) - 384: for |v| < 128 the sum lies
+// in [256, 512), whose spacing is 2^-2; larger E5M2 values are multiples of
+// 32 and pass unchanged) and lo = v - hi (a multiple of 2^-16, |lo| <=
+// 2^-3); 16 ranks of each stay below 2^22 units.
+template <int FMT>
+struct DqSums {
+    static constexpr int NA = FMT == 0 ? 1 : 2;
+    float s[NA][kDqElems];
+    __device__ __forceinline__ void clear() {
 #pragma unroll
-    for (int a = 0; a < NA; ++a)
+        for (int a = 0; a < NA; ++a)
 #pragma unroll
-        for (int p = 0; p < kDqElems / 2; ++p) s[a][p] = 0u;
-    // four ranks' codes in flight at a time (every partial sum is exact, so
-    // the order in which ranks are added does not matter)
-    for (int r0 = r_begin; r0 < r_end; r0 += 4) {
-        uint4 c[4];
+            for (int e = 0; e < kDqElems; ++e) s[a][e] = 0.0f;
+    }
+    // add the 16 codes of one rank (one 16-byte vector)
+    __device__ __forceinline__ void add(const uint4 c, uint32_t &special) {
+        const uint32_t cw[4] = {c.x, c.y, c.z, c.w};
 #pragma unroll
-        for (int u = 0; u < 4; ++u)
-            c[u] = r0 + u < r_end ? *reinterpret_cast<const uint4 *>(
-                                        q + static_cast<int64_t>(r0 + u) * n + i)
-                                  : make_uint4(0u, 0u, 0u, 0u);   // code 0 adds +0
+        for (int h = 0; h < 4; ++h) {
+            special |= dq_special_bits<FMT>(cw[h]);
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const uint32_t cw[4] = {c[u].x, c[u].y, c[u].z, c[u].w};
-#pragma unroll
-            for (int h = 0; h < 4; ++h) {
-                dq_special_flags<FMT>(cw[h], 4 * h, flags);
-#pragma unroll
-                for (int k = 0; k < 2; ++k) {
-                    const uint64_t v = fp8x2_to_f32x2<FMT>(cw[h] >> (16 * k));
-                    const int p = 2 * h + k;
-                    if constexpr (FMT == 0) {
-                        s[0][p] = f32x2_add(s[0][p], v);
-                    } else {
-                        const uint64_t hi = f32x2_sub(f32x2_add(v, C2), C2);
-                        s[0][p] = f32x2_add(s[0][p], hi);
-                        s[NA - 1][p] = f32x2_add(s[NA - 1][p], f32x2_sub(v, hi));
-                    }
+            for (int k = 0; k < 4; k += 2) {
+                const int e = 4 * h + k;
+                uint32_t v2;   // FP16 values of codes k (low half) and k + 1
+                if constexpr (FMT == 0) {
+                    asm("cvt.rn.f16x2.e4m3x2 %0, %1;"
+                        : "=r"(v2)
+                        : "h"(static_cast<uint16_t>(cw[h] >> (8 * k))));
+                    s[0][e] = add_f32_f16(s[0][e], static_cast<uint16_t>(v2));
+                    s[0][e + 1] = add_f32_f16(s[0][e + 1], static_cast<uint16_t>(v2 >> 16));
+                } else {
+                    v2 = __byte_perm(cw[h], 0u, k == 0 ? 0x1404u : 0x3424u);
+                    const __half2 v = *reinterpret_cast<const __half2 *>(&v2);
+                    const __half2 c384 = __half2half2(__ushort_as_half(0x5E00u));   // 384
+                    const __half2 hi = __hsub2(__hadd2(v, c384), c384);
+                    const __half2 lo = __hsub2(v, hi);
+                    s[0][e] = add_f32_f16(s[0][e], __half_as_ushort(__low2half(hi)));
+                    s[0][e + 1] = add_f32_f16(s[0][e + 1], __half_as_ushort(__high2half(hi)));
+                    s[1][e] = add_f32_f16(s[1][e], __half_as_ushort(__low2half(lo)));
+                    s[1][e + 1] = add_f32_f16(s[1][e + 1], __half_as_ushort(__high2half(lo)));
                 }
             }
         }
     }
-}
-
-// Element e's exact fp32 sums as an integer count of quanta (2^-9 / 2^-16).
-template <int FMT, int NA>
-__device__ __forceinline__ long long dq_quanta(const uint64_t (&s)[NA][kDqElems / 2], int e) {
-    float a0, a1;
-    f32x2_unpack(s[0][e >> 1], a0, a1);
-    const float a = (e & 1) ? a1 : a0;
-    if constexpr (FMT == 0) {
-        return __float2ll_rn(a * 512.0f);
-    } else {
-        float b0, b1;
-        f32x2_unpack(s[NA - 1][e >> 1], b0, b1);
-        const float b = (e & 1) ? b1 : b0;
-        return (__float2ll_rn(a * 4.0f) << 14) + __float2ll_rn(b * 65536.0f);
+    // element e's exact sum as an integer count of quanta (2^-9 / 2^-16)
+    __device__ __forceinline__ long long quanta(int e) const {
+        if constexpr (FMT == 0)
+            return f32_units<-9>(s[0][e]);
+        else
+            return (f32_units<-2>(s[0][e]) << 14) + f32_units<-16>(s[NA - 1][e]);
     }
-}
+};
 
-// MODE 0: at most 64 ranks (one pass of fp32 sums, 64-bit product);
-// MODE 1: at most 256 ranks (int64 sums every 64 ranks, 64-bit product);
-// MODE 2: more (128-bit product).
+// MODE 0: at most 8 ranks (one stage, no int64 sums during the walk);
+// MODE 1: at most 256 ranks (int64 sums after every stage, 64-bit product);
+// MODE 2: more (128-bit product on the general path).
 template <int FMT, int MODE>
-__global__ void __launch_bounds__(256) dequant_sum_kernel(const uint8_t *__restrict__ q,
-                                                          int nranks, int64_t n,
-                                                          const float *__restrict__ scale,
-                                                          uint16_t *__restrict__ out) {
+__global__ void __launch_bounds__(kDqConsumers + 32, 2)
+    dequant_sum_kernel(const uint8_t *__restrict__ q, int nranks, int64_t n,
+                       const float *__restrict__ scale, uint16_t *__restrict__ out) {
+    extern __shared__ uint8_t dq_smem_raw[];
+    uint8_t *buf = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(dq_smem_raw) + 127) & ~static_cast<uintptr_t>(127));
+    uint64_t *bars = reinterpret_cast<uint64_t *>(buf + static_cast<size_t>(kDqStages) *
+                                                            kDqGroup * kDqChunk);
+    const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + kDqStages);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + 2 * kDqStages);
+    const int tid = threadIdx.x;
+    if (tid == 0) {
+        for (int st = 0; st < kDqStages; ++st) {
+            mbar_init(full0 + 8 * st, 1);
+            mbar_init(empty0 + 8 * st, kDqConsumers / 32);
+        }
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
     pdl_wait();
     pdl_trigger();
-    const DqFactor fac = dq_factor(__fdiv_rn(1.0f, *scale));
-    constexpr int NA = FMT == 0 ? 1 : 2;           // fp32 sums per element (E5M2: hi, lo)
-    constexpr bool WIDE = MODE == 2;
-    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x * kDqElems;
-    for (int64_t i = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) * kDqElems;
-         i < n; i += stride) {
-        uint64_t flags = 0;
-        long long acc[kDqElems];
-        uint64_t s[NA][kDqElems / 2];
-        if constexpr (MODE == 0) {
-            dq_sum_ranks<FMT, NA>(q, n, i, 0, nranks, s, flags);
-#pragma unroll
-            for (int e = 0; e < kDqElems; ++e) acc[e] = dq_quanta<FMT, NA>(s, e);
-        } else {
+    const int64_t nchunks = (n + kDqChunk - 1) / kDqChunk;
+    const int groups = (nranks + kDqGroup - 1) / kDqGroup;
+
+    if (tid >= kDqConsumers) {
+        // ------------------------------------------------------- producer
+        if (tid == kDqConsumers) {
+            int issued[kDqStages] = {};
+            int64_t j = 0;
+            bool ok = true;
+            for (int64_t c = blockIdx.x; ok && c < nchunks; c += gridDim.x) {
+                const int64_t e0 = c * kDqChunk;
+                const int64_t left = n - e0;
+                const uint32_t bytes = static_cast<uint32_t>(left < kDqChunk ? left : kDqChunk);
+                for (int gi = 0; gi < groups; ++gi, ++j) {
+                    const int st = static_cast<int>(j % kDqStages);
+                    if (j >= kDqStages &&
+                        !mbar_wait(empty0 + 8 * st,
+                                   static_cast<uint32_t>(((j / kDqStages) & 1) ^ 1), abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    const int r0 = gi * kDqGroup, nr = min(kDqGroup, nranks - r0);
+                    mbar_arrive_expect_tx(full0 + 8 * st, static_cast<uint32_t>(nr) * bytes);
+                    for (int u = 0; u < nr; ++u)
+                        bulk_load_1d(smem_u32(buf + (static_cast<size_t>(st) * kDqGroup + u) *
+                                                        kDqChunk),
+                                     q + static_cast<int64_t>(r0 + u) * n + e0, bytes,
+                                     full0 + 8 * st);
+                    ++issued[st];
+                }
+            }
+            if (!ok) {
+                atomicOr(&g_sum_error_flags, kErrWaitTimeout);
+                *abort_flag = 1;
+            }
+            // every copy issued must land before the block may exit
+            for (int st = 0; st < kDqStages; ++st)
+                if (issued[st] > 0)
+                    mbar_wait(full0 + 8 * st, static_cast<uint32_t>((issued[st] - 1) & 1), nullptr,
+                              100000000ull);
+        }
+        return;
+    }
+
+    // ---------------------------------------------------------- consumers
+    const int lane = tid & 31;
+    const float sinv = __fdiv_rn(1.0f, *scale);
+    const DqFactor fac = dq_factor(sinv);
+    const bool general = fac.is_nan || fac.is_inf || fac.sig == 0 || MODE == 2;
+    int64_t j = 0;
+    for (int64_t c = blockIdx.x; c < nchunks; c += gridDim.x) {
+        const int64_t i = c * kDqChunk + static_cast<int64_t>(tid) * kDqElems;
+        const bool in = i < n;
+        DqSums<FMT> sums;
+        sums.clear();
+        long long acc[MODE == 0 ? 1 : kDqElems];
+        if constexpr (MODE != 0) {
 #pragma unroll
             for (int e = 0; e < kDqElems; ++e) acc[e] = 0;
-            for (int f0 = 0; f0 < nranks; f0 += kDqFlushRanks) {
-                dq_sum_ranks<FMT, NA>(q, n, i, f0, min(nranks, f0 + kDqFlushRanks), s, flags);
+        }
+        uint32_t special = 0;
+        for (int gi = 0; gi < groups; ++gi, ++j) {
+            const int st = static_cast<int>(j % kDqStages);
+            const bool got = mbar_wait(full0 + 8 * st, static_cast<uint32_t>((j / kDqStages) & 1),
+                                       abort_flag);
+            if (!__all_sync(0xFFFFFFFFu, got)) {
+                if (lane == 0) {
+                    atomicOr(&g_sum_error_flags, kErrWaitTimeout);
+                    *abort_flag = 1;
+                }
+                return;
+            }
+            const int nr = min(kDqGroup, nranks - gi * kDqGroup);
+            if (in) {
+                const uint8_t *src = buf + static_cast<size_t>(st) * kDqGroup * kDqChunk +
+                                     static_cast<size_t>(tid) * kDqElems;
 #pragma unroll
-                for (int e = 0; e < kDqElems; ++e) acc[e] += dq_quanta<FMT, NA>(s, e);
+                for (int u = 0; u < kDqGroup; ++u)
+                    if (u < nr)
+                        sums.add(*reinterpret_cast<const uint4 *>(src + static_cast<size_t>(u) *
+                                                                            kDqChunk),
+                                 special);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(empty0 + 8 * st);
+            if constexpr (MODE != 0) {
+#pragma unroll
+                for (int e = 0; e < kDqElems; ++e) acc[e] += sums.quanta(e);
+                sums.clear();
             }
         }
+        if (!in) continue;
+        // special codes (re-read from global memory; rare) for the general path
+        uint64_t flags = 0;
+        if ((special & 0x80808080u) != 0u) {
+            for (int r = 0; r < nranks; ++r) {
+                const uint4 cv = *reinterpret_cast<const uint4 *>(q + static_cast<int64_t>(r) * n + i);
+                dq_special_flags<FMT>(cv.x, 0, flags);
+                dq_special_flags<FMT>(cv.y, 4, flags);
+                dq_special_flags<FMT>(cv.z, 8, flags);
+                dq_special_flags<FMT>(cv.w, 12, flags);
+            }
+        }
+        // three tiers: (1) binary32 arithmetic (up to 8 ranks, a sum that is
+        // one binary32 value), straight-line for all 16 elements; the
+        // elements it declines (bits of `declined`) then take (2) the
+        // normalised 64-bit integer rounding (results in BF16's normal
+        // range) or (3) the general path (special codes, non-finite factors,
+        // subnormal or overflowing results)
         uint32_t o[kDqElems / 2];
+        uint32_t declined = (general || MODE != 0) ? 0xFFFFu : 0u;
+        if (flags != 0u) {
 #pragma unroll
-        for (int j = 0; j < kDqElems / 2; ++j)
-            o[j] = dq_finish<FMT, WIDE>(acc[2 * j], static_cast<uint32_t>(flags >> (6 * j)) & 7u,
-                                        fac) |
-                   (dq_finish<FMT, WIDE>(acc[2 * j + 1],
-                                         static_cast<uint32_t>(flags >> (6 * j + 3)) & 7u, fac)
-                    << 16);
+            for (int e = 0; e < kDqElems; ++e)
+                if ((flags >> (3 * e)) & 7u) declined |= 1u << e;
+        }
+        if constexpr (MODE == 0) {
+            if (!general) {
+#pragma unroll
+                for (int e = 0; e < kDqElems; ++e) {
+                    bool slow = false;
+                    const float a = dq_exact_value<FMT>(sums.s[0][e],
+                                                        sums.s[DqSums<FMT>::NA - 1][e], slow);
+                    const uint32_t b = a == 0.0f ? 0u : dq_round_product(a, sinv, slow);
+                    if (slow) declined |= 1u << e;
+                    if (e & 1)
+                        o[e >> 1] |= (b & 0xFFFFu) << 16;
+                    else
+                        o[e >> 1] = b & 0xFFFFu;
+                }
+            }
+        }
+        if (declined != 0u) {
+#pragma unroll
+            for (int e = 0; e < kDqElems; ++e) {
+                if (!((declined >> e) & 1u)) continue;
+                const uint32_t fe = static_cast<uint32_t>(flags >> (3 * e)) & 7u;
+                const long long a = MODE == 0 ? sums.quanta(e) : acc[MODE == 0 ? 0 : e];
+                bool outside = general || fe != 0u;
+                uint32_t b = 0;
+                if (!outside) b = bf16_fast<FMT>(a, fac, outside);
+                if (outside) b = dq_finish<FMT, MODE == 2>(a, fe, fac);
+                const int w = e >> 1, sh = (e & 1) * 16;
+                o[w] = (o[w] & ~(0xFFFFu << sh)) | ((b & 0xFFFFu) << sh);
+            }
+        }
         uint4 *dst = reinterpret_cast<uint4 *>(out + i);
         dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
         dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
@@ -547,27 +769,47 @@ __global__ void __launch_bounds__(256) adam_init_kernel(const uint16_t *__restri
 
 }  // namespace
 
+template <int FMT, int MODE>
+cudaError_t launch_dq(int64_t grid, const uint8_t *parts, int nranks, int64_t n,
+                      const float *scale, uint16_t *o, cudaStream_t st) {
+    static std::once_flag once;
+    static cudaError_t attr = cudaSuccess;
+    std::call_once(once, [] {
+        attr = cudaFuncSetAttribute(dequant_sum_kernel<FMT, MODE>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    static_cast<int>(kDqSmem));
+    });
+    if (attr != cudaSuccess) return attr;
+    return launch_pdl(dequant_sum_kernel<FMT, MODE>, dim3(static_cast<unsigned>(grid)),
+                      dim3(kDqConsumers + 32), kDqSmem, st, parts, nranks, n, scale, o);
+}
+
 cudaError_t launch_dequant_sum(const uint8_t *parts, int nranks, int64_t n, int fmt,
                                const float *scale, void *out, int sm_count, cudaStream_t st) {
     if (n == 0) return cudaSuccess;
-    const int threads = 256;
-    int64_t blocks = (n / kDqElems + threads - 1) / threads;
-    const int64_t cap = static_cast<int64_t>(sm_count) * 8;
-    if (blocks > cap) blocks = cap;
+    const int64_t nchunks = (n + kDqChunk - 1) / kDqChunk;
+    const int64_t cap = static_cast<int64_t>(sm_count) * 2;   // two blocks per SM
+    const int64_t grid = nchunks < cap ? nchunks : cap;
     auto *o = static_cast<uint16_t *>(out);
-    const dim3 g(static_cast<unsigned>(blocks)), b(threads);
-    // up to 64 ranks the fp32 sums are exact in one pass; up to 256 the
-    // exact count of quanta stays below 2^40 (E5M2: 256 * 57344 * 2^16), so
-    // its product with a 24-bit significand fits 64 bits
-    const int mode = nranks <= kDqFlushRanks ? 0 : (nranks <= 256 ? 1 : 2);
+    // up to 8 ranks one stage holds them all; up to 256 the exact count of
+    // quanta stays below 2^40 (E5M2: 256 * 57344 * 2^16), so its product with
+    // a 24-bit significand fits 64 bits
+    const int mode = nranks <= kDqGroup ? 0 : (nranks <= 256 ? 1 : 2);
     if (fmt == 0) {
-        if (mode == 0) return launch_pdl(dequant_sum_kernel<0, 0>, g, b, 0, st, parts, nranks, n, scale, o);
-        if (mode == 1) return launch_pdl(dequant_sum_kernel<0, 1>, g, b, 0, st, parts, nranks, n, scale, o);
-        return launch_pdl(dequant_sum_kernel<0, 2>, g, b, 0, st, parts, nranks, n, scale, o);
+        if (mode == 0) return launch_dq<0, 0>(grid, parts, nranks, n, scale, o, st);
+        if (mode == 1) return launch_dq<0, 1>(grid, parts, nranks, n, scale, o, st);
+        return launch_dq<0, 2>(grid, parts, nranks, n, scale, o, st);
     }
-    if (mode == 0) return launch_pdl(dequant_sum_kernel<1, 0>, g, b, 0, st, parts, nranks, n, scale, o);
-    if (mode == 1) return launch_pdl(dequant_sum_kernel<1, 1>, g, b, 0, st, parts, nranks, n, scale, o);
-    return launch_pdl(dequant_sum_kernel<1, 2>, g, b, 0, st, parts, nranks, n, scale, o);
+    if (mode == 0) return launch_dq<1, 0>(grid, parts, nranks, n, scale, o, st);
+    if (mode == 1) return launch_dq<1, 1>(grid, parts, nranks, n, scale, o, st);
+    return launch_dq<1, 2>(grid, parts, nranks, n, scale, o, st);
+}
+
+cudaError_t read_and_clear_sum_error_flag(unsigned *flags) {
+    cudaError_t e = cudaMemcpyFromSymbol(flags, g_sum_error_flags, sizeof(unsigned));
+    if (e != cudaSuccess) return e;
+    const unsigned zero = 0;
+    return cudaMemcpyToSymbol(g_sum_error_flags, &zero, sizeof(unsigned));
 }
 
 cudaError_t launch_adam_init(const AdamInitSpec &s, int sm_count, cudaStream_t st) {
