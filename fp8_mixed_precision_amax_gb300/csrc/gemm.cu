@@ -57,7 +57,8 @@ namespace {
 constexpr int BM = 128, BN = 256, BK = 128;
 constexpr int NUM_THREADS = 192;
 constexpr int TMEM_COLS = 2 * BN;
-constexpr int GROUP_M = 16;                 // row-blocks per raster group when neither operand fits
+constexpr int GROUP_M = 16;                 // row-blocks per raster group when neither operand
+constexpr int GROUP_M_SMALL = 8;            // fits: GROUP_M when A is the smaller, else GROUP_M_SMALL
 constexpr int64_t RESIDENT_BYTES = 48 << 20;   // an operand this small is kept in L2
 constexpr int MAX_PROBLEMS = 2;
 constexpr int EPI_COLS = 64;                      // output columns per TMA store (128 B of BF16)
@@ -534,14 +535,19 @@ cudaError_t launch_gemm_group(const GemmSpec *specs, int n, int sm_count, cudaSt
         // one operand is small enough to stay in L2, walk so that it does
         // and the other streams through once: all row-blocks at a time when
         // A is the smaller (A resident), two row-blocks when B is (B
-        // resident).  Otherwise groups of GROUP_M row-blocks.
+        // resident).  When neither fits: groups of GROUP_M row-blocks when
+        // A is the smaller, so that the larger B is walked fewer times, and
+        // of GROUP_M_SMALL otherwise, which keeps more of B in L2 from one
+        // group's waves to the next.  (70B-shaped layer, DRAM bytes per
+        // launch: fprop 1.10 GB with 16 against 1.47 GB with 8; the grouped
+        // backward 3.85 GB with 8 and 8 against 4.51 GB with 16 and 16.)
         const int64_t a_bytes = g.M * g.K, b_bytes = g.N * g.K;
         if (a_bytes <= b_bytes && a_bytes <= RESIDENT_BYTES)
             p.group_m = p.tiles_m;
         else if (b_bytes < a_bytes && b_bytes <= RESIDENT_BYTES)
             p.group_m = 2;
         else
-            p.group_m = GROUP_M;
+            p.group_m = a_bytes < b_bytes ? GROUP_M : GROUP_M_SMALL;
         p.tile_begin = tiles;
         p.idesc = idesc_f8(static_cast<uint32_t>(g.fa), static_cast<uint32_t>(g.fb),
                            static_cast<uint32_t>(tile_m), BN);
