@@ -579,7 +579,7 @@ __global__ void __launch_bounds__(512) ln_stats_bulk_kernel(const uint16_t *__re
     const int64_t first = static_cast<int64_t>(blockIdx.x) * nw + wib;
     const int nvec = static_cast<int>(cols / 8);
     const float inv_c = __fdiv_rn(1.0f, static_cast<float>(cols));
-    int issued[kLnBufs] = {0, 0}, consumed[kLnBufs] = {0, 0};   // lane 0's counts
+    int issued[kLnBufs] = {}, consumed[kLnBufs] = {};   // lane 0's counts
     auto issue = [&](int b, int64_t r) {
         ++issued[b];
         mbar_arrive_expect_tx(bar0 + 8 * b, row_bytes);

@@ -386,13 +386,20 @@ fp8_status fp8_adam_init(const void *w, int64_t n, int32_t margin, uint8_t *m1, 
 /* The summing half of an FP8 all-reduce with one shared scale (wiki note,
  * bullet "per-tensor scaling is the key": every rank casts with the one
  * scalar s'_g = min(s'_1, ..., s'_N), so the exchanged FP8 codes of all ranks
- * can be summed directly).  After the ranks' codes have been gathered:
- *   out[i] = bf16_rne(fl32(sum_r dec(parts[r][i]) * fl32(1 / scale)))
- * with the sum (in rank order, exact) and the product in double.
- *   parts   DEVICE [nranks][n] FP8 codes of format fmt
+ * can be summed directly).  After this rank's shard of every rank's codes
+ * has been exchanged:
+ *   out[i] = bf16_rne( sum_r dec(parts[r][i]) * fl32(1 / scale) )
+ * with the sum and the product exact, rounded once to BF16 (nearest, ties to
+ * even; overflow to +-inf; gradual underflow, a nonzero result that rounds
+ * to zero keeps its sign; an exact zero is +0).  Special codes follow IEEE
+ * arithmetic: a NaN code, or +inf and -inf together, give NaN; one kind of
+ * infinity gives that infinity times fl32(1 / scale) (NaN when that factor
+ * is 0 or NaN).  The result does not depend on the order of the ranks.
+ *   parts   DEVICE [nranks][n] FP8 codes of format fmt, 16-byte aligned
  *   scale   DEVICE, 1 float: the shared scale the parts were cast with
  *   out     DEVICE [n] BF16 output
- * 1 <= nranks <= 65536; n >= 0, a multiple of 16. */
+ * 1 <= nranks <= 65536; n >= 0, a multiple of 16.  One kernel; it uses 96 KB
+ * of shared memory per block and no global scratch memory. */
 fp8_status fp8_dequant_sum(const uint8_t *parts, int32_t nranks, int64_t n, int32_t fmt,
                            const float *scale, void *out, void *stream);
 
