@@ -735,7 +735,9 @@ def secondary_cast_sweep(f):
 
 def secondary_layernorm_cast(f, w7, flush):
     """LayerNorm + cast of the 7B layer's X (statistics kernel + fused cast),
-    against the plain cast of the same tensor; 4 B/element algorithmic."""
+    against the plain cast of the same tensor; 4 B/element algorithmic.  The
+    forward-only cast (no transposed copy: one kernel, one read of X) is
+    timed too, 3 B/element algorithmic."""
     X = wl.layer_x(w7, 0, "cuda")
     g = torch.ones(w7.K, dtype=torch.bfloat16, device="cuda")
     b = torch.zeros(w7.K, dtype=torch.bfloat16, device="cuda")
@@ -751,12 +753,19 @@ def secondary_layernorm_cast(f, w7, flush):
                                                                       rstd, o8, o8t))
         flush.zero_()
         tm.time("cast", lambda: f.fp8_quantize_transpose(X, sc, 0, o8, o8t))
+        flush.zero_()
+        tm.time("ln_cast_rows", lambda: f.fp8_layernorm_quantize_transpose(
+            X, g, b, 1e-5, sc, 0, mean, rstd, o8, None))
     torch.cuda.synchronize()
     tm.pairs = {k: v[3:] for k, v in tm.pairs.items()}
     ne = w7.M * w7.K
     return {"ln_cast_us": tm.mean_ms("ln_cast") * 1e3, "cast_us": tm.mean_ms("cast") * 1e3,
             "ln_cast_gbs": 4 * ne / (tm.mean_ms("ln_cast") / 1e3) / 1e9,
-            "note": "4 B/element algorithmic; L2 flushed before each launch"}
+            "ln_cast_rows_us": tm.mean_ms("ln_cast_rows") * 1e3,
+            "ln_cast_rows_gbs": 3 * ne / (tm.mean_ms("ln_cast_rows") / 1e3) / 1e9,
+            "note": "4 B/element algorithmic with the transposed copy (two kernels), 3 B/element "
+                    "without it (ln_cast_rows: one kernel, one read of X); L2 flushed before "
+                    "each launch"}
 
 
 def secondary_adam(f, w7, flush):

@@ -480,6 +480,12 @@ fp8_status fp8_layernorm_quantize_transpose(const void *x, const void *gamma, co
     int sms;
     FP8_TRY(current_device(&sms));
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (out_t == nullptr && fp8k::ln_cast_rows_fits(rows, cols)) {   // one pass over x
+        FP8_CUDA(fp8k::launch_ln_cast_rows(x, gamma, beta, rows, cols, eps, scale, fmt, out, amax,
+                                           true, mean, rstd, sms, st),
+                 fn);
+        return FP8_OK;
+    }
     FP8_CUDA(fp8k::launch_ln_stats(x, gamma, beta, rows, cols, eps, mean, rstd, nullptr, sms, st),
              fn);
     const fp8k::CastSpec c{x, rows, cols, const_cast<float *>(scale), nullptr, out, out_t, amax,

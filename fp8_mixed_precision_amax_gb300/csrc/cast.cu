@@ -686,6 +686,184 @@ __global__ void __launch_bounds__(512) ln_stats_bulk_kernel(const uint16_t *__re
     }
 }
 
+// ------------------------------------ LayerNorm + row-major cast, one pass --
+//
+// Delayed scaling knows the scale before the cast, so when no transposed copy
+// is wanted (a forward-only LayerNorm cast) the statistics, the normalisation
+// and the cast can share one read of x (rows of at most 4096 columns).  Each
+// CTA owns a balanced, contiguous range of rows and has 16 warps; warp w
+// takes rows w, w + 16, ... of the range.  Every warp owns one row buffer: it
+// copies its row from the buffer into registers (16 vectors of 8 BF16 per
+// lane at most), at once starts the untiled bulk copy of its next row into
+// the same buffer, and works on the registers meanwhile.  From them it
+// computes mean and rstd with the same operations in the same order as
+// ln_stats_bulk_kernel (the results are identical bit for bit), then
+// y = ((x - mean) * rstd) * gamma + beta and its cast exactly as the
+// LayerNorm branch of quantize_transpose_kernel (gamma and beta staged in
+// shared memory once per CTA), and writes the codes.  (With a transposed copy
+// the codes of enough rows to write whole sectors of it do not fit in shared
+// memory beside the row buffers; that case keeps the two kernels.)  Waits
+// are bounded.
+
+constexpr int kLnfWarps = 16;
+constexpr int kLnfThreads = kLnfWarps * 32;
+constexpr int kLnfMaxCols = 4096;
+constexpr int kLnfVecs = kLnfMaxCols / 256;         // 16-byte vectors per lane
+
+template <int FMT>
+__global__ void __launch_bounds__(kLnfThreads, 1)
+    ln_cast_rows_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict__ gamma,
+                        const uint16_t *__restrict__ beta, int64_t rows, int cols, float eps,
+                        const float *__restrict__ scale, float *__restrict__ mean,
+                        float *__restrict__ rstd, uint8_t *__restrict__ out,
+                        unsigned *__restrict__ amax_bits) {
+    extern __shared__ uint8_t lnf_smem_raw[];
+    uint64_t *bars = reinterpret_cast<uint64_t *>(lnf_smem_raw);   // one per warp
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + kLnfWarps);
+    uint8_t *ring = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(bars + kLnfWarps + 1) + 127) & ~static_cast<uintptr_t>(127));
+    const uint32_t row_bytes = static_cast<uint32_t>(cols) * 2u;
+    uint16_t *gb_s = reinterpret_cast<uint16_t *>(ring + static_cast<size_t>(kLnfWarps) * row_bytes);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const uint32_t bar = smem_u32(bars + warp);
+    uint8_t *mybuf = ring + static_cast<size_t>(warp) * row_bytes;
+    const int64_t rbeg = rows * blockIdx.x / gridDim.x;
+    const int nrows = static_cast<int>(rows * (blockIdx.x + 1) / gridDim.x - rbeg);
+    if (lane == 0) mbar_init(bar, 1);
+    if (tid == 0) *abort_flag = 0;
+    fence_mbar_init();
+    __syncthreads();
+    pdl_wait();
+    pdl_trigger();
+    // this warp's first row in flight, then gamma and beta into shared memory
+    int issued = 0, consumed = 0;   // lane 0's copies into this warp's buffer
+    if (lane == 0 && warp < nrows) {
+        mbar_arrive_expect_tx(bar, row_bytes);
+        bulk_load_1d(smem_u32(mybuf), x + (rbeg + warp) * cols, row_bytes, bar);
+        ++issued;
+    }
+    const int nvec = cols / 8;
+    for (int i = tid; i < nvec; i += kLnfThreads) {
+        reinterpret_cast<uint4 *>(gb_s)[i] = reinterpret_cast<const uint4 *>(gamma)[i];
+        reinterpret_cast<uint4 *>(gb_s + cols)[i] = reinterpret_cast<const uint4 *>(beta)[i];
+    }
+    __syncthreads();
+
+    const float inv_c = __fdiv_rn(1.0f, static_cast<float>(cols));
+    const float s = *scale;
+    const uint64_t s2 = splat_f32x2(s);
+    float ymax = 0.0f;   // max |y|; fmaxf skips NaN
+    int use = 0;         // this warp's rows so far (the parity of its buffer)
+    for (int j = warp; j < nrows; j += kLnfWarps, ++use) {
+        const int64_t r = rbeg + j;
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait(bar, static_cast<uint32_t>(use & 1), abort_flag))) {
+            if (lane == 0) {
+                atomicOr(&g_cast_error_flags, kErrWaitTimeout);
+                *abort_flag = 1;
+            }
+            break;
+        }
+        if (lane == 0) ++consumed;
+        uint4 v[kLnfVecs];
+        const uint4 *xr = reinterpret_cast<const uint4 *>(mybuf);
+#pragma unroll
+        for (int t = 0; t < kLnfVecs; ++t) {
+            const int i = lane + 32 * t;
+            v[t] = i < nvec ? xr[i] : make_uint4(0u, 0u, 0u, 0u);
+        }
+        // the row is in registers: the buffer takes this warp's next row
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0 && j + kLnfWarps < nrows) {
+            mbar_arrive_expect_tx(bar, row_bytes);
+            bulk_load_1d(smem_u32(mybuf), x + (r + kLnfWarps) * cols, row_bytes, bar);
+            ++issued;
+        }
+        // the sum: eight partial sums per lane over vectors lane, lane + 32, ...
+        uint64_t part2[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+        for (int t = 0; t < kLnfVecs; ++t) {
+            if (lane + 32 * t >= nvec) break;
+            const uint32_t w[4] = {v[t].x, v[t].y, v[t].z, v[t].w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) part2[q] = f32x2_add(part2[q], f32x2_from_bf16x2(w[q]));
+        }
+        float part[8];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) f32x2_unpack(part2[q], part[2 * q], part[2 * q + 1]);
+        float sum = 0.0f;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) sum = __fadd_rn(sum, part[q]);
+        const float mu = __fmul_rn(warp_sum(sum), inv_c);
+        // the squared deviations, one fused multiply-add each
+        const uint64_t mu2 = splat_f32x2(mu);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) part2[q] = 0u;
+#pragma unroll
+        for (int t = 0; t < kLnfVecs; ++t) {
+            if (lane + 32 * t >= nvec) break;
+            const uint32_t w[4] = {v[t].x, v[t].y, v[t].z, v[t].w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const uint64_t d = f32x2_sub(f32x2_from_bf16x2(w[q]), mu2);
+                part2[q] = f32x2_fma(d, d, part2[q]);
+            }
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q) f32x2_unpack(part2[q], part[2 * q], part[2 * q + 1]);
+        float sq = 0.0f;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) sq = __fadd_rn(sq, part[q]);
+        const float var = __fmul_rn(warp_sum(sq), inv_c);
+        const float rs = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(var, eps)));
+        if (lane == 0) {
+            mean[r] = mu;
+            rstd[r] = rs;
+        }
+        // y and its codes: the subtract and both multiplies two lanes at a
+        // time, the add of beta scalar (a packed add of a packed product
+        // would be fused into an fma)
+        const uint64_t rs2 = splat_f32x2(rs);
+#pragma unroll
+        for (int t = 0; t < kLnfVecs; ++t) {
+            const int i = lane + 32 * t;
+            if (i >= nvec) break;
+            const uint4 g4 = reinterpret_cast<const uint4 *>(gb_s)[i];
+            const uint4 b4 = reinterpret_cast<const uint4 *>(gb_s + cols)[i];
+            const uint32_t xw[4] = {v[t].x, v[t].y, v[t].z, v[t].w};
+            const uint32_t gw[4] = {g4.x, g4.y, g4.z, g4.w}, bw[4] = {b4.x, b4.y, b4.z, b4.w};
+            uint32_t qw[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                float p0, p1, c0, c1;
+                f32x2_unpack(f32x2_mul(f32x2_mul(f32x2_sub(f32x2_from_bf16x2(xw[q]), mu2), rs2),
+                                       f32x2_from_bf16x2(gw[q])),
+                             p0, p1);
+                const float y0 = __fadd_rn(p0, bf16_lo(bw[q]));
+                const float y1 = __fadd_rn(p1, bf16_hi(bw[q]));
+                ymax = fmaxf(ymax, fmaxf(fabsf(y0), fabsf(y1)));
+                f32x2_unpack(f32x2_mul(f32x2_pack(y0, y1), s2), c0, c1);
+                qw[q] = cvt2_fp8<FMT>(c0, c1);
+            }
+            *reinterpret_cast<uint2 *>(out + r * cols + 8 * i) =
+                make_uint2(qw[0] | (qw[1] << 16), qw[2] | (qw[3] << 16));
+        }
+    }
+    // a copy still in flight (only after a wait gave up) lands before exit
+    if (lane == 0 && issued > consumed)
+        mbar_wait(bar, static_cast<uint32_t>((issued - 1) & 1), nullptr, 100000000ull);
+    // max |y| over the CTA
+    __shared__ uint32_t warp_max[kLnfWarps];
+    const uint32_t m = __reduce_max_sync(0xFFFFFFFFu, __float_as_uint(ymax));
+    if (lane == 0) warp_max[warp] = m;
+    __syncthreads();
+    if (tid < 32) {
+        uint32_t mm = tid < kLnfWarps ? warp_max[tid] : 0u;
+        mm = __reduce_max_sync(0xFFFFFFFFu, mm);
+        if (tid == 0 && mm != 0 && amax_bits != nullptr) atomicMax(amax_bits, mm);
+    }
+}
+
 // Warps per block and dynamic shared memory of ln_stats_bulk_kernel for
 // rows of `cols` columns: two row buffers per warp in at most ~200 KB.
 inline int ln_bulk_warps(int64_t cols) {
@@ -739,6 +917,57 @@ cudaError_t launch_ln_stats(const void *x, const void *gamma, const void *beta, 
                       reinterpret_cast<const uint16_t *>(x), reinterpret_cast<const uint16_t *>(gamma),
                       reinterpret_cast<const uint16_t *>(beta), rows, cols, eps, mean, rstd,
                       reinterpret_cast<unsigned *>(amax));
+}
+
+// Dynamic shared memory of ln_cast_rows_kernel: barriers, one row buffer per
+// warp, gamma and beta (BF16).
+inline size_t lnf_smem(int cols) {
+    return static_cast<size_t>(8 * kLnfWarps + 8 + 128) +
+           static_cast<size_t>(kLnfWarps) * 2 * static_cast<size_t>(cols) +
+           2 * 2 * static_cast<size_t>(cols);
+}
+
+bool ln_cast_rows_fits(int64_t rows, int64_t cols) {
+    return rows >= 0 && cols % 16 == 0 && cols >= 16 && cols <= kLnfMaxCols;
+}
+
+template <int FMT>
+static cudaError_t lnf_launch(dim3 grid, size_t smem, cudaStream_t st, const uint16_t *x,
+                              const uint16_t *g, const uint16_t *b, int64_t rows, int cols,
+                              float eps, const float *scale, float *mean, float *rstd,
+                              uint8_t *out, unsigned *ab) {
+    static std::once_flag once;
+    static cudaError_t attr = cudaSuccess;
+    std::call_once(once, [] {
+        attr = cudaFuncSetAttribute(ln_cast_rows_kernel<FMT>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, 160 * 1024);
+    });
+    if (attr != cudaSuccess) return attr;
+    return launch_pdl(ln_cast_rows_kernel<FMT>, grid, dim3(kLnfThreads), smem, st, x, g, b, rows,
+                      cols, eps, scale, mean, rstd, out, ab);
+}
+
+cudaError_t launch_ln_cast_rows(const void *x, const void *gamma, const void *beta, int64_t rows,
+                                int64_t cols, float eps, const float *scale, int fmt,
+                                uint8_t *out, float *amax, bool zero_amax, float *mean,
+                                float *rstd, int sm_count, cudaStream_t st) {
+    if (!ln_cast_rows_fits(rows, cols) || out == nullptr) return cudaErrorInvalidValue;
+    if (amax != nullptr && zero_amax) {
+        cudaError_t e = cudaMemsetAsync(amax, 0, sizeof(float), st);
+        if (e != cudaSuccess) return e;
+    }
+    if (rows == 0) return cudaSuccess;
+    const int c = static_cast<int>(cols);
+    const size_t smem = lnf_smem(c);
+    int64_t grid = (rows + kLnfWarps - 1) / kLnfWarps;
+    if (grid > sm_count) grid = sm_count;
+    const auto *xb = reinterpret_cast<const uint16_t *>(x);
+    const auto *gb = reinterpret_cast<const uint16_t *>(gamma);
+    const auto *bb = reinterpret_cast<const uint16_t *>(beta);
+    auto *ab = reinterpret_cast<unsigned *>(amax);
+    const dim3 g(static_cast<unsigned>(grid));
+    return fmt == 0 ? lnf_launch<0>(g, smem, st, xb, gb, bb, rows, c, eps, scale, mean, rstd, out, ab)
+                    : lnf_launch<1>(g, smem, st, xb, gb, bb, rows, c, eps, scale, mean, rstd, out, ab);
 }
 
 // ----------------------------------------------------------- scale update --

@@ -65,6 +65,16 @@ cudaError_t launch_ln_stats(const void *x, const void *gamma, const void *beta, 
                             int64_t cols, float eps, float *mean, float *rstd, float *amax,
                             int sm_count, cudaStream_t st);
 
+// LayerNorm statistics, normalisation and the row-major cast in one pass over
+// x (delayed scaling: the scale is given; no transposed copy).  Only where
+// ln_cast_rows_fits(rows, cols): cols a multiple of 16 of at most 4096.  max
+// |y| is max-combined into amax (optional), cleared first when zero_amax.
+bool ln_cast_rows_fits(int64_t rows, int64_t cols);
+cudaError_t launch_ln_cast_rows(const void *x, const void *gamma, const void *beta, int64_t rows,
+                                int64_t cols, float eps, const float *scale, int fmt,
+                                uint8_t *out, float *amax, bool zero_amax, float *mean,
+                                float *rstd, int sm_count, cudaStream_t st);
+
 // Up to two tensors of one format in one persistent cast launch (tiles form
 // one list).  current = just-in-time scaling (an amax pass per tensor first).
 cudaError_t launch_cast_group(const CastSpec *specs, int n, int fmt, bool current, int margin,

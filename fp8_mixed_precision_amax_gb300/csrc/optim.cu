@@ -269,9 +269,11 @@ __global__ void adam_scales_kernel(const AdamArgs a) {
 // FP16 values two at a time (an E5M2 code is the top byte of its FP16
 // pattern; E4M3 takes cvt.rn.f16x2.e4m3x2), and PTX mixed-precision adds
 // (add.rn.f32.f16) put them into fp32 accumulators whose partial sums stay
-// exact integer multiples below 2^22 units: E4M3 in one accumulator, E5M2
-// split exactly in packed FP16 into a 2^-2 grid part and the remainder
-// (DqSums).  The fp32 sums become int64 counts of quanta (2^-9 for E4M3,
+// exact integer multiples below 2^24 units: E4M3 in one accumulator; E5M2
+// in one accumulator too when each of a thread's codes is zero or at least
+// 2^-3 (those are multiples of 2^-5, and 8 of them stay below 2^24 such
+// units), else split exactly in packed FP16 into a 2^-2 grid part and the
+// remainder (DqSums).  The fp32 sums become int64 counts of quanta (2^-9 for E4M3,
 // 2^-16 for E5M2) by the exact "magic number" conversion (adding 1.5 * 2^23
 // units puts the integer in the low mantissa bits), after every stage of 8
 // ranks when there are more than 8.  fl32(1 / scale) is sig * 2^es with a
@@ -282,10 +284,13 @@ __global__ void adam_scales_kernel(const AdamArgs a) {
 // 64-bit product |sum| * sig, normalised, its top 8 bits rounded to nearest
 // even with a sticky bit; (3) the general integer path (subnormal and
 // overflowing results, special codes, non-finite factors; a 128-bit product
-// beyond 256 ranks).  Special codes are detected with three integer
-// operations per four codes; a thread that saw one re-reads its codes and
-// follows IEEE arithmetic (a NaN code, or +inf with -inf, give NaN; one
-// infinity gives that infinity times the factor).
+// beyond 256 ranks).  Special codes decode to FP16 infinities and NaN, so up
+// to 8 ranks an element's fp32 sum is not finite exactly when it holds one,
+// and only such an element reads its codes again; beyond 8 ranks they are
+// detected with three integer operations per four codes and a thread that
+// saw one re-reads its codes.  Either way they follow IEEE arithmetic (a NaN
+// code, or +inf with -inf, give NaN; one infinity gives that infinity times
+// the factor).
 
 constexpr uint32_t kBf16Nan = 0x7FC0u, kBf16Inf = 0x7F80u;
 
@@ -400,41 +405,6 @@ __device__ __forceinline__ uint32_t bf16_fast(int64_t acc, const DqFactor &f, bo
     return bits | sign;
 }
 
-// The fast path of up to 8 ranks, in binary32 arithmetic.  The element's
-// exact sum is a single binary32 value a (always for E4M3, whose sum stays
-// below 2^22 quanta; for E5M2 when the hi and lo parts add without rounding,
-// which a TwoSum shows).  p = fl32(a * sinv) and its exact error
-// e = fma(a, sinv, -p) then give the BF16 of a * sinv: rounding p to BF16
-// rounds a * sinv correctly unless p lies exactly on a BF16 midpoint while
-// e != 0 (rounding twice can differ only there, since every midpoint is a
-// binary32 value); then a * sinv lies beyond the midpoint on e's side.  A
-// product below 2^-100 (where e may not be exact) or an E5M2 sum that does
-// not fit sets `slow`.  hs / ls: the fp32 sums (E4M3: hs alone).
-template <int FMT>
-__device__ __forceinline__ float dq_exact_value(float hs, float ls, bool &slow) {
-    if constexpr (FMT == 0) {
-        return hs;
-    } else {
-        const float a = __fadd_rn(hs, ls);
-        const float bb = __fsub_rn(a, hs);
-        const float err = __fadd_rn(__fsub_rn(hs, __fsub_rn(a, bb)), __fsub_rn(ls, bb));
-        if (err != 0.0f) slow = true;                     // hs + ls needs more than 24 bits
-        return a;
-    }
-}
-
-// BF16 bits (in a 32-bit word, low half) of the exact a * sinv, a finite and
-// nonzero, sinv finite and nonzero.
-__device__ __forceinline__ uint32_t dq_round_product(float a, float sinv, bool &slow) {
-    const float p = __fmul_rn(a, sinv);
-    const float e = __fmaf_rn(a, sinv, -p);
-    if (!(fabsf(p) >= 0x1p-100f)) slow = true;
-    const uint32_t pb = __float_as_uint(p);
-    if ((pb & 0xFFFFu) == 0x8000u && e != 0.0f)         // on a midpoint, rounded: go e's way
-        return (pb >> 16) + (((pb ^ __float_as_uint(e)) >> 31) ? 0u : 1u);
-    return static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(p)));
-}
-
 // Flags of one word of four codes: 3 bits per code (NaN, +inf, -inf) at bit
 // 3 * (base + b).
 template <int FMT>
@@ -541,6 +511,31 @@ struct DqSums {
             }
         }
     }
+    // Add the 16 codes of one rank unsplit: one accumulator per element.
+    // E4M3 sums are always exact this way.  An E5M2 value of magnitude
+    // >= 2^-3 is a multiple of 2^-5, and 8 of them (at most 8 * 57344 <
+    // 2^19) stay below 2^24 such units, so their fp32 sum is exact too
+    // (e5m2_small_bits marks the codes for which it may not be).
+    __device__ __forceinline__ void add_direct(const uint4 c) {
+        const uint32_t cw[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+#pragma unroll
+            for (int k = 0; k < 4; k += 2) {
+                const int e = 4 * h + k;
+                uint32_t v2;
+                if constexpr (FMT == 0) {
+                    asm("cvt.rn.f16x2.e4m3x2 %0, %1;"
+                        : "=r"(v2)
+                        : "h"(static_cast<uint16_t>(cw[h] >> (8 * k))));
+                } else {
+                    v2 = __byte_perm(cw[h], 0u, k == 0 ? 0x1404u : 0x3424u);
+                }
+                s[0][e] = add_f32_f16(s[0][e], static_cast<uint16_t>(v2));
+                s[0][e + 1] = add_f32_f16(s[0][e + 1], static_cast<uint16_t>(v2 >> 16));
+            }
+        }
+    }
     // element e's exact sum as an integer count of quanta (2^-9 / 2^-16)
     __device__ __forceinline__ long long quanta(int e) const {
         if constexpr (FMT == 0)
@@ -549,6 +544,59 @@ struct DqSums {
             return (f32_units<-2>(s[0][e]) << 14) + f32_units<-16>(s[NA - 1][e]);
     }
 };
+
+// Bit 7 of a byte of the result is set where the E5M2 code in that byte of
+// the vector is nonzero and below 2^-3 in magnitude ((c & 0x7F) in 1 ..
+// 0x2F); no carry leaves a byte.
+__device__ __forceinline__ uint32_t e5m2_small_bits(const uint4 c) {
+    const uint32_t cw[4] = {c.x, c.y, c.z, c.w};
+    uint32_t small = 0;
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+        const uint32_t x = cw[h] & 0x7F7F7F7Fu;
+        small |= (x + 0x7F7F7F7Fu) & ~(x + 0x50505050u);
+    }
+    return small;
+}
+
+// The exact count of 2^-16 quanta of an unsplit E5M2 sum a (a multiple of
+// 2^-5 below 2^19): a = h + l with h = a rounded to a multiple of 2^-2 (by
+// adding and removing 1.5 * 2^21) and l = a - h, both exact.
+__device__ __forceinline__ long long e5m2_direct_quanta(float a) {
+    const float m = __uint_as_float(magic_bits(21));
+    const float t = __fadd_rn(a, m);
+    const long long hi = static_cast<int32_t>(__float_as_uint(t) - magic_bits(21));
+    return (hi << 14) + f32_units<-16>(__fsub_rn(a, __fsub_rn(t, m)));
+}
+
+// Special flags (NaN 1, +inf 2, -inf 4) of element k of the ranks' codes
+// (read from global memory; only for an element whose sum is not finite).
+template <int FMT>
+__device__ __forceinline__ uint32_t dq_element_flags(const uint8_t *q, int nranks, int64_t n,
+                                                     int64_t k) {
+    uint32_t fe = 0;
+    for (int r = 0; r < nranks; ++r) {
+        const uint32_t cb = q[static_cast<int64_t>(r) * n + k];
+        if (FMT == 0) {
+            if ((cb & 0x7Fu) == 0x7Fu) fe |= 1u;
+        } else if ((cb & 0x7Cu) == 0x7Cu) {
+            fe |= (cb & 3u) ? 1u : ((cb & 0x80u) ? 4u : 2u);
+        }
+    }
+    return fe;
+}
+
+// Tier 1 of the 8-rank path for a finite nonzero factor: p = fl32(a * sinv)
+// and e = fma(a, sinv, -p) (its exact error) give BF16(a * sinv) as the
+// rounding of p unless p is below 2^-100 (e may be inexact there), not
+// finite, or exactly a BF16 midpoint while e != 0 (there rounding twice can
+// differ from rounding once; every midpoint is a binary32 value).  A zero
+// sum gives +0 when the factor is positive.
+__device__ __forceinline__ bool dq_tier1_ok(float a, float p, float e, bool pos_factor) {
+    const float ap = fabsf(p);
+    const bool mid = (__float_as_uint(p) & 0xFFFFu) == 0x8000u && e != 0.0f;
+    return (ap >= 0x1p-100f && ap <= 0x1.fffffep127f && !mid) || (a == 0.0f && pos_factor);
+}
 
 // MODE 0: at most 8 ranks (one stage, no int64 sums during the walk);
 // MODE 1: at most 256 ranks (int64 sums after every stage, 64-bit product);
@@ -626,18 +674,16 @@ __global__ void __launch_bounds__(kDqConsumers + 32, 2)
     const DqFactor fac = dq_factor(sinv);
     const bool general = fac.is_nan || fac.is_inf || fac.sig == 0 || MODE == 2;
     int64_t j = 0;
-    for (int64_t c = blockIdx.x; c < nchunks; c += gridDim.x) {
-        const int64_t i = c * kDqChunk + static_cast<int64_t>(tid) * kDqElems;
-        const bool in = i < n;
-        DqSums<FMT> sums;
-        sums.clear();
-        long long acc[MODE == 0 ? 1 : kDqElems];
-        if constexpr (MODE != 0) {
-#pragma unroll
-            for (int e = 0; e < kDqElems; ++e) acc[e] = 0;
-        }
-        uint32_t special = 0;
-        for (int gi = 0; gi < groups; ++gi, ++j) {
+    if constexpr (MODE == 0) {
+        // one stage holds every rank; a thread's codes are added unsplit
+        // unless one of them is an E5M2 code below 2^-3, which needs the
+        // hi/lo split; special codes make the sum non-finite, and only such
+        // elements look at their codes again
+        const bool pos_factor = sinv > 0.0f;
+        const uint64_t sinv2 = splat_f32x2(sinv);
+        for (int64_t c = blockIdx.x; c < nchunks; c += gridDim.x, ++j) {
+            const int64_t i = c * kDqChunk + static_cast<int64_t>(tid) * kDqElems;
+            const bool in = i < n;
             const int st = static_cast<int>(j % kDqStages);
             const bool got = mbar_wait(full0 + 8 * st, static_cast<uint32_t>((j / kDqStages) & 1),
                                        abort_flag);
@@ -648,83 +694,191 @@ __global__ void __launch_bounds__(kDqConsumers + 32, 2)
                 }
                 return;
             }
-            const int nr = min(kDqGroup, nranks - gi * kDqGroup);
+            // the ranks' codes are added unsplit, or split when an E5M2 code
+            // below 2^-3 is among them
+            DqSums<FMT> sums;
+            sums.clear();
+            bool split = false;
             if (in) {
                 const uint8_t *src = buf + static_cast<size_t>(st) * kDqGroup * kDqChunk +
                                      static_cast<size_t>(tid) * kDqElems;
+                // rank 0's codes first: with a code below 2^-3 among them
+                // (codes spread over all binades) the thread splits at once
+                const uint4 c0 = *reinterpret_cast<const uint4 *>(src);
+                uint32_t small = 0;
+                if constexpr (FMT == 1) small = e5m2_small_bits(c0);
+                if ((small & 0x80808080u) == 0u) {
+                    sums.add_direct(c0);
 #pragma unroll
-                for (int u = 0; u < kDqGroup; ++u)
-                    if (u < nr)
-                        sums.add(*reinterpret_cast<const uint4 *>(src + static_cast<size_t>(u) *
-                                                                            kDqChunk),
-                                 special);
+                    for (int u = 1; u < kDqGroup; ++u) {
+                        if (u < nranks) {
+                            const uint4 cv = *reinterpret_cast<const uint4 *>(
+                                src + static_cast<size_t>(u) * kDqChunk);
+                            if constexpr (FMT == 1) small |= e5m2_small_bits(cv);
+                            sums.add_direct(cv);
+                        }
+                    }
+                }
+                if constexpr (FMT == 1) {
+                    if ((small & 0x80808080u) != 0u) {
+                        split = true;
+                        sums.clear();
+                        uint32_t unused = 0;
+#pragma unroll
+                        for (int u = 0; u < kDqGroup; ++u)
+                            if (u < nranks)
+                                sums.add(*reinterpret_cast<const uint4 *>(
+                                             src + static_cast<size_t>(u) * kDqChunk),
+                                         unused);
+                    }
+                }
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(empty0 + 8 * st);
-            if constexpr (MODE != 0) {
+            if (!in) continue;
+            // tier 1 takes a = the element's sum as one binary32 value: the
+            // unsplit sum, or hs + ls when that addition is exact, which
+            // (hs + ls) - hs == ls shows (Fast2Sum when |hs| >= |ls|;
+            // otherwise |hs| < |ls| <= 1 and the sum has at most 17 bits)
+            uint32_t o[kDqElems / 2];
+            bool odd = general;
+            if (!odd) {
+                float a[kDqElems];
+#pragma unroll
+                for (int e = 0; e < kDqElems; ++e) a[e] = sums.s[0][e];
+                if (split) {
+#pragma unroll
+                    for (int e = 0; e < kDqElems; ++e) {
+                        const float hs = sums.s[0][e], ls = sums.s[DqSums<FMT>::NA - 1][e];
+                        a[e] = __fadd_rn(hs, ls);
+                        if (__fsub_rn(a[e], hs) != ls) odd = true;
+                    }
+                }
+#pragma unroll
+                for (int e = 0; e < kDqElems; e += 2) {
+                    const uint64_t a2 = f32x2_pack(a[e], a[e + 1]);
+                    const uint64_t p2 = f32x2_mul(a2, sinv2);
+                    const uint64_t e2 = f32x2_fma(a2, sinv2, p2 ^ 0x8000000080000000ull);
+                    float p0, p1, e0, e1;
+                    f32x2_unpack(p2, p0, p1);
+                    f32x2_unpack(e2, e0, e1);
+                    if (!dq_tier1_ok(a[e], p0, e0, pos_factor) ||
+                        !dq_tier1_ok(a[e + 1], p1, e1, pos_factor))
+                        odd = true;
+                    uint32_t h;
+                    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(h) : "f"(p1), "f"(p0));
+                    o[e >> 1] = h;
+                }
+            } else {
+#pragma unroll
+                for (int w = 0; w < kDqElems / 2; ++w) o[w] = 0u;
+            }
+            if (odd) {
+                // the elements tier 1 declines: the exact count of quanta,
+                // rounded by the 64-bit path or the general one
+#pragma unroll
+                for (int e = 0; e < kDqElems; ++e) {
+                    const float hs = sums.s[0][e], ls = sums.s[DqSums<FMT>::NA - 1][e];
+                    bool declined = general;
+                    if (!declined) {
+                        const float a = split ? __fadd_rn(hs, ls) : hs;
+                        const float p = __fmul_rn(a, sinv);
+                        declined = (split && __fsub_rn(a, hs) != ls) ||
+                                   !dq_tier1_ok(a, p, __fmaf_rn(a, sinv, -p), pos_factor);
+                    }
+                    if (!declined) continue;
+                    const uint32_t fe =
+                        fabsf(hs) <= 0x1.fffffep127f ? 0u : dq_element_flags<FMT>(q, nranks, n, i + e);
+                    long long qa = 0;
+                    if (fe == 0u) {
+                        if constexpr (FMT == 0)
+                            qa = sums.quanta(e);
+                        else
+                            qa = split ? sums.quanta(e) : e5m2_direct_quanta(hs);
+                    }
+                    bool outside = general || fe != 0u;
+                    uint32_t b = 0;
+                    if (!outside) b = bf16_fast<FMT>(qa, fac, outside);
+                    if (outside) b = dq_finish<FMT, false>(qa, fe, fac);
+                    const int w = e >> 1, sh = (e & 1) * 16;
+                    o[w] = (o[w] & ~(0xFFFFu << sh)) | ((b & 0xFFFFu) << sh);
+                }
+            }
+            uint4 *dst = reinterpret_cast<uint4 *>(out + i);
+            dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+            dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+        }
+    } else {
+        // more than 8 ranks: int64 sums of quanta after every stage of 8
+        for (int64_t c = blockIdx.x; c < nchunks; c += gridDim.x) {
+            const int64_t i = c * kDqChunk + static_cast<int64_t>(tid) * kDqElems;
+            const bool in = i < n;
+            DqSums<FMT> sums;
+            sums.clear();
+            long long acc[kDqElems];
+#pragma unroll
+            for (int e = 0; e < kDqElems; ++e) acc[e] = 0;
+            uint32_t special = 0;
+            for (int gi = 0; gi < groups; ++gi, ++j) {
+                const int st = static_cast<int>(j % kDqStages);
+                const bool got = mbar_wait(full0 + 8 * st, static_cast<uint32_t>((j / kDqStages) & 1),
+                                           abort_flag);
+                if (!__all_sync(0xFFFFFFFFu, got)) {
+                    if (lane == 0) {
+                        atomicOr(&g_sum_error_flags, kErrWaitTimeout);
+                        *abort_flag = 1;
+                    }
+                    return;
+                }
+                const int nr = min(kDqGroup, nranks - gi * kDqGroup);
+                if (in) {
+                    const uint8_t *src = buf + static_cast<size_t>(st) * kDqGroup * kDqChunk +
+                                         static_cast<size_t>(tid) * kDqElems;
+#pragma unroll
+                    for (int u = 0; u < kDqGroup; ++u)
+                        if (u < nr)
+                            sums.add(*reinterpret_cast<const uint4 *>(src + static_cast<size_t>(u) *
+                                                                                kDqChunk),
+                                     special);
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(empty0 + 8 * st);
 #pragma unroll
                 for (int e = 0; e < kDqElems; ++e) acc[e] += sums.quanta(e);
                 sums.clear();
             }
-        }
-        if (!in) continue;
-        // special codes (re-read from global memory; rare) for the general path
-        uint64_t flags = 0;
-        if ((special & 0x80808080u) != 0u) {
-            for (int r = 0; r < nranks; ++r) {
-                const uint4 cv = *reinterpret_cast<const uint4 *>(q + static_cast<int64_t>(r) * n + i);
-                dq_special_flags<FMT>(cv.x, 0, flags);
-                dq_special_flags<FMT>(cv.y, 4, flags);
-                dq_special_flags<FMT>(cv.z, 8, flags);
-                dq_special_flags<FMT>(cv.w, 12, flags);
-            }
-        }
-        // three tiers: (1) binary32 arithmetic (up to 8 ranks, a sum that is
-        // one binary32 value), straight-line for all 16 elements; the
-        // elements it declines (bits of `declined`) then take (2) the
-        // normalised 64-bit integer rounding (results in BF16's normal
-        // range) or (3) the general path (special codes, non-finite factors,
-        // subnormal or overflowing results)
-        uint32_t o[kDqElems / 2];
-        uint32_t declined = (general || MODE != 0) ? 0xFFFFu : 0u;
-        if (flags != 0u) {
-#pragma unroll
-            for (int e = 0; e < kDqElems; ++e)
-                if ((flags >> (3 * e)) & 7u) declined |= 1u << e;
-        }
-        if constexpr (MODE == 0) {
-            if (!general) {
-#pragma unroll
-                for (int e = 0; e < kDqElems; ++e) {
-                    bool slow = false;
-                    const float a = dq_exact_value<FMT>(sums.s[0][e],
-                                                        sums.s[DqSums<FMT>::NA - 1][e], slow);
-                    const uint32_t b = a == 0.0f ? 0u : dq_round_product(a, sinv, slow);
-                    if (slow) declined |= 1u << e;
-                    if (e & 1)
-                        o[e >> 1] |= (b & 0xFFFFu) << 16;
-                    else
-                        o[e >> 1] = b & 0xFFFFu;
+            if (!in) continue;
+            // special codes (re-read from global memory; rare) for the general path
+            uint64_t flags = 0;
+            if ((special & 0x80808080u) != 0u) {
+                for (int r = 0; r < nranks; ++r) {
+                    const uint4 cv = *reinterpret_cast<const uint4 *>(q + static_cast<int64_t>(r) * n + i);
+                    dq_special_flags<FMT>(cv.x, 0, flags);
+                    dq_special_flags<FMT>(cv.y, 4, flags);
+                    dq_special_flags<FMT>(cv.z, 8, flags);
+                    dq_special_flags<FMT>(cv.w, 12, flags);
                 }
             }
-        }
-        if (declined != 0u) {
+            // each element: the normalised 64-bit integer rounding (results in
+            // BF16's normal range) or the general path (special codes,
+            // non-finite factors, subnormal or overflowing results)
+            uint32_t o[kDqElems / 2];
 #pragma unroll
             for (int e = 0; e < kDqElems; ++e) {
-                if (!((declined >> e) & 1u)) continue;
                 const uint32_t fe = static_cast<uint32_t>(flags >> (3 * e)) & 7u;
-                const long long a = MODE == 0 ? sums.quanta(e) : acc[MODE == 0 ? 0 : e];
                 bool outside = general || fe != 0u;
                 uint32_t b = 0;
-                if (!outside) b = bf16_fast<FMT>(a, fac, outside);
-                if (outside) b = dq_finish<FMT, MODE == 2>(a, fe, fac);
-                const int w = e >> 1, sh = (e & 1) * 16;
-                o[w] = (o[w] & ~(0xFFFFu << sh)) | ((b & 0xFFFFu) << sh);
+                if (!outside) b = bf16_fast<FMT>(acc[e], fac, outside);
+                if (outside) b = dq_finish<FMT, MODE == 2>(acc[e], fe, fac);
+                if (e & 1)
+                    o[e >> 1] |= (b & 0xFFFFu) << 16;
+                else
+                    o[e >> 1] = b & 0xFFFFu;
             }
+            uint4 *dst = reinterpret_cast<uint4 *>(out + i);
+            dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+            dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
         }
-        uint4 *dst = reinterpret_cast<uint4 *>(out + i);
-        dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
-        dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
     }
 }
 

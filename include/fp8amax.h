@@ -272,7 +272,9 @@ fp8_status fp8_quantize_transpose_grouped(const fp8_cast_desc *descs, int32_t n,
  *   rstd[r] = 1 / sqrt(var[r] + eps),
  *   y[r][c] = ((x[r][c] - mean[r]) * rstd[r]) * gamma[c] + beta[c]   (fp32),
  * then the cast of y exactly as fp8_quantize_transpose casts x (y is never
- * written out in BF16).  Two kernels: row statistics, then LayerNorm + cast.
+ * written out in BF16).  Two kernels: row statistics, then LayerNorm + cast;
+ * without out_t (a forward-only cast) and with rows of at most 4096 columns,
+ * one kernel and one read of x, with the same statistics bit for bit.
  *   x      DEVICE [rows][cols] BF16;  gamma, beta  DEVICE [cols] BF16
  *   eps    >= 0;  scale  DEVICE, 1 float;  fmt, out, out_t as fp8_quantize_transpose
  *   amax   DEVICE, 1 float overwritten with max |y| (fp32 y, NaN skipped), or NULL

@@ -122,6 +122,59 @@ def _grads(world, shape, seed):
     return out
 
 
+@pytest.mark.parametrize("nranks", [1, 3, 8])
+def test_dequant_sum_unsplit_e5m2_sums(nranks):
+    """E5M2 values that are zero or at least 2^-3 in magnitude are multiples
+    of 2^-5, so up to 8 of them add exactly in one fp32 sum; a nonzero value
+    below 2^-3 is not.  Threads whose 16 elements hold only the former take
+    the unsplit sum: here most do, a few elements carry one small code (so a
+    warp mixes both kinds), some cancel to an exact zero, some hold infinities
+    or NaN; the scales reach overflow, BF16's subnormal range, zero, negative
+    and non-finite factors.  Gradient-shaped codes (N(0, sigma_r) cast at a
+    shared scale, as the all-reduce makes them) follow."""
+    import fp8_mixed_precision_amax_gb300 as f
+    rng = np.random.default_rng(40 + nranks)
+    table = o.fp8_decode_table(o.E5M2)
+    finite = np.isfinite(table)
+    small = finite & (table != 0) & (np.abs(table) < 0.125)
+    big = np.nonzero(finite & ~small)[0].astype(np.uint8)
+    tiny = np.nonzero(small)[0].astype(np.uint8)
+    n = 8 * 4096 + 16
+    parts = rng.choice(big, size=(nranks, n))
+    k = np.arange(n)
+    sel = (k % 997 == 5)
+    parts[rng.integers(0, nranks, sel.sum()), k[sel]] = rng.choice(tiny, sel.sum())
+    if nranks >= 2:
+        z = (k % 61 == 7)
+        parts[:, z] = 0
+        parts[0, z] = rng.choice(big, z.sum())
+        parts[1, z] = parts[0, z] ^ 0x80
+    sp = (k % 1409 == 11)
+    parts[rng.integers(0, nranks, sp.sum()), k[sp]] = rng.choice(
+        np.array([0x7C, 0xFC, 0x7D, 0xFF], np.uint8), sp.sum())
+    assert not np.isin(parts[:, k % 997 != 5], tiny).any()
+    dev = torch.from_numpy(parts).cuda()
+    scales = [np.float32(10.0 ** rng.uniform(-3, 3)), np.float32(1.0), np.float32(-3.0),
+              np.float32(1e-30), np.float32(3e38), np.float32(2.0 ** -100),
+              np.float32(2.0 ** 120), np.float32(1e-45), np.float32(0.0),
+              np.float32(np.inf), np.float32(np.nan)]
+    for s in scales:
+        out = torch.empty(n, dtype=torch.bfloat16, device="cuda")
+        f.fp8_dequant_sum(dev, o.E5M2, torch.tensor([s], device="cuda"), out)
+        torch.cuda.synchronize()
+        assert _same_bf16(_u16(out), o.dequant_sum(parts, o.E5M2, s)), s
+    # gradient-shaped codes
+    n = 1 << 18
+    g = [rng.normal(0.0, 1e-3 * (1 + r / 10), n).astype(np.float32) for r in range(nranks)]
+    s = np.float32(57344.0 / max(float(np.abs(x).max()) for x in g))
+    parts = np.stack([o.quantize_f32(x, s, o.E5M2).reshape(-1) for x in g])
+    out = torch.empty(n, dtype=torch.bfloat16, device="cuda")
+    f.fp8_dequant_sum(torch.from_numpy(parts).cuda(), o.E5M2, torch.tensor([s], device="cuda"),
+                      out)
+    torch.cuda.synchronize()
+    assert np.array_equal(_u16(out), o.dequant_sum(parts, o.E5M2, s))
+
+
 def _worker(rank, world, port, shape, fmt, margin, q):
     import datetime
 

@@ -129,6 +129,49 @@ def test_layernorm_linear_step_matches_oracle():
     f.fp8_sync_status()
 
 
+def _ln_cast(f, x, gamma, beta, s, fmt, transposed):
+    rows, cols = x.shape
+    out = torch.empty((rows, cols), dtype=torch.uint8, device="cuda")
+    out_t = torch.empty((cols, rows), dtype=torch.uint8, device="cuda") if transposed else None
+    am = torch.full((1,), -1.0, device="cuda")
+    mean = torch.full((rows,), float("nan"), device="cuda")
+    rstd = torch.full((rows,), float("nan"), device="cuda")
+    f.fp8_layernorm_quantize_transpose(x, gamma, beta, 1e-5, torch.tensor([s], device="cuda"),
+                                       fmt, mean, rstd, out, out_t, am)
+    f.fp8_sync_status()
+    bits = lambda t: t.cpu().numpy().view(np.uint32)
+    return host_u8(out), (host_u8(out_t) if transposed else None), bits(mean), bits(rstd), \
+        bits(am)[0]
+
+
+@pytest.mark.parametrize("rows,cols", [(16, 16), (48, 272), (1040, 1024), (1040, 4096),
+                                       (8192, 4096), (48, 4112)])
+@pytest.mark.parametrize("fmt", [o.E4M3, o.E5M2])
+def test_layernorm_cast_one_pass_matches_two_kernels(rows, cols, fmt):
+    """Without a transposed copy, rows of up to 4096 columns take the one-pass
+    kernel (statistics, normalisation and cast from one read of x).  Its
+    codes, mean, rstd and amax must equal, bit for bit, those of the two-kernel
+    path (statistics kernel, then the cast with its transposed copy) on the
+    same input -- up to the 7B layer's X (8192 x 4096); the two-kernel result
+    is checked against the oracle as above.  (48, 4112) is past the one-pass
+    limit and takes two kernels both times."""
+    f = _lib()
+    x, gamma, beta = _inputs(rows, cols, 77 + rows + fmt)
+    s = np.float32(448.0 / 6.0) if fmt == o.E4M3 else np.float32(57344.0 / 6.0)
+    q1, _, m1, r1, a1 = _ln_cast(f, x, gamma, beta, s, fmt, False)
+    q2, q2t, m2, r2, a2 = _ln_cast(f, x, gamma, beta, s, fmt, True)
+    assert np.array_equal(m1, m2) and np.array_equal(r1, r2) and a1 == a2
+    assert np.array_equal(q1, q2)
+    assert np.array_equal(q2t, q2.T)
+    xb, gb, bb = host_bf16_bits(x), host_bf16_bits(gamma), host_bf16_bits(beta)
+    y, mu, rs = o.layernorm(xb, gb, bb, 1e-5)
+    mean = m2.view(np.float32)
+    assert np.allclose(mean, mu, rtol=1e-5, atol=1e-5 * np.abs(mu).max())
+    assert np.allclose(r2.view(np.float32), rs, rtol=1e-5)
+    check_elementwise_exact(q2, xb, gb, bb, mean, r2.view(np.float32), s, fmt,
+                            np.uint32(a2).view(np.float32), f"{rows}x{cols}")
+
+
 @pytest.mark.parametrize("cols", [4096, 8192, 12288])
 def test_layernorm_constant_rows(cols):
     """Degenerate rows whose elements are all equal: the variance is 0, so
