@@ -542,13 +542,14 @@ __global__ void __launch_bounds__(256) ln_stats_kernel(const uint16_t *__restric
 }
 
 // The same statistics for rows of at most 8192 columns, each row staged in
-// shared memory by an untiled bulk copy.  Every warp owns two row buffers:
-// while it reduces one row its next row is already in flight, so the loads
-// of all warps keep HBM busy through the reductions (a row read only into
-// registers left the loads idle while each warp reduced).  The sum, the
-// squared deviations and the optional amax(y) read the staged row; each lane
-// visits its vectors in the same order as ln_stats_kernel, so the fp32
-// results are the same bit for bit.  Waits are bounded.
+// shared memory by an untiled bulk copy.  Each CTA owns a balanced
+// contiguous range of rows, dealt to its warps in turn.  Every warp owns two
+// row buffers: while it reduces one row its next row is already in flight,
+// so the loads of all warps keep HBM busy through the reductions (a row read
+// only into registers left the loads idle while each warp reduced).  The
+// sum, the squared deviations and the optional amax(y) read the staged row;
+// each lane visits its vectors in the same order as ln_stats_kernel, so the
+// fp32 results are the same bit for bit.  Waits are bounded.
 constexpr int kLnBufs = 2;
 
 __global__ void __launch_bounds__(512) ln_stats_bulk_kernel(const uint16_t *__restrict__ x,
@@ -575,8 +576,11 @@ __global__ void __launch_bounds__(512) ln_stats_bulk_kernel(const uint16_t *__re
     __syncwarp();
     pdl_wait();
     pdl_trigger();
-    const int64_t warps = static_cast<int64_t>(gridDim.x) * nw;
-    const int64_t first = static_cast<int64_t>(blockIdx.x) * nw + wib;
+    // this CTA's rows: a balanced contiguous range, dealt to its warps in turn
+    // (a grid-wide deal would give some SMs a whole extra round of rows)
+    const int64_t rend = rows * (blockIdx.x + 1) / gridDim.x;
+    const int64_t first = rows * blockIdx.x / gridDim.x + wib;
+    const int64_t warps = nw;
     const int nvec = static_cast<int>(cols / 8);
     const float inv_c = __fdiv_rn(1.0f, static_cast<float>(cols));
     int issued[kLnBufs] = {}, consumed[kLnBufs] = {};   // lane 0's counts
@@ -587,11 +591,11 @@ __global__ void __launch_bounds__(512) ln_stats_bulk_kernel(const uint16_t *__re
     };
     if (lane == 0)
         for (int b = 0; b < kLnBufs; ++b)
-            if (first + b * warps < rows) issue(b, first + b * warps);
+            if (first + b * warps < rend) issue(b, first + b * warps);
     uint32_t m = 0;
     bool failed = false;
     int64_t j = 0;
-    for (int64_t r = first; r < rows; r += warps, ++j) {
+    for (int64_t r = first; r < rend; r += warps, ++j) {
         const int b = static_cast<int>(j % kLnBufs);
         const uint32_t parity = static_cast<uint32_t>((j / kLnBufs) & 1);
         if (!__all_sync(0xFFFFFFFFu, mbar_wait(bar0 + 8 * b, parity, nullptr))) {
@@ -666,7 +670,7 @@ __global__ void __launch_bounds__(512) ln_stats_bulk_kernel(const uint16_t *__re
         }
         // every lane is done with this buffer: refill it with a later row
         __syncwarp();
-        if (lane == 0 && r + kLnBufs * warps < rows) issue(b, r + kLnBufs * warps);
+        if (lane == 0 && r + kLnBufs * warps < rend) issue(b, r + kLnBufs * warps);
     }
     if (failed) {
         // a wait gave up: record it, and let this warp's copies still in
@@ -690,7 +694,9 @@ __global__ void __launch_bounds__(512) ln_stats_bulk_kernel(const uint16_t *__re
 //
 // Delayed scaling knows the scale before the cast, so when no transposed copy
 // is wanted (a forward-only LayerNorm cast) the statistics, the normalisation
-// and the cast can share one read of x (rows of at most 4096 columns).  Each
+// and the cast can share one read of x (rows of at most 4096 columns).  The
+// same kernel computes the statistics alone (and max |y| for just-in-time
+// scaling) ahead of the two-kernel cast of such rows.  Each
 // CTA owns a balanced, contiguous range of rows and has 16 warps; warp w
 // takes rows w, w + 16, ... of the range.  Every warp owns one row buffer: it
 // copies its row from the buffer into registers (16 vectors of 8 BF16 per
@@ -710,7 +716,11 @@ constexpr int kLnfThreads = kLnfWarps * 32;
 constexpr int kLnfMaxCols = 4096;
 constexpr int kLnfVecs = kLnfMaxCols / 256;         // 16-byte vectors per lane
 
-template <int FMT>
+// MODE kLnfStats: mean and rstd only; kLnfStatsAmax: and max |y|; kLnfCast:
+// and the codes of y (out) with max |y|.
+constexpr int kLnfStats = 0, kLnfStatsAmax = 1, kLnfCast = 2;
+
+template <int FMT, int MODE>
 __global__ void __launch_bounds__(kLnfThreads, 1)
     ln_cast_rows_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict__ gamma,
                         const uint16_t *__restrict__ beta, int64_t rows, int cols, float eps,
@@ -743,15 +753,16 @@ __global__ void __launch_bounds__(kLnfThreads, 1)
         ++issued;
     }
     const int nvec = cols / 8;
-    for (int i = tid; i < nvec; i += kLnfThreads) {
-        reinterpret_cast<uint4 *>(gb_s)[i] = reinterpret_cast<const uint4 *>(gamma)[i];
-        reinterpret_cast<uint4 *>(gb_s + cols)[i] = reinterpret_cast<const uint4 *>(beta)[i];
+    if constexpr (MODE != kLnfStats) {
+        for (int i = tid; i < nvec; i += kLnfThreads) {
+            reinterpret_cast<uint4 *>(gb_s)[i] = reinterpret_cast<const uint4 *>(gamma)[i];
+            reinterpret_cast<uint4 *>(gb_s + cols)[i] = reinterpret_cast<const uint4 *>(beta)[i];
+        }
     }
     __syncthreads();
 
     const float inv_c = __fdiv_rn(1.0f, static_cast<float>(cols));
-    const float s = *scale;
-    const uint64_t s2 = splat_f32x2(s);
+    const uint64_t s2 = splat_f32x2(MODE == kLnfCast ? *scale : 1.0f);
     float ymax = 0.0f;   // max |y|; fmaxf skips NaN
     int use = 0;         // this warp's rows so far (the parity of its buffer)
     for (int j = warp; j < nrows; j += kLnfWarps, ++use) {
@@ -820,6 +831,7 @@ __global__ void __launch_bounds__(kLnfThreads, 1)
             mean[r] = mu;
             rstd[r] = rs;
         }
+        if constexpr (MODE == kLnfStats) continue;
         // y and its codes: the subtract and both multiplies two lanes at a
         // time, the add of beta scalar (a packed add of a packed product
         // would be fused into an fma)
@@ -842,11 +854,14 @@ __global__ void __launch_bounds__(kLnfThreads, 1)
                 const float y0 = __fadd_rn(p0, bf16_lo(bw[q]));
                 const float y1 = __fadd_rn(p1, bf16_hi(bw[q]));
                 ymax = fmaxf(ymax, fmaxf(fabsf(y0), fabsf(y1)));
-                f32x2_unpack(f32x2_mul(f32x2_pack(y0, y1), s2), c0, c1);
-                qw[q] = cvt2_fp8<FMT>(c0, c1);
+                if constexpr (MODE == kLnfCast) {
+                    f32x2_unpack(f32x2_mul(f32x2_pack(y0, y1), s2), c0, c1);
+                    qw[q] = cvt2_fp8<FMT>(c0, c1);
+                }
             }
-            *reinterpret_cast<uint2 *>(out + r * cols + 8 * i) =
-                make_uint2(qw[0] | (qw[1] << 16), qw[2] | (qw[3] << 16));
+            if constexpr (MODE == kLnfCast)
+                *reinterpret_cast<uint2 *>(out + r * cols + 8 * i) =
+                    make_uint2(qw[0] | (qw[1] << 16), qw[2] | (qw[3] << 16));
         }
     }
     // a copy still in flight (only after a wait gave up) lands before exit
@@ -877,6 +892,39 @@ inline size_t ln_bulk_smem(int warps, int64_t cols) {
            static_cast<size_t>(warps) * kLnBufs * static_cast<size_t>(cols) * 2;
 }
 
+// Dynamic shared memory of ln_cast_rows_kernel: barriers, one row buffer per
+// warp, gamma and beta (BF16).
+inline size_t lnf_smem(int cols) {
+    return static_cast<size_t>(8 * kLnfWarps + 8 + 128) +
+           static_cast<size_t>(kLnfWarps) * 2 * static_cast<size_t>(cols) +
+           2 * 2 * static_cast<size_t>(cols);
+}
+
+bool ln_cast_rows_fits(int64_t rows, int64_t cols) {
+    return rows >= 0 && cols % 16 == 0 && cols >= 16 && cols <= kLnfMaxCols;
+}
+
+template <int FMT, int MODE>
+static cudaError_t lnf_launch(int64_t rows, int cols, int sm_count, cudaStream_t st,
+                              const void *x, const void *g, const void *b, float eps,
+                              const float *scale, float *mean, float *rstd, uint8_t *out,
+                              float *amax) {
+    static std::once_flag once;
+    static cudaError_t attr = cudaSuccess;
+    std::call_once(once, [] {
+        attr = cudaFuncSetAttribute(ln_cast_rows_kernel<FMT, MODE>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, 160 * 1024);
+    });
+    if (attr != cudaSuccess) return attr;
+    int64_t grid = (rows + kLnfWarps - 1) / kLnfWarps;
+    if (grid > sm_count) grid = sm_count;
+    return launch_pdl(ln_cast_rows_kernel<FMT, MODE>, dim3(static_cast<unsigned>(grid)),
+                      dim3(kLnfThreads), lnf_smem(cols), st,
+                      reinterpret_cast<const uint16_t *>(x), reinterpret_cast<const uint16_t *>(g),
+                      reinterpret_cast<const uint16_t *>(b), rows, cols, eps, scale, mean, rstd,
+                      out, reinterpret_cast<unsigned *>(amax));
+}
+
 cudaError_t launch_ln_stats(const void *x, const void *gamma, const void *beta, int64_t rows,
                             int64_t cols, float eps, float *mean, float *rstd, float *amax,
                             int sm_count, cudaStream_t st) {
@@ -895,6 +943,15 @@ cudaError_t launch_ln_stats(const void *x, const void *gamma, const void *beta, 
     const uint16_t *gb = reinterpret_cast<const uint16_t *>(gamma);
     const uint16_t *bb = reinterpret_cast<const uint16_t *>(beta);
     unsigned *ab = reinterpret_cast<unsigned *>(amax);
+    // rows of up to 4096 columns: held in registers, one HBM read of x
+    if (ln_cast_rows_fits(rows, cols)) {
+        const int c = static_cast<int>(cols);
+        return amax != nullptr
+                   ? lnf_launch<0, kLnfStatsAmax>(rows, c, sm_count, st, x, gamma, beta, eps,
+                                                   nullptr, mean, rstd, nullptr, amax)
+                   : lnf_launch<0, kLnfStats>(rows, c, sm_count, st, x, gamma, beta, eps, nullptr,
+                                              mean, rstd, nullptr, nullptr);
+    }
     // rows of up to 8192 columns: staged in shared memory, one HBM read of x
     if (nvec <= 1024) {
         const int warps = ln_bulk_warps(cols);
@@ -919,34 +976,6 @@ cudaError_t launch_ln_stats(const void *x, const void *gamma, const void *beta, 
                       reinterpret_cast<unsigned *>(amax));
 }
 
-// Dynamic shared memory of ln_cast_rows_kernel: barriers, one row buffer per
-// warp, gamma and beta (BF16).
-inline size_t lnf_smem(int cols) {
-    return static_cast<size_t>(8 * kLnfWarps + 8 + 128) +
-           static_cast<size_t>(kLnfWarps) * 2 * static_cast<size_t>(cols) +
-           2 * 2 * static_cast<size_t>(cols);
-}
-
-bool ln_cast_rows_fits(int64_t rows, int64_t cols) {
-    return rows >= 0 && cols % 16 == 0 && cols >= 16 && cols <= kLnfMaxCols;
-}
-
-template <int FMT>
-static cudaError_t lnf_launch(dim3 grid, size_t smem, cudaStream_t st, const uint16_t *x,
-                              const uint16_t *g, const uint16_t *b, int64_t rows, int cols,
-                              float eps, const float *scale, float *mean, float *rstd,
-                              uint8_t *out, unsigned *ab) {
-    static std::once_flag once;
-    static cudaError_t attr = cudaSuccess;
-    std::call_once(once, [] {
-        attr = cudaFuncSetAttribute(ln_cast_rows_kernel<FMT>,
-                                    cudaFuncAttributeMaxDynamicSharedMemorySize, 160 * 1024);
-    });
-    if (attr != cudaSuccess) return attr;
-    return launch_pdl(ln_cast_rows_kernel<FMT>, grid, dim3(kLnfThreads), smem, st, x, g, b, rows,
-                      cols, eps, scale, mean, rstd, out, ab);
-}
-
 cudaError_t launch_ln_cast_rows(const void *x, const void *gamma, const void *beta, int64_t rows,
                                 int64_t cols, float eps, const float *scale, int fmt,
                                 uint8_t *out, float *amax, bool zero_amax, float *mean,
@@ -958,16 +987,10 @@ cudaError_t launch_ln_cast_rows(const void *x, const void *gamma, const void *be
     }
     if (rows == 0) return cudaSuccess;
     const int c = static_cast<int>(cols);
-    const size_t smem = lnf_smem(c);
-    int64_t grid = (rows + kLnfWarps - 1) / kLnfWarps;
-    if (grid > sm_count) grid = sm_count;
-    const auto *xb = reinterpret_cast<const uint16_t *>(x);
-    const auto *gb = reinterpret_cast<const uint16_t *>(gamma);
-    const auto *bb = reinterpret_cast<const uint16_t *>(beta);
-    auto *ab = reinterpret_cast<unsigned *>(amax);
-    const dim3 g(static_cast<unsigned>(grid));
-    return fmt == 0 ? lnf_launch<0>(g, smem, st, xb, gb, bb, rows, c, eps, scale, mean, rstd, out, ab)
-                    : lnf_launch<1>(g, smem, st, xb, gb, bb, rows, c, eps, scale, mean, rstd, out, ab);
+    return fmt == 0 ? lnf_launch<0, kLnfCast>(rows, c, sm_count, st, x, gamma, beta, eps, scale,
+                                              mean, rstd, out, amax)
+                    : lnf_launch<1, kLnfCast>(rows, c, sm_count, st, x, gamma, beta, eps, scale,
+                                              mean, rstd, out, amax);
 }
 
 // ----------------------------------------------------------- scale update --
