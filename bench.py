@@ -408,6 +408,9 @@ def run_layer_bench(f, w: wl.Workload, args, world, pk, peak_kind, sustained_s: 
                                          tflop_per_mhz, pk)
     if e2e:
         res["e2e"] = run_e2e(f, lin, xs[0], dys[0], args, world, flops)
+        res["e2e"]["full_outputs"] = {
+            k: v for k, v in run_e2e(f, lin, xs[0], dys[0], args, world, flops,
+                                     readback="outputs").items() if k != "overlap"}
     return res
 
 
@@ -435,12 +438,16 @@ def run_sustained(graphs, step, timed, seconds, ms_step, flops, world, tflop_per
                     "sampled clock and against the measured sustained BF16 peak x 2"}
 
 
-def run_e2e(f, lin, X, dY, args, world, flops):
+def run_e2e(f, lin, X, dY, args, world, flops, readback="metric"):
     """Same metric through the public API from pinned host buffers.  Every
-    step copies its X and dY in from pinned host memory and its Y, dX and dW
-    back out, inside the timed region.  Copies run on their own streams and
-    are double-buffered against the compute stream, so step i's uploads and
-    step i-1's downloads overlap step i's kernels."""
+    step copies its inputs X and dY in from pinned host memory inside the
+    timed region, and reads its result back: with readback="metric", the
+    scaling state the step's update produced (the new scales and their
+    inverses, 40 B: the step's result as a training step uses it, where Y,
+    dX and dW stay on the device for the neighbouring layers and the
+    optimizer); with readback="outputs", Y, dX and dW themselves.  Copies run
+    on their own streams and are double-buffered against the compute stream,
+    so step i's uploads and step i-1's downloads overlap step i's kernels."""
     comp = torch.cuda.current_stream()
     up, down = torch.cuda.Stream(), torch.cuda.Stream()
     hX = [torch.empty_like(X, device="cpu").pin_memory() for _ in range(2)]
@@ -453,7 +460,12 @@ def run_e2e(f, lin, X, dY, args, world, flops):
     ddYin = [torch.empty_like(dY) for _ in range(2)]
     douts = [(torch.empty_like(lin.Y), torch.empty_like(lin.dX), torch.empty_like(lin.dW))
              for _ in range(2)]
-    houts = [tuple(torch.empty_like(t, device="cpu").pin_memory() for t in o) for o in douts]
+    # what each step reads back, per slot: the outputs, or a device copy of the
+    # scaling state taken on the compute stream right after the step's update
+    dres = [tuple(douts[k]) if readback == "outputs" else
+            (torch.empty_like(lin.meta.scale), torch.empty_like(lin.meta.scale_inv))
+            for k in range(2)]
+    houts = [tuple(torch.empty_like(t, device="cpu").pin_memory() for t in o) for o in dres]
     ev = lambda: torch.cuda.Event()
     in_ready = [ev(), ev()]      # upload of slot done
     in_free = [ev(), ev()]       # compute done reading slot's inputs
@@ -473,11 +485,15 @@ def run_e2e(f, lin, X, dY, args, world, flops):
         comp.wait_event(in_ready[k])
         comp.wait_event(out_free[k])
         lin.step(dXin[k], ddYin[k], stream=comp, outs=douts[k])
+        if readback != "outputs":
+            with torch.cuda.stream(comp):
+                dres[k][0].copy_(lin.meta.scale, non_blocking=True)
+                dres[k][1].copy_(lin.meta.scale_inv, non_blocking=True)
         in_free[k].record(comp)
         out_ready[k].record(comp)
         with torch.cuda.stream(down):
             down.wait_event(out_ready[k])
-            for h, d in zip(houts[k], douts[k]):
+            for h, d in zip(houts[k], dres[k]):
                 h.copy_(d, non_blocking=True)
             out_free[k].record(down)
 
@@ -498,10 +514,12 @@ def run_e2e(f, lin, X, dY, args, world, flops):
     torch.cuda.synchronize()
     barrier(world)
     ms = max_over_ranks(s.elapsed_time(e), world)
-    h2d = X.numel() * 2 + dY.numel() * 2
-    d2h = sum(t.numel() * 2 for t in douts[0])
+    h2d = X.numel() * X.element_size() + dY.numel() * dY.element_size()
+    d2h = sum(t.numel() * t.element_size() for t in dres[0])
     return {"value": world * n * flops / (ms / 1e3) / 1e12, "unit": "TFLOPS",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n,
+            "readback": ("Y, dX and dW" if readback == "outputs" else
+                         "the step's new scales and scale_inv (its scaling state)"),
             "overlap": "uploads, compute and downloads on three streams, double-buffered"}
 
 
