@@ -278,11 +278,11 @@ __global__ void adam_scales_kernel(const AdamArgs a) {
 // units puts the integer in the low mantissa bits), after every stage of 8
 // ranks when there are more than 8.  fl32(1 / scale) is sig * 2^es with a
 // 24-bit integer sig.  Each element is rounded once, by the first of three
-// tiers that applies: (1) up to 8 ranks, a sum that is one binary32 value a
-// (always for E4M3; for E5M2 when its parts add exactly): p = fl32(a * sinv)
-// with its exact fma error; (2) a result in BF16's normal range: the exact
-// 64-bit product |sum| * sig, normalised, its top 8 bits rounded to nearest
-// even with a sticky bit; (3) the general integer path (subnormal and
+// tiers that applies: (1) up to 8 ranks, a = fl32(sum) and p = fl32(a * sinv)
+// rounded to BF16, unless p's exact error (a exact) or a rounding test (a
+// inexact) says that may differ (dq_tier1_ok); (2) a result in BF16's normal
+// range: the exact 64-bit product |sum| * sig, normalised, its top 8 bits
+// rounded to nearest even with a sticky bit; (3) the general integer path (subnormal and
 // overflowing results, special codes, non-finite factors; a 128-bit product
 // beyond 256 ranks).  Special codes decode to FP16 infinities and NaN, so up
 // to 8 ranks an element's fp32 sum is not finite exactly when it holds one,
@@ -586,16 +586,62 @@ __device__ __forceinline__ uint32_t dq_element_flags(const uint8_t *q, int nrank
     return fe;
 }
 
-// Tier 1 of the 8-rank path for a finite nonzero factor: p = fl32(a * sinv)
-// and e = fma(a, sinv, -p) (its exact error) give BF16(a * sinv) as the
-// rounding of p unless p is below 2^-100 (e may be inexact there), not
-// finite, or exactly a BF16 midpoint while e != 0 (there rounding twice can
-// differ from rounding once; every midpoint is a binary32 value).  A zero
-// sum gives +0 when the factor is positive.
-__device__ __forceinline__ bool dq_tier1_ok(float a, float p, float e, bool pos_factor) {
+// Tier 1 of the 8-rank path for a finite nonzero factor: a = fl32(S) for the
+// element's exact sum S, p = fl32(a * sinv) and e = fma(a, sinv, -p), its
+// exact error (p at least 2^-100).  BF16 rounds at bit 16 of the binary32
+// pattern; its midpoints have low 16 bits 0x8000, and every midpoint is a
+// binary32 value.
+//  * a exact (a == S): a * sinv = p + e, so rounding p to BF16 rounds
+//    S * sinv correctly unless p is a midpoint while e != 0.
+//  * a inexact (the split sums do not add exactly; a rounding test in the
+//    manner of Ziv): |S - a| <= 2^-24 |a| gives |S * sinv - p| < 1.5 ulp(p),
+//    so when p's low 16 bits differ from 0x8000 by at least 2, S * sinv lies
+//    on p's side of every midpoint and BF16(S * sinv) is p rounded.  (The
+//    window is not used for exact sums: a factor such as fl32(amax / 57344),
+//    whose significand repeats the bits of 1/7, puts the products of short
+//    sums next to midpoints far more often than chance.)
+// Otherwise, and when p is below 2^-100 or not finite, the element takes the
+// integer tiers.  A zero sum gives +0 when the factor is positive.
+__device__ __forceinline__ bool dq_tier1_ok(float a, float p, float e, bool exact,
+                                            bool pos_factor) {
     const float ap = fabsf(p);
-    const bool mid = (__float_as_uint(p) & 0xFFFFu) == 0x8000u && e != 0.0f;
-    return (ap >= 0x1p-100f && ap <= 0x1.fffffep127f && !mid) || (a == 0.0f && pos_factor);
+    const uint32_t low = __float_as_uint(p) & 0xFFFFu;
+    const bool declined = exact ? (low == 0x8000u && e != 0.0f) : (low - 0x7FFFu <= 2u);
+    return (ap >= 0x1p-100f && ap <= 0x1.fffffep127f && !declined) || (a == 0.0f && pos_factor);
+}
+
+// One element of the 8-rank path after tier 1 declined some element of its
+// thread: BF16 bits of its result when tier 1 does not stand for it (the
+// integer tiers on its exact count of quanta), else 0xFFFFFFFF.  hs / ls:
+// its fp32 sums (ls = 0 unless split; E4M3: hs alone).  Not inlined, so that
+// the integer tiers take one copy of code rather than one per element: warps
+// enter them often on codes spread over many binades, and sixteen inlined
+// copies overflowed the instruction cache.
+template <int FMT>
+__device__ __noinline__ uint32_t dq_slow_element(float hs, float ls, bool split, bool general,
+                                                 bool pos_factor, float sinv, DqFactor fac,
+                                                 const uint8_t *q, int nranks, int64_t n,
+                                                 int64_t k) {
+    if (!general) {
+        const float a = split ? __fadd_rn(hs, ls) : hs;
+        const float p = __fmul_rn(a, sinv);
+        if (dq_tier1_ok(a, p, __fmaf_rn(a, sinv, -p), !split || __fsub_rn(a, hs) == ls,
+                        pos_factor))
+            return 0xFFFFFFFFu;
+    }
+    const uint32_t fe = fabsf(hs) <= 0x1.fffffep127f ? 0u : dq_element_flags<FMT>(q, nranks, n, k);
+    long long qa = 0;
+    if (fe == 0u) {
+        if constexpr (FMT == 0)
+            qa = f32_units<-9>(hs);
+        else
+            qa = split ? (f32_units<-2>(hs) << 14) + f32_units<-16>(ls) : e5m2_direct_quanta(hs);
+    }
+    bool outside = general || fe != 0u;
+    uint32_t b = 0;
+    if (!outside) b = bf16_fast<FMT>(qa, fac, outside);
+    if (outside) b = dq_finish<FMT, false>(qa, fe, fac);
+    return b & 0xFFFFu;
 }
 
 // MODE 0: at most 8 ranks (one stage, no int64 sums during the walk);
@@ -736,34 +782,48 @@ __global__ void __launch_bounds__(kDqConsumers + 32, 2)
             __syncwarp();
             if (lane == 0) mbar_arrive(empty0 + 8 * st);
             if (!in) continue;
-            // tier 1 takes a = the element's sum as one binary32 value: the
-            // unsplit sum, or hs + ls when that addition is exact, which
-            // (hs + ls) - hs == ls shows (Fast2Sum when |hs| >= |ls|;
-            // otherwise |hs| < |ls| <= 1 and the sum has at most 17 bits)
+            // tier 1 takes a = fl32 of the element's exact sum: the unsplit
+            // sum itself (exact), or hs + ls rounded once, exact when
+            // (hs + ls) - hs == ls (Fast2Sum when |hs| >= |ls|; otherwise
+            // |hs| < |ls| <= 1 and the sum has at most 17 bits)
             uint32_t o[kDqElems / 2];
             bool odd = general;
-            if (!odd) {
-                float a[kDqElems];
-#pragma unroll
-                for (int e = 0; e < kDqElems; ++e) a[e] = sums.s[0][e];
-                if (split) {
-#pragma unroll
-                    for (int e = 0; e < kDqElems; ++e) {
-                        const float hs = sums.s[0][e], ls = sums.s[DqSums<FMT>::NA - 1][e];
-                        a[e] = __fadd_rn(hs, ls);
-                        if (__fsub_rn(a[e], hs) != ls) odd = true;
-                    }
-                }
+            if (!odd && !split) {
 #pragma unroll
                 for (int e = 0; e < kDqElems; e += 2) {
-                    const uint64_t a2 = f32x2_pack(a[e], a[e + 1]);
+                    const float a0 = sums.s[0][e], a1 = sums.s[0][e + 1];
+                    const uint64_t a2 = f32x2_pack(a0, a1);
                     const uint64_t p2 = f32x2_mul(a2, sinv2);
                     const uint64_t e2 = f32x2_fma(a2, sinv2, p2 ^ 0x8000000080000000ull);
                     float p0, p1, e0, e1;
                     f32x2_unpack(p2, p0, p1);
                     f32x2_unpack(e2, e0, e1);
-                    if (!dq_tier1_ok(a[e], p0, e0, pos_factor) ||
-                        !dq_tier1_ok(a[e + 1], p1, e1, pos_factor))
+                    if (!dq_tier1_ok(a0, p0, e0, true, pos_factor) ||
+                        !dq_tier1_ok(a1, p1, e1, true, pos_factor))
+                        odd = true;
+                    uint32_t h;
+                    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(h) : "f"(p1), "f"(p0));
+                    o[e >> 1] = h;
+                }
+            } else if (!odd) {
+#pragma unroll
+                for (int e = 0; e < kDqElems; e += 2) {
+                    float a[2];
+                    bool exact[2];
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const float hs = sums.s[0][e + h], ls = sums.s[DqSums<FMT>::NA - 1][e + h];
+                        a[h] = __fadd_rn(hs, ls);
+                        exact[h] = __fsub_rn(a[h], hs) == ls;
+                    }
+                    const uint64_t a2 = f32x2_pack(a[0], a[1]);
+                    const uint64_t p2 = f32x2_mul(a2, sinv2);
+                    const uint64_t e2 = f32x2_fma(a2, sinv2, p2 ^ 0x8000000080000000ull);
+                    float p0, p1, e0, e1;
+                    f32x2_unpack(p2, p0, p1);
+                    f32x2_unpack(e2, e0, e1);
+                    if (!dq_tier1_ok(a[0], p0, e0, exact[0], pos_factor) ||
+                        !dq_tier1_ok(a[1], p1, e1, exact[1], pos_factor))
                         odd = true;
                     uint32_t h;
                     asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(h) : "f"(p1), "f"(p0));
@@ -778,30 +838,12 @@ __global__ void __launch_bounds__(kDqConsumers + 32, 2)
                 // rounded by the 64-bit path or the general one
 #pragma unroll
                 for (int e = 0; e < kDqElems; ++e) {
-                    const float hs = sums.s[0][e], ls = sums.s[DqSums<FMT>::NA - 1][e];
-                    bool declined = general;
-                    if (!declined) {
-                        const float a = split ? __fadd_rn(hs, ls) : hs;
-                        const float p = __fmul_rn(a, sinv);
-                        declined = (split && __fsub_rn(a, hs) != ls) ||
-                                   !dq_tier1_ok(a, p, __fmaf_rn(a, sinv, -p), pos_factor);
-                    }
-                    if (!declined) continue;
-                    const uint32_t fe =
-                        fabsf(hs) <= 0x1.fffffep127f ? 0u : dq_element_flags<FMT>(q, nranks, n, i + e);
-                    long long qa = 0;
-                    if (fe == 0u) {
-                        if constexpr (FMT == 0)
-                            qa = sums.quanta(e);
-                        else
-                            qa = split ? sums.quanta(e) : e5m2_direct_quanta(hs);
-                    }
-                    bool outside = general || fe != 0u;
-                    uint32_t b = 0;
-                    if (!outside) b = bf16_fast<FMT>(qa, fac, outside);
-                    if (outside) b = dq_finish<FMT, false>(qa, fe, fac);
+                    const uint32_t b = dq_slow_element<FMT>(
+                        sums.s[0][e], sums.s[DqSums<FMT>::NA - 1][e], split, general, pos_factor,
+                        sinv, fac, q, nranks, n, i + e);
+                    if (b == 0xFFFFFFFFu) continue;
                     const int w = e >> 1, sh = (e & 1) * 16;
-                    o[w] = (o[w] & ~(0xFFFFu << sh)) | ((b & 0xFFFFu) << sh);
+                    o[w] = (o[w] & ~(0xFFFFu << sh)) | (b << sh);
                 }
             }
             uint4 *dst = reinterpret_cast<uint4 *>(out + i);
