@@ -175,6 +175,32 @@ def test_dequant_sum_unsplit_e5m2_sums(nranks):
     assert np.array_equal(_u16(out), o.dequant_sum(parts, o.E5M2, s))
 
 
+@pytest.mark.parametrize("amax", [0.0057678, 1.0, 3.140625, 0.000244140625, 448.0])
+def test_dequant_sum_recipe_scales(amax):
+    """Scales as the recipe makes them, fl32(57344 / amax) for a BF16 amax:
+    their inverses repeat the bits of 1/7, so the products of short exact
+    sums land on and next to BF16 midpoints far more often than chance.
+    Uniformly random codes (split sums that mostly do not add exactly in
+    binary32, rounded through the rounding test) and gradient-shaped codes
+    (exact unsplit sums) must both match the oracle bit for bit."""
+    import fp8_mixed_precision_amax_gb300 as f
+    rng = np.random.default_rng(int(amax * 1e6) % 1000 + 3)
+    a16 = np.float32(torch.tensor(amax, dtype=torch.bfloat16).float().item())
+    s = np.float32(np.float32(57344.0) / a16)
+    n = 1 << 17
+    table = o.fp8_decode_table(o.E5M2)
+    finite = np.nonzero(np.isfinite(table))[0].astype(np.uint8)
+    cases = [rng.choice(finite, size=(8, n))]
+    g = [rng.normal(0.0, a16 / 5.5, n).astype(np.float32) for _ in range(8)]
+    cases.append(np.stack([o.quantize_f32(x, s, o.E5M2).reshape(-1) for x in g]))
+    for parts in cases:
+        out = torch.empty(n, dtype=torch.bfloat16, device="cuda")
+        f.fp8_dequant_sum(torch.from_numpy(parts).cuda(), o.E5M2, torch.tensor([s], device="cuda"),
+                          out)
+        torch.cuda.synchronize()
+        assert _same_bf16(_u16(out), o.dequant_sum(parts, o.E5M2, s))
+
+
 def _worker(rank, world, port, shape, fmt, margin, q):
     import datetime
 
