@@ -64,6 +64,55 @@ def test_adam_steps_bit_exact(n, wd, margin):
     f.fp8_sync_status()
 
 
+def test_adam_extreme_gradients():
+    """Gradients spread over 1e-30 .. 3e38 with infinities and NaN: second
+    moments past FP16's largest value saturate to 65504, first moments and
+    weights go non-finite where the pages' arithmetic says so, and NaN
+    propagates.  The E4M3 / FP16 state codes, amaxes and scales match the
+    oracle bit for bit; the BF16 weight copy too, except that its NaN
+    entries are compared as a class (the pages fix no NaN payload: the
+    oracle keeps a NaN's sign and payload when it rounds to BF16, the
+    kernel's packed conversion writes the canonical NaN), as for the GEMM
+    outputs."""
+    f = _lib()
+    n = 4096 + 16
+    g = torch.Generator().manual_seed(99)
+    w = (torch.randn(n, generator=g) * 0.02).to(torch.bfloat16)
+    state = f.Fp8AdamState(w.cuda())
+    hp = f.AdamHyper(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01)
+    ohp = o.AdamHyper(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01)
+    m1, ms, msi, m2, w16, ws, wsi, _ = o.adam_init(_u16(w), 0)
+    ost = dict(m1=m1, m1_scale=ms, m1_scale_inv=msi, m2=m2, w16=w16, w_scale=ws, w_scale_inv=wsi)
+    wout = torch.empty(n, dtype=torch.bfloat16, device="cuda")
+    for t in range(1, 4):
+        mag = torch.pow(10.0, torch.empty(n).uniform_(-30, 38.5, generator=g))
+        sign = torch.where(torch.rand(n, generator=g) < 0.5, -1.0, 1.0)
+        grad = (mag * sign).to(torch.bfloat16)
+        if t >= 2:
+            grad[7::997] = float("nan")
+            grad[11::1009] = float("inf")
+        state.step(grad.cuda(), wout, hp)
+        torch.cuda.synchronize()
+        m1, ms, msi, m2, w16, ws, wsi, wb, am = o.adam_step(
+            _u16(grad), ost["m1"], ost["m1_scale"], ost["m1_scale_inv"], ost["m2"], ost["w16"],
+            ost["w_scale"], ost["w_scale_inv"], ohp, t)
+        assert np.array_equal(state.m1.cpu().numpy(), m1), t
+        assert np.array_equal(_u16(state.m2), m2), t
+        assert np.array_equal(_u16(state.w16), w16), t
+        got = _u16(wout)
+        nan16 = lambda b: (b & 0x7FFF) > 0x7F80
+        assert np.array_equal(nan16(got), nan16(wb)), t
+        assert np.array_equal(got[~nan16(got)], wb[~nan16(wb)]), t
+        assert np.array_equal(state.amax.cpu().numpy().view(np.uint32), am.view(np.uint32)), t
+        gs = state.scales.cpu().numpy()
+        assert np.array_equal(gs.view(np.uint32),
+                              np.array([ms, msi, ws, wsi], np.float32).view(np.uint32)), t
+        ost = dict(m1=m1, m1_scale=ms, m1_scale_inv=msi, m2=m2, w16=w16, w_scale=ws,
+                   w_scale_inv=wsi)
+    assert (_u16(state.m2) == 0x7BFF).any()   # saturated second moments occurred
+    f.fp8_sync_status()
+
+
 def test_state_is_five_bytes_per_parameter():
     """First moment 1 B + second moment 2 B + master weights 2 B.  (FP8-LM's
     6 B per parameter also counts an FP8 gradient; this path's gradient, the
