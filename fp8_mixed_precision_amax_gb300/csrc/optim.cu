@@ -35,11 +35,20 @@ constexpr float kF16Max = 65504.0f;
 
 __device__ __forceinline__ float f16_dec(uint16_t h) { return __half2float(__ushort_as_half(h)); }
 
-// Nearest FP16 value, ties to even, saturating at +-65504; NaN stays NaN.
-__device__ __forceinline__ uint16_t f16_enc_sat(float v) {
-    if (v != v) return 0x7e00;
-    v = fminf(fmaxf(v, -kF16Max), kF16Max);
-    return __half_as_ushort(__float2half_rn(v));
+// Two values to their nearest FP16 values, ties to even, saturating at
+// +-65504 (lo in the low half): one packed saturating conversion.  It rounds
+// first and then saturates, which gives the same codes as clamping first: a
+// value that rounds past 65504 is at least 65520 and saturates to 65504.  Its
+// NaN result is the canonical FP16 NaN, so a NaN input is set to 0x7e00, the
+// library's FP16 NaN code.
+__device__ __forceinline__ uint32_t f16x2_enc_sat(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    if (lo != lo || hi != hi) {
+        if (lo != lo) r = (r & 0xFFFF0000u) | 0x7e00u;
+        if (hi != hi) r = (r & 0x0000FFFFu) | 0x7e000000u;
+    }
+    return r;
 }
 
 // Two E4M3 codes (low byte first) to two floats, exactly.
@@ -221,9 +230,9 @@ __global__ void __launch_bounds__(256) adam_apply_kernel(const AdamArgs a) {
                 mq[j >> 1] |= c << 16;
             else
                 mq[j >> 1] = c;
-            vq[j] = f16_enc_sat(e.v[2 * j]) | (static_cast<uint32_t>(f16_enc_sat(e.v[2 * j + 1])) << 16);
+            vq[j] = f16x2_enc_sat(e.v[2 * j], e.v[2 * j + 1]);
             f32x2_unpack(f32x2_mul(f32x2_pack(e.w[2 * j], e.w[2 * j + 1]), sw2), c0, c1);
-            wq[j] = f16_enc_sat(c0) | (static_cast<uint32_t>(f16_enc_sat(c1)) << 16);
+            wq[j] = f16x2_enc_sat(c0, c1);
             const __nv_bfloat162 b2 = __floats2bfloat162_rn(e.w[2 * j], e.w[2 * j + 1]);
             bq[j] = *reinterpret_cast<const uint32_t *>(&b2);
         }
@@ -955,7 +964,7 @@ __global__ void __launch_bounds__(256) adam_init_kernel(const uint16_t *__restri
         for (int j = 0; j < 4; ++j) {
             float c0, c1;
             f32x2_unpack(f32x2_mul(f32x2_from_bf16x2(xw[j]), sw2), c0, c1);
-            wq[j] = f16_enc_sat(c0) | (static_cast<uint32_t>(f16_enc_sat(c1)) << 16);
+            wq[j] = f16x2_enc_sat(c0, c1);
         }
         *reinterpret_cast<uint2 *>(m1 + i) = make_uint2(0u, 0u);
         *reinterpret_cast<uint4 *>(m2 + i) = make_uint4(0u, 0u, 0u, 0u);
