@@ -31,6 +31,19 @@ __device__ unsigned g_cast_error_flags = 0;
 
 // Grid-stride max of |x| over 16-byte vectors (8 BF16), 4 vectors in flight
 // per thread, packed BF16 abs / max (NaN skipped), one atomicMax per block.
+// STREAM: evict-first loads, for a tensor larger than L2; a tensor that fits
+// is read with plain loads and stays in L2 for the cast that follows (the
+// just-in-time cast of a 67 MB tensor: 37.9 -> 35.8 us; evict-first loads
+// are 2 % faster on a 537 MB one).
+template <bool STREAM>
+__device__ __forceinline__ uint4 amax_load(const uint4 *p) {
+    if constexpr (STREAM)
+        return __ldcs(p);
+    else
+        return *p;
+}
+
+template <bool STREAM>
 __global__ void __launch_bounds__(512) amax_kernel(const uint4 *__restrict__ x, int64_t nvec,
                                                    unsigned *__restrict__ amax_bits) {
     pdl_wait();
@@ -41,7 +54,7 @@ __global__ void __launch_bounds__(512) amax_kernel(const uint4 *__restrict__ x, 
     for (; i + 3 * stride < nvec; i += 4 * stride) {
         uint4 v[4];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) v[u] = __ldcs(x + i + u * stride);
+        for (int u = 0; u < 4; ++u) v[u] = amax_load<STREAM>(x + i + u * stride);
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
             m2 = absmax_bf16x2(m2, v[u].x);
@@ -51,7 +64,7 @@ __global__ void __launch_bounds__(512) amax_kernel(const uint4 *__restrict__ x, 
         }
     }
     for (; i < nvec; i += stride) {
-        uint4 v = __ldcs(x + i);
+        uint4 v = amax_load<STREAM>(x + i);
         m2 = absmax_bf16x2(m2, v.x);
         m2 = absmax_bf16x2(m2, v.y);
         m2 = absmax_bf16x2(m2, v.z);
@@ -1049,8 +1062,12 @@ cudaError_t launch_amax(const void *x, int64_t n, float *amax, int sm_count, cud
     const int64_t cap = static_cast<int64_t>(sm_count) * 4;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
-    return launch_pdl(amax_kernel, dim3(static_cast<unsigned>(blocks)), dim3(threads), 0, st,
-                      reinterpret_cast<const uint4 *>(x), nvec, reinterpret_cast<unsigned *>(amax));
+    const dim3 grid(static_cast<unsigned>(blocks)), block(threads);
+    const auto *xv = reinterpret_cast<const uint4 *>(x);
+    auto *ab = reinterpret_cast<unsigned *>(amax);
+    // tensors up to 96 MB (of the 129 MB L2) are left in L2 for a following cast
+    return n * 2 <= (96ll << 20) ? launch_pdl(amax_kernel<false>, grid, block, 0, st, xv, nvec, ab)
+                                 : launch_pdl(amax_kernel<true>, grid, block, 0, st, xv, nvec, ab);
 }
 
 cudaError_t launch_quantize_f32(const float *x, int64_t n, const float *scale, int fmt,
@@ -1132,7 +1149,9 @@ static bool cast_args(CastArgs &args, const CastSpec *specs, int n, int margin) 
 cudaError_t launch_cast_group(const CastSpec *specs, int n, int fmt, bool current, int margin,
                               int sm_count, cudaStream_t st) {
     if (n < 1 || n > 2) return cudaErrorInvalidValue;
-    for (int i = 0; i < n; ++i) {
+    // the amax passes run last tensor first, so that the first tensor, whose
+    // tiles the cast takes first, is the one left in L2
+    for (int i = n - 1; i >= 0; --i) {
         if (current && specs[i].ln_mean != nullptr) {
             // the LayerNorm statistics kernel has already written amax(y)
         } else if (current) {
