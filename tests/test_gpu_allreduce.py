@@ -201,6 +201,29 @@ def test_dequant_sum_recipe_scales(amax):
         assert _same_bf16(_u16(out), o.dequant_sum(parts, o.E5M2, s))
 
 
+def test_dequant_sum_full_size_8_ranks_7b_dw():
+    """The bench's FP8 all-reduce sum at full size: 8 ranks' N(0, sigma_r)
+    gradients of the 7B layer's dW ([11008, 4096], sigma_r = 1e-3 (1 + r/10),
+    BF16) cast to E5M2 with their shared scale (the minimum of the ranks'
+    recipe scales), summed in one launch; every one of the 45 M outputs
+    against the oracle, bit for bit."""
+    import fp8_mixed_precision_amax_gb300 as f
+    n = 11008 * 4096
+    g = torch.Generator().manual_seed(8)
+    grads = [(torch.randn(n, generator=g) * (1e-3 * (1 + 0.1 * r))).to(torch.bfloat16)
+             for r in range(8)]
+    scales = [np.float32(np.float32(57344.0) / np.float32(x.float().abs().max().item()))
+              for x in grads]
+    s = min(scales)
+    parts = np.stack([o.quantize_f32(x.float().numpy(), s, o.E5M2).reshape(-1) for x in grads])
+    del grads
+    out = torch.empty(n, dtype=torch.bfloat16, device="cuda")
+    f.fp8_dequant_sum(torch.from_numpy(parts).cuda(), o.E5M2, torch.tensor([s], device="cuda"),
+                      out)
+    f.fp8_sync_status()
+    assert np.array_equal(_u16(out), o.dequant_sum(parts, o.E5M2, s))
+
+
 def _worker(rank, world, port, shape, fmt, margin, q):
     import datetime
 

@@ -64,6 +64,41 @@ def test_adam_steps_bit_exact(n, wd, margin):
     f.fp8_sync_status()
 
 
+def test_adam_full_size_7b_w():
+    """Two Adam steps over the full 7B W (11008 x 4096 = 45 M parameters, the
+    bench's size and launch): every code of both moments and the master
+    weights, the BF16 weights, amaxes and scales against the oracle, bit for
+    bit."""
+    f = _lib()
+    n = 11008 * 4096
+    g = torch.Generator().manual_seed(7)
+    w = (torch.randn(n, generator=g) * 0.02).to(torch.bfloat16)
+    state = f.Fp8AdamState(w.cuda())
+    hp = f.AdamHyper(lr=1e-4, weight_decay=0.1)
+    ohp = o.AdamHyper(lr=1e-4, weight_decay=0.1)
+    m1, ms, msi, m2, w16, ws, wsi, _ = o.adam_init(_u16(w), 0)
+    ost = dict(m1=m1, m1_scale=ms, m1_scale_inv=msi, m2=m2, w16=w16, w_scale=ws, w_scale_inv=wsi)
+    wout = torch.empty(n, dtype=torch.bfloat16, device="cuda")
+    for t in (1, 2):
+        grad = (torch.randn(n, generator=g) * 1e-3).to(torch.bfloat16)
+        state.step(grad.cuda(), wout, hp)
+        torch.cuda.synchronize()
+        m1, ms, msi, m2, w16, ws, wsi, wb, am = o.adam_step(
+            _u16(grad), ost["m1"], ost["m1_scale"], ost["m1_scale_inv"], ost["m2"], ost["w16"],
+            ost["w_scale"], ost["w_scale_inv"], ohp, t)
+        assert np.array_equal(state.m1.cpu().numpy(), m1), t
+        assert np.array_equal(_u16(state.m2), m2), t
+        assert np.array_equal(_u16(state.w16), w16), t
+        assert np.array_equal(_u16(wout), wb), t
+        assert np.array_equal(state.amax.cpu().numpy().view(np.uint32), am.view(np.uint32)), t
+        gs = state.scales.cpu().numpy()
+        assert np.array_equal(gs.view(np.uint32),
+                              np.array([ms, msi, ws, wsi], np.float32).view(np.uint32)), t
+        ost = dict(m1=m1, m1_scale=ms, m1_scale_inv=msi, m2=m2, w16=w16, w_scale=ws,
+                   w_scale_inv=wsi)
+    f.fp8_sync_status()
+
+
 def test_adam_extreme_gradients():
     """Gradients spread over 1e-30 .. 3e38 with infinities and NaN: second
     moments past FP16's largest value saturate to 65504, first moments and
