@@ -42,6 +42,33 @@ def test_dequant_sum_bit_exact(fmt, nranks):
     assert np.array_equal(_u16(out), o.dequant_sum(parts, fmt, s))
 
 
+@pytest.mark.parametrize("fmt", [o.E4M3, o.E5M2])
+@pytest.mark.parametrize("nranks", [9, 64, 300, 1000])
+def test_dequant_sum_many_ranks(fmt, nranks):
+    """More than 8 ranks: the sums become int64 counts of quanta after every
+    stage of 8 ranks; beyond 256 ranks the general path multiplies with 128
+    bits.  Random finite codes, then every rank at the largest magnitude of
+    one sign (1000 x 57344 x 2^16 quanta needs more than 40 bits), at
+    ordinary, overflowing and BF16-subnormal scales; bit-exact."""
+    import fp8_mixed_precision_amax_gb300 as f
+    rng = np.random.default_rng(nranks + 17 * fmt)
+    table = o.fp8_decode_table(fmt)
+    finite = np.nonzero(np.isfinite(table))[0].astype(np.uint8)
+    top = 0x7E if fmt == o.E4M3 else 0x7B
+    n = 4096 + 16
+    cases = [rng.choice(finite, size=(nranks, n)),
+             np.where(np.arange(n)[None, :] % 2 == 0, top, top | 0x80).repeat(nranks, 0)
+             .astype(np.uint8)]
+    for parts in cases:
+        dev = torch.from_numpy(np.ascontiguousarray(parts)).cuda()
+        for s in (np.float32(10.0 ** rng.uniform(-2, 2)), np.float32(1e-36), np.float32(1e36),
+                  np.float32(-0.7)):
+            out = torch.empty(n, dtype=torch.bfloat16, device="cuda")
+            f.fp8_dequant_sum(dev, fmt, torch.tensor([s], device="cuda"), out)
+            torch.cuda.synchronize()
+            assert _same_bf16(_u16(out), o.dequant_sum(parts, fmt, s)), (nranks, s)
+
+
 def test_dequant_sum_rounds_once():
     """E5M2 parts 57344 + 128 + 2^-16 at scale 1: the exact sum lies just
     above the midpoint between the BF16 neighbours 57344 and 57600, so one
