@@ -480,10 +480,13 @@ fp8_status fp8_layernorm_quantize_transpose(const void *x, const void *gamma, co
     int sms;
     FP8_TRY(current_device(&sms));
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (out_t == nullptr && fp8k::ln_cast_rows_fits(rows, cols)) {   // one pass over x
+    if (out != nullptr && fp8k::ln_cast_rows_fits(rows, cols)) {
+        // one pass over x; the transposed copy from the codes just written
         FP8_CUDA(fp8k::launch_ln_cast_rows(x, gamma, beta, rows, cols, eps, scale, fmt, out, amax,
                                            true, mean, rstd, sms, st),
                  fn);
+        if (out_t != nullptr)
+            FP8_CUDA(fp8k::launch_transpose_u8(out, rows, cols, out_t, sms, st), fn);
         return FP8_OK;
     }
     FP8_CUDA(fp8k::launch_ln_stats(x, gamma, beta, rows, cols, eps, mean, rstd, nullptr, sms, st),
@@ -546,17 +549,27 @@ static fp8_status linear_fwd_impl(const char *fn, const void *X, const void *gam
     // amax of X, W and Y are max-combined into their slots, which the
     // previous fp8_amax_scale_update cleared (a fresh meta starts at 0).
     const bool cur = recipe->scaling == FP8_SCALING_CURRENT;
-    if (mean != nullptr)   // LayerNorm statistics (and, for current scaling, amax of LN(X))
-        FP8_CUDA(fp8k::launch_ln_stats(X, gamma, beta, M, K, eps, mean, rstd,
-                                       cur ? am + FP8_SLOT_X : nullptr, sms, st),
-                 fn);
-    // X (or LN(X)) and W (both E4M3) in one cast launch
     const fp8k::CastSpec c[2] = {
         {X, M, K, meta->scale + FP8_SLOT_X, meta->scale_inv + FP8_SLOT_X, X8, X8t,
          am + FP8_SLOT_X, false, mean, rstd, gamma, beta},
         {W, N, K, meta->scale + FP8_SLOT_W, meta->scale_inv + FP8_SLOT_W, W8, W8t,
          am + FP8_SLOT_W, false, nullptr, nullptr, nullptr, nullptr}};
-    FP8_CUDA(fp8k::launch_cast_group(c, 2, FP8_E4M3, cur, recipe->margin, sms, st), fn);
+    if (mean != nullptr && !cur && fp8k::ln_cast_rows_fits(M, K)) {
+        // LN(X) in one pass over X, X8t transposed from X8, then W on its own
+        FP8_CUDA(fp8k::launch_ln_cast_rows(X, gamma, beta, M, K, eps, meta->scale + FP8_SLOT_X,
+                                           FP8_E4M3, X8, am + FP8_SLOT_X, false, mean, rstd, sms,
+                                           st),
+                 fn);
+        FP8_CUDA(fp8k::launch_transpose_u8(X8, M, K, X8t, sms, st), fn);
+        FP8_CUDA(fp8k::launch_cast_group(c + 1, 1, FP8_E4M3, false, recipe->margin, sms, st), fn);
+    } else {
+        if (mean != nullptr)   // LayerNorm statistics (and, for current scaling, amax of LN(X))
+            FP8_CUDA(fp8k::launch_ln_stats(X, gamma, beta, M, K, eps, mean, rstd,
+                                           cur ? am + FP8_SLOT_X : nullptr, sms, st),
+                     fn);
+        // X (or LN(X)) and W (both E4M3) in one cast launch
+        FP8_CUDA(fp8k::launch_cast_group(c, 2, FP8_E4M3, cur, recipe->margin, sms, st), fn);
+    }
     return gemm_checked(fn, X8, FP8_E4M3, W8, FP8_E4M3, M, N, K, meta->scale_inv + FP8_SLOT_X,
                         meta->scale_inv + FP8_SLOT_W, Y, am + FP8_SLOT_Y, false, sms, st);
 }

@@ -442,6 +442,68 @@ __global__ void __launch_bounds__(kQtThreads, 2)
     }
 }
 
+// ------------------------------------------------------- FP8 transpose --
+//
+// out_t[c][r] = in[r][c] for a [rows][cols] array of bytes (FP8 codes), in
+// 128 x 128 tiles, with the word tile and the second phase of
+// quantize_transpose_kernel: each thread loads 8 x 8 bytes of the tile
+// (16 threads cover a 128-byte row segment), stores them into the
+// XOR-swizzled word tile, and after a barrier turns 4 x 4 byte blocks around
+// and writes four 16-byte runs of the transposed output.  The LayerNorm cast
+// uses it to transpose the row-major codes it has just written (still in L2)
+// instead of reading x a second time.
+
+__global__ void __launch_bounds__(kQtThreads) transpose_u8_kernel(const uint8_t *__restrict__ in,
+                                                                 int64_t rows, int64_t cols,
+                                                                 int64_t tiles_c, int64_t num_tiles,
+                                                                 uint8_t *__restrict__ out_t) {
+    __shared__ uint32_t tile[kQtTile * kQtTile / 4];
+    pdl_wait();
+    pdl_trigger();
+    const int tid = threadIdx.x;
+    for (int64_t t = blockIdx.x; t < num_tiles; t += gridDim.x) {
+        const int64_t r0 = (t / tiles_c) * kQtTile, c0 = (t % tiles_c) * kQtTile;
+        uint2 v[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int idx = i * kQtThreads + tid;
+            const int64_t r = r0 + (idx >> 4), c = c0 + (idx & 15) * 8;
+            v[i] = r < rows && c < cols ? *reinterpret_cast<const uint2 *>(in + r * cols + c)
+                                        : make_uint2(0u, 0u);
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int idx = i * kQtThreads + tid;
+            const int rr = idx >> 4, vv = idx & 15;
+            *reinterpret_cast<uint2 *>(&tile[rr * 32 + ((vv * 2) ^ qt_swz(rr))]) = v[i];
+        }
+        __syncthreads();
+        const int lane = tid & 31, warp = tid >> 5;
+        const int rblk = lane & 7;              // 16-row block of the tile
+        const int cw = warp * 4 + (lane >> 3);  // word column = 4 tile columns
+        uint32_t w[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            const int rr = rblk * 16 + j;
+            w[j] = tile[rr * 32 + (cw ^ qt_swz(rr))];
+        }
+        uint32_t o[4][4];
+#pragma unroll
+        for (int g = 0; g < 4; ++g)
+            transpose4x4(w[4 * g], w[4 * g + 1], w[4 * g + 2], w[4 * g + 3], o[0][g], o[1][g],
+                         o[2][g], o[3][g]);
+        const int64_t r = r0 + rblk * 16;
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
+            const int64_t c = c0 + cw * 4 + cc;
+            if (r < rows && c < cols)
+                *reinterpret_cast<uint4 *>(out_t + c * rows + r) =
+                    make_uint4(o[cc][0], o[cc][1], o[cc][2], o[cc][3]);
+        }
+        __syncthreads();   // the word tile is refilled by the next tile
+    }
+}
+
 // ------------------------------------------------------ LayerNorm row stats --
 //
 // One warp per row (grid-stride over rows): mean = sum(x) / C, then
@@ -1004,6 +1066,18 @@ cudaError_t launch_ln_cast_rows(const void *x, const void *gamma, const void *be
                                               mean, rstd, out, amax)
                     : lnf_launch<1, kLnfCast>(rows, c, sm_count, st, x, gamma, beta, eps, scale,
                                               mean, rstd, out, amax);
+}
+
+cudaError_t launch_transpose_u8(const uint8_t *in, int64_t rows, int64_t cols, uint8_t *out_t,
+                                int sm_count, cudaStream_t st) {
+    if (rows % 16 != 0 || cols % 16 != 0) return cudaErrorInvalidValue;
+    if (rows == 0 || cols == 0) return cudaSuccess;
+    const int64_t tiles_c = (cols + kQtTile - 1) / kQtTile;
+    const int64_t num_tiles = ((rows + kQtTile - 1) / kQtTile) * tiles_c;
+    int64_t grid = static_cast<int64_t>(sm_count) * 8;
+    if (grid > num_tiles) grid = num_tiles;
+    return launch_pdl(transpose_u8_kernel, dim3(static_cast<unsigned>(grid)), dim3(kQtThreads), 0,
+                      st, in, rows, cols, tiles_c, num_tiles, out_t);
 }
 
 // ----------------------------------------------------------- scale update --

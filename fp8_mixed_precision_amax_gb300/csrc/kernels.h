@@ -75,6 +75,11 @@ cudaError_t launch_ln_cast_rows(const void *x, const void *gamma, const void *be
                                 uint8_t *out, float *amax, bool zero_amax, float *mean,
                                 float *rstd, int sm_count, cudaStream_t st);
 
+// out_t[c][r] = in[r][c] for a [rows][cols] byte array (FP8 codes); rows
+// and cols multiples of 16.
+cudaError_t launch_transpose_u8(const uint8_t *in, int64_t rows, int64_t cols, uint8_t *out_t,
+                                int sm_count, cudaStream_t st);
+
 // Up to two tensors of one format in one persistent cast launch (tiles form
 // one list).  current = just-in-time scaling (an amax pass per tensor first).
 cudaError_t launch_cast_group(const CastSpec *specs, int n, int fmt, bool current, int margin,

@@ -272,9 +272,11 @@ fp8_status fp8_quantize_transpose_grouped(const fp8_cast_desc *descs, int32_t n,
  *   rstd[r] = 1 / sqrt(var[r] + eps),
  *   y[r][c] = ((x[r][c] - mean[r]) * rstd[r]) * gamma[c] + beta[c]   (fp32),
  * then the cast of y exactly as fp8_quantize_transpose casts x (y is never
- * written out in BF16).  Two kernels: row statistics, then LayerNorm + cast;
- * without out_t (a forward-only cast) and with rows of at most 4096 columns,
- * one kernel and one read of x, with the same statistics bit for bit.
+ * written out in BF16).  Rows of at most 4096 columns with out given: one
+ * kernel computes the statistics and the row-major codes from one read of x,
+ * and out_t (if given) is the byte transpose of those codes.  Otherwise two
+ * kernels: row statistics, then LayerNorm + cast.  Both compute the same
+ * statistics bit for bit.
  *   x      DEVICE [rows][cols] BF16;  gamma, beta  DEVICE [cols] BF16
  *   eps    >= 0;  scale  DEVICE, 1 float;  fmt, out, out_t as fp8_quantize_transpose
  *   amax   DEVICE, 1 float overwritten with max |y| (fp32 y, NaN skipped), or NULL
@@ -289,7 +291,8 @@ fp8_status fp8_layernorm_quantize_transpose(const void *x, const void *gamma, co
                                             void *stream);
 
 /* Forward of LayerNorm + FP8 linear (te.LayerNormLinear): Y = LN(X) W^T with
- * LN(X) cast to E4M3 by the fused kernel above (its amax is slot X's), W cast
+ * LN(X) cast to E4M3 as fp8_layernorm_quantize_transpose casts it (its amax
+ * is slot X's; under delayed scaling X8t is the byte transpose of X8), W cast
  * as in fp8_linear_fwd, then fprop.  Arguments as fp8_linear_fwd plus gamma,
  * beta [K] (BF16), eps, and mean, rstd [M] (fp32 outputs).  X8 / X8t hold the
  * FP8 LayerNorm output, so fp8_linear_bwd follows unchanged. */

@@ -109,6 +109,7 @@ def test_layernorm_linear_step_matches_oracle():
         assert abs(lin.meta.scale[o.SLOT_X].item() - sx) <= 1e-5 * sx
         assert abs(lin.meta.amax[o.SLOT_X].item() - np.abs(y).max()) <= 1e-5 * np.abs(y).max()
         X8 = host_u8(lin.X8)
+        assert np.array_equal(host_u8(lin.X8t), X8.T)
         check_codes(X8, xb, gb, bb, mu, rs, y, lin.meta.scale[o.SLOT_X].item(), o.E4M3,
                     "LN(X) codes")
         check_elementwise_exact(X8, xb, gb, bb, lin.mean.cpu().numpy(), lin.rstd.cpu().numpy(),
@@ -129,9 +130,9 @@ def test_layernorm_linear_step_matches_oracle():
     f.fp8_sync_status()
 
 
-def _ln_cast(f, x, gamma, beta, s, fmt, transposed):
+def _ln_cast(f, x, gamma, beta, s, fmt, row_major, transposed):
     rows, cols = x.shape
-    out = torch.empty((rows, cols), dtype=torch.uint8, device="cuda")
+    out = torch.empty((rows, cols), dtype=torch.uint8, device="cuda") if row_major else None
     out_t = torch.empty((cols, rows), dtype=torch.uint8, device="cuda") if transposed else None
     am = torch.full((1,), -1.0, device="cuda")
     mean = torch.full((rows,), float("nan"), device="cuda")
@@ -140,29 +141,35 @@ def _ln_cast(f, x, gamma, beta, s, fmt, transposed):
                                        fmt, mean, rstd, out, out_t, am)
     f.fp8_sync_status()
     bits = lambda t: t.cpu().numpy().view(np.uint32)
-    return host_u8(out), (host_u8(out_t) if transposed else None), bits(mean), bits(rstd), \
-        bits(am)[0]
+    return (host_u8(out) if row_major else None), (host_u8(out_t) if transposed else None), \
+        bits(mean), bits(rstd), bits(am)[0]
 
 
 @pytest.mark.parametrize("rows,cols", [(16, 16), (48, 272), (1040, 1024), (1040, 4096),
-                                       (8192, 4096), (48, 4112)])
+                                       (8192, 4096), (48, 4112), (144, 400)])
 @pytest.mark.parametrize("fmt", [o.E4M3, o.E5M2])
 def test_layernorm_cast_one_pass_matches_two_kernels(rows, cols, fmt):
-    """Without a transposed copy, rows of up to 4096 columns take the one-pass
-    kernel (statistics, normalisation and cast from one read of x).  Its
-    codes, mean, rstd and amax must equal, bit for bit, those of the two-kernel
-    path (statistics kernel, then the cast with its transposed copy) on the
-    same input -- up to the 7B layer's X (8192 x 4096); the two-kernel result
-    is checked against the oracle as above.  (48, 4112) is past the one-pass
-    limit and takes two kernels both times."""
+    """Rows of up to 4096 columns with a row-major output take the one-pass
+    kernel (statistics, normalisation and cast from one read of x), and the
+    transposed copy, when asked for, is the byte transpose of its codes.
+    Three calls on the same input: row-major only, both outputs, transposed
+    only (this last one takes the two-kernel path: statistics kernel, then the
+    cast with its transposed copy).  Codes, mean, rstd and amax agree bit for
+    bit across all three, up to the 7B layer's X (8192 x 4096), and the
+    result is checked against the oracle as above.  (48, 4112) is past the
+    one-pass limit and takes two kernels every time; (144, 400) has ragged
+    128 x 128 transpose tiles."""
     f = _lib()
     x, gamma, beta = _inputs(rows, cols, 77 + rows + fmt)
     s = np.float32(448.0 / 6.0) if fmt == o.E4M3 else np.float32(57344.0 / 6.0)
-    q1, _, m1, r1, a1 = _ln_cast(f, x, gamma, beta, s, fmt, False)
-    q2, q2t, m2, r2, a2 = _ln_cast(f, x, gamma, beta, s, fmt, True)
+    q1, _, m1, r1, a1 = _ln_cast(f, x, gamma, beta, s, fmt, True, False)
+    q2, q2t, m2, r2, a2 = _ln_cast(f, x, gamma, beta, s, fmt, True, True)
+    _, q3t, m3, r3, a3 = _ln_cast(f, x, gamma, beta, s, fmt, False, True)
     assert np.array_equal(m1, m2) and np.array_equal(r1, r2) and a1 == a2
+    assert np.array_equal(m1, m3) and np.array_equal(r1, r3) and a1 == a3
     assert np.array_equal(q1, q2)
-    assert np.array_equal(q2t, q2.T)
+    assert np.array_equal(q2t, q1.T)
+    assert np.array_equal(q3t, q1.T)
     xb, gb, bb = host_bf16_bits(x), host_bf16_bits(gamma), host_bf16_bits(beta)
     y, mu, rs = o.layernorm(xb, gb, bb, 1e-5)
     mean = m2.view(np.float32)
