@@ -768,10 +768,9 @@ def secondary_cast_sweep(f):
 
 
 def secondary_layernorm_cast(f, w7, flush):
-    """LayerNorm + cast of the 7B layer's X (statistics kernel + fused cast),
-    against the plain cast of the same tensor; 4 B/element algorithmic.  The
-    forward-only cast (no transposed copy: one kernel, one read of X) is
-    timed too, 3 B/element algorithmic."""
+    """LayerNorm + cast of the 7B layer's X against the plain cast of the same
+    tensor: with the transposed copy, without it, and the transposed copy
+    alone (the two-kernel path: row statistics, then the cast)."""
     X = wl.layer_x(w7, 0, "cuda")
     g = torch.ones(w7.K, dtype=torch.bfloat16, device="cuda")
     b = torch.zeros(w7.K, dtype=torch.bfloat16, device="cuda")
@@ -790,6 +789,9 @@ def secondary_layernorm_cast(f, w7, flush):
         flush()
         tm.time("ln_cast_rows", lambda: f.fp8_layernorm_quantize_transpose(
             X, g, b, 1e-5, sc, 0, mean, rstd, o8, None))
+        flush()
+        tm.time("ln_cast_t_only", lambda: f.fp8_layernorm_quantize_transpose(
+            X, g, b, 1e-5, sc, 0, mean, rstd, None, o8t))
     torch.cuda.synchronize()
     tm.pairs = {k: v[3:] for k, v in tm.pairs.items()}
     ne = w7.M * w7.K
@@ -797,9 +799,12 @@ def secondary_layernorm_cast(f, w7, flush):
             "ln_cast_gbs": 4 * ne / (tm.mean_ms("ln_cast") / 1e3) / 1e9,
             "ln_cast_rows_us": tm.mean_ms("ln_cast_rows") * 1e3,
             "ln_cast_rows_gbs": 3 * ne / (tm.mean_ms("ln_cast_rows") / 1e3) / 1e9,
-            "note": "4 B/element algorithmic with the transposed copy (two kernels), 3 B/element "
-                    "without it (ln_cast_rows: one kernel, one read of X); L2 flushed before "
-                    "each launch"}
+            "ln_cast_t_only_us": tm.mean_ms("ln_cast_t_only") * 1e3,
+            "note": "ln_cast: the codes and their transposed copy (one pass over X, then a byte "
+                    "transpose of the codes), 4 B/element algorithmic; ln_cast_rows: the codes "
+                    "only (one kernel, one read of X), 3 B/element; ln_cast_t_only: the "
+                    "transposed copy only (row statistics, then the cast kernel); L2 flushed "
+                    "before each launch"}
 
 
 def secondary_adam(f, w7, flush):

@@ -325,8 +325,8 @@ __global__ void __launch_bounds__(kQtThreads, 2)
         } else {
             // LayerNorm first: y = ((x - mean) * rstd) * gamma + beta in fp32,
             // one rounding per operation in that order: the subtract and the
-            // two multiplies two lanes at a time, the add of beta scalar (a
-            // packed add of a packed product would be fused into an fma).
+            // add of beta in the mixed-precision scalar forms (x and beta stay
+            // BF16), the two multiplies two lanes at a time.
             // This thread's 8 columns are the same for all 8 of its vectors.
             const int vv = lvv;
             const int64_t c = lc;
@@ -344,19 +344,17 @@ __global__ void __launch_bounds__(kQtThreads, 2)
                 const int rr = (i * kQtThreads + tid) >> 4;
                 const int64_t r = r0 + rr;
                 const bool in = r < rows && c < cols;
-                const uint64_t mu2 = splat_f32x2(in ? lmu[i] : 0.0f);
+                const float mu = in ? lmu[i] : 0.0f;
                 const uint64_t rs2 = splat_f32x2(in ? lrs[i] : 0.0f);
                 const uint32_t xw[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
                 uint32_t qw[4];
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
                     float p0, p1, q0, q1;
-                    f32x2_unpack(
-                        f32x2_mul(f32x2_mul(f32x2_sub(f32x2_from_bf16x2(xw[j]), mu2), rs2),
-                                  gam2[j]),
-                        p0, p1);
-                    const float y0 = __fadd_rn(p0, bf16_lo(bw[j]));
-                    const float y1 = __fadd_rn(p1, bf16_hi(bw[j]));
+                    const float d0 = bf16lo_sub_f32(xw[j], mu), d1 = bf16hi_sub_f32(xw[j], mu);
+                    f32x2_unpack(f32x2_mul(f32x2_mul(f32x2_pack(d0, d1), rs2), gam2[j]), p0, p1);
+                    const float y0 = bf16lo_add_f32(bw[j], p0);
+                    const float y1 = bf16hi_add_f32(bw[j], p1);
                     const uint64_t y2 = f32x2_pack(y0, y1);
                     if (in) ymax = fmaxf(ymax, fmaxf(fabsf(y0), fabsf(y1)));
                     f32x2_unpack(f32x2_mul(y2, s2), q0, q1);
@@ -680,38 +678,36 @@ __global__ void __launch_bounds__(512) ln_stats_bulk_kernel(const uint16_t *__re
         if (lane == 0) ++consumed[b];
         const uint4 *xr = reinterpret_cast<const uint4 *>(mybuf + b * row_bytes);
         // the sum: eight partial sums per lane (one per element position of
-        // a 16-byte vector), vectors lane, lane + 32, ...; two lanes of an
-        // fp32 pair at a time (each lane one IEEE add, as the scalar adds)
-        uint64_t part2[4] = {0u, 0u, 0u, 0u};
+        // a 16-byte vector), vectors lane, lane + 32, ...; each one IEEE add
+        // of the widened BF16 (the mixed-precision form)
+        float part[8] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
         for (int i = lane; i < nvec; i += 32) {
             const uint4 v = xr[i];
             const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-            for (int q = 0; q < 4; ++q) part2[q] = f32x2_add(part2[q], f32x2_from_bf16x2(w[q]));
+            for (int q = 0; q < 4; ++q) {
+                part[2 * q] = bf16lo_add_f32(w[q], part[2 * q]);
+                part[2 * q + 1] = bf16hi_add_f32(w[q], part[2 * q + 1]);
+            }
         }
-        float part[8];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) f32x2_unpack(part2[q], part[2 * q], part[2 * q + 1]);
         float sum = 0.0f;
 #pragma unroll
         for (int q = 0; q < 8; ++q) sum = __fadd_rn(sum, part[q]);
         const float mu = __fmul_rn(warp_sum(sum), inv_c);
         // the squared deviations, each accumulated with one fused
         // multiply-add (d * d + part, rounded once)
-        const uint64_t mu2 = splat_f32x2(mu);
 #pragma unroll
-        for (int q = 0; q < 4; ++q) part2[q] = 0u;
+        for (int q = 0; q < 8; ++q) part[q] = 0.0f;
         for (int i = lane; i < nvec; i += 32) {
             const uint4 v = xr[i];
             const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-                const uint64_t d = f32x2_sub(f32x2_from_bf16x2(w[q]), mu2);
-                part2[q] = f32x2_fma(d, d, part2[q]);
+                const float d0 = bf16lo_sub_f32(w[q], mu), d1 = bf16hi_sub_f32(w[q], mu);
+                part[2 * q] = __fmaf_rn(d0, d0, part[2 * q]);
+                part[2 * q + 1] = __fmaf_rn(d1, d1, part[2 * q + 1]);
             }
         }
-#pragma unroll
-        for (int q = 0; q < 4; ++q) f32x2_unpack(part2[q], part[2 * q], part[2 * q + 1]);
         float sq = 0.0f;
 #pragma unroll
         for (int q = 0; q < 8; ++q) sq = __fadd_rn(sq, part[q]);
@@ -767,9 +763,9 @@ __global__ void __launch_bounds__(512) ln_stats_bulk_kernel(const uint16_t *__re
 
 // ------------------------------------ LayerNorm + row-major cast, one pass --
 //
-// Delayed scaling knows the scale before the cast, so when no transposed copy
-// is wanted (a forward-only LayerNorm cast) the statistics, the normalisation
-// and the cast can share one read of x (rows of at most 4096 columns).  The
+// Delayed scaling knows the scale before the cast, so the statistics, the
+// normalisation and the row-major cast can share one read of x (rows of at
+// most 4096 columns).  The
 // same kernel computes the statistics alone (and max |y| for just-in-time
 // scaling) ahead of the two-kernel cast of such rows.  Each
 // CTA owns a balanced, contiguous range of rows and has 16 warps; warp w
@@ -781,10 +777,10 @@ __global__ void __launch_bounds__(512) ln_stats_bulk_kernel(const uint16_t *__re
 // ln_stats_bulk_kernel (the results are identical bit for bit), then
 // y = ((x - mean) * rstd) * gamma + beta and its cast exactly as the
 // LayerNorm branch of quantize_transpose_kernel (gamma and beta staged in
-// shared memory once per CTA), and writes the codes.  (With a transposed copy
-// the codes of enough rows to write whole sectors of it do not fit in shared
-// memory beside the row buffers; that case keeps the two kernels.)  Waits
-// are bounded.
+// shared memory once per CTA), and writes the codes; a transposed copy, when
+// wanted, is a byte transpose of those codes afterwards.  The two statistics
+// passes use the mixed-precision BF16 + fp32 forms, which round exactly as
+// widening first does.  Waits are bounded.
 
 constexpr int kLnfWarps = 16;
 constexpr int kLnfThreads = kLnfWarps * 32;
@@ -866,37 +862,36 @@ __global__ void __launch_bounds__(kLnfThreads, 1)
             ++issued;
         }
         // the sum: eight partial sums per lane over vectors lane, lane + 32, ...
-        uint64_t part2[4] = {0u, 0u, 0u, 0u};
-#pragma unroll
-        for (int t = 0; t < kLnfVecs; ++t) {
-            if (lane + 32 * t >= nvec) break;
-            const uint32_t w[4] = {v[t].x, v[t].y, v[t].z, v[t].w};
-#pragma unroll
-            for (int q = 0; q < 4; ++q) part2[q] = f32x2_add(part2[q], f32x2_from_bf16x2(w[q]));
-        }
-        float part[8];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) f32x2_unpack(part2[q], part[2 * q], part[2 * q + 1]);
-        float sum = 0.0f;
-#pragma unroll
-        for (int q = 0; q < 8; ++q) sum = __fadd_rn(sum, part[q]);
-        const float mu = __fmul_rn(warp_sum(sum), inv_c);
-        // the squared deviations, one fused multiply-add each
-        const uint64_t mu2 = splat_f32x2(mu);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) part2[q] = 0u;
+        // (partial 2q + h takes the half h of word q)
+        float part[8] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
         for (int t = 0; t < kLnfVecs; ++t) {
             if (lane + 32 * t >= nvec) break;
             const uint32_t w[4] = {v[t].x, v[t].y, v[t].z, v[t].w};
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-                const uint64_t d = f32x2_sub(f32x2_from_bf16x2(w[q]), mu2);
-                part2[q] = f32x2_fma(d, d, part2[q]);
+                part[2 * q] = bf16lo_add_f32(w[q], part[2 * q]);
+                part[2 * q + 1] = bf16hi_add_f32(w[q], part[2 * q + 1]);
             }
         }
+        float sum = 0.0f;
 #pragma unroll
-        for (int q = 0; q < 4; ++q) f32x2_unpack(part2[q], part[2 * q], part[2 * q + 1]);
+        for (int q = 0; q < 8; ++q) sum = __fadd_rn(sum, part[q]);
+        const float mu = __fmul_rn(warp_sum(sum), inv_c);
+        // the squared deviations, one fused multiply-add each
+#pragma unroll
+        for (int q = 0; q < 8; ++q) part[q] = 0.0f;
+#pragma unroll
+        for (int t = 0; t < kLnfVecs; ++t) {
+            if (lane + 32 * t >= nvec) break;
+            const uint32_t w[4] = {v[t].x, v[t].y, v[t].z, v[t].w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const float d0 = bf16lo_sub_f32(w[q], mu), d1 = bf16hi_sub_f32(w[q], mu);
+                part[2 * q] = __fmaf_rn(d0, d0, part[2 * q]);
+                part[2 * q + 1] = __fmaf_rn(d1, d1, part[2 * q + 1]);
+            }
+        }
         float sq = 0.0f;
 #pragma unroll
         for (int q = 0; q < 8; ++q) sq = __fadd_rn(sq, part[q]);
@@ -907,9 +902,9 @@ __global__ void __launch_bounds__(kLnfThreads, 1)
             rstd[r] = rs;
         }
         if constexpr (MODE == kLnfStats) continue;
-        // y and its codes: the subtract and both multiplies two lanes at a
-        // time, the add of beta scalar (a packed add of a packed product
-        // would be fused into an fma)
+        // y and its codes: the subtract of the mean and the add of beta in
+        // the mixed-precision scalar forms (x and beta stay BF16), both
+        // multiplies two lanes at a time
         const uint64_t rs2 = splat_f32x2(rs);
 #pragma unroll
         for (int t = 0; t < kLnfVecs; ++t) {
@@ -923,11 +918,12 @@ __global__ void __launch_bounds__(kLnfThreads, 1)
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 float p0, p1, c0, c1;
-                f32x2_unpack(f32x2_mul(f32x2_mul(f32x2_sub(f32x2_from_bf16x2(xw[q]), mu2), rs2),
+                const float d0 = bf16lo_sub_f32(xw[q], mu), d1 = bf16hi_sub_f32(xw[q], mu);
+                f32x2_unpack(f32x2_mul(f32x2_mul(f32x2_pack(d0, d1), rs2),
                                        f32x2_from_bf16x2(gw[q])),
                              p0, p1);
-                const float y0 = __fadd_rn(p0, bf16_lo(bw[q]));
-                const float y1 = __fadd_rn(p1, bf16_hi(bw[q]));
+                const float y0 = bf16lo_add_f32(bw[q], p0);
+                const float y1 = bf16hi_add_f32(bw[q], p1);
                 ymax = fmaxf(ymax, fmaxf(fabsf(y0), fabsf(y1)));
                 if constexpr (MODE == kLnfCast) {
                     f32x2_unpack(f32x2_mul(f32x2_pack(y0, y1), s2), c0, c1);

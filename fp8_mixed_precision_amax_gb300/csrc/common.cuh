@@ -402,6 +402,34 @@ __device__ __forceinline__ uint64_t f32x2_fma(uint64_t a, uint64_t b, uint64_t c
 }
 __device__ __forceinline__ uint64_t splat_f32x2(float s) { return f32x2_pack(s, s); }
 
+// Mixed-precision scalar forms: the low or high BF16 of w, widened to fp32
+// exactly, added to or less c with one rounding (the same result as widening
+// first, without the register pairing of the packed forms).
+__device__ __forceinline__ float bf16lo_add_f32(uint32_t w, float c) {
+    float d;
+    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tadd.rn.f32.bf16 %0, lo, %2;\n\t}"
+        : "=f"(d) : "r"(w), "f"(c));
+    return d;
+}
+__device__ __forceinline__ float bf16hi_add_f32(uint32_t w, float c) {
+    float d;
+    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tadd.rn.f32.bf16 %0, hi, %2;\n\t}"
+        : "=f"(d) : "r"(w), "f"(c));
+    return d;
+}
+__device__ __forceinline__ float bf16lo_sub_f32(uint32_t w, float c) {
+    float d;
+    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tsub.rn.f32.bf16 %0, lo, %2;\n\t}"
+        : "=f"(d) : "r"(w), "f"(c));
+    return d;
+}
+__device__ __forceinline__ float bf16hi_sub_f32(uint32_t w, float c) {
+    float d;
+    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tsub.rn.f32.bf16 %0, hi, %2;\n\t}"
+        : "=f"(d) : "r"(w), "f"(c));
+    return d;
+}
+
 // Two fp32 values (bit patterns lo, hi) times s2 = {s, s}, rounded to BF16
 // and packed (lo in the low half).
 __device__ __forceinline__ uint32_t scale_bf16x2(uint32_t lo, uint32_t hi, uint64_t s2) {

@@ -146,7 +146,7 @@ def _ln_cast(f, x, gamma, beta, s, fmt, row_major, transposed):
 
 
 @pytest.mark.parametrize("rows,cols", [(16, 16), (48, 272), (1040, 1024), (1040, 4096),
-                                       (8192, 4096), (48, 4112), (144, 400)])
+                                       (8192, 4096), (48, 4112), (144, 400), (6080, 400)])
 @pytest.mark.parametrize("fmt", [o.E4M3, o.E5M2])
 def test_layernorm_cast_one_pass_matches_two_kernels(rows, cols, fmt):
     """Rows of up to 4096 columns with a row-major output take the one-pass
@@ -158,7 +158,8 @@ def test_layernorm_cast_one_pass_matches_two_kernels(rows, cols, fmt):
     bit across all three, up to the 7B layer's X (8192 x 4096), and the
     result is checked against the oracle as above.  (48, 4112) is past the
     one-pass limit and takes two kernels every time; (144, 400) has ragged
-    128 x 128 transpose tiles."""
+    128 x 128 transpose tiles; (6080, 400) gives each CTA 40 rows over its 32
+    row buffers, so the warps owning two buffers take rows from both."""
     f = _lib()
     x, gamma, beta = _inputs(rows, cols, 77 + rows + fmt)
     s = np.float32(448.0 / 6.0) if fmt == o.E4M3 else np.float32(57344.0 / 6.0)
