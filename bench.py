@@ -717,7 +717,7 @@ def run_secondary(f, args, pk):
     if want("cast_sweep"):
         out["cast_sweep"] = secondary_cast_sweep(f)
     if want("layernorm_cast"):
-        out["layernorm_cast_mlp7b_X"] = secondary_layernorm_cast(f, w7, flush)
+        out["layernorm_cast_mlp7b_X"] = secondary_layernorm_cast(f, w7, flush, pk)
     if want("fp8_adam"):
         out["fp8_adam_step_mlp7b_W"] = secondary_adam(f, w7, flush)
     if want("jit_scaling"):
@@ -767,10 +767,12 @@ def secondary_cast_sweep(f):
     return sweep
 
 
-def secondary_layernorm_cast(f, w7, flush):
+def secondary_layernorm_cast(f, w7, flush, pk):
     """LayerNorm + cast of the 7B layer's X against the plain cast of the same
     tensor: with the transposed copy, without it, and the transposed copy
-    alone (the two-kernel path: row statistics, then the cast)."""
+    alone (the two-kernel path: row statistics, then the cast).  Then the row
+    statistics alone (2 B/element algorithmic), on X and on 16 copies of X
+    stacked (1 GiB), where the fixed cost of a launch no longer counts."""
     X = wl.layer_x(w7, 0, "cuda")
     g = torch.ones(w7.K, dtype=torch.bfloat16, device="cuda")
     b = torch.zeros(w7.K, dtype=torch.bfloat16, device="cuda")
@@ -792,10 +794,25 @@ def secondary_layernorm_cast(f, w7, flush):
         flush()
         tm.time("ln_cast_t_only", lambda: f.fp8_layernorm_quantize_transpose(
             X, g, b, 1e-5, sc, 0, mean, rstd, None, o8t))
+    big = X.repeat(16, 1)
+    mean_b = torch.empty(big.shape[0], device="cuda")
+    rstd_b = torch.empty(big.shape[0], device="cuda")
+    for i in range(23):
+        flush()
+        tm.time("ln_stats", lambda: f.fp8_layernorm_stats(X, g, b, 1e-5, mean, rstd))
+        flush()
+        tm.time("ln_stats_1g", lambda: f.fp8_layernorm_stats(big, g, b, 1e-5, mean_b, rstd_b))
     torch.cuda.synchronize()
+    del big
     tm.pairs = {k: v[3:] for k, v in tm.pairs.items()}
     ne = w7.M * w7.K
-    return {"ln_cast_us": tm.mean_ms("ln_cast") * 1e3, "cast_us": tm.mean_ms("cast") * 1e3,
+    stats = {}
+    for k, n in (("ln_stats", ne), ("ln_stats_1g", 16 * ne)):
+        us = tm.mean_ms(k) * 1e3
+        gbs = 2 * n / us / 1e3
+        stats[k] = {"us": us, "gbs": gbs, "frac": gbs / pk["hbm_gbs"], "elements": n}
+    return {"ln_stats": stats["ln_stats"], "ln_stats_16x": stats["ln_stats_1g"],
+            "ln_cast_us": tm.mean_ms("ln_cast") * 1e3, "cast_us": tm.mean_ms("cast") * 1e3,
             "ln_cast_gbs": 4 * ne / (tm.mean_ms("ln_cast") / 1e3) / 1e9,
             "ln_cast_rows_us": tm.mean_ms("ln_cast_rows") * 1e3,
             "ln_cast_rows_gbs": 3 * ne / (tm.mean_ms("ln_cast_rows") / 1e3) / 1e9,
@@ -803,8 +820,9 @@ def secondary_layernorm_cast(f, w7, flush):
             "note": "ln_cast: the codes and their transposed copy (one pass over X, then a byte "
                     "transpose of the codes), 4 B/element algorithmic; ln_cast_rows: the codes "
                     "only (one kernel, one read of X), 3 B/element; ln_cast_t_only: the "
-                    "transposed copy only (row statistics, then the cast kernel); L2 flushed "
-                    "before each launch"}
+                    "transposed copy only (row statistics, then the cast kernel); ln_stats: "
+                    "the row statistics alone on X and on 16 copies of X (2 B/element), frac "
+                    "of measured HBM; L2 flushed before each launch"}
 
 
 def secondary_adam(f, w7, flush):

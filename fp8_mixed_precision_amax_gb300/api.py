@@ -97,6 +97,8 @@ def _load() -> ctypes.CDLL:
                            ctypes.c_int),
         "fp8_layernorm_quantize_transpose": ([vp, vp, vp, i64, i64, ctypes.c_float, vp, i32, vp,
                                               vp, vp, vp, vp, vp], ctypes.c_int),
+        "fp8_layernorm_stats": ([vp, vp, vp, i64, i64, ctypes.c_float, vp, vp, vp, vp],
+                                ctypes.c_int),
         "fp8_layernorm_linear_fwd": ([vp, vp, vp, ctypes.c_float, vp, i64, i64, i64,
                                       ctypes.POINTER(fp8_meta), ctypes.POINTER(fp8_recipe), vp, vp,
                                       vp, vp, vp, vp, vp, vp], ctypes.c_int),
@@ -365,6 +367,15 @@ def fp8_layernorm_quantize_transpose(x, gamma, beta, eps: float, scale, fmt: int
         _ptr(scale, torch.float32, "scale"), fmt, _p8(out, "out"), _p8(out_t, "out_t"),
         _ptr(amax, torch.float32, "amax"), _ptr(mean, torch.float32, "mean"),
         _ptr(rstd, torch.float32, "rstd"), _stream(stream)))
+
+
+def fp8_layernorm_stats(x, gamma, beta, eps: float, mean, rstd, amax=None, stream=None) -> None:
+    rows, cols = x.shape
+    _check(_lib.fp8_layernorm_stats(
+        _ptr(x, torch.bfloat16, "x"), _ptr(gamma, torch.bfloat16, "gamma"),
+        _ptr(beta, torch.bfloat16, "beta"), rows, cols, float(eps),
+        _ptr(mean, torch.float32, "mean"), _ptr(rstd, torch.float32, "rstd"),
+        _ptr(amax, torch.float32, "amax"), _stream(stream)))
 
 
 def fp8_layernorm_linear_fwd(X, gamma, beta, eps: float, W, meta: "Meta", recipe: "Recipe", X8, X8t,

@@ -497,6 +497,30 @@ fp8_status fp8_layernorm_quantize_transpose(const void *x, const void *gamma, co
     return FP8_OK;
 }
 
+fp8_status fp8_layernorm_stats(const void *x, const void *gamma, const void *beta, int64_t rows,
+                               int64_t cols, float eps, float *mean, float *rstd, float *amax,
+                               void *stream) {
+    const char *fn = "fp8_layernorm_stats";
+    const fp8k::CallRange range(fn);
+    FP8_TRY(check_dims16(fn, rows, "rows", cols, "cols"));
+    if (cols < 16) return fail(FP8_ERR_ARG, "%s: cols must be >= 16", fn);
+    if (!(eps >= 0.0f)) return fail(FP8_ERR_ARG, "%s: eps must be >= 0", fn);
+    const bool empty = rows == 0;
+    FP8_TRY(check_ptr(fn, x, "x", empty));
+    // gamma and beta enter only max |y|
+    FP8_TRY(check_ptr(fn, gamma, "gamma", amax == nullptr));
+    FP8_TRY(check_ptr(fn, beta, "beta", amax == nullptr));
+    FP8_TRY(check_scalar(fn, amax, "amax", true));
+    FP8_TRY(check_scalar(fn, mean, "mean", empty));
+    FP8_TRY(check_scalar(fn, rstd, "rstd", empty));
+    int sms;
+    FP8_TRY(current_device(&sms));
+    FP8_CUDA(fp8k::launch_ln_stats(x, gamma, beta, rows, cols, eps, mean, rstd, amax, sms,
+                                   static_cast<cudaStream_t>(stream)),
+             fn);
+    return FP8_OK;
+}
+
 static fp8_status linear_fwd_impl(const char *fn, const void *X, const void *gamma,
                                   const void *beta, float eps, const void *W, int64_t M, int64_t N,
                                   int64_t K, const fp8_meta *meta, const fp8_recipe *recipe,

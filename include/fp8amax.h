@@ -290,6 +290,24 @@ fp8_status fp8_layernorm_quantize_transpose(const void *x, const void *gamma, co
                                             uint8_t *out_t, float *amax, float *mean, float *rstd,
                                             void *stream);
 
+/* LayerNorm row statistics alone (te.LayerNormLinear's LayerNorm; the same
+ * page and section as fp8_layernorm_quantize_transpose): mean[r] and rstd[r]
+ * exactly as that call computes them (bit for bit), which the LayerNorm
+ * backward keeps, and, if amax is given, max |y| over y = LN(x) as defined
+ * there: the amax that just-in-time scaling needs before any code is written.
+ *   x      DEVICE [rows][cols] BF16
+ *   gamma, beta  DEVICE [cols] BF16, read only when amax is given (else may be NULL)
+ *   eps    >= 0
+ *   mean, rstd  DEVICE [rows] fp32 outputs
+ *   amax   DEVICE, 1 float overwritten with max |y| (fp32 y, NaN skipped; 0 for
+ *          no rows), or NULL
+ * rows, cols multiples of 16, cols >= 16; x, gamma, beta 16-byte aligned.
+ * Rows of at most 4096 columns are held in registers (one HBM read of x);
+ * wider rows are staged in shared memory or, past 8192 columns, read twice. */
+fp8_status fp8_layernorm_stats(const void *x, const void *gamma, const void *beta, int64_t rows,
+                               int64_t cols, float eps, float *mean, float *rstd, float *amax,
+                               void *stream);
+
 /* Forward of LayerNorm + FP8 linear (te.LayerNormLinear): Y = LN(X) W^T with
  * LN(X) cast to E4M3 as fp8_layernorm_quantize_transpose casts it (its amax
  * is slot X's; under delayed scaling X8t is the byte transpose of X8), W cast

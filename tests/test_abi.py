@@ -143,6 +143,16 @@ def test_host_side_checks_of_the_grouped_layernorm_optimizer_and_reduction_calls
     assert _err(ln(16, 16, float("nan"), p16, p16))[0] == ERR_ARG
     assert _err(ln(16, 16, 1e-5, None, None))[0] == ERR_ARG
     assert _err(ln(16, 24, 1e-5, p16, p16))[0] == ERR_ALIGN
+    # LayerNorm statistics alone: gamma and beta are needed only with amax
+    st = lambda rows, cols, eps, g, am: lib.fp8_layernorm_stats(p16, g, g, rows, cols, eps, p16,
+                                                                p16, am, None)
+    s, msg = _err(st(16, 0, 1e-5, p16, None))
+    assert s == ERR_ARG and "cols" in msg
+    assert _err(st(16, 16, -1.0, p16, None))[0] == ERR_ARG
+    s, msg = _err(st(16, 16, 1e-5, None, p16))
+    assert s == ERR_ARG and "gamma" in msg
+    assert _err(st(16, 24, 1e-5, p16, None))[0] == ERR_ALIGN
+    assert _err(st(-16, 16, 1e-5, p16, None))[0] == ERR_ARG
     # the allocation-free backward takes at most 2^25 dY elements
     meta = api.fp8_meta(0x1000, 0x1000, 0x1000, 0x1000, 16)
     rec = api.fp8_recipe(0, 16, 1, 0)

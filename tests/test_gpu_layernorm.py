@@ -180,6 +180,47 @@ def test_layernorm_cast_one_pass_matches_two_kernels(rows, cols, fmt):
                             np.uint32(a2).view(np.float32), f"{rows}x{cols}")
 
 
+@pytest.mark.parametrize("rows,cols", [(16, 16), (1040, 4096), (6080, 400), (256, 8192),
+                                       (48, 12288)])
+def test_layernorm_stats_alone(rows, cols):
+    """fp8_layernorm_stats gives the mean, rstd and max |y| of the LayerNorm
+    cast bit for bit (the register, shared-memory and looping statistics
+    kernels), and without amax needs neither gamma nor beta."""
+    f = _lib()
+    x, gamma, beta = _inputs(rows, cols, 5 + rows + cols)
+    s = np.float32(448.0 / 6.0)
+    q, _, m_ref, r_ref, a_ref = _ln_cast(f, x, gamma, beta, s, o.E4M3, True, False)
+    mean = torch.full((rows,), float("nan"), device="cuda")
+    rstd = torch.full((rows,), float("nan"), device="cuda")
+    am = torch.full((1,), -1.0, device="cuda")
+    f.fp8_layernorm_stats(x, gamma, beta, 1e-5, mean, rstd, am)
+    f.fp8_sync_status()
+    bits = lambda t: t.cpu().numpy().view(np.uint32)
+    assert np.array_equal(bits(mean), m_ref) and np.array_equal(bits(rstd), r_ref)
+    assert bits(am)[0] == a_ref
+    mean.fill_(float("nan"))
+    rstd.fill_(float("nan"))
+    f.fp8_layernorm_stats(x, None, None, 1e-5, mean, rstd)
+    f.fp8_sync_status()
+    assert np.array_equal(bits(mean), m_ref) and np.array_equal(bits(rstd), r_ref)
+    # and against the oracle's fp64 statistics
+    _, mu, rs = o.layernorm(host_bf16_bits(x), host_bf16_bits(gamma), host_bf16_bits(beta), 1e-5)
+    assert np.allclose(m_ref.view(np.float32), mu, rtol=1e-5, atol=1e-5 * np.abs(mu).max())
+    assert np.allclose(r_ref.view(np.float32), rs, rtol=1e-5)
+
+
+def test_layernorm_stats_no_rows():
+    """No rows: nothing is read, and amax is overwritten with 0."""
+    f = _lib()
+    x = torch.empty((0, 64), dtype=torch.bfloat16, device="cuda")
+    g = torch.ones(64, dtype=torch.bfloat16, device="cuda")
+    am = torch.full((1,), -1.0, device="cuda")
+    e = torch.empty(0, device="cuda")
+    f.fp8_layernorm_stats(x, g, g, 1e-5, e, e, am)
+    f.fp8_sync_status()
+    assert am.item() == 0.0
+
+
 @pytest.mark.parametrize("cols", [4096, 8192, 12288])
 def test_layernorm_constant_rows(cols):
     """Degenerate rows whose elements are all equal: the variance is 0, so
