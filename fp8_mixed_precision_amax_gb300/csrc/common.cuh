@@ -402,6 +402,48 @@ __device__ __forceinline__ uint64_t f32x2_fma(uint64_t a, uint64_t b, uint64_t c
 }
 __device__ __forceinline__ uint64_t splat_f32x2(float s) { return f32x2_pack(s, s); }
 
+// Division by a divisor known in advance, correctly rounded (to nearest,
+// ties to even), two lanes at a time.  With y = RN(1/b) (itself an IEEE
+// division, once), q0 = RN(a*y) is within 1.5 ulp of a/b; one correction
+// q1 = RN(q0 + RN(a - b*q0)*y) makes it faithful, and a second one is exact
+// by Markstein's theorem (y within half an ulp of 1/b and q1 within one ulp
+// of a/b give RN(q1 + (a - b*q1)*y) = RN(a/b), the remainder a - b*q1 being
+// exact in an fma).  The theorem needs no overflow or underflow on the way,
+// which holds for 2^-20 <= b <= 1 and 2^-100 <= |a| <= 2^100; other a
+// (zeros, whose sign the corrections would lose, NaN, infinities, the
+// extremes) and other b take __fdiv_rn.
+struct DivConst {
+    uint64_t y2, nb2;   // {y, y} and {-b, -b}
+    float b;
+    bool fast;          // 2^-20 <= b <= 1
+};
+__device__ __forceinline__ DivConst div_const(float b) {
+    DivConst d;
+    d.b = b;
+    d.fast = b >= 0x1p-20f && b <= 1.0f;
+    d.y2 = splat_f32x2(__fdiv_rn(1.0f, b));
+    d.nb2 = splat_f32x2(-b);
+    return d;
+}
+__device__ __forceinline__ bool div_const_in_range(float a) {
+    const float aa = fabsf(a);
+    return aa >= 0x1p-100f && aa <= 0x1p100f;   // false for NaN
+}
+static __device__ __noinline__ float div_const_slow(float a, float b) { return __fdiv_rn(a, b); }
+__device__ __forceinline__ void div_by_const2(float a0, float a1, const DivConst &d, float &q0,
+                                              float &q1) {
+    const uint64_t a2 = f32x2_pack(a0, a1);
+    uint64_t q = f32x2_mul(a2, d.y2);
+    q = f32x2_fma(f32x2_fma(d.nb2, q, a2), d.y2, q);
+    q = f32x2_fma(f32x2_fma(d.nb2, q, a2), d.y2, q);
+    f32x2_unpack(q, q0, q1);
+    const bool ok0 = d.fast && div_const_in_range(a0), ok1 = d.fast && div_const_in_range(a1);
+    if (!(ok0 && ok1)) {
+        if (!ok0) q0 = div_const_slow(a0, d.b);
+        if (!ok1) q1 = div_const_slow(a1, d.b);
+    }
+}
+
 // Mixed-precision scalar forms: the low or high BF16 of w, widened to fp32
 // exactly, added to or less c with one rounding (the same result as widening
 // first, without the register pairing of the packed forms).

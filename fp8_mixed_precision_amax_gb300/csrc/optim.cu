@@ -76,11 +76,11 @@ struct Elem8 {
     float m[8], v[8], w[8];
 };
 
-// Loop-invariant operands, each duplicated into both lanes of an fp32 pair
-// (the bias corrections are divisors, used one lane at a time).
+// Loop-invariant operands, each duplicated into both lanes of an fp32 pair;
+// the bias corrections as divisors known in advance.
 struct AdamConst {
     uint64_t b1, omb1, b2, omb2, eps, lr, wd, msi, wsi;
-    float bc1, bc2;
+    DivConst bc1, bc2;
 };
 
 __device__ __forceinline__ AdamConst adam_const(const AdamArgs &a, float msi, float wsi) {
@@ -89,8 +89,8 @@ __device__ __forceinline__ AdamConst adam_const(const AdamArgs &a, float msi, fl
     c.omb1 = splat_f32x2(__fsub_rn(1.0f, a.b1));
     c.b2 = splat_f32x2(a.b2);
     c.omb2 = splat_f32x2(__fsub_rn(1.0f, a.b2));
-    c.bc1 = a.bc1;
-    c.bc2 = a.bc2;
+    c.bc1 = div_const(a.bc1);
+    c.bc2 = div_const(a.bc2);
     c.eps = splat_f32x2(a.eps);
     c.lr = splat_f32x2(a.lr);
     c.wd = splat_f32x2(a.wd);
@@ -123,6 +123,19 @@ __device__ __forceinline__ Raw8 adam_load8(const AdamArgs &a, int64_t i) {
     return r;
 }
 
+// m = b1*m + (1-b1)*g for one pair: m decoded from its two E4M3 codes times
+// the first moment's scale_inv, g the pair's gradient widened to fp32.
+__device__ __forceinline__ void adam_m_pair(uint16_t mcodes, uint64_t g, const AdamConst &k,
+                                            float &m0, float &m1) {
+    float md0, md1, a0, a1, b0, b1;
+    e4m3x2_dec(mcodes, md0, md1);
+    const uint64_t m_old = f32x2_mul(f32x2_pack(md0, md1), k.msi);
+    f32x2_unpack(f32x2_mul(k.b1, m_old), a0, a1);
+    f32x2_unpack(f32x2_mul(k.omb1, g), b0, b1);
+    m0 = __fadd_rn(a0, b0);
+    m1 = __fadd_rn(a1, b1);
+}
+
 __device__ __forceinline__ void adam8(const Raw8 &raw, const AdamConst &k, Elem8 &e) {
     const uint4 g4 = raw.g4, v4 = raw.v4, w4 = raw.w4;
     const uint2 m8 = raw.m8;
@@ -130,25 +143,21 @@ __device__ __forceinline__ void adam8(const Raw8 &raw, const AdamConst &k, Elem8
                    ww[4] = {w4.x, w4.y, w4.z, w4.w}, mw[2] = {m8.x, m8.y};
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-        float md0, md1;
-        e4m3x2_dec(static_cast<uint16_t>(mw[j >> 1] >> (16 * (j & 1))), md0, md1);
         const uint64_t g = f32x2_from_bf16x2(gw[j]);
-        const uint64_t m_old = f32x2_mul(f32x2_pack(md0, md1), k.msi);
         const uint64_t v_old = f16x2_to_f32x2(vw[j]);
         const uint64_t w_old = f32x2_mul(f16x2_to_f32x2(ww[j]), k.wsi);
-        float a0, a1, b0, b1;
+        float a0, a1, b0, b1, m0, m1;
         // m = b1*m + (1-b1)*g
-        f32x2_unpack(f32x2_mul(k.b1, m_old), a0, a1);
-        f32x2_unpack(f32x2_mul(k.omb1, g), b0, b1);
-        const float m0 = __fadd_rn(a0, b0), m1 = __fadd_rn(a1, b1);
+        adam_m_pair(static_cast<uint16_t>(mw[j >> 1] >> (16 * (j & 1))), g, k, m0, m1);
         // v = b2*v + (1-b2)*(g*g)
         f32x2_unpack(f32x2_mul(k.b2, v_old), a0, a1);
         f32x2_unpack(f32x2_mul(k.omb2, f32x2_mul(g, g)), b0, b1);
         const float v0 = __fadd_rn(a0, b0), v1 = __fadd_rn(a1, b1);
-        // u = (m / bc1) / (sqrt(v / bc2) + eps)
-        float e0, e1;
-        const float n0 = __fdiv_rn(m0, k.bc1), n1 = __fdiv_rn(m1, k.bc1);
-        const float q0 = __fdiv_rn(v0, k.bc2), q1 = __fdiv_rn(v1, k.bc2);
+        // u = (m / bc1) / (sqrt(v / bc2) + eps); the bias corrections are
+        // divisors known in advance, each quotient correctly rounded
+        float e0, e1, n0, n1, q0, q1;
+        div_by_const2(m0, m1, k.bc1, n0, n1);
+        div_by_const2(v0, v1, k.bc2, q0, q1);
         f32x2_unpack(k.eps, e0, e1);
         const float u0 = __fdiv_rn(n0, __fadd_rn(__fsqrt_rn(q0), e0));
         const float u1 = __fdiv_rn(n1, __fadd_rn(__fsqrt_rn(q1), e1));
