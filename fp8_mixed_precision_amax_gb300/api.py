@@ -10,12 +10,14 @@ fallback: if ``libfp8amax.so`` is missing, importing this module fails.
 from __future__ import annotations
 
 import ctypes
+import logging
 import os
 import re
 from dataclasses import dataclass
 
 import torch
 
+_log = logging.getLogger(__name__)
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libfp8amax.so")
 HEADER_PATH = os.path.join(os.path.dirname(_PKG), "include", "fp8amax.h")
@@ -312,6 +314,12 @@ class Recipe:
         return fp8_recipe(self.margin, self.history_len, 1 if self.hybrid else 0,
                           SCALING_CURRENT if self.current else SCALING_DELAYED)
 
+    def describe(self) -> str:
+        """The precision mode in words, as a layer logs it when it is built."""
+        return (f"E4M3 forward, {'E5M2' if self.hybrid else 'E4M3'} backward, "
+                f"{'just-in-time' if self.current else 'delayed'} scaling, margin "
+                f"{self.margin}, amax history {self.history_len}")
+
 
 class Meta:
     """Per-layer scaling state on the device: history [5, L], amax [5],
@@ -441,6 +449,7 @@ class Fp8Linear:
         self.recipe = recipe or Recipe()
         self.W = W
         N, K = W.shape
+        _log.info("FP8 linear [%d x %d], up to %d tokens: %s", N, K, M, self.recipe.describe())
         dev = W.device
         self.M, self.N, self.K = M, N, K
         self.meta = Meta(self.recipe.history_len, dev)

@@ -186,3 +186,19 @@ def test_clock_probe_pointer_must_be_aligned():
     assert lib.fp8_set_clock_probe(ctypes.c_void_p(0x1004)) == 2
     assert b"8-byte aligned" in lib.fp8_last_error()
     assert lib.fp8_set_clock_probe(None) == 0
+
+
+def test_layer_logs_its_precision_mode(caplog):
+    """A layer logs the precision mode it runs in when it is built (the
+    implementation guide's advice to log it at start); building allocates
+    buffers only, so CPU tensors serve here."""
+    import logging
+    import torch
+    W = torch.zeros(32, 16, dtype=torch.bfloat16)
+    with caplog.at_level(logging.INFO, logger="fp8_mixed_precision_amax_gb300.api"):
+        f.Fp8Linear(W, 48, f.Recipe(margin=1, history_len=16, hybrid=True))
+        f.Fp8Linear(W, 48, f.Recipe(hybrid=False, current=True))
+    msgs = [r.getMessage() for r in caplog.records]
+    assert any("[32 x 16]" in m and "E5M2 backward" in m and "delayed" in m and "margin 1" in m
+               and "history 16" in m for m in msgs), msgs
+    assert any("E4M3 backward" in m and "just-in-time" in m for m in msgs), msgs
