@@ -180,6 +180,31 @@ def test_layernorm_cast_one_pass_matches_two_kernels(rows, cols, fmt):
                             np.uint32(a2).view(np.float32), f"{rows}x{cols}")
 
 
+def _random_shapes(n, seed):
+    rng = np.random.default_rng(seed)
+    return [(16 * int(rng.integers(1, 190)), 16 * int(rng.integers(1, 257))) for _ in range(n)]
+
+
+@pytest.mark.parametrize("rows,cols", _random_shapes(12, 4242))
+def test_layernorm_cast_random_shapes(rows, cols):
+    """Seeded random shapes (multiples of 16 up to 3024 x 4096, mostly not of
+    128: ragged transpose tiles and uneven rows per CTA): the one-pass cast,
+    its byte transpose and the two-kernel path agree bit for bit, and the
+    codes are exact given the kernels' statistics."""
+    f = _lib()
+    x, gamma, beta = _inputs(rows, cols, rows * 7 + cols)
+    s = np.float32(448.0 / 6.0)
+    q1, _, m1, r1, a1 = _ln_cast(f, x, gamma, beta, s, o.E4M3, True, False)
+    q2, q2t, m2, r2, a2 = _ln_cast(f, x, gamma, beta, s, o.E4M3, True, True)
+    _, q3t, m3, r3, a3 = _ln_cast(f, x, gamma, beta, s, o.E4M3, False, True)
+    assert np.array_equal(q1, q2) and np.array_equal(q2t, q1.T) and np.array_equal(q3t, q1.T)
+    assert np.array_equal(m1, m2) and np.array_equal(m1, m3)
+    assert np.array_equal(r1, r2) and np.array_equal(r1, r3) and a1 == a2 == a3
+    xb, gb, bb = host_bf16_bits(x), host_bf16_bits(gamma), host_bf16_bits(beta)
+    check_elementwise_exact(q1, xb, gb, bb, m1.view(np.float32), r1.view(np.float32), s, o.E4M3,
+                            np.uint32(a1).view(np.float32), f"{rows}x{cols}")
+
+
 @pytest.mark.parametrize("rows,cols", [(16, 16), (1040, 4096), (6080, 400), (256, 8192),
                                        (48, 12288)])
 def test_layernorm_stats_alone(rows, cols):
