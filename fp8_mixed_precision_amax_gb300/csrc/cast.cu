@@ -765,11 +765,11 @@ __global__ void __launch_bounds__(512) ln_stats_bulk_kernel(const uint16_t *__re
 //
 // Delayed scaling knows the scale before the cast, so the statistics, the
 // normalisation and the row-major cast can share one read of x (rows of at
-// most 4096 columns).  The
-// same kernel computes the statistics alone (and max |y| for just-in-time
-// scaling) ahead of the two-kernel cast of such rows.  Each
-// CTA owns a balanced, contiguous range of rows and has 16 warps; warp w
-// takes rows w, w + 16, ... of the range.  Every warp owns one row buffer: it
+// most 4096 columns).  The same kernel computes the statistics alone (and
+// max |y| for just-in-time scaling), for fp8_layernorm_stats and ahead of
+// the two-kernel cast of such rows.  Each CTA owns a balanced, contiguous
+// range of rows and has 16 warps; warp w takes rows w, w + 16, ... of the
+// range.  Every warp owns one row buffer: it
 // copies its row from the buffer into registers (16 vectors of 8 BF16 per
 // lane at most), at once starts the untiled bulk copy of its next row into
 // the same buffer, and works on the registers meanwhile.  From them it
@@ -779,8 +779,9 @@ __global__ void __launch_bounds__(512) ln_stats_bulk_kernel(const uint16_t *__re
 // LayerNorm branch of quantize_transpose_kernel (gamma and beta staged in
 // shared memory once per CTA), and writes the codes; a transposed copy, when
 // wanted, is a byte transpose of those codes afterwards.  The two statistics
-// passes use the mixed-precision BF16 + fp32 forms, which round exactly as
-// widening first does.  Waits are bounded.
+// passes, the subtract of the mean and the add of beta use the
+// mixed-precision BF16 + fp32 forms, which round exactly as widening first
+// does.  Waits are bounded.
 
 constexpr int kLnfWarps = 16;
 constexpr int kLnfThreads = kLnfWarps * 32;
