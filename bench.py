@@ -515,6 +515,17 @@ def run_e2e(f, lin, X, dY, args, world, flops, readback="metric"):
     for i in range(3):
         step(i)
     torch.cuda.synchronize()
+    # the host link alone: the step's two uploads with nothing else running
+    link_ms = []
+    for _ in range(3):
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(up):
+            a0.record(up)
+            dXin[0].copy_(hX[0], non_blocking=True)
+            ddYin[0].copy_(hdY[0], non_blocking=True)
+            a1.record(up)
+        torch.cuda.synchronize()
+        link_ms.append(a0.elapsed_time(a1))
     barrier(world)
     s = torch.cuda.Event(enable_timing=True)
     e = torch.cuda.Event(enable_timing=True)
@@ -531,8 +542,11 @@ def run_e2e(f, lin, X, dY, args, world, flops, readback="metric"):
     ms = max_over_ranks(s.elapsed_time(e), world)
     h2d = X.numel() * X.element_size() + dY.numel() * dY.element_size()
     d2h = sum(t.numel() * t.element_size() for t in dres[0])
+    link = min(link_ms)
     return {"value": world * n * flops / (ms / 1e3) / 1e12, "unit": "TFLOPS",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n,
+            "h2d_gbs_alone": h2d / (link / 1e3) / 1e9,
+            "upload_bound_tflops": world * flops / (link / 1e3) / 1e12,
             "readback": ("Y, dX and dW" if readback == "outputs" else
                          "the step's new scales and scale_inv (its scaling state)"),
             "overlap": "uploads, compute and downloads on three streams, double-buffered"}
