@@ -88,12 +88,16 @@ def test_layernorm_cast_matches_oracle(rows, cols, fmt):
     assert np.array_equal(host_u8(out_t), q.T)
 
 
-def test_layernorm_linear_step_matches_oracle():
+@pytest.mark.parametrize("M,K,N", [(1040, 1024, 784), (272, 4112, 144)])
+def test_layernorm_linear_step_matches_oracle(M, K, N):
     """One step of LayerNorm + FP8 linear (te.LayerNormLinear) then the
     linear's backward, against the oracle: LN(X) codes as above, Y / dX / dW
-    within the GEMM tolerance; a second step under just-in-time scaling."""
+    within the GEMM tolerance; a second step under just-in-time scaling.
+    K = 1024 takes the one-pass LayerNorm cast under delayed scaling, K = 4112
+    (past its 4096-column limit) the statistics kernel and the cast kernel's
+    LayerNorm branch."""
     f = _lib()
-    w = wl.Workload("ln", 1040, 1024, 784, "normal", 1.0, 0.03, 1e-2, 16, 0, True, 2)
+    w = wl.Workload("ln", M, K, N, "normal", 1.0, 0.03, 1e-2, 16, 0, True, 2)
     W = wl.layer_weight(w, "cuda")
     for current in (False, True):
         _, gamma, beta = _inputs(16, w.K, 5)
