@@ -1,7 +1,8 @@
 """CPU oracle for the FP8 delayed-scaling linear layer -- TEST INFRASTRUCTURE.
 
 Only the test suite, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
-``bench.py`` may import this package.  The product library never imports,
+``bench.py`` may import this package (``python -m oracle`` runs it on its own
+and prints its results for a workload's seeded inputs).  The product library never imports,
 links or runs it, and it shares no code with the CUDA path: the arithmetic
 lives in ``fp8_oracle.c`` (plain C, built here with gcc), and this module only
 marshals numpy arrays into it and strings the steps of one training step
