@@ -11,10 +11,12 @@ full tensors), runs the forward, the backward and the scale update of one
 FP8 linear layer, and prints one JSON line: the five slots' amax, scale and
 scale_inv (values and binary32 bit patterns, the state after the update)
 and SHA-256 digests of every FP8 array (X8, X8t, W8, W8t, dY8, dY8t) and
-BF16 output (Y, dX, dW) as stored bytes.  The same tensors run through the
-GPU library's Fp8Linear give the same FP8 arrays and the same X, W and dY
-state bit for bit; its BF16 outputs (and so the Y and dX amax) match within
-the GEMM tolerance, since the GPU accumulates in fp32.
+BF16 output (Y, dX, dW) as stored bytes.  The inputs are drawn on the CPU;
+the bench and the GPU tests draw theirs on the device, whose generator gives
+other values, and hand copies of them to the oracle.  The same tensors run
+through the GPU library's Fp8Linear give the same FP8 arrays and the same
+X, W and dY state bit for bit; its BF16 outputs (and so the Y and dX amax)
+match within the GEMM tolerance, since the GPU accumulates in fp32.
 """
 import argparse
 import dataclasses
