@@ -238,6 +238,12 @@ def test_just_in_time_scaling_mlp7b_full_size():
     run_layer(wl.WORKLOADS["mlp7b"], 2, full=False, current=True)
 
 
+def test_just_in_time_scaling_mlp70b_full_size():
+    """Just-in-time scaling at the 70B shape, where X, W and dY are all larger
+    than the 96 MB that the amax pass leaves in L2 (its streaming loads)."""
+    run_layer(wl.WORKLOADS["mlp70b"], 2, full=False, current=True)
+
+
 def test_graph_replay_matches_eager_steps():
     """A captured step replays exactly what eager steps compute: two layers
     from the same state, one stepping eagerly, one through graph replays, stay
