@@ -131,7 +131,7 @@ def assert_codes_on_device(gpu_codes, x, table: np.ndarray, fmt: int, transposed
     comparison run on the device, the values are the oracle's), NaN codes
     compared as a class.  ``transposed``: gpu_codes is the [cols, rows] copy."""
     import torch
-    t = torch.from_numpy(np.ascontiguousarray(table)).to(gpu_codes.device)
+    t = torch.from_numpy(np.array(table, copy=True)).to(gpu_codes.device)
     idx = x.contiguous().view(torch.int16).to(torch.int64) & 0xFFFF
     exp = t[idx]
     if transposed:
