@@ -266,6 +266,35 @@ def test_graph_replay_matches_eager_steps():
     f.fp8_sync_status()
 
 
+@pytest.mark.parametrize("K,current", [(512, False), (512, True), (4112, False)])
+def test_graph_replay_of_the_layernorm_linear(K, current):
+    """The same for LayerNorm + FP8 linear: the one-pass LayerNorm cast and the
+    byte transpose (K = 512, delayed scaling), the statistics kernel and the
+    cast kernel's LayerNorm branch (just-in-time scaling; K = 4112, past the
+    one-pass limit) replay bit-identically, mean and rstd included."""
+    f = _lib()
+    w = wl.Workload("graph_ln", 384, K, 272, "normal", 1.0, 0.05, 1e-2, 16, 0, True, 4)
+    W = wl.layer_weight(w, "cuda")
+    X, dY = wl.layer_x(w, 0, "cuda"), wl.layer_dy(w, 0, "cuda")
+    gen = torch.Generator().manual_seed(K)
+    gamma = (1 + 0.1 * torch.randn(K, generator=gen)).to(torch.bfloat16).cuda()
+    beta = (0.1 * torch.randn(K, generator=gen)).to(torch.bfloat16).cuda()
+    rec = lambda: f.Recipe(w.margin, w.history_len, w.hybrid, current=current)
+    a = f.Fp8LayerNormLinear(W, w.M, gamma, beta, 1e-5, rec())
+    b = f.Fp8LayerNormLinear(W, w.M, gamma, beta, 1e-5, rec())
+    g = b.capture_step(X, dY)      # includes one eager warm-up step
+    a.step(X, dY)
+    for _ in range(3):
+        a.step(X, dY)
+        g.replay()
+        torch.cuda.synchronize()
+        for t1, t2 in [(a.Y, b.Y), (a.dX, b.dX), (a.dW, b.dW), (a.X8, b.X8), (a.X8t, b.X8t),
+                       (a.mean, b.mean), (a.rstd, b.rstd), (a.meta.history, b.meta.history),
+                       (a.meta.scale, b.meta.scale), (a.meta.scale_inv, b.meta.scale_inv)]:
+            assert torch.equal(t1.view(torch.uint8), t2.view(torch.uint8))
+    f.fp8_sync_status()
+
+
 def test_special_values_through_the_layer():
     """Degenerate inputs through whole steps: X holds +-inf, NaN and the
     largest BF16 values.  The amax of X is inf, so the X history holds inf
