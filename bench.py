@@ -461,8 +461,9 @@ def run_e2e(f, lin, X, dY, args, world, flops, readback="metric"):
     inverses, 40 B: the step's result as a training step uses it, where Y,
     dX and dW stay on the device for the neighbouring layers and the
     optimizer); with readback="outputs", Y, dX and dW themselves.  Copies run
-    on their own streams and are double-buffered against the compute stream,
-    so step i's uploads and step i-1's downloads overlap step i's kernels."""
+    on their own streams, the inputs double-buffered against the compute
+    stream, so step i+1's uploads and step i's downloads overlap step i's
+    kernels."""
     comp = torch.cuda.current_stream()
     up, down = torch.cuda.Stream(), torch.cuda.Stream()
     hX = [torch.empty_like(X, device="cpu").pin_memory() for _ in range(2)]
@@ -475,42 +476,47 @@ def run_e2e(f, lin, X, dY, args, world, flops, readback="metric"):
     ddYin = [torch.empty_like(dY) for _ in range(2)]
     douts = [(torch.empty_like(lin.Y), torch.empty_like(lin.dX), torch.empty_like(lin.dW))
              for _ in range(2)]
-    # what each step reads back, per slot: the outputs, or a device copy of the
-    # scaling state taken on the compute stream right after the step's update
+    # what each step reads back, per slot: the outputs (two slots), or a
+    # snapshot of the scaling state taken on the compute stream right after
+    # the step's update (a ring of eight, so that the compute stream never
+    # waits for a recent download; the snapshot is an elementwise kernel, x1.0,
+    # not a memcpy, so the compute stream never queues on a copy engine that
+    # an upload holds)
+    nres = 2 if readback == "outputs" else 8
     dres = [tuple(douts[k]) if readback == "outputs" else
             (torch.empty_like(lin.meta.scale), torch.empty_like(lin.meta.scale_inv))
-            for k in range(2)]
+            for k in range(nres)]
     houts = [tuple(torch.empty_like(t, device="cpu").pin_memory() for t in o) for o in dres]
     ev = lambda: torch.cuda.Event()
     in_ready = [ev(), ev()]      # upload of slot done
     in_free = [ev(), ev()]       # compute done reading slot's inputs
-    out_ready = [ev(), ev()]     # compute done writing slot's outputs
-    out_free = [ev(), ev()]      # download of slot's outputs done
+    out_ready = [ev() for _ in range(nres)]   # compute done writing slot's results
+    out_free = [ev() for _ in range(nres)]    # download of slot's results done
     for e in in_free + out_free:
         e.record(comp)
     n = max(5, min(args.steps, 50))
 
     def step(i):
-        k = i % 2
+        k, kr = i % 2, i % nres
         with torch.cuda.stream(up):
             up.wait_event(in_free[k])
             dXin[k].copy_(hX[k], non_blocking=True)
             ddYin[k].copy_(hdY[k], non_blocking=True)
             in_ready[k].record(up)
         comp.wait_event(in_ready[k])
-        comp.wait_event(out_free[k])
+        comp.wait_event(out_free[kr])
         lin.step(dXin[k], ddYin[k], stream=comp, outs=douts[k])
         if readback != "outputs":
             with torch.cuda.stream(comp):
-                dres[k][0].copy_(lin.meta.scale, non_blocking=True)
-                dres[k][1].copy_(lin.meta.scale_inv, non_blocking=True)
+                torch.mul(lin.meta.scale, 1.0, out=dres[kr][0])
+                torch.mul(lin.meta.scale_inv, 1.0, out=dres[kr][1])
         in_free[k].record(comp)
-        out_ready[k].record(comp)
+        out_ready[kr].record(comp)
         with torch.cuda.stream(down):
-            down.wait_event(out_ready[k])
-            for h, d in zip(houts[k], dres[k]):
+            down.wait_event(out_ready[kr])
+            for h, d in zip(houts[kr], dres[kr]):
                 h.copy_(d, non_blocking=True)
-            out_free[k].record(down)
+            out_free[kr].record(down)
 
     for i in range(3):
         step(i)
@@ -534,7 +540,7 @@ def run_e2e(f, lin, X, dY, args, world, flops, readback="metric"):
     down.wait_stream(comp)
     for i in range(n):
         step(i)
-    for k in range(2):
+    for k in range(nres):
         comp.wait_event(out_free[k])
     e.record(comp)
     torch.cuda.synchronize()
